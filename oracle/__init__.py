@@ -1,0 +1,231 @@
+"""fp64 CPU oracle for the speculative-decoding verification step.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+CPU-baseline leg of ``bench.py`` may import this package.  The CUDA product
+path never imports it, shares no code with it and never falls back to it.
+
+The arithmetic lives in ``spec_oracle.c`` (plain serial double-precision
+loops, one request at a time; see its header for the pages each step
+follows).  This module only builds that file with the system C compiler,
+marshals numpy arrays into it and, for speed on large inputs, runs disjoint
+request ranges on a thread pool (ctypes releases the GIL during a call).
+
+Logit arrays are numpy ``float32`` (fp32 logits) or ``uint16`` holding raw
+bfloat16 bit patterns.  Uniform arrays are widened to float64 exactly.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+from concurrent.futures import ThreadPoolExecutor
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "spec_oracle.c")
+_LIB = os.path.join(_HERE, "libspecoracle.so")
+_lock = threading.Lock()
+_lib = None
+
+BAD_TOKEN = 1
+BAD_LOGITS = 2
+BAD_DRAFT_LEN = 4
+FLAG_ACCEPT = 1
+FLAG_CDF = 2
+FLAG_TOL = 1e-5
+
+
+def build(force: bool = False) -> str:
+    """Compile spec_oracle.c into libspecoracle.so next to it (if stale)."""
+    with _lock:
+        if (not force and os.path.exists(_LIB)
+                and os.path.getmtime(_LIB) >= os.path.getmtime(_SRC)):
+            return _LIB
+        tmp = _LIB + ".%d.tmp" % os.getpid()
+        # ISO C with FP contraction off: the same rounding on x86-64 and AArch64.
+        cmd = ["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math",
+               "-fPIC", "-shared", "-o", tmp, _SRC, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+        return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        _lib = configure(ctypes.CDLL(build()))
+    return _lib
+
+
+def configure(lib):
+    """Declare the C signatures on a loaded copy of the oracle library."""
+    P = ctypes.c_void_p
+    I = ctypes.c_int
+    D = ctypes.c_double
+    lib.sv_oracle_tempered_softmax.argtypes = [P, I, D, P]
+    lib.sv_oracle_tempered_softmax.restype = None
+    lib.sv_oracle_argmax.argtypes = [P, I]
+    lib.sv_oracle_argmax.restype = I
+    lib.sv_oracle_inverse_cdf.argtypes = [P, I, D, P]
+    lib.sv_oracle_inverse_cdf.restype = I
+    lib.sv_oracle_greedy.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P]
+    lib.sv_oracle_greedy.restype = I
+    lib.sv_oracle_sample.argtypes = [P, P, I, P, P, P, D, I, I, I, I, I, P, P, P, P, P, P]
+    lib.sv_oracle_sample.restype = I
+    lib.sv_oracle_tree.argtypes = [P, I, P, P, I, I, I, I, I, I, P, P, P, P]
+    lib.sv_oracle_tree.restype = I
+    lib.sv_oracle_compact.argtypes = [P, P, I, I, P, P, P]
+    lib.sv_oracle_compact.restype = None
+    return lib
+
+
+def _ptr(a):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _logits(a):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.float32:
+        return a, 0
+    if a.dtype == np.uint16:
+        return a, 1
+    raise TypeError("oracle logits must be float32 or uint16 (bfloat16 bits), got %s" % a.dtype)
+
+
+def _ranges(B, threads):
+    threads = max(1, min(int(threads), B)) if B > 0 else 1
+    edges = np.linspace(0, B, threads + 1).astype(int)
+    return [(int(edges[i]), int(edges[i + 1])) for i in range(threads)]
+
+
+def _run(fn, B, threads, b_range):
+    lo, hi = (0, B) if b_range is None else b_range
+    parts = [(lo + a, lo + b) for a, b in _ranges(hi - lo, threads)]
+    if len(parts) == 1:
+        rc = fn(*parts[0])
+        if rc != 0:
+            raise ValueError("oracle rejected its arguments (code %d)" % rc)
+        return
+    with ThreadPoolExecutor(len(parts)) as ex:
+        for rc in ex.map(lambda ab: fn(*ab), parts):
+            if rc != 0:
+                raise ValueError("oracle rejected its arguments (code %d)" % rc)
+
+
+# ---------------------------------------------------------------------------
+# single steps (exposed so that the tests can pin them against library code)
+# ---------------------------------------------------------------------------
+
+def tempered_softmax(logits, temperature):
+    l = np.ascontiguousarray(logits, dtype=np.float64)
+    out = np.empty_like(l)
+    _load().sv_oracle_tempered_softmax(_ptr(l), l.size, float(temperature), _ptr(out))
+    return out
+
+
+def argmax(logits):
+    l = np.ascontiguousarray(logits, dtype=np.float64)
+    return int(_load().sv_oracle_argmax(_ptr(l), l.size))
+
+
+def inverse_cdf(weights, u):
+    w = np.ascontiguousarray(weights, dtype=np.float64)
+    m = np.zeros(1, dtype=np.float64)
+    t = _load().sv_oracle_inverse_cdf(_ptr(w), w.size, float(u), _ptr(m))
+    return int(t), float(m[0])
+
+
+# ---------------------------------------------------------------------------
+# batched verification
+# ---------------------------------------------------------------------------
+
+def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=None,
+           threads=1, b_range=None):
+    """Rejection-sampling verify (temperature 0 = greedy rule).
+
+    target [B, K+1, V], draft [B, K, V] or None (one-hot drafts),
+    draft_tokens [B, K] int32, uniforms [B, K+1] (float32 or float64),
+    draft_lens [B] or None.  Requests outside ``b_range`` keep -1 / 0.
+    Returns a dict of numpy arrays: tokens, accept_len, accept_prob, flags,
+    margins, status.
+    """
+    target, dt = _logits(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    if draft is not None:
+        draft, dt2 = _logits(draft)
+        if dt2 != dt or draft.shape != (B, K, V):
+            raise ValueError("draft logits must match target dtype and be [B, K, V]")
+    toks = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, K)
+    u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, K + 1)
+    lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, dtype=np.int32)
+    out = dict(tokens=np.full((B, K + 1), -1, np.int32), accept_len=np.zeros(B, np.int32),
+               accept_prob=np.full((B, K), -1.0), flags=np.zeros((B, K + 1), np.int32),
+               margins=np.full((B, K + 1), np.inf), status=np.zeros(B, np.int32))
+    lib = _load()
+
+    def fn(lo, hi):
+        return lib.sv_oracle_sample(
+            _ptr(target), _ptr(draft), dt, _ptr(toks), _ptr(lens), _ptr(u),
+            float(temperature), B, K, V, lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
+            _ptr(out["accept_prob"]), _ptr(out["flags"]), _ptr(out["margins"]),
+            _ptr(out["status"]))
+
+    _run(fn, B, threads, b_range)
+    return out
+
+
+def greedy(target, draft_tokens, *, draft_lens=None, threads=1, b_range=None):
+    """Greedy verify: tokens [B, K+1], accept_len [B], status [B]."""
+    target, dt = _logits(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    toks = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, K)
+    lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, dtype=np.int32)
+    out = dict(tokens=np.full((B, K + 1), -1, np.int32), accept_len=np.zeros(B, np.int32),
+               status=np.zeros(B, np.int32))
+    lib = _load()
+
+    def fn(lo, hi):
+        return lib.sv_oracle_greedy(_ptr(target), dt, _ptr(toks), _ptr(lens), B, K, V, lo, hi,
+                                    _ptr(out["tokens"]), _ptr(out["accept_len"]),
+                                    _ptr(out["status"]))
+
+    _run(fn, B, threads, b_range)
+    return out
+
+
+def tree(target, parent, node_tokens, max_depth, *, threads=1, b_range=None):
+    """Greedy tree verify: tokens / path [B, max_depth+1], accept_len, status."""
+    target, dt = _logits(target)
+    B, N1, V = target.shape
+    N = N1 - 1
+    par = np.ascontiguousarray(parent, dtype=np.int32).reshape(N)
+    nt = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
+    W = max_depth + 1
+    out = dict(tokens=np.full((B, W), -1, np.int32), accept_len=np.zeros(B, np.int32),
+               path=np.full((B, W), -1, np.int32), status=np.zeros(B, np.int32))
+    lib = _load()
+
+    def fn(lo, hi):
+        return lib.sv_oracle_tree(_ptr(target), dt, _ptr(par), _ptr(nt), B, N, V, int(max_depth),
+                                  lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
+                                  _ptr(out["path"]), _ptr(out["status"]))
+
+    _run(fn, B, threads, b_range)
+    return out
+
+
+def compact(tokens, accept_len):
+    """Padding-free layout: cu [B+1], packed [B*W], batch_id [B*W]."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    a = np.ascontiguousarray(accept_len, dtype=np.int32)
+    B, W = t.shape
+    cu = np.zeros(B + 1, np.int32)
+    packed = np.empty(B * W, np.int32)
+    bid = np.empty(B * W, np.int32)
+    _load().sv_oracle_compact(_ptr(t), _ptr(a), B, W, _ptr(cu), _ptr(packed), _ptr(bid))
+    return cu, packed, bid
+

@@ -1,0 +1,461 @@
+/*
+ * spec_oracle.c - plain fp64 CPU oracle for the speculative-decoding
+ * verification step.
+ *
+ * TEST INFRASTRUCTURE.  Only the test suite, the package's smoke check and
+ * the benchmark's CPU-baseline leg may load this code.  The product path
+ * (the CUDA library) never calls it, shares no source with it and does not
+ * fall back to it.
+ *
+ * What it computes follows these pages:
+ *   [SD]   "【大模型基础设施工程】15：推测解码与 MTP" (juejin.cn)
+ *          §2.1 "算法骨架" (the verification rule), the following "1.2 正确性
+ *          保证" (exactness), §2.3 (1 <= accept length <= K+1),
+ *          §3.3 "Tree Attention" (ancestor-only paths, longest accepted path),
+ *          §11 (the hand-written sketch: softmax over the K+1 target positions,
+ *          strict "r < min(1, p/q)" test, clamp-then-normalise residual).
+ *   [FD]   "投机解码" (FastDeploy docs), "高效投机解码框架设计"
+ *          (per-sample parallel verify; padding-free batch-id lookup).
+ *
+ * Every quantity is computed in double precision, one request at a time,
+ * with plain serial loops: no blocking, fusion or reordering.  Where the
+ * pages leave a step open, the reading taken is named R1..R12 in the
+ * comments (the same labels are used in the design notes).
+ *
+ * Logit storage: dtype 0 = IEEE fp32, dtype 1 = bfloat16 given as raw
+ * 16-bit patterns.  Both are widened exactly to double before any
+ * arithmetic.
+ *
+ * Per-request status bits (0 = valid request):
+ *   1  a draft / tree token outside [0, V)
+ *   2  a needed logit row holds NaN or +inf, or holds no finite value
+ *   4  a draft length outside [0, K]
+ * A request with a nonzero status emits nothing: accept_len = 0 and all its
+ * token slots are -1.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_BAD_TOKEN 1
+#define OR_BAD_LOGITS 2
+#define OR_BAD_DRAFT_LEN 4
+
+#define OR_FLAG_ACCEPT 1 /* u within 1e-5 (relative) of the acceptance threshold */
+#define OR_FLAG_CDF 2    /* u*W within 1e-5*W of a CDF step around the chosen token */
+
+#define OR_FLAG_TOL 1e-5
+
+/* ------------------------------------------------------------------ */
+/* input decoding                                                      */
+/* ------------------------------------------------------------------ */
+
+static double load_logit(const void* base, int dtype, size_t idx) {
+  if (dtype == 0) return (double)((const float*)base)[idx];
+  /* bfloat16 is the top half of an IEEE binary32 word */
+  uint32_t word = (uint32_t)((const uint16_t*)base)[idx] << 16;
+  float f;
+  memcpy(&f, &word, sizeof f);
+  return (double)f;
+}
+
+static void load_row(const void* base, int dtype, size_t row, int V, double* out) {
+  for (int j = 0; j < V; ++j) out[j] = load_logit(base, dtype, row * (size_t)V + (size_t)j);
+}
+
+/* R12: a row is usable when every entry is finite or -inf (masking) and at
+ * least one entry is finite. */
+static int row_is_valid(const double* l, int V) {
+  int any_finite = 0;
+  for (int j = 0; j < V; ++j) {
+    if (isnan(l[j])) return 0;
+    if (isinf(l[j]) && l[j] > 0) return 0;
+    if (isfinite(l[j])) any_finite = 1;
+  }
+  return any_finite;
+}
+
+/* ------------------------------------------------------------------ */
+/* the steps                                                           */
+/* ------------------------------------------------------------------ */
+
+/* Tempered softmax [SD §11: softmax over the vocabulary at each target
+ * position; temperature as in the SamplingParams of the vLLM guide]:
+ *   p[j] = exp(l[j]/T - M) / sum_k exp(l[k]/T - M),  M = max_k l[k]/T.
+ * Subtracting M does not change the value; it keeps exp() in range. */
+void sv_oracle_tempered_softmax(const double* l, int V, double T, double* p) {
+  double M = -INFINITY;
+  for (int j = 0; j < V; ++j) {
+    double s = l[j] / T;
+    if (s > M) M = s;
+  }
+  double Z = 0.0;
+  for (int j = 0; j < V; ++j) {
+    p[j] = exp(l[j] / T - M);
+    Z += p[j];
+  }
+  for (int j = 0; j < V; ++j) p[j] /= Z;
+}
+
+/* Argmax with the lowest index among equal maxima (R8; -0.0 == +0.0). */
+int sv_oracle_argmax(const double* l, int V) {
+  int best = 0;
+  for (int j = 1; j < V; ++j)
+    if (l[j] > l[best]) best = j;
+  return best;
+}
+
+/* Inverse-CDF draw from non-negative weights w (unnormalised):
+ *   C_j = sum_{k<=j} w_k,  W = C_{V-1},
+ *   token = the smallest j with C_j > u*W;
+ *   if no j qualifies (only through rounding), the largest j with w_j > 0 (R4).
+ * *margin receives min(|u*W - C_{t-1}|, |u*W - C_t|) / W, the distance of
+ * the draw to the nearer edge of the chosen token's CDF step. */
+int sv_oracle_inverse_cdf(const double* w, int V, double u, double* margin) {
+  double W = 0.0;
+  for (int j = 0; j < V; ++j) W += w[j];
+  double target = u * W;
+  double C = 0.0, C_prev = 0.0;
+  int t = -1;
+  for (int j = 0; j < V; ++j) {
+    C_prev = C;
+    C += w[j];
+    if (C > target) {
+      t = j;
+      break;
+    }
+  }
+  if (t < 0) {
+    for (int j = V - 1; j >= 0; --j)
+      if (w[j] > 0) {
+        t = j;
+        break;
+      }
+    C_prev = W - (t >= 0 ? w[t] : 0.0);
+    C = W;
+  }
+  if (margin) {
+    double a = fabs(target - C_prev), b = fabs(target - C);
+    *margin = (W > 0) ? (a < b ? a : b) / W : 0.0;
+  }
+  return t;
+}
+
+/* Acceptance threshold theta = min(1, p/q) [SD §2.1].  R2: q = 0 < p gives
+ * 1 (always accept under the strict test below); p = q = 0 gives 0. */
+static double accept_threshold(double p, double q) {
+  if (q > 0) return p / q < 1.0 ? p / q : 1.0;
+  return p > 0 ? 1.0 : 0.0;
+}
+
+/* ------------------------------------------------------------------ */
+/* greedy verification                                                 */
+/* ------------------------------------------------------------------ */
+
+static void clear_request(int32_t* tokens, int width, int32_t* accept_len) {
+  for (int k = 0; k < width; ++k) tokens[k] = -1;
+  *accept_len = 0;
+}
+
+/* Greedy verify (temperature 0) [SD §11: do_sample=False gives output
+ * identical to plain decoding]: draft x_i is accepted while it equals the
+ * argmax of target row i; the first mismatch emits that argmax; if all
+ * drafts match, the argmax of the last row is the bonus token.  The argmax
+ * is taken on the raw logits, so the temperature plays no part. */
+static int greedy_request(const void* target, int dtype, const int32_t* draft_tokens,
+                          int K, int K_b, int V, size_t b, double* row, int32_t* tokens,
+                          int32_t* accept_len, double* accept_prob) {
+  for (int i = 0; i < K_b; ++i) {
+    int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
+    if (x < 0 || x >= V) return OR_BAD_TOKEN;
+  }
+  int n = K_b;
+  int emitted = -1;
+  for (int i = 0; i <= K_b; ++i) {
+    load_row(target, dtype, b * (size_t)(K + 1) + (size_t)i, V, row);
+    if (!row_is_valid(row, V)) return OR_BAD_LOGITS;
+    int a = sv_oracle_argmax(row, V);
+    if (i == K_b) {
+      emitted = a;
+      break;
+    }
+    int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
+    if (accept_prob) accept_prob[i] = (x == a) ? 1.0 : 0.0;
+    if (x != a) {
+      n = i;
+      emitted = a;
+      break;
+    }
+  }
+  for (int i = 0; i < n; ++i) tokens[i] = draft_tokens[b * (size_t)K + (size_t)i];
+  tokens[n] = emitted;
+  *accept_len = n + 1;
+  return 0;
+}
+
+int sv_oracle_greedy(const void* target, int dtype, const int32_t* draft_tokens,
+                     const int32_t* draft_lens, int B, int K, int V, int b_begin, int b_end,
+                     int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_status) {
+  if (B < 0 || K < 0 || V < 1 || b_begin < 0 || b_end > B) return -1;
+  double* row = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!row) return -2;
+  for (int b = b_begin; b < b_end; ++b) {
+    int32_t* tokens = out_tokens + (size_t)b * (size_t)(K + 1);
+    clear_request(tokens, K + 1, &out_accept_len[b]);
+    int K_b = draft_lens ? draft_lens[b] : K;
+    int st = 0;
+    if (K_b < 0 || K_b > K)
+      st = OR_BAD_DRAFT_LEN;
+    else
+      st = greedy_request(target, dtype, draft_tokens, K, K_b, V, (size_t)b, row, tokens,
+                          &out_accept_len[b], NULL);
+    if (st) clear_request(tokens, K + 1, &out_accept_len[b]);
+    out_status[b] = st;
+  }
+  free(row);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* rejection-sampling verification                                     */
+/* ------------------------------------------------------------------ */
+
+/* One request of the verification rule [SD §2.1]:
+ *   for i = 0..K_b-1 in order: accept x_i iff u_i * q_i(x_i) < p_i(x_i)
+ *     (the strict "r < min(1, p/q)" of the §11 sketch, written without a
+ *     division; R2);
+ *   at the first rejection n: draw from norm(max(0, p_n - q_n)) and stop;
+ *   if all K_b are accepted (n = K_b): draw the bonus token from p_{K_b}.
+ * Dense drafts: q_i = tempered softmax of the draft logits with the same T
+ * (R1).  One-hot drafts (deterministic proposer): q_i = delta at x_i, so the
+ * residual is p_n with x_n removed (R9).  If the residual has no mass (only
+ * through rounding, since max(0, p - q) sums to 0 only when p = q), draw
+ * from p_n instead (R3).  The draw uses uniform u_K (R5). */
+static int sample_request(const void* target, const void* draft, int dtype,
+                          const int32_t* draft_tokens, const double* uniforms, double T, int K,
+                          int K_b, int V, size_t b, double* lrow, double* p, double* q,
+                          double* w, int32_t* tokens, int32_t* accept_len, double* accept_prob,
+                          int32_t* flags, double* margins) {
+  for (int i = 0; i < K_b; ++i) {
+    int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
+    if (x < 0 || x >= V) return OR_BAD_TOKEN;
+  }
+  const double* u = uniforms + b * (size_t)(K + 1);
+  int n = K_b;
+  for (int i = 0; i < K_b; ++i) {
+    int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
+    load_row(target, dtype, b * (size_t)(K + 1) + (size_t)i, V, lrow);
+    if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
+    sv_oracle_tempered_softmax(lrow, V, T, p);
+    double qx = 1.0;
+    if (draft) {
+      load_row(draft, dtype, b * (size_t)K + (size_t)i, V, lrow);
+      if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
+      sv_oracle_tempered_softmax(lrow, V, T, q);
+      qx = q[x];
+    }
+    double theta = accept_threshold(p[x], qx);
+    if (accept_prob) accept_prob[i] = theta;
+    if (margins) margins[i] = theta > 0 ? fabs(u[i] - theta) / theta : INFINITY;
+    if (fabs(u[i] - theta) <= OR_FLAG_TOL * theta) flags[i] |= OR_FLAG_ACCEPT;
+    if (!(u[i] * qx < p[x])) {
+      n = i;
+      /* residual weights max(0, p - q) */
+      for (int j = 0; j < V; ++j) {
+        double qj = draft ? q[j] : (j == x ? 1.0 : 0.0);
+        double r = p[j] - qj;
+        w[j] = r > 0 ? r : 0.0;
+      }
+      break;
+    }
+  }
+  if (n == K_b) {
+    load_row(target, dtype, b * (size_t)(K + 1) + (size_t)K_b, V, lrow);
+    if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
+    sv_oracle_tempered_softmax(lrow, V, T, p);
+    for (int j = 0; j < V; ++j) w[j] = p[j];
+  } else {
+    double W = 0.0;
+    for (int j = 0; j < V; ++j) W += w[j];
+    if (!(W > 0)) /* R3 */
+      for (int j = 0; j < V; ++j) w[j] = p[j];
+  }
+  double margin = 0.0;
+  int t = sv_oracle_inverse_cdf(w, V, u[K], &margin);
+  if (margins) margins[K] = margin;
+  if (margin <= OR_FLAG_TOL) flags[n] |= OR_FLAG_CDF;
+  for (int i = 0; i < n; ++i) tokens[i] = draft_tokens[b * (size_t)K + (size_t)i];
+  tokens[n] = t;
+  *accept_len = n + 1;
+  return 0;
+}
+
+/* Batched entry over requests [b_begin, b_end).  Requests are independent
+ * (R6: the per-sample parallel verify of the FastDeploy design; the sketch's
+ * batch-wide ".all()" is not followed).
+ *   target       [B, K+1, V]   draft  [B, K, V] or NULL (one-hot drafts)
+ *   draft_tokens [B, K]        draft_lens [B] or NULL (all K)
+ *   uniforms     [B, K+1] doubles: column i < K for the acceptance test of
+ *                position i, column K for the residual / bonus draw (R5)
+ *   temperature  0 selects greedy verification; otherwise > 0 and finite
+ *   outputs: tokens [B, K+1] (-1 padded), accept_len [B] (R7: accepted
+ *   drafts + 1), accept_prob [B, K] (min(1, p/q) at the tested positions,
+ *   -1 elsewhere), flags [B, K+1], margins [B, K+1] or NULL, status [B].
+ * Returns 0, or a negative code for arguments outside the domain. */
+int sv_oracle_sample(const void* target, const void* draft, int dtype,
+                     const int32_t* draft_tokens, const int32_t* draft_lens,
+                     const double* uniforms, double temperature, int B, int K, int V,
+                     int b_begin, int b_end, int32_t* out_tokens, int32_t* out_accept_len,
+                     double* out_accept_prob, int32_t* out_flags, double* out_margins,
+                     int32_t* out_status) {
+  if (B < 0 || K < 0 || V < 1 || b_begin < 0 || b_end > B) return -1;
+  if (!(temperature >= 0) || isinf(temperature)) return -3;
+  double* buf = (double*)malloc(sizeof(double) * (size_t)V * 4);
+  if (!buf) return -2;
+  double *lrow = buf, *p = buf + V, *q = buf + 2 * (size_t)V, *w = buf + 3 * (size_t)V;
+  for (int b = b_begin; b < b_end; ++b) {
+    int32_t* tokens = out_tokens + (size_t)b * (size_t)(K + 1);
+    int32_t* flags = out_flags + (size_t)b * (size_t)(K + 1);
+    double* aprob = out_accept_prob + (size_t)b * (size_t)K;
+    double* margins = out_margins ? out_margins + (size_t)b * (size_t)(K + 1) : NULL;
+    clear_request(tokens, K + 1, &out_accept_len[b]);
+    for (int i = 0; i <= K; ++i) flags[i] = 0;
+    for (int i = 0; i < K; ++i) aprob[i] = -1.0;
+    if (margins)
+      for (int i = 0; i <= K; ++i) margins[i] = INFINITY;
+    int K_b = draft_lens ? draft_lens[b] : K;
+    int st;
+    if (K_b < 0 || K_b > K)
+      st = OR_BAD_DRAFT_LEN;
+    else if (temperature == 0)
+      st = greedy_request(target, dtype, draft_tokens, K, K_b, V, (size_t)b, lrow, tokens,
+                          &out_accept_len[b], aprob);
+    else
+      st = sample_request(target, draft, dtype, draft_tokens, uniforms, temperature, K, K_b,
+                          V, (size_t)b, lrow, p, q, w, tokens, &out_accept_len[b], aprob,
+                          flags, margins);
+    if (st) {
+      clear_request(tokens, K + 1, &out_accept_len[b]);
+      for (int i = 0; i < K; ++i) aprob[i] = -1.0;
+      for (int i = 0; i <= K; ++i) flags[i] = 0;
+    }
+    out_status[b] = st;
+  }
+  free(buf);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* greedy tree verification                                            */
+/* ------------------------------------------------------------------ */
+
+/* Medusa / EAGLE tree [SD §3.3]: candidate nodes form a tree under the root
+ * (node 0, the last committed token); each node's target row was computed
+ * seeing only its ancestors.  A node is accepted when its token equals the
+ * target argmax at its parent and its parent is accepted; the result is the
+ * longest accepted root path plus the argmax at its last node.
+ *   parent [N]: parent of node n (n = 1..N) at index n-1, with parent < n.
+ *   tokens [B, N]: token of node n at index n-1.
+ *   target [B, N+1, V]: row n holds node n's logits.
+ * Outputs: tokens [B, max_depth+1] (argmax along the path, -1 padded),
+ * accept_len [B] = accepted nodes + 1, path [B, max_depth+1] (node ids from
+ * the root, -1 padded), status [B].
+ * With distinct sibling tokens (top-k candidates) at most one child of a
+ * node can match, so walking from the root finds the longest path; when a
+ * caller repeats a token among siblings, the lowest node index wins (R11).
+ * Returns -4 if the parent array is not a tree of depth <= max_depth. */
+int sv_oracle_tree(const void* target, int dtype, const int32_t* parent,
+                   const int32_t* node_tokens, int B, int N, int V, int max_depth,
+                   int b_begin, int b_end, int32_t* out_tokens, int32_t* out_accept_len,
+                   int32_t* out_path, int32_t* out_status) {
+  if (B < 0 || N < 0 || V < 1 || max_depth < 0 || b_begin < 0 || b_end > B) return -1;
+  int* depth = (int*)malloc(sizeof(int) * (size_t)(N + 1));
+  double* row = (double*)malloc(sizeof(double) * (size_t)V);
+  if (!depth || !row) {
+    free(depth);
+    free(row);
+    return -2;
+  }
+  depth[0] = 0;
+  for (int n = 1; n <= N; ++n) {
+    int pa = parent[n - 1];
+    if (pa < 0 || pa >= n) {
+      free(depth);
+      free(row);
+      return -4;
+    }
+    depth[n] = depth[pa] + 1;
+    if (depth[n] > max_depth) {
+      free(depth);
+      free(row);
+      return -4;
+    }
+  }
+  int width = max_depth + 1;
+  for (int b = b_begin; b < b_end; ++b) {
+    int32_t* tokens = out_tokens + (size_t)b * (size_t)width;
+    int32_t* path = out_path + (size_t)b * (size_t)width;
+    clear_request(tokens, width, &out_accept_len[b]);
+    for (int k = 0; k < width; ++k) path[k] = -1;
+    int st = 0;
+    for (int n = 1; n <= N; ++n) {
+      int32_t t = node_tokens[(size_t)b * (size_t)N + (size_t)(n - 1)];
+      if (t < 0 || t >= V) st = OR_BAD_TOKEN;
+    }
+    int node = 0, len = 0;
+    while (!st) {
+      load_row(target, dtype, (size_t)b * (size_t)(N + 1) + (size_t)node, V, row);
+      if (!row_is_valid(row, V)) {
+        st = OR_BAD_LOGITS;
+        break;
+      }
+      int a = sv_oracle_argmax(row, V);
+      path[len] = node;
+      tokens[len] = a;
+      ++len;
+      int next = -1;
+      for (int c = 1; c <= N; ++c)
+        if (parent[c - 1] == node &&
+            node_tokens[(size_t)b * (size_t)N + (size_t)(c - 1)] == a) {
+          next = c;
+          break;
+        }
+      if (next < 0) break;
+      node = next;
+    }
+    if (st) {
+      clear_request(tokens, width, &out_accept_len[b]);
+      for (int k = 0; k < width; ++k) path[k] = -1;
+    } else {
+      out_accept_len[b] = len;
+    }
+    out_status[b] = st;
+  }
+  free(depth);
+  free(row);
+  return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* padding-free output layout                                          */
+/* ------------------------------------------------------------------ */
+
+/* [FD "高效投机解码框架设计": locate each output token's batch id without
+ * copies or slices]: cu[0] = 0, cu[b+1] = cu[b] + accept_len[b]; the
+ * emitted tokens of request b sit at packed[cu[b] .. cu[b+1]-1] and
+ * batch_id there is b.  Slots from cu[B] to B*width-1 hold -1. */
+void sv_oracle_compact(const int32_t* tokens, const int32_t* accept_len, int B, int width,
+                       int32_t* cu, int32_t* packed, int32_t* batch_id) {
+  cu[0] = 0;
+  for (int b = 0; b < B; ++b) cu[b + 1] = cu[b] + accept_len[b];
+  for (size_t s = 0; s < (size_t)B * (size_t)width; ++s) {
+    packed[s] = -1;
+    batch_id[s] = -1;
+  }
+  for (int b = 0; b < B; ++b)
+    for (int k = 0; k < accept_len[b]; ++k) {
+      packed[cu[b] + k] = tokens[(size_t)b * (size_t)width + (size_t)k];
+      batch_id[cu[b] + k] = b;
+    }
+}

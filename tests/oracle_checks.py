@@ -1,0 +1,516 @@
+"""Checks that pin the fp64 oracle to facts outside itself.
+
+Each ``check_*`` function raises AssertionError on a mismatch.  The pytest
+wrappers live in test_oracle_pins.py; test_oracle_mutants.py runs the same
+checks against deliberately broken copies of the oracle to show that every
+plausible mistake is caught by at least one of them.
+
+What pins what:
+  * library routines: scipy's softmax, numpy's argmax (first maximum) and
+    searchsorted over a cumulative sum (smallest j with C_j > u*W);
+  * hand-derived worked examples under tests/golden/ (closed forms);
+  * the exactness theorem of rejection sampling ("推测解码与 MTP" (juejin.cn),
+    the "正确性保证" part of §2): the token emitted at each position is
+    distributed exactly as the target distribution there.  Measured by
+    treating the oracle as a black box and locating, by bisection over the
+    uniforms, the exact u-intervals that lead to each outcome;
+  * a chi-square test over 10^6 seeded draws;
+  * invariants: 1 <= accept_len <= K+1 (§2.3 of the same page), all
+    accepted => K+1 tokens, q == p => everything accepted, one-hot drafts
+    accepted exactly when u < p(x), zero-probability drafts never accepted;
+  * the T -> 0 limit of sampling equals greedy verification;
+  * tree verification against a brute-force enumeration of root paths.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+import scipy.special
+import scipy.stats
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _golden(name):
+    with open(os.path.join(GOLDEN, name)) as f:
+        return json.load(f)
+
+
+def _f(v):
+    if isinstance(v, str):
+        return {"-inf": -np.inf, "inf": np.inf, "nan": np.nan}[v]
+    return float(v)
+
+
+def _rows(rows):
+    return np.asarray([[_f(v) for v in r] for r in rows], dtype=np.float32)
+
+
+# ---------------------------------------------------------------------------
+# library pins
+# ---------------------------------------------------------------------------
+
+def check_softmax_matches_scipy():
+    rng = np.random.default_rng(101)
+    for V in (1, 2, 7, 1000, 32000):
+        for T in (0.05, 0.8, 1.0, 2.0):
+            l = rng.standard_normal(V) * 3.0
+            if V > 2:
+                l[rng.random(V) < 0.1] = -np.inf
+                l[0] = 0.5
+            got = oracle.tempered_softmax(l, T)
+            ref = scipy.special.softmax(l / T)
+            np.testing.assert_allclose(got, ref, rtol=1e-12, atol=1e-300)
+    # far from zero: exp() stays in range only because of the max shift
+    l = np.array([1000.0, 999.0, 998.5, -1e4])
+    np.testing.assert_allclose(oracle.tempered_softmax(l, 0.7),
+                               scipy.special.softmax(l / 0.7), rtol=1e-12)
+
+
+def check_argmax_matches_numpy():
+    rng = np.random.default_rng(102)
+    for V in (1, 2, 3, 17, 1000):
+        for _ in range(20):
+            l = rng.integers(-3, 4, size=V).astype(np.float64)  # many exact ties
+            assert oracle.argmax(l) == int(np.argmax(l)), (l, oracle.argmax(l))
+    l = np.array([-0.0, 0.0, -1.0])
+    assert oracle.argmax(l) == 0
+    l = np.array([-np.inf, -5.0, 2.0, 2.0, -np.inf])
+    assert oracle.argmax(l) == 2
+
+
+def _searchsorted_draw(w, u):
+    c = np.cumsum(w)
+    j = int(np.searchsorted(c, u * c[-1], side="right"))
+    if j >= len(w):
+        j = int(np.nonzero(w > 0)[0][-1])
+    return j
+
+
+def check_inverse_cdf_matches_searchsorted():
+    rng = np.random.default_rng(103)
+    for V in (1, 2, 5, 64, 5000):
+        for _ in range(50):
+            w = rng.random(V)
+            w[rng.random(V) < 0.3] = 0.0
+            if not (w > 0).any():
+                w[V // 2] = 1.0
+            u = float(rng.random())
+            t, _ = oracle.inverse_cdf(w, u)
+            assert t == _searchsorted_draw(w, u), (V, u, t)
+    # zero-weight tokens are never drawn, not even at u = 0 or with a
+    # leading run of zeros
+    w = np.array([0.0, 0.0, 0.25, 0.0, 0.75])
+    for u in (0.0, 1e-300, 0.2499999, 0.25, 0.9999999):
+        t, _ = oracle.inverse_cdf(w, u)
+        assert w[t] > 0 and t == _searchsorted_draw(w, u), (u, t)
+
+
+# ---------------------------------------------------------------------------
+# worked examples
+# ---------------------------------------------------------------------------
+
+def check_golden_sampling():
+    for name in ("verify_dense_v3.json", "verify_onehot_v4.json"):
+        g = _golden(name)
+        V, K, T = g["V"], g["K"], g["T"]
+        target = np.log(np.asarray(g["target_probs"])).astype(np.float32)
+        draft = None
+        if g["mode"] == "dense":
+            draft = np.log(np.asarray(g["draft_probs"])).astype(np.float32)[None]
+        for case in g["cases"]:
+            out = oracle.sample(target[None], draft, np.asarray([case["draft_tokens"]]),
+                                np.asarray([case["uniforms"]], np.float32), T)
+            assert out["status"][0] == 0
+            assert list(out["tokens"][0]) == case["tokens"], (name, case, out["tokens"][0])
+            assert out["accept_len"][0] == case["accept_len"], (name, case)
+            np.testing.assert_allclose(out["accept_prob"][0], case["accept_prob"], atol=1e-6)
+
+
+def check_golden_greedy():
+    g = _golden("verify_greedy_ties.json")
+    target = _rows(g["target_logits"])[None]
+    for case in g["cases"]:
+        lens = None if "draft_len" not in case else np.asarray([case["draft_len"]])
+        out = oracle.greedy(target, np.asarray([case["draft_tokens"]]), draft_lens=lens)
+        assert out["status"][0] == 0
+        assert list(out["tokens"][0]) == case["tokens"], (case, out["tokens"][0])
+        assert out["accept_len"][0] == case["accept_len"]
+        # the sampling entry at temperature 0 is the same rule
+        out2 = oracle.sample(target, None, np.asarray([case["draft_tokens"]]),
+                             np.zeros((1, g["K"] + 1), np.float32), 0.0, draft_lens=lens)
+        assert list(out2["tokens"][0]) == case["tokens"]
+
+
+def check_golden_tree():
+    g = _golden("verify_tree_small.json")
+    parent = np.asarray(g["parent"], np.int32)
+    for req in g["requests"]:
+        target = _rows(req["target_logits"])[None]
+        out = oracle.tree(target, parent, np.asarray([g["node_tokens"]]), g["max_depth"])
+        assert out["status"][0] == 0
+        assert list(out["tokens"][0]) == req["tokens"], (req, out["tokens"][0])
+        assert list(out["path"][0]) == req["path"], (req, out["path"][0])
+        assert out["accept_len"][0] == req["accept_len"]
+
+
+def check_golden_compact():
+    g = _golden("compact_small.json")
+    cu, packed, bid = oracle.compact(np.asarray(g["tokens"]), np.asarray(g["accept_len"]))
+    assert list(cu) == g["cu"] and list(packed) == g["packed"] and list(bid) == g["batch_id"]
+
+
+# ---------------------------------------------------------------------------
+# exactness by measure (the oracle as a black box)
+# ---------------------------------------------------------------------------
+
+_ONE_MINUS = float(np.nextafter(1.0, 0.0))
+
+
+def _bisect(pred, iters=64):
+    """Boundary b in [0, 1] with pred true on [0, b) and false on [b, 1),
+    for a pred that is monotone (true then false)."""
+    if not pred(0.0):
+        return 0.0
+    if pred(_ONE_MINUS):
+        return 1.0
+    lo, hi = 0.0, _ONE_MINUS
+    for _ in range(iters):
+        mid = 0.5 * (lo + hi)
+        if mid <= lo or mid >= hi:
+            break
+        if pred(mid):
+            lo = mid
+        else:
+            hi = mid
+    return hi
+
+
+class _Request:
+    """One request evaluated by the oracle for chosen drafts and uniforms."""
+
+    def __init__(self, target, draft, T):
+        self.target = np.ascontiguousarray(target[None], np.float32)
+        self.draft = None if draft is None else np.ascontiguousarray(draft[None], np.float32)
+        self.K = target.shape[0] - 1
+        self.T = T
+
+    def run(self, drafts, u):
+        out = oracle.sample(self.target, self.draft, np.asarray([drafts], np.int32),
+                            np.asarray([u], np.float64), self.T)
+        assert out["status"][0] == 0
+        return out["tokens"][0], int(out["accept_len"][0])
+
+
+def _emission_law(req, drafts, i):
+    """Exact law of the token emitted at position i given drafts (with the
+    drafts before i accepted through u_j = 0): returns (theta, residual law)
+    where theta is the measure of u_i giving acceptance and the residual
+    law is the measure of u_K over each token after a rejection at i."""
+    K, V = req.K, req.target.shape[2]
+    base = [0.0] * (K + 1)
+
+    def accepted(a):
+        u = list(base)
+        u[i] = a
+        _, L = req.run(drafts, u)
+        return L > i + 1
+
+    theta = _bisect(accepted) if i < K else 1.0
+    law = np.zeros(V)
+    if i < K and theta >= 1.0:
+        return theta, law
+    u_rej = list(base)
+    if i < K:
+        u_rej[i] = 0.5 * (theta + 1.0) if theta < _ONE_MINUS else _ONE_MINUS
+
+    def token(s):
+        u = list(u_rej)
+        u[K] = s
+        toks, L = req.run(drafts, u)
+        assert L == i + 1
+        return int(toks[i])
+
+    prev = 0.0
+    for t in range(V):
+        edge = 1.0 if t == V - 1 else _bisect(lambda s: token(s) <= t)
+        law[t] = edge - prev
+        prev = edge
+    return theta, law
+
+
+def check_exact_dense(V=5, K=3, T=0.8, seed=0, mask=False):
+    """P(y_i = t | drafts before i accepted) = p_i(t) with x_i ~ q_i, for
+    every position including the bonus, to 1e-12."""
+    rng = np.random.default_rng(seed)
+    l = (rng.standard_normal((K + 1, V)) * 1.3).astype(np.float32)
+    d = (l[:K] + rng.standard_normal((K, V)) * 0.9).astype(np.float32)
+    if mask:
+        l[0, 1] = -np.inf          # a token the target rules out
+        d[min(1, K - 1), 2] = -np.inf  # a token the draft never proposes
+    req = _Request(l, d, T)
+    p = scipy.special.softmax(l.astype(np.float64) / T, axis=-1)
+    q = scipy.special.softmax(d.astype(np.float64) / T, axis=-1)
+    prefix = [int(np.argmax(p[j] * q[j])) for j in range(K)]  # p > 0 and q > 0
+    for i in range(K + 1):
+        emitted = np.zeros(V)
+        xs = range(V) if i < K else [0]
+        for x in xs:
+            if i < K and q[i, x] == 0:
+                continue
+            drafts = prefix[:i] + [x] + prefix[i + 1:] if i < K else list(prefix)
+            theta, law = _emission_law(req, drafts, i)
+            if i < K:
+                emitted[x] += q[i, x] * theta
+                emitted += q[i, x] * (1.0 - theta) * law
+            else:
+                emitted = law
+        np.testing.assert_allclose(emitted, p[i], rtol=0, atol=1e-12,
+                                   err_msg="position %d" % i)
+
+
+def check_exact_onehot(V=5, K=2, T=1.3, seed=1):
+    """Deterministic proposer: for every proposed x, P(y_i = t) = p_i(t);
+    acceptance has measure p_i(x) and the residual never emits x."""
+    rng = np.random.default_rng(seed)
+    l = (rng.standard_normal((K + 1, V)) * 1.5).astype(np.float32)
+    req = _Request(l, None, T)
+    p = scipy.special.softmax(l.astype(np.float64) / T, axis=-1)
+    prefix = [int(np.argmax(p[j])) for j in range(K)]
+    for i in range(K + 1):
+        for x in (range(V) if i < K else [0]):
+            drafts = prefix[:i] + [x] + prefix[i + 1:] if i < K else list(prefix)
+            theta, law = _emission_law(req, drafts, i)
+            if i < K:
+                assert abs(theta - min(1.0, p[i, x])) < 1e-12, (i, x, theta, p[i, x])
+                assert law[x] == 0.0, "residual emitted the rejected draft"
+                emitted = (1.0 - theta) * law
+                emitted[x] += theta
+            else:
+                emitted = law
+            np.testing.assert_allclose(emitted, p[i], rtol=0, atol=1e-12,
+                                       err_msg="position %d draft %d" % (i, x))
+
+
+def check_chi_square(B=1_000_000, V=16, K=3, T=0.9, seed=7, threads=8):
+    """10^6 seeded draws with drafts sampled from q: the emitted token at
+    each position, given the earlier drafts were accepted, follows p_i."""
+    rng = np.random.default_rng(seed)
+    l = (rng.standard_normal((K + 1, V)) * 1.5).astype(np.float32)
+    d = (l[:K] + rng.standard_normal((K, V)) * 0.8).astype(np.float32)
+    p = scipy.special.softmax(l.astype(np.float64) / T, axis=-1)
+    q = scipy.special.softmax(d.astype(np.float64) / T, axis=-1)
+    drafts = np.stack([rng.choice(V, size=B, p=q[i]) for i in range(K)], axis=1).astype(np.int32)
+    u = rng.random((B, K + 1))
+    target = np.ascontiguousarray(np.broadcast_to(l, (B, K + 1, V)))
+    draft = np.ascontiguousarray(np.broadcast_to(d, (B, K, V)))
+    out = oracle.sample(target, draft, drafts, u, T, threads=threads)
+    L = out["accept_len"]
+    assert (out["status"] == 0).all()
+    for i in range(K + 1):
+        sel = L >= i + 1
+        obs = np.bincount(out["tokens"][sel, i], minlength=V)
+        exp = p[i] * sel.sum()
+        pval = scipy.stats.chisquare(obs, exp).pvalue
+        assert pval > 1e-3, "position %d: chi-square p-value %.3g" % (i, pval)
+
+
+# ---------------------------------------------------------------------------
+# invariants and limits
+# ---------------------------------------------------------------------------
+
+def check_invariants(seed=11):
+    rng = np.random.default_rng(seed)
+    B, K, V, T = 400, 4, 50, 1.1
+    l = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    d = (l[:, :K] + rng.standard_normal((B, K, V))).astype(np.float32)
+    drafts = rng.integers(0, V, size=(B, K)).astype(np.int32)
+    lens = rng.integers(0, K + 1, size=B).astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    for dr in (d, None):
+        out = oracle.sample(l, dr, drafts, u, T, draft_lens=lens)
+        L = out["accept_len"]
+        assert (out["status"] == 0).all()
+        assert ((L >= 1) & (L <= lens + 1)).all()
+        for b in range(B):
+            toks = out["tokens"][b]
+            assert (toks[:L[b]] >= 0).all() and (toks[L[b]:] == -1).all()
+            assert (toks[:L[b] - 1] == drafts[b, :L[b] - 1]).all()
+            if L[b] == lens[b] + 1:
+                assert (toks >= 0).sum() == lens[b] + 1
+    # q == p (draft logits equal to the target logits): always accepted
+    out = oracle.sample(l, np.ascontiguousarray(l[:, :K]), drafts, u, T)
+    assert (out["accept_len"] == K + 1).all()
+    np.testing.assert_array_equal(out["accept_prob"], 1.0)
+
+
+def check_onehot_accept_iff_u_below_p(seed=12):
+    rng = np.random.default_rng(seed)
+    B, V, T = 2000, 30, 0.7
+    l = (rng.standard_normal((B, 2, V)) * 2).astype(np.float32)
+    drafts = rng.integers(0, V, size=(B, 1)).astype(np.int32)
+    u = rng.random((B, 2)).astype(np.float32)
+    out = oracle.sample(l, None, drafts, u, T)
+    px = scipy.special.softmax(l[:, 0].astype(np.float64) / T, axis=-1)[np.arange(B), drafts[:, 0]]
+    clear = np.abs(u[:, 0] - px) > 1e-9
+    acc = out["accept_len"] == 2
+    assert (acc[clear] == (u[clear, 0] < px[clear])).all()
+    np.testing.assert_allclose(out["accept_prob"][:, 0], px, rtol=1e-12)
+
+
+def check_zero_probability_draft_rejected():
+    """A draft the target rules out (logit -inf, p = 0) is never accepted,
+    even with u = 0; nor is it drawn by the residual."""
+    l = np.array([[[0.0, -np.inf, 1.0], [0.0, 0.0, 0.0]]], np.float32)
+    for draft in (None, np.array([[[0.0, 2.0, 0.0]]], np.float32)):
+        out = oracle.sample(l, draft, np.array([[1]]), np.array([[0.0, 0.0]], np.float32), 1.0)
+        assert out["accept_len"][0] == 1 and out["tokens"][0, 0] == 0
+        out = oracle.sample(l, draft, np.array([[1]]), np.array([[0.0, 0.6]], np.float32), 1.0)
+        assert out["accept_len"][0] == 1 and out["tokens"][0, 0] == 2
+
+
+def check_temperature_to_zero_is_greedy(seed=13):
+    rng = np.random.default_rng(seed)
+    B, K, V = 300, 3, 40
+    l = rng.permuted(np.tile(np.arange(V, dtype=np.float32) * 0.25, (B, K + 1, 1)), axis=2)
+    am = np.argmax(l, axis=2)
+    drafts = np.where(rng.random((B, K)) < 0.7, am[:, :K], rng.integers(0, V, (B, K)))
+    drafts = drafts.astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32) * 0.98 + 0.01
+    g = oracle.greedy(l, drafts)
+    s = oracle.sample(l, None, drafts, u, 1e-3)
+    np.testing.assert_array_equal(s["tokens"], g["tokens"])
+    np.testing.assert_array_equal(s["accept_len"], g["accept_len"])
+
+
+def check_errors():
+    l = np.zeros((3, 3, 4), np.float32)
+    l[:, :, 0] = 1.0
+    drafts = np.array([[0, 0], [4, 0], [0, -1]], np.int32)
+    out = oracle.sample(l, None, drafts, np.zeros((3, 3), np.float32), 1.0)
+    assert list(out["status"]) == [0, oracle.BAD_TOKEN, oracle.BAD_TOKEN]
+    assert list(out["accept_len"]) == [3, 0, 0]
+    assert (out["tokens"][1:] == -1).all()
+    for bad in (np.nan, np.inf):
+        lb = l[:1].copy()
+        lb[0, 0, 2] = bad
+        out = oracle.sample(lb, None, drafts[:1], np.zeros((1, 3), np.float32), 1.0)
+        assert out["status"][0] == oracle.BAD_LOGITS
+        out = oracle.greedy(lb, drafts[:1])
+        assert out["status"][0] == oracle.BAD_LOGITS
+    lb = l[:1].copy()
+    lb[0, 1, :] = -np.inf
+    assert oracle.sample(lb, None, drafts[:1], np.zeros((1, 3)), 1.0)["status"][0] == oracle.BAD_LOGITS
+    # rows after the first rejection are never needed, so they are not checked
+    lb = l[:1].copy()
+    lb[0, 2, 1] = np.nan
+    out = oracle.sample(lb, None, np.array([[1, 0]]), np.array([[0.9, 0, 0.5]], np.float32), 1.0)
+    assert out["status"][0] == 0 and out["accept_len"][0] == 1
+    out = oracle.sample(l[:1], None, drafts[:1], np.zeros((1, 3)), 1.0,
+                        draft_lens=np.array([3], np.int32))
+    assert out["status"][0] == oracle.BAD_DRAFT_LEN and out["accept_len"][0] == 0
+
+
+# ---------------------------------------------------------------------------
+# tree
+# ---------------------------------------------------------------------------
+
+def _random_tree(rng, N):
+    parent = []
+    for n in range(1, N + 1):
+        parent.append(int(rng.integers(0, n)))
+    return np.asarray(parent, np.int32)
+
+
+def _brute_force_tree(logits, parent, node_tokens):
+    """Longest root path whose every node token equals the argmax of its
+    parent's row (numpy argmax), by enumerating all root paths."""
+    N = len(parent)
+    best = [0]
+    for n in range(1, N + 1):
+        path = [n]
+        while path[-1] != 0:
+            path.append(int(parent[path[-1] - 1]))
+        path = path[::-1]
+        ok = all(node_tokens[c - 1] == int(np.argmax(logits[p])) for p, c in zip(path, path[1:]))
+        if ok and len(path) > len(best):
+            best = path
+    toks = [int(np.argmax(logits[v])) for v in best]
+    return best, toks
+
+
+def check_tree_brute_force(seed=14):
+    rng = np.random.default_rng(seed)
+    for trial in range(60):
+        N = int(rng.integers(1, 25))
+        V = int(rng.integers(2, 9))
+        parent = _random_tree(rng, N)
+        depth = [0]
+        for p in parent:
+            depth.append(depth[p] + 1)
+        D = max(depth)
+        B = 6
+        logits = rng.integers(0, 3, size=(B, N + 1, V)).astype(np.float32)
+        tokens = np.zeros((B, N), np.int32)
+        for b in range(B):
+            for p in range(N + 1):
+                ch = [c for c in range(1, N + 1) if parent[c - 1] == p]
+                if not ch:
+                    continue
+                cand = [int(t) for t in rng.permutation(V)]
+                if rng.random() < 0.8:  # make the matching child likely
+                    a = int(np.argmax(logits[b, p]))
+                    cand.remove(a)
+                    cand.insert(int(rng.integers(0, min(len(ch), V))), a)
+                while len(cand) < len(ch):  # more children than tokens: repeats
+                    cand.append(int(rng.integers(0, V)))
+                for c, t in zip(ch, cand):
+                    tokens[b, c - 1] = t
+        out = oracle.tree(logits, parent, tokens, D)
+        for b in range(B):
+            sib_distinct = all(len({int(tokens[b, c - 1]) for c in range(1, N + 1)
+                                    if parent[c - 1] == p}) ==
+                               sum(1 for c in range(1, N + 1) if parent[c - 1] == p)
+                               for p in range(N + 1))
+            if not sib_distinct:
+                continue
+            path, toks = _brute_force_tree(logits[b], parent, tokens[b])
+            L = int(out["accept_len"][b])
+            assert L == len(path), (trial, b, L, path)
+            assert list(out["path"][b, :L]) == path
+            assert list(out["tokens"][b, :L]) == toks
+            assert (out["tokens"][b, L:] == -1).all() and (out["path"][b, L:] == -1).all()
+
+
+def check_tree_errors():
+    parent = np.array([0, 0, 1], np.int32)
+    l = np.zeros((2, 4, 3), np.float32)
+    toks = np.array([[0, 1, 2], [0, 3, 2]], np.int32)
+    out = oracle.tree(l, parent, toks, 2)
+    assert list(out["status"]) == [0, oracle.BAD_TOKEN]
+    try:
+        oracle.tree(l, np.array([0, 2, 1], np.int32), toks, 2)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a parent that is not an earlier node must be rejected")
+    try:
+        oracle.tree(l, parent, toks, 1)
+    except ValueError:
+        pass
+    else:
+        raise AssertionError("a tree deeper than max_depth must be rejected")
+
+
+ALL_CHECKS = [
+    check_softmax_matches_scipy, check_argmax_matches_numpy,
+    check_inverse_cdf_matches_searchsorted, check_golden_sampling, check_golden_greedy,
+    check_golden_tree, check_golden_compact, check_exact_dense, check_exact_onehot,
+    check_invariants, check_onehot_accept_iff_u_below_p,
+    check_zero_probability_draft_rejected, check_temperature_to_zero_is_greedy,
+    check_errors, check_tree_brute_force, check_tree_errors,
+]

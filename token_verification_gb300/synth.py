@@ -1,0 +1,260 @@
+"""Seeded synthetic inputs for the verification step.
+
+This module is the one piece shared by the tests, the benchmark and the
+oracle runs: it draws inputs and nothing else.  It holds none of the
+verification arithmetic (no softmax, no acceptance test, no inverse-CDF
+draw).  Where a workload needs draft tokens *sampled* from a draft
+distribution, they are drawn with the Gumbel-max construction
+(argmax of d/T + Gumbel noise), which samples from softmax(d/T) without
+computing it; where the proposer is deterministic, drafts come from a plain
+argmax or a uniform id, as that proposer would produce them.
+
+Recipe (all draws from numpy's PCG64 streams, seeded per quantity):
+  target logits  l = 3 * N(0, 1) + prior[j],  prior[perm[r]] = -1.1 * ln(r + 1)
+                 with perm a seeded permutation of the vocabulary (a log-Zipf
+                 prior with s = 1.1), then rounded to bfloat16 (round to
+                 nearest even) unless the workload is fp32;
+  draft logits   d = l + N(0, sigma^2) on the rounded l, rounded the same way;
+  draft tokens   dense drafts: Gumbel-max samples of softmax(d / T) taken in
+                 float64 from the rounded d; one-hot (n-gram style) drafts: per
+                 position with probability p_argmax the argmax of the target
+                 row, otherwise a uniform id;
+  uniforms       U[0, 1) float32, one per position for the acceptance test and
+                 one per request (last column) for the residual / bonus draw;
+  tree tokens    children of a node take the top-k ids of a noisy copy
+                 (sigma = 0.5) of the node's own target row, in descending
+                 order, k = the node's child count.
+
+The five workloads mirror the vocabularies and draft lengths the pages use
+(Llama-3, Qwen, DeepSeek-V3 vocabularies; K = 1..5; batch up to 256).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import Optional
+
+import numpy as np
+
+# name, shapes and draft structure of the five standard workloads
+WORKLOADS = {
+    0: dict(name="tiny-dense-B4-K3-V1024-fp32", kind="sample", B=4, K=3, V=1024,
+            dtype="f32", T=1.0, drafts="dense", sigma=0.7),
+    1: dict(name="llama3-vocab-dense-B64-K3-V128256", kind="sample", B=64, K=3, V=128256,
+            dtype="bf16", T=0.8, drafts="dense", sigma=0.5),
+    2: dict(name="qwen-vocab-onehot-B256-K5-V152064", kind="sample", B=256, K=5, V=152064,
+            dtype="bf16", T=1.0, drafts="onehot", p_argmax=0.6),
+    3: dict(name="dsv3-vocab-mtp-B128-K1-V129280", kind="sample", B=128, K=1, V=129280,
+            dtype="bf16", T=1.0, drafts="dense", sigma=0.25),
+    4: dict(name="medusa-tree-B32-N60-V32000", kind="tree", B=32, V=32000, dtype="bf16",
+            sigma=0.5, tree="medusa60"),
+}
+
+
+@dataclass
+class Workload:
+    """Host-side inputs.  Logits are float32 arrays for fp32 workloads and
+    uint16 arrays of bfloat16 bit patterns for bf16 workloads."""
+    dtype: str
+    B: int
+    V: int
+    target: np.ndarray
+    K: int = 0
+    T: float = 1.0
+    draft: Optional[np.ndarray] = None
+    draft_tokens: Optional[np.ndarray] = None
+    draft_lens: Optional[np.ndarray] = None
+    uniforms: Optional[np.ndarray] = None
+    parent: Optional[np.ndarray] = None
+    node_tokens: Optional[np.ndarray] = None
+    max_depth: int = 0
+    meta: dict = field(default_factory=dict)
+
+    def logits_as_float(self, which="target"):
+        a = getattr(self, which)
+        return bf16_bits_to_float(a) if self.dtype == "bf16" else a
+
+
+# ---------------------------------------------------------------------------
+# elementary draws
+# ---------------------------------------------------------------------------
+
+def _rng(seed, *stream):
+    return np.random.default_rng([int(seed)] + [int(s) for s in stream])
+
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns, round to nearest even (torch's
+    conversion)."""
+    import torch
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32))
+    return t.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_to_float(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
+def zipf_prior(rng, V, s=1.1):
+    perm = rng.permutation(V)
+    prior = np.empty(V, np.float32)
+    prior[perm] = (-s * np.log(np.arange(1, V + 1, dtype=np.float64))).astype(np.float32)
+    return prior
+
+
+def target_logits(rng, rows, V, scale=3.0):
+    """[rows, V] float32: scale * N(0,1) + a log-Zipf prior over a seeded
+    permutation of the vocabulary."""
+    prior = zipf_prior(rng, V)
+    out = rng.standard_normal((rows, V), dtype=np.float32)
+    out *= np.float32(scale)
+    out += prior[None, :]
+    return out
+
+
+def gumbel_max_tokens(rng, logits_f64, T):
+    """One sample per row from softmax(logits / T) by the Gumbel-max
+    construction (argmax of logits / T + Gumbel noise)."""
+    g = -np.log(-np.log(rng.random(logits_f64.shape)))
+    return np.argmax(logits_f64 / T + g, axis=-1).astype(np.int32)
+
+
+def _finish(x, dtype):
+    return round_to_bf16_bits(x) if dtype == "bf16" else np.ascontiguousarray(x, np.float32)
+
+
+def _as_float(x, dtype):
+    return bf16_bits_to_float(x) if dtype == "bf16" else x
+
+
+# ---------------------------------------------------------------------------
+# sampling / greedy workloads
+# ---------------------------------------------------------------------------
+
+def make_sample_case(B, K, V, *, dtype="bf16", T=1.0, drafts="dense", sigma=0.5,
+                     p_argmax=0.6, seed=0, draft_lens=None, mask_frac=0.0,
+                     quantize=None, uniform_seed=None) -> Workload:
+    """A verification batch.  ``drafts`` is 'dense' (draft logits given) or
+    'onehot' (deterministic proposer, no draft logits).  ``mask_frac`` sets
+    that fraction of logits to -inf (never a whole row); ``quantize`` rounds
+    logits to multiples of that step (to create exact ties)."""
+    r_l, r_d, r_t, r_m = (_rng(seed, 1), _rng(seed, 2), _rng(seed, 3), _rng(seed, 4))
+    r_u = np.random.default_rng(int(seed) if uniform_seed is None else int(uniform_seed))
+    tl = target_logits(r_l, B * (K + 1), V)
+    if quantize:
+        tl = (np.round(tl / quantize) * quantize).astype(np.float32)
+    if mask_frac > 0:
+        m = r_m.random(tl.shape) < mask_frac
+        m[:, 0] = False  # keep one finite logit per row
+        tl[m] = -np.inf
+    target = _finish(tl, dtype).reshape(B, K + 1, V)
+    tf = _as_float(target, dtype)
+    draft = None
+    if drafts == "dense":
+        noise = r_d.standard_normal((B, K, V), dtype=np.float32) * np.float32(sigma)
+        dl = tf[:, :K, :] + noise
+        draft = _finish(dl, dtype).reshape(B, K, V)
+        df = _as_float(draft, dtype).astype(np.float64)
+        if T > 0:
+            toks = gumbel_max_tokens(r_t, df, T)
+        else:
+            toks = np.argmax(df, axis=-1).astype(np.int32)
+    elif drafts == "onehot":
+        take_argmax = r_t.random((B, K)) < p_argmax
+        rand_ids = r_t.integers(0, V, size=(B, K), dtype=np.int64).astype(np.int32)
+        am = np.argmax(tf[:, :K, :], axis=-1).astype(np.int32) if K > 0 else rand_ids
+        toks = np.where(take_argmax, am, rand_ids).astype(np.int32)
+    else:
+        raise ValueError("drafts must be 'dense' or 'onehot'")
+    uniforms = r_u.random((B, K + 1), dtype=np.float32)
+    lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, np.int32)
+    return Workload(dtype=dtype, B=B, V=V, K=K, T=float(T), target=target, draft=draft,
+                    draft_tokens=np.ascontiguousarray(toks.reshape(B, K), np.int32),
+                    draft_lens=lens, uniforms=uniforms,
+                    meta=dict(drafts=drafts, sigma=sigma, seed=seed))
+
+
+# ---------------------------------------------------------------------------
+# tree workloads
+# ---------------------------------------------------------------------------
+
+def medusa60_parent():
+    """The 60-node candidate tree: top-3 x top-3 x top-2 x top-1 beneath the
+    root in breadth-first order (3 + 9 + 18 + 18 = 48 nodes), plus one
+    top-1 child under each of the first 12 depth-4 nodes (nodes 49..60),
+    so N = 60 and the depth is 5.  Returns parent[n-1] for n = 1..60."""
+    parent = []
+    level = [0]
+    nid = 1
+    for k in (3, 3, 2, 1):
+        nxt = []
+        for p in level:
+            for _ in range(k):
+                parent.append(p)
+                nxt.append(nid)
+                nid += 1
+        level = nxt
+    for p in level[:12]:
+        parent.append(p)
+        nid += 1
+    return np.asarray(parent, np.int32)
+
+
+def tree_depths(parent):
+    d = [0]
+    for n, p in enumerate(parent, start=1):
+        d.append(d[p] + 1)
+    return np.asarray(d, np.int32)
+
+
+def make_tree_case(B, V, parent, *, dtype="bf16", sigma=0.5, seed=0, mask_frac=0.0,
+                   quantize=None) -> Workload:
+    parent = np.asarray(parent, np.int32)
+    N = parent.size
+    r_l, r_d, r_m = _rng(seed, 11), _rng(seed, 12), _rng(seed, 14)
+    tl = target_logits(r_l, B * (N + 1), V)
+    if quantize:
+        tl = (np.round(tl / quantize) * quantize).astype(np.float32)
+    if mask_frac > 0:
+        m = r_m.random(tl.shape) < mask_frac
+        m[:, 0] = False
+        tl[m] = -np.inf
+    target = _finish(tl, dtype).reshape(B, N + 1, V)
+    tf = _as_float(target, dtype)
+    children = [[] for _ in range(N + 1)]
+    for n, p in enumerate(parent, start=1):
+        children[p].append(n)
+    node_tokens = np.zeros((B, N), np.int32)
+    for b in range(B):
+        for p in range(N + 1):
+            ch = children[p]
+            if not ch:
+                continue
+            noisy = tf[b, p].astype(np.float64) + sigma * r_d.standard_normal(V)
+            order = np.argsort(-noisy, kind="stable")[: len(ch)]
+            for c, tok in zip(ch, order):
+                node_tokens[b, c - 1] = tok
+    depth = int(tree_depths(parent).max()) if N else 0
+    return Workload(dtype=dtype, B=B, V=V, target=target, parent=parent,
+                    node_tokens=node_tokens, max_depth=depth,
+                    meta=dict(sigma=sigma, seed=seed, N=N))
+
+
+# ---------------------------------------------------------------------------
+# the standard workloads
+# ---------------------------------------------------------------------------
+
+def make_workload(index: int, seed: int = 0) -> Workload:
+    """The standard workload ``index`` (0..4), seeded by ``seed + index``
+    for its uniforms and by (seed + index, stream) for everything else."""
+    w = WORKLOADS[index]
+    s = seed + index
+    if w["kind"] == "tree":
+        wl = make_tree_case(w["B"], w["V"], medusa60_parent(), dtype=w["dtype"],
+                            sigma=w["sigma"], seed=s)
+    else:
+        wl = make_sample_case(w["B"], w["K"], w["V"], dtype=w["dtype"], T=w["T"],
+                              drafts=w["drafts"], sigma=w.get("sigma", 0.0),
+                              p_argmax=w.get("p_argmax", 0.6), seed=s, uniform_seed=s)
+    wl.meta["workload"] = w["name"]
+    wl.meta["index"] = index
+    return wl
