@@ -1,0 +1,403 @@
+#!/usr/bin/env python
+"""Throughput of the speculative-decoding verification step on GB300.
+
+One step = one verify call over one batch of the workload: B=256 requests,
+K=5 one-hot draft positions, V=152064 bf16 logits (Qwen vocabulary), T=1.
+The default prints one JSON line with calls/s (device-timed, inputs resident
+in HBM), the roofline of the dominant kernel (logit bytes / kernel time
+against the measured HBM copy bandwidth), an end-to-end figure through the
+C ABI with host buffers, and the fp64 CPU oracle timed on the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload I]
+  python bench.py --impl reference ...   (the oracle as the reference arm)
+
+Multi-GPU (torchrun, one rank per GPU): every rank verifies its own batch
+(weak scaling, no collective on the data path); timing is bracketed by
+barriers and the slowest rank's time is used.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "verify calls/s and logits HBM GB/s (% of GB300 peak) at B=256 K=5 V=152064"
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SOURCES = ["token_verification_gb300/csrc/sv_verify.cu",
+                  "token_verification_gb300/csrc/sv_common.cuh"]
+
+
+# ---------------------------------------------------------------------------
+# distributed helpers (host logic; tested with gloo on CPU)
+# ---------------------------------------------------------------------------
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_seed(base_seed, rank):
+    """Each rank verifies its own batch (weak scaling): seed offset by rank."""
+    return base_seed + 1000 * rank
+
+
+def aggregate(elapsed_s, units, world, backend_device=None):
+    """(max elapsed over ranks, total units over ranks); identity when world = 1."""
+    if world <= 1:
+        return elapsed_s, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_s], dtype=torch.float64, device=backend_device)
+    u = torch.tensor([float(units)], dtype=torch.float64, device=backend_device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ---------------------------------------------------------------------------
+# peaks, clocks, profile traffic
+# ---------------------------------------------------------------------------
+
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            v = float(json.load(f)["hbm_gbs"])
+        return v, "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(name):
+    """DRAM bytes per launch recorded in profiles/<name>.md, if the profile
+    was taken on the current kernel sources (else None)."""
+    path = os.path.join(ROOT, "profiles", name + ".md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
+    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+        return None
+    return int(m_bytes.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons (read-only)."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.samples = []
+        self._stop = threading.Event()
+        self._proc = None
+        self._thread = None
+        self.window = None
+
+    def start(self):
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self._proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self._proc.stdout:
+            self.samples.append((time.time(), line.strip()))
+
+    def mark(self, t0, t1):
+        self.window = (t0, t1)
+
+    def stop(self):
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except Exception:
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        rows = []
+        for ts, line in self.samples:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((ts, parts))
+        if self.window:
+            inside = [r for r in rows if self.window[0] <= r[0] <= self.window[1]]
+            if inside:
+                rows = inside
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(p[1]) for _, p in rows if p[1].replace(".", "").isdigit()]
+        smax = [float(p[2]) for _, p in rows if p[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, p in rows:
+            for name, val in zip(names, p[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# the CPU oracle baseline
+# ---------------------------------------------------------------------------
+
+def oracle_sample_run(wl, requests, threads):
+    import oracle
+    sub = slice(0, requests)
+    t0 = time.perf_counter()
+    oracle.sample(wl.target[sub], None if wl.draft is None else wl.draft[sub],
+                  wl.draft_tokens[sub], wl.uniforms[sub], wl.T, threads=threads)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline(wl, budget_s=12.0):
+    threads = os.cpu_count() or 1
+    probe = min(wl.B, max(threads, 8))
+    dt = oracle_sample_run(wl, probe, threads)
+    per_req = dt / probe
+    reps = max(1, min(50, int(budget_s / max(per_req * wl.B, 1e-9))))
+    reqs = min(wl.B, max(probe, int(budget_s / max(per_req, 1e-9))))
+    total = 0.0
+    done = 0
+    for _ in range(reps if reqs == wl.B else 1):
+        total += oracle_sample_run(wl, reqs, threads)
+        done += reqs
+    calls_per_s = (done / wl.B) / total
+    return {"value": calls_per_s, "unit": "calls/s", "cores": threads, "kind": "oracle",
+            "sample": "%d requests of the B=%d batch (%.1f s of fp64 CPU work, %d threads)"
+                      % (done, wl.B, total, threads)}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    from token_verification_gb300 import synth
+    wl = synth.make_workload(args.workload)
+    threads = os.cpu_count() or 1
+    req = args.ref_requests
+    for _ in range(args.warmup):
+        oracle_sample_run(wl, req, threads)
+    t = 0.0
+    for _ in range(args.steps):
+        t += oracle_sample_run(wl, req, threads)
+    value = (args.steps * req / wl.B) / t
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "calls/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": workload_config(wl, args),
+            "cpu_baseline": {"value": value, "unit": "calls/s", "cores": threads, "kind": "oracle",
+                             "sample": "%d of %d requests per step" % (req, wl.B)},
+            "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(wl, args):
+    return {"workload": wl.meta["workload"], "B": wl.B, "K": wl.K, "V": wl.V,
+            "logits": wl.dtype, "drafts": wl.meta.get("drafts"), "temperature": wl.T,
+            "l2": "inputs larger than L2: %d MB of logits per call, 2 rotating input sets"
+                  % (wl.target.nbytes // 2**20),
+            "parallelism": "dp%d" % dist_env()[0]}
+
+
+def run_ours(args):
+    import torch
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    from token_verification_gb300 import api, synth
+    from token_verification_gb300 import _native
+    _native.lib()
+
+    wl = synth.make_workload(args.workload, seed=shard_seed(0, rank))
+    assert wl.draft is None, "the benchmarked workload has one-hot drafts"
+    B, K, V = wl.B, wl.K, wl.V
+    tgt_host = torch.from_numpy(wl.target.view(np.int16)).view(torch.bfloat16)
+    sets = []
+    for s in range(2):  # two resident input sets, used alternately
+        perm = np.roll(np.arange(B), s * (B // 2))
+        sets.append(dict(
+            target=tgt_host[perm].contiguous().to(device),
+            tokens=torch.from_numpy(wl.draft_tokens[perm]).to(device),
+            uniforms=torch.from_numpy(wl.uniforms[perm]).to(device)))
+    out = api.alloc_outputs(B, K, device)
+    out_kernel = api.alloc_outputs(B, K, device, packed=False, accept_prob=False, status=False)
+    stream = torch.cuda.current_stream(device)
+
+    def step(i, o=out):
+        s = sets[i & 1]
+        api.spec_verify_sample(s["target"], None, s["tokens"], s["uniforms"], wl.T, o)
+
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(local) if rank == 0 else None
+    if sampler:
+        sampler.start()
+        time.sleep(0.3)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    w0 = time.time()
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    w1 = time.time()
+    if world > 1:
+        torch.distributed.barrier()
+    elapsed = ev0.elapsed_time(ev1) / 1e3
+    if sampler:
+        sampler.mark(w0, w1)
+    max_elapsed, total_calls = aggregate(elapsed, args.steps, world, device)
+    mean_len = float(out.accept_len.float().mean().item())
+
+    # dominant kernel alone: the call without packed outputs is one launch of
+    # the row-statistics kernel; per-launch event pairs on the same stream
+    kernel_iters = max(20, min(args.steps, 2000))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(kernel_iters)]
+    for i in range(kernel_iters):
+        evs[i][0].record(stream)
+        step(i, out_kernel)
+        evs[i][1].record(stream)
+    torch.cuda.synchronize()
+    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    if sampler:
+        sampler.stop()
+
+    # end to end through the C ABI with host buffers (pinned): H2D of the
+    # step's inputs, the call, D2H of its results, every step
+    e2e = None
+    if rank == 0:
+        pin = dict(target=tgt_host.pin_memory(),
+                   tokens=torch.from_numpy(wl.draft_tokens).pin_memory(),
+                   uniforms=torch.from_numpy(wl.uniforms).pin_memory())
+        res_tok = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
+        res_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+        dev_in = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
+        e2e_steps = max(3, min(args.steps, args.e2e_steps))
+
+        def e2e_step():
+            for k in pin:
+                dev_in[k].copy_(pin[k], non_blocking=True)
+            api.spec_verify_sample(dev_in["target"], None, dev_in["tokens"], dev_in["uniforms"],
+                                   wl.T, out)
+            res_tok.copy_(out.tokens, non_blocking=True)
+            res_len.copy_(out.accept_len, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        b.record(stream)
+        torch.cuda.synchronize()
+        e2e_s = a.elapsed_time(b) / 1e3
+        h2d = sum(v.numel() * v.element_size() for v in pin.values())
+        d2h = res_tok.numel() * 4 + res_len.numel() * 4
+        e2e = {"value": e2e_steps / e2e_s, "unit": "calls/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "steps": e2e_steps}
+
+    if rank == 0:
+        logit_bytes = B * (K + 1) * V * 2
+        peak, peak_kind = hbm_peak()
+        achieved = logit_bytes / (kern_ms / 1e3) / 1e9
+        value = total_calls / max_elapsed
+        line = {
+            "metric": METRIC, "value": value, "unit": "calls/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": workload_config(wl, args),
+            "draft_tokens_per_s": value * B * K,
+            "hbm_gbs": logit_bytes * value / 1e9,
+            "mean_accept_len": mean_len,
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                         "frac": achieved / peak, "peak_source": peak_kind,
+                         "kernel": "verify_rows_kernel (one-hot, bf16)",
+                         "kernel_ms": kern_ms, "algorithmic_bytes": logit_bytes,
+                         "traffic": profiled_traffic("verify_rows_onehot_B256_K5_V152064")},
+            "gpu_launches": args.steps * 2,
+            "clocks": sampler.summary() if sampler else None,
+            "e2e": e2e,
+        }
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline(wl)
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--workload", type=int, default=2)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--ref-requests", type=int, default=8)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

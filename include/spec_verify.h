@@ -1,0 +1,186 @@
+/*
+ * spec_verify.h - C ABI of libspecverify, the GB300 (sm_103a) implementation
+ * of the target-model verification step of speculative decoding.
+ *
+ * The method is the one stated on these pages:
+ *   "【大模型基础设施工程】15：推测解码与 MTP" (juejin.cn), §2.1 "算法骨架":
+ *     accept draft x_i with probability min(1, p_i(x_i) / q_i(x_i)); at the
+ *     first rejection draw one token from norm(max(0, p_i - q_i)) and stop;
+ *     if all K drafts are accepted draw one extra token from p_{K+1}.
+ *   the same page, "1.2 正确性保证" (inside part 2): the emitted tokens are
+ *     distributed exactly as sampling from the target;
+ *   the same page, §2.3: 1 <= accept length <= K+1;
+ *   the same page, §3.3 "Tree Attention": candidate trees, each node sees only
+ *     its ancestors, the longest accepted root path wins;
+ *   the same page, §11: greedy (do_sample=False) output equals plain decoding;
+ *   "投机解码" (FastDeploy docs), "高效投机解码框架设计": per-sample parallel
+ *     sampling+verification; output tokens located by batch id through
+ *     padding-free indexing instead of copies and slices.
+ *
+ * Conventions shared by every entry point
+ *   - Tensor pointers are DEVICE pointers to caller-owned, contiguous,
+ *     row-major memory, unless marked HOST.  The library never allocates,
+ *     frees or retains them; it reads inputs and writes outputs on `stream`.
+ *   - Calls are asynchronous and stream-ordered: they return after queueing
+ *     the kernels; nothing is synchronised.  `stream` is a cudaStream_t
+ *     (NULL = the legacy default stream).
+ *   - The return value reports ARGUMENT errors found on the host before any
+ *     launch (nothing is queued then), or SV_ERR_CUDA if a launch failed.
+ *   - DATA errors found on the device never trap or hang: they set bits in
+ *     the request's status word (SV_REQ_*), and that request emits nothing
+ *     (accept_len 0, all token slots -1).
+ *   - Token ids are int32.  Unused output token slots hold -1.
+ *   - Logits are bfloat16 or IEEE fp32 (sv_dtype).  Every logit must be finite
+ *     or -inf (masking); each row that the rule needs must hold at least one
+ *     finite logit.  NaN or +inf in a needed row is a data error.  |logit / T|
+ *     must be representable in fp32.
+ *   - A workspace (device memory, >= spec_verify_workspace_size bytes,
+ *     256-byte aligned) holds per-call scratch: chunk records, row summaries
+ *     and arrival counters.  Zero-fill a newly allocated workspace once with
+ *     spec_verify_workspace_init.  The counters must be zero when a call
+ *     starts; every call leaves them zero, and when a workspace is used with a
+ *     different (B, K, mode) than on its previous call, the library first
+ *     zero-fills the counter region on the call's stream (one small
+ *     cudaMemsetAsync).  Calls that share a workspace must be ordered on one
+ *     stream: concurrent calls need separate workspaces.
+ */
+#ifndef SPEC_VERIFY_H_
+#define SPEC_VERIFY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* sv_stream_t;
+
+typedef enum sv_status {
+  SV_OK = 0,
+  SV_ERR_NULL = 1,        /* a required pointer is NULL */
+  SV_ERR_SHAPE = 2,       /* B, K, V, N or max_depth outside the supported range */
+  SV_ERR_DTYPE = 3,       /* unknown sv_dtype */
+  SV_ERR_TEMPERATURE = 4, /* temperature negative, NaN or infinite */
+  SV_ERR_TREE = 5,        /* parent array: a parent not an earlier node, or depth > max_depth */
+  SV_ERR_WORKSPACE = 6,   /* workspace NULL, not 256-byte aligned, or too small */
+  SV_ERR_CUDA = 7         /* a CUDA runtime call or kernel launch failed */
+} sv_status;
+
+typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
+
+/* Per-request device status bits (out_status). */
+#define SV_REQ_BAD_TOKEN 1     /* a draft / tree token outside [0, V) */
+#define SV_REQ_BAD_LOGITS 2    /* a needed row has NaN or +inf, or no finite logit */
+#define SV_REQ_BAD_DRAFT_LEN 4 /* draft_lens[b] outside [0, K] */
+
+/* Limits. */
+#define SV_MAX_K 31             /* draft positions per request */
+#define SV_MAX_B 65536          /* requests per call */
+#define SV_MAX_V (1 << 24)      /* vocabulary size */
+#define SV_MAX_TREE_NODES 256   /* candidate nodes per tree (root excluded) */
+
+/* Bytes of workspace that spec_verify_sample / _greedy need for B requests
+ * of K draft positions over a vocabulary of V (the dense-draft sampling case,
+ * the largest).  spec_verify_tree needs none.  Returns 0 if out of range. */
+size_t spec_verify_workspace_size(int B, int K, int V);
+
+/* Zero-fill a workspace on `stream` (one cudaMemsetAsync).  Needed once per
+ * workspace before its first use. */
+sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream);
+
+/* Rejection-sampling verification ("推测解码与 MTP" §2.1).
+ *
+ *   target_logits  [B, K+1, V] dtype: row i < K scores draft position i,
+ *                  row K is the extra (bonus) position.
+ *   draft_logits   [B, K, V] dtype, or NULL.  Given: q_i = softmax(d_i / T),
+ *                  the same temperature as the target (the drafts are assumed
+ *                  sampled from exactly that q).  NULL: one-hot drafts from a
+ *                  deterministic proposer (n-gram / prompt lookup), q_i is the
+ *                  point mass at x_i: acceptance probability p_i(x_i), residual
+ *                  p_i with x_i removed and renormalised.
+ *   draft_tokens   [B, K] int32, the drafts x_i.  May be NULL when K == 0.
+ *   uniforms       [B, K+1] fp32 in [0, 1): column i < K drives the test at
+ *                  position i (accept iff u_i * q_i(x_i) < p_i(x_i)); column K
+ *                  drives the residual or bonus draw: the emitted token is the
+ *                  smallest j whose cumulative weight exceeds u_K times the total.
+ *   temperature    T > 0: p_i = softmax(target_i / T).  T == 0 selects the greedy
+ *                  rule of spec_verify_greedy (draft_logits and uniforms unused;
+ *                  out_accept_prob reports 1 for a match and 0 for a mismatch).
+ *   out_tokens     [B, K+1] int32: x_0 .. x_{n-1}, then the drawn token, then -1.
+ *   out_accept_len [B] int32: n + 1 emitted tokens (1 <= n+1 <= K_b+1), or 0 for
+ *                  a request with a data error.
+ *   dtype, B, K, V 1 <= B <= SV_MAX_B, 0 <= K <= SV_MAX_K, 1 <= V <= SV_MAX_V.
+ *   draft_lens     [B] int32 or NULL: per-request draft count K_b <= K (ragged
+ *                  drafts).  Rows beyond K_b are never read; the bonus position
+ *                  of request b is row K_b; the draw still uses column K.
+ *   out_cu_accept  [B+1] int32 or NULL: exclusive prefix sum of out_accept_len.
+ *   out_packed     [B*(K+1)] int32 or NULL: the emitted tokens of all requests
+ *                  back to back (request b at out_cu_accept[b]..), then -1.
+ *   out_batch_id   [B*(K+1)] int32 or NULL: the request of each packed token, -1
+ *                  past the end.  (Any of the three packed outputs may be given
+ *                  alone; out_cu_accept is computed either way.)
+ *   out_accept_prob [B, K] fp32 or NULL: min(1, p_i(x_i)/q_i(x_i)) at each
+ *                  tested position (i <= n, i < K_b), -1 elsewhere.
+ *   out_status     [B] int32 or NULL: SV_REQ_* bits per request.
+ *   workspace, ws_bytes  see the conventions above.
+ */
+sv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
+                             const int32_t* draft_tokens, const float* uniforms,
+                             float temperature, int32_t* out_tokens, int32_t* out_accept_len,
+                             sv_dtype dtype, int B, int K, int V, const int32_t* draft_lens,
+                             int32_t* out_cu_accept, int32_t* out_packed,
+                             int32_t* out_batch_id, float* out_accept_prob,
+                             int32_t* out_status, void* workspace, size_t ws_bytes,
+                             sv_stream_t stream);
+
+/* Greedy verification ("推测解码与 MTP" §11, temperature 0): x_i is accepted
+ * while it equals the argmax of target row i (lowest index among equal
+ * maxima; -0.0 == +0.0); the first mismatch emits that argmax; if all K_b
+ * match, the argmax of row K_b is the extra token.  Arguments as in
+ * spec_verify_sample.  Bit-exact: the argmax is taken on the stored values. */
+sv_status spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens,
+                             int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype,
+                             int B, int K, int V, const int32_t* draft_lens,
+                             int32_t* out_cu_accept, int32_t* out_packed,
+                             int32_t* out_batch_id, int32_t* out_status, void* workspace,
+                             size_t ws_bytes, sv_stream_t stream);
+
+/* Greedy tree verification (Medusa / EAGLE; "推测解码与 MTP" §3.3).
+ *
+ *   target_logits  [B, N+1, V] dtype: row 0 is the root (the last committed
+ *                  token), row n the target's logits after candidate node n.
+ *   tree_parent    HOST [N] int32: parent of node n (n = 1..N) at index n-1;
+ *                  must satisfy 0 <= parent < n (an earlier node; breadth-first
+ *                  order qualifies).  Copied into the launch; not retained.
+ *   tree_tokens    [B, N] int32: the candidate token of node n at index n-1.
+ *   out_tokens     [B, max_depth+1] int32: the target argmax at each node of the
+ *                  accepted path (root first): the accepted node tokens followed
+ *                  by the extra token; -1 after.
+ *   out_accept_len [B] int32: accepted nodes + 1, or 0 on a data error.
+ *   N, max_depth   0 <= N <= SV_MAX_TREE_NODES; max_depth >= the tree's depth.
+ *   out_path       [B, max_depth+1] int32 or NULL: node ids of the path from the
+ *                  root (0) on, -1 after.
+ *   out_status     [B] int32 or NULL: SV_REQ_* bits.
+ * A node is accepted when its token equals the argmax at its parent and its
+ * parent is accepted.  With distinct sibling tokens (top-k candidates) the
+ * accepted nodes form one chain and the walk returns the longest accepted
+ * path; if a caller repeats a token among siblings, the lowest node id wins.
+ * Only the rows on the accepted path are read. */
+sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent,
+                           const int32_t* tree_tokens, int32_t* out_tokens,
+                           int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
+                           int max_depth, int32_t* out_path, int32_t* out_status,
+                           sv_stream_t stream);
+
+/* Human-readable name of a status code (static storage). */
+const char* spec_verify_status_string(sv_status status);
+
+/* Library ABI version: 100 * major + minor. */
+int spec_verify_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPEC_VERIFY_H_ */

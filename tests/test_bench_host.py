@@ -1,0 +1,77 @@
+"""Host-side logic of bench.py (no GPU): multi-rank aggregation over two
+gloo ranks, per-rank sharding, clock-sample parsing, and the reference arm
+(the fp64 oracle) end to end on the tiny workload."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    t, u = bench.aggregate(elapsed_s=1.0 + rank, units=10 * (rank + 1), world=world)
+    q.put((rank, t, u, bench.shard_seed(0, rank)))
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_aggregate_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    for rank, t, u, seed in res:
+        assert t == 2.0            # slowest rank's time
+        assert u == 30.0           # all ranks' units
+    assert res[0][3] != res[1][3]  # each rank verifies its own batch
+
+
+def test_aggregate_single_rank_identity():
+    assert bench.aggregate(1.5, 7, world=1) == (1.5, 7)
+
+
+def test_clock_summary_parsing():
+    s = bench.ClockSampler(0)
+    s.samples = [(1.0, "0, 1900, 2070, 800.5, 0x0, Not Active, Not Active, Not Active, Not Active"),
+                 (2.0, "0, 1950, 2070, 900.0, 0x4, Not Active, Not Active, Not Active, Active"),
+                 (9.0, "0, 500, 2070, 100.0, 0x0, Not Active, Not Active, Not Active, Not Active")]
+    s.mark(0.5, 2.5)
+    out = s.summary()
+    assert out["sm_mhz"] == 1925.0 and out["sm_max_mhz"] == 2070.0
+    assert out["reasons"] == ["sw_power_cap"] and out["samples"] == 2
+
+
+def test_reference_arm_prints_one_json_line():
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--workload", "0", "--steps", "2", "--warmup", "3"],
+                       capture_output=True, text=True, timeout=300, cwd=ROOT)
+    assert r.returncode == 0, r.stderr
+    lines = [l for l in r.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["value"] > 0 and d["unit"] == "calls/s"
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["cpu_baseline"]["kind"] == "oracle"

@@ -1,0 +1,216 @@
+"""CUDA path vs the fp64 oracle, through the C ABI (needs a GPU).
+
+Every case draws seeded synthetic inputs (token_verification_gb300.synth),
+runs the CUDA kernels through the Python binding of libspecverify, and
+compares with the oracle on the same inputs: greedy and tree verification
+bit-exactly, rejection sampling token-exactly outside the oracle-flagged
+boundary draws (tests/parity.py).  The five standard workloads run at full
+size in the launch configuration the benchmark times."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import parity
+from token_verification_gb300 import api, synth
+
+pytestmark = pytest.mark.gpu
+THREADS = 16
+
+
+def run_sample(wl, T=None, **kw):
+    d = parity.to_device(wl)
+    T = wl.T if T is None else T
+    out = api.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], T,
+                                 draft_lens=d["draft_lens"], **kw)
+    torch.cuda.synchronize()
+    return out
+
+
+def check_sample(wl, T=None, flag_rate=None):
+    out = run_sample(wl, T)
+    ref = parity.oracle_sample(wl, threads=THREADS, temperature=T)
+    rep = parity.compare_sample(ref, out, wl.K, wl.V, greedy=(T == 0))
+    parity.assert_report(rep, flag_rate)
+    parity.compare_compaction(out, wl.K)
+    return out, ref, rep
+
+
+# ---------------------------------------------------------------------------
+# the standard workloads at full size
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("index", [0, 1, 2, 3])
+def test_standard_workload_sampling(index):
+    wl = synth.make_workload(index)
+    out, ref, rep = check_sample(wl)
+    L = out.accept_len.cpu().numpy()
+    assert ((L >= 1) & (L <= wl.K + 1)).all()
+
+
+def test_standard_workload_3_greedy():
+    wl = synth.make_workload(3)
+    d = parity.to_device(wl)
+    out = api.spec_verify_greedy(d["target"], d["draft_tokens"])
+    ref = oracle.greedy(wl.target, wl.draft_tokens, threads=THREADS)
+    assert (out.tokens.cpu().numpy() == ref["tokens"]).all()
+    assert (out.accept_len.cpu().numpy() == ref["accept_len"]).all()
+    parity.compare_compaction(out, wl.K)
+    # temperature 0 through the sampling entry is the same rule
+    out2 = run_sample(wl, T=0.0)
+    assert (out2.tokens.cpu().numpy() == ref["tokens"]).all()
+    prob = out2.accept_prob.cpu().numpy()
+    assert set(np.unique(prob)).issubset({-1.0, 0.0, 1.0})
+
+
+def test_standard_workload_4_tree():
+    wl = synth.make_workload(4)
+    d = parity.to_device(wl)
+    out = api.spec_verify_tree(d["target"], wl.parent, d["node_tokens"], wl.max_depth)
+    ref = oracle.tree(wl.target, wl.parent, wl.node_tokens, wl.max_depth, threads=THREADS)
+    for k in ("tokens", "accept_len", "path", "status"):
+        assert (getattr(out, k).cpu().numpy() == ref[k]).all(), k
+    assert (ref["accept_len"] >= 2).mean() > 0.5  # the workload exercises deep paths
+
+
+# ---------------------------------------------------------------------------
+# edge grid: vocabulary sizes around the chunk and vector widths, K, T, dtype
+# ---------------------------------------------------------------------------
+
+GRID = [
+    # V, K, T, dtype, drafts
+    (1, 2, 1.0, "bf16", "onehot"), (7, 3, 0.8, "f32", "dense"), (8, 1, 1.0, "bf16", "dense"),
+    (1000, 5, 2.0, "bf16", "onehot"), (1024, 3, 0.05, "f32", "onehot"),
+    (1025, 2, 1.0, "bf16", "dense"), (4104, 4, 0.8, "bf16", "onehot"),
+    (32000, 5, 1.0, "bf16", "dense"), (32001, 1, 1.3, "f32", "onehot"),
+    (9000, 0, 1.0, "bf16", "onehot"), (5000, 31, 0.9, "bf16", "onehot"),
+    (65536, 2, 0.7, "f32", "dense"),
+]
+
+
+@pytest.mark.parametrize("V,K,T,dtype,drafts", GRID)
+def test_sampling_grid(V, K, T, dtype, drafts):
+    B = 24
+    wl = synth.make_sample_case(B, K, V, dtype=dtype, T=T, drafts=drafts, sigma=0.6, seed=V + K)
+    check_sample(wl)
+
+
+@pytest.mark.parametrize("V,K,dtype", [(1, 1, "bf16"), (7, 3, "f32"), (1000, 5, "bf16"),
+                                       (1025, 2, "f32"), (32000, 4, "bf16"), (0 + 129280, 1, "bf16")])
+def test_greedy_grid_with_ties(V, K, dtype):
+    wl = synth.make_sample_case(16, K, V, dtype=dtype, drafts="onehot", p_argmax=0.8, seed=V,
+                                quantize=1.0)  # integer logits: many exact ties
+    d = parity.to_device(wl)
+    out = api.spec_verify_greedy(d["target"], d["draft_tokens"])
+    ref = oracle.greedy(wl.target, wl.draft_tokens)
+    assert (out.tokens.cpu().numpy() == ref["tokens"]).all()
+    assert (out.accept_len.cpu().numpy() == ref["accept_len"]).all()
+
+
+def test_ragged_draft_lens():
+    B, K, V = 40, 5, 6000
+    lens = np.random.default_rng(5).integers(0, K + 1, size=B).astype(np.int32)
+    for drafts in ("dense", "onehot"):
+        wl = synth.make_sample_case(B, K, V, drafts=drafts, seed=9, draft_lens=lens)
+        check_sample(wl)
+    wl = synth.make_sample_case(B, K, V, drafts="onehot", p_argmax=0.9, seed=10, draft_lens=lens)
+    d = parity.to_device(wl)
+    out = api.spec_verify_greedy(d["target"], d["draft_tokens"], draft_lens=d["draft_lens"])
+    ref = oracle.greedy(wl.target, wl.draft_tokens, draft_lens=lens)
+    assert (out.tokens.cpu().numpy() == ref["tokens"]).all()
+
+
+def test_masked_logits():
+    for drafts in ("dense", "onehot"):
+        wl = synth.make_sample_case(32, 3, 20000, drafts=drafts, seed=12, mask_frac=0.5)
+        check_sample(wl)
+
+
+def test_flag_rate_many_positions():
+    """Sampling parity over ~1.2e5 positions; flagged positions < 1e-4."""
+    total = parity.SampleReport()
+    for seed in range(10):
+        wl = synth.make_sample_case(2048, 5, 4096, drafts="onehot", seed=100 + seed)
+        out = run_sample(wl)
+        rep = parity.compare_sample(parity.oracle_sample(wl, threads=THREADS), out, 5, 4096)
+        total.merge(rep)
+    parity.assert_report(total, max_flag_rate=1e-4)
+
+
+def test_data_errors_match_oracle():
+    B, K, V = 8, 3, 3000
+    wl = synth.make_sample_case(B, K, V, drafts="onehot", seed=21)
+    tgt = synth.bf16_bits_to_float(wl.target).copy()
+    wl.draft_tokens[1, 0] = V          # token out of range
+    wl.draft_tokens[2, 2] = -5
+    tgt[3, 0, 17] = np.nan             # NaN in a needed row
+    tgt[4, 0, :] = -np.inf             # no finite logit
+    tgt[5, 0, 3] = np.inf
+    wl.uniforms[6, 0] = 0.999999       # reject at 0 ...
+    tgt[6, 2, 5] = np.nan              # ... so the NaN in row 2 is never needed
+    wl.target = synth.round_to_bf16_bits(tgt)
+    for T in (1.0, 0.0):
+        out = run_sample(wl, T=T)
+        ref = parity.oracle_sample(wl, temperature=T)
+        assert (out.status.cpu().numpy() == ref["status"]).all(), (out.status, ref["status"])
+        parity.assert_report(parity.compare_sample(ref, out, K, V, greedy=(T == 0)))
+    lens = np.full(B, K, np.int32)
+    lens[7] = K + 1
+    wl.draft_lens = lens
+    out = run_sample(wl)
+    assert out.status.cpu().numpy()[7] == api.REQ_BAD_DRAFT_LEN
+    assert out.accept_len.cpu().numpy()[7] == 0
+
+
+def test_tree_random_shapes_and_ties():
+    rng = np.random.default_rng(31)
+    for trial in range(6):
+        N = int(rng.integers(1, 80))
+        parent = [int(rng.integers(0, n)) for n in range(1, N + 1)]
+        V = int(rng.choice([7, 1000, 1024, 32000, 50001]))
+        dtype = "f32" if trial % 3 == 0 else "bf16"
+        wl = synth.make_tree_case(12, V, parent, dtype=dtype, seed=trial,
+                                  quantize=1.0 if trial % 2 else None)
+        d = parity.to_device(wl)
+        out = api.spec_verify_tree(d["target"], wl.parent, d["node_tokens"], wl.max_depth)
+        ref = oracle.tree(wl.target, wl.parent, wl.node_tokens, wl.max_depth)
+        for k in ("tokens", "accept_len", "path", "status"):
+            assert (getattr(out, k).cpu().numpy() == ref[k]).all(), (trial, k)
+
+
+def test_tree_errors():
+    wl = synth.make_tree_case(4, 5000, synth.medusa60_parent(), seed=3)
+    wl.node_tokens[1, 7] = 5000
+    tgt = synth.bf16_bits_to_float(wl.target).copy()
+    tgt[2, 0, 9] = np.nan
+    wl.target = synth.round_to_bf16_bits(tgt)
+    d = parity.to_device(wl)
+    out = api.spec_verify_tree(d["target"], wl.parent, d["node_tokens"], wl.max_depth)
+    ref = oracle.tree(wl.target, wl.parent, wl.node_tokens, wl.max_depth)
+    assert (out.status.cpu().numpy() == ref["status"]).all()
+    assert (out.tokens.cpu().numpy() == ref["tokens"]).all()
+    with pytest.raises(api.VerifyError):
+        api.spec_verify_tree(d["target"], wl.parent, d["node_tokens"], wl.max_depth - 1)
+
+
+def test_repeatable_and_workspace_reuse():
+    """Bit-identical repeat runs (no races), and a workspace shared by calls
+    of different shapes stays consistent (every call returns it to zero)."""
+    wl_a = synth.make_sample_case(64, 5, 40000, drafts="onehot", seed=41)
+    wl_b = synth.make_sample_case(16, 2, 70000, drafts="dense", seed=42)
+    outs = []
+    for wl in (wl_a, wl_b, wl_a, wl_b, wl_a):
+        o = run_sample(wl)
+        outs.append((o.tokens.cpu().numpy().copy(), o.accept_prob.cpu().numpy().copy()))
+    for i, j in ((0, 2), (2, 4), (1, 3)):
+        assert (outs[i][0] == outs[j][0]).all() and (outs[i][1] == outs[j][1]).all()
+    parity.assert_report(parity.compare_sample(parity.oracle_sample(wl_a), run_sample(wl_a), 5, 40000))
+
+
+def test_empty_batch():
+    t = torch.empty((0, 3, 100), dtype=torch.bfloat16, device="cuda")
+    dt = torch.empty((0, 2), dtype=torch.int32, device="cuda")
+    u = torch.empty((0, 3), dtype=torch.float32, device="cuda")
+    out = api.spec_verify_sample(t, None, dt, u, 1.0)
+    torch.cuda.synchronize()
+    assert out.cu_accept.cpu().tolist() == [0]

@@ -1,0 +1,52 @@
+"""ctypes declarations of libspecverify.so (include/spec_verify.h).
+
+There is no fallback: if the library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libspecverify.so")
+
+SYMBOLS = (
+    "spec_verify_workspace_size", "spec_verify_workspace_init", "spec_verify_sample",
+    "spec_verify_greedy", "spec_verify_tree", "spec_verify_status_string",
+    "spec_verify_version",
+)
+
+_lock = threading.Lock()
+_lib = None
+
+
+def lib():
+    global _lib
+    if _lib is not None:
+        return _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                "libspecverify.so is not built (expected at %s); build it with "
+                "token_verification_gb300.build.build()" % LIB_PATH)
+        l = ctypes.CDLL(LIB_PATH)
+        P, I, F, Z = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        l.spec_verify_workspace_size.argtypes = [I, I, I]
+        l.spec_verify_workspace_size.restype = Z
+        l.spec_verify_workspace_init.argtypes = [P, Z, P]
+        l.spec_verify_workspace_init.restype = I
+        l.spec_verify_sample.argtypes = [P, P, P, P, F, P, P, I, I, I, I, P, P, P, P, P, P, P, Z, P]
+        l.spec_verify_sample.restype = I
+        l.spec_verify_greedy.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
+        l.spec_verify_greedy.restype = I
+        l.spec_verify_tree.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P]
+        l.spec_verify_tree.restype = I
+        l.spec_verify_status_string.argtypes = [I]
+        l.spec_verify_status_string.restype = ctypes.c_char_p
+        l.spec_verify_version.argtypes = []
+        l.spec_verify_version.restype = I
+        _lib = l
+        return l

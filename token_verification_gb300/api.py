@@ -1,0 +1,211 @@
+"""Python binding of the C ABI: argument marshalling only.
+
+Every step of the verification runs in the CUDA kernels of libspecverify;
+PyTorch provides device memory and the current stream.  Function names and
+argument order follow include/spec_verify.h.
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional
+
+import numpy as np
+import torch
+
+from . import _native
+
+SV_F32 = 0
+SV_BF16 = 1
+REQ_BAD_TOKEN = 1
+REQ_BAD_LOGITS = 2
+REQ_BAD_DRAFT_LEN = 4
+MAX_K = 31
+
+
+class VerifyError(RuntimeError):
+    def __init__(self, code):
+        msg = _native.lib().spec_verify_status_string(int(code)).decode()
+        super().__init__("spec_verify failed (%d): %s" % (code, msg))
+        self.code = int(code)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SV_BF16
+    if t.dtype == torch.float32:
+        return SV_F32
+    raise TypeError("logits must be torch.bfloat16 or torch.float32, got %s" % t.dtype)
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(device: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _check(t: torch.Tensor, name, device, dtype=None, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError("%s must be a torch.Tensor" % name)
+    if t.device != device:
+        raise ValueError("%s must be on %s (got %s)" % (name, device, t.device))
+    if not t.is_contiguous():
+        raise ValueError("%s must be contiguous" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError("%s must be %s (got %s)" % (name, dtype, t.dtype))
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError("%s must have shape %s (got %s)" % (name, tuple(shape), tuple(t.shape)))
+
+
+# ---------------------------------------------------------------------------
+# workspaces: one per (device, stream), grown on demand, zero-filled once
+# ---------------------------------------------------------------------------
+
+_workspaces = {}
+
+
+def workspace(B: int, K: int, V: int, device: torch.device):
+    lib = _native.lib()
+    need = int(lib.spec_verify_workspace_size(B, K, V))
+    if need == 0 and B > 0:
+        raise ValueError("unsupported shape B=%d K=%d V=%d" % (B, K, V))
+    stream = torch.cuda.current_stream(device)
+    key = (device.index, stream.cuda_stream)
+    ws = _workspaces.get(key)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 256), dtype=torch.uint8, device=device)
+        rc = lib.spec_verify_workspace_init(_p(ws), ws.numel(), _stream(device))
+        if rc:
+            raise VerifyError(rc)
+        _workspaces[key] = ws
+    return ws
+
+
+@dataclass
+class VerifyOutputs:
+    tokens: torch.Tensor           # [B, K+1] int32
+    accept_len: torch.Tensor       # [B] int32
+    cu_accept: Optional[torch.Tensor] = None   # [B+1]
+    packed: Optional[torch.Tensor] = None      # [B*(K+1)]
+    batch_id: Optional[torch.Tensor] = None    # [B*(K+1)]
+    accept_prob: Optional[torch.Tensor] = None  # [B, K] fp32
+    status: Optional[torch.Tensor] = None      # [B]
+
+
+def alloc_outputs(B, K, device, *, packed=True, accept_prob=True, status=True):
+    i32 = dict(dtype=torch.int32, device=device)
+    return VerifyOutputs(
+        tokens=torch.empty((B, K + 1), **i32), accept_len=torch.empty((B,), **i32),
+        cu_accept=torch.empty((B + 1,), **i32) if packed else None,
+        packed=torch.empty((B * (K + 1),), **i32) if packed else None,
+        batch_id=torch.empty((B * (K + 1),), **i32) if packed else None,
+        accept_prob=torch.empty((B, K), dtype=torch.float32, device=device) if accept_prob else None,
+        status=torch.empty((B,), **i32) if status else None)
+
+
+def _validate_batch(target_logits, draft_tokens, draft_lens):
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    device = target_logits.device
+    if device.type != "cuda":
+        raise ValueError("target_logits must be a CUDA tensor")
+    _check(target_logits, "target_logits", device)
+    if K > 0 or draft_tokens is not None:
+        _check(draft_tokens, "draft_tokens", device, torch.int32, (B, K))
+    if draft_lens is not None:
+        _check(draft_lens, "draft_lens", device, torch.int32, (B,))
+    return B, K, V, device
+
+
+def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature,
+                       out: Optional[VerifyOutputs] = None, *, draft_lens=None,
+                       packed=True, accept_prob=True, status=True) -> VerifyOutputs:
+    """Rejection-sampling verification of one batch (see spec_verify.h).
+
+    target_logits [B, K+1, V] bf16/fp32 CUDA; draft_logits [B, K, V] same
+    dtype or None (one-hot drafts); draft_tokens [B, K] int32; uniforms
+    [B, K+1] fp32; temperature >= 0 (0 = greedy rule)."""
+    B, K, V, device = _validate_batch(target_logits, draft_tokens, draft_lens)
+    if draft_logits is not None:
+        _check(draft_logits, "draft_logits", device, target_logits.dtype, (B, K, V))
+    _check(uniforms, "uniforms", device, torch.float32, (B, K + 1))
+    if out is None:
+        out = alloc_outputs(B, K, device, packed=packed, accept_prob=accept_prob, status=status)
+    ws = workspace(B, K, V, device)
+    rc = _native.lib().spec_verify_sample(
+        _p(target_logits), _p(draft_logits), _p(draft_tokens), _p(uniforms),
+        ctypes.c_float(float(temperature)), _p(out.tokens), _p(out.accept_len),
+        _dtype_code(target_logits), B, K, V, _p(draft_lens), _p(out.cu_accept), _p(out.packed),
+        _p(out.batch_id), _p(out.accept_prob), _p(out.status), _p(ws), ws.numel(),
+        _stream(device))
+    if rc:
+        raise VerifyError(rc)
+    return out
+
+
+def spec_verify_greedy(target_logits, draft_tokens, out: Optional[VerifyOutputs] = None, *,
+                       draft_lens=None, packed=True, status=True) -> VerifyOutputs:
+    """Greedy verification: accept while the draft equals the target argmax."""
+    B, K, V, device = _validate_batch(target_logits, draft_tokens, draft_lens)
+    if out is None:
+        out = alloc_outputs(B, K, device, packed=packed, accept_prob=False, status=status)
+    ws = workspace(B, K, V, device)
+    rc = _native.lib().spec_verify_greedy(
+        _p(target_logits), _p(draft_tokens), _p(out.tokens), _p(out.accept_len),
+        _dtype_code(target_logits), B, K, V, _p(draft_lens), _p(out.cu_accept), _p(out.packed),
+        _p(out.batch_id), _p(out.status), _p(ws), ws.numel(), _stream(device))
+    if rc:
+        raise VerifyError(rc)
+    return out
+
+
+@dataclass
+class TreeOutputs:
+    tokens: torch.Tensor      # [B, max_depth+1]
+    accept_len: torch.Tensor  # [B]
+    path: Optional[torch.Tensor] = None
+    status: Optional[torch.Tensor] = None
+
+
+def tree_depth(parent) -> int:
+    d = [0]
+    for n, p in enumerate(np.asarray(parent, dtype=np.int64).reshape(-1), start=1):
+        if p < 0 or p >= n:
+            raise ValueError("parent of node %d must be an earlier node (got %d)" % (n, p))
+        d.append(d[p] + 1)
+    return max(d)
+
+
+def spec_verify_tree(target_logits, tree_parent, tree_tokens, max_depth=None,
+                     out: Optional[TreeOutputs] = None, *, path=True, status=True) -> TreeOutputs:
+    """Greedy tree verification.  tree_parent: host sequence [N] (parent of
+    node n at index n-1); tree_tokens [B, N] int32 CUDA."""
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N+1, V]")
+    B, N1, V = target_logits.shape
+    N = N1 - 1
+    device = target_logits.device
+    _check(target_logits, "target_logits", device)
+    parent = np.ascontiguousarray(np.asarray(tree_parent, dtype=np.int32).reshape(-1))
+    if parent.size != N:
+        raise ValueError("tree_parent must have N = %d entries" % N)
+    _check(tree_tokens, "tree_tokens", device, torch.int32, (B, N))
+    if max_depth is None:
+        max_depth = tree_depth(parent)
+    D1 = int(max_depth) + 1
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=device)
+        out = TreeOutputs(tokens=torch.empty((B, D1), **i32), accept_len=torch.empty((B,), **i32),
+                          path=torch.empty((B, D1), **i32) if path else None,
+                          status=torch.empty((B,), **i32) if status else None)
+    rc = _native.lib().spec_verify_tree(
+        _p(target_logits), parent.ctypes.data_as(ctypes.c_void_p), _p(tree_tokens),
+        _p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, N, V, int(max_depth),
+        _p(out.path), _p(out.status), _stream(device))
+    if rc:
+        raise VerifyError(rc)
+    return out

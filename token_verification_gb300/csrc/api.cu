@@ -1,0 +1,256 @@
+// api.cu - the extern "C" entry points declared in include/spec_verify.h:
+// argument validation on the host, workspace carving, and dispatch to the
+// kernels of sv_verify.cu / sv_tree.cu.  Nothing here allocates memory or
+// synchronises the stream.
+#include <math.h>
+#include <string.h>
+
+#include <mutex>
+#include <unordered_map>
+
+#include "../../include/spec_verify.h"
+#include "sv_common.cuh"
+#include "sv_launch.h"
+
+namespace sv {
+
+static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// The regions that must hold zeros when a call starts (counters and the
+// pending flags) come first; every call leaves them zero again.
+static WorkspaceLayout layout_for(int B, int R, int V) {
+  const size_t NC = ((size_t)V + kChunk - 1) / kChunk;
+  WorkspaceLayout l;
+  size_t o = 0;
+  l.row_ticket = o; o = align256(o + sizeof(int) * (size_t)B * R);
+  l.req_ticket = o; o = align256(o + sizeof(int) * (size_t)B);
+  l.res_ticket = o; o = align256(o + sizeof(int) * (size_t)B);
+  l.state = o;      o = align256(o + sizeof(ReqState) * (size_t)B);
+  l.zero_bytes = o;
+  l.row_sum = o;    o = align256(o + sizeof(RowSum) * (size_t)B * R);
+  l.rec = o;        o = align256(o + sizeof(float2) * (size_t)B * R * NC);
+  l.res_rec = o;    o = align256(o + sizeof(float) * (size_t)B * NC);
+  l.total = o;
+  return l;
+}
+
+WorkspaceLayout workspace_layout(int B, int K, int V) { return layout_for(B, 2 * K + 1, V); }
+
+cudaError_t device_info(DeviceInfo* out) {
+  static int sms[64] = {0};
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!sms[dev]) {
+    int n = 0;
+    err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (err != cudaSuccess) return err;
+    sms[dev] = n;
+  }
+  out->sms = sms[dev];
+  return cudaSuccess;
+}
+
+// Which zero-region layout each workspace was last used with.  A call whose
+// layout differs (or a workspace not seen before) first zero-fills the
+// region on its stream, so calls of different shapes may share a workspace.
+namespace {
+struct WsKey {
+  int B, R;
+  bool operator==(const WsKey& o) const { return B == o.B && R == o.R; }
+};
+std::mutex g_ws_mu;
+std::unordered_map<const void*, WsKey> g_ws_keys;
+}  // namespace
+
+static cudaError_t prepare_workspace(void* ws, const WorkspaceLayout& l, int B, int R,
+                                     cudaStream_t stream) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  const WsKey key{B, R};
+  auto it = g_ws_keys.find(ws);
+  if (it != g_ws_keys.end() && it->second == key) return cudaSuccess;
+  const cudaError_t err = cudaMemsetAsync(ws, 0, l.zero_bytes, stream);
+  if (err == cudaSuccess) g_ws_keys[ws] = key;
+  return err;
+}
+
+static void forget_workspace(const void* ws) {
+  std::lock_guard<std::mutex> lock(g_ws_mu);
+  g_ws_keys.erase(ws);
+}
+
+static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+static int chunks_per_task(int dtype, bool vec) {
+  if (!vec) return Lane<float, 1>::G;
+  return dtype == kBF16 ? Lane<uint16_t, 8>::G : Lane<float, 4>::G;
+}
+
+static sv_status verify_common(int mode, const void* target, const void* draft,
+                               const int32_t* draft_tokens, const float* uniforms, float T,
+                               int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
+                               int K, int V, const int32_t* draft_lens, int32_t* out_cu,
+                               int32_t* out_packed, int32_t* out_batch_id, float* out_accept_prob,
+                               int32_t* out_status, void* ws, size_t ws_bytes,
+                               cudaStream_t stream, int greedy_prob) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return SV_ERR_SHAPE;
+  if (B == 0) {
+    if (out_cu && cudaMemsetAsync(out_cu, 0, sizeof(int32_t), stream) != cudaSuccess)
+      return SV_ERR_CUDA;
+    return SV_OK;
+  }
+  if (!target || !out_tokens || !out_accept_len) return SV_ERR_NULL;
+  if (K > 0 && !draft_tokens) return SV_ERR_NULL;
+  if (mode != kGreedy && !uniforms) return SV_ERR_NULL;
+  const int R = (mode == kDense) ? 2 * K + 1 : K + 1;
+  const WorkspaceLayout l = layout_for(B, R, V);
+  if (!ws || ((uintptr_t)ws & 255u) || ws_bytes < l.total) return SV_ERR_WORKSPACE;
+
+  const int vec_elems = dtype == SV_BF16 ? 8 : 4;
+  const bool vec = (V % vec_elems == 0) && aligned16(target) && (!draft || aligned16(draft));
+  const int G = chunks_per_task(dtype, vec);
+  const int Gr = G > 1 ? G / 2 : 1;
+
+  VerifyParams p;
+  memset(&p, 0, sizeof p);
+  p.target = target;
+  p.draft = draft;
+  p.draft_tokens = draft_tokens;
+  p.draft_lens = draft_lens;
+  p.uniforms = uniforms;
+  p.out_tokens = out_tokens;
+  p.out_accept_len = out_accept_len;
+  p.out_accept_prob = out_accept_prob;
+  p.out_status = out_status;
+  p.out_cu = out_cu;
+  p.out_packed = out_packed;
+  p.out_batch_id = out_batch_id;
+  char* base = static_cast<char*>(ws);
+  p.row_ticket = reinterpret_cast<int*>(base + l.row_ticket);
+  p.req_ticket = reinterpret_cast<int*>(base + l.req_ticket);
+  p.res_ticket = reinterpret_cast<int*>(base + l.res_ticket);
+  p.row_sum = reinterpret_cast<RowSum*>(base + l.row_sum);
+  p.state = reinterpret_cast<ReqState*>(base + l.state);
+  p.rec = reinterpret_cast<float2*>(base + l.rec);
+  p.res_rec = reinterpret_cast<float*>(base + l.res_rec);
+  p.B = B;
+  p.K = K;
+  p.V = V;
+  p.NC = (V + kChunk - 1) / kChunk;
+  p.R = R;
+  p.TPR = (p.NC + G - 1) / G;
+  p.TPR_res = (p.NC + Gr - 1) / Gr;
+  p.total_tasks = (long long)B * R * p.TPR;
+  p.cc = mode == kGreedy ? 0.f : (float)(1.4426950408889634 / (double)T);
+  p.greedy_prob = greedy_prob;
+  const bool compact = out_cu || out_packed || out_batch_id;
+  if (prepare_workspace(ws, l, B, R, stream) != cudaSuccess) return SV_ERR_CUDA;
+  return launch_verify(mode, dtype, vec, p, compact, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace sv
+
+using namespace sv;
+
+extern "C" {
+
+size_t spec_verify_workspace_size(int B, int K, int V) {
+  if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return 0;
+  return workspace_layout(B, K, V).total;
+}
+
+sv_status spec_verify_workspace_init(void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (!workspace) return SV_ERR_NULL;
+  forget_workspace(workspace);
+  if (cudaMemsetAsync(workspace, 0, ws_bytes, (cudaStream_t)stream) != cudaSuccess) return SV_ERR_CUDA;
+  return SV_OK;
+}
+
+sv_status spec_verify_sample(const void* target_logits, const void* draft_logits,
+                             const int32_t* draft_tokens, const float* uniforms, float temperature,
+                             int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
+                             int K, int V, const int32_t* draft_lens, int32_t* out_cu_accept,
+                             int32_t* out_packed, int32_t* out_batch_id, float* out_accept_prob,
+                             int32_t* out_status, void* workspace, size_t ws_bytes,
+                             sv_stream_t stream) {
+  if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
+  const int mode = temperature == 0.f ? kGreedy : (draft_logits ? kDense : kOneHot);
+  return verify_common(mode, target_logits, mode == kDense ? draft_logits : nullptr, draft_tokens,
+                       uniforms, temperature, out_tokens, out_accept_len, dtype, B, K, V,
+                       draft_lens, out_cu_accept, out_packed, out_batch_id, out_accept_prob,
+                       out_status, workspace, ws_bytes, (cudaStream_t)stream, 1);
+}
+
+sv_status spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens,
+                             int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
+                             int K, int V, const int32_t* draft_lens, int32_t* out_cu_accept,
+                             int32_t* out_packed, int32_t* out_batch_id, int32_t* out_status,
+                             void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  return verify_common(kGreedy, target_logits, nullptr, draft_tokens, nullptr, 0.f, out_tokens,
+                       out_accept_len, dtype, B, K, V, draft_lens, out_cu_accept, out_packed,
+                       out_batch_id, nullptr, out_status, workspace, ws_bytes,
+                       (cudaStream_t)stream, 0);
+}
+
+sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent,
+                           const int32_t* tree_tokens, int32_t* out_tokens,
+                           int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
+                           int max_depth, int32_t* out_path, int32_t* out_status,
+                           sv_stream_t stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || B > SV_MAX_B || N < 0 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_V ||
+      max_depth < 0 || max_depth > SV_MAX_TREE_NODES)
+    return SV_ERR_SHAPE;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !out_tokens || !out_accept_len) return SV_ERR_NULL;
+  if (N > 0 && (!tree_parent || !tree_tokens)) return SV_ERR_NULL;
+  TreeParams p;
+  memset(&p, 0, sizeof p);
+  int depth[SV_MAX_TREE_NODES + 1];
+  depth[0] = 0;
+  int last_child[SV_MAX_TREE_NODES + 1];
+  for (int n = 0; n <= N; ++n) last_child[n] = 0;
+  for (int n = 1; n <= N; ++n) {
+    const int pa = tree_parent[n - 1];
+    if (pa < 0 || pa >= n) return SV_ERR_TREE;
+    depth[n] = depth[pa] + 1;
+    if (depth[n] > max_depth) return SV_ERR_TREE;
+    if (last_child[pa]) p.next_sibling[last_child[pa]] = (short)n;
+    else p.first_child[pa] = (short)n;
+    last_child[pa] = n;
+  }
+  p.target = target_logits;
+  p.tokens = tree_tokens;
+  p.out_tokens = out_tokens;
+  p.out_accept_len = out_accept_len;
+  p.out_path = out_path;
+  p.out_status = out_status;
+  p.B = B;
+  p.N = N;
+  p.V = V;
+  p.D1 = max_depth + 1;
+  p.NC = (V + kChunk - 1) / kChunk;
+  const int vec_elems = dtype == SV_BF16 ? 8 : 4;
+  const bool vec = (V % vec_elems == 0) && aligned16(target_logits);
+  return launch_tree(dtype, vec, p, (cudaStream_t)stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+const char* spec_verify_status_string(sv_status s) {
+  switch (s) {
+    case SV_OK: return "ok";
+    case SV_ERR_NULL: return "a required pointer is NULL";
+    case SV_ERR_SHAPE: return "shape outside the supported range";
+    case SV_ERR_DTYPE: return "unknown dtype";
+    case SV_ERR_TEMPERATURE: return "temperature negative, NaN or infinite";
+    case SV_ERR_TREE: return "parent array is not a tree of depth <= max_depth";
+    case SV_ERR_WORKSPACE: return "workspace NULL, misaligned or too small";
+    case SV_ERR_CUDA: return "CUDA launch failed";
+  }
+  return "unknown status";
+}
+
+int spec_verify_version(void) { return 100; }
+
+}  // extern "C"
