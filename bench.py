@@ -257,6 +257,12 @@ def run_ours(args):
 
     wl = synth.make_workload(args.workload, seed=shard_seed(0, rank))
     assert wl.draft is None, "the benchmarked workload has one-hot drafts"
+    if args.batch:  # a smaller batch of the same workload (profiling captures)
+        wl.B = args.batch
+        wl.target, wl.draft_tokens, wl.uniforms = (wl.target[:args.batch],
+                                                   wl.draft_tokens[:args.batch],
+                                                   wl.uniforms[:args.batch])
+        wl.meta["workload"] += "-first%d" % args.batch
     B, K, V = wl.B, wl.K, wl.V
     tgt_host = torch.from_numpy(wl.target.view(np.int16)).view(torch.bfloat16)
     sets = []
@@ -318,7 +324,7 @@ def run_ours(args):
     # end to end through the C ABI with host buffers (pinned): H2D of the
     # step's inputs, the call, D2H of its results, every step
     e2e = None
-    if rank == 0:
+    if rank == 0 and not args.no_e2e:
         pin = dict(target=tgt_host.pin_memory(),
                    tokens=torch.from_numpy(wl.draft_tokens).pin_memory(),
                    uniforms=torch.from_numpy(wl.uniforms).pin_memory())
@@ -391,6 +397,9 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=200)
     ap.add_argument("--ref-requests", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="use only the first BATCH requests (small profiling cases)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
