@@ -72,7 +72,7 @@ def configure(lib):
     lib.sv_oracle_inverse_cdf.restype = I
     lib.sv_oracle_greedy.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P]
     lib.sv_oracle_greedy.restype = I
-    lib.sv_oracle_sample.argtypes = [P, P, I, P, P, P, D, I, I, I, I, I, P, P, P, P, P, P]
+    lib.sv_oracle_sample.argtypes = [P, P, I, P, P, P, D, I, I, I, I, I, P, P, P, P, P, P, P, P]
     lib.sv_oracle_sample.restype = I
     lib.sv_oracle_tree.argtypes = [P, I, P, P, I, I, I, I, I, I, P, P, P, P]
     lib.sv_oracle_tree.restype = I
@@ -142,14 +142,15 @@ def inverse_cdf(weights, u):
 # ---------------------------------------------------------------------------
 
 def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=None,
-           threads=1, b_range=None):
+           threads=1, b_range=None, probe_tokens=None):
     """Rejection-sampling verify (temperature 0 = greedy rule).
 
     target [B, K+1, V], draft [B, K, V] or None (one-hot drafts),
     draft_tokens [B, K] int32, uniforms [B, K+1] (float32 or float64),
     draft_lens [B] or None.  Requests outside ``b_range`` keep -1 / 0.
     Returns a dict of numpy arrays: tokens, accept_len, accept_prob, flags,
-    margins, status.
+    margins, status (and probe [B, 2] when probe_tokens [B] is given: the
+    normalised CDF step of that token in the request's final draw).
     """
     target, dt = _logits(target)
     B, K1, V = target.shape
@@ -164,6 +165,10 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
     out = dict(tokens=np.full((B, K + 1), -1, np.int32), accept_len=np.zeros(B, np.int32),
                accept_prob=np.full((B, K), -1.0), flags=np.zeros((B, K + 1), np.int32),
                margins=np.full((B, K + 1), np.inf), status=np.zeros(B, np.int32))
+    probes = None
+    if probe_tokens is not None:
+        probes = np.ascontiguousarray(probe_tokens, dtype=np.int32).reshape(B)
+        out["probe"] = np.full((B, 2), np.nan)
     lib = _load()
 
     def fn(lo, hi):
@@ -171,7 +176,7 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
             _ptr(target), _ptr(draft), dt, _ptr(toks), _ptr(lens), _ptr(u),
             float(temperature), B, K, V, lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
             _ptr(out["accept_prob"]), _ptr(out["flags"]), _ptr(out["margins"]),
-            _ptr(out["status"]))
+            _ptr(out["status"]), _ptr(probes), _ptr(out.get("probe")))
 
     _run(fn, B, threads, b_range)
     return out

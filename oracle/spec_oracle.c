@@ -236,7 +236,7 @@ static int sample_request(const void* target, const void* draft, int dtype,
                           const int32_t* draft_tokens, const double* uniforms, double T, int K,
                           int K_b, int V, size_t b, double* lrow, double* p, double* q,
                           double* w, int32_t* tokens, int32_t* accept_len, double* accept_prob,
-                          int32_t* flags, double* margins) {
+                          int32_t* flags, double* margins, int32_t probe, double* probe_out) {
   for (int i = 0; i < K_b; ++i) {
     int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
     if (x < 0 || x >= V) return OR_BAD_TOKEN;
@@ -281,6 +281,17 @@ static int sample_request(const void* target, const void* draft, int dtype,
     if (!(W > 0)) /* R3 */
       for (int j = 0; j < V; ++j) w[j] = p[j];
   }
+  if (probe_out) {
+    /* the normalised CDF step [C_{probe-1}, C_probe) / W of a given token */
+    double W = 0.0, below = 0.0;
+    for (int j = 0; j < V; ++j) {
+      if (j < probe) below += w[j];
+      W += w[j];
+    }
+    int ok = probe >= 0 && probe < V && W > 0;
+    probe_out[0] = ok ? below / W : NAN;
+    probe_out[1] = ok ? (below + w[probe]) / W : NAN;
+  }
   double margin = 0.0;
   int t = sv_oracle_inverse_cdf(w, V, u[K], &margin);
   if (margins) margins[K] = margin;
@@ -301,14 +312,20 @@ static int sample_request(const void* target, const void* draft, int dtype,
  *   temperature  0 selects greedy verification; otherwise > 0 and finite
  *   outputs: tokens [B, K+1] (-1 padded), accept_len [B] (R7: accepted
  *   drafts + 1), accept_prob [B, K] (min(1, p/q) at the tested positions,
- *   -1 elsewhere), flags [B, K+1], margins [B, K+1] or NULL, status [B].
+ *   -1 elsewhere), flags [B, K+1], margins [B, K+1] or NULL (relative
+ *   distances of u_i to theta_i at i < K, and of the draw to the nearer edge
+ *   of its CDF step at K), status [B].
+ *   probe_tokens [B] / probe_interval [B, 2] (both optional): for a request
+ *   whose draw happened, the normalised CDF step [C_{t-1}/W, C_t/W) that
+ *   token t = probe_tokens[b] occupies in that draw's distribution (NaN if
+ *   t is out of range).  Used to check a draw made elsewhere.
  * Returns 0, or a negative code for arguments outside the domain. */
 int sv_oracle_sample(const void* target, const void* draft, int dtype,
                      const int32_t* draft_tokens, const int32_t* draft_lens,
                      const double* uniforms, double temperature, int B, int K, int V,
                      int b_begin, int b_end, int32_t* out_tokens, int32_t* out_accept_len,
                      double* out_accept_prob, int32_t* out_flags, double* out_margins,
-                     int32_t* out_status) {
+                     int32_t* out_status, const int32_t* probe_tokens, double* probe_interval) {
   if (B < 0 || K < 0 || V < 1 || b_begin < 0 || b_end > B) return -1;
   if (!(temperature >= 0) || isinf(temperature)) return -3;
   double* buf = (double*)malloc(sizeof(double) * (size_t)V * 4);
@@ -334,7 +351,8 @@ int sv_oracle_sample(const void* target, const void* draft, int dtype,
     else
       st = sample_request(target, draft, dtype, draft_tokens, uniforms, temperature, K, K_b,
                           V, (size_t)b, lrow, p, q, w, tokens, &out_accept_len[b], aprob,
-                          flags, margins);
+                          flags, margins, probe_tokens ? probe_tokens[b] : -1,
+                          probe_interval ? probe_interval + 2 * (size_t)b : NULL);
     if (st) {
       clear_request(tokens, K + 1, &out_accept_len[b]);
       for (int i = 0; i < K; ++i) aprob[i] = -1.0;

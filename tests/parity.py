@@ -9,9 +9,12 @@ of a decision boundary):
   * the oracle flags an acceptance test at position i (u within 1e-5 * theta
     of theta): positions before i must match and the GPU must have reached
     position i; positions i.. are excluded;
-  * the oracle flags the final draw at position n (u*W within 1e-5 * W of a
-    CDF step edge): everything but token n must match; token n is excluded
-    (it must still be a valid id).
+  * the oracle flags the final draw at position n (u*W within 1e-5 * W of an
+    edge of the chosen token's CDF step - which always holds when the draw
+    lands on a token lighter than 1e-5 of the total): everything but token n
+    must match, and token n is still checked: it must equal the oracle's
+    token unless the oracle's margin is below STRICT_TOL, and in any case its
+    exact (fp64) CDF step must lie within 1e-5 * W of u*W (verify_draws).
 Greedy and tree verification are compared bit-exactly.
 """
 from __future__ import annotations
@@ -24,6 +27,8 @@ import torch
 import oracle
 
 PROB_ATOL = 1e-5
+FLAG_TOL = 1e-5     # the oracle's flag band
+STRICT_TOL = 1e-6   # flagged draws farther than this from an edge must still match
 
 
 def to_device(wl, device="cuda"):
@@ -52,16 +57,28 @@ def oracle_sample(wl, threads=8, temperature=None):
 class SampleReport:
     requests: int = 0
     positions: int = 0
-    flagged: int = 0
-    excluded: int = 0
+    acc_flagged: int = 0      # acceptance tests within 1e-5 of theta
+    excluded: int = 0         # positions not compared because of them
+    cdf_flagged: int = 0      # final draws within 1e-5 * W of a CDF edge
+    cdf_differ: int = 0       # ... whose GPU token differs from the oracle's
     errors: list = field(default_factory=list)
+    to_verify: list = field(default_factory=list)  # (b, n, gpu token)
+
+    @property
+    def flagged(self):
+        return self.acc_flagged + self.cdf_flagged
 
     def merge(self, o):
-        self.requests += o.requests
-        self.positions += o.positions
-        self.flagged += o.flagged
-        self.excluded += o.excluded
+        for k in ("requests", "positions", "acc_flagged", "excluded", "cdf_flagged",
+                  "cdf_differ"):
+            setattr(self, k, getattr(self, k) + getattr(o, k))
         self.errors += o.errors
+
+    def summary(self):
+        return ("%d requests, %d positions: %d acceptance-flagged (%d positions excluded), "
+                "%d draws CDF-flagged of which %d differ from the oracle (all verified)"
+                % (self.requests, self.positions, self.acc_flagged, self.excluded,
+                   self.cdf_flagged, self.cdf_differ))
 
 
 def compare_sample(ref, gpu, K, V, greedy=False) -> SampleReport:
@@ -89,7 +106,7 @@ def compare_sample(ref, gpu, K, V, greedy=False) -> SampleReport:
         rt = ref["tokens"][b]
         if acc_flag is not None:
             i = acc_flag
-            rep.flagged += 1
+            rep.acc_flagged += 1
             rep.excluded += K + 1 - i
             if not (g_tok[b, :i] == rt[:i]).all() or g_len[b] < i + 1:
                 rep.errors.append((b, "prefix before flagged test at %d differs" % i))
@@ -103,12 +120,17 @@ def compare_sample(ref, gpu, K, V, greedy=False) -> SampleReport:
             continue
         if cdf_flag is not None:
             n = cdf_flag
-            rep.flagged += 1
-            rep.excluded += 1
+            rep.cdf_flagged += 1
             same = np.ones(K + 1, bool)
             same[n] = False
             if not (g_tok[b][same] == rt[same]).all() or not (0 <= g_tok[b, n] < V):
                 rep.errors.append((b, "tokens differ outside the flagged draw"))
+            elif g_tok[b, n] != rt[n]:
+                rep.cdf_differ += 1
+                if ref["margins"][b, K] > STRICT_TOL:
+                    rep.errors.append((b, "draw differs at margin %.2e > %.0e"
+                                       % (ref["margins"][b, K], STRICT_TOL)))
+                rep.to_verify.append((b, n, int(g_tok[b, n])))
         elif not (g_tok[b] == rt).all():
             rep.errors.append((b, "tokens %s vs oracle %s" % (g_tok[b].tolist(), rt.tolist())))
         if g_prob is not None and not greedy:
@@ -116,6 +138,29 @@ def compare_sample(ref, gpu, K, V, greedy=False) -> SampleReport:
             if not (diff <= PROB_ATOL).all():
                 rep.errors.append((b, "accept_prob max diff %.3g" % diff.max()))
     return rep
+
+
+def verify_draws(wl, rep: SampleReport, temperature=None):
+    """Flagged draws where the GPU chose another token than the oracle: the
+    GPU token's exact CDF step must come within FLAG_TOL * W of u * W."""
+    if not rep.to_verify:
+        return
+    idx = np.array([b for b, _, _ in rep.to_verify])
+    toks = np.array([t for _, _, t in rep.to_verify], np.int32)
+
+    def sub(a):
+        return None if a is None else np.ascontiguousarray(a[idx])
+
+    T = wl.T if temperature is None else temperature
+    out = oracle.sample(sub(wl.target), sub(wl.draft), sub(wl.draft_tokens), sub(wl.uniforms),
+                        T, draft_lens=sub(wl.draft_lens), probe_tokens=toks)
+    u = wl.uniforms[idx, wl.K].astype(np.float64)
+    lo, hi = out["probe"][:, 0], out["probe"][:, 1]
+    ok = (hi > lo) & (lo <= u + FLAG_TOL) & (hi >= u - FLAG_TOL)
+    for j in np.nonzero(~ok)[0]:
+        rep.errors.append((int(idx[j]), "GPU draw %d outside the window: step [%.9f, %.9f) u %.9f"
+                           % (toks[j], lo[j], hi[j], u[j])))
+    rep.to_verify = []
 
 
 def compare_compaction(gpu, K):
@@ -128,7 +173,7 @@ def compare_compaction(gpu, K):
 
 
 def assert_report(rep: SampleReport, max_flag_rate=None):
+    assert not rep.to_verify, "verify_draws() was not run"
     assert not rep.errors, "%d mismatching requests, first: %s" % (len(rep.errors), rep.errors[:5])
     if max_flag_rate is not None:
-        assert rep.flagged <= max_flag_rate * rep.positions, (
-            "flagged %d of %d positions" % (rep.flagged, rep.positions))
+        assert rep.acc_flagged <= max_flag_rate * rep.positions, rep.summary()

@@ -31,6 +31,7 @@ def check_sample(wl, T=None, flag_rate=None):
     out = run_sample(wl, T)
     ref = parity.oracle_sample(wl, threads=THREADS, temperature=T)
     rep = parity.compare_sample(ref, out, wl.K, wl.V, greedy=(T == 0))
+    parity.verify_draws(wl, rep, T)
     parity.assert_report(rep, flag_rate)
     parity.compare_compaction(out, wl.K)
     return out, ref, rep
@@ -126,14 +127,20 @@ def test_masked_logits():
         check_sample(wl)
 
 
-def test_flag_rate_many_positions():
-    """Sampling parity over ~1.2e5 positions; flagged positions < 1e-4."""
+@pytest.mark.parametrize("drafts,V", [("onehot", 4096), ("dense", 4096), ("onehot", 152064)])
+def test_flag_rate_many_positions(drafts, V, capsys):
+    """Sampling parity over many positions: acceptance tests flagged on fewer
+    than 1e-4 of the positions; every flagged final draw is still verified."""
     total = parity.SampleReport()
-    for seed in range(10):
-        wl = synth.make_sample_case(2048, 5, 4096, drafts="onehot", seed=100 + seed)
+    B = 2048 if V < 10000 else 256
+    for seed in range(10 if V < 10000 else 8):
+        wl = synth.make_sample_case(B, 5, V, drafts=drafts, seed=100 + seed)
         out = run_sample(wl)
-        rep = parity.compare_sample(parity.oracle_sample(wl, threads=THREADS), out, 5, 4096)
+        rep = parity.compare_sample(parity.oracle_sample(wl, threads=THREADS), out, 5, V)
+        parity.verify_draws(wl, rep)
         total.merge(rep)
+    with capsys.disabled():
+        print("\n[flag rate %s V=%d] %s" % (drafts, V, total.summary()))
     parity.assert_report(total, max_flag_rate=1e-4)
 
 
@@ -153,7 +160,9 @@ def test_data_errors_match_oracle():
         out = run_sample(wl, T=T)
         ref = parity.oracle_sample(wl, temperature=T)
         assert (out.status.cpu().numpy() == ref["status"]).all(), (out.status, ref["status"])
-        parity.assert_report(parity.compare_sample(ref, out, K, V, greedy=(T == 0)))
+        rep = parity.compare_sample(ref, out, K, V, greedy=(T == 0))
+        parity.verify_draws(wl, rep, T)
+        parity.assert_report(rep)
     lens = np.full(B, K, np.int32)
     lens[7] = K + 1
     wl.draft_lens = lens
@@ -204,7 +213,9 @@ def test_repeatable_and_workspace_reuse():
         outs.append((o.tokens.cpu().numpy().copy(), o.accept_prob.cpu().numpy().copy()))
     for i, j in ((0, 2), (2, 4), (1, 3)):
         assert (outs[i][0] == outs[j][0]).all() and (outs[i][1] == outs[j][1]).all()
-    parity.assert_report(parity.compare_sample(parity.oracle_sample(wl_a), run_sample(wl_a), 5, 40000))
+    rep = parity.compare_sample(parity.oracle_sample(wl_a), run_sample(wl_a), 5, 40000)
+    parity.verify_draws(wl_a, rep)
+    parity.assert_report(rep)
 
 
 def test_empty_batch():
