@@ -73,6 +73,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_REQ_BAD_TOKEN 1     /* a draft / tree token outside [0, V) */
 #define SV_REQ_BAD_LOGITS 2    /* a needed row has NaN or +inf, or no finite logit */
 #define SV_REQ_BAD_DRAFT_LEN 4 /* draft_lens[b] outside [0, K] */
+#define SV_REQ_TIMEOUT 8       /* a bounded wait for staged logits gave up (device fault) */
 
 /* Limits. */
 #define SV_MAX_K 31             /* draft positions per request */

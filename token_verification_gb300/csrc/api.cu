@@ -25,6 +25,7 @@ static WorkspaceLayout layout_for(int B, int R, int V) {
   l.row_ticket = o; o = align256(o + sizeof(int) * (size_t)B * R);
   l.req_ticket = o; o = align256(o + sizeof(int) * (size_t)B);
   l.res_ticket = o; o = align256(o + sizeof(int) * (size_t)B);
+  l.counters = o;   o = align256(o + 2 * sizeof(int));
   l.state = o;      o = align256(o + sizeof(ReqState) * (size_t)B);
   l.zero_bytes = o;
   l.row_sum = o;    o = align256(o + sizeof(RowSum) * (size_t)B * R);
@@ -82,11 +83,6 @@ static void forget_workspace(const void* ws) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-static int chunks_per_task(int dtype, bool vec) {
-  if (!vec) return Lane<float, 1>::G;
-  return dtype == kBF16 ? Lane<uint16_t, 8>::G : Lane<float, 4>::G;
-}
-
 static sv_status verify_common(int mode, const void* target, const void* draft,
                                const int32_t* draft_tokens, const float* uniforms, float T,
                                int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
@@ -111,7 +107,7 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   const int vec_elems = dtype == SV_BF16 ? 8 : 4;
   const bool vec = (V % vec_elems == 0) && aligned16(target) && (!draft || aligned16(draft));
   const int G = chunks_per_task(dtype, vec);
-  const int Gr = G > 1 ? G / 2 : 1;
+  const int Gr = residual_chunks_per_task(dtype, vec);
 
   VerifyParams p;
   memset(&p, 0, sizeof p);
@@ -131,6 +127,8 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.row_ticket = reinterpret_cast<int*>(base + l.row_ticket);
   p.req_ticket = reinterpret_cast<int*>(base + l.req_ticket);
   p.res_ticket = reinterpret_cast<int*>(base + l.res_ticket);
+  p.err = reinterpret_cast<int*>(base + l.counters);
+  p.fin_ticket = p.err + 1;
   p.row_sum = reinterpret_cast<RowSum*>(base + l.row_sum);
   p.state = reinterpret_cast<ReqState*>(base + l.state);
   p.rec = reinterpret_cast<float2*>(base + l.rec);

@@ -31,6 +31,7 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr int kBadToken = 1;
 constexpr int kBadLogits = 2;
 constexpr int kBadDraftLen = 4;
+constexpr int kTimeout = 8;
 
 enum Mode : int { kOneHot = 0, kDense = 1, kGreedy = 2 };
 
@@ -99,6 +100,102 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 }
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
+// One add with release + acquire semantics at GPU scope: publishes this
+// thread's earlier writes (chunk records) and, for the last arriver, makes
+// the other arrivers' writes visible.  Replaces a fence + plain atomic.
+__device__ __forceinline__ int atomic_add_acq_rel(int* addr, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(addr), "r"(v)
+               : "memory");
+  return old;
+}
+
+// ---------------------------------------------------------------------------
+// packed arithmetic (two bf16 in a 32-bit word, two fp32 in a 64-bit pair)
+// ---------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+typedef unsigned long long f32x2;
+__device__ __forceinline__ f32x2 pack2(float lo, float hi) {
+  f32x2 r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void unpack2(f32x2 v, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+}
+__device__ __forceinline__ f32x2 fma2(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
+  f32x2 r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// shared-memory staging: bulk copies completed on an mbarrier
+// ---------------------------------------------------------------------------
+
+constexpr uint32_t kWaitHintNs = 1000000;  // max suspension per try_wait (1 ms)
+constexpr int kWaitTries = 2000;           // so no wait lasts longer than ~2 s
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
+}
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Copy `bytes` (a multiple of 16, both ends 16-byte aligned) from global
+// into shared memory; completion is signalled on mbarrier `bar`.
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(kWaitHintNs)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for phase `parity` of `bar`; false if it did not complete.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+  for (int i = 0; i < kWaitTries; ++i)
+    if (mbar_try_wait(bar, parity)) return true;
+  return false;
+}
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
+}
+
 // ---------------------------------------------------------------------------
 // per-lane tiles
 // ---------------------------------------------------------------------------
@@ -121,6 +218,16 @@ struct Lane<uint16_t, 8> {  // bf16, 8 per 128-bit load
     const uint32_t w = (e >> 1) == 0 ? r.x : (e >> 1) == 1 ? r.y : (e >> 1) == 2 ? r.z : r.w;
     return __uint_as_float((e & 1) ? (w & 0xffff0000u) : (w << 16));
   }
+  // overwrite element e with -inf
+  static __device__ __forceinline__ void kill(Raw& r, int e) {
+    const uint32_t keep = (e & 1) ? 0x0000ffffu : 0xffff0000u;
+    const uint32_t ninf = (e & 1) ? 0xff800000u : 0x0000ff80u;
+    const int q = e >> 1;
+    if (q == 0) r.x = (r.x & keep) | ninf;
+    if (q == 1) r.y = (r.y & keep) | ninf;
+    if (q == 2) r.z = (r.z & keep) | ninf;
+    if (q == 3) r.w = (r.w & keep) | ninf;
+  }
 };
 
 template <>
@@ -136,6 +243,12 @@ struct Lane<float, 4> {  // fp32, 4 per 128-bit load
   static __device__ __forceinline__ float get(const Raw& r, int e) {
     return __uint_as_float(e == 0 ? r.x : e == 1 ? r.y : e == 2 ? r.z : r.w);
   }
+  static __device__ __forceinline__ void kill(Raw& r, int e) {
+    if (e == 0) r.x = 0xff800000u;
+    if (e == 1) r.y = 0xff800000u;
+    if (e == 2) r.z = 0xff800000u;
+    if (e == 3) r.w = 0xff800000u;
+  }
 };
 
 template <>
@@ -149,6 +262,7 @@ struct Lane<uint16_t, 1> {  // bf16, scalar path
   static __device__ __forceinline__ float get(const Raw& r, int) {
     return __uint_as_float((uint32_t)r << 16);
   }
+  static __device__ __forceinline__ void kill(Raw& r, int) { r = pad(); }
 };
 
 template <>
@@ -158,6 +272,7 @@ struct Lane<float, 1> {  // fp32, scalar path
   static __device__ __forceinline__ Raw load(const float* p) { return __ldg(p); }
   static __device__ __forceinline__ Raw pad() { return -INFINITY; }
   static __device__ __forceinline__ float get(const Raw& r, int) { return r; }
+  static __device__ __forceinline__ void kill(Raw& r, int) { r = pad(); }
 };
 
 // one logit, widened to fp32
@@ -184,25 +299,95 @@ __device__ __forceinline__ void load_chunk(const T* row, int V, int c,
   }
 }
 
-// Softmax record of one chunk: {m_c, sum_j 2^(l_j*cc - m_c*cc)}, skipping the
-// element at chunk offset mask_local (>= 0) - the one-hot residual excludes
-// the draft token.  m_c = -inf for an all -inf chunk; NaN marks a chunk that
-// holds NaN or +inf.
+// The same tile from a chunk staged in shared memory at `stage` (vector
+// paths only); groups at or past V get the -inf pad.
 template <typename T, int VEC>
-__device__ __forceinline__ float2 chunk_softmax(const typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
-                                                float cc, int mask_local) {
+__device__ __forceinline__ void load_chunk_smem(uint32_t stage, int V, int c,
+                                                typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV]) {
+  using L = Lane<T, VEC>;
+  static_assert(VEC * sizeof(T) == 16, "shared-memory tiles are 128-bit groups");
+  const int lane = lane_id();
+#pragma unroll
+  for (int k = 0; k < L::NV; ++k) {
+    const int off = tile_offset<VEC>(k, 0, lane);
+    raw[k] = (c * kChunk + off < V) ? lds128(stage + off * (int)sizeof(T)) : L::pad();
+  }
+}
+
+// Overwrite the element at chunk offset mask_local (held by one lane) with -inf.
+template <typename T, int VEC>
+__device__ __forceinline__ void mask_element(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
+                                             int mask_local) {
   using L = Lane<T, VEC>;
   const int lane = lane_id();
+#pragma unroll
+  for (int k = 0; k < L::NV; ++k) {
+    const int base = tile_offset<VEC>(k, 0, lane);
+    if (mask_local >= base && mask_local < base + VEC) L::kill(raw[k], mask_local - base);
+  }
+}
+
+// bf16 vector tile (4 x 128-bit groups = 16 words = 32 logits per lane):
+// NaN-propagating max on packed bf16 pairs.
+__device__ __forceinline__ float lane_max_bf16(const uint4 (&raw)[4]) {
+  uint32_t m = bf16x2_max_nan(raw[0].x, raw[0].y);
+  m = bf16x2_max_nan(m, raw[0].z);
+  m = bf16x2_max_nan(m, raw[0].w);
+#pragma unroll
+  for (int k = 1; k < 4; ++k) {
+    m = bf16x2_max_nan(m, raw[k].x);
+    m = bf16x2_max_nan(m, raw[k].y);
+    m = bf16x2_max_nan(m, raw[k].z);
+    m = bf16x2_max_nan(m, raw[k].w);
+  }
+  return max_nan(bf16_lo(m), bf16_hi(m));
+}
+
+// Softmax record of one chunk: {m_c, sum_j 2^(l_j*cc - m_c*cc)}, leaving
+// out the element at chunk offset mask_local (>= 0) - the one-hot residual
+// excludes the draft token; the max still includes it.  m_c = -inf for an
+// all -inf chunk; NaN marks a chunk that holds NaN or +inf.  The bf16 vector
+// tile uses packed instructions (bf16x2 max, fma.rn.f32x2, add.rn.f32x2);
+// every weight is rounded exactly as the scalar fmaf + ex2 of the rescan.
+template <typename T, int VEC>
+__device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
+                                                float cc, int mask_local) {
+  using L = Lane<T, VEC>;
+  constexpr bool kPacked = sizeof(T) == 2 && VEC == 8;
   float lm = -INFINITY;
+  if constexpr (kPacked) {
+    lm = lane_max_bf16(raw);
+  } else {
 #pragma unroll
-  for (int k = 0; k < L::NV; ++k)
+    for (int k = 0; k < L::NV; ++k)
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) lm = max_nan(lm, L::get(raw[k], e));
+      for (int e = 0; e < VEC; ++e) lm = max_nan(lm, L::get(raw[k], e));
+  }
   const float cm = warp_max_nan(lm);
   if (!is_finite(cm)) return make_float2(cm == -INFINITY ? -INFINITY : qnan(), 0.f);
+  if (mask_local >= 0) mask_element<T, VEC>(raw, mask_local);
   const float nb = -cm * cc;
-  float s0 = 0.f, s1 = 0.f;
-  if (mask_local < 0) {
+  float s;
+  if constexpr (kPacked) {
+    const f32x2 c2 = pack2(cc, cc), nb2 = pack2(nb, nb);
+    f32x2 acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        float a0, a1;
+        unpack2(fma2(pack2(bf16_lo(w[q]), bf16_hi(w[q])), c2, nb2), a0, a1);
+        const f32x2 e2 = pack2(ex2(a0), ex2(a1));
+        if (q & 1) acc1 = add2(acc1, e2); else acc0 = add2(acc0, e2);
+      }
+    }
+    float s0, s1, s2, s3;
+    unpack2(acc0, s0, s1);
+    unpack2(acc1, s2, s3);
+    s = (s0 + s1) + (s2 + s3);
+  } else {
+    float s0 = 0.f, s1 = 0.f;
 #pragma unroll
     for (int k = 0; k < L::NV; ++k)
 #pragma unroll
@@ -210,17 +395,9 @@ __device__ __forceinline__ float2 chunk_softmax(const typename Lane<T, VEC>::Raw
         const float w = ex2(fmaf(L::get(raw[k], e), cc, nb));
         if ((k * VEC + e) & 1) s1 += w; else s0 += w;
       }
-  } else {
-#pragma unroll
-    for (int k = 0; k < L::NV; ++k)
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        float w = ex2(fmaf(L::get(raw[k], e), cc, nb));
-        if (tile_offset<VEC>(k, e, lane) == mask_local) w = 0.f;
-        if ((k * VEC + e) & 1) s1 += w; else s0 += w;
-      }
+    s = s0 + s1;
   }
-  return make_float2(cm, warp_sum(s0 + s1));
+  return make_float2(cm, warp_sum(s));
 }
 
 // Argmax record of one chunk: {max, lowest global index attaining it} (index
@@ -231,10 +408,14 @@ __device__ __forceinline__ float2 chunk_argmax(const typename Lane<T, VEC>::Raw 
   using L = Lane<T, VEC>;
   const int lane = lane_id();
   float lm = -INFINITY;
+  if constexpr (sizeof(T) == 2 && VEC == 8) {
+    lm = lane_max_bf16(raw);
+  } else {
 #pragma unroll
-  for (int k = 0; k < L::NV; ++k)
+    for (int k = 0; k < L::NV; ++k)
 #pragma unroll
-    for (int e = 0; e < VEC; ++e) lm = max_nan(lm, L::get(raw[k], e));
+      for (int e = 0; e < VEC; ++e) lm = max_nan(lm, L::get(raw[k], e));
+  }
   const float cm = warp_max_nan(lm);
   unsigned idx = 0x7fffffffu;
   if (lm == cm) {  // this lane holds a maximum (rare branch)

@@ -44,6 +44,8 @@ struct VerifyParams {
   int* row_ticket;   // [B*R]
   int* req_ticket;   // [B]
   int* res_ticket;   // [B]
+  int* err;          // [1] set when a bounded wait gave up
+  int* fin_ticket;   // [1] requests finalised in this call
   RowSum* row_sum;   // [B*R]
   ReqState* state;   // [B]
   float2* rec;       // [B*R*NC]
@@ -76,7 +78,8 @@ enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Workspace layout for B requests, K positions, V vocabulary (dense case).
 struct WorkspaceLayout {
-  size_t row_ticket, req_ticket, res_ticket, state, zero_bytes, row_sum, rec, res_rec, total;
+  size_t row_ticket, req_ticket, res_ticket, counters, state, zero_bytes, row_sum, rec, res_rec,
+      total;
 };
 WorkspaceLayout workspace_layout(int B, int K, int V);
 
@@ -84,6 +87,10 @@ struct DeviceInfo {
   int sms;
 };
 cudaError_t device_info(DeviceInfo* out);
+
+// Chunks per row-statistics task and per residual task.
+int chunks_per_task(int dtype, bool vec);
+int residual_chunks_per_task(int dtype, bool vec);
 
 // mode: 0 one-hot sampling, 1 dense sampling, 2 greedy
 cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p, bool compact,

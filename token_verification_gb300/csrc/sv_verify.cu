@@ -218,10 +218,16 @@ template <int MODE, typename T, int VEC>
 __device__ __noinline__ void request_finalize(const VerifyParams& p, int b, int Kb) {
   const int lane = lane_id();
   const int K = p.K;
-  if (lane == 0) p.req_ticket[b] = 0;
+  // A bounded wait that gave up earlier in this call marks every request
+  // finalised after it (its chunks may be among the unread ones).
   int status = 0;
+  if (lane == 0) {
+    p.req_ticket[b] = 0;
+    if (__ldcg(p.err)) status = kTimeout;
+  }
+  status = __shfl_sync(0xffffffffu, status, 0);
   if (Kb < 0 || Kb > K) {
-    status = kBadDraftLen;
+    status |= kBadDraftLen;
     Kb = 0;
   }
   int x = -1;
@@ -294,6 +300,11 @@ __device__ __noinline__ void request_finalize(const VerifyParams& p, int b, int 
       }
     }
   }
+  // the last request finalised in this call clears the call's counters
+  if (lane == 0 && atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
+    *p.err = 0;
+    *p.fin_ticket = 0;
+  }
   if (p.out_accept_prob && lane < K && (MODE != kGreedy || p.greedy_prob))
     p.out_accept_prob[(long long)b * K + lane] =
         (!status && lane < Kb && lane <= n) ? theta : -1.f;
@@ -332,20 +343,72 @@ __device__ __noinline__ void row_finalize(const VerifyParams& p, int b, int r, l
   if (lane == 0) {
     store_rowsum(p.row_sum + rowid, rs);
     p.row_ticket[rowid] = 0;
-    __threadfence();
-    old = atomicAdd(p.req_ticket + b, 1);
+    old = atomic_add_acq_rel(p.req_ticket + b, 1);
   }
   old = __shfl_sync(0xffffffffu, old, 0);
-  if (old + 1 == p.R) {
-    __threadfence();
-    request_finalize<MODE, T, VEC>(p, b, Kb);
-  }
+  if (old + 1 == p.R) request_finalize<MODE, T, VEC>(p, b, Kb);
 }
 
 // ---------------------------------------------------------------------------
 // kernel A: row statistics + finalisation
 // ---------------------------------------------------------------------------
 
+// A task is up to G consecutive chunks of one row.  Tasks are numbered
+// request-major (request, row, chunk group), so requests complete one after
+// another while the grid streams.
+struct Task {
+  long long rowid;
+  int b, r, i, Kb, c0, nch;
+  bool is_draft, need;
+};
+
+template <int G>
+__device__ __forceinline__ Task decode_task(const VerifyParams& p, long long t) {
+  Task k;
+  k.rowid = t / p.TPR;
+  const int tc = (int)(t % p.TPR);
+  k.r = (int)(k.rowid % p.R);
+  k.b = (int)(k.rowid / p.R);
+  k.Kb = p.draft_lens ? __ldg(p.draft_lens + k.b) : p.K;
+  k.is_draft = k.r > p.K;
+  k.i = k.is_draft ? k.r - p.K - 1 : k.r;
+  k.need = k.Kb >= 0 && k.Kb <= p.K && (k.is_draft ? k.i < k.Kb : k.i <= k.Kb);
+  k.c0 = tc * G;
+  k.nch = min(G, p.NC - k.c0);
+  return k;
+}
+
+template <typename T>
+__device__ __forceinline__ const T* task_row(const VerifyParams& p, const Task& k) {
+  return k.is_draft ? row_ptr<T>(p.draft, (long long)k.b * p.K + k.i, p.V)
+                    : row_ptr<T>(p.target, (long long)k.b * (p.K + 1) + k.i, p.V);
+}
+
+// The one-hot draft token of this task's row (excluded from its sums), or -1.
+template <int MODE>
+__device__ __forceinline__ int task_mask(const VerifyParams& p, const Task& k) {
+  if (MODE != kOneHot || k.is_draft || k.i >= k.Kb) return -1;
+  return __ldg(p.draft_tokens + (long long)k.b * p.K + k.i);
+}
+
+template <int MODE, typename T, int VEC>
+__device__ __forceinline__ float2 chunk_record(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
+                                               int c, float cc, int mask_x) {
+  if (MODE == kGreedy) return chunk_argmax<T, VEC>(raw, c * kChunk);
+  const int ml = (mask_x >= c * kChunk && mask_x < (c + 1) * kChunk) ? mask_x - c * kChunk : -1;
+  return chunk_softmax<T, VEC>(raw, cc, ml);
+}
+
+// A task's arrival on its row's counter is issued at the end of the task and
+// its result read only at the end of the next one, so the atomic's round trip
+// overlaps work; the warp that completes the row finalises it.
+template <int MODE, typename T, int VEC>
+__device__ __forceinline__ void settle_task(const VerifyParams& p, const Task& k, int old_lane0) {
+  const int old = __shfl_sync(0xffffffffu, old_lane0, 0);
+  if (old + k.nch == p.NC) row_finalize<MODE, T, VEC>(p, k.b, k.r, k.rowid, k.need, k.Kb);
+}
+
+// Register-tile variant: the scalar path (any V, any alignment).
 template <int MODE, typename T, int VEC>
 __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyParams p) {
   using L = Lane<T, VEC>;
@@ -354,54 +417,150 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
   const int lane = lane_id();
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  bool have_prev = false;
+  Task prev{};
+  int prev_old = 0;
   for (long long t = gw; t < p.total_tasks; t += nw) {
-    const int tc = (int)(t % p.TPR);
-    const long long rowid = t / p.TPR;
-    const int r = (int)(rowid % p.R);
-    const int b = (int)(rowid / p.R);
-    const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : p.K;
-    const bool is_draft = r > p.K;
-    const int i = is_draft ? r - p.K - 1 : r;
-    const bool need = Kb >= 0 && Kb <= p.K && (is_draft ? i < Kb : i <= Kb);
-    const int c0 = tc * G;
-    const int nch = min(G, p.NC - c0);
-    if (need) {
-      const T* row = is_draft ? row_ptr<T>(p.draft, (long long)b * p.K + i, p.V)
-                              : row_ptr<T>(p.target, (long long)b * (p.K + 1) + i, p.V);
+    const Task k = decode_task<G>(p, t);
+    if (k.need) {
+      const T* row = task_row<T>(p, k);
       typename L::Raw raw[G][L::NV];
 #pragma unroll
       for (int g = 0; g < G; ++g)
-        if (g < nch) load_chunk<T, VEC>(row, p.V, c0 + g, raw[g]);
-      int mask_x = -1;
-      if (MODE == kOneHot && !is_draft && i < Kb)
-        mask_x = __ldg(p.draft_tokens + (long long)b * p.K + i);
-      float2* rec = p.rec + rowid * p.NC;
+        if (g < k.nch) load_chunk<T, VEC>(row, p.V, k.c0 + g, raw[g]);
+      const int mask_x = task_mask<MODE>(p, k);
+      float2* rec = p.rec + k.rowid * p.NC;
 #pragma unroll
-      for (int g = 0; g < G; ++g) {
-        if (g < nch) {
-          const int c = c0 + g;
-          float2 out;
-          if (MODE == kGreedy) {
-            out = chunk_argmax<T, VEC>(raw[g], c * kChunk);
-          } else {
-            const int ml = (mask_x >= c * kChunk && mask_x < (c + 1) * kChunk) ? mask_x - c * kChunk
-                                                                               : -1;
-            out = chunk_softmax<T, VEC>(raw[g], p.cc, ml);
+      for (int g = 0; g < G; ++g)
+        if (g < k.nch) {
+          const float2 out = chunk_record<MODE, T, VEC>(raw[g], k.c0 + g, p.cc, mask_x);
+          if (lane == 0) rec[k.c0 + g] = out;
+        }
+    }
+    int old = 0;
+    if (lane == 0) old = atomic_add_acq_rel(p.row_ticket + k.rowid, k.nch);
+    if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
+    prev = k;
+    prev_old = old;
+    have_prev = true;
+  }
+  if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
+}
+
+// Shared-memory ring of the bulk-copy variant (vector paths): each warp owns
+// kStages chunk buffers, each with an mbarrier.  Lane 0 keeps the next chunks
+// of the warp's task sequence in flight with cp.async.bulk while the warp
+// reduces the oldest one, so the bytes in flight do not depend on registers.
+template <typename T>
+struct Ring {
+  static constexpr int kChunkBytes = kChunk * (int)sizeof(T);
+  static constexpr int kStages = sizeof(T) == 2 ? 6 : 3;
+  static constexpr int kWarpBytes = kStages * kChunkBytes;
+  static constexpr int kBulkG = 8;  // chunks per task
+  static constexpr int smem_bytes() { return (kThreads / kWarp) * (kWarpBytes + kStages * 8); }
+};
+
+template <int MODE, typename T, int VEC>
+__global__ void __launch_bounds__(kThreads) verify_rows_bulk_kernel(const VerifyParams p) {
+  using L = Lane<T, VEC>;
+  using RG = Ring<T>;
+  constexpr int S = RG::kStages;
+  constexpr int G = RG::kBulkG;
+  extern __shared__ __align__(128) unsigned char smem[];
+  pdl_launch_dependents();
+  const int lane = lane_id(), warp = threadIdx.x >> 5;
+  const uint32_t ring = smem_u32(smem) + warp * RG::kWarpBytes;
+  const uint32_t bars = smem_u32(smem) + (kThreads / kWarp) * RG::kWarpBytes + warp * S * 8;
+  if (lane == 0) {
+    for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+
+  // producer state (lane 0): the next chunk of the warp's task sequence
+  long long pt = gw;
+  int pg = 0;
+  Task ptask{};
+  bool pdone = true;
+  uint32_t issued = 0;
+  auto skip_empty = [&]() {
+    while (!pdone && (!ptask.need || pg >= ptask.nch)) {
+      pt += nw;
+      pg = 0;
+      if (pt >= p.total_tasks) {
+        pdone = true;
+        break;
+      }
+      ptask = decode_task<G>(p, pt);
+    }
+  };
+  auto issue_next = [&]() {
+    if (pdone) return;
+    const int c = ptask.c0 + pg;
+    const T* src = task_row<T>(p, ptask) + (long long)c * kChunk;
+    const uint32_t bytes = (uint32_t)(min(kChunk, p.V - c * kChunk) * (int)sizeof(T));
+    const int stage = (int)(issued % S);
+    bulk_load(ring + stage * RG::kChunkBytes, src, bytes, bars + 8 * stage);
+    ++issued;
+    ++pg;
+    skip_empty();
+  };
+  if (lane == 0 && pt < p.total_tasks) {
+    pdone = false;
+    ptask = decode_task<G>(p, pt);
+    skip_empty();
+    for (int s = 0; s < S; ++s) issue_next();
+  }
+
+  uint32_t consumed = 0;  // chunks whose copy landed and was reduced
+  bool failed = false;
+  bool have_prev = false;
+  Task prev{};
+  int prev_old = 0;
+  for (long long t = gw; t < p.total_tasks; t += nw) {
+    const Task k = decode_task<G>(p, t);
+    if (k.need) {
+      const int mask_x = task_mask<MODE>(p, k);
+      float2* rec = p.rec + k.rowid * p.NC;
+      for (int g = 0; g < k.nch; ++g) {
+        const int c = k.c0 + g;
+        const int stage = (int)(consumed % S);
+        bool ok = !failed && mbar_wait(bars + 8 * stage, (consumed / S) & 1u);
+        ok = __all_sync(0xffffffffu, ok);
+        float2 out = make_float2(qnan(), 0.f);
+        if (ok) {
+          typename L::Raw raw[L::NV];
+          load_chunk_smem<T, VEC>(ring + stage * RG::kChunkBytes, p.V, c, raw);
+          out = chunk_record<MODE, T, VEC>(raw, c, p.cc, mask_x);
+          ++consumed;
+        } else if (!failed) {
+          // a copy did not land in time: issue no more copies; this and the
+          // warp's remaining chunks are recorded as unusable
+          failed = true;
+          if (lane == 0) atomicOr(p.err, 1);
+        }
+        __syncwarp();
+        if (lane == 0) {
+          rec[c] = out;
+          if (!failed) {
+            fence_proxy_async();
+            issue_next();
           }
-          if (lane == 0) rec[c] = out;
         }
       }
     }
     int old = 0;
-    if (lane == 0) {
-      __threadfence();
-      old = atomicAdd(p.row_ticket + rowid, nch);
-    }
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old + nch == p.NC) {
-      __threadfence();
-      row_finalize<MODE, T, VEC>(p, b, r, rowid, need, Kb);
-    }
+    if (lane == 0) old = atomic_add_acq_rel(p.row_ticket + k.rowid, k.nch);
+    if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
+    prev = k;
+    prev_old = old;
+    have_prev = true;
+  }
+  if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
+  if (failed && lane == 0) {  // let copies still in flight land before the CTA exits
+    for (uint32_t j = consumed; j < issued; ++j) mbar_wait(bars + 8 * (j % S), (j / S) & 1u);
   }
 }
 
@@ -458,9 +617,14 @@ __device__ __noinline__ void residual_finalize(const VerifyParams& p, int b, con
 }
 
 template <typename T, int VEC>
+__host__ __device__ constexpr int residual_group() {
+  return Lane<T, VEC>::G > 1 ? Lane<T, VEC>::G / 2 : 1;
+}
+
+template <typename T, int VEC>
 __global__ void __launch_bounds__(kThreads, 2) residual_kernel(const VerifyParams p) {
   using L = Lane<T, VEC>;
-  constexpr int G = L::G > 1 ? L::G / 2 : 1;
+  constexpr int G = residual_group<T, VEC>();
   pdl_wait();
   pdl_launch_dependents();
   const int lane = lane_id();
@@ -500,15 +664,9 @@ __global__ void __launch_bounds__(kThreads, 2) residual_kernel(const VerifyParam
       }
     }
     int old = 0;
-    if (lane == 0) {
-      __threadfence();
-      old = atomicAdd(p.res_ticket + b, nch);
-    }
+    if (lane == 0) old = atomic_add_acq_rel(p.res_ticket + b, nch);
     old = __shfl_sync(0xffffffffu, old, 0);
-    if (old + nch == p.NC) {
-      __threadfence();
-      residual_finalize<T, VEC>(p, b, st);
-    }
+    if (old + nch == p.NC) residual_finalize<T, VEC>(p, b, st);
   }
 }
 
@@ -603,16 +761,32 @@ cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
   cudaError_t err = device_info(&di);
   if (err != cudaSuccess) return err;
   const int warps_per_cta = kThreads / kWarp;
-  {
+  if constexpr (VEC * sizeof(T) == 16) {
+    constexpr int smem = Ring<T>::smem_bytes();
+    static int occ = 0;
+    if (!occ) {
+      err = cudaFuncSetAttribute(verify_rows_bulk_kernel<MODE, T, VEC>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      if (err != cudaSuccess) return err;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+              &occ, verify_rows_bulk_kernel<MODE, T, VEC>, kThreads, smem) != cudaSuccess ||
+          occ < 1)
+        occ = 1;
+    }
+    const long long want = (p.total_tasks + warps_per_cta - 1) / warps_per_cta;
+    const long long cap = (long long)di.sms * occ;
+    const int grid = (int)(want < cap ? want : cap);
+    verify_rows_bulk_kernel<MODE, T, VEC><<<grid, kThreads, smem, s>>>(p);
+  } else {
     static int occ = 0;
     if (!occ) occ = blocks_per_sm(verify_rows_kernel<MODE, T, VEC>);
     const long long want = (p.total_tasks + warps_per_cta - 1) / warps_per_cta;
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(want < cap ? want : cap);
     verify_rows_kernel<MODE, T, VEC><<<grid, kThreads, 0, s>>>(p);
-    err = cudaGetLastError();
-    if (err != cudaSuccess) return err;
   }
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
   if (MODE == kDense) {
     static int occ = 0;
     if (!occ) occ = blocks_per_sm(residual_kernel<T, VEC>);
@@ -646,6 +820,16 @@ cudaError_t launch_mode(int dtype, bool vec, const VerifyParams& p, bool compact
 }
 
 }  // namespace
+
+int chunks_per_task(int dtype, bool vec) {
+  if (vec) return dtype == kBF16 ? Ring<uint16_t>::kBulkG : Ring<float>::kBulkG;
+  return Lane<float, 1>::G;
+}
+
+int residual_chunks_per_task(int dtype, bool vec) {
+  if (!vec) return residual_group<float, 1>();
+  return dtype == kBF16 ? residual_group<uint16_t, 8>() : residual_group<float, 4>();
+}
 
 cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p, bool compact,
                           cudaStream_t stream) {
