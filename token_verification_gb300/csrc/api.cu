@@ -22,13 +22,10 @@ static WorkspaceLayout layout_for(int B, int R, int V) {
   const size_t NC = ((size_t)V + kChunk - 1) / kChunk;
   WorkspaceLayout l;
   size_t o = 0;
-  l.row_ticket = o; o = align256(o + sizeof(int) * (size_t)B * R);
-  l.req_ticket = o; o = align256(o + sizeof(int) * (size_t)B);
   l.res_ticket = o; o = align256(o + sizeof(int) * (size_t)B);
   l.counters = o;   o = align256(o + 2 * sizeof(int));
   l.state = o;      o = align256(o + sizeof(ReqState) * (size_t)B);
   l.zero_bytes = o;
-  l.row_sum = o;    o = align256(o + sizeof(RowSum) * (size_t)B * R);
   l.rec = o;        o = align256(o + sizeof(float2) * (size_t)B * R * NC);
   l.res_rec = o;    o = align256(o + sizeof(float) * (size_t)B * NC);
   l.total = o;
@@ -124,12 +121,9 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.out_packed = out_packed;
   p.out_batch_id = out_batch_id;
   char* base = static_cast<char*>(ws);
-  p.row_ticket = reinterpret_cast<int*>(base + l.row_ticket);
-  p.req_ticket = reinterpret_cast<int*>(base + l.req_ticket);
   p.res_ticket = reinterpret_cast<int*>(base + l.res_ticket);
   p.err = reinterpret_cast<int*>(base + l.counters);
   p.fin_ticket = p.err + 1;
-  p.row_sum = reinterpret_cast<RowSum*>(base + l.row_sum);
   p.state = reinterpret_cast<ReqState*>(base + l.state);
   p.rec = reinterpret_cast<float2*>(base + l.rec);
   p.res_rec = reinterpret_cast<float*>(base + l.res_rec);
@@ -139,8 +133,12 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.NC = (V + kChunk - 1) / kChunk;
   p.R = R;
   p.TPR = (p.NC + G - 1) / G;
+  p.item_chunks = G;
   p.TPR_res = (p.NC + Gr - 1) / Gr;
   p.total_tasks = (long long)B * R * p.TPR;
+  if (p.total_tasks >= (1LL << 31)) return SV_ERR_SHAPE;
+  p.div_tpr = make_fastdiv((uint32_t)p.TPR);
+  p.div_r = make_fastdiv((uint32_t)R);
   p.cc = mode == kGreedy ? 0.f : (float)(1.4426950408889634 / (double)T);
   p.greedy_prob = greedy_prob;
   const bool compact = out_cu || out_packed || out_batch_id;

@@ -64,6 +64,28 @@ __device__ __forceinline__ float warp_max_nan(float x) {
 
 __device__ __forceinline__ bool is_finite(float x) { return fabsf(x) <= FLT_MAX; }
 
+// Unsigned division by a run-time invariant d >= 1 through a multiply and
+// shifts (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", 1994): with l = ceil(log2 d) and m = floor(2^32 (2^l - d) / d) + 1,
+// q = (t + ((n - t) >> 1)) >> (l - 1) where t = mulhi(m, n), for every 32-bit n.
+struct FastDiv {
+  uint32_t d, m, s1, s2;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  uint32_t l = 0;
+  while (l < 32 && (1ull << l) < d) ++l;
+  FastDiv f;
+  f.d = d;
+  f.m = (uint32_t)(((1ull << 32) * ((1ull << l) - d)) / d + 1);
+  f.s1 = l > 0 ? 1 : 0;
+  f.s2 = l > 0 ? l - 1 : 0;
+  return f;
+}
+__device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+  const uint32_t t = __umulhi(f.m, n);
+  return (t + ((n - t) >> f.s1)) >> f.s2;
+}
+
 __device__ __forceinline__ float qnan() { return __int_as_float(0x7fffffff); }
 
 __device__ __forceinline__ float warp_sum(float x) {
@@ -146,8 +168,7 @@ __device__ __forceinline__ f32x2 add2(f32x2 a, f32x2 b) {
 // shared-memory staging: bulk copies completed on an mbarrier
 // ---------------------------------------------------------------------------
 
-constexpr uint32_t kWaitHintNs = 1000000;  // max suspension per try_wait (1 ms)
-constexpr int kWaitTries = 2000;           // so no wait lasts longer than ~2 s
+constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // no wait lasts longer than 2 s
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return (uint32_t)__cvta_generic_to_shared(p);
@@ -175,18 +196,28 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
       " selp.u32 %0, 1, 0, p;\n}"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(kWaitHintNs)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
-// Bounded wait for phase `parity` of `bar`; false if it did not complete.
+__device__ __forceinline__ unsigned long long global_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+// Wait for phase `parity` of `bar`, for at most kWaitLimitNs of wall time;
+// false if it did not complete.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-  for (int i = 0; i < kWaitTries; ++i)
-    if (mbar_try_wait(bar, parity)) return true;
-  return false;
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = global_ns();
+  for (;;) {
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > kWaitLimitNs) return false;
+  }
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   uint4 v;
@@ -330,17 +361,13 @@ __device__ __forceinline__ void mask_element(typename Lane<T, VEC>::Raw (&raw)[L
 // bf16 vector tile (4 x 128-bit groups = 16 words = 32 logits per lane):
 // NaN-propagating max on packed bf16 pairs.
 __device__ __forceinline__ float lane_max_bf16(const uint4 (&raw)[4]) {
-  uint32_t m = bf16x2_max_nan(raw[0].x, raw[0].y);
-  m = bf16x2_max_nan(m, raw[0].z);
-  m = bf16x2_max_nan(m, raw[0].w);
+  // a depth-4 tree over the 16 words (a serial chain would be 15 deep)
+  uint32_t m[4];
 #pragma unroll
-  for (int k = 1; k < 4; ++k) {
-    m = bf16x2_max_nan(m, raw[k].x);
-    m = bf16x2_max_nan(m, raw[k].y);
-    m = bf16x2_max_nan(m, raw[k].z);
-    m = bf16x2_max_nan(m, raw[k].w);
-  }
-  return max_nan(bf16_lo(m), bf16_hi(m));
+  for (int k = 0; k < 4; ++k)
+    m[k] = bf16x2_max_nan(bf16x2_max_nan(raw[k].x, raw[k].y), bf16x2_max_nan(raw[k].z, raw[k].w));
+  const uint32_t t = bf16x2_max_nan(bf16x2_max_nan(m[0], m[1]), bf16x2_max_nan(m[2], m[3]));
+  return max_nan(bf16_lo(t), bf16_hi(t));
 }
 
 // Softmax record of one chunk: {m_c, sum_j 2^(l_j*cc - m_c*cc)}, leaving
@@ -370,7 +397,9 @@ __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw
   float s;
   if constexpr (kPacked) {
     const f32x2 c2 = pack2(cc, cc), nb2 = pack2(nb, nb);
-    f32x2 acc0 = pack2(0.f, 0.f), acc1 = pack2(0.f, 0.f);
+    f32x2 acc[4];  // four independent accumulation chains
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = pack2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
@@ -378,13 +407,12 @@ __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw
       for (int q = 0; q < 4; ++q) {
         float a0, a1;
         unpack2(fma2(pack2(bf16_lo(w[q]), bf16_hi(w[q])), c2, nb2), a0, a1);
-        const f32x2 e2 = pack2(ex2(a0), ex2(a1));
-        if (q & 1) acc1 = add2(acc1, e2); else acc0 = add2(acc0, e2);
+        acc[q] = add2(acc[q], pack2(ex2(a0), ex2(a1)));
       }
     }
     float s0, s1, s2, s3;
-    unpack2(acc0, s0, s1);
-    unpack2(acc1, s2, s3);
+    unpack2(add2(acc[0], acc[1]), s0, s1);
+    unpack2(add2(acc[2], acc[3]), s2, s3);
     s = (s0 + s1) + (s2 + s3);
   } else {
     float s0 = 0.f, s1 = 0.f;

@@ -4,13 +4,15 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "sv_common.cuh"
+
 namespace sv {
 
-// Summary of one logit row, written by the warp that finishes the row.
-// Softmax rows: m = row max (NaN if the row is unusable), s = sum of
-// 2^((l_j - m) c) (without the draft token for the rows of one-hot drafts),
-// wx = 2^((l_x - m) c) for the row's draft token x.  Argmax rows: m = max,
-// idx = lowest index attaining it.
+// Summary of one logit row, built by the finalize kernel from the row's
+// chunk records.  Softmax rows: m = row max (NaN if the row is unusable),
+// s = sum of 2^((l_j - m) c) (without the draft token for the rows of one-hot
+// drafts), wx = 2^((l_x - m) c) for the row's draft token x.  Argmax rows:
+// m = max, idx = lowest index attaining it.
 struct RowSum {
   float m;
   float s;
@@ -41,21 +43,20 @@ struct VerifyParams {
   int* out_packed;
   int* out_batch_id;
   // workspace
-  int* row_ticket;   // [B*R]
-  int* req_ticket;   // [B]
   int* res_ticket;   // [B]
   int* err;          // [1] set when a bounded wait gave up
   int* fin_ticket;   // [1] requests finalised in this call
-  RowSum* row_sum;   // [B*R]
   ReqState* state;   // [B]
   float2* rec;       // [B*R*NC]
   float* res_rec;    // [B*NC]
   int B, K, V;
   int NC;            // chunks per row
   int R;             // rows per request: K+1 target (+ K draft rows when dense)
-  int TPR;           // row-statistics tasks per row
+  int TPR;           // stream items per row
+  int item_chunks;   // chunks per stream item
   int TPR_res;       // residual tasks per row pair
-  long long total_tasks;
+  long long total_tasks;  // < 2^31 (checked on the host)
+  FastDiv div_tpr, div_r; // divide by TPR and by R
   float cc;          // log2(e) / T
   int greedy_prob;   // greedy rule reached through the sampling entry
 };
@@ -78,8 +79,7 @@ enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Workspace layout for B requests, K positions, V vocabulary (dense case).
 struct WorkspaceLayout {
-  size_t row_ticket, req_ticket, res_ticket, counters, state, zero_bytes, row_sum, rec, res_rec,
-      total;
+  size_t res_ticket, counters, state, zero_bytes, rec, res_rec, total;
 };
 WorkspaceLayout workspace_layout(int B, int K, int V);
 
@@ -88,7 +88,7 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo* out);
 
-// Chunks per row-statistics task and per residual task.
+// Chunks per stream item (row-statistics kernel) and per residual task.
 int chunks_per_task(int dtype, bool vec);
 int residual_chunks_per_task(int dtype, bool vec);
 

@@ -8,21 +8,23 @@
 // while x_i equals the target argmax.  Requests are independent and verified
 // in parallel ("投机解码" (FastDeploy), "高效投机解码框架设计").
 //
-// Kernel A (verify_rows_kernel, persistent): every warp streams tasks of up
-//   to G chunks of one logit row and writes one record per chunk.  Each logit
-//   is read once.  The warp that completes a row (atomic ticket per row)
-//   combines its records into a RowSum; the warp that completes a request's
-//   last row (ticket per request) runs the acceptance tests for all positions
-//   at once (one lane per position), then draws the residual / bonus token:
-//   it locates the chunk from the records and rescans that single chunk.
-//   No warp ever waits for another: whoever arrives last does the work.
+// Kernel A (verify_stream_kernel; verify_rows_kernel on the scalar path)
+//   reads every needed logit once and reduces each 1024-logit chunk of a row
+//   to one 8-byte record.  One producer thread per CTA copies items of 15
+//   consecutive chunks (30 KB of bf16) into a ring of shared-memory stages
+//   with cp.async.bulk; each of the 15 consumer warps reduces one chunk of
+//   every stage.  It has no atomics, fences or cross-CTA communication.
+// Kernel F (finalize_kernel, one CTA per request) combines each row's chunk
+//   records, runs the acceptance tests of all positions at once (one lane
+//   per position), then draws the residual / bonus token: the crossing chunk
+//   from the records, then one rescan of that single chunk.
 // Kernel B (residual_kernel, dense drafts only): for each request rejected at
 //   n, sums max(0, p_n - q_n) per chunk of the (target, draft) row pair, and
 //   the last warp of the request draws the token the same way.
 // Kernel C (compact_kernel): exclusive scan of accept_len and the packed,
 //   padding-free output with per-token batch ids.
-// B and C start with programmatic dependent launch and wait for their
-// predecessor's results on the device.
+// F, B and C start with programmatic dependent launch and wait on the device
+// for their predecessor's results.
 #include "sv_common.cuh"
 #include "sv_launch.h"
 
@@ -32,21 +34,6 @@ namespace {
 template <typename T>
 __device__ __forceinline__ const T* row_ptr(const void* base, long long row, int V) {
   return reinterpret_cast<const T*>(base) + row * (long long)V;
-}
-
-__device__ __forceinline__ RowSum load_rowsum(const RowSum* p) {
-  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
-  RowSum r;
-  r.m = __int_as_float(v.x);
-  r.s = __int_as_float(v.y);
-  r.wx = __int_as_float(v.z);
-  r.idx = v.w;
-  return r;
-}
-
-__device__ __forceinline__ void store_rowsum(RowSum* p, const RowSum& r) {
-  *reinterpret_cast<int4*>(p) =
-      make_int4(__float_as_int(r.m), __float_as_int(r.s), __float_as_int(r.wx), r.idx);
 }
 
 __device__ __forceinline__ ReqState load_state(const ReqState* p) {
@@ -72,13 +59,14 @@ __device__ __forceinline__ ReqState load_state(const ReqState* p) {
 // weight that lies below the target; if rounding leaves the target past the
 // last chunk, returns the last chunk of positive weight with fraction 2
 // (which selects its last positive element).  c = -1 if no weight at all.
+// The chunk weights of the first kRecCache * 32 chunks come from `wc`
+// (cached per lane: chunk lane + 32 t in wc[t]); later chunks from weight(c).
 template <class F>
-__device__ int find_chunk(F weight, int NC, float target, float* frac) {
+__device__ int find_chunk(const float (&wc)[kRecCache], F weight, int NC, float target,
+                          float* frac) {
   const int lane = lane_id();
   float base = 0.f;
-  for (int c0 = 0; c0 < NC; c0 += kWarp) {
-    const int c = c0 + lane;
-    const float w = c < NC ? weight(c) : 0.f;
+  auto round = [&](int c0, float w, int* out) {
     const float incl = warp_incl_scan(w);
     const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && base + incl > target);
     if (hit) {
@@ -86,9 +74,20 @@ __device__ int find_chunk(F weight, int NC, float target, float* frac) {
       const float below = target - (base + __shfl_sync(0xffffffffu, incl - w, l));
       const float wl = __shfl_sync(0xffffffffu, w, l);
       *frac = fminf(fmaxf(below / wl, 0.f), 1.f);
-      return c0 + l;
+      *out = c0 + l;
+      return true;
     }
     base += __shfl_sync(0xffffffffu, incl, kWarp - 1);
+    return false;
+  };
+  int found = -1;
+#pragma unroll
+  for (int t = 0; t < kRecCache; ++t)
+    if (found < 0 && t * kWarp < NC && round(t * kWarp, wc[t], &found)) break;
+  if (found >= 0) return found;
+  for (int c0 = kRecCache * kWarp; c0 < NC; c0 += kWarp) {
+    const int c = c0 + lane;
+    if (round(c0, c < NC ? weight(c) : 0.f, &found)) return found;
   }
   for (int c0 = ((NC - 1) / kWarp) * kWarp; c0 >= 0; c0 -= kWarp) {
     const int c = c0 + lane;
@@ -165,11 +164,18 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
     const float2 r = __ldcg(rec + c);
     return r.y * ex2(fmaf(r.x, cc, nb));
   };
+  float wc[kRecCache];  // one batch of loads for the first 256 chunks
   float tot = 0.f;
-  for (int c = lane; c < NC; c += kWarp) tot += weight(c);
+#pragma unroll
+  for (int t = 0; t < kRecCache; ++t) {
+    const int c = lane + t * kWarp;
+    wc[t] = c < NC ? weight(c) : 0.f;
+    tot += wc[t];
+  }
+  for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
   tot = warp_sum(tot);
   float frac = 0.f;
-  const int c = find_chunk(weight, NC, u * tot, &frac);
+  const int c = find_chunk(wc, weight, NC, u * tot, &frac);
   if (c < 0) return -1;
   typename L::Raw raw[L::NV];
   load_chunk<T, VEC>(row, V, c, raw);
@@ -211,21 +217,71 @@ __device__ __forceinline__ void write_request(const VerifyParams& p, int b, int 
 }
 
 // ---------------------------------------------------------------------------
-// request / row finalisation (run by the last-arriving warp)
+// kernel F: per-request finalisation (one CTA per request, after kernel A)
 // ---------------------------------------------------------------------------
 
-template <int MODE, typename T, int VEC>
-__device__ __noinline__ void request_finalize(const VerifyParams& p, int b, int Kb) {
-  const int lane = lane_id();
-  const int K = p.K;
-  // A bounded wait that gave up earlier in this call marks every request
-  // finalised after it (its chunks may be among the unread ones).
-  int status = 0;
-  if (lane == 0) {
-    p.req_ticket[b] = 0;
-    if (__ldcg(p.err)) status = kTimeout;
+// Whether row r of request b is needed: target rows 0..K_b, draft rows
+// 0..K_b-1 (K_b = draft_lens[b] or K; nothing when K_b is invalid).
+__device__ __forceinline__ bool row_needed(const VerifyParams& p, int r, int Kb) {
+  if (Kb < 0 || Kb > p.K) return false;
+  return r > p.K ? (r - p.K - 1) < Kb : r <= Kb;
+}
+
+// Summary of one row from its chunk records (one warp).
+template <int MODE, typename T>
+__device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb) {
+  RowSum rs{qnan(), 0.f, 0.f, -1};
+  const long long rowid = (long long)b * p.R + r;
+  const float2* rec = p.rec + rowid * p.NC;
+  if (MODE == kGreedy) {
+    const float2 a = combine_argmax_records(rec, p.NC);
+    rs.m = a.x;
+    rs.idx = __float_as_int(a.y);
+    return rs;
   }
-  status = __shfl_sync(0xffffffffu, status, 0);
+  const bool is_draft = r > p.K;
+  const int i = is_draft ? r - p.K - 1 : r;
+  const int x = i < Kb ? __ldg(p.draft_tokens + (long long)b * p.K + i) : -1;
+  const bool has_x = x >= 0 && x < p.V;
+  float lx = 0.f;
+  if (has_x) {
+    const T* row = is_draft ? row_ptr<T>(p.draft, (long long)b * p.K + i, p.V)
+                            : row_ptr<T>(p.target, (long long)b * (p.K + 1) + i, p.V);
+    lx = load_logit(row, x);
+  }
+  const float2 ms = combine_softmax_records(rec, p.NC, p.cc);
+  rs.m = ms.x;
+  rs.s = ms.y;
+  if (has_x && is_finite(ms.x)) rs.wx = ex2(fmaf(lx, p.cc, -ms.x * p.cc));
+  return rs;
+}
+
+constexpr int kFinThreads = 256;
+constexpr int kMaxRows = 2 * kMaxK + 1;
+
+// The acceptance tests of all positions at once (one lane per position),
+// then the residual / bonus draw (rejection sampling, [SD] §2.1) or the
+// argmax (greedy).  Rows are summarised by the CTA's warps first.
+template <int MODE, typename T, int VEC>
+__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParams p) {
+  __shared__ RowSum srow[kMaxRows];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x;
+  const int lane = lane_id(), warp = threadIdx.x >> 5;
+  const int K = p.K;
+  int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
+  for (int r = warp; r < p.R; r += kFinThreads / kWarp) {
+    RowSum rs{qnan(), 0.f, 0.f, -1};
+    if (row_needed(p, r, Kb)) rs = summarise_row<MODE, T>(p, b, r, Kb);
+    if (lane == 0) srow[r] = rs;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+
+  // A bounded wait that gave up in kernel A (a device fault) invalidates the
+  // whole call: its chunk records may be missing.
+  int status = __ldcg(p.err) ? kTimeout : 0;
   if (Kb < 0 || Kb > K) {
     status |= kBadDraftLen;
     Kb = 0;
@@ -237,10 +293,9 @@ __device__ __noinline__ void request_finalize(const VerifyParams& p, int b, int 
   float theta = -1.f;
   bool pending = false;
   if (!status) {
-    const long long rb = (long long)b * p.R;
     RowSum rt{qnan(), 0.f, 0.f, -1}, rd{qnan(), 0.f, 0.f, -1};
-    if (lane <= Kb) rt = load_rowsum(p.row_sum + rb + lane);
-    if (MODE == kDense && lane < Kb) rd = load_rowsum(p.row_sum + rb + K + 1 + lane);
+    if (lane <= Kb) rt = srow[lane];
+    if (MODE == kDense && lane < Kb) rd = srow[K + 1 + lane];
     bool bad = lane <= Kb && !is_finite(rt.m);
     if (MODE == kDense && lane < Kb) bad = bad || !is_finite(rd.m);
     bool acc = false;
@@ -293,14 +348,14 @@ __device__ __noinline__ void request_finalize(const VerifyParams& p, int b, int 
           token = x_n;  // no mass left beside x_n: p_n itself is the point mass at x_n
         } else {
           const T* row = row_ptr<T>(p.target, (long long)b * (K + 1) + n, p.V);
-          token = draw_from_records<T, VEC>(row, p.rec + (rb + n) * p.NC, p.NC, p.V, m_n, p.cc,
-                                            uK, residual ? x_n : -1);
+          token = draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + n) * p.NC, p.NC,
+                                            p.V, m_n, p.cc, uK, residual ? x_n : -1);
           if (token < 0) status = kBadLogits;
         }
       }
     }
   }
-  // the last request finalised in this call clears the call's counters
+  // the last request finalised in this call clears the call's error flag
   if (lane == 0 && atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
     *p.err = 0;
     *p.fin_ticket = 0;
@@ -311,85 +366,9 @@ __device__ __noinline__ void request_finalize(const VerifyParams& p, int b, int 
   if (!pending) write_request(p, b, status, n, token, x);
 }
 
-template <int MODE, typename T, int VEC>
-__device__ __noinline__ void row_finalize(const VerifyParams& p, int b, int r, long long rowid,
-                                          bool need, int Kb) {
-  const int lane = lane_id();
-  RowSum rs{qnan(), 0.f, 0.f, -1};
-  if (need) {
-    const float2* rec = p.rec + rowid * p.NC;
-    if (MODE == kGreedy) {
-      const float2 a = combine_argmax_records(rec, p.NC);
-      rs.m = a.x;
-      rs.idx = __float_as_int(a.y);
-    } else {
-      const bool is_draft = r > p.K;
-      const int i = is_draft ? r - p.K - 1 : r;
-      const int x = i < Kb ? __ldg(p.draft_tokens + (long long)b * p.K + i) : -1;
-      const bool has_x = x >= 0 && x < p.V;
-      float lx = 0.f;
-      if (has_x) {
-        const T* row = is_draft ? row_ptr<T>(p.draft, (long long)b * p.K + i, p.V)
-                                : row_ptr<T>(p.target, (long long)b * (p.K + 1) + i, p.V);
-        lx = load_logit(row, x);
-      }
-      const float2 ms = combine_softmax_records(rec, p.NC, p.cc);
-      rs.m = ms.x;
-      rs.s = ms.y;
-      if (has_x && is_finite(ms.x)) rs.wx = ex2(fmaf(lx, p.cc, -ms.x * p.cc));
-    }
-  }
-  int old = 0;
-  if (lane == 0) {
-    store_rowsum(p.row_sum + rowid, rs);
-    p.row_ticket[rowid] = 0;
-    old = atomic_add_acq_rel(p.req_ticket + b, 1);
-  }
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old + 1 == p.R) request_finalize<MODE, T, VEC>(p, b, Kb);
-}
-
 // ---------------------------------------------------------------------------
-// kernel A: row statistics + finalisation
+// kernel A: chunk records (a single streaming read of the logits)
 // ---------------------------------------------------------------------------
-
-// A task is up to G consecutive chunks of one row.  Tasks are numbered
-// request-major (request, row, chunk group), so requests complete one after
-// another while the grid streams.
-struct Task {
-  long long rowid;
-  int b, r, i, Kb, c0, nch;
-  bool is_draft, need;
-};
-
-template <int G>
-__device__ __forceinline__ Task decode_task(const VerifyParams& p, long long t) {
-  Task k;
-  k.rowid = t / p.TPR;
-  const int tc = (int)(t % p.TPR);
-  k.r = (int)(k.rowid % p.R);
-  k.b = (int)(k.rowid / p.R);
-  k.Kb = p.draft_lens ? __ldg(p.draft_lens + k.b) : p.K;
-  k.is_draft = k.r > p.K;
-  k.i = k.is_draft ? k.r - p.K - 1 : k.r;
-  k.need = k.Kb >= 0 && k.Kb <= p.K && (k.is_draft ? k.i < k.Kb : k.i <= k.Kb);
-  k.c0 = tc * G;
-  k.nch = min(G, p.NC - k.c0);
-  return k;
-}
-
-template <typename T>
-__device__ __forceinline__ const T* task_row(const VerifyParams& p, const Task& k) {
-  return k.is_draft ? row_ptr<T>(p.draft, (long long)k.b * p.K + k.i, p.V)
-                    : row_ptr<T>(p.target, (long long)k.b * (p.K + 1) + k.i, p.V);
-}
-
-// The one-hot draft token of this task's row (excluded from its sums), or -1.
-template <int MODE>
-__device__ __forceinline__ int task_mask(const VerifyParams& p, const Task& k) {
-  if (MODE != kOneHot || k.is_draft || k.i >= k.Kb) return -1;
-  return __ldg(p.draft_tokens + (long long)k.b * p.K + k.i);
-}
 
 template <int MODE, typename T, int VEC>
 __device__ __forceinline__ float2 chunk_record(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
@@ -399,16 +378,40 @@ __device__ __forceinline__ float2 chunk_record(typename Lane<T, VEC>::Raw (&raw)
   return chunk_softmax<T, VEC>(raw, cc, ml);
 }
 
-// A task's arrival on its row's counter is issued at the end of the task and
-// its result read only at the end of the next one, so the atomic's round trip
-// overlaps work; the warp that completes the row finalises it.
-template <int MODE, typename T, int VEC>
-__device__ __forceinline__ void settle_task(const VerifyParams& p, const Task& k, int old_lane0) {
-  const int old = __shfl_sync(0xffffffffu, old_lane0, 0);
-  if (old + k.nch == p.NC) row_finalize<MODE, T, VEC>(p, k.b, k.r, k.rowid, k.need, k.Kb);
+// The row of a stream item and what the chunk reductions need to know.
+struct Item {
+  int rowid, c0, nch, mask;  // mask: one-hot draft token of a target row, else -1
+  bool need;
+};
+
+template <int MODE>
+__device__ __forceinline__ Item decode_item(const VerifyParams& p, uint32_t it) {
+  Item k;
+  const uint32_t row = fast_div(it, p.div_tpr);  // total items < 2^31
+  const int part = (int)(it - row * (uint32_t)p.TPR);
+  const int b = (int)fast_div(row, p.div_r);
+  const int r = (int)(row - (uint32_t)b * (uint32_t)p.R);
+  const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : p.K;
+  k.rowid = (int)row;
+  k.c0 = part * p.item_chunks;
+  k.nch = min(p.item_chunks, p.NC - k.c0);
+  k.need = row_needed(p, r, Kb);
+  k.mask = (MODE == kOneHot && r <= p.K && r < Kb && k.need)
+               ? __ldg(p.draft_tokens + (long long)b * p.K + r)
+               : -1;
+  return k;
 }
 
-// Register-tile variant: the scalar path (any V, any alignment).
+template <typename T>
+__device__ __forceinline__ const T* item_row(const VerifyParams& p, int rowid) {
+  const int b = (int)fast_div((uint32_t)rowid, p.div_r);
+  const int r = rowid - b * p.R;
+  return r > p.K ? row_ptr<T>(p.draft, (long long)b * p.K + (r - p.K - 1), p.V)
+                 : row_ptr<T>(p.target, (long long)b * (p.K + 1) + r, p.V);
+}
+
+// Register-tile variant (scalar path: any V, any alignment): warps stride
+// over items of G chunks.
 template <int MODE, typename T, int VEC>
 __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyParams p) {
   using L = Lane<T, VEC>;
@@ -417,150 +420,145 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
   const int lane = lane_id();
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-  bool have_prev = false;
-  Task prev{};
-  int prev_old = 0;
   for (long long t = gw; t < p.total_tasks; t += nw) {
-    const Task k = decode_task<G>(p, t);
-    if (k.need) {
-      const T* row = task_row<T>(p, k);
-      typename L::Raw raw[G][L::NV];
+    const Item k = decode_item<MODE>(p, (uint32_t)t);
+    if (!k.need) continue;
+    const T* row = item_row<T>(p, k.rowid);
+    typename L::Raw raw[G][L::NV];
 #pragma unroll
-      for (int g = 0; g < G; ++g)
-        if (g < k.nch) load_chunk<T, VEC>(row, p.V, k.c0 + g, raw[g]);
-      const int mask_x = task_mask<MODE>(p, k);
-      float2* rec = p.rec + k.rowid * p.NC;
+    for (int g = 0; g < G; ++g)
+      if (g < k.nch) load_chunk<T, VEC>(row, p.V, k.c0 + g, raw[g]);
+    float2* rec = p.rec + (long long)k.rowid * p.NC;
 #pragma unroll
-      for (int g = 0; g < G; ++g)
-        if (g < k.nch) {
-          const float2 out = chunk_record<MODE, T, VEC>(raw[g], k.c0 + g, p.cc, mask_x);
-          if (lane == 0) rec[k.c0 + g] = out;
-        }
-    }
-    int old = 0;
-    if (lane == 0) old = atomic_add_acq_rel(p.row_ticket + k.rowid, k.nch);
-    if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
-    prev = k;
-    prev_old = old;
-    have_prev = true;
+    for (int g = 0; g < G; ++g)
+      if (g < k.nch) {
+        const float2 out = chunk_record<MODE, T, VEC>(raw[g], k.c0 + g, p.cc, k.mask);
+        if (lane == 0) rec[k.c0 + g] = out;
+      }
   }
-  if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
 }
 
-// Shared-memory ring of the bulk-copy variant (vector paths): each warp owns
-// kStages chunk buffers, each with an mbarrier.  Lane 0 keeps the next chunks
-// of the warp's task sequence in flight with cp.async.bulk while the warp
-// reduces the oldest one, so the bytes in flight do not depend on registers.
+// Streaming variant (vector paths).  Warp 0, lane 0 is the producer: it
+// walks the CTA's contiguous range of items (an item = up to kConsumers
+// consecutive chunks of one row, 30 KB of bf16), and copies each item with
+// one cp.async.bulk into the next of kStages shared-memory stages, together
+// with the item's description.  Each consumer warp w reduces chunk w of every
+// stage into one record.  A stage has a "full" mbarrier (completed by the
+// copy) and an "empty" one (completed when all consumers are done with it).
+// No atomics, fences or cross-CTA traffic: per-request work happens in the
+// finalize kernel.  After the last item the producer publishes an end marker.
+#ifndef SV_STREAM_STAGES_BF16
+#define SV_STREAM_STAGES_BF16 3
+#endif
+#ifndef SV_STREAM_STAGES_F32
+#define SV_STREAM_STAGES_F32 3
+#endif
+constexpr int kStreamThreads = 512;
+constexpr int kConsumers = kStreamThreads / kWarp - 1;  // 15
+
 template <typename T>
-struct Ring {
+struct Stream {
   static constexpr int kChunkBytes = kChunk * (int)sizeof(T);
-  static constexpr int kStages = sizeof(T) == 2 ? 6 : 3;
-  static constexpr int kWarpBytes = kStages * kChunkBytes;
-  static constexpr int kBulkG = 8;  // chunks per task
-  static constexpr int smem_bytes() { return (kThreads / kWarp) * (kWarpBytes + kStages * 8); }
+  static constexpr int kStageBytes = kConsumers * kChunkBytes;
+  static constexpr int kStages = sizeof(T) == 2 ? SV_STREAM_STAGES_BF16 : SV_STREAM_STAGES_F32;
+  static constexpr int kBarOffset = kStages * kStageBytes;
+  static constexpr int kMetaOffset = kBarOffset + kStages * 16;
+  static constexpr int smem_bytes() { return kMetaOffset + kStages * 16; }
 };
 
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
 template <int MODE, typename T, int VEC>
-__global__ void __launch_bounds__(kThreads) verify_rows_bulk_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const VerifyParams p) {
   using L = Lane<T, VEC>;
-  using RG = Ring<T>;
-  constexpr int S = RG::kStages;
-  constexpr int G = RG::kBulkG;
+  using ST = Stream<T>;
+  constexpr int S = ST::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
   const int lane = lane_id(), warp = threadIdx.x >> 5;
-  const uint32_t ring = smem_u32(smem) + warp * RG::kWarpBytes;
-  const uint32_t bars = smem_u32(smem) + (kThreads / kWarp) * RG::kWarpBytes + warp * S * 8;
-  if (lane == 0) {
-    for (int s = 0; s < S; ++s) mbar_init(bars + 8 * s, 1);
+  const uint32_t base = smem_u32(smem);
+  auto stage_of = [&](int s) { return base + s * ST::kStageBytes; };
+  auto full_of = [&](int s) { return base + ST::kBarOffset + s * 16; };
+  auto empty_of = [&](int s) { return full_of(s) + 8; };
+  int4* meta = reinterpret_cast<int4*>(smem + ST::kMetaOffset);
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full_of(s), 1);
+      mbar_init(empty_of(s), kConsumers);
+    }
     fence_mbar_init();
   }
-  __syncwarp();
-  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
+  __syncthreads();
+  // this CTA's contiguous range of items
+  const uint32_t total = (uint32_t)p.total_tasks;
+  const uint32_t lo = (uint32_t)(((unsigned long long)total * blockIdx.x) / gridDim.x);
+  const uint32_t hi = (uint32_t)(((unsigned long long)total * (blockIdx.x + 1)) / gridDim.x);
 
-  // producer state (lane 0): the next chunk of the warp's task sequence
-  long long pt = gw;
-  int pg = 0;
-  Task ptask{};
-  bool pdone = true;
-  uint32_t issued = 0;
-  auto skip_empty = [&]() {
-    while (!pdone && (!ptask.need || pg >= ptask.nch)) {
-      pt += nw;
-      pg = 0;
-      if (pt >= p.total_tasks) {
-        pdone = true;
+  if (warp == 0) {
+    if (lane != 0) return;
+    uint32_t k = 0;  // stages issued
+    bool ok = true;
+    auto acquire = [&](int s) {  // wait until stage s may be refilled
+      return k < (uint32_t)S || mbar_wait(empty_of(s), ((k / S) - 1) & 1u);
+    };
+    for (uint32_t it = lo; it < hi && ok; ++it) {
+      const Item item = decode_item<MODE>(p, it);
+      if (!item.need) continue;
+      const int s = (int)(k % S);
+      if (!acquire(s)) {
+        ok = false;
+        atomicOr(p.err, 1);
         break;
       }
-      ptask = decode_task<G>(p, pt);
+      meta[s] = make_int4(item.rowid, item.c0, item.nch, item.mask);
+      const T* src = item_row<T>(p, item.rowid) + (long long)item.c0 * kChunk;
+      const uint32_t bytes =
+          (uint32_t)(min(item.nch * kChunk, p.V - item.c0 * kChunk) * (int)sizeof(T));
+      bulk_load(stage_of(s), src, bytes, full_of(s));
+      ++k;
     }
-  };
-  auto issue_next = [&]() {
-    if (pdone) return;
-    const int c = ptask.c0 + pg;
-    const T* src = task_row<T>(p, ptask) + (long long)c * kChunk;
-    const uint32_t bytes = (uint32_t)(min(kChunk, p.V - c * kChunk) * (int)sizeof(T));
-    const int stage = (int)(issued % S);
-    bulk_load(ring + stage * RG::kChunkBytes, src, bytes, bars + 8 * stage);
-    ++issued;
-    ++pg;
-    skip_empty();
-  };
-  if (lane == 0 && pt < p.total_tasks) {
-    pdone = false;
-    ptask = decode_task<G>(p, pt);
-    skip_empty();
-    for (int s = 0; s < S; ++s) issue_next();
+    // end marker (a stage whose full barrier completes without a copy)
+    const int s = (int)(k % S);
+    bool marked = false;
+    if (ok && acquire(s)) {
+      meta[s] = make_int4(-1, 0, 0, -1);
+      mbar_arrive(full_of(s));
+      marked = true;
+    } else if (ok) {
+      atomicOr(p.err, 1);
+    }
+    // No copy may be in flight when this thread leaves: wait until the last
+    // copy into each slot has landed.  The marker reused the slot of copy
+    // k - S, whose consumption acquire() already waited for; a parity wait
+    // on that slot would now name a phase two completions back.
+    for (uint32_t j = (k > (uint32_t)S ? k - S : 0) + (marked && k >= (uint32_t)S ? 1 : 0); j < k;
+         ++j)
+      mbar_wait(full_of((int)(j % S)), (j / S) & 1u);
+    return;
   }
 
-  uint32_t consumed = 0;  // chunks whose copy landed and was reduced
-  bool failed = false;
-  bool have_prev = false;
-  Task prev{};
-  int prev_old = 0;
-  for (long long t = gw; t < p.total_tasks; t += nw) {
-    const Task k = decode_task<G>(p, t);
-    if (k.need) {
-      const int mask_x = task_mask<MODE>(p, k);
-      float2* rec = p.rec + k.rowid * p.NC;
-      for (int g = 0; g < k.nch; ++g) {
-        const int c = k.c0 + g;
-        const int stage = (int)(consumed % S);
-        bool ok = !failed && mbar_wait(bars + 8 * stage, (consumed / S) & 1u);
-        ok = __all_sync(0xffffffffu, ok);
-        float2 out = make_float2(qnan(), 0.f);
-        if (ok) {
-          typename L::Raw raw[L::NV];
-          load_chunk_smem<T, VEC>(ring + stage * RG::kChunkBytes, p.V, c, raw);
-          out = chunk_record<MODE, T, VEC>(raw, c, p.cc, mask_x);
-          ++consumed;
-        } else if (!failed) {
-          // a copy did not land in time: issue no more copies; this and the
-          // warp's remaining chunks are recorded as unusable
-          failed = true;
-          if (lane == 0) atomicOr(p.err, 1);
-        }
-        __syncwarp();
-        if (lane == 0) {
-          rec[c] = out;
-          if (!failed) {
-            fence_proxy_async();
-            issue_next();
-          }
-        }
-      }
+  const int w = warp - 1;  // consumer index: chunk w of every stage
+  for (uint32_t k = 0;; ++k) {
+    const int s = (int)(k % S);
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(full_of(s), (k / S) & 1u));
+    if (!ok) {  // the producer or a copy stopped: leave (the call reports a timeout)
+      if (lane == 0) atomicOr(p.err, 1);
+      break;
     }
-    int old = 0;
-    if (lane == 0) old = atomic_add_acq_rel(p.row_ticket + k.rowid, k.nch);
-    if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
-    prev = k;
-    prev_old = old;
-    have_prev = true;
-  }
-  if (have_prev) settle_task<MODE, T, VEC>(p, prev, prev_old);
-  if (failed && lane == 0) {  // let copies still in flight land before the CTA exits
-    for (uint32_t j = consumed; j < issued; ++j) mbar_wait(bars + 8 * (j % S), (j / S) & 1u);
+    const int4 m = meta[s];
+    if (m.x < 0) break;  // end marker
+    if (w < m.z) {
+      const int c = m.y + w;
+      typename L::Raw raw[L::NV];
+      load_chunk_smem<T, VEC>(stage_of(s) + w * ST::kChunkBytes, p.V, c, raw);
+      const float2 out = chunk_record<MODE, T, VEC>(raw, c, p.cc, m.w);
+      if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
+    }
+    // this warp's values from the stage are consumed: hand it back
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty_of(s));
   }
 }
 
@@ -579,8 +577,15 @@ __device__ __noinline__ void residual_finalize(const VerifyParams& p, int b, con
   const T* dr = row_ptr<T>(p.draft, (long long)b * K + st.n, p.V);
   const float* rr = p.res_rec + (long long)b * p.NC;
   auto weight = [&](int c) { return __ldcg(rr + c); };
+  float wc[kRecCache];
   float tot = 0.f;
-  for (int c = lane; c < p.NC; c += kWarp) tot += weight(c);
+#pragma unroll
+  for (int t = 0; t < kRecCache; ++t) {
+    const int c = lane + t * kWarp;
+    wc[t] = c < p.NC ? weight(c) : 0.f;
+    tot += wc[t];
+  }
+  for (int c = lane + kRecCache * kWarp; c < p.NC; c += kWarp) tot += weight(c);
   tot = warp_sum(tot);
   int token;
   if (!(tot > 0.f)) {  // no residual mass (rounding only): draw from p_n
@@ -588,7 +593,7 @@ __device__ __noinline__ void residual_finalize(const VerifyParams& p, int b, con
                                       st.mp, cc, uK, -1);
   } else {
     float frac = 0.f;
-    const int c = find_chunk(weight, p.NC, uK * tot, &frac);
+    const int c = find_chunk(wc, weight, p.NC, uK * tot, &frac);
     typename L::Raw rt[L::NV], rd[L::NV];
     load_chunk<T, VEC>(tr, p.V, c, rt);
     load_chunk<T, VEC>(dr, p.V, c, rd);
@@ -760,26 +765,28 @@ cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
   DeviceInfo di;
   cudaError_t err = device_info(&di);
   if (err != cudaSuccess) return err;
-  const int warps_per_cta = kThreads / kWarp;
+  VerifyParams pc = p;
+  void* args[] = {&pc};
+  // A: chunk records
   if constexpr (VEC * sizeof(T) == 16) {
-    constexpr int smem = Ring<T>::smem_bytes();
+    constexpr int smem = Stream<T>::smem_bytes();
     static int occ = 0;
     if (!occ) {
-      err = cudaFuncSetAttribute(verify_rows_bulk_kernel<MODE, T, VEC>,
+      err = cudaFuncSetAttribute(verify_stream_kernel<MODE, T, VEC>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       if (err != cudaSuccess) return err;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-              &occ, verify_rows_bulk_kernel<MODE, T, VEC>, kThreads, smem) != cudaSuccess ||
+              &occ, verify_stream_kernel<MODE, T, VEC>, kStreamThreads, smem) != cudaSuccess ||
           occ < 1)
         occ = 1;
     }
-    const long long want = (p.total_tasks + warps_per_cta - 1) / warps_per_cta;
     const long long cap = (long long)di.sms * occ;
-    const int grid = (int)(want < cap ? want : cap);
-    verify_rows_bulk_kernel<MODE, T, VEC><<<grid, kThreads, smem, s>>>(p);
+    const int grid = (int)(p.total_tasks < cap ? p.total_tasks : cap);
+    verify_stream_kernel<MODE, T, VEC><<<grid, kStreamThreads, smem, s>>>(p);
   } else {
     static int occ = 0;
     if (!occ) occ = blocks_per_sm(verify_rows_kernel<MODE, T, VEC>);
+    const int warps_per_cta = kThreads / kWarp;
     const long long want = (p.total_tasks + warps_per_cta - 1) / warps_per_cta;
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(want < cap ? want : cap);
@@ -787,23 +794,26 @@ cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
   }
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  // F: acceptance tests and draws, one CTA per request
+  err = launch_pdl(reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>), dim3(p.B),
+                   dim3(kFinThreads), s, args);
+  if (err != cudaSuccess) return err;
+  // B: dense residual draws
   if (MODE == kDense) {
     static int occ = 0;
     if (!occ) occ = blocks_per_sm(residual_kernel<T, VEC>);
+    const int warps_per_cta = kThreads / kWarp;
     const long long want = ((long long)p.B * p.TPR_res + warps_per_cta - 1) / warps_per_cta;
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(want < cap ? want : cap);
-    VerifyParams pc = p;
-    void* args[] = {&pc};
     err = launch_pdl(reinterpret_cast<const void*>(residual_kernel<T, VEC>), dim3(grid),
                      dim3(kThreads), s, args);
     if (err != cudaSuccess) return err;
   }
+  // C: padding-free packed output
   if (compact) {
     const int threads = p.B >= 1024 ? 1024 : ((p.B + kWarp - 1) / kWarp) * kWarp;
     const int grid = (p.B + threads - 1) / threads;
-    VerifyParams pc = p;
-    void* args[] = {&pc};
     err = launch_pdl(reinterpret_cast<const void*>(compact_kernel), dim3(grid), dim3(threads), s,
                      args);
     if (err != cudaSuccess) return err;
@@ -822,7 +832,7 @@ cudaError_t launch_mode(int dtype, bool vec, const VerifyParams& p, bool compact
 }  // namespace
 
 int chunks_per_task(int dtype, bool vec) {
-  if (vec) return dtype == kBF16 ? Ring<uint16_t>::kBulkG : Ring<float>::kBulkG;
+  if (vec) return kConsumers;
   return Lane<float, 1>::G;
 }
 
