@@ -174,6 +174,38 @@ sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent
                            int max_depth, int32_t* out_path, int32_t* out_status,
                            sv_stream_t stream);
 
+/* Allocation-free variant of spec_verify_sample.  The pages have no
+ * counterpart to this entry point; it exists for callers that cannot
+ * allocate device memory - for example an inference runtime that reserves the
+ * whole device for its own pool and hands a plugin only its input and output
+ * buffers, or a path on which a cudaMalloc (which may synchronise the device)
+ * is not allowed.
+ *
+ * Arguments and results are those of spec_verify_sample, without the
+ * workspace.  Its scratch is one fixed device array of
+ * SV_NOALLOC_SCRATCH_BYTES inside the library, held by every GPU that loads
+ * the library until the process exits; the call itself allocates nothing.
+ *   - Limit: spec_verify_workspace_size(B, K, V) must not exceed
+ *     SV_NOALLOC_SCRATCH_BYTES; larger problems return SV_ERR_WORKSPACE with
+ *     nothing queued.  (B = 256, K = 5, V = 152064 needs about 3.4 MB.)
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, which may load the module on that device); make
+ *     that first call before any stream capture.
+ *   - Every call on a device uses the same array, which keeps the previous
+ *     call's contents; each call first clears, on its stream, the counters
+ *     that must start at zero.  Calls that overlap on the GPU (different
+ *     streams, or different host threads without ordering) race on the
+ *     array and give wrong results: order them on one stream. */
+#define SV_NOALLOC_SCRATCH_BYTES (8u << 20)
+sv_status spec_verify_sample_noalloc(const void* target_logits, const void* draft_logits,
+                                     const int32_t* draft_tokens, const float* uniforms,
+                                     float temperature, int32_t* out_tokens,
+                                     int32_t* out_accept_len, sv_dtype dtype, int B, int K, int V,
+                                     const int32_t* draft_lens, int32_t* out_cu_accept,
+                                     int32_t* out_packed, int32_t* out_batch_id,
+                                     float* out_accept_prob, int32_t* out_status,
+                                     sv_stream_t stream);
+
 /* Human-readable name of a status code (static storage). */
 const char* spec_verify_status_string(sv_status status);
 

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(HERE, "libspecverify.so")
 SYMBOLS = (
     "spec_verify_workspace_size", "spec_verify_workspace_init", "spec_verify_sample",
     "spec_verify_greedy", "spec_verify_tree", "spec_verify_status_string",
-    "spec_verify_version",
+    "spec_verify_version", "spec_verify_sample_noalloc",
 )
 
 _lock = threading.Lock()
@@ -40,6 +40,9 @@ def lib():
         l.spec_verify_workspace_init.restype = I
         l.spec_verify_sample.argtypes = [P, P, P, P, F, P, P, I, I, I, I, P, P, P, P, P, P, P, Z, P]
         l.spec_verify_sample.restype = I
+        l.spec_verify_sample_noalloc.argtypes = [P, P, P, P, F, P, P, I, I, I, I, P, P, P, P, P,
+                                                 P, P]
+        l.spec_verify_sample_noalloc.restype = I
         l.spec_verify_greedy.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
         l.spec_verify_greedy.restype = I
         l.spec_verify_tree.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P]
