@@ -27,6 +27,7 @@ static WorkspaceLayout layout_for(int B, int R, int V) {
   l.state = o;      o = align256(o + sizeof(ReqState) * (size_t)B);
   l.zero_bytes = o;
   l.rec = o;        o = align256(o + sizeof(float2) * (size_t)B * R * NC);
+  l.lx = o;         o = align256(o + sizeof(float) * (size_t)B * R);
   l.res_rec = o;    o = align256(o + sizeof(float) * (size_t)B * NC);
   l.total = o;
   return l;
@@ -126,6 +127,7 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.fin_ticket = p.err + 1;
   p.state = reinterpret_cast<ReqState*>(base + l.state);
   p.rec = reinterpret_cast<float2*>(base + l.rec);
+  p.lx = reinterpret_cast<float*>(base + l.lx);
   p.res_rec = reinterpret_cast<float*>(base + l.res_rec);
   p.B = B;
   p.K = K;
@@ -142,6 +144,8 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.cc = mode == kGreedy ? 0.f : (float)(1.4426950408889634 / (double)T);
   p.greedy_prob = greedy_prob;
   const bool compact = out_cu || out_packed || out_batch_id;
+  p.compact_in_finalize = compact ? 1 : 0;
+  p.fin_cache = fin_cache_bytes(p) <= kFinCacheLimit ? 1 : 0;
   if (prepare_workspace(ws, l, B, R, stream) != cudaSuccess) return SV_ERR_CUDA;
   return launch_verify(mode, dtype, vec, p, compact, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }

@@ -482,7 +482,9 @@ __device__ __forceinline__ float2 combine_argmax_records(const float2* rec, int 
 // Combine a row's softmax chunk records into {m, S} with S in the frame of m.
 constexpr int kRecCache = 8;  // records cached per lane (rows of up to 256 chunks)
 
-__device__ __forceinline__ float2 combine_softmax_records(const float2* rec, int NC, float cc) {
+// `copy` (shared memory, or nullptr) receives the records as they are read.
+__device__ __forceinline__ float2 combine_softmax_records(const float2* rec, int NC, float cc,
+                                                          float2* copy = nullptr) {
   const int lane = lane_id();
   float2 cache[kRecCache];
   float lm = -INFINITY;
@@ -490,9 +492,14 @@ __device__ __forceinline__ float2 combine_softmax_records(const float2* rec, int
   for (int t = 0; t < kRecCache; ++t) {
     const int c = lane + t * kWarp;
     cache[t] = c < NC ? __ldcg(rec + c) : make_float2(-INFINITY, 0.f);
+    if (copy && c < NC) copy[c] = cache[t];
     lm = max_nan(lm, cache[t].x);
   }
-  for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) lm = max_nan(lm, __ldcg(rec + c).x);
+  for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) {
+    const float2 r = __ldcg(rec + c);
+    if (copy) copy[c] = r;
+    lm = max_nan(lm, r.x);
+  }
   const float m = warp_max_nan(lm);
   if (!is_finite(m)) return make_float2(m == -INFINITY ? -INFINITY : qnan(), 0.f);
   const float nb = -m * cc;

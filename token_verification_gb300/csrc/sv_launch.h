@@ -48,6 +48,7 @@ struct VerifyParams {
   int* fin_ticket;   // [1] requests finalised in this call
   ReqState* state;   // [B]
   float2* rec;       // [B*R*NC]
+  float* lx;         // [B*R] the logit of each row's draft token
   float* res_rec;    // [B*NC]
   int B, K, V;
   int NC;            // chunks per row
@@ -59,6 +60,8 @@ struct VerifyParams {
   FastDiv div_tpr, div_r; // divide by TPR and by R
   float cc;          // log2(e) / T
   int greedy_prob;   // greedy rule reached through the sampling entry
+  int compact_in_finalize;  // the finalize kernel writes the packed output
+  int fin_cache;     // the finalize kernel keeps the request's records in shared memory
 };
 
 constexpr int kMaxTreeNodes = 256;
@@ -79,7 +82,7 @@ enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Workspace layout for B requests, K positions, V vocabulary (dense case).
 struct WorkspaceLayout {
-  size_t res_ticket, counters, state, zero_bytes, rec, res_rec, total;
+  size_t res_ticket, counters, state, zero_bytes, rec, lx, res_rec, total;
 };
 WorkspaceLayout workspace_layout(int B, int K, int V);
 
@@ -90,6 +93,9 @@ cudaError_t device_info(DeviceInfo* out);
 
 // Chunks per stream item (row-statistics kernel) and per residual task.
 int chunks_per_task(int dtype, bool vec);
+// Shared memory the finalize kernel uses to keep a request's chunk records.
+size_t fin_cache_bytes(const VerifyParams& p);
+constexpr size_t kFinCacheLimit = 48 * 1024;  // without the large-shared-memory opt-in
 int residual_chunks_per_task(int dtype, bool vec);
 
 // mode: 0 one-hot sampling, 1 dense sampling, 2 greedy

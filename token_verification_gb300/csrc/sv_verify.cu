@@ -154,14 +154,15 @@ __device__ int select_in_tile(const float (&w)[NV * VEC], const float (&gsum)[NV
 // Draw from w_j = 2^((l_j - m) c) over one row (w = 0 at mask_x) given the
 // row's softmax chunk records: the crossing chunk from the records, then one
 // rescan of that chunk in its own frame.
-template <typename T, int VEC>
+template <typename T, int VEC, bool kSharedRecords = false>
 __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V, float m, float cc,
                                  float u, int mask_x) {
   using L = Lane<T, VEC>;
   const int lane = lane_id();
   const float nb = -m * cc;
+  auto record = [&](int c) { return kSharedRecords ? rec[c] : __ldcg(rec + c); };
   auto weight = [&](int c) {
-    const float2 r = __ldcg(rec + c);
+    const float2 r = record(c);
     return r.y * ex2(fmaf(r.x, cc, nb));
   };
   float wc[kRecCache];  // one batch of loads for the first 256 chunks
@@ -179,7 +180,7 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
   if (c < 0) return -1;
   typename L::Raw raw[L::NV];
   load_chunk<T, VEC>(row, V, c, raw);
-  const float nbc = -__ldcg(rec + c).x * cc;
+  const float nbc = -record(c).x * cc;
   float w[L::NV * VEC];
   float gsum[L::NV];
 #pragma unroll
@@ -217,6 +218,58 @@ __device__ __forceinline__ void write_request(const VerifyParams& p, int b, int 
 }
 
 // ---------------------------------------------------------------------------
+// padding-free output ("投机解码" (FastDeploy), "高效投机解码框架设计")
+// ---------------------------------------------------------------------------
+
+__device__ int block_sum(int v, int* smem) {
+  const int lane = lane_id(), warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  __syncthreads();
+  if (lane == 0) smem[warp] = v;
+  __syncthreads();
+  int t = 0;
+  for (int w = 0; w < nwarps; ++w) t += smem[w];
+  return t;
+}
+
+__device__ int block_excl_scan(int v, int* smem) {
+  const int lane = lane_id(), warp = threadIdx.x >> 5;
+  const int incl = warp_incl_scan_int(v);
+  __syncthreads();
+  if (lane == kWarp - 1) smem[warp] = incl;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += smem[w];
+  return before + incl - v;
+}
+
+// Exclusive scan of accept_len, packed tokens and per-token batch ids, by
+// one CTA over all B requests (their outputs are complete and visible).
+__device__ void compact_all(const VerifyParams& p, int* smem) {
+  const int B = p.B, W = p.K + 1;
+  int offset = 0;
+  for (int b0 = 0; b0 < B; b0 += blockDim.x) {
+    const int b = b0 + threadIdx.x;
+    const int L = b < B ? __ldcg(p.out_accept_len + b) : 0;
+    const int cu = offset + block_excl_scan(L, smem);
+    if (b < B) {
+      if (p.out_cu) p.out_cu[b] = cu;
+      for (int k = 0; k < L; ++k) {
+        if (p.out_packed) p.out_packed[cu + k] = __ldcg(p.out_tokens + (long long)b * W + k);
+        if (p.out_batch_id) p.out_batch_id[cu + k] = b;
+      }
+    }
+    offset += block_sum(L, smem);
+  }
+  if (p.out_cu && threadIdx.x == 0) p.out_cu[B] = offset;
+  for (long long q = offset + threadIdx.x; q < (long long)B * W; q += blockDim.x) {
+    if (p.out_packed) p.out_packed[q] = -1;
+    if (p.out_batch_id) p.out_batch_id[q] = -1;
+  }
+}
+
+// ---------------------------------------------------------------------------
 // kernel F: per-request finalisation (one CTA per request, after kernel A)
 // ---------------------------------------------------------------------------
 
@@ -229,7 +282,8 @@ __device__ __forceinline__ bool row_needed(const VerifyParams& p, int r, int Kb)
 
 // Summary of one row from its chunk records (one warp).
 template <int MODE, typename T>
-__device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb) {
+__device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb, int x,
+                                float2* copy) {
   RowSum rs{qnan(), 0.f, 0.f, -1};
   const long long rowid = (long long)b * p.R + r;
   const float2* rec = p.rec + rowid * p.NC;
@@ -239,17 +293,9 @@ __device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb) {
     rs.idx = __float_as_int(a.y);
     return rs;
   }
-  const bool is_draft = r > p.K;
-  const int i = is_draft ? r - p.K - 1 : r;
-  const int x = i < Kb ? __ldg(p.draft_tokens + (long long)b * p.K + i) : -1;
   const bool has_x = x >= 0 && x < p.V;
-  float lx = 0.f;
-  if (has_x) {
-    const T* row = is_draft ? row_ptr<T>(p.draft, (long long)b * p.K + i, p.V)
-                            : row_ptr<T>(p.target, (long long)b * (p.K + 1) + i, p.V);
-    lx = load_logit(row, x);
-  }
-  const float2 ms = combine_softmax_records(rec, p.NC, p.cc);
+  const float lx = __ldcg(p.lx + rowid);  // recorded by kernel A (meaningful if has_x)
+  const float2 ms = combine_softmax_records(rec, p.NC, p.cc, copy);
   rs.m = ms.x;
   rs.s = ms.y;
   if (has_x && is_finite(ms.x)) rs.wx = ex2(fmaf(lx, p.cc, -ms.x * p.cc));
@@ -259,26 +305,73 @@ __device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb) {
 constexpr int kFinThreads = 256;
 constexpr int kMaxRows = 2 * kMaxK + 1;
 
+template <int MODE, typename T, int VEC>
+__device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
+                                              const RowSum* srow, const float2* srec, int x,
+                                              float u, float uK);
+
+// Draft token of row r of request b, or -1 (rows without one, or K_b invalid).
+__device__ __forceinline__ int row_token(const VerifyParams& p, int b, int r, int Kb) {
+  if (!row_needed(p, r, Kb)) return -1;
+  const int i = r > p.K ? r - p.K - 1 : r;
+  return i < Kb ? __ldg(p.draft_tokens + (long long)b * p.K + i) : -1;
+}
+
 // The acceptance tests of all positions at once (one lane per position),
 // then the residual / bonus draw (rejection sampling, [SD] §2.1) or the
-// argmax (greedy).  Rows are summarised by the CTA's warps first.
+// argmax (greedy).  Rows are summarised by the CTA's warps first; their chunk
+// records are kept in shared memory (dynamic, when they fit) for the draw.
 template <int MODE, typename T, int VEC>
 __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParams p) {
+  extern __shared__ float2 s_rec[];
   __shared__ RowSum srow[kMaxRows];
-  pdl_wait();
-  pdl_launch_dependents();
+  __shared__ int s_last[32];
   const int b = blockIdx.x;
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const int K = p.K;
-  int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
+  // The request's inputs do not depend on kernel A: read them before waiting.
+  const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
+  const int Kv = (Kb >= 0 && Kb <= K) ? Kb : 0;
+  const int x0 = warp < p.R ? row_token(p, b, warp, Kb) : -1;
+  int x = -1;
+  float u = 0.f, uK = 0.f;
+  if (warp == 0) {
+    if (lane < Kv) x = __ldg(p.draft_tokens + (long long)b * K + lane);
+    if (MODE != kGreedy) {
+      if (lane < Kv) u = __ldg(p.uniforms + (long long)b * (K + 1) + lane);
+      uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
+    }
+  }
+  pdl_wait();
+  pdl_launch_dependents();
   for (int r = warp; r < p.R; r += kFinThreads / kWarp) {
     RowSum rs{qnan(), 0.f, 0.f, -1};
-    if (row_needed(p, r, Kb)) rs = summarise_row<MODE, T>(p, b, r, Kb);
+    if (row_needed(p, r, Kb))
+      rs = summarise_row<MODE, T>(p, b, r, Kb, r == warp ? x0 : row_token(p, b, r, Kb),
+                                  p.fin_cache ? s_rec + (long long)r * p.NC : nullptr);
     if (lane == 0) srow[r] = rs;
   }
   __syncthreads();
-  if (warp != 0) return;
+  if (warp == 0) finalize_request<MODE, T, VEC>(p, b, Kb, srow, p.fin_cache ? s_rec : nullptr, x, u, uK);
+  // The last CTA of the call clears its counters and, unless the dense
+  // residual kernel still owes outputs, writes the packed output.
+  __syncthreads();
+  if (threadIdx.x == 0) s_last[0] = atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B;
+  __syncthreads();
+  if (!s_last[0]) return;
+  if (threadIdx.x == 0) {
+    *p.err = 0;
+    *p.fin_ticket = 0;
+  }
+  if (MODE != kDense && p.compact_in_finalize) compact_all(p, s_last);
+}
 
+template <int MODE, typename T, int VEC>
+__device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
+                                              const RowSum* srow, const float2* srec, int x,
+                                              float u, float uK) {
+  const int lane = lane_id();
+  const int K = p.K;
   // A bounded wait that gave up in kernel A (a device fault) invalidates the
   // whole call: its chunk records may be missing.
   int status = __ldcg(p.err) ? kTimeout : 0;
@@ -286,8 +379,6 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParam
     status |= kBadDraftLen;
     Kb = 0;
   }
-  int x = -1;
-  if (lane < Kb) x = __ldg(p.draft_tokens + (long long)b * K + lane);
   if (!status && __any_sync(0xffffffffu, lane < Kb && (x < 0 || x >= p.V))) status = kBadToken;
   int n = 0, token = -1;
   float theta = -1.f;
@@ -304,7 +395,6 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParam
         acc = (x == rt.idx);
         theta = acc ? 1.f : 0.f;
       } else {
-        const float u = __ldg(p.uniforms + (long long)b * (K + 1) + lane);
         if (MODE == kOneHot) {  // q = point mass at x: accept iff u < p(x)
           const float px = rt.wx / (rt.s + rt.wx);
           theta = fminf(1.f, px);
@@ -342,23 +432,20 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParam
           p.state[b] = st;
         }
       } else {
-        const float uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
         const bool residual = MODE == kOneHot && n < Kb;
         if (residual && !(s_n > 0.f)) {
           token = x_n;  // no mass left beside x_n: p_n itself is the point mass at x_n
         } else {
           const T* row = row_ptr<T>(p.target, (long long)b * (K + 1) + n, p.V);
-          token = draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + n) * p.NC, p.NC,
-                                            p.V, m_n, p.cc, uK, residual ? x_n : -1);
+          token = srec ? draw_from_records<T, VEC, true>(row, srec + (long long)n * p.NC, p.NC,
+                                                         p.V, m_n, p.cc, uK, residual ? x_n : -1)
+                       : draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + n) * p.NC,
+                                                   p.NC, p.V, m_n, p.cc, uK,
+                                                   residual ? x_n : -1);
           if (token < 0) status = kBadLogits;
         }
       }
     }
-  }
-  // the last request finalised in this call clears the call's error flag
-  if (lane == 0 && atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
-    *p.err = 0;
-    *p.fin_ticket = 0;
   }
   if (p.out_accept_prob && lane < K && (MODE != kGreedy || p.greedy_prob))
     p.out_accept_prob[(long long)b * K + lane] =
@@ -380,7 +467,7 @@ __device__ __forceinline__ float2 chunk_record(typename Lane<T, VEC>::Raw (&raw)
 
 // The row of a stream item and what the chunk reductions need to know.
 struct Item {
-  int rowid, c0, nch, mask;  // mask: one-hot draft token of a target row, else -1
+  int rowid, c0, nch, x;  // x: the row's draft token (sampling modes), else -1
   bool need;
 };
 
@@ -396,10 +483,27 @@ __device__ __forceinline__ Item decode_item(const VerifyParams& p, uint32_t it) 
   k.c0 = part * p.item_chunks;
   k.nch = min(p.item_chunks, p.NC - k.c0);
   k.need = row_needed(p, r, Kb);
-  k.mask = (MODE == kOneHot && r <= p.K && r < Kb && k.need)
-               ? __ldg(p.draft_tokens + (long long)b * p.K + r)
-               : -1;
+  const int i = r > p.K ? r - p.K - 1 : r;
+  k.x = (MODE != kGreedy && k.need && i < Kb) ? __ldg(p.draft_tokens + (long long)b * p.K + i)
+                                              : -1;
   return k;
+}
+
+// If the row's draft token x lies in chunk c, the lane holding it records
+// the logit l_x for the finalize kernel (p(x) = 2^((l_x - m) c) / S).
+template <typename T, int VEC>
+__device__ __forceinline__ void record_draft_logit(
+    const VerifyParams& p, const typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV], int c,
+    int rowid, int x) {
+  using L = Lane<T, VEC>;
+  const int off = x - c * kChunk;
+  if (off < 0 || off >= kChunk) return;
+  const int lane = lane_id();
+#pragma unroll
+  for (int k = 0; k < L::NV; ++k) {
+    const int base = tile_offset<VEC>(k, 0, lane);
+    if (off >= base && off < base + VEC) p.lx[rowid] = L::get(raw[k], off - base);
+  }
 }
 
 template <typename T>
@@ -432,7 +536,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
 #pragma unroll
     for (int g = 0; g < G; ++g)
       if (g < k.nch) {
-        const float2 out = chunk_record<MODE, T, VEC>(raw[g], k.c0 + g, p.cc, k.mask);
+        record_draft_logit<T, VEC>(p, raw[g], k.c0 + g, k.rowid, k.x);
+        const float2 out =
+            chunk_record<MODE, T, VEC>(raw[g], k.c0 + g, p.cc, MODE == kOneHot ? k.x : -1);
         if (lane == 0) rec[k.c0 + g] = out;
       }
   }
@@ -512,7 +618,7 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
         atomicOr(p.err, 1);
         break;
       }
-      meta[s] = make_int4(item.rowid, item.c0, item.nch, item.mask);
+      meta[s] = make_int4(item.rowid, item.c0, item.nch, item.x);
       const T* src = item_row<T>(p, item.rowid) + (long long)item.c0 * kChunk;
       const uint32_t bytes =
           (uint32_t)(min(item.nch * kChunk, p.V - item.c0 * kChunk) * (int)sizeof(T));
@@ -553,7 +659,8 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
       const int c = m.y + w;
       typename L::Raw raw[L::NV];
       load_chunk_smem<T, VEC>(stage_of(s) + w * ST::kChunkBytes, p.V, c, raw);
-      const float2 out = chunk_record<MODE, T, VEC>(raw, c, p.cc, m.w);
+      record_draft_logit<T, VEC>(p, raw, c, m.x, m.w);
+      const float2 out = chunk_record<MODE, T, VEC>(raw, c, p.cc, MODE == kOneHot ? m.w : -1);
       if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
     }
     // this warp's values from the stage are consumed: hand it back
@@ -679,29 +786,6 @@ __global__ void __launch_bounds__(kThreads, 2) residual_kernel(const VerifyParam
 // kernel C: padding-free packed output
 // ---------------------------------------------------------------------------
 
-__device__ int block_sum(int v, int* smem) {
-  const int lane = lane_id(), warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) smem[warp] = v;
-  __syncthreads();
-  int t = 0;
-  for (int w = 0; w < nwarps; ++w) t += smem[w];
-  return t;
-}
-
-__device__ int block_excl_scan(int v, int* smem) {
-  const int lane = lane_id(), warp = threadIdx.x >> 5;
-  const int incl = warp_incl_scan_int(v);
-  __syncthreads();
-  if (lane == kWarp - 1) smem[warp] = incl;
-  __syncthreads();
-  int before = 0;
-  for (int w = 0; w < warp; ++w) before += smem[w];
-  return before + incl - v;
-}
-
 __global__ void compact_kernel(const VerifyParams p) {
   __shared__ int smem[32];
   pdl_wait();
@@ -746,11 +830,12 @@ int blocks_per_sm(K kernel) {
   return n;
 }
 
-cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, cudaStream_t s, void** args) {
+cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, cudaStream_t s, void** args,
+                       size_t smem = 0) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
-  cfg.dynamicSmemBytes = 0;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -796,7 +881,7 @@ cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
   if (err != cudaSuccess) return err;
   // F: acceptance tests and draws, one CTA per request
   err = launch_pdl(reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>), dim3(p.B),
-                   dim3(kFinThreads), s, args);
+                   dim3(kFinThreads), s, args, p.fin_cache ? fin_cache_bytes(p) : 0);
   if (err != cudaSuccess) return err;
   // B: dense residual draws
   if (MODE == kDense) {
@@ -810,8 +895,8 @@ cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
                      dim3(kThreads), s, args);
     if (err != cudaSuccess) return err;
   }
-  // C: padding-free packed output
-  if (compact) {
+  // C: padding-free packed output (one-hot and greedy calls build it in F)
+  if (compact && MODE == kDense) {
     const int threads = p.B >= 1024 ? 1024 : ((p.B + kWarp - 1) / kWarp) * kWarp;
     const int grid = (p.B + threads - 1) / threads;
     err = launch_pdl(reinterpret_cast<const void*>(compact_kernel), dim3(grid), dim3(threads), s,
@@ -830,6 +915,8 @@ cudaError_t launch_mode(int dtype, bool vec, const VerifyParams& p, bool compact
 }
 
 }  // namespace
+
+size_t fin_cache_bytes(const VerifyParams& p) { return sizeof(float2) * (size_t)p.R * p.NC; }
 
 int chunks_per_task(int dtype, bool vec) {
   if (vec) return kConsumers;
