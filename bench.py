@@ -93,6 +93,8 @@ def kernel_source_hash():
 def profiled_traffic(name):
     """DRAM bytes per launch recorded in profiles/<name>.md, if the profile
     was taken on the current kernel sources (else None)."""
+    if not name:
+        return None
     path = os.path.join(ROOT, "profiles", name + ".md")
     if not os.path.exists(path):
         return None
@@ -177,31 +179,48 @@ class ClockSampler:
 # the CPU oracle baseline
 # ---------------------------------------------------------------------------
 
-def oracle_sample_run(wl, requests, threads):
+def oracle_run(wl, mode, requests, threads):
+    """Seconds the fp64 oracle takes on the first `requests` requests."""
     import oracle
     sub = slice(0, requests)
     t0 = time.perf_counter()
-    oracle.sample(wl.target[sub], None if wl.draft is None else wl.draft[sub],
-                  wl.draft_tokens[sub], wl.uniforms[sub], wl.T, threads=threads)
+    if mode == "tree":
+        oracle.tree(wl.target[sub], wl.parent, wl.node_tokens[sub], wl.max_depth, threads=threads)
+    elif mode == "greedy":
+        oracle.greedy(wl.target[sub], wl.draft_tokens[sub], threads=threads)
+    else:
+        oracle.sample(wl.target[sub], None if wl.draft is None else wl.draft[sub],
+                      wl.draft_tokens[sub], wl.uniforms[sub], wl.T, threads=threads)
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, budget_s=12.0):
+def cpu_baseline(wl, mode, budget_s=12.0):
     threads = os.cpu_count() or 1
     probe = min(wl.B, max(threads, 8))
-    dt = oracle_sample_run(wl, probe, threads)
-    per_req = dt / probe
-    reps = max(1, min(50, int(budget_s / max(per_req * wl.B, 1e-9))))
+    per_req = oracle_run(wl, mode, probe, threads) / probe
     reqs = min(wl.B, max(probe, int(budget_s / max(per_req, 1e-9))))
-    total = 0.0
-    done = 0
-    for _ in range(reps if reqs == wl.B else 1):
-        total += oracle_sample_run(wl, reqs, threads)
+    reps = max(1, min(400, int(budget_s / max(per_req * reqs, 1e-9)))) if reqs == wl.B else 1
+    total, done = 0.0, 0
+    for _ in range(reps):
+        total += oracle_run(wl, mode, reqs, threads)
         done += reqs
-    calls_per_s = (done / wl.B) / total
-    return {"value": calls_per_s, "unit": "calls/s", "cores": threads, "kind": "oracle",
+    return {"value": (done / wl.B) / total, "unit": "calls/s", "cores": threads, "kind": "oracle",
             "sample": "%d requests of the B=%d batch (%.1f s of fp64 CPU work, %d threads)"
                       % (done, wl.B, total, threads)}
+
+
+def load_workload(args, seed=0):
+    from token_verification_gb300 import synth
+    wl = synth.make_workload(args.workload, seed=seed)
+    mode = "tree" if wl.parent is not None else ("greedy" if args.greedy else "sample")
+    if args.batch:  # a smaller batch of the same workload (profiling captures)
+        wl.B = args.batch
+        for name in ("target", "draft", "draft_tokens", "uniforms", "node_tokens"):
+            v = getattr(wl, name)
+            if v is not None:
+                setattr(wl, name, v[:args.batch])
+        wl.meta["workload"] += "-first%d" % args.batch
+    return wl, mode
 
 
 # ---------------------------------------------------------------------------
@@ -212,21 +231,20 @@ def run_reference(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    from token_verification_gb300 import synth
-    wl = synth.make_workload(args.workload)
+    wl, mode = load_workload(args)
     threads = os.cpu_count() or 1
-    req = args.ref_requests
+    req = min(args.ref_requests, wl.B)
     for _ in range(args.warmup):
-        oracle_sample_run(wl, req, threads)
+        oracle_run(wl, mode, req, threads)
     t = 0.0
     for _ in range(args.steps):
-        t += oracle_sample_run(wl, req, threads)
+        t += oracle_run(wl, mode, req, threads)
     value = (args.steps * req / wl.B) / t
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "calls/s",
-            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+    line = {"impl": "reference", "metric": metric_name(wl, mode, args), "value": value,
+            "unit": "calls/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": workload_config(wl, args),
+            "config": workload_config(wl, mode),
             "cpu_baseline": {"value": value, "unit": "calls/s", "cores": threads, "kind": "oracle",
                              "sample": "%d of %d requests per step" % (req, wl.B)},
             "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0,
@@ -235,12 +253,100 @@ def run_reference(args):
     return 0
 
 
-def workload_config(wl, args):
-    return {"workload": wl.meta["workload"], "B": wl.B, "K": wl.K, "V": wl.V,
-            "logits": wl.dtype, "drafts": wl.meta.get("drafts"), "temperature": wl.T,
-            "l2": "inputs larger than L2: %d MB of logits per call, 2 rotating input sets"
-                  % (wl.target.nbytes // 2**20),
-            "parallelism": "dp%d" % dist_env()[0]}
+def metric_name(wl, mode, args):
+    if args.workload == 2 and mode == "sample" and not args.batch:
+        return METRIC
+    return "verify calls/s and logits HBM GB/s (%% of GB300 peak) on %s (%s)" % (
+        wl.meta["workload"], mode)
+
+
+def workload_config(wl, mode):
+    cfg = {"workload": wl.meta["workload"], "mode": mode, "B": wl.B, "V": wl.V,
+           "logits": wl.dtype, "parallelism": "dp%d" % dist_env()[0]}
+    if mode == "tree":
+        cfg.update(N=int(wl.parent.size), max_depth=wl.max_depth)
+    else:
+        cfg.update(K=wl.K, drafts=wl.meta.get("drafts"), temperature=0.0 if mode == "greedy" else wl.T)
+    total = wl.target.nbytes + (wl.draft.nbytes if (wl.draft is not None and mode == "sample") else 0)
+    cfg["l2"] = ("inputs larger than L2: %d MB of logits per call, 2 rotating input sets"
+                 % (total // 2**20) if total > 129 * 2**20 else
+                 "inputs smaller than L2 (%d KB per call): 2 rotating input sets; the figure "
+                 "includes L2 reuse" % (total // 1024))
+    return cfg
+
+
+class Case:
+    """One workload resident on the device (two rotating input sets, the
+    second with its requests rotated by B/2) and the C-ABI call on it."""
+
+    def __init__(self, wl, mode, device):
+        import torch
+        from token_verification_gb300 import api
+        self.api, self.torch = api, torch
+        self.wl, self.mode, self.device = wl, mode, device
+        to_t = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)) \
+            if wl.dtype == "bf16" else (lambda a: torch.from_numpy(a))
+        self.host = {"target": to_t(wl.target)}
+        if mode == "tree":
+            self.host["node_tokens"] = torch.from_numpy(wl.node_tokens)
+        else:
+            self.host["tokens"] = torch.from_numpy(wl.draft_tokens)
+            if mode == "sample":
+                self.host["uniforms"] = torch.from_numpy(wl.uniforms)
+                if wl.draft is not None:
+                    self.host["draft"] = to_t(wl.draft)
+        B = wl.B
+        self.sets = []
+        for s in range(2):
+            perm = torch.from_numpy(np.roll(np.arange(B), s * (B // 2)))
+            self.sets.append({k: v[perm].contiguous().to(device) for k, v in self.host.items()})
+
+    def alloc(self, packed=True):
+        if self.mode == "tree":
+            return None
+        return self.api.alloc_outputs(self.wl.B, self.wl.K, self.device, packed=packed,
+                                      accept_prob=packed and self.mode == "sample",
+                                      status=packed)
+
+    def call(self, inputs, out):
+        wl, api = self.wl, self.api
+        if self.mode == "tree":
+            return api.spec_verify_tree(inputs["target"], wl.parent, inputs["node_tokens"],
+                                        wl.max_depth, out, path=False, status=False)
+        if self.mode == "greedy":
+            return api.spec_verify_greedy(inputs["target"], inputs["tokens"], out)
+        return api.spec_verify_sample(inputs["target"], inputs.get("draft"), inputs["tokens"],
+                                      inputs["uniforms"], wl.T, out)
+
+    def step(self, i, out):
+        return self.call(self.sets[i & 1], out)
+
+    def launches(self, packed):
+        if self.mode == "tree":
+            return 1
+        if self.mode == "sample" and self.wl.draft is not None:
+            return 3 + (1 if packed else 0)  # stream, finalize, residual, compaction
+        return 2  # stream, finalize (which also writes the packed output)
+
+    def kernel_label(self):
+        if self.mode == "tree":
+            return "tree_kernel"
+        if self.mode == "sample" and self.wl.draft is not None:
+            return "verify_stream_kernel + finalize_kernel + residual_kernel (dense)"
+        return "verify_stream_kernel + finalize_kernel (%s)" % (
+            "greedy" if self.mode == "greedy" else "one-hot")
+
+    def algorithmic_bytes(self, out):
+        """Logit bytes the method needs per call: every row once (sampling,
+        greedy); the rows on the accepted path (tree)."""
+        wl = self.wl
+        esz = 2 if wl.dtype == "bf16" else 4
+        if self.mode == "tree":
+            rows = int(out.accept_len.sum().item())
+            return rows * wl.V * esz
+        rows = wl.B * (wl.K + 1) + (wl.B * wl.K if (self.mode == "sample" and wl.draft is not None)
+                                     else 0)
+        return rows * wl.V * esz
 
 
 def run_ours(args):
@@ -251,37 +357,19 @@ def run_ours(args):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
-    from token_verification_gb300 import api, synth
     from token_verification_gb300 import _native
     _native.lib()
 
-    wl = synth.make_workload(args.workload, seed=shard_seed(0, rank))
-    assert wl.draft is None, "the benchmarked workload has one-hot drafts"
-    if args.batch:  # a smaller batch of the same workload (profiling captures)
-        wl.B = args.batch
-        wl.target, wl.draft_tokens, wl.uniforms = (wl.target[:args.batch],
-                                                   wl.draft_tokens[:args.batch],
-                                                   wl.uniforms[:args.batch])
-        wl.meta["workload"] += "-first%d" % args.batch
-    B, K, V = wl.B, wl.K, wl.V
-    tgt_host = torch.from_numpy(wl.target.view(np.int16)).view(torch.bfloat16)
-    sets = []
-    for s in range(2):  # two resident input sets, used alternately
-        perm = np.roll(np.arange(B), s * (B // 2))
-        sets.append(dict(
-            target=tgt_host[perm].contiguous().to(device),
-            tokens=torch.from_numpy(wl.draft_tokens[perm]).to(device),
-            uniforms=torch.from_numpy(wl.uniforms[perm]).to(device)))
-    out = api.alloc_outputs(B, K, device)
-    out_kernel = api.alloc_outputs(B, K, device, packed=False, accept_prob=False, status=False)
+    wl, mode = load_workload(args, seed=shard_seed(0, rank))
+    case = Case(wl, mode, device)
+    out = case.alloc(packed=True)
+    out_kernel = case.alloc(packed=False)
     stream = torch.cuda.current_stream(device)
 
-    def step(i, o=out):
-        s = sets[i & 1]
-        api.spec_verify_sample(s["target"], None, s["tokens"], s["uniforms"], wl.T, o)
-
     for i in range(args.warmup):
-        step(i)
+        out = case.step(i, out) or out
+    if out_kernel is None:  # the tree call has no packed output: same outputs
+        out_kernel = out
     torch.cuda.synchronize()
 
     sampler = ClockSampler(local) if rank == 0 else None
@@ -295,7 +383,7 @@ def run_ours(args):
     w0 = time.time()
     ev0.record(stream)
     for i in range(args.steps):
-        step(i)
+        case.step(i, out)
     ev1.record(stream)
     torch.cuda.synchronize()
     w1 = time.time()
@@ -306,18 +394,17 @@ def run_ours(args):
         sampler.mark(w0, w1)
     max_elapsed, total_calls = aggregate(elapsed, args.steps, world, device)
     mean_len = float(out.accept_len.float().mean().item())
+    algo_bytes = case.algorithmic_bytes(out)
 
-    # the dominant kernel: the call without packed output launches the
-    # streaming row-statistics kernel and the per-request finalize kernel
-    # (about 10% of the pair, see profiles/); per-call event pairs on the
-    # launching stream, so the fraction below is a lower bound for the
-    # streaming kernel alone
+    # the dominant kernels, timed per call without the packed output, with
+    # event pairs on the launching stream (see profiles/ for each kernel's
+    # share of the call)
     kernel_iters = max(20, min(args.steps, 2000))
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(kernel_iters)]
     for i in range(kernel_iters):
         evs[i][0].record(stream)
-        step(i, out_kernel)
+        out_kernel = case.step(i, out_kernel) or out_kernel
         evs[i][1].record(stream)
     torch.cuda.synchronize()
     kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
@@ -328,19 +415,16 @@ def run_ours(args):
     # step's inputs, the call, D2H of its results, every step
     e2e = None
     if rank == 0 and not args.no_e2e:
-        pin = dict(target=tgt_host.pin_memory(),
-                   tokens=torch.from_numpy(wl.draft_tokens).pin_memory(),
-                   uniforms=torch.from_numpy(wl.uniforms).pin_memory())
-        res_tok = torch.empty((B, K + 1), dtype=torch.int32).pin_memory()
-        res_len = torch.empty((B,), dtype=torch.int32).pin_memory()
+        pin = {k: v.pin_memory() for k, v in case.host.items()}
         dev_in = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
+        res_tok = torch.empty(tuple(out.tokens.shape), dtype=torch.int32).pin_memory()
+        res_len = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
 
         def e2e_step():
             for k in pin:
                 dev_in[k].copy_(pin[k], non_blocking=True)
-            api.spec_verify_sample(dev_in["target"], None, dev_in["tokens"], dev_in["uniforms"],
-                                   wl.T, out)
+            case.call(dev_in, out)
             res_tok.copy_(out.tokens, non_blocking=True)
             res_len.copy_(out.accept_len, non_blocking=True)
 
@@ -360,36 +444,38 @@ def run_ours(args):
                "d2h_bytes_per_step": d2h, "steps": e2e_steps}
 
     if rank == 0:
-        logit_bytes = B * (K + 1) * V * 2
         peak, peak_kind = hbm_peak()
-        achieved = logit_bytes / (kern_ms / 1e3) / 1e9
+        achieved = algo_bytes / (kern_ms / 1e3) / 1e9
         value = total_calls / max_elapsed
         line = {
-            "metric": METRIC, "value": value, "unit": "calls/s", "n_gpus": world,
+            "metric": metric_name(wl, mode, args), "value": value, "unit": "calls/s",
+            "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": workload_config(wl, args),
-            "draft_tokens_per_s": value * B * K,
-            "hbm_gbs": logit_bytes * value / 1e9,
+            "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+            "config": workload_config(wl, mode),
+            "draft_tokens_per_s": None if mode == "tree" else value * wl.B * wl.K,
+            "hbm_gbs": algo_bytes * value / 1e9,
             "mean_accept_len": mean_len,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "kernel": "verify_stream_kernel + finalize_kernel (one-hot, bf16)",
-                         "kernel_ms": kern_ms, "algorithmic_bytes": logit_bytes,
-                         "traffic": profiled_traffic("verify_stream_onehot_B256_K5_V152064")},
-            # per call: the streaming kernel and the finalize kernel (which
-            # also writes the packed output)
-            "gpu_launches": args.steps * 2,
+                         "kernel": case.kernel_label(), "kernel_ms": kern_ms,
+                         "algorithmic_bytes": algo_bytes,
+                         "traffic": profiled_traffic(PROFILE_NAMES.get((args.workload, mode)))},
+            "gpu_launches": args.steps * case.launches(True),
             "clocks": sampler.summary() if sampler else None,
             "e2e": e2e,
         }
         if not args.no_cpu_baseline and world == 1:
-            line["cpu_baseline"] = cpu_baseline(wl)
+            line["cpu_baseline"] = cpu_baseline(wl, mode)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+# ncu summaries under profiles/ that record DRAM traffic per launch
+PROFILE_NAMES = {(2, "sample"): "verify_stream_onehot_B256_K5_V152064"}
 
 
 def main(argv=None):
@@ -405,6 +491,8 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first BATCH requests (small profiling cases)")
+    ap.add_argument("--greedy", action="store_true",
+                    help="greedy verification (temperature 0) of the workload's drafts")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         args.warmup = 3
