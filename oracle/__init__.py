@@ -70,14 +70,17 @@ def configure(lib):
     lib.sv_oracle_argmax.restype = I
     lib.sv_oracle_inverse_cdf.argtypes = [P, I, D, P]
     lib.sv_oracle_inverse_cdf.restype = I
-    lib.sv_oracle_greedy.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P]
+    lib.sv_oracle_greedy.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
     lib.sv_oracle_greedy.restype = I
-    lib.sv_oracle_sample.argtypes = [P, P, I, P, P, P, D, I, I, I, I, I, P, P, P, P, P, P, P, P]
+    lib.sv_oracle_sample.argtypes = [P, P, I, P, P, P, D, I, I, I, I, I, P, P, P, P, P, P, P, P,
+                                     P]
     lib.sv_oracle_sample.restype = I
     lib.sv_oracle_tree.argtypes = [P, I, P, P, I, I, I, I, I, I, P, P, P, P]
     lib.sv_oracle_tree.restype = I
     lib.sv_oracle_compact.argtypes = [P, P, I, I, P, P, P]
     lib.sv_oracle_compact.restype = None
+    lib.sv_oracle_ngram.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
+    lib.sv_oracle_ngram.restype = I
     return lib
 
 
@@ -92,6 +95,16 @@ def _logits(a):
     if a.dtype == np.uint16:
         return a, 1
     raise TypeError("oracle logits must be float32 or uint16 (bfloat16 bits), got %s" % a.dtype)
+
+
+def _mask(token_mask, B, K1, V):
+    """Grammar masks as contiguous uint32 [B, K+1, ceil(V/32)] (or None)."""
+    if token_mask is None:
+        return None
+    m = np.ascontiguousarray(token_mask)
+    if m.dtype not in (np.int32, np.uint32) or m.shape != (B, K1, (V + 31) // 32):
+        raise ValueError("token_mask must be int32/uint32 [B, K+1, ceil(V/32)]")
+    return m.view(np.uint32)
 
 
 def _ranges(B, threads):
@@ -142,12 +155,14 @@ def inverse_cdf(weights, u):
 # ---------------------------------------------------------------------------
 
 def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=None,
-           threads=1, b_range=None, probe_tokens=None):
+           threads=1, b_range=None, probe_tokens=None, token_mask=None):
     """Rejection-sampling verify (temperature 0 = greedy rule).
 
     target [B, K+1, V], draft [B, K, V] or None (one-hot drafts),
     draft_tokens [B, K] int32, uniforms [B, K+1] (float32 or float64),
     draft_lens [B] or None.  Requests outside ``b_range`` keep -1 / 0.
+    token_mask [B, K+1, ceil(V/32)] int32 / uint32 or None: grammar masks
+    (bit j % 32 of word j // 32 set = token j allowed at that position).
     Returns a dict of numpy arrays: tokens, accept_len, accept_prob, flags,
     margins, status (and probe [B, 2] when probe_tokens [B] is given: the
     normalised CDF step of that token in the request's final draw).
@@ -162,6 +177,7 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
     toks = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, K)
     u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, K + 1)
     lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, dtype=np.int32)
+    mask = _mask(token_mask, B, K + 1, V)
     out = dict(tokens=np.full((B, K + 1), -1, np.int32), accept_len=np.zeros(B, np.int32),
                accept_prob=np.full((B, K), -1.0), flags=np.zeros((B, K + 1), np.int32),
                margins=np.full((B, K + 1), np.inf), status=np.zeros(B, np.int32))
@@ -176,17 +192,19 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
             _ptr(target), _ptr(draft), dt, _ptr(toks), _ptr(lens), _ptr(u),
             float(temperature), B, K, V, lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
             _ptr(out["accept_prob"]), _ptr(out["flags"]), _ptr(out["margins"]),
-            _ptr(out["status"]), _ptr(probes), _ptr(out.get("probe")))
+            _ptr(out["status"]), _ptr(probes), _ptr(out.get("probe")), _ptr(mask))
 
     _run(fn, B, threads, b_range)
     return out
 
 
-def greedy(target, draft_tokens, *, draft_lens=None, threads=1, b_range=None):
-    """Greedy verify: tokens [B, K+1], accept_len [B], status [B]."""
+def greedy(target, draft_tokens, *, draft_lens=None, threads=1, b_range=None, token_mask=None):
+    """Greedy verify: tokens [B, K+1], accept_len [B], status [B]
+    (token_mask as for ``sample``)."""
     target, dt = _logits(target)
     B, K1, V = target.shape
     K = K1 - 1
+    mask = _mask(token_mask, B, K1, V)
     toks = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, K)
     lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, dtype=np.int32)
     out = dict(tokens=np.full((B, K + 1), -1, np.int32), accept_len=np.zeros(B, np.int32),
@@ -196,7 +214,7 @@ def greedy(target, draft_tokens, *, draft_lens=None, threads=1, b_range=None):
     def fn(lo, hi):
         return lib.sv_oracle_greedy(_ptr(target), dt, _ptr(toks), _ptr(lens), B, K, V, lo, hi,
                                     _ptr(out["tokens"]), _ptr(out["accept_len"]),
-                                    _ptr(out["status"]))
+                                    _ptr(out["status"]), _ptr(mask))
 
     _run(fn, B, threads, b_range)
     return out
@@ -234,3 +252,21 @@ def compact(tokens, accept_len):
     _load().sv_oracle_compact(_ptr(t), _ptr(a), B, W, _ptr(cu), _ptr(packed), _ptr(bid))
     return cu, packed, bid
 
+
+
+def ngram(tokens, lens, n_min, n_max, K):
+    """Prompt-lookup proposer: drafts [B, K] (-1 padded), draft_lens [B],
+    match [B] (start of the matched n-gram or -1), ngram [B] (its n or 0),
+    status [B] (BAD_DRAFT_LEN for a context length outside [0, L])."""
+    t = np.ascontiguousarray(tokens, dtype=np.int32)
+    B, L = t.shape
+    ln = np.ascontiguousarray(lens, dtype=np.int32).reshape(B)
+    out = dict(drafts=np.full((B, K), -1, np.int32), draft_lens=np.zeros(B, np.int32),
+               match=np.full(B, -1, np.int32), ngram=np.zeros(B, np.int32),
+               status=np.zeros(B, np.int32))
+    rc = _load().sv_oracle_ngram(_ptr(t), _ptr(ln), B, L, int(n_min), int(n_max), int(K),
+                                 _ptr(out["drafts"]), _ptr(out["draft_lens"]), _ptr(out["match"]),
+                                 _ptr(out["ngram"]), _ptr(out["status"]))
+    if rc != 0:
+        raise ValueError("oracle rejected its arguments (code %d)" % rc)
+    return out

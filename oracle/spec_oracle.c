@@ -16,10 +16,13 @@
  *          strict "r < min(1, p/q)" test, clamp-then-normalise residual).
  *   [FD]   "投机解码" (FastDeploy docs), "高效投机解码框架设计"
  *          (per-sample parallel verify; padding-free batch-id lookup).
+ *   [LD]   "Speculative Decoding" (LMDeploy docs), "投机解码与结构化输出",
+ *          "工作原理" (grammar masks applied to the target logits of every
+ *          verified position, and to the draft's).
  *
  * Every quantity is computed in double precision, one request at a time,
  * with plain serial loops: no blocking, fusion or reordering.  Where the
- * pages leave a step open, the reading taken is named R1..R12 in the
+ * pages leave a step open, the reading taken is named R1..R18 in the
  * comments (the same labels are used in the design notes).
  *
  * Logit storage: dtype 0 = IEEE fp32, dtype 1 = bfloat16 given as raw
@@ -74,6 +77,25 @@ static int row_is_valid(const double* l, int V) {
     if (isfinite(l[j])) any_finite = 1;
   }
   return any_finite;
+}
+
+/* Grammar mask [LD "工作原理"]: the mask of position i is applied to the
+ * logits of position i before anything else is computed from them.  R18:
+ * one row of ceil(V/32) 32-bit words per position; token j is allowed when
+ * bit (j mod 32) of word floor(j/32) is set.  A disallowed token's logit
+ * becomes -inf, so it has probability 0 and never wins an argmax; a row
+ * left with no finite logit is unusable (R12).  mask_row NULL: no mask. */
+static void apply_token_mask(double* l, int V, const uint32_t* mask_row) {
+  if (!mask_row) return;
+  for (int j = 0; j < V; ++j)
+    if (!((mask_row[j / 32] >> (j % 32)) & 1u)) l[j] = -INFINITY;
+}
+
+/* The mask row of position i of request b (R18: draft row i shares it). */
+static const uint32_t* mask_row_of(const uint32_t* mask, int K, int V, size_t b, int i) {
+  if (!mask) return NULL;
+  const size_t words = ((size_t)V + 31) / 32;
+  return mask + (b * (size_t)(K + 1) + (size_t)i) * words;
 }
 
 /* ------------------------------------------------------------------ */
@@ -164,8 +186,8 @@ static void clear_request(int32_t* tokens, int width, int32_t* accept_len) {
  * drafts match, the argmax of the last row is the bonus token.  The argmax
  * is taken on the raw logits, so the temperature plays no part. */
 static int greedy_request(const void* target, int dtype, const int32_t* draft_tokens,
-                          int K, int K_b, int V, size_t b, double* row, int32_t* tokens,
-                          int32_t* accept_len, double* accept_prob) {
+                          const uint32_t* mask, int K, int K_b, int V, size_t b, double* row,
+                          int32_t* tokens, int32_t* accept_len, double* accept_prob) {
   for (int i = 0; i < K_b; ++i) {
     int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
     if (x < 0 || x >= V) return OR_BAD_TOKEN;
@@ -174,6 +196,7 @@ static int greedy_request(const void* target, int dtype, const int32_t* draft_to
   int emitted = -1;
   for (int i = 0; i <= K_b; ++i) {
     load_row(target, dtype, b * (size_t)(K + 1) + (size_t)i, V, row);
+    apply_token_mask(row, V, mask_row_of(mask, K, V, b, i));
     if (!row_is_valid(row, V)) return OR_BAD_LOGITS;
     int a = sv_oracle_argmax(row, V);
     if (i == K_b) {
@@ -196,7 +219,8 @@ static int greedy_request(const void* target, int dtype, const int32_t* draft_to
 
 int sv_oracle_greedy(const void* target, int dtype, const int32_t* draft_tokens,
                      const int32_t* draft_lens, int B, int K, int V, int b_begin, int b_end,
-                     int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_status) {
+                     int32_t* out_tokens, int32_t* out_accept_len, int32_t* out_status,
+                     const uint32_t* token_mask) {
   if (B < 0 || K < 0 || V < 1 || b_begin < 0 || b_end > B) return -1;
   double* row = (double*)malloc(sizeof(double) * (size_t)V);
   if (!row) return -2;
@@ -208,8 +232,8 @@ int sv_oracle_greedy(const void* target, int dtype, const int32_t* draft_tokens,
     if (K_b < 0 || K_b > K)
       st = OR_BAD_DRAFT_LEN;
     else
-      st = greedy_request(target, dtype, draft_tokens, K, K_b, V, (size_t)b, row, tokens,
-                          &out_accept_len[b], NULL);
+      st = greedy_request(target, dtype, draft_tokens, token_mask, K, K_b, V, (size_t)b, row,
+                          tokens, &out_accept_len[b], NULL);
     if (st) clear_request(tokens, K + 1, &out_accept_len[b]);
     out_status[b] = st;
   }
@@ -233,7 +257,8 @@ int sv_oracle_greedy(const void* target, int dtype, const int32_t* draft_tokens,
  * through rounding, since max(0, p - q) sums to 0 only when p = q), draw
  * from p_n instead (R3).  The draw uses uniform u_K (R5). */
 static int sample_request(const void* target, const void* draft, int dtype,
-                          const int32_t* draft_tokens, const double* uniforms, double T, int K,
+                          const int32_t* draft_tokens, const uint32_t* mask,
+                          const double* uniforms, double T, int K,
                           int K_b, int V, size_t b, double* lrow, double* p, double* q,
                           double* w, int32_t* tokens, int32_t* accept_len, double* accept_prob,
                           int32_t* flags, double* margins, int32_t probe, double* probe_out) {
@@ -246,11 +271,13 @@ static int sample_request(const void* target, const void* draft, int dtype,
   for (int i = 0; i < K_b; ++i) {
     int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
     load_row(target, dtype, b * (size_t)(K + 1) + (size_t)i, V, lrow);
+    apply_token_mask(lrow, V, mask_row_of(mask, K, V, b, i));
     if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
     sv_oracle_tempered_softmax(lrow, V, T, p);
     double qx = 1.0;
     if (draft) {
       load_row(draft, dtype, b * (size_t)K + (size_t)i, V, lrow);
+      apply_token_mask(lrow, V, mask_row_of(mask, K, V, b, i));
       if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
       sv_oracle_tempered_softmax(lrow, V, T, q);
       qx = q[x];
@@ -272,6 +299,7 @@ static int sample_request(const void* target, const void* draft, int dtype,
   }
   if (n == K_b) {
     load_row(target, dtype, b * (size_t)(K + 1) + (size_t)K_b, V, lrow);
+    apply_token_mask(lrow, V, mask_row_of(mask, K, V, b, K_b));
     if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
     sv_oracle_tempered_softmax(lrow, V, T, p);
     for (int j = 0; j < V; ++j) w[j] = p[j];
@@ -319,13 +347,15 @@ static int sample_request(const void* target, const void* draft, int dtype,
  *   whose draw happened, the normalised CDF step [C_{t-1}/W, C_t/W) that
  *   token t = probe_tokens[b] occupies in that draw's distribution (NaN if
  *   t is out of range).  Used to check a draw made elsewhere.
+ *   token_mask [B, K+1, ceil(V/32)] words or NULL: grammar masks (R18).
  * Returns 0, or a negative code for arguments outside the domain. */
 int sv_oracle_sample(const void* target, const void* draft, int dtype,
                      const int32_t* draft_tokens, const int32_t* draft_lens,
                      const double* uniforms, double temperature, int B, int K, int V,
                      int b_begin, int b_end, int32_t* out_tokens, int32_t* out_accept_len,
                      double* out_accept_prob, int32_t* out_flags, double* out_margins,
-                     int32_t* out_status, const int32_t* probe_tokens, double* probe_interval) {
+                     int32_t* out_status, const int32_t* probe_tokens, double* probe_interval,
+                     const uint32_t* token_mask) {
   if (B < 0 || K < 0 || V < 1 || b_begin < 0 || b_end > B) return -1;
   if (!(temperature >= 0) || isinf(temperature)) return -3;
   double* buf = (double*)malloc(sizeof(double) * (size_t)V * 4);
@@ -346,10 +376,11 @@ int sv_oracle_sample(const void* target, const void* draft, int dtype,
     if (K_b < 0 || K_b > K)
       st = OR_BAD_DRAFT_LEN;
     else if (temperature == 0)
-      st = greedy_request(target, dtype, draft_tokens, K, K_b, V, (size_t)b, lrow, tokens,
-                          &out_accept_len[b], aprob);
+      st = greedy_request(target, dtype, draft_tokens, token_mask, K, K_b, V, (size_t)b, lrow,
+                          tokens, &out_accept_len[b], aprob);
     else
-      st = sample_request(target, draft, dtype, draft_tokens, uniforms, temperature, K, K_b,
+      st = sample_request(target, draft, dtype, draft_tokens, token_mask, uniforms, temperature,
+                          K, K_b,
                           V, (size_t)b, lrow, p, q, w, tokens, &out_accept_len[b], aprob,
                           flags, margins, probe_tokens ? probe_tokens[b] : -1,
                           probe_interval ? probe_interval + 2 * (size_t)b : NULL);
@@ -476,4 +507,68 @@ void sv_oracle_compact(const int32_t* tokens, const int32_t* accept_len, int B, 
       packed[cu[b] + k] = tokens[(size_t)b * (size_t)width + (size_t)k];
       batch_id[cu[b] + k] = b;
     }
+}
+
+/* ------------------------------------------------------------------ */
+/* n-gram (prompt-lookup) proposer                                     */
+/* ------------------------------------------------------------------ */
+
+/* The deterministic proposer whose drafts the one-hot verification checks
+ * ["投机解码" (FastDeploy docs), "使用 Ngram 解码": drafts come from matching an
+ * n-gram window against the prompt and the tokens generated so far; the vLLM
+ * Ascend guide's n-gram example and "推测解码与 MTP" §9.1: prompt lookup with
+ * prompt_lookup_max = 4 and num_speculative_tokens = 5].
+ * R19: for n = n_max down to n_min, the pattern is the last n tokens of the
+ * request's context c[0..len); the match is the EARLIEST start s with
+ * c[s..s+n) equal to the pattern and at least one token after it
+ * (s + n < len, so the pattern's own position never counts); the drafts
+ * are the up to K tokens that follow, c[s+n .. min(s+n+K, len)).  The first
+ * n (longest) that matches decides; with no match there are no drafts.
+ *   tokens [B, L] int32 (row b holds its context in the first lens[b]
+ *   entries), lens [B].
+ *   Outputs: drafts [B, K] (-1 padded), draft_lens [B] (0..K), match [B]
+ *   (the start s, or -1), ngram [B] (the n that matched, or 0), status [B]
+ *   (4 when lens[b] is outside [0, L]: no drafts).
+ * Returns 0, or -1 for arguments outside the domain. */
+int sv_oracle_ngram(const int32_t* tokens, const int32_t* lens, int B, int L, int n_min,
+                    int n_max, int K, int32_t* drafts, int32_t* draft_lens, int32_t* match,
+                    int32_t* ngram, int32_t* status) {
+  if (B < 0 || L < 0 || n_min < 1 || n_max < n_min || K < 0) return -1;
+  for (int b = 0; b < B; ++b) {
+    const int32_t* c = tokens + (size_t)b * (size_t)L;
+    int len = lens[b];
+    for (int k = 0; k < K; ++k) drafts[(size_t)b * (size_t)K + (size_t)k] = -1;
+    draft_lens[b] = 0;
+    match[b] = -1;
+    ngram[b] = 0;
+    status[b] = 0;
+    if (len < 0 || len > L) {
+      status[b] = OR_BAD_DRAFT_LEN;
+      continue;
+    }
+    for (int n = n_max; n >= n_min; --n) {
+      if (len < n + 1) continue;
+      const int32_t* pattern = c + (len - n);
+      int found = -1;
+      for (int s = 0; s + n < len && found < 0; ++s) {
+        int equal = 1;
+        for (int t = 0; t < n; ++t)
+          if (c[s + t] != pattern[t]) {
+            equal = 0;
+            break;
+          }
+        if (equal) found = s;
+      }
+      if (found >= 0) {
+        int k = len - (found + n);
+        if (k > K) k = K;
+        for (int t = 0; t < k; ++t) drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t];
+        draft_lens[b] = k;
+        match[b] = found;
+        ngram[b] = n;
+        break;
+      }
+    }
+  }
+  return 0;
 }

@@ -193,15 +193,16 @@ def _bisect(pred, iters=64):
 class _Request:
     """One request evaluated by the oracle for chosen drafts and uniforms."""
 
-    def __init__(self, target, draft, T):
+    def __init__(self, target, draft, T, mask=None):
         self.target = np.ascontiguousarray(target[None], np.float32)
         self.draft = None if draft is None else np.ascontiguousarray(draft[None], np.float32)
+        self.mask = None if mask is None else np.ascontiguousarray(mask[None], np.uint32)
         self.K = target.shape[0] - 1
         self.T = T
 
     def run(self, drafts, u):
         out = oracle.sample(self.target, self.draft, np.asarray([drafts], np.int32),
-                            np.asarray([u], np.float64), self.T)
+                            np.asarray([u], np.float64), self.T, token_mask=self.mask)
         assert out["status"][0] == 0
         return out["tokens"][0], int(out["accept_len"][0])
 
@@ -416,6 +417,198 @@ def check_errors():
 
 
 # ---------------------------------------------------------------------------
+# grammar masks
+# ---------------------------------------------------------------------------
+
+def _allowed(mask_words, V):
+    """Decode mask words with numpy's little-endian bit unpacking (an
+    independent reading of the layout: bit j % 32 of word j // 32)."""
+    w = np.ascontiguousarray(mask_words, dtype="<u4")
+    bits = np.unpackbits(w.view(np.uint8), axis=-1, bitorder="little")
+    return bits[..., :V].astype(bool)
+
+
+def _probs_table(rows, V):
+    out = np.zeros((len(rows), V))
+    for r, row in enumerate(rows):
+        for j, v in row.items():
+            out[r, int(j)] = v
+    return out
+
+
+def check_golden_masked():
+    g = _golden("verify_masked_v40.json")
+    V, K, T = g["V"], g["K"], g["T"]
+    with np.errstate(divide="ignore"):
+        target = np.log(_probs_table(g["target_probs"], V)).astype(np.float32)[None]
+        draft = np.log(_probs_table(g["draft_probs"], V)).astype(np.float32)[None]
+    mask = np.asarray(g["mask_words"], np.uint32)[None]
+    for key, dr in (("onehot_cases", None), ("dense_cases", draft)):
+        for case in g[key]:
+            out = oracle.sample(target, dr, np.asarray([case["draft_tokens"]]),
+                                np.asarray([case["uniforms"]], np.float32), T, token_mask=mask)
+            assert out["status"][0] == 0
+            assert list(out["tokens"][0]) == case["tokens"], (key, case, out["tokens"][0])
+            assert out["accept_len"][0] == case["accept_len"], (key, case)
+            np.testing.assert_allclose(out["accept_prob"][0], case["accept_prob"], atol=1e-6)
+    for case in g["greedy_cases"]:
+        out = oracle.greedy(target, np.asarray([case["draft_tokens"]]), token_mask=mask)
+        assert out["status"][0] == 0
+        assert list(out["tokens"][0]) == case["tokens"], (case, out["tokens"][0])
+        assert out["accept_len"][0] == case["accept_len"]
+
+
+def check_mask_layout(seed=15):
+    """Masks spanning three words: the masked argmax and the masked p(x)
+    agree with numpy on the bit-unpacked allowed sets, row by row."""
+    rng = np.random.default_rng(seed)
+    B, K, V, T = 200, 3, 70, 0.9
+    l = (rng.standard_normal((B, K + 1, V)) * 2).astype(np.float32)
+    mask = rng.integers(0, 2 ** 32, size=(B, K + 1, (V + 31) // 32), dtype=np.uint64)
+    mask = mask.astype(np.uint32)
+    allowed = _allowed(mask, V)
+    mask[~allowed.any(-1)] |= np.uint32(1)  # keep every row usable
+    allowed = _allowed(mask, V)
+    ml = np.where(allowed, l.astype(np.float64), -np.inf)
+    am = np.argmax(ml, axis=2)
+    drafts = np.where(rng.random((B, K)) < 0.6, am[:, :K], rng.integers(0, V, (B, K)))
+    drafts = drafts.astype(np.int32)
+    g = oracle.greedy(l, drafts, token_mask=mask)
+    assert (g["status"] == 0).all()
+    for b in range(B):
+        n = int(g["accept_len"][b]) - 1
+        assert (drafts[b, :n] == am[b, :n]).all() and (n == K or drafts[b, n] != am[b, n])
+        assert g["tokens"][b, n] == am[b, n]
+    # one-hot sampling with every u = 0: all allowed drafts are accepted and
+    # accept_prob is the masked p(x); a disallowed draft has p(x) = 0
+    p = scipy.special.softmax(ml / T, axis=-1)
+    u = np.zeros((B, K + 1), np.float32)
+    s = oracle.sample(l, None, drafts, u, T, token_mask=mask)
+    for b in range(B):
+        n = int(s["accept_len"][b]) - 1
+        px = p[b, np.arange(K), drafts[b]]
+        np.testing.assert_allclose(s["accept_prob"][b, :n + (n < K)], np.minimum(1, px)[:n + (n < K)],
+                                   rtol=1e-12, atol=0)
+        ok = np.nonzero(px == 0)[0]
+        assert n == (ok[0] if ok.size else K)
+        assert allowed[b, n, s["tokens"][b, n]]
+
+
+def check_exact_masked(V=6, K=2, T=0.8, seed=16):
+    """Exactness under grammar masks: with x_i drawn from the masked draft
+    distribution, the emitted token at every position follows the masked,
+    renormalised target distribution (scipy softmax over the allowed
+    tokens), to 1e-12; dense and one-hot drafts."""
+    rng = np.random.default_rng(seed)
+    l = (rng.standard_normal((K + 1, V)) * 1.3).astype(np.float32)
+    d = (l[:K] + rng.standard_normal((K, V)) * 0.9).astype(np.float32)
+    allowed = rng.random((K + 1, V)) < 0.6
+    allowed[:, 0] = True
+    allowed[np.arange(K + 1), np.arange(K + 1) % V] = False  # a different hole per row
+    allowed[:, 0] |= ~allowed.any(-1)
+    mask = np.zeros((K + 1, (V + 31) // 32), np.uint32)
+    for i in range(K + 1):
+        for j in np.nonzero(allowed[i])[0]:
+            mask[i, j // 32] |= np.uint32(1 << (j % 32))
+    p = np.zeros((K + 1, V))
+    q = np.zeros((K, V))
+    for i in range(K + 1):
+        a = allowed[i]
+        p[i, a] = scipy.special.softmax(l[i, a].astype(np.float64) / T)
+        if i < K:
+            q[i, a] = scipy.special.softmax(d[i, a].astype(np.float64) / T)
+    # dense drafts: x_i ~ masked q_i, averaged
+    req = _Request(l, d, T, mask)
+    prefix = [int(np.argmax(p[j] * q[j])) for j in range(K)]
+    for i in range(K + 1):
+        emitted = np.zeros(V)
+        for x in (range(V) if i < K else [0]):
+            if i < K and q[i, x] == 0:
+                continue
+            drafts = prefix[:i] + [x] + prefix[i + 1:] if i < K else list(prefix)
+            theta, law = _emission_law(req, drafts, i)
+            if i < K:
+                emitted[x] += q[i, x] * theta
+                emitted += q[i, x] * (1.0 - theta) * law
+            else:
+                emitted = law
+        np.testing.assert_allclose(emitted, p[i], rtol=0, atol=1e-12,
+                                   err_msg="dense position %d" % i)
+    # one-hot drafts: for every proposed x, allowed or not, the emitted law is p_i
+    req = _Request(l, None, T, mask)
+    prefix = [int(np.argmax(p[j])) for j in range(K)]
+    for i in range(K):
+        for x in range(V):
+            drafts = prefix[:i] + [x] + prefix[i + 1:]
+            theta, law = _emission_law(req, drafts, i)
+            assert abs(theta - min(1.0, p[i, x])) < 1e-12, (i, x, theta, p[i, x])
+            emitted = (1.0 - theta) * law
+            emitted[x] += theta
+            np.testing.assert_allclose(emitted, p[i], rtol=0, atol=1e-12,
+                                       err_msg="one-hot position %d draft %d" % (i, x))
+
+
+# ---------------------------------------------------------------------------
+# n-gram proposer
+# ---------------------------------------------------------------------------
+
+def check_golden_ngram():
+    g = _golden("ngram_small.json")
+    for case in g["cases"]:
+        ctx = case["context"]
+        L = max(1, len(ctx) + 3)
+        t = np.full((1, L), 99, np.int32)  # junk past the context is never read
+        t[0, :len(ctx)] = ctx
+        out = oracle.ngram(t, [len(ctx)], case["n_min"], case["n_max"], case["K"])
+        k = len(case["drafts"])
+        assert out["draft_lens"][0] == k, (case, out)
+        assert list(out["drafts"][0, :k]) == case["drafts"] and (out["drafts"][0, k:] == -1).all()
+        assert out["match"][0] == case["match"] and out["ngram"][0] == case["ngram"], (case, out)
+
+
+def _ngram_numpy(c, n_min, n_max, K):
+    """The same rule through numpy's sliding windows: starts s with
+    s + n < len are the windows of c[:len-1]."""
+    c = np.asarray(c)
+    for n in range(n_max, n_min - 1, -1):
+        if len(c) < n + 1:
+            continue
+        win = np.lib.stride_tricks.sliding_window_view(c[:-1], n)
+        hit = np.flatnonzero((win == c[len(c) - n:]).all(axis=1))
+        if hit.size:
+            s = int(hit[0])
+            return list(c[s + n:s + n + K]), s, n
+    return [], -1, 0
+
+
+def check_ngram_matches_numpy(seed=17):
+    """Random contexts over small alphabets (many repeats): the oracle agrees
+    with the sliding-window search, the drafts continue a real earlier
+    occurrence, and no longer n-gram (up to n_max) occurs earlier."""
+    rng = np.random.default_rng(seed)
+    B, L = 300, 60
+    for n_min, n_max, K in ((1, 4, 5), (2, 3, 2), (1, 1, 7), (3, 6, 4)):
+        alpha = rng.integers(2, 6, size=B)
+        t = (rng.integers(0, 1 << 30, size=(B, L)) % alpha[:, None]).astype(np.int32)
+        lens = rng.integers(0, L + 1, size=B).astype(np.int32)
+        out = oracle.ngram(t, lens, n_min, n_max, K)
+        assert (out["status"] == 0).all()
+        for b in range(B):
+            c = t[b, :lens[b]]
+            d, s, n = _ngram_numpy(c, n_min, n_max, K)
+            k = int(out["draft_lens"][b])
+            assert list(out["drafts"][b, :k]) == d and int(out["match"][b]) == s, (b, n_min, n_max)
+            assert int(out["ngram"][b]) == n
+            if s >= 0:
+                assert (c[s:s + n] == c[len(c) - n:]).all() and s + n < len(c)
+                assert k == min(K, len(c) - s - n) and k >= 1
+    # a context length outside [0, L] is a per-request error
+    out = oracle.ngram(np.zeros((3, 4), np.int32), [2, 5, -1], 1, 2, 3)
+    assert list(out["status"]) == [0, oracle.BAD_DRAFT_LEN, oracle.BAD_DRAFT_LEN]
+    assert list(out["draft_lens"]) == [1, 0, 0]
+
+
+# ---------------------------------------------------------------------------
 # tree
 # ---------------------------------------------------------------------------
 
@@ -512,5 +705,6 @@ ALL_CHECKS = [
     check_golden_tree, check_golden_compact, check_exact_dense, check_exact_onehot,
     check_invariants, check_onehot_accept_iff_u_below_p,
     check_zero_probability_draft_rejected, check_temperature_to_zero_is_greedy,
-    check_errors, check_tree_brute_force, check_tree_errors,
+    check_errors, check_tree_brute_force, check_tree_errors, check_golden_masked,
+    check_mask_layout, check_exact_masked, check_golden_ngram, check_ngram_matches_numpy,
 ]

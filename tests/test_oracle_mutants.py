@@ -42,6 +42,30 @@ MUTANTS = [
     ("accepted drafts not copied",
      "for (int i = 0; i < n; ++i) tokens[i] = draft_tokens[b * (size_t)K + (size_t)i];\n  tokens[n] = t;",
      "for (int i = 0; i < n; ++i) tokens[i] = 0;\n  tokens[n] = t;", 1),
+    ("mask bits read from the top", "(mask_row[j / 32] >> (j % 32)) & 1u",
+     "(mask_row[j / 32] >> (31 - j % 32)) & 1u", 1),
+    ("mask words indexed by token modulo", "(mask_row[j / 32] >> (j % 32)) & 1u",
+     "(mask_row[j % 32 % ((V + 31) / 32)] >> (j % 32)) & 1u", 1),
+    ("draft row left unmasked",
+     "      apply_token_mask(lrow, V, mask_row_of(mask, K, V, b, i));\n      if (!row_is_valid",
+     "      if (!row_is_valid", 1),
+    ("bonus row takes the previous position's mask", "mask_row_of(mask, K, V, b, K_b)",
+     "mask_row_of(mask, K, V, b, K_b > 0 ? K_b - 1 : 0)", 1),
+    ("mask rows strided by K", "return mask + (b * (size_t)(K + 1) + (size_t)i) * words;",
+     "return mask + (b * (size_t)K + (size_t)i) * words;", 1),
+    ("greedy ignores the mask", "    apply_token_mask(row, V, mask_row_of(mask, K, V, b, i));\n",
+     "", 1),
+    ("n-gram pattern may match itself", "for (int s = 0; s + n < len && found < 0; ++s) {",
+     "for (int s = 0; s + n <= len && found < 0; ++s) {", 1),
+    ("n-gram takes the latest occurrence", "if (equal) found = s;",
+     "if (equal) { found = s; for (int s2 = s + 1; s2 + n < len; ++s2) { int e2 = 1; "
+     "for (int t = 0; t < n; ++t) if (c[s2 + t] != pattern[t]) { e2 = 0; break; } "
+     "if (e2) found = s2; } }", 1),
+    ("n-gram tries the shortest n first",
+     "for (int n = n_max; n >= n_min; --n) {\n      if (len < n + 1) continue;",
+     "for (int n = n_min; n <= n_max; ++n) {\n      if (len < n + 1) continue;", 1),
+    ("n-gram drafts start one late", "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t];",
+     "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t + 1 < len ? found + n + t + 1 : found + n + t];", 1),
 ]
 
 FAST_CHECKS = [c for c in oc.ALL_CHECKS] + [

@@ -23,10 +23,24 @@ Recipe (all draws from numpy's PCG64 streams, seeded per quantity):
                  one per request (last column) for the residual / bonus draw;
   tree tokens    children of a node take the top-k ids of a noisy copy
                  (sigma = 0.5) of the node's own target row, in descending
-                 order, k = the node's child count.
+                 order, k = the node's child count;
+  n-gram contexts  (the proposer's input) token histories of length
+                 U[L/2, L] built from spans of 8..64 tokens: with probability
+                 p_copy a copy of an earlier span of the same history (the
+                 overlap that code editing and document question answering
+                 show), otherwise fresh ids (uniform over the vocabulary);
+  grammar masks  (structured output) per position, with probability p_free the
+                 grammar allows every token (free text), otherwise a set of
+                 round(allowed_frac * V) uniform ids (duplicates merge); packed
+                 32 tokens per 32-bit word, token j at bit j % 32 of word
+                 j // 32.  Drafts then follow the mask as a grammar-constrained
+                 proposer's would: the argmax / Gumbel-max over the allowed
+                 tokens, and random ids drawn among the allowed ones.
 
-The five workloads mirror the vocabularies and draft lengths the pages use
-(Llama-3, Qwen, DeepSeek-V3 vocabularies; K = 1..5; batch up to 256).
+The standard workloads mirror the vocabularies and draft lengths the pages
+use (Llama-3, Qwen, DeepSeek-V3 vocabularies; K = 1..5; batch up to 256);
+workload 5 is workload 2 under grammar masks, workload 6 the n-gram proposer
+that makes workload 2's kind of drafts.
 """
 from __future__ import annotations
 
@@ -47,6 +61,13 @@ WORKLOADS = {
             dtype="bf16", T=1.0, drafts="dense", sigma=0.25),
     4: dict(name="medusa-tree-B32-N60-V32000", kind="tree", B=32, V=32000, dtype="bf16",
             sigma=0.5, tree="medusa60"),
+    # workload 2 under grammar masks (structured output)
+    5: dict(name="qwen-vocab-onehot-grammar-B256-K5-V152064", kind="sample", B=256, K=5,
+            V=152064, dtype="bf16", T=1.0, drafts="onehot", p_argmax=0.6,
+            grammar=dict(p_free=0.3, allowed_frac=0.02)),
+    # the n-gram proposer that makes workload 2's drafts (prompt_lookup_max 4, K 5)
+    6: dict(name="ngram-propose-B256-L4096-V152064", kind="ngram", B=256, K=5, V=152064,
+            L=4096, n_min=1, n_max=4),
 }
 
 
@@ -67,6 +88,9 @@ class Workload:
     parent: Optional[np.ndarray] = None
     node_tokens: Optional[np.ndarray] = None
     max_depth: int = 0
+    token_mask: Optional[np.ndarray] = None  # [B, K+1, ceil(V/32)] uint32
+    history: Optional[np.ndarray] = None     # [B, L] int32 n-gram proposer contexts
+    history_lens: Optional[np.ndarray] = None
     meta: dict = field(default_factory=dict)
 
     def logits_as_float(self, which="target"):
@@ -126,17 +150,44 @@ def _as_float(x, dtype):
     return bf16_bits_to_float(x) if dtype == "bf16" else x
 
 
+def grammar_masks(rng, B, K1, V, p_free=0.3, allowed_frac=0.02, junk_tail=False):
+    """[B, K1, ceil(V/32)] uint32 bitmasks (see the recipe above).  Bits past
+    V are clear, or random when ``junk_tail`` (they must be ignored)."""
+    W = (V + 31) // 32
+    words = np.full((B, K1, W), 0xFFFFFFFF, np.uint32)
+    constrained = rng.random((B, K1)) >= p_free
+    n = max(1, int(round(allowed_frac * V)))
+    for b, i in zip(*np.nonzero(constrained)):
+        ids = rng.integers(0, V, n)
+        row = np.zeros(W, np.uint32)
+        np.bitwise_or.at(row, ids >> 5, np.left_shift(np.uint32(1), (ids & 31).astype(np.uint32)))
+        words[b, i] = row
+    if V % 32:
+        tail = np.uint32((1 << (V % 32)) - 1)
+        junk = rng.integers(0, 2 ** 32, size=(B, K1), dtype=np.uint64).astype(np.uint32)
+        words[..., -1] = (words[..., -1] & tail) | ((junk & ~tail) if junk_tail else np.uint32(0))
+    return words
+
+
+def allowed_tokens(words_row, V):
+    """Boolean [V] of the tokens one mask row allows."""
+    return np.unpackbits(np.ascontiguousarray(words_row, "<u4").view(np.uint8),
+                         bitorder="little")[:V].astype(bool)
+
+
 # ---------------------------------------------------------------------------
 # sampling / greedy workloads
 # ---------------------------------------------------------------------------
 
 def make_sample_case(B, K, V, *, dtype="bf16", T=1.0, drafts="dense", sigma=0.5,
                      p_argmax=0.6, seed=0, draft_lens=None, mask_frac=0.0,
-                     quantize=None, uniform_seed=None) -> Workload:
+                     quantize=None, uniform_seed=None, grammar=None) -> Workload:
     """A verification batch.  ``drafts`` is 'dense' (draft logits given) or
     'onehot' (deterministic proposer, no draft logits).  ``mask_frac`` sets
     that fraction of logits to -inf (never a whole row); ``quantize`` rounds
-    logits to multiples of that step (to create exact ties)."""
+    logits to multiples of that step (to create exact ties); ``grammar``
+    (a dict of grammar_masks keyword arguments) adds grammar masks, with the
+    drafts drawn under them."""
     r_l, r_d, r_t, r_m = (_rng(seed, 1), _rng(seed, 2), _rng(seed, 3), _rng(seed, 4))
     r_u = np.random.default_rng(int(seed) if uniform_seed is None else int(uniform_seed))
     tl = target_logits(r_l, B * (K + 1), V)
@@ -165,12 +216,28 @@ def make_sample_case(B, K, V, *, dtype="bf16", T=1.0, drafts="dense", sigma=0.5,
         toks = np.where(take_argmax, am, rand_ids).astype(np.int32)
     else:
         raise ValueError("drafts must be 'dense' or 'onehot'")
+    masks = None
+    if grammar is not None:
+        r_g = _rng(seed, 5)
+        masks = grammar_masks(r_g, B, K + 1, V, **grammar)
+        toks = toks.reshape(B, K).copy()
+        for b in range(B):
+            for i in range(K):
+                ok = allowed_tokens(masks[b, i], V)
+                if drafts == "dense":
+                    g = -np.log(-np.log(r_g.random(V)))
+                    score = _as_float(draft[b, i], dtype).astype(np.float64) / (T if T > 0 else 1)
+                    toks[b, i] = np.argmax(np.where(ok, score + (g if T > 0 else 0), -np.inf))
+                elif take_argmax[b, i]:
+                    toks[b, i] = np.argmax(np.where(ok, tf[b, i], -np.inf))
+                else:
+                    toks[b, i] = r_g.choice(np.nonzero(ok)[0])
     uniforms = r_u.random((B, K + 1), dtype=np.float32)
     lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, np.int32)
     return Workload(dtype=dtype, B=B, V=V, K=K, T=float(T), target=target, draft=draft,
                     draft_tokens=np.ascontiguousarray(toks.reshape(B, K), np.int32),
-                    draft_lens=lens, uniforms=uniforms,
-                    meta=dict(drafts=drafts, sigma=sigma, seed=seed))
+                    draft_lens=lens, uniforms=uniforms, token_mask=masks,
+                    meta=dict(drafts=drafts, sigma=sigma, seed=seed, grammar=grammar))
 
 
 # ---------------------------------------------------------------------------
@@ -244,17 +311,47 @@ def make_tree_case(B, V, parent, *, dtype="bf16", sigma=0.5, seed=0, mask_frac=0
 # ---------------------------------------------------------------------------
 
 def make_workload(index: int, seed: int = 0) -> Workload:
-    """The standard workload ``index`` (0..4), seeded by ``seed + index``
+    """The standard workload ``index`` (0..6), seeded by ``seed + index``
     for its uniforms and by (seed + index, stream) for everything else."""
     w = WORKLOADS[index]
     s = seed + index
-    if w["kind"] == "tree":
+    if w["kind"] == "ngram":
+        ctx = make_ngram_case(w["B"], w["L"], w["V"], seed=s)
+        wl = Workload(dtype="int32", B=w["B"], V=w["V"], target=np.empty(0, np.float32),
+                      K=w["K"], history=ctx["tokens"], history_lens=ctx["lens"],
+                      meta=dict(n_min=w["n_min"], n_max=w["n_max"], L=w["L"]))
+    elif w["kind"] == "tree":
         wl = make_tree_case(w["B"], w["V"], medusa60_parent(), dtype=w["dtype"],
                             sigma=w["sigma"], seed=s)
     else:
         wl = make_sample_case(w["B"], w["K"], w["V"], dtype=w["dtype"], T=w["T"],
                               drafts=w["drafts"], sigma=w.get("sigma", 0.0),
-                              p_argmax=w.get("p_argmax", 0.6), seed=s, uniform_seed=s)
+                              p_argmax=w.get("p_argmax", 0.6), seed=s, uniform_seed=s,
+                              grammar=w.get("grammar"))
     wl.meta["workload"] = w["name"]
     wl.meta["index"] = index
     return wl
+
+
+# ---------------------------------------------------------------------------
+# n-gram proposer inputs
+# ---------------------------------------------------------------------------
+
+def make_ngram_case(B, L, V, *, p_copy=0.5, seed=0):
+    """Token histories for the prompt-lookup proposer: tokens [B, L] int32
+    (entries past lens[b] hold junk ids), lens [B] int32 in [L/2, L]."""
+    rng = _rng(seed, 6)
+    tokens = rng.integers(0, V, size=(B, L), dtype=np.int64).astype(np.int32)
+    lens = rng.integers(max(0, L // 2), L + 1, size=B).astype(np.int32)
+    for b in range(B):
+        pos = 0
+        row = tokens[b]
+        while pos < lens[b]:
+            span = int(rng.integers(8, 65))
+            end = min(pos + span, int(lens[b]))
+            if pos >= 8 and rng.random() < p_copy:
+                src = int(rng.integers(0, pos - 1))
+                for t in range(pos, end):  # element by element: a copy may overlap itself
+                    row[t] = row[src + t - pos]
+            pos = end
+    return dict(tokens=tokens, lens=lens)
