@@ -184,13 +184,18 @@ def oracle_run(wl, mode, requests, threads):
     import oracle
     sub = slice(0, requests)
     t0 = time.perf_counter()
-    if mode == "tree":
+    if mode == "propose":
+        oracle.ngram(wl.history[sub], wl.history_lens[sub], wl.meta["n_min"], wl.meta["n_max"],
+                     wl.K)
+    elif mode == "tree":
         oracle.tree(wl.target[sub], wl.parent, wl.node_tokens[sub], wl.max_depth, threads=threads)
     elif mode == "greedy":
-        oracle.greedy(wl.target[sub], wl.draft_tokens[sub], threads=threads)
+        oracle.greedy(wl.target[sub], wl.draft_tokens[sub], threads=threads,
+                      token_mask=None if wl.token_mask is None else wl.token_mask[sub])
     else:
         oracle.sample(wl.target[sub], None if wl.draft is None else wl.draft[sub],
-                      wl.draft_tokens[sub], wl.uniforms[sub], wl.T, threads=threads)
+                      wl.draft_tokens[sub], wl.uniforms[sub], wl.T, threads=threads,
+                      token_mask=None if wl.token_mask is None else wl.token_mask[sub])
     return time.perf_counter() - t0
 
 
@@ -212,10 +217,12 @@ def cpu_baseline(wl, mode, budget_s=12.0):
 def load_workload(args, seed=0):
     from token_verification_gb300 import synth
     wl = synth.make_workload(args.workload, seed=seed)
-    mode = "tree" if wl.parent is not None else ("greedy" if args.greedy else "sample")
+    mode = ("propose" if wl.history is not None else "tree" if wl.parent is not None
+            else "greedy" if args.greedy else "sample")
     if args.batch:  # a smaller batch of the same workload (profiling captures)
         wl.B = args.batch
-        for name in ("target", "draft", "draft_tokens", "uniforms", "node_tokens"):
+        for name in ("target", "draft", "draft_tokens", "uniforms", "node_tokens", "token_mask",
+                     "history", "history_lens"):
             v = getattr(wl, name)
             if v is not None:
                 setattr(wl, name, v[:args.batch])
@@ -256,6 +263,8 @@ def run_reference(args):
 def metric_name(wl, mode, args):
     if args.workload == 2 and mode == "sample" and not args.batch:
         return METRIC
+    if mode == "propose":
+        return "n-gram proposer calls/s and context GB/s on %s" % wl.meta["workload"]
     return "verify calls/s and logits HBM GB/s (%% of GB300 peak) on %s (%s)" % (
         wl.meta["workload"], mode)
 
@@ -263,10 +272,18 @@ def metric_name(wl, mode, args):
 def workload_config(wl, mode):
     cfg = {"workload": wl.meta["workload"], "mode": mode, "B": wl.B, "V": wl.V,
            "logits": wl.dtype, "parallelism": "dp%d" % dist_env()[0]}
+    if mode == "propose":
+        del cfg["logits"]
+        cfg.update(L=wl.meta["L"], K=wl.K, n_min=wl.meta["n_min"], n_max=wl.meta["n_max"],
+                   l2="inputs smaller than L2 (%d KB of contexts per call): 2 rotating input "
+                      "sets; the figure includes L2 reuse" % (wl.history.nbytes // 1024))
+        return cfg
     if mode == "tree":
         cfg.update(N=int(wl.parent.size), max_depth=wl.max_depth)
     else:
         cfg.update(K=wl.K, drafts=wl.meta.get("drafts"), temperature=0.0 if mode == "greedy" else wl.T)
+        if wl.token_mask is not None:
+            cfg["grammar_masks"] = dict(wl.meta["grammar"], bytes=int(wl.token_mask.nbytes))
     total = wl.target.nbytes + (wl.draft.nbytes if (wl.draft is not None and mode == "sample") else 0)
     cfg["l2"] = ("inputs larger than L2: %d MB of logits per call, 2 rotating input sets"
                  % (total // 2**20) if total > 129 * 2**20 else
@@ -286,11 +303,17 @@ class Case:
         self.wl, self.mode, self.device = wl, mode, device
         to_t = (lambda a: torch.from_numpy(a.view(np.int16)).view(torch.bfloat16)) \
             if wl.dtype == "bf16" else (lambda a: torch.from_numpy(a))
-        self.host = {"target": to_t(wl.target)}
-        if mode == "tree":
+        self.host = {"target": to_t(wl.target)} if mode != "propose" else {
+            "history": torch.from_numpy(wl.history),
+            "history_lens": torch.from_numpy(wl.history_lens)}
+        if mode == "propose":
+            pass
+        elif mode == "tree":
             self.host["node_tokens"] = torch.from_numpy(wl.node_tokens)
         else:
             self.host["tokens"] = torch.from_numpy(wl.draft_tokens)
+            if wl.token_mask is not None:
+                self.host["token_mask"] = torch.from_numpy(wl.token_mask.view(np.int32))
             if mode == "sample":
                 self.host["uniforms"] = torch.from_numpy(wl.uniforms)
                 if wl.draft is not None:
@@ -302,7 +325,7 @@ class Case:
             self.sets.append({k: v[perm].contiguous().to(device) for k, v in self.host.items()})
 
     def alloc(self, packed=True):
-        if self.mode == "tree":
+        if self.mode in ("tree", "propose"):
             return None
         return self.api.alloc_outputs(self.wl.B, self.wl.K, self.device, packed=packed,
                                       accept_prob=packed and self.mode == "sample",
@@ -310,43 +333,60 @@ class Case:
 
     def call(self, inputs, out):
         wl, api = self.wl, self.api
+        if self.mode == "propose":
+            return api.spec_ngram_propose(inputs["history"], inputs["history_lens"], K=wl.K,
+                                          n_min=wl.meta["n_min"], n_max=wl.meta["n_max"], out=out)
         if self.mode == "tree":
             return api.spec_verify_tree(inputs["target"], wl.parent, inputs["node_tokens"],
                                         wl.max_depth, out, path=False, status=False)
         if self.mode == "greedy":
-            return api.spec_verify_greedy(inputs["target"], inputs["tokens"], out)
+            return api.spec_verify_greedy(inputs["target"], inputs["tokens"], out,
+                                          token_mask=inputs.get("token_mask"))
         return api.spec_verify_sample(inputs["target"], inputs.get("draft"), inputs["tokens"],
-                                      inputs["uniforms"], wl.T, out)
+                                      inputs["uniforms"], wl.T, out,
+                                      token_mask=inputs.get("token_mask"))
 
     def step(self, i, out):
         return self.call(self.sets[i & 1], out)
 
+    def results(self, out):
+        """The call's per-request token rows and lengths (what a caller reads back)."""
+        if self.mode == "propose":
+            return out.drafts, out.draft_lens
+        return out.tokens, out.accept_len
+
     def launches(self, packed):
-        if self.mode == "tree":
+        if self.mode in ("tree", "propose"):
             return 1
-        if self.mode == "sample" and self.wl.draft is not None:
-            return 3 + (1 if packed else 0)  # stream, finalize, residual, compaction
-        return 2  # stream, finalize (which also writes the packed output)
+        # stream, finalize (the residual draw and the packed output included)
+        return 2
 
     def kernel_label(self):
+        if self.mode == "propose":
+            return "ngram_kernel"
         if self.mode == "tree":
             return "tree_kernel"
+        masked = ", grammar-masked" if self.wl.token_mask is not None else ""
         if self.mode == "sample" and self.wl.draft is not None:
-            return "verify_stream_kernel + finalize_kernel + residual_kernel (dense)"
-        return "verify_stream_kernel + finalize_kernel (%s)" % (
-            "greedy" if self.mode == "greedy" else "one-hot")
+            return "verify_stream_kernel + finalize_kernel (dense%s)" % masked
+        return "verify_stream_kernel + finalize_kernel (%s%s)" % (
+            "greedy" if self.mode == "greedy" else "one-hot", masked)
 
     def algorithmic_bytes(self, out):
         """Logit bytes the method needs per call: every row once (sampling,
-        greedy); the rows on the accepted path (tree)."""
+        greedy), plus the grammar mask words when masked; the rows on the
+        accepted path (tree)."""
         wl = self.wl
+        if self.mode == "propose":  # every context token once
+            return int(wl.history_lens.astype(np.int64).sum()) * 4
         esz = 2 if wl.dtype == "bf16" else 4
         if self.mode == "tree":
             rows = int(out.accept_len.sum().item())
             return rows * wl.V * esz
         rows = wl.B * (wl.K + 1) + (wl.B * wl.K if (self.mode == "sample" and wl.draft is not None)
                                      else 0)
-        return rows * wl.V * esz
+        masks = 0 if wl.token_mask is None else wl.token_mask.nbytes
+        return rows * wl.V * esz + masks
 
 
 def run_ours(args):
@@ -393,7 +433,7 @@ def run_ours(args):
     if sampler:
         sampler.mark(w0, w1)
     max_elapsed, total_calls = aggregate(elapsed, args.steps, world, device)
-    mean_len = float(out.accept_len.float().mean().item())
+    mean_len = float(case.results(out)[1].float().mean().item())
     algo_bytes = case.algorithmic_bytes(out)
 
     # the dominant kernels, timed per call without the packed output, with
@@ -417,7 +457,8 @@ def run_ours(args):
     if rank == 0 and not args.no_e2e:
         pin = {k: v.pin_memory() for k, v in case.host.items()}
         dev_in = {k: torch.empty_like(v, device=device) for k, v in pin.items()}
-        res_tok = torch.empty(tuple(out.tokens.shape), dtype=torch.int32).pin_memory()
+        out_tok, out_len = case.results(out)
+        res_tok = torch.empty(tuple(out_tok.shape), dtype=torch.int32).pin_memory()
         res_len = torch.empty((wl.B,), dtype=torch.int32).pin_memory()
         e2e_steps = max(3, min(args.steps, args.e2e_steps))
 
@@ -425,8 +466,8 @@ def run_ours(args):
             for k in pin:
                 dev_in[k].copy_(pin[k], non_blocking=True)
             case.call(dev_in, out)
-            res_tok.copy_(out.tokens, non_blocking=True)
-            res_len.copy_(out.accept_len, non_blocking=True)
+            res_tok.copy_(out_tok, non_blocking=True)
+            res_len.copy_(out_len, non_blocking=True)
 
         for _ in range(2):
             e2e_step()
@@ -454,9 +495,9 @@ def run_ours(args):
             "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": workload_config(wl, mode),
-            "draft_tokens_per_s": None if mode == "tree" else value * wl.B * wl.K,
+            "draft_tokens_per_s": None if mode in ("tree", "propose") else value * wl.B * wl.K,
             "hbm_gbs": algo_bytes * value / 1e9,
-            "mean_accept_len": mean_len,
+            ("mean_draft_len" if mode == "propose" else "mean_accept_len"): mean_len,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
                          "kernel": case.kernel_label(), "kernel_ms": kern_ms,

@@ -80,6 +80,7 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_MAX_B 65536          /* requests per call */
 #define SV_MAX_V (1 << 24)      /* vocabulary size */
 #define SV_MAX_TREE_NODES 256   /* candidate nodes per tree (root excluded) */
+#define SV_MAX_NGRAM 32         /* longest n-gram the proposer matches */
 
 /* Bytes of workspace that spec_verify_sample / _greedy need for B requests
  * of K draft positions over a vocabulary of V (the dense-draft sampling case,
@@ -147,6 +148,43 @@ sv_status spec_verify_greedy(const void* target_logits, const int32_t* draft_tok
                              int32_t* out_batch_id, int32_t* out_status, void* workspace,
                              size_t ws_bytes, sv_stream_t stream);
 
+/* Grammar-constrained verification ("Speculative Decoding" (LMDeploy docs),
+ * "投机解码与结构化输出" / "工作原理"): with structured output (a JSON schema, a
+ * regular expression) each position may only emit the tokens its grammar
+ * state allows.  The mask of position i is applied to target row i - and to
+ * draft row i, since the draft was proposed under the same mask - before the
+ * rule runs: a ruled-out token has probability 0, so it is never accepted,
+ * drawn or taken as the argmax.  The masks of positions 1..K depend on the
+ * drafts before them; the caller's grammar matcher computes them all (on a
+ * fork advanced through the drafts) before the call.
+ *
+ *   token_mask  [B, K+1, ceil(V/32)] 32-bit words, 4-byte aligned: request b,
+ *               position i allows token j iff bit j % 32 of word j / 32 of row
+ *               (b, i) is set.  Bits at j >= V are ignored.  When the rows are
+ *               16-byte aligned (16-byte aligned base and ceil(V/32) a multiple
+ *               of 4) the words travel with the logits in the same bulk copies;
+ *               otherwise they are read word by word.
+ * A needed position whose mask leaves no finite logit is a data error
+ * (SV_REQ_BAD_LOGITS).  NULL or misaligned token_mask: SV_ERR_NULL.  All other
+ * arguments, results and the workspace size are those of spec_verify_sample
+ * and spec_verify_greedy. */
+sv_status spec_verify_sample_masked(const void* target_logits, const void* draft_logits,
+                                    const int32_t* draft_tokens, const float* uniforms,
+                                    float temperature, const uint32_t* token_mask,
+                                    int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype,
+                                    int B, int K, int V, const int32_t* draft_lens,
+                                    int32_t* out_cu_accept, int32_t* out_packed,
+                                    int32_t* out_batch_id, float* out_accept_prob,
+                                    int32_t* out_status, void* workspace, size_t ws_bytes,
+                                    sv_stream_t stream);
+sv_status spec_verify_greedy_masked(const void* target_logits, const int32_t* draft_tokens,
+                                    const uint32_t* token_mask, int32_t* out_tokens,
+                                    int32_t* out_accept_len, sv_dtype dtype, int B, int K, int V,
+                                    const int32_t* draft_lens, int32_t* out_cu_accept,
+                                    int32_t* out_packed, int32_t* out_batch_id,
+                                    int32_t* out_status, void* workspace, size_t ws_bytes,
+                                    sv_stream_t stream);
+
 /* Greedy tree verification (Medusa / EAGLE; "推测解码与 MTP" §3.3).
  *
  *   target_logits  [B, N+1, V] dtype: row 0 is the root (the last committed
@@ -173,6 +211,36 @@ sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent
                            int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
                            int max_depth, int32_t* out_path, int32_t* out_status,
                            sv_stream_t stream);
+
+/* n-gram (prompt-lookup) proposer: the step before verification that makes
+ * the one-hot drafts ("投机解码" (FastDeploy docs), "使用 Ngram 解码": drafts
+ * come from matching an n-gram window against the prompt and the generated
+ * tokens; the vLLM Ascend guide's n-gram example, prompt_lookup_max = 4 and 5
+ * speculative tokens; "推测解码与 MTP" §9.1 prompt lookup).
+ *
+ * For n = n_max down to n_min, the last n tokens of request b's context
+ * c = tokens[b, 0 .. lens[b]) are looked up earlier in c: the match is the
+ * EARLIEST start s with c[s .. s+n) equal to them and at least one token
+ * after it (s + n < lens[b]).  The first n that matches decides; the drafts
+ * are the tokens after the match, c[s+n .. min(s+n+K, lens[b])).
+ *
+ *   tokens          [B, L] int32: request b's context in its first lens[b]
+ *                   entries (prompt then generated tokens); the rest is never
+ *                   read.  Any int32 values (they are only compared).
+ *   lens            [B] int32, 0 <= lens[b] <= L; outside that range the
+ *                   request gets no drafts and SV_REQ_BAD_DRAFT_LEN.
+ *   n_min, n_max    1 <= n_min <= n_max <= SV_MAX_NGRAM.
+ *   K               0 <= K <= SV_MAX_K drafts per request.
+ *   out_drafts      [B, K] int32: the drafts, -1 after them.
+ *   out_draft_lens  [B] int32: how many (0..K); pass it as draft_lens to
+ *                   spec_verify_sample with draft_logits = NULL.
+ *   out_match       [B] int32 or NULL: the start s, or -1 without a match.
+ *   out_status      [B] int32 or NULL: SV_REQ_* bits.
+ * B * L < 2^31.  One pass over each context; no workspace. */
+sv_status spec_ngram_propose(const int32_t* tokens, const int32_t* lens, int B, int L,
+                             int n_min, int n_max, int K, int32_t* out_drafts,
+                             int32_t* out_draft_lens, int32_t* out_match, int32_t* out_status,
+                             sv_stream_t stream);
 
 /* Allocation-free variant of spec_verify_sample.  The pages have no
  * counterpart to this entry point; it exists for callers that cannot

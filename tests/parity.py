@@ -44,13 +44,15 @@ def to_device(wl, device="cuda"):
     for name in ("draft_tokens", "draft_lens", "uniforms", "node_tokens"):
         v = getattr(wl, name)
         d[name] = None if v is None else torch.from_numpy(np.ascontiguousarray(v)).to(device)
+    d["token_mask"] = None if wl.token_mask is None else torch.from_numpy(
+        np.ascontiguousarray(wl.token_mask).view(np.int32)).to(device)
     return d
 
 
 def oracle_sample(wl, threads=8, temperature=None):
     T = wl.T if temperature is None else temperature
     return oracle.sample(wl.target, wl.draft, wl.draft_tokens, wl.uniforms, T,
-                         draft_lens=wl.draft_lens, threads=threads)
+                         draft_lens=wl.draft_lens, threads=threads, token_mask=wl.token_mask)
 
 
 @dataclass
@@ -153,7 +155,8 @@ def verify_draws(wl, rep: SampleReport, temperature=None):
 
     T = wl.T if temperature is None else temperature
     out = oracle.sample(sub(wl.target), sub(wl.draft), sub(wl.draft_tokens), sub(wl.uniforms),
-                        T, draft_lens=sub(wl.draft_lens), probe_tokens=toks)
+                        T, draft_lens=sub(wl.draft_lens), probe_tokens=toks,
+                        token_mask=sub(wl.token_mask))
     u = wl.uniforms[idx, wl.K].astype(np.float64)
     lo, hi = out["probe"][:, 0], out["probe"][:, 1]
     ok = (hi > lo) & (lo <= u + FLAG_TOL) & (hi >= u - FLAG_TOL)

@@ -85,7 +85,7 @@ GRID = [
     (1025, 2, 1.0, "bf16", "dense"), (4104, 4, 0.8, "bf16", "onehot"),
     (32000, 5, 1.0, "bf16", "dense"), (32001, 1, 1.3, "f32", "onehot"),
     (9000, 0, 1.0, "bf16", "onehot"), (5000, 31, 0.9, "bf16", "onehot"),
-    (65536, 2, 0.7, "f32", "dense"),
+    (65536, 2, 0.7, "f32", "dense"), (300000, 2, 1.0, "bf16", "dense"),
 ]
 
 

@@ -14,7 +14,8 @@ LIB_PATH = os.path.join(HERE, "libspecverify.so")
 SYMBOLS = (
     "spec_verify_workspace_size", "spec_verify_workspace_init", "spec_verify_sample",
     "spec_verify_greedy", "spec_verify_tree", "spec_verify_status_string",
-    "spec_verify_version", "spec_verify_sample_noalloc",
+    "spec_verify_version", "spec_verify_sample_noalloc", "spec_verify_sample_masked",
+    "spec_verify_greedy_masked", "spec_ngram_propose",
 )
 
 _lock = threading.Lock()
@@ -45,6 +46,13 @@ def lib():
         l.spec_verify_sample_noalloc.restype = I
         l.spec_verify_greedy.argtypes = [P, P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
         l.spec_verify_greedy.restype = I
+        l.spec_verify_sample_masked.argtypes = [P, P, P, P, F, P, P, P, I, I, I, I, P, P, P, P, P,
+                                                P, P, Z, P]
+        l.spec_verify_sample_masked.restype = I
+        l.spec_verify_greedy_masked.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
+        l.spec_verify_greedy_masked.restype = I
+        l.spec_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
+        l.spec_ngram_propose.restype = I
         l.spec_verify_tree.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P]
         l.spec_verify_tree.restype = I
         l.spec_verify_status_string.argtypes = [I]

@@ -121,43 +121,64 @@ def _validate_batch(target_logits, draft_tokens, draft_lens):
     return B, K, V, device
 
 
+def _check_mask(token_mask, B, K, V, device):
+    if token_mask is not None:
+        _check(token_mask, "token_mask", device, torch.int32, (B, K + 1, (V + 31) // 32))
+
+
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature,
                        out: Optional[VerifyOutputs] = None, *, draft_lens=None,
-                       packed=True, accept_prob=True, status=True) -> VerifyOutputs:
+                       packed=True, accept_prob=True, status=True,
+                       token_mask=None) -> VerifyOutputs:
     """Rejection-sampling verification of one batch (see spec_verify.h).
 
     target_logits [B, K+1, V] bf16/fp32 CUDA; draft_logits [B, K, V] same
     dtype or None (one-hot drafts); draft_tokens [B, K] int32; uniforms
-    [B, K+1] fp32; temperature >= 0 (0 = greedy rule)."""
+    [B, K+1] fp32; temperature >= 0 (0 = greedy rule); token_mask
+    [B, K+1, ceil(V/32)] int32 grammar masks or None (bit j % 32 of word
+    j // 32 set = token j allowed at that position)."""
     B, K, V, device = _validate_batch(target_logits, draft_tokens, draft_lens)
     if draft_logits is not None:
         _check(draft_logits, "draft_logits", device, target_logits.dtype, (B, K, V))
     _check(uniforms, "uniforms", device, torch.float32, (B, K + 1))
+    _check_mask(token_mask, B, K, V, device)
     if out is None:
         out = alloc_outputs(B, K, device, packed=packed, accept_prob=accept_prob, status=status)
     ws = workspace(B, K, V, device)
-    rc = _native.lib().spec_verify_sample(
-        _p(target_logits), _p(draft_logits), _p(draft_tokens), _p(uniforms),
-        ctypes.c_float(float(temperature)), _p(out.tokens), _p(out.accept_len),
-        _dtype_code(target_logits), B, K, V, _p(draft_lens), _p(out.cu_accept), _p(out.packed),
-        _p(out.batch_id), _p(out.accept_prob), _p(out.status), _p(ws), ws.numel(),
-        _stream(device))
+    lib = _native.lib()
+    head = (_p(target_logits), _p(draft_logits), _p(draft_tokens), _p(uniforms),
+            ctypes.c_float(float(temperature)))
+    tail = (_p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, K, V,
+            _p(draft_lens), _p(out.cu_accept), _p(out.packed), _p(out.batch_id),
+            _p(out.accept_prob), _p(out.status), _p(ws), ws.numel(), _stream(device))
+    if token_mask is None:
+        rc = lib.spec_verify_sample(*head, *tail)
+    else:
+        rc = lib.spec_verify_sample_masked(*head, _p(token_mask), *tail)
     if rc:
         raise VerifyError(rc)
     return out
 
 
 def spec_verify_greedy(target_logits, draft_tokens, out: Optional[VerifyOutputs] = None, *,
-                       draft_lens=None, packed=True, status=True) -> VerifyOutputs:
-    """Greedy verification: accept while the draft equals the target argmax."""
+                       draft_lens=None, packed=True, status=True,
+                       token_mask=None) -> VerifyOutputs:
+    """Greedy verification: accept while the draft equals the target argmax
+    (over the tokens token_mask allows, when given)."""
     B, K, V, device = _validate_batch(target_logits, draft_tokens, draft_lens)
+    _check_mask(token_mask, B, K, V, device)
     if out is None:
         out = alloc_outputs(B, K, device, packed=packed, accept_prob=False, status=status)
     ws = workspace(B, K, V, device)
-    rc = _native.lib().spec_verify_greedy(
-        _p(target_logits), _p(draft_tokens), _p(out.tokens), _p(out.accept_len),
-        _dtype_code(target_logits), B, K, V, _p(draft_lens), _p(out.cu_accept), _p(out.packed),
-        _p(out.batch_id), _p(out.status), _p(ws), ws.numel(), _stream(device))
+    lib = _native.lib()
+    tail = (_p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, K, V,
+            _p(draft_lens), _p(out.cu_accept), _p(out.packed), _p(out.batch_id), _p(out.status),
+            _p(ws), ws.numel(), _stream(device))
+    if token_mask is None:
+        rc = lib.spec_verify_greedy(_p(target_logits), _p(draft_tokens), *tail)
+    else:
+        rc = lib.spec_verify_greedy_masked(_p(target_logits), _p(draft_tokens), _p(token_mask),
+                                           *tail)
     if rc:
         raise VerifyError(rc)
     return out
@@ -206,6 +227,40 @@ def spec_verify_tree(target_logits, tree_parent, tree_tokens, max_depth=None,
         _p(target_logits), parent.ctypes.data_as(ctypes.c_void_p), _p(tree_tokens),
         _p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, N, V, int(max_depth),
         _p(out.path), _p(out.status), _stream(device))
+    if rc:
+        raise VerifyError(rc)
+    return out
+
+
+@dataclass
+class NgramOutputs:
+    drafts: torch.Tensor      # [B, K], -1 after the drafts
+    draft_lens: torch.Tensor  # [B]
+    match: Optional[torch.Tensor] = None
+    status: Optional[torch.Tensor] = None
+
+
+def spec_ngram_propose(tokens, lens, K=5, n_min=1, n_max=4, out: Optional[NgramOutputs] = None,
+                       *, match=True, status=True) -> NgramOutputs:
+    """n-gram (prompt-lookup) proposer (see spec_verify.h): tokens [B, L]
+    int32 contexts, lens [B] int32.  The drafts feed spec_verify_sample as
+    one-hot drafts with draft_lens = out.draft_lens."""
+    if tokens.dim() != 2:
+        raise ValueError("tokens must be [B, L]")
+    B, L = tokens.shape
+    device = tokens.device
+    if device.type != "cuda":
+        raise ValueError("tokens must be a CUDA tensor")
+    _check(tokens, "tokens", device, torch.int32)
+    _check(lens, "lens", device, torch.int32, (B,))
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=device)
+        out = NgramOutputs(drafts=torch.empty((B, K), **i32), draft_lens=torch.empty((B,), **i32),
+                           match=torch.empty((B,), **i32) if match else None,
+                           status=torch.empty((B,), **i32) if status else None)
+    rc = _native.lib().spec_ngram_propose(_p(tokens), _p(lens), B, L, int(n_min), int(n_max),
+                                          int(K), _p(out.drafts), _p(out.draft_lens),
+                                          _p(out.match), _p(out.status), _stream(device))
     if rc:
         raise VerifyError(rc)
     return out

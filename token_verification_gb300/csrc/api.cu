@@ -16,19 +16,16 @@ namespace sv {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// The regions that must hold zeros when a call starts (counters and the
-// pending flags) come first; every call leaves them zero again.
+// The region that must hold zeros when a call starts (the error flag and
+// the finalize ticket) comes first; every call leaves it zero again.
 static WorkspaceLayout layout_for(int B, int R, int V) {
   const size_t NC = ((size_t)V + kChunk - 1) / kChunk;
   WorkspaceLayout l;
   size_t o = 0;
-  l.res_ticket = o; o = align256(o + sizeof(int) * (size_t)B);
   l.counters = o;   o = align256(o + 2 * sizeof(int));
-  l.state = o;      o = align256(o + sizeof(ReqState) * (size_t)B);
   l.zero_bytes = o;
   l.rec = o;        o = align256(o + sizeof(float2) * (size_t)B * R * NC);
   l.lx = o;         o = align256(o + sizeof(float) * (size_t)B * R);
-  l.res_rec = o;    o = align256(o + sizeof(float) * (size_t)B * NC);
   l.total = o;
   return l;
 }
@@ -87,7 +84,8 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
                                int K, int V, const int32_t* draft_lens, int32_t* out_cu,
                                int32_t* out_packed, int32_t* out_batch_id, float* out_accept_prob,
                                int32_t* out_status, void* ws, size_t ws_bytes,
-                               cudaStream_t stream, int greedy_prob) {
+                               cudaStream_t stream, int greedy_prob,
+                               const uint32_t* mask = nullptr) {
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
   if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return SV_ERR_SHAPE;
   if (B == 0) {
@@ -105,7 +103,6 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   const int vec_elems = dtype == SV_BF16 ? 8 : 4;
   const bool vec = (V % vec_elems == 0) && aligned16(target) && (!draft || aligned16(draft));
   const int G = chunks_per_task(dtype, vec);
-  const int Gr = residual_chunks_per_task(dtype, vec);
 
   VerifyParams p;
   memset(&p, 0, sizeof p);
@@ -121,14 +118,14 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.out_cu = out_cu;
   p.out_packed = out_packed;
   p.out_batch_id = out_batch_id;
+  p.mask = mask;
+  p.mask_words = (V + 31) / 32;
+  p.mask_bulk = (mask && vec && aligned16(mask) && p.mask_words % 4 == 0) ? 1 : 0;
   char* base = static_cast<char*>(ws);
-  p.res_ticket = reinterpret_cast<int*>(base + l.res_ticket);
   p.err = reinterpret_cast<int*>(base + l.counters);
   p.fin_ticket = p.err + 1;
-  p.state = reinterpret_cast<ReqState*>(base + l.state);
   p.rec = reinterpret_cast<float2*>(base + l.rec);
   p.lx = reinterpret_cast<float*>(base + l.lx);
-  p.res_rec = reinterpret_cast<float*>(base + l.res_rec);
   p.B = B;
   p.K = K;
   p.V = V;
@@ -136,18 +133,16 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.R = R;
   p.TPR = (p.NC + G - 1) / G;
   p.item_chunks = G;
-  p.TPR_res = (p.NC + Gr - 1) / Gr;
   p.total_tasks = (long long)B * R * p.TPR;
   if (p.total_tasks >= (1LL << 31)) return SV_ERR_SHAPE;
   p.div_tpr = make_fastdiv((uint32_t)p.TPR);
   p.div_r = make_fastdiv((uint32_t)R);
   p.cc = mode == kGreedy ? 0.f : (float)(1.4426950408889634 / (double)T);
   p.greedy_prob = greedy_prob;
-  const bool compact = out_cu || out_packed || out_batch_id;
-  p.compact_in_finalize = compact ? 1 : 0;
+  p.compact_in_finalize = (out_cu || out_packed || out_batch_id) ? 1 : 0;
   p.fin_cache = fin_cache_bytes(p) <= kFinCacheLimit ? 1 : 0;
   if (prepare_workspace(ws, l, B, R, stream) != cudaSuccess) return SV_ERR_CUDA;
-  return launch_verify(mode, dtype, vec, p, compact, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+  return launch_verify(mode, dtype, vec, p, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
 }  // namespace sv
@@ -181,6 +176,38 @@ sv_status spec_verify_sample(const void* target_logits, const void* draft_logits
                        uniforms, temperature, out_tokens, out_accept_len, dtype, B, K, V,
                        draft_lens, out_cu_accept, out_packed, out_batch_id, out_accept_prob,
                        out_status, workspace, ws_bytes, (cudaStream_t)stream, 1);
+}
+
+sv_status spec_verify_sample_masked(const void* target_logits, const void* draft_logits,
+                                    const int32_t* draft_tokens, const float* uniforms,
+                                    float temperature, const uint32_t* token_mask,
+                                    int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype,
+                                    int B, int K, int V, const int32_t* draft_lens,
+                                    int32_t* out_cu_accept, int32_t* out_packed,
+                                    int32_t* out_batch_id, float* out_accept_prob,
+                                    int32_t* out_status, void* workspace, size_t ws_bytes,
+                                    sv_stream_t stream) {
+  if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
+  if (B > 0 && (!token_mask || ((uintptr_t)token_mask & 3u))) return SV_ERR_NULL;
+  const int mode = temperature == 0.f ? kGreedy : (draft_logits ? kDense : kOneHot);
+  return verify_common(mode, target_logits, mode == kDense ? draft_logits : nullptr, draft_tokens,
+                       uniforms, temperature, out_tokens, out_accept_len, dtype, B, K, V,
+                       draft_lens, out_cu_accept, out_packed, out_batch_id, out_accept_prob,
+                       out_status, workspace, ws_bytes, (cudaStream_t)stream, 1, token_mask);
+}
+
+sv_status spec_verify_greedy_masked(const void* target_logits, const int32_t* draft_tokens,
+                                    const uint32_t* token_mask, int32_t* out_tokens,
+                                    int32_t* out_accept_len, sv_dtype dtype, int B, int K, int V,
+                                    const int32_t* draft_lens, int32_t* out_cu_accept,
+                                    int32_t* out_packed, int32_t* out_batch_id,
+                                    int32_t* out_status, void* workspace, size_t ws_bytes,
+                                    sv_stream_t stream) {
+  if (B > 0 && (!token_mask || ((uintptr_t)token_mask & 3u))) return SV_ERR_NULL;
+  return verify_common(kGreedy, target_logits, nullptr, draft_tokens, nullptr, 0.f, out_tokens,
+                       out_accept_len, dtype, B, K, V, draft_lens, out_cu_accept, out_packed,
+                       out_batch_id, nullptr, out_status, workspace, ws_bytes,
+                       (cudaStream_t)stream, 0, token_mask);
 }
 
 sv_status spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens,

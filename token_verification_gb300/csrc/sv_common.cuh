@@ -193,6 +193,19 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           "r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// One arrival that also announces `bytes` of copies, and a copy that only
+// completes bytes (for several copies signalling one barrier phase).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void bulk_copy(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(dst), "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
@@ -259,6 +272,18 @@ struct Lane<uint16_t, 8> {  // bf16, 8 per 128-bit load
     if (q == 2) r.z = (r.z & keep) | ninf;
     if (q == 3) r.w = (r.w & keep) | ninf;
   }
+  // overwrite with -inf every element e whose bit e of `bits` is clear
+  static __device__ __forceinline__ void allow_only(Raw& r, uint32_t bits) {
+    // byte i of flags(n) is 0xff when bit i of the nibble n is set (the four
+    // shifted copies of n in the product do not overlap, so nothing carries)
+    auto flags = [](uint32_t n) { return ((n * 0x00204081u) & 0x01010101u) * 0xffu; };
+    auto keep = [](uint32_t w, uint32_t k) { return (w & k) | (0xff80ff80u & ~k); };
+    const uint32_t lo = flags(bits & 15u), hi = flags((bits >> 4) & 15u);
+    r.x = keep(r.x, __byte_perm(lo, 0, 0x1100));
+    r.y = keep(r.y, __byte_perm(lo, 0, 0x3322));
+    r.z = keep(r.z, __byte_perm(hi, 0, 0x1100));
+    r.w = keep(r.w, __byte_perm(hi, 0, 0x3322));
+  }
 };
 
 template <>
@@ -280,6 +305,12 @@ struct Lane<float, 4> {  // fp32, 4 per 128-bit load
     if (e == 2) r.z = 0xff800000u;
     if (e == 3) r.w = 0xff800000u;
   }
+  static __device__ __forceinline__ void allow_only(Raw& r, uint32_t bits) {
+    r.x = (bits & 1u) ? r.x : 0xff800000u;
+    r.y = (bits & 2u) ? r.y : 0xff800000u;
+    r.z = (bits & 4u) ? r.z : 0xff800000u;
+    r.w = (bits & 8u) ? r.w : 0xff800000u;
+  }
 };
 
 template <>
@@ -294,6 +325,9 @@ struct Lane<uint16_t, 1> {  // bf16, scalar path
     return __uint_as_float((uint32_t)r << 16);
   }
   static __device__ __forceinline__ void kill(Raw& r, int) { r = pad(); }
+  static __device__ __forceinline__ void allow_only(Raw& r, uint32_t bits) {
+    if (!(bits & 1u)) r = pad();
+  }
 };
 
 template <>
@@ -304,6 +338,9 @@ struct Lane<float, 1> {  // fp32, scalar path
   static __device__ __forceinline__ Raw pad() { return -INFINITY; }
   static __device__ __forceinline__ float get(const Raw& r, int) { return r; }
   static __device__ __forceinline__ void kill(Raw& r, int) { r = pad(); }
+  static __device__ __forceinline__ void allow_only(Raw& r, uint32_t bits) {
+    if (!(bits & 1u)) r = pad();
+  }
 };
 
 // one logit, widened to fp32
@@ -316,6 +353,33 @@ __device__ __forceinline__ float load_logit(const float* row, int j) { return __
 template <int VEC>
 __device__ __forceinline__ int tile_offset(int k, int e, int lane) {
   return k * kWarp * VEC + lane * VEC + e;
+}
+
+// ---------------------------------------------------------------------------
+// grammar masks: ceil(V/32) 32-bit words per row; token j is allowed when
+// bit j % 32 of word j / 32 is set.  One chunk's 1024 tokens are 32 words:
+// lane l holds word (chunk * 32 + l).
+// ---------------------------------------------------------------------------
+
+// The chunk's mask word of this lane from global memory (0 past the row).
+__device__ __forceinline__ uint32_t mask_word(const uint32_t* mrow, int words, int c) {
+  const int i = c * kWarp + lane_id();
+  return i < words ? __ldg(mrow + i) : 0u;
+}
+
+// Disallowed elements of this lane's chunk tile become -inf (a warp-wide
+// call: each group's bits come from the lane holding their word).
+template <typename T, int VEC>
+__device__ __forceinline__ void allow_only_chunk(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
+                                                 uint32_t word) {
+  using L = Lane<T, VEC>;
+  const int lane = lane_id();
+#pragma unroll
+  for (int k = 0; k < L::NV; ++k) {
+    const int first = tile_offset<VEC>(k, 0, lane);  // VEC consecutive tokens, one word
+    const uint32_t w = __shfl_sync(0xffffffffu, word, first >> 5);
+    L::allow_only(raw[k], (w >> (first & 31)) & ((1u << VEC) - 1u));
+  }
 }
 
 template <typename T, int VEC>

@@ -20,15 +20,6 @@ struct RowSum {
   int idx;
 };
 
-// A request whose dense-draft residual still has to be drawn.
-struct ReqState {
-  int n;        // rejected position
-  int pending;  // 1 while the residual kernel owes this request its outputs
-  float mp, ip; // target row n: max and 1 / sum
-  float mq, iq; // draft row n: max and 1 / sum
-  int pad0, pad1;
-};
-
 struct VerifyParams {
   const void* target;
   const void* draft;
@@ -42,20 +33,19 @@ struct VerifyParams {
   int* out_cu;
   int* out_packed;
   int* out_batch_id;
+  const uint32_t* mask;  // [B, K+1, mask_words] grammar masks, or null
+  int mask_words;        // ceil(V / 32)
+  int mask_bulk;         // mask rows are 16-byte aligned: copied with the logits
   // workspace
-  int* res_ticket;   // [B]
   int* err;          // [1] set when a bounded wait gave up
   int* fin_ticket;   // [1] requests finalised in this call
-  ReqState* state;   // [B]
   float2* rec;       // [B*R*NC]
   float* lx;         // [B*R] the logit of each row's draft token
-  float* res_rec;    // [B*NC]
   int B, K, V;
   int NC;            // chunks per row
   int R;             // rows per request: K+1 target (+ K draft rows when dense)
   int TPR;           // stream items per row
   int item_chunks;   // chunks per stream item
-  int TPR_res;       // residual tasks per row pair
   long long total_tasks;  // < 2^31 (checked on the host)
   FastDiv div_tpr, div_r; // divide by TPR and by R
   float cc;          // log2(e) / T
@@ -82,7 +72,7 @@ enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Workspace layout for B requests, K positions, V vocabulary (dense case).
 struct WorkspaceLayout {
-  size_t res_ticket, counters, state, zero_bytes, rec, lx, res_rec, total;
+  size_t counters, zero_bytes, rec, lx, total;
 };
 WorkspaceLayout workspace_layout(int B, int K, int V);
 
@@ -91,15 +81,18 @@ struct DeviceInfo {
 };
 cudaError_t device_info(DeviceInfo* out);
 
-// Chunks per stream item (row-statistics kernel) and per residual task.
+// Chunks per stream item (row-statistics kernel).
 int chunks_per_task(int dtype, bool vec);
-// Shared memory the finalize kernel uses to keep a request's chunk records.
+// Shared memory the finalize kernel uses to keep a request's chunk records,
+// and its whole dynamic shared memory (the records when cached, then the
+// residual chunk sums of dense drafts).
 size_t fin_cache_bytes(const VerifyParams& p);
-constexpr size_t kFinCacheLimit = 48 * 1024;  // without the large-shared-memory opt-in
-int residual_chunks_per_task(int dtype, bool vec);
+size_t fin_smem_bytes(const VerifyParams& p, bool dense);
+constexpr size_t kFinCacheLimit = 48 * 1024;
+constexpr size_t kFinSmemMax = kFinCacheLimit + sizeof(float) * ((1 << 24) / kChunk);  // V <= 2^24
 
 // mode: 0 one-hot sampling, 1 dense sampling, 2 greedy
-cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p, bool compact,
+cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream);
 cudaError_t launch_tree(int dtype, bool vec, const TreeParams& p, cudaStream_t stream);
 

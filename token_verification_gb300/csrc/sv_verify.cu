@@ -17,37 +17,35 @@
 // Kernel F (finalize_kernel, one CTA per request) combines each row's chunk
 //   records, runs the acceptance tests of all positions at once (one lane
 //   per position), then draws the residual / bonus token: the crossing chunk
-//   from the records, then one rescan of that single chunk.
-// Kernel B (residual_kernel, dense drafts only): for each request rejected at
-//   n, sums max(0, p_n - q_n) per chunk of the (target, draft) row pair, and
-//   the last warp of the request draws the token the same way.
-// Kernel C (compact_kernel): exclusive scan of accept_len and the packed,
-//   padding-free output with per-token batch ids.
-// F, B and C start with programmatic dependent launch and wait on the device
-// for their predecessor's results.
+//   from the records, then one rescan of that single chunk.  With dense
+//   drafts a request rejected at n first needs the chunk sums of
+//   max(0, p_n - q_n): a cluster of CTAs per request (each one redoing the
+//   cheap acceptance tests) reads the (target, draft) row pair once for
+//   them, writing into the first CTA's shared memory, whose warp 0 then
+//   draws the token the same way.  The last CTA of the call writes the
+//   padding-free packed output (exclusive scan of accept_len, packed tokens,
+//   per-token batch ids).
+// F starts with programmatic dependent launch and waits on the device for
+// kernel A's records.
+#include <cooperative_groups.h>
+
 #include "sv_common.cuh"
 #include "sv_launch.h"
 
 namespace sv {
 namespace {
 
+namespace cg = cooperative_groups;
+
 template <typename T>
 __device__ __forceinline__ const T* row_ptr(const void* base, long long row, int V) {
   return reinterpret_cast<const T*>(base) + row * (long long)V;
 }
 
-__device__ __forceinline__ ReqState load_state(const ReqState* p) {
-  const int4 a = __ldcg(reinterpret_cast<const int4*>(p));
-  const int4 b = __ldcg(reinterpret_cast<const int4*>(p) + 1);
-  ReqState s;
-  s.n = a.x;
-  s.pending = a.y;
-  s.mp = __int_as_float(a.z);
-  s.ip = __int_as_float(a.w);
-  s.mq = __int_as_float(b.x);
-  s.iq = __int_as_float(b.y);
-  s.pad0 = s.pad1 = 0;
-  return s;
+// Grammar mask row of position i of request b (target row i and dense
+// draft row i share it), or null without masks.
+__device__ __forceinline__ const uint32_t* mask_row(const VerifyParams& p, int b, int i) {
+  return p.mask ? p.mask + ((long long)b * (p.K + 1) + i) * p.mask_words : nullptr;
 }
 
 // ---------------------------------------------------------------------------
@@ -151,12 +149,13 @@ __device__ int select_in_tile(const float (&w)[NV * VEC], const float (&gsum)[NV
   return tok;
 }
 
-// Draw from w_j = 2^((l_j - m) c) over one row (w = 0 at mask_x) given the
-// row's softmax chunk records: the crossing chunk from the records, then one
-// rescan of that chunk in its own frame.
+// Draw from w_j = 2^((l_j - m) c) over one row (w = 0 at mask_x and at the
+// tokens the grammar mask row `mrow` rules out) given the row's softmax
+// chunk records: the crossing chunk from the records, then one rescan of
+// that chunk in its own frame.
 template <typename T, int VEC, bool kSharedRecords = false>
 __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V, float m, float cc,
-                                 float u, int mask_x) {
+                                 float u, int mask_x, const uint32_t* mrow, int mask_words) {
   using L = Lane<T, VEC>;
   const int lane = lane_id();
   const float nb = -m * cc;
@@ -180,6 +179,7 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
   if (c < 0) return -1;
   typename L::Raw raw[L::NV];
   load_chunk<T, VEC>(row, V, c, raw);
+  if (mrow) allow_only_chunk<T, VEC>(raw, mask_word(mrow, mask_words, c));
   const float nbc = -record(c).x * cc;
   float w[L::NV * VEC];
   float gsum[L::NV];
@@ -246,19 +246,27 @@ __device__ int block_excl_scan(int v, int* smem) {
 
 // Exclusive scan of accept_len, packed tokens and per-token batch ids, by
 // one CTA over all B requests (their outputs are complete and visible).
+// Each thread reads all of its request's tokens before writing any, so the
+// copy costs one memory round trip.
 __device__ void compact_all(const VerifyParams& p, int* smem) {
   const int B = p.B, W = p.K + 1;
   int offset = 0;
   for (int b0 = 0; b0 < B; b0 += blockDim.x) {
     const int b = b0 + threadIdx.x;
     const int L = b < B ? __ldcg(p.out_accept_len + b) : 0;
+    int tok[kMaxK + 1];
+#pragma unroll
+    for (int k = 0; k <= kMaxK; ++k)
+      tok[k] = (p.out_packed && k < L) ? __ldcg(p.out_tokens + (long long)b * W + k) : -1;
     const int cu = offset + block_excl_scan(L, smem);
     if (b < B) {
       if (p.out_cu) p.out_cu[b] = cu;
-      for (int k = 0; k < L; ++k) {
-        if (p.out_packed) p.out_packed[cu + k] = __ldcg(p.out_tokens + (long long)b * W + k);
-        if (p.out_batch_id) p.out_batch_id[cu + k] = b;
-      }
+#pragma unroll
+      for (int k = 0; k <= kMaxK; ++k)
+        if (k < L) {
+          if (p.out_packed) p.out_packed[cu + k] = tok[k];
+          if (p.out_batch_id) p.out_batch_id[cu + k] = b;
+        }
     }
     offset += block_sum(L, smem);
   }
@@ -302,13 +310,29 @@ __device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb, int
   return rs;
 }
 
-constexpr int kFinThreads = 256;
+// Threads of a finalize CTA: 16 warps where a rejected request reads its
+// dense row pair, 8 elsewhere.
+template <int MODE>
+__host__ __device__ constexpr int fin_threads() { return MODE == kDense ? 512 : 256; }
 constexpr int kMaxRows = 2 * kMaxK + 1;
+
+// The rejected position of a dense-draft request and its two rows' maxima
+// and reciprocal sums (n < 0: nothing left to draw).
+struct Residual {
+  int n;
+  float mp, ip, mq, iq;
+};
 
 template <int MODE, typename T, int VEC>
 __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const float2* srec, int x,
-                                              float u, float uK);
+                                              float u, float uK, Residual* resid);
+template <typename T, int VEC>
+__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
+                                           float* sums, int rank, int ncta);
+template <typename T, int VEC>
+__device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const Residual& st,
+                                           const float* sums, const float2* srec);
 
 // Draft token of row r of request b, or -1 (rows without one, or K_b invalid).
 __device__ __forceinline__ int row_token(const VerifyParams& p, int b, int r, int Kb) {
@@ -321,14 +345,29 @@ __device__ __forceinline__ int row_token(const VerifyParams& p, int b, int r, in
 // then the residual / bonus draw (rejection sampling, [SD] §2.1) or the
 // argmax (greedy).  Rows are summarised by the CTA's warps first; their chunk
 // records are kept in shared memory (dynamic, when they fit) for the draw.
+// Dynamic shared memory: [R*NC] records when cached, then [NC] residual
+// chunk sums (dense drafts).  Dense calls may run a cluster of CTAs per
+// request: the first one does all of the above and writes the outputs; the
+// others only help to read the rejected row pair.
 template <int MODE, typename T, int VEC>
-__global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParams p) {
-  extern __shared__ float2 s_rec[];
+__global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const VerifyParams p) {
+  constexpr int kWarps = fin_threads<MODE>() / kWarp;
+  extern __shared__ float2 s_dyn[];
   __shared__ RowSum srow[kMaxRows];
+  __shared__ Residual s_resid;
   __shared__ int s_last[32];
-  const int b = blockIdx.x;
+  int ncta = 1, rank = 0;
+  if (MODE == kDense) {
+    const cg::cluster_group cluster = cg::this_cluster();
+    ncta = (int)cluster.num_blocks();
+    rank = (int)cluster.block_rank();
+  }
+  const int b = blockIdx.x / ncta;
+  const bool leader = rank == 0;
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const int K = p.K;
+  float2* s_rec = p.fin_cache ? s_dyn : nullptr;
+  float* s_sums = reinterpret_cast<float*>(s_dyn + (p.fin_cache ? (long long)p.R * p.NC : 0));
   // The request's inputs do not depend on kernel A: read them before waiting.
   const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
   const int Kv = (Kb >= 0 && Kb <= K) ? Kb : 0;
@@ -342,19 +381,43 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParam
       uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
     }
   }
+  if (threadIdx.x == 0) s_resid.n = -1;
   pdl_wait();
   pdl_launch_dependents();
-  for (int r = warp; r < p.R; r += kFinThreads / kWarp) {
-    RowSum rs{qnan(), 0.f, 0.f, -1};
-    if (row_needed(p, r, Kb))
-      rs = summarise_row<MODE, T>(p, b, r, Kb, r == warp ? x0 : row_token(p, b, r, Kb),
-                                  p.fin_cache ? s_rec + (long long)r * p.NC : nullptr);
-    if (lane == 0) srow[r] = rs;
+  if (leader) {
+    for (int r = warp; r < p.R; r += kWarps) {
+      RowSum rs{qnan(), 0.f, 0.f, -1};
+      if (row_needed(p, r, Kb))
+        rs = summarise_row<MODE, T>(p, b, r, Kb, r == warp ? x0 : row_token(p, b, r, Kb),
+                                    s_rec ? s_rec + (long long)r * p.NC : nullptr);
+      if (lane == 0) srow[r] = rs;
+    }
+    __syncthreads();
+    if (warp == 0) finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_rec, x, u, uK, &s_resid);
   }
-  __syncthreads();
-  if (warp == 0) finalize_request<MODE, T, VEC>(p, b, Kb, srow, p.fin_cache ? s_rec : nullptr, x, u, uK);
-  // The last CTA of the call clears its counters and, unless the dense
-  // residual kernel still owes outputs, writes the packed output.
+  if (MODE == kDense) {
+    // Dense drafts: the request's CTAs learn n from the first one, read the
+    // rejected row pair for the residual chunk sums, and the first CTA draws.
+    // Both cluster barriers are passed by every thread of every CTA.
+    cg::cluster_group cluster = cg::this_cluster();
+    if (ncta > 1) {
+      cluster.sync();
+      if (!leader && threadIdx.x == 0) s_resid = *cluster.map_shared_rank(&s_resid, 0);
+    }
+    __syncthreads();
+    const Residual st = s_resid;
+    if (st.n >= 0)
+      residual_sums<T, VEC>(p, b, st, ncta > 1 ? cluster.map_shared_rank(s_sums, 0) : s_sums,
+                            rank, ncta);
+    if (ncta > 1)
+      cluster.sync();  // every sum is in the first CTA's shared memory
+    else
+      __syncthreads();
+    if (leader && warp == 0 && st.n >= 0) residual_pick<T, VEC>(p, b, st, s_sums, s_rec);
+  }
+  if (!leader) return;
+  // The last request of the call clears the counters and writes the packed
+  // output.
   __syncthreads();
   if (threadIdx.x == 0) s_last[0] = atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B;
   __syncthreads();
@@ -363,13 +426,13 @@ __global__ void __launch_bounds__(kFinThreads) finalize_kernel(const VerifyParam
     *p.err = 0;
     *p.fin_ticket = 0;
   }
-  if (MODE != kDense && p.compact_in_finalize) compact_all(p, s_last);
+  if (p.compact_in_finalize) compact_all(p, s_last);
 }
 
 template <int MODE, typename T, int VEC>
 __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const float2* srec, int x,
-                                              float u, float uK) {
+                                              float u, float uK, Residual* resid) {
   const int lane = lane_id();
   const int K = p.K;
   // A bounded wait that gave up in kernel A (a device fault) invalidates the
@@ -419,29 +482,21 @@ __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int 
       if (MODE == kGreedy) {
         token = idx_n;
       } else if (MODE == kDense && n < Kb) {
-        pending = true;  // the residual kernel draws from max(0, p_n - q_n)
-        if (lane == 0) {
-          ReqState st;
-          st.n = n;
-          st.pending = 1;
-          st.mp = m_n;
-          st.ip = 1.f / s_n;
-          st.mq = mq_n;
-          st.iq = 1.f / sq_n;
-          st.pad0 = st.pad1 = 0;
-          p.state[b] = st;
-        }
+        pending = true;  // the whole CTA draws from max(0, p_n - q_n) next
+        if (lane == 0) *resid = Residual{n, m_n, 1.f / s_n, mq_n, 1.f / sq_n};
       } else {
         const bool residual = MODE == kOneHot && n < Kb;
         if (residual && !(s_n > 0.f)) {
           token = x_n;  // no mass left beside x_n: p_n itself is the point mass at x_n
         } else {
           const T* row = row_ptr<T>(p.target, (long long)b * (K + 1) + n, p.V);
+          const uint32_t* mrow = mask_row(p, b, n);
           token = srec ? draw_from_records<T, VEC, true>(row, srec + (long long)n * p.NC, p.NC,
-                                                         p.V, m_n, p.cc, uK, residual ? x_n : -1)
+                                                         p.V, m_n, p.cc, uK, residual ? x_n : -1,
+                                                         mrow, p.mask_words)
                        : draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + n) * p.NC,
-                                                   p.NC, p.V, m_n, p.cc, uK,
-                                                   residual ? x_n : -1);
+                                                   p.NC, p.V, m_n, p.cc, uK, residual ? x_n : -1,
+                                                   mrow, p.mask_words);
           if (token < 0) status = kBadLogits;
         }
       }
@@ -514,6 +569,15 @@ __device__ __forceinline__ const T* item_row(const VerifyParams& p, int rowid) {
                  : row_ptr<T>(p.target, (long long)b * (p.K + 1) + r, p.V);
 }
 
+// The grammar mask row of a logit row (target row i or draft row i of
+// request b: the mask of position i), or null without masks.
+__device__ __forceinline__ const uint32_t* item_mask(const VerifyParams& p, int rowid) {
+  if (!p.mask) return nullptr;
+  const int b = (int)fast_div((uint32_t)rowid, p.div_r);
+  const int r = rowid - b * p.R;
+  return mask_row(p, b, r > p.K ? r - p.K - 1 : r);
+}
+
 // Register-tile variant (scalar path: any V, any alignment): warps stride
 // over items of G chunks.
 template <int MODE, typename T, int VEC>
@@ -528,14 +592,20 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
     const Item k = decode_item<MODE>(p, (uint32_t)t);
     if (!k.need) continue;
     const T* row = item_row<T>(p, k.rowid);
+    const uint32_t* mrow = item_mask(p, k.rowid);
     typename L::Raw raw[G][L::NV];
+    uint32_t word[G];
 #pragma unroll
     for (int g = 0; g < G; ++g)
-      if (g < k.nch) load_chunk<T, VEC>(row, p.V, k.c0 + g, raw[g]);
+      if (g < k.nch) {
+        load_chunk<T, VEC>(row, p.V, k.c0 + g, raw[g]);
+        if (mrow) word[g] = mask_word(mrow, p.mask_words, k.c0 + g);
+      }
     float2* rec = p.rec + (long long)k.rowid * p.NC;
 #pragma unroll
     for (int g = 0; g < G; ++g)
       if (g < k.nch) {
+        if (mrow) allow_only_chunk<T, VEC>(raw[g], word[g]);
         record_draft_logit<T, VEC>(p, raw[g], k.c0 + g, k.rowid, k.x);
         const float2 out =
             chunk_record<MODE, T, VEC>(raw[g], k.c0 + g, p.cc, MODE == kOneHot ? k.x : -1);
@@ -562,14 +632,22 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
 constexpr int kStreamThreads = 512;
 constexpr int kConsumers = kStreamThreads / kWarp - 1;  // 15
 
+// Shared memory: kStages logit stages, their (full, empty) barrier pairs,
+// their item descriptions and, for masked calls, the stages' mask words
+// (32 words per chunk).
 template <typename T>
 struct Stream {
   static constexpr int kChunkBytes = kChunk * (int)sizeof(T);
   static constexpr int kStageBytes = kConsumers * kChunkBytes;
+  static constexpr int kMaskChunkBytes = kChunk / 8;
+  static constexpr int kMaskStageBytes = kConsumers * kMaskChunkBytes;
   static constexpr int kStages = sizeof(T) == 2 ? SV_STREAM_STAGES_BF16 : SV_STREAM_STAGES_F32;
   static constexpr int kBarOffset = kStages * kStageBytes;
   static constexpr int kMetaOffset = kBarOffset + kStages * 16;
-  static constexpr int smem_bytes() { return kMetaOffset + kStages * 16; }
+  static constexpr int kMaskOffset = kMetaOffset + kStages * 16;
+  static constexpr int smem_bytes(bool masked) {
+    return kMaskOffset + (masked ? kStages * kMaskStageBytes : 0);
+  }
 };
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -588,6 +666,7 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
   auto stage_of = [&](int s) { return base + s * ST::kStageBytes; };
   auto full_of = [&](int s) { return base + ST::kBarOffset + s * 16; };
   auto empty_of = [&](int s) { return full_of(s) + 8; };
+  auto mask_of = [&](int s) { return base + ST::kMaskOffset + s * ST::kMaskStageBytes; };
   int4* meta = reinterpret_cast<int4*>(smem + ST::kMetaOffset);
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -622,7 +701,15 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
       const T* src = item_row<T>(p, item.rowid) + (long long)item.c0 * kChunk;
       const uint32_t bytes =
           (uint32_t)(min(item.nch * kChunk, p.V - item.c0 * kChunk) * (int)sizeof(T));
-      bulk_load(stage_of(s), src, bytes, full_of(s));
+      if (p.mask_bulk) {  // the item's mask words travel with its logits
+        const int w0 = item.c0 * kWarp;
+        const uint32_t mbytes = (uint32_t)(min(item.nch * kWarp, p.mask_words - w0) * 4);
+        mbar_arrive_expect_tx(full_of(s), bytes + mbytes);
+        bulk_copy(stage_of(s), src, bytes, full_of(s));
+        bulk_copy(mask_of(s), item_mask(p, item.rowid) + w0, mbytes, full_of(s));
+      } else {
+        bulk_load(stage_of(s), src, bytes, full_of(s));
+      }
       ++k;
     }
     // end marker (a stage whose full barrier completes without a copy)
@@ -659,6 +746,15 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
       const int c = m.y + w;
       typename L::Raw raw[L::NV];
       load_chunk_smem<T, VEC>(stage_of(s) + w * ST::kChunkBytes, p.V, c, raw);
+      if (p.mask) {
+        uint32_t word = 0;
+        if (c * kWarp + lane < p.mask_words)
+          word = p.mask_bulk ? reinterpret_cast<const uint32_t*>(
+                                   smem + ST::kMaskOffset + s * ST::kMaskStageBytes +
+                                   w * ST::kMaskChunkBytes)[lane]
+                             : __ldg(item_mask(p, m.x) + c * kWarp + lane);
+        allow_only_chunk<T, VEC>(raw, word);
+      }
       record_draft_logit<T, VEC>(p, raw, c, m.x, m.w);
       const float2 out = chunk_record<MODE, T, VEC>(raw, c, p.cc, MODE == kOneHot ? m.w : -1);
       if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
@@ -670,41 +766,105 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
 }
 
 // ---------------------------------------------------------------------------
-// kernel B: dense-draft residual
+// dense-draft residual (inside kernel F, by all warps of the request's CTA)
 // ---------------------------------------------------------------------------
 
 template <typename T, int VEC>
-__device__ __noinline__ void residual_finalize(const VerifyParams& p, int b, const ReqState& st) {
+__host__ __device__ constexpr int residual_group() {
+  return Lane<T, VEC>::G > 1 ? Lane<T, VEC>::G / 2 : 1;
+}
+
+// Request b was rejected at st.n: the chunk sums of max(0, p_n - q_n) over
+// the (target, draft) row pair.  CTA `rank` of the request's `ncta` takes a
+// contiguous range of chunks, its warps groups of consecutive chunks; each
+// sum goes to sums[c] (the first CTA's shared memory).  Called by every
+// thread of the CTA.
+template <typename T, int VEC>
+__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
+                                           float* sums, int rank, int ncta) {
   using L = Lane<T, VEC>;
-  const int lane = lane_id();
-  const int K = p.K;
+  constexpr int G = residual_group<T, VEC>();
+  const int lane = lane_id(), warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int K = p.K, NC = p.NC;
   const float cc = p.cc;
-  const float uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
   const T* tr = row_ptr<T>(p.target, (long long)b * (K + 1) + st.n, p.V);
   const T* dr = row_ptr<T>(p.draft, (long long)b * K + st.n, p.V);
-  const float* rr = p.res_rec + (long long)b * p.NC;
-  auto weight = [&](int c) { return __ldcg(rr + c); };
+  const float nbp = -st.mp * cc, nbq = -st.mq * cc;
+  const int lo = (int)((long long)NC * rank / ncta);
+  const int hi = (int)((long long)NC * (rank + 1) / ncta);
+  const uint32_t* mrow = mask_row(p, b, st.n);
+  for (int c0 = lo + warp * G; c0 < hi; c0 += nwarps * G) {
+    typename L::Raw rt[G][L::NV], rd[G][L::NV];
+    uint32_t word[G];
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (c0 + g < hi) {
+        load_chunk<T, VEC>(tr, p.V, c0 + g, rt[g]);
+        load_chunk<T, VEC>(dr, p.V, c0 + g, rd[g]);
+        if (mrow) word[g] = mask_word(mrow, p.mask_words, c0 + g);
+      }
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+      if (c0 + g < hi) {
+        if (mrow) {
+          allow_only_chunk<T, VEC>(rt[g], word[g]);
+          allow_only_chunk<T, VEC>(rd[g], word[g]);
+        }
+        float w = 0.f;
+#pragma unroll
+        for (int k = 0; k < L::NV; ++k)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e)
+            w += residual_weight(L::get(rt[g][k], e), L::get(rd[g][k], e), cc, nbp, st.ip, nbq,
+                                 st.iq);
+        w = warp_sum(w);
+        if (lane == 0) sums[c0 + g] = w;
+      }
+  }
+}
+
+// One warp: the residual draw from the chunk sums (the crossing chunk, then
+// a rescan of that chunk of both rows), and the request's outputs.
+template <typename T, int VEC>
+__device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const Residual& st,
+                                           const float* sums, const float2* srec) {
+  using L = Lane<T, VEC>;
+  const int lane = lane_id();
+  const int K = p.K, NC = p.NC;
+  const float cc = p.cc;
+  const T* tr = row_ptr<T>(p.target, (long long)b * (K + 1) + st.n, p.V);
+  const T* dr = row_ptr<T>(p.draft, (long long)b * K + st.n, p.V);
+  const float nbp = -st.mp * cc, nbq = -st.mq * cc;
+  const float uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
+  const uint32_t* mrow = mask_row(p, b, st.n);
+  auto weight = [&](int c) { return sums[c]; };
   float wc[kRecCache];
   float tot = 0.f;
 #pragma unroll
   for (int t = 0; t < kRecCache; ++t) {
     const int c = lane + t * kWarp;
-    wc[t] = c < p.NC ? weight(c) : 0.f;
+    wc[t] = c < NC ? weight(c) : 0.f;
     tot += wc[t];
   }
-  for (int c = lane + kRecCache * kWarp; c < p.NC; c += kWarp) tot += weight(c);
+  for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
   tot = warp_sum(tot);
   int token;
   if (!(tot > 0.f)) {  // no residual mass (rounding only): draw from p_n
-    token = draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * p.NC, p.NC, p.V,
-                                      st.mp, cc, uK, -1);
+    token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V, st.mp,
+                                                   cc, uK, -1, mrow, p.mask_words)
+                 : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
+                                             p.V, st.mp, cc, uK, -1, mrow, p.mask_words);
   } else {
     float frac = 0.f;
-    const int c = find_chunk(wc, weight, p.NC, uK * tot, &frac);
+    const int c = find_chunk(wc, weight, NC, uK * tot, &frac);
     typename L::Raw rt[L::NV], rd[L::NV];
     load_chunk<T, VEC>(tr, p.V, c, rt);
     load_chunk<T, VEC>(dr, p.V, c, rd);
-    const float nbp = -st.mp * cc, nbq = -st.mq * cc;
+    if (mrow) {
+      const uint32_t word = mask_word(mrow, p.mask_words, c);
+      allow_only_chunk<T, VEC>(rt, word);
+      allow_only_chunk<T, VEC>(rd, word);
+    }
     float w[L::NV * VEC];
     float gsum[L::NV];
 #pragma unroll
@@ -712,8 +872,8 @@ __device__ __noinline__ void residual_finalize(const VerifyParams& p, int b, con
       gsum[k] = 0.f;
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float we = residual_weight(L::get(rt[k], e), L::get(rd[k], e), cc, nbp, st.ip, nbq,
-                                         st.iq);
+        const float we =
+            residual_weight(L::get(rt[k], e), L::get(rd[k], e), cc, nbp, st.ip, nbq, st.iq);
         w[k * VEC + e] = we;
         gsum[k] += we;
       }
@@ -722,100 +882,6 @@ __device__ __noinline__ void residual_finalize(const VerifyParams& p, int b, con
   }
   const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
   write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
-  if (lane == 0) {
-    p.res_ticket[b] = 0;
-    p.state[b].pending = 0;
-  }
-}
-
-template <typename T, int VEC>
-__host__ __device__ constexpr int residual_group() {
-  return Lane<T, VEC>::G > 1 ? Lane<T, VEC>::G / 2 : 1;
-}
-
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kThreads, 2) residual_kernel(const VerifyParams p) {
-  using L = Lane<T, VEC>;
-  constexpr int G = residual_group<T, VEC>();
-  pdl_wait();
-  pdl_launch_dependents();
-  const int lane = lane_id();
-  const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
-  const long long total = (long long)p.B * p.TPR_res;
-  const float cc = p.cc;
-  for (long long t = gw; t < total; t += nw) {
-    const int b = (int)(t / p.TPR_res);
-    const int tc = (int)(t % p.TPR_res);
-    const ReqState st = load_state(p.state + b);
-    if (!st.pending || st.n < 0 || st.n >= p.K) continue;
-    const T* tr = row_ptr<T>(p.target, (long long)b * (p.K + 1) + st.n, p.V);
-    const T* dr = row_ptr<T>(p.draft, (long long)b * p.K + st.n, p.V);
-    const int c0 = tc * G;
-    const int nch = min(G, p.NC - c0);
-    typename L::Raw rt[G][L::NV], rd[G][L::NV];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (g < nch) {
-        load_chunk<T, VEC>(tr, p.V, c0 + g, rt[g]);
-        load_chunk<T, VEC>(dr, p.V, c0 + g, rd[g]);
-      }
-    const float nbp = -st.mp * cc, nbq = -st.mq * cc;
-#pragma unroll
-    for (int g = 0; g < G; ++g) {
-      if (g < nch) {
-        float s = 0.f;
-#pragma unroll
-        for (int k = 0; k < L::NV; ++k)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            s += residual_weight(L::get(rt[g][k], e), L::get(rd[g][k], e), cc, nbp, st.ip, nbq,
-                                 st.iq);
-        s = warp_sum(s);
-        if (lane == 0) p.res_rec[(long long)b * p.NC + c0 + g] = s;
-      }
-    }
-    int old = 0;
-    if (lane == 0) old = atomic_add_acq_rel(p.res_ticket + b, nch);
-    old = __shfl_sync(0xffffffffu, old, 0);
-    if (old + nch == p.NC) residual_finalize<T, VEC>(p, b, st);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// kernel C: padding-free packed output
-// ---------------------------------------------------------------------------
-
-__global__ void compact_kernel(const VerifyParams p) {
-  __shared__ int smem[32];
-  pdl_wait();
-  const int B = p.B, W = p.K + 1;
-  const int b0 = blockIdx.x * blockDim.x;
-  int before = 0, all = 0;
-  for (int b = threadIdx.x; b < B; b += blockDim.x) {
-    const int L = __ldcg(p.out_accept_len + b);
-    all += L;
-    if (b < b0) before += L;
-  }
-  before = block_sum(before, smem);
-  all = block_sum(all, smem);
-  const int b = b0 + threadIdx.x;
-  const int L = b < B ? __ldcg(p.out_accept_len + b) : 0;
-  const int cu = before + block_excl_scan(L, smem);
-  if (b < B) {
-    if (p.out_cu) p.out_cu[b] = cu;
-    for (int k = 0; k < L; ++k) {
-      if (p.out_packed) p.out_packed[cu + k] = __ldcg(p.out_tokens + (long long)b * W + k);
-      if (p.out_batch_id) p.out_batch_id[cu + k] = b;
-    }
-  }
-  if (p.out_cu && blockIdx.x == 0 && threadIdx.x == 0) p.out_cu[B] = all;
-  const long long cap = (long long)B * W;
-  for (long long s = all + (long long)blockIdx.x * blockDim.x + threadIdx.x; s < cap;
-       s += (long long)gridDim.x * blockDim.x) {
-    if (p.out_packed) p.out_packed[s] = -1;
-    if (p.out_batch_id) p.out_batch_id[s] = -1;
-  }
 }
 
 // ---------------------------------------------------------------------------
@@ -831,22 +897,37 @@ int blocks_per_sm(K kernel) {
 }
 
 cudaError_t launch_pdl(const void* fn, dim3 grid, dim3 block, cudaStream_t s, void** args,
-                       size_t smem = 0) {
+                       size_t smem = 0, int cluster = 1) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = grid;
   cfg.blockDim = block;
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cluster > 1) {
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cluster;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
+  }
   return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// CTAs per request for the dense-draft residual: enough to cover the SMs
+// with one CTA each, at most one per 32 chunks of the row, at most 8.
+int residual_cluster(const VerifyParams& p, int sms) {
+  int c = p.B > 0 ? sms / p.B : 1;
+  c = c < (p.NC + 31) / 32 ? c : (p.NC + 31) / 32;
+  return c < 1 ? 1 : (c > 8 ? 8 : c);
+}
+
 template <int MODE, typename T, int VEC>
-cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
+cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
   DeviceInfo di;
   cudaError_t err = device_info(&di);
   if (err != cudaSuccess) return err;
@@ -854,14 +935,15 @@ cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
   void* args[] = {&pc};
   // A: chunk records
   if constexpr (VEC * sizeof(T) == 16) {
-    constexpr int smem = Stream<T>::smem_bytes();
+    constexpr int smem_max = Stream<T>::smem_bytes(true);
+    const int smem = Stream<T>::smem_bytes(p.mask_bulk != 0);
     static int occ = 0;
     if (!occ) {
       err = cudaFuncSetAttribute(verify_stream_kernel<MODE, T, VEC>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
       if (err != cudaSuccess) return err;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-              &occ, verify_stream_kernel<MODE, T, VEC>, kStreamThreads, smem) != cudaSuccess ||
+              &occ, verify_stream_kernel<MODE, T, VEC>, kStreamThreads, smem_max) != cudaSuccess ||
           occ < 1)
         occ = 1;
     }
@@ -880,60 +962,45 @@ cudaError_t launch_typed(const VerifyParams& p, bool compact, cudaStream_t s) {
   err = cudaGetLastError();
   if (err != cudaSuccess) return err;
   // F: acceptance tests and draws, one CTA per request
-  err = launch_pdl(reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>), dim3(p.B),
-                   dim3(kFinThreads), s, args, p.fin_cache ? fin_cache_bytes(p) : 0);
-  if (err != cudaSuccess) return err;
-  // B: dense residual draws
-  if (MODE == kDense) {
-    static int occ = 0;
-    if (!occ) occ = blocks_per_sm(residual_kernel<T, VEC>);
-    const int warps_per_cta = kThreads / kWarp;
-    const long long want = ((long long)p.B * p.TPR_res + warps_per_cta - 1) / warps_per_cta;
-    const long long cap = (long long)di.sms * occ;
-    const int grid = (int)(want < cap ? want : cap);
-    err = launch_pdl(reinterpret_cast<const void*>(residual_kernel<T, VEC>), dim3(grid),
-                     dim3(kThreads), s, args);
+  const void* fin = reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>);
+  const size_t fin_smem = fin_smem_bytes(p, MODE == kDense);
+  static bool fin_attr = false;
+  if (!fin_attr) {
+    err = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kFinSmemMax);
     if (err != cudaSuccess) return err;
+    fin_attr = true;
   }
-  // C: padding-free packed output (one-hot and greedy calls build it in F)
-  if (compact && MODE == kDense) {
-    const int threads = p.B >= 1024 ? 1024 : ((p.B + kWarp - 1) / kWarp) * kWarp;
-    const int grid = (p.B + threads - 1) / threads;
-    err = launch_pdl(reinterpret_cast<const void*>(compact_kernel), dim3(grid), dim3(threads), s,
-                     args);
-    if (err != cudaSuccess) return err;
-  }
-  return cudaSuccess;
+  const int ncta = MODE == kDense ? residual_cluster(p, di.sms) : 1;
+  return launch_pdl(fin, dim3(p.B * ncta), dim3(fin_threads<MODE>()), s, args, fin_smem, ncta);
 }
 
 template <int MODE>
-cudaError_t launch_mode(int dtype, bool vec, const VerifyParams& p, bool compact, cudaStream_t s) {
+cudaError_t launch_mode(int dtype, bool vec, const VerifyParams& p, cudaStream_t s) {
   if (dtype == kBF16)
-    return vec ? launch_typed<MODE, uint16_t, 8>(p, compact, s)
-               : launch_typed<MODE, uint16_t, 1>(p, compact, s);
-  return vec ? launch_typed<MODE, float, 4>(p, compact, s) : launch_typed<MODE, float, 1>(p, compact, s);
+    return vec ? launch_typed<MODE, uint16_t, 8>(p, s) : launch_typed<MODE, uint16_t, 1>(p, s);
+  return vec ? launch_typed<MODE, float, 4>(p, s) : launch_typed<MODE, float, 1>(p, s);
 }
 
 }  // namespace
 
 size_t fin_cache_bytes(const VerifyParams& p) { return sizeof(float2) * (size_t)p.R * p.NC; }
 
+size_t fin_smem_bytes(const VerifyParams& p, bool dense) {
+  return (p.fin_cache ? fin_cache_bytes(p) : 0) + (dense ? sizeof(float) * (size_t)p.NC : 0);
+}
+
 int chunks_per_task(int dtype, bool vec) {
   if (vec) return kConsumers;
   return Lane<float, 1>::G;
 }
 
-int residual_chunks_per_task(int dtype, bool vec) {
-  if (!vec) return residual_group<float, 1>();
-  return dtype == kBF16 ? residual_group<uint16_t, 8>() : residual_group<float, 4>();
-}
-
-cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p, bool compact,
+cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream) {
   switch (mode) {
-    case kOneHot: return launch_mode<kOneHot>(dtype, vec, p, compact, stream);
-    case kDense: return launch_mode<kDense>(dtype, vec, p, compact, stream);
-    default: return launch_mode<kGreedy>(dtype, vec, p, compact, stream);
+    case kOneHot: return launch_mode<kOneHot>(dtype, vec, p, stream);
+    case kDense: return launch_mode<kDense>(dtype, vec, p, stream);
+    default: return launch_mode<kGreedy>(dtype, vec, p, stream);
   }
 }
 
