@@ -34,6 +34,7 @@ BAD_LOGITS = 2
 BAD_DRAFT_LEN = 4
 FLAG_ACCEPT = 1
 FLAG_CDF = 2
+FLAG_CUT = 4
 FLAG_TOL = 1e-5
 
 
@@ -73,7 +74,7 @@ def configure(lib):
     lib.sv_oracle_greedy.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
     lib.sv_oracle_greedy.restype = I
     lib.sv_oracle_sample.argtypes = [P, P, I, P, P, P, D, I, I, I, I, I, P, P, P, P, P, P, P, P,
-                                     P]
+                                     P, I, D]
     lib.sv_oracle_sample.restype = I
     lib.sv_oracle_tree.argtypes = [P, I, P, P, I, I, I, I, I, I, P, P, P, P]
     lib.sv_oracle_tree.restype = I
@@ -155,7 +156,7 @@ def inverse_cdf(weights, u):
 # ---------------------------------------------------------------------------
 
 def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=None,
-           threads=1, b_range=None, probe_tokens=None, token_mask=None):
+           threads=1, b_range=None, probe_tokens=None, token_mask=None, top_k=0, top_p=1.0):
     """Rejection-sampling verify (temperature 0 = greedy rule).
 
     target [B, K+1, V], draft [B, K, V] or None (one-hot drafts),
@@ -163,6 +164,9 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
     draft_lens [B] or None.  Requests outside ``b_range`` keep -1 / 0.
     token_mask [B, K+1, ceil(V/32)] int32 / uint32 or None: grammar masks
     (bit j % 32 of word j // 32 set = token j allowed at that position).
+    top_k (0 = off) and top_p (1.0 = off) filter every sampled distribution,
+    target and dense draft alike; flags gain FLAG_CUT where a top-p cut is
+    within FLAG_TOL of moving.
     Returns a dict of numpy arrays: tokens, accept_len, accept_prob, flags,
     margins, status (and probe [B, 2] when probe_tokens [B] is given: the
     normalised CDF step of that token in the request's final draw).
@@ -192,7 +196,8 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
             _ptr(target), _ptr(draft), dt, _ptr(toks), _ptr(lens), _ptr(u),
             float(temperature), B, K, V, lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
             _ptr(out["accept_prob"]), _ptr(out["flags"]), _ptr(out["margins"]),
-            _ptr(out["status"]), _ptr(probes), _ptr(out.get("probe")), _ptr(mask))
+            _ptr(out["status"]), _ptr(probes), _ptr(out.get("probe")), _ptr(mask), int(top_k),
+            float(top_p))
 
     _run(fn, B, threads, b_range)
     return out

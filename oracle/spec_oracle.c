@@ -19,6 +19,10 @@
  *   [LD]   "Speculative Decoding" (LMDeploy docs), "投机解码与结构化输出",
  *          "工作原理" (grammar masks applied to the target logits of every
  *          verified position, and to the draft's).
+ *   [VA]   "Speculative Decoding Guide" (vLLM Ascend docs): the examples'
+ *          SamplingParams(temperature=0.8, top_p=0.95) (top-p filtering of
+ *          the sampled distributions), with "推测解码与 MTP" §8.3 (non-greedy
+ *          decoding with wide top-p).
  *
  * Every quantity is computed in double precision, one request at a time,
  * with plain serial loops: no blocking, fusion or reordering.  Where the
@@ -47,6 +51,7 @@
 
 #define OR_FLAG_ACCEPT 1 /* u within 1e-5 (relative) of the acceptance threshold */
 #define OR_FLAG_CDF 2    /* u*W within 1e-5*W of a CDF step around the chosen token */
+#define OR_FLAG_CUT 4    /* a top-p cut of the position's rows within 1e-5 of moving */
 
 #define OR_FLAG_TOL 1e-5
 
@@ -164,6 +169,68 @@ int sv_oracle_inverse_cdf(const double* w, int V, double u, double* margin) {
   return t;
 }
 
+/* Top-k / top-p filtering of one row's distribution [VA: SamplingParams
+ * with top_p; SD §8.3].  R20: l are the row's logits (after any grammar
+ * mask), p its tempered softmax; both filters keep whole value classes
+ * (tokens with equal logits are kept or dropped together):
+ *   top_k > 0: keep the tokens whose logit is >= the k-th largest logit,
+ *     counted with multiplicity; renormalise;
+ *   top_p < 1: over what is left, keep the tokens for which the mass of
+ *     tokens with a strictly larger logit is < top_p (so the smallest set of
+ *     leading value classes whose mass reaches top_p); renormalise.
+ * The cut is flagged (return OR_FLAG_CUT) when the mass in front of the
+ * last kept class, or in front of the first dropped one, lies within
+ * OR_FLAG_TOL of top_p: an fp32 evaluation may keep one class more or less.
+ * order: scratch of V ints. */
+static _Thread_local const double* g_sort_key; /* qsort has no context argument */
+static int by_logit_desc(const void* a, const void* b) {
+  double x = g_sort_key[*(const int*)a], y = g_sort_key[*(const int*)b];
+  if (x > y) return -1;
+  if (x < y) return 1;
+  return (*(const int*)a > *(const int*)b) - (*(const int*)a < *(const int*)b);
+}
+
+static int filter_top_k_top_p(const double* l, double* p, int V, int top_k, double top_p,
+                              int* order) {
+  int use_k = top_k > 0 && top_k < V, use_p = top_p < 1.0;
+  if (!use_k && !use_p) return 0;
+  for (int j = 0; j < V; ++j) order[j] = j;
+  g_sort_key = l;
+  qsort(order, (size_t)V, sizeof(int), by_logit_desc);
+  if (use_k) {
+    double vk = l[order[top_k - 1]];
+    double Z = 0.0;
+    for (int j = 0; j < V; ++j) {
+      if (l[j] < vk) p[j] = 0.0;
+      Z += p[j];
+    }
+    for (int j = 0; j < V; ++j) p[j] /= Z;
+  }
+  int flag = 0;
+  if (use_p) {
+    double above = 0.0; /* mass of the classes before the current one */
+    int t = 0, dropping = 0;
+    while (t < V) {
+      int e = t;
+      double mass = 0.0;
+      while (e < V && l[order[e]] == l[order[t]]) mass += p[order[e++]];
+      if (!dropping && above < top_p) {
+        if (top_p - above <= OR_FLAG_TOL) flag = OR_FLAG_CUT;
+      } else {
+        if (!dropping && above - top_p <= OR_FLAG_TOL) flag = OR_FLAG_CUT;
+        dropping = 1;
+        for (int r = t; r < e; ++r) p[order[r]] = 0.0;
+      }
+      above += mass;
+      t = e;
+    }
+    double Z = 0.0;
+    for (int j = 0; j < V; ++j) Z += p[j];
+    for (int j = 0; j < V; ++j) p[j] /= Z;
+  }
+  return flag;
+}
+
 /* Acceptance threshold theta = min(1, p/q) [SD §2.1].  R2: q = 0 < p gives
  * 1 (always accept under the strict test below); p = q = 0 gives 0. */
 static double accept_threshold(double p, double q) {
@@ -258,10 +325,11 @@ int sv_oracle_greedy(const void* target, int dtype, const int32_t* draft_tokens,
  * from p_n instead (R3).  The draw uses uniform u_K (R5). */
 static int sample_request(const void* target, const void* draft, int dtype,
                           const int32_t* draft_tokens, const uint32_t* mask,
-                          const double* uniforms, double T, int K,
+                          const double* uniforms, double T, int top_k, double top_p, int K,
                           int K_b, int V, size_t b, double* lrow, double* p, double* q,
-                          double* w, int32_t* tokens, int32_t* accept_len, double* accept_prob,
-                          int32_t* flags, double* margins, int32_t probe, double* probe_out) {
+                          double* w, int* order, int32_t* tokens, int32_t* accept_len,
+                          double* accept_prob, int32_t* flags, double* margins, int32_t probe,
+                          double* probe_out) {
   for (int i = 0; i < K_b; ++i) {
     int32_t x = draft_tokens[b * (size_t)K + (size_t)i];
     if (x < 0 || x >= V) return OR_BAD_TOKEN;
@@ -274,12 +342,14 @@ static int sample_request(const void* target, const void* draft, int dtype,
     apply_token_mask(lrow, V, mask_row_of(mask, K, V, b, i));
     if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
     sv_oracle_tempered_softmax(lrow, V, T, p);
+    flags[i] |= filter_top_k_top_p(lrow, p, V, top_k, top_p, order);
     double qx = 1.0;
     if (draft) {
       load_row(draft, dtype, b * (size_t)K + (size_t)i, V, lrow);
       apply_token_mask(lrow, V, mask_row_of(mask, K, V, b, i));
       if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
       sv_oracle_tempered_softmax(lrow, V, T, q);
+      flags[i] |= filter_top_k_top_p(lrow, q, V, top_k, top_p, order);
       qx = q[x];
     }
     double theta = accept_threshold(p[x], qx);
@@ -302,6 +372,7 @@ static int sample_request(const void* target, const void* draft, int dtype,
     apply_token_mask(lrow, V, mask_row_of(mask, K, V, b, K_b));
     if (!row_is_valid(lrow, V)) return OR_BAD_LOGITS;
     sv_oracle_tempered_softmax(lrow, V, T, p);
+    flags[K_b] |= filter_top_k_top_p(lrow, p, V, top_k, top_p, order);
     for (int j = 0; j < V; ++j) w[j] = p[j];
   } else {
     double W = 0.0;
@@ -348,6 +419,8 @@ static int sample_request(const void* target, const void* draft, int dtype,
  *   token t = probe_tokens[b] occupies in that draw's distribution (NaN if
  *   t is out of range).  Used to check a draw made elsewhere.
  *   token_mask [B, K+1, ceil(V/32)] words or NULL: grammar masks (R18).
+ *   top_k (0 = off), top_p (1 = off): filters of every sampled distribution,
+ *   target and dense draft alike (R20); the greedy rule ignores them.
  * Returns 0, or a negative code for arguments outside the domain. */
 int sv_oracle_sample(const void* target, const void* draft, int dtype,
                      const int32_t* draft_tokens, const int32_t* draft_lens,
@@ -355,11 +428,17 @@ int sv_oracle_sample(const void* target, const void* draft, int dtype,
                      int b_begin, int b_end, int32_t* out_tokens, int32_t* out_accept_len,
                      double* out_accept_prob, int32_t* out_flags, double* out_margins,
                      int32_t* out_status, const int32_t* probe_tokens, double* probe_interval,
-                     const uint32_t* token_mask) {
+                     const uint32_t* token_mask, int top_k, double top_p) {
   if (B < 0 || K < 0 || V < 1 || b_begin < 0 || b_end > B) return -1;
   if (!(temperature >= 0) || isinf(temperature)) return -3;
+  if (top_k < 0 || !(top_p > 0.0 && top_p <= 1.0)) return -5;
   double* buf = (double*)malloc(sizeof(double) * (size_t)V * 4);
-  if (!buf) return -2;
+  int* order = (int*)malloc(sizeof(int) * (size_t)V);
+  if (!buf || !order) {
+    free(buf);
+    free(order);
+    return -2;
+  }
   double *lrow = buf, *p = buf + V, *q = buf + 2 * (size_t)V, *w = buf + 3 * (size_t)V;
   for (int b = b_begin; b < b_end; ++b) {
     int32_t* tokens = out_tokens + (size_t)b * (size_t)(K + 1);
@@ -380,8 +459,8 @@ int sv_oracle_sample(const void* target, const void* draft, int dtype,
                           tokens, &out_accept_len[b], aprob);
     else
       st = sample_request(target, draft, dtype, draft_tokens, token_mask, uniforms, temperature,
-                          K, K_b,
-                          V, (size_t)b, lrow, p, q, w, tokens, &out_accept_len[b], aprob,
+                          top_k, top_p, K, K_b,
+                          V, (size_t)b, lrow, p, q, w, order, tokens, &out_accept_len[b], aprob,
                           flags, margins, probe_tokens ? probe_tokens[b] : -1,
                           probe_interval ? probe_interval + 2 * (size_t)b : NULL);
     if (st) {
@@ -392,6 +471,7 @@ int sv_oracle_sample(const void* target, const void* draft, int dtype,
     out_status[b] = st;
   }
   free(buf);
+  free(order);
   return 0;
 }
 

@@ -193,7 +193,8 @@ def _bisect(pred, iters=64):
 class _Request:
     """One request evaluated by the oracle for chosen drafts and uniforms."""
 
-    def __init__(self, target, draft, T, mask=None):
+    def __init__(self, target, draft, T, mask=None, top_k=0, top_p=1.0):
+        self.top_k, self.top_p = top_k, top_p
         self.target = np.ascontiguousarray(target[None], np.float32)
         self.draft = None if draft is None else np.ascontiguousarray(draft[None], np.float32)
         self.mask = None if mask is None else np.ascontiguousarray(mask[None], np.uint32)
@@ -202,7 +203,8 @@ class _Request:
 
     def run(self, drafts, u):
         out = oracle.sample(self.target, self.draft, np.asarray([drafts], np.int32),
-                            np.asarray([u], np.float64), self.T, token_mask=self.mask)
+                            np.asarray([u], np.float64), self.T, token_mask=self.mask,
+                            top_k=self.top_k, top_p=self.top_p)
         assert out["status"][0] == 0
         return out["tokens"][0], int(out["accept_len"][0])
 
@@ -549,6 +551,124 @@ def check_exact_masked(V=6, K=2, T=0.8, seed=16):
 
 
 # ---------------------------------------------------------------------------
+# top-k / top-p
+# ---------------------------------------------------------------------------
+
+def np_filter(l, T, top_k, top_p):
+    """Filtered distribution of one row through numpy: sort for the k-th
+    largest logit, unique value classes and cumulative sums for top-p."""
+    l = np.asarray(l, np.float64)
+    p = scipy.special.softmax(l / T)
+    keep = np.ones(l.size, bool)
+    if 0 < top_k < l.size:
+        keep &= l >= np.sort(l)[::-1][top_k - 1]
+    p = np.where(keep, p, 0.0)
+    p /= p.sum()
+    if top_p < 1.0:
+        vals = np.unique(l[keep])[::-1]
+        mass = np.array([p[l == v].sum() for v in vals])
+        front = np.concatenate([[0.0], np.cumsum(mass)[:-1]])
+        keep &= l >= vals[front < top_p].min()
+        p = np.where(keep, p, 0.0)
+        p /= p.sum()
+    return p
+
+
+def check_golden_topk_topp():
+    g = _golden("verify_topk_topp_v6.json")
+    target = np.log(np.asarray(g["target_probs"])).astype(np.float32)[None]
+    draft = np.log(np.asarray(g["draft_probs"])).astype(np.float32)[None]
+    for case in g["cases"]:
+        out = oracle.sample(target, draft if case["mode"] == "dense" else None,
+                            np.asarray([case["draft_tokens"]]),
+                            np.asarray([case["uniforms"]], np.float32), g["T"],
+                            top_k=case["top_k"], top_p=case["top_p"])
+        assert out["status"][0] == 0
+        assert list(out["tokens"][0]) == case["tokens"], (case, out["tokens"][0])
+        assert out["accept_len"][0] == case["accept_len"], case
+        np.testing.assert_allclose(out["accept_prob"][0], case["accept_prob"], atol=1e-6)
+        assert (out["flags"][0] & oracle.FLAG_CUT).sum() == 0
+
+
+def check_filter_matches_numpy(seed=18):
+    """On rows with many exact ties (logits on a 0.5 grid), the oracle's
+    filtered p(x) (one-hot acceptance probability) and p/q (dense) agree
+    with the numpy filter for every (top_k, top_p) pair."""
+    rng = np.random.default_rng(seed)
+    B, V, T = 300, 40, 0.9
+    l = (np.round(rng.standard_normal((B, 2, V)) * 4) / 2).astype(np.float32)
+    d = (np.round(rng.standard_normal((B, 1, V)) * 4) / 2).astype(np.float32)
+    x = rng.integers(0, V, size=(B, 1)).astype(np.int32)
+    u = np.full((B, 2), 0.5, np.float32)
+    for top_k, top_p in ((0, 0.9), (5, 1.0), (3, 0.5), (1, 1.0), (0, 0.3), (12, 0.95)):
+        one = oracle.sample(l, None, x, u, T, top_k=top_k, top_p=top_p)
+        den = oracle.sample(l, d, x, u, T, top_k=top_k, top_p=top_p)
+        for b in range(B):
+            p = np_filter(l[b, 0], T, top_k, top_p)
+            q = np_filter(d[b, 0], T, top_k, top_p)
+            if one["flags"][b, 0] & oracle.FLAG_CUT:
+                continue
+            assert abs(one["accept_prob"][b, 0] - min(1.0, p[x[b, 0]])) < 1e-12, (b, top_k, top_p)
+            px, qx = p[x[b, 0]], q[x[b, 0]]
+            want = min(1.0, px / qx) if qx > 0 else (1.0 if px > 0 else 0.0)
+            if not den["flags"][b, 0] & oracle.FLAG_CUT:
+                assert abs(den["accept_prob"][b, 0] - want) < 1e-12, (b, top_k, top_p)
+    # off-switches: top_k = 0 or >= V and top_p = 1 give the unfiltered result
+    a = oracle.sample(l, d, x, u, T)
+    for k in (0, V, V + 7):
+        b2 = oracle.sample(l, d, x, u, T, top_k=k, top_p=1.0)
+        assert (a["tokens"] == b2["tokens"]).all()
+        np.testing.assert_array_equal(a["accept_prob"], b2["accept_prob"])
+    # top_k = 1 with the argmax as the draft: always accepted, and the
+    # residual never happens; the bonus is the last row's argmax class
+    am = np.argmax(l[:, 0], axis=1).astype(np.int32)[:, None]
+    uniq = np.array([(l[b, 0] == l[b, 0].max()).sum() == 1 for b in range(B)])
+    one = oracle.sample(l, None, am, np.full((B, 2), 0.999, np.float32), T, top_k=1)
+    assert (one["accept_len"][uniq] == 2).all()
+    ok = np.array([(l[b, 1] == l[b, 1].max()).sum() == 1 for b in range(B)]) & uniq
+    assert (one["tokens"][ok, 1] == np.argmax(l[ok, 1], axis=1)).all()
+
+
+def check_exact_filtered(V=6, K=2, T=0.8, seed=19):
+    """Exactness with top-k / top-p: with x_i drawn from the filtered draft
+    distribution, the emitted token at every position follows the filtered
+    target distribution (numpy filter) to 1e-12; dense and one-hot drafts,
+    on logits with ties."""
+    rng = np.random.default_rng(seed)
+    l = (np.round(rng.standard_normal((K + 1, V)) * 3) / 2).astype(np.float32)
+    d = (l[:K] + np.round(rng.standard_normal((K, V)) * 2) / 2).astype(np.float32)
+    for top_k, top_p in ((4, 1.0), (0, 0.7), (5, 0.8)):
+        p = np.array([np_filter(l[i], T, top_k, top_p) for i in range(K + 1)])
+        q = np.array([np_filter(d[i], T, top_k, top_p) for i in range(K)])
+        req = _Request(l, d, T, top_k=top_k, top_p=top_p)
+        prefix = [int(np.argmax(p[j] * q[j])) for j in range(K)]
+        for i in range(K + 1):
+            emitted = np.zeros(V)
+            for x in (range(V) if i < K else [0]):
+                if i < K and q[i, x] == 0:
+                    continue
+                drafts = prefix[:i] + [x] + prefix[i + 1:] if i < K else list(prefix)
+                theta, law = _emission_law(req, drafts, i)
+                if i < K:
+                    emitted[x] += q[i, x] * theta
+                    emitted += q[i, x] * (1.0 - theta) * law
+                else:
+                    emitted = law
+            np.testing.assert_allclose(emitted, p[i], rtol=0, atol=1e-12,
+                                       err_msg="dense k=%d p=%g position %d" % (top_k, top_p, i))
+        req = _Request(l, None, T, top_k=top_k, top_p=top_p)
+        prefix = [int(np.argmax(p[j])) for j in range(K)]
+        for i in range(K):
+            for x in range(V):
+                drafts = prefix[:i] + [x] + prefix[i + 1:]
+                theta, law = _emission_law(req, drafts, i)
+                assert abs(theta - min(1.0, p[i, x])) < 1e-12
+                emitted = (1.0 - theta) * law
+                emitted[x] += theta
+                np.testing.assert_allclose(emitted, p[i], rtol=0, atol=1e-12)
+
+
+# ---------------------------------------------------------------------------
 # n-gram proposer
 # ---------------------------------------------------------------------------
 
@@ -707,4 +827,5 @@ ALL_CHECKS = [
     check_zero_probability_draft_rejected, check_temperature_to_zero_is_greedy,
     check_errors, check_tree_brute_force, check_tree_errors, check_golden_masked,
     check_mask_layout, check_exact_masked, check_golden_ngram, check_ngram_matches_numpy,
+    check_golden_topk_topp, check_filter_matches_numpy, check_exact_filtered,
 ]

@@ -64,6 +64,14 @@ MUTANTS = [
     ("n-gram tries the shortest n first",
      "for (int n = n_max; n >= n_min; --n) {\n      if (len < n + 1) continue;",
      "for (int n = n_min; n <= n_max; ++n) {\n      if (len < n + 1) continue;", 1),
+    ("top-k drops the class at the cut", "if (l[j] < vk) p[j] = 0.0;", "if (l[j] <= vk) p[j] = 0.0;", 1),
+    ("top-p counts the class itself", "if (!dropping && above < top_p) {",
+     "if (!dropping && above + mass < top_p) {", 1),
+    ("top-p on the unrenormalised top-k", "    for (int j = 0; j < V; ++j) p[j] /= Z;\n  }\n  int flag = 0;",
+     "  }\n  int flag = 0;", 1),
+    ("draft left unfiltered", "      flags[i] |= filter_top_k_top_p(lrow, q, V, top_k, top_p, order);\n", "", 1),
+    ("bonus row left unfiltered", "    flags[K_b] |= filter_top_k_top_p(lrow, p, V, top_k, top_p, order);\n",
+     "", 1),
     ("n-gram drafts start one late", "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t];",
      "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t + 1 < len ? found + n + t + 1 : found + n + t];", 1),
 ]
