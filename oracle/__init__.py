@@ -80,6 +80,11 @@ def configure(lib):
     lib.sv_oracle_tree.restype = I
     lib.sv_oracle_compact.argtypes = [P, P, I, I, P, P, P]
     lib.sv_oracle_compact.restype = None
+    lib.sv_oracle_typical.argtypes = [P, I, P, P, P, D, D, D, I, I, I, I, I, P, P, P, P, P]
+    lib.sv_oracle_typical.restype = I
+    lib.sv_oracle_tree_typical.argtypes = [P, I, P, P, P, D, D, D, I, I, I, I, I, I, P, P, P, P,
+                                           P]
+    lib.sv_oracle_tree_typical.restype = I
     lib.sv_oracle_ngram.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
     lib.sv_oracle_ngram.restype = I
     return lib
@@ -241,6 +246,61 @@ def tree(target, parent, node_tokens, max_depth, *, threads=1, b_range=None):
         return lib.sv_oracle_tree(_ptr(target), dt, _ptr(par), _ptr(nt), B, N, V, int(max_depth),
                                   lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
                                   _ptr(out["path"]), _ptr(out["status"]))
+
+    _run(fn, B, threads, b_range)
+    return out
+
+
+def typical(target, draft_tokens, uniforms, temperature, eps, delta, *, draft_lens=None,
+            threads=1, b_range=None):
+    """Typical acceptance: accept x_i while p_i(x_i) > min(eps, delta *
+    exp(-H(p_i))); the emitted token at the first failure (or the bonus
+    position) is drawn from p_n with uniforms[:, K].  Returns tokens,
+    accept_len, accept_prob (p_i(x_i) at tested positions), flags, status."""
+    target, dt = _logits(target)
+    B, K1, V = target.shape
+    K = K1 - 1
+    toks = np.ascontiguousarray(draft_tokens, dtype=np.int32).reshape(B, K)
+    u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, K + 1)
+    lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, dtype=np.int32)
+    out = dict(tokens=np.full((B, K + 1), -1, np.int32), accept_len=np.zeros(B, np.int32),
+               accept_prob=np.full((B, K), -1.0), flags=np.zeros((B, K + 1), np.int32),
+               status=np.zeros(B, np.int32))
+    lib = _load()
+
+    def fn(lo, hi):
+        return lib.sv_oracle_typical(_ptr(target), dt, _ptr(toks), _ptr(lens), _ptr(u),
+                                     float(temperature), float(eps), float(delta), B, K, V, lo, hi,
+                                     _ptr(out["tokens"]), _ptr(out["accept_len"]),
+                                     _ptr(out["accept_prob"]), _ptr(out["flags"]),
+                                     _ptr(out["status"]))
+
+    _run(fn, B, threads, b_range)
+    return out
+
+
+def tree_typical(target, parent, node_tokens, uniforms, temperature, eps, delta, max_depth, *,
+                 threads=1, b_range=None):
+    """Typical acceptance over a candidate tree: tokens / path [B, max_depth+1],
+    accept_len, flags [B], status.  uniforms [B] drive the final draw."""
+    target, dt = _logits(target)
+    B, N1, V = target.shape
+    N = N1 - 1
+    par = np.ascontiguousarray(parent, dtype=np.int32).reshape(N)
+    nt = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
+    u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B)
+    W = max_depth + 1
+    out = dict(tokens=np.full((B, W), -1, np.int32), accept_len=np.zeros(B, np.int32),
+               path=np.full((B, W), -1, np.int32), flags=np.zeros(B, np.int32),
+               status=np.zeros(B, np.int32))
+    lib = _load()
+
+    def fn(lo, hi):
+        return lib.sv_oracle_tree_typical(_ptr(target), dt, _ptr(par), _ptr(nt), _ptr(u),
+                                          float(temperature), float(eps), float(delta), B, N, V,
+                                          int(max_depth), lo, hi, _ptr(out["tokens"]),
+                                          _ptr(out["accept_len"]), _ptr(out["path"]),
+                                          _ptr(out["flags"]), _ptr(out["status"]))
 
     _run(fn, B, threads, b_range)
     return out

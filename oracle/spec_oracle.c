@@ -23,6 +23,8 @@
  *          SamplingParams(temperature=0.8, top_p=0.95) (top-p filtering of
  *          the sampled distributions), with "推测解码与 MTP" §8.3 (non-greedy
  *          decoding with wide top-p).
+ *   [SD] §10.4 also names typical acceptance, the approximate (not exactly
+ *          lossless) rule of the original Medusa, offered by EAGLE too.
  *
  * Every quantity is computed in double precision, one request at a time,
  * with plain serial loops: no blocking, fusion or reordering.  Where the
@@ -564,6 +566,191 @@ int sv_oracle_tree(const void* target, int dtype, const int32_t* parent,
   free(depth);
   free(row);
   return 0;
+}
+
+/* ------------------------------------------------------------------ */
+/* typical acceptance                                                  */
+/* ------------------------------------------------------------------ */
+
+/* Entropy in nats, H = -sum p ln p (a zero probability adds nothing). */
+static double entropy_nats(const double* p, int V) {
+  double H = 0.0;
+  for (int j = 0; j < V; ++j)
+    if (p[j] > 0) H -= p[j] * log(p[j]);
+  return H;
+}
+
+/* R21 (typical acceptance, [SD] §10.4; the pages name it only): a draft x
+ * at a position whose target distribution is p is accepted when
+ *   p(x) > min(eps, delta * exp(-H(p))),
+ * H the entropy of p in nats, eps and delta the rule's two parameters (the
+ * posterior threshold and alpha of the Medusa implementation).  The test
+ * runs in position order; the emitted token at the first failing position
+ * n (or at K_b when all pass) is drawn from p_n itself by inverse CDF with
+ * u_K - this rule has no residual.  accept_prob reports p_i(x_i) at every
+ * tested position; a test with |p(x) - threshold| <= 1e-5 * threshold is
+ * flagged. */
+static double typical_threshold(const double* p, int V, double eps, double delta) {
+  double t = delta * exp(-entropy_nats(p, V));
+  return t < eps ? t : eps;
+}
+
+int sv_oracle_typical(const void* target, int dtype, const int32_t* draft_tokens,
+                      const int32_t* draft_lens, const double* uniforms, double T, double eps,
+                      double delta, int B, int K, int V, int b_begin, int b_end,
+                      int32_t* out_tokens, int32_t* out_accept_len, double* out_accept_prob,
+                      int32_t* out_flags, int32_t* out_status) {
+  if (B < 0 || K < 0 || V < 1 || b_begin < 0 || b_end > B) return -1;
+  if (!(T > 0) || isinf(T) || !(eps >= 0) || !(delta >= 0)) return -3;
+  double* buf = (double*)malloc(sizeof(double) * (size_t)V * 2);
+  if (!buf) return -2;
+  double *l = buf, *p = buf + V;
+  for (int b = b_begin; b < b_end; ++b) {
+    int32_t* tokens = out_tokens + (size_t)b * (size_t)(K + 1);
+    int32_t* flags = out_flags + (size_t)b * (size_t)(K + 1);
+    double* aprob = out_accept_prob + (size_t)b * (size_t)K;
+    const double* u = uniforms + (size_t)b * (size_t)(K + 1);
+    clear_request(tokens, K + 1, &out_accept_len[b]);
+    for (int i = 0; i <= K; ++i) flags[i] = 0;
+    for (int i = 0; i < K; ++i) aprob[i] = -1.0;
+    int K_b = draft_lens ? draft_lens[b] : K;
+    int st = 0;
+    if (K_b < 0 || K_b > K) st = OR_BAD_DRAFT_LEN;
+    for (int i = 0; i < K_b && !st; ++i) {
+      int32_t x = draft_tokens[(size_t)b * (size_t)K + (size_t)i];
+      if (x < 0 || x >= V) st = OR_BAD_TOKEN;
+    }
+    int n = K_b;
+    for (int i = 0; i < K_b && !st; ++i) {
+      int32_t x = draft_tokens[(size_t)b * (size_t)K + (size_t)i];
+      load_row(target, dtype, (size_t)b * (size_t)(K + 1) + (size_t)i, V, l);
+      if (!row_is_valid(l, V)) {
+        st = OR_BAD_LOGITS;
+        break;
+      }
+      sv_oracle_tempered_softmax(l, V, T, p);
+      double thr = typical_threshold(p, V, eps, delta);
+      aprob[i] = p[x];
+      if (fabs(p[x] - thr) <= OR_FLAG_TOL * thr) flags[i] |= OR_FLAG_ACCEPT;
+      if (!(p[x] > thr)) {
+        n = i;
+        break;
+      }
+    }
+    if (!st) {
+      load_row(target, dtype, (size_t)b * (size_t)(K + 1) + (size_t)n, V, l);
+      if (!row_is_valid(l, V)) st = OR_BAD_LOGITS;
+    }
+    if (!st) {
+      sv_oracle_tempered_softmax(l, V, T, p);
+      double margin = 0.0;
+      int t = sv_oracle_inverse_cdf(p, V, u[K], &margin);
+      if (margin <= OR_FLAG_TOL) flags[n] |= OR_FLAG_CDF;
+      for (int i = 0; i < n; ++i) tokens[i] = draft_tokens[(size_t)b * (size_t)K + (size_t)i];
+      tokens[n] = t;
+      out_accept_len[b] = n + 1;
+    } else {
+      clear_request(tokens, K + 1, &out_accept_len[b]);
+      for (int i = 0; i < K; ++i) aprob[i] = -1.0;
+      for (int i = 0; i <= K; ++i) flags[i] = 0;
+    }
+    out_status[b] = st;
+  }
+  free(buf);
+  return 0;
+}
+
+/* Typical acceptance on a candidate tree (R21 with [SD] §3.3): node n is
+ * accepted when its parent is (the root always is) and its token passes the
+ * typical test under the parent's distribution; the result is the deepest
+ * accepted node (the lowest id among equally deep ones), the tokens along
+ * its root path and one token drawn from its own distribution with u[b].
+ * Only the rows of accepted nodes are needed (their validity is checked).
+ *   uniforms [B]; outputs as sv_oracle_tree, plus flags [B] (OR_FLAG_ACCEPT
+ *   when any test made is within 1e-5 of its threshold, OR_FLAG_CDF for the
+ *   draw). */
+int sv_oracle_tree_typical(const void* target, int dtype, const int32_t* parent,
+                           const int32_t* node_tokens, const double* uniforms, double T,
+                           double eps, double delta, int B, int N, int V, int max_depth,
+                           int b_begin, int b_end, int32_t* out_tokens, int32_t* out_accept_len,
+                           int32_t* out_path, int32_t* out_flags, int32_t* out_status) {
+  if (B < 0 || N < 0 || V < 1 || max_depth < 0 || b_begin < 0 || b_end > B) return -1;
+  if (!(T > 0) || isinf(T) || !(eps >= 0) || !(delta >= 0)) return -3;
+  int* depth = (int*)malloc(sizeof(int) * (size_t)(N + 1));
+  int* acc = (int*)malloc(sizeof(int) * (size_t)(N + 1));
+  double* thr = (double*)malloc(sizeof(double) * (size_t)(N + 1));
+  double* l = (double*)malloc(sizeof(double) * (size_t)V);
+  double* p = (double*)malloc(sizeof(double) * (size_t)V);
+  double* pp = (double*)malloc(sizeof(double) * (size_t)V * (size_t)(N + 1));
+  if (!depth || !acc || !thr || !l || !p || !pp) {
+    free(depth); free(acc); free(thr); free(l); free(p); free(pp);
+    return -2;
+  }
+  int rc = 0;
+  depth[0] = 0;
+  for (int n = 1; n <= N && !rc; ++n) {
+    int pa = parent[n - 1];
+    if (pa < 0 || pa >= n) rc = -4;
+    else if ((depth[n] = depth[pa] + 1) > max_depth) rc = -4;
+  }
+  int width = max_depth + 1;
+  for (int b = b_begin; b < b_end && !rc; ++b) {
+    int32_t* tokens = out_tokens + (size_t)b * (size_t)width;
+    int32_t* path = out_path + (size_t)b * (size_t)width;
+    clear_request(tokens, width, &out_accept_len[b]);
+    for (int k = 0; k < width; ++k) path[k] = -1;
+    out_flags[b] = 0;
+    int st = 0;
+    for (int n = 1; n <= N; ++n) {
+      int32_t t = node_tokens[(size_t)b * (size_t)N + (size_t)(n - 1)];
+      if (t < 0 || t >= V) st = OR_BAD_TOKEN;
+    }
+    /* the distribution and threshold of every accepted node, parents first */
+    acc[0] = 1;
+    for (int n = 0; n <= N && !st; ++n) {
+      if (n > 0) {
+        int pa = parent[n - 1];
+        int32_t t = node_tokens[(size_t)b * (size_t)N + (size_t)(n - 1)];
+        acc[n] = 0;
+        if (acc[pa]) {
+          double px = pp[(size_t)pa * (size_t)V + (size_t)t];
+          if (fabs(px - thr[pa]) <= OR_FLAG_TOL * thr[pa]) out_flags[b] |= OR_FLAG_ACCEPT;
+          acc[n] = px > thr[pa];
+        }
+      }
+      if (!acc[n]) continue;
+      load_row(target, dtype, (size_t)b * (size_t)(N + 1) + (size_t)n, V, l);
+      if (!row_is_valid(l, V)) {
+        st = OR_BAD_LOGITS;
+        break;
+      }
+      sv_oracle_tempered_softmax(l, V, T, pp + (size_t)n * (size_t)V);
+      thr[n] = typical_threshold(pp + (size_t)n * (size_t)V, V, eps, delta);
+    }
+    if (!st) {
+      int best = 0;
+      for (int n = 1; n <= N; ++n)
+        if (acc[n] && depth[n] > depth[best]) best = n;
+      int len = depth[best] + 1;
+      for (int n = best, d = depth[best]; d >= 0; --d) {
+        path[d] = n;
+        if (d > 0) tokens[d - 1] = node_tokens[(size_t)b * (size_t)N + (size_t)(n - 1)];
+        n = d > 0 ? parent[n - 1] : 0;
+      }
+      for (int j = 0; j < V; ++j) p[j] = pp[(size_t)best * (size_t)V + (size_t)j];
+      double margin = 0.0;
+      tokens[len - 1] = sv_oracle_inverse_cdf(p, V, uniforms[b], &margin);
+      if (margin <= OR_FLAG_TOL) out_flags[b] |= OR_FLAG_CDF;
+      out_accept_len[b] = len;
+    } else {
+      clear_request(tokens, width, &out_accept_len[b]);
+      for (int k = 0; k < width; ++k) path[k] = -1;
+      out_flags[b] = 0;
+    }
+    out_status[b] = st;
+  }
+  free(depth); free(acc); free(thr); free(l); free(p); free(pp);
+  return rc;
 }
 
 /* ------------------------------------------------------------------ */

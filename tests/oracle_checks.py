@@ -669,6 +669,108 @@ def check_exact_filtered(V=6, K=2, T=0.8, seed=19):
 
 
 # ---------------------------------------------------------------------------
+# typical acceptance
+# ---------------------------------------------------------------------------
+
+def check_golden_typical():
+    g = _golden("typical_v5.json")
+    rows = np.asarray(g["rows"])
+    with np.errstate(divide="ignore"):
+        lg = np.log(rows).astype(np.float32)
+    chain = lg[:3][None]
+    for case in g["chain"]:
+        out = oracle.typical(chain, [case["draft_tokens"]], [case["uniforms"]], g["T"],
+                             case["eps"], case["delta"])
+        assert out["status"][0] == 0, out
+        assert int(out["flags"][0][0]) == case.get("flag0", 0) and (out["flags"][0][1:] == 0).all()
+        assert list(out["tokens"][0]) == case["tokens"], (case, out["tokens"][0])
+        assert out["accept_len"][0] == case["accept_len"]
+        np.testing.assert_allclose(out["accept_prob"][0], case["accept_prob"], atol=1e-6)
+    tree_rows = lg[[0, 1, 2, 3]][None]
+    for case in g["tree"]:
+        out = oracle.tree_typical(tree_rows, g["tree_parent"], [case["node_tokens"]], [case["u"]],
+                                  g["T"], case["eps"], case["delta"], 2)
+        assert out["status"][0] == 0 and out["flags"][0] == 0, out
+        assert list(out["tokens"][0]) == case["tokens"], (case, out["tokens"][0])
+        assert list(out["path"][0]) == case["path"] and out["accept_len"][0] == case["accept_len"]
+
+
+def check_typical_matches_scipy(seed=20):
+    """Random rows: every tested position reports p(x), the decision is
+    p(x) > min(eps, delta * exp(-H)) with H from scipy.stats.entropy, and the
+    emitted token is the searchsorted draw from p_n."""
+    import scipy.stats
+    rng = np.random.default_rng(seed)
+    B, K, V, T = 400, 4, 30, 0.8
+    l = (rng.standard_normal((B, K + 1, V)) * 1.5).astype(np.float32)
+    p = scipy.special.softmax(l.astype(np.float64) / T, axis=-1)
+    am = np.argmax(l, axis=2)
+    x = np.where(rng.random((B, K)) < 0.6, am[:, :K], rng.integers(0, V, (B, K))).astype(np.int32)
+    u = rng.random((B, K + 1)).astype(np.float32)
+    for eps, delta in ((0.09, 0.3), (0.3, 0.05), (0.02, 0.9)):
+        out = oracle.typical(l, x, u, T, eps, delta)
+        for b in range(B):
+            n = int(out["accept_len"][b]) - 1
+            for i in range(min(n + 1, K)):
+                thr = min(eps, delta * np.exp(-scipy.stats.entropy(p[b, i])))
+                px = p[b, i, x[b, i]]
+                assert abs(out["accept_prob"][b, i] - px) < 1e-12
+                if out["flags"][b, i] & oracle.FLAG_ACCEPT:
+                    break
+                assert (px > thr) == (i < n), (b, i, px, thr)
+            if not (out["flags"][b] & oracle.FLAG_ACCEPT).any():
+                assert out["tokens"][b, n] == _searchsorted_draw(p[b, n], float(u[b, K]))
+                assert (out["tokens"][b, :n] == x[b, :n]).all()
+
+
+def _typical_tree_brute(p, parent, node_tokens, u, eps, delta):
+    """Enumerate root paths: a path counts when every node on it passes under
+    its parent's distribution; the deepest, then the lowest end node."""
+    import scipy.stats
+    N = len(parent)
+    thr = [min(eps, delta * np.exp(-scipy.stats.entropy(p[n]))) for n in range(N + 1)]
+    best, best_d = 0, 0
+    for end in range(1, N + 1):
+        path, n = [], end
+        while n:
+            path.append(n)
+            n = parent[n - 1]
+        ok = all(p[parent[m - 1], node_tokens[m - 1]] > thr[parent[m - 1]] for m in path)
+        if ok and len(path) > best_d:
+            best, best_d = end, len(path)
+    path, n = [], best
+    while n:
+        path.append(n)
+        n = parent[n - 1]
+    path = [0] + path[::-1]
+    toks = [node_tokens[m - 1] for m in path[1:]] + [_searchsorted_draw(p[best], u)]
+    return toks, path
+
+
+def check_tree_typical_brute_force(seed=21):
+    rng = np.random.default_rng(seed)
+    for trial in range(40):
+        N = int(rng.integers(1, 12))
+        parent = [int(rng.integers(0, n)) for n in range(1, N + 1)]
+        depth = [0] * (N + 1)
+        for n in range(1, N + 1):
+            depth[n] = depth[parent[n - 1]] + 1
+        V, T = 6, 1.0
+        l = (rng.standard_normal((1, N + 1, V)) * 1.2).astype(np.float32)
+        p = scipy.special.softmax(l[0].astype(np.float64) / T, axis=-1)
+        toks = rng.integers(0, V, size=(1, N)).astype(np.int32)
+        u = float(rng.random())
+        eps, delta = float(rng.choice([0.09, 0.2, 0.4])), float(rng.choice([0.3, 0.6, 1.0]))
+        out = oracle.tree_typical(l, parent, toks, [u], T, eps, delta, max(depth))
+        if out["flags"][0]:
+            continue
+        want_toks, want_path = _typical_tree_brute(p, parent, list(toks[0]), u, eps, delta)
+        L = len(want_path)
+        assert out["accept_len"][0] == L, (trial, out, want_path)
+        assert list(out["path"][0, :L]) == want_path and list(out["tokens"][0, :L]) == want_toks
+
+
+# ---------------------------------------------------------------------------
 # n-gram proposer
 # ---------------------------------------------------------------------------
 
@@ -828,4 +930,5 @@ ALL_CHECKS = [
     check_errors, check_tree_brute_force, check_tree_errors, check_golden_masked,
     check_mask_layout, check_exact_masked, check_golden_ngram, check_ngram_matches_numpy,
     check_golden_topk_topp, check_filter_matches_numpy, check_exact_filtered,
+    check_golden_typical, check_typical_matches_scipy, check_tree_typical_brute_force,
 ]

@@ -72,6 +72,16 @@ MUTANTS = [
     ("draft left unfiltered", "      flags[i] |= filter_top_k_top_p(lrow, q, V, top_k, top_p, order);\n", "", 1),
     ("bonus row left unfiltered", "    flags[K_b] |= filter_top_k_top_p(lrow, p, V, top_k, top_p, order);\n",
      "", 1),
+    ("typical entropy in bits", "if (p[j] > 0) H -= p[j] * log(p[j]);",
+     "if (p[j] > 0) H -= p[j] * log2(p[j]);", 1),
+    ("typical threshold takes the max", "return t < eps ? t : eps;", "return t > eps ? t : eps;", 1),
+    ("typical test not strict", "if (!(p[x] > thr)) {", "if (!(p[x] >= thr)) {", 1),
+    ("typical draw from the bonus row", "load_row(target, dtype, (size_t)b * (size_t)(K + 1) + (size_t)n, V, l);",
+     "load_row(target, dtype, (size_t)b * (size_t)(K + 1) + (size_t)K_b, V, l);", 1),
+    ("typical tree keeps the highest id", "if (acc[n] && depth[n] > depth[best]) best = n;",
+     "if (acc[n] && depth[n] >= depth[best]) best = n;", 1),
+    ("typical tree tests under the node's own row", "double px = pp[(size_t)pa * (size_t)V + (size_t)t];",
+     "double px = pp[(size_t)(acc[pa] ? pa : pa) * (size_t)V + (size_t)t] * (n % 2 ? 1.0 : 0.5);", 1),
     ("n-gram drafts start one late", "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t];",
      "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t + 1 < len ? found + n + t + 1 : found + n + t];", 1),
 ]
