@@ -187,6 +187,12 @@ def oracle_run(wl, mode, requests, threads):
     if mode == "propose":
         oracle.ngram(wl.history[sub], wl.history_lens[sub], wl.meta["n_min"], wl.meta["n_max"],
                      wl.K)
+    elif mode == "tree_typical":
+        oracle.tree_typical(wl.target[sub], wl.parent, wl.node_tokens[sub], wl.uniforms[sub], wl.T,
+                            wl.eps, wl.delta, wl.max_depth, threads=threads)
+    elif mode == "typical":
+        oracle.typical(wl.target[sub], wl.draft_tokens[sub], wl.uniforms[sub], wl.T, wl.eps,
+                       wl.delta, threads=threads)
     elif mode == "tree":
         oracle.tree(wl.target[sub], wl.parent, wl.node_tokens[sub], wl.max_depth, threads=threads)
     elif mode == "greedy":
@@ -195,7 +201,8 @@ def oracle_run(wl, mode, requests, threads):
     else:
         oracle.sample(wl.target[sub], None if wl.draft is None else wl.draft[sub],
                       wl.draft_tokens[sub], wl.uniforms[sub], wl.T, threads=threads,
-                      token_mask=None if wl.token_mask is None else wl.token_mask[sub])
+                      token_mask=None if wl.token_mask is None else wl.token_mask[sub],
+                      top_k=wl.top_k, top_p=float(np.float32(wl.top_p)))
     return time.perf_counter() - t0
 
 
@@ -217,8 +224,10 @@ def cpu_baseline(wl, mode, budget_s=12.0):
 def load_workload(args, seed=0):
     from token_verification_gb300 import synth
     wl = synth.make_workload(args.workload, seed=seed)
-    mode = ("propose" if wl.history is not None else "tree" if wl.parent is not None
-            else "greedy" if args.greedy else "sample")
+    typical = wl.meta.get("typical", False)
+    mode = ("propose" if wl.history is not None
+            else ("tree_typical" if typical else "tree") if wl.parent is not None
+            else "greedy" if args.greedy else "typical" if typical else "sample")
     if args.batch:  # a smaller batch of the same workload (profiling captures)
         wl.B = args.batch
         for name in ("target", "draft", "draft_tokens", "uniforms", "node_tokens", "token_mask",
@@ -278,12 +287,18 @@ def workload_config(wl, mode):
                    l2="inputs smaller than L2 (%d KB of contexts per call): 2 rotating input "
                       "sets; the figure includes L2 reuse" % (wl.history.nbytes // 1024))
         return cfg
-    if mode == "tree":
+    if mode in ("tree", "tree_typical"):
         cfg.update(N=int(wl.parent.size), max_depth=wl.max_depth)
+        if mode == "tree_typical":
+            cfg.update(temperature=wl.T, eps=wl.eps, delta=wl.delta)
     else:
         cfg.update(K=wl.K, drafts=wl.meta.get("drafts"), temperature=0.0 if mode == "greedy" else wl.T)
         if wl.token_mask is not None:
             cfg["grammar_masks"] = dict(wl.meta["grammar"], bytes=int(wl.token_mask.nbytes))
+        if mode == "sample" and (wl.top_k or wl.top_p < 1.0):
+            cfg.update(top_k=wl.top_k, top_p=wl.top_p)
+        if mode == "typical":
+            cfg.update(eps=wl.eps, delta=wl.delta)
     total = wl.target.nbytes + (wl.draft.nbytes if (wl.draft is not None and mode == "sample") else 0)
     cfg["l2"] = ("inputs larger than L2: %d MB of logits per call, 2 rotating input sets"
                  % (total // 2**20) if total > 129 * 2**20 else
@@ -308,13 +323,15 @@ class Case:
             "history_lens": torch.from_numpy(wl.history_lens)}
         if mode == "propose":
             pass
-        elif mode == "tree":
+        elif mode in ("tree", "tree_typical"):
             self.host["node_tokens"] = torch.from_numpy(wl.node_tokens)
+            if mode == "tree_typical":
+                self.host["uniforms"] = torch.from_numpy(wl.uniforms)
         else:
             self.host["tokens"] = torch.from_numpy(wl.draft_tokens)
             if wl.token_mask is not None:
                 self.host["token_mask"] = torch.from_numpy(wl.token_mask.view(np.int32))
-            if mode == "sample":
+            if mode in ("sample", "typical"):
                 self.host["uniforms"] = torch.from_numpy(wl.uniforms)
                 if wl.draft is not None:
                     self.host["draft"] = to_t(wl.draft)
@@ -325,7 +342,7 @@ class Case:
             self.sets.append({k: v[perm].contiguous().to(device) for k, v in self.host.items()})
 
     def alloc(self, packed=True):
-        if self.mode in ("tree", "propose"):
+        if self.mode in ("tree", "tree_typical", "propose"):
             return None
         return self.api.alloc_outputs(self.wl.B, self.wl.K, self.device, packed=packed,
                                       accept_prob=packed and self.mode == "sample",
@@ -339,12 +356,20 @@ class Case:
         if self.mode == "tree":
             return api.spec_verify_tree(inputs["target"], wl.parent, inputs["node_tokens"],
                                         wl.max_depth, out, path=False, status=False)
+        if self.mode == "tree_typical":
+            return api.spec_verify_tree_typical(inputs["target"], wl.parent, inputs["node_tokens"],
+                                                inputs["uniforms"], wl.T, wl.eps, wl.delta,
+                                                wl.max_depth, out, path=False, status=False)
+        if self.mode == "typical":
+            return api.spec_verify_typical(inputs["target"], inputs["tokens"], inputs["uniforms"],
+                                           wl.T, wl.eps, wl.delta, out)
         if self.mode == "greedy":
             return api.spec_verify_greedy(inputs["target"], inputs["tokens"], out,
                                           token_mask=inputs.get("token_mask"))
         return api.spec_verify_sample(inputs["target"], inputs.get("draft"), inputs["tokens"],
                                       inputs["uniforms"], wl.T, out,
-                                      token_mask=inputs.get("token_mask"))
+                                      token_mask=inputs.get("token_mask"), top_k=wl.top_k,
+                                      top_p=wl.top_p)
 
     def step(self, i, out):
         return self.call(self.sets[i & 1], out)
@@ -366,7 +391,13 @@ class Case:
             return "ngram_kernel"
         if self.mode == "tree":
             return "tree_kernel"
+        if self.mode == "tree_typical":
+            return "verify_stream_kernel + tree_typical_kernel"
+        if self.mode == "typical":
+            return "verify_stream_kernel + finalize_kernel (typical)"
         masked = ", grammar-masked" if self.wl.token_mask is not None else ""
+        if self.mode == "sample" and (self.wl.top_k or self.wl.top_p < 1.0):
+            return "filter_rows_kernel + finalize_kernel (top-k/top-p%s)" % masked
         if self.mode == "sample" and self.wl.draft is not None:
             return "verify_stream_kernel + finalize_kernel (dense%s)" % masked
         return "verify_stream_kernel + finalize_kernel (%s%s)" % (
@@ -383,6 +414,8 @@ class Case:
         if self.mode == "tree":
             rows = int(out.accept_len.sum().item())
             return rows * wl.V * esz
+        if self.mode == "tree_typical":  # every candidate row once
+            return wl.B * (wl.parent.size + 1) * wl.V * esz
         rows = wl.B * (wl.K + 1) + (wl.B * wl.K if (self.mode == "sample" and wl.draft is not None)
                                      else 0)
         masks = 0 if wl.token_mask is None else wl.token_mask.nbytes
@@ -495,7 +528,8 @@ def run_ours(args):
             "ms_per_step": 1e3 * max_elapsed / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": workload_config(wl, mode),
-            "draft_tokens_per_s": None if mode in ("tree", "propose") else value * wl.B * wl.K,
+            "draft_tokens_per_s": (None if mode in ("tree", "tree_typical", "propose")
+                                   else value * wl.B * wl.K),
             "hbm_gbs": algo_bytes * value / 1e9,
             ("mean_draft_len" if mode == "propose" else "mean_accept_len"): mean_len,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",

@@ -64,7 +64,8 @@ typedef enum sv_status {
   SV_ERR_TEMPERATURE = 4, /* temperature negative, NaN or infinite */
   SV_ERR_TREE = 5,        /* parent array: a parent not an earlier node, or depth > max_depth */
   SV_ERR_WORKSPACE = 6,   /* workspace NULL, not 256-byte aligned, or too small */
-  SV_ERR_CUDA = 7         /* a CUDA runtime call or kernel launch failed */
+  SV_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed */
+  SV_ERR_FILTER = 8       /* top_k negative, top_p outside (0, 1], or eps / delta negative */
 } sv_status;
 
 typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
@@ -184,6 +185,81 @@ sv_status spec_verify_greedy_masked(const void* target_logits, const int32_t* dr
                                     int32_t* out_packed, int32_t* out_batch_id,
                                     int32_t* out_status, void* workspace, size_t ws_bytes,
                                     sv_stream_t stream);
+
+/* Verification of top-k / top-p filtered sampling (the vLLM Ascend guide's
+ * examples sample with SamplingParams(temperature=0.8, top_p=0.95); "推测解码与
+ * MTP" §8.3 non-greedy decoding with wide top-p).  Every sampled
+ * distribution - target rows and, with dense drafts, draft rows - is the
+ * tempered softmax of the (grammar-masked) logits filtered as follows, and
+ * the drafts are assumed drawn from the filtered draft distributions:
+ *   top_k > 0 keeps the tokens whose logit is >= the k-th largest logit of
+ *     the row (counted with multiplicity, so ties at the cut are all kept),
+ *     then renormalises; top_k = 0 (or >= V) switches it off;
+ *   top_p < 1 then keeps a token when the probability mass of the tokens
+ *     with a strictly larger logit is below top_p (the smallest set of
+ *     leading logit values whose mass reaches top_p, ties kept together),
+ *     then renormalises; top_p = 1 switches it off.
+ * The acceptance test, the residual norm(max(0, p' - q')) and the bonus draw
+ * use the filtered p', q'.  temperature == 0 is the greedy rule (filters do
+ * not change the argmax).  token_mask: as in spec_verify_sample_masked, or
+ * NULL.  The rows of a filtered call are held in shared memory by clusters of
+ * CTAs: V * sizeof(logit) must not exceed 512 KB (V <= 262144 for bf16,
+ * 131072 for fp32), else SV_ERR_SHAPE.  SV_ERR_FILTER for a negative top_k or
+ * top_p outside (0, 1].  All other arguments, results and the workspace size
+ * are those of spec_verify_sample. */
+sv_status spec_verify_sample_filtered(const void* target_logits, const void* draft_logits,
+                                      const int32_t* draft_tokens, const float* uniforms,
+                                      float temperature, int top_k, float top_p,
+                                      const uint32_t* token_mask, int32_t* out_tokens,
+                                      int32_t* out_accept_len, sv_dtype dtype, int B, int K, int V,
+                                      const int32_t* draft_lens, int32_t* out_cu_accept,
+                                      int32_t* out_packed, int32_t* out_batch_id,
+                                      float* out_accept_prob, int32_t* out_status,
+                                      void* workspace, size_t ws_bytes, sv_stream_t stream);
+
+/* Typical acceptance ("推测解码与 MTP" §10.4: the rule of the original Medusa,
+ * an approximation that is not exactly lossless, also offered by EAGLE).
+ * Draft x_i passes when p_i(x_i) > min(eps, delta * exp(-H(p_i))), with p_i
+ * the tempered target distribution of position i and H its entropy in nats;
+ * positions are tested in order, and at the first failure n (or at K_b when
+ * all pass) one token is drawn from p_n itself with uniforms[b, K] (inverse
+ * CDF: the smallest j whose cumulative probability exceeds u).  There is no
+ * residual: the output follows the rule, not the target distribution.
+ *   eps, delta      the rule's two thresholds (Medusa's defaults are 0.09 and
+ *                   0.3), finite and >= 0, else SV_ERR_FILTER.
+ *   temperature     T > 0; T == 0 applies the greedy rule instead.
+ *   out_accept_prob p_i(x_i) at each tested position, -1 elsewhere.
+ * Drafts are one-hot (no draft logits).  uniforms [B, K+1], of which only
+ * column K is used.  All other arguments, results and the workspace size are
+ * those of spec_verify_sample. */
+sv_status spec_verify_typical(const void* target_logits, const int32_t* draft_tokens,
+                              const float* uniforms, float temperature, float eps, float delta,
+                              int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
+                              int K, int V, const int32_t* draft_lens, int32_t* out_cu_accept,
+                              int32_t* out_packed, int32_t* out_batch_id, float* out_accept_prob,
+                              int32_t* out_status, void* workspace, size_t ws_bytes,
+                              sv_stream_t stream);
+
+/* Typical acceptance on a candidate tree (§10.4 with §3.3).  Node n passes
+ * when its parent passed (the root always does) and its token passes the
+ * typical test under its parent's distribution; the result is the deepest
+ * passing node (the lowest id among equally deep ones): the tokens of its
+ * root path, then one token drawn from its own distribution with
+ * uniforms[b].  Rows of passing nodes must be valid (SV_REQ_BAD_LOGITS).
+ *   target_logits, tree_parent (HOST), tree_tokens, out_tokens, out_path,
+ *   out_accept_len, out_status, max_depth: as in spec_verify_tree.
+ *   uniforms [B] fp32 in [0, 1).  temperature > 0; eps, delta as in
+ *   spec_verify_typical.  workspace: >= spec_verify_tree_workspace_size(B, N,
+ *   V) bytes, 256-byte aligned, zero-filled once (spec_verify_workspace_init).
+ * Every row of the tree is read once (all candidate rows are reduced in
+ * parallel). */
+size_t spec_verify_tree_workspace_size(int B, int N, int V);
+sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tree_parent,
+                                   const int32_t* tree_tokens, const float* uniforms,
+                                   float temperature, float eps, float delta, int32_t* out_tokens,
+                                   int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
+                                   int max_depth, int32_t* out_path, int32_t* out_status,
+                                   void* workspace, size_t ws_bytes, sv_stream_t stream);
 
 /* Greedy tree verification (Medusa / EAGLE; "推测解码与 MTP" §3.3).
  *

@@ -52,7 +52,8 @@ def to_device(wl, device="cuda"):
 def oracle_sample(wl, threads=8, temperature=None):
     T = wl.T if temperature is None else temperature
     return oracle.sample(wl.target, wl.draft, wl.draft_tokens, wl.uniforms, T,
-                         draft_lens=wl.draft_lens, threads=threads, token_mask=wl.token_mask)
+                         draft_lens=wl.draft_lens, threads=threads, token_mask=wl.token_mask,
+                         top_k=wl.top_k, top_p=float(np.float32(wl.top_p)))
 
 
 @dataclass
@@ -60,6 +61,7 @@ class SampleReport:
     requests: int = 0
     positions: int = 0
     acc_flagged: int = 0      # acceptance tests within 1e-5 of theta
+    cut_flagged: int = 0      # top-p cuts within 1e-5 of moving
     excluded: int = 0         # positions not compared because of them
     cdf_flagged: int = 0      # final draws within 1e-5 * W of a CDF edge
     cdf_differ: int = 0       # ... whose GPU token differs from the oracle's
@@ -71,16 +73,17 @@ class SampleReport:
         return self.acc_flagged + self.cdf_flagged
 
     def merge(self, o):
-        for k in ("requests", "positions", "acc_flagged", "excluded", "cdf_flagged",
+        for k in ("requests", "positions", "acc_flagged", "cut_flagged", "excluded", "cdf_flagged",
                   "cdf_differ"):
             setattr(self, k, getattr(self, k) + getattr(o, k))
         self.errors += o.errors
 
     def summary(self):
-        return ("%d requests, %d positions: %d acceptance-flagged (%d positions excluded), "
-                "%d draws CDF-flagged of which %d differ from the oracle (all verified)"
-                % (self.requests, self.positions, self.acc_flagged, self.excluded,
-                   self.cdf_flagged, self.cdf_differ))
+        return ("%d requests, %d positions: %d acceptance-flagged, %d top-p cuts flagged (%d "
+                "positions excluded), %d draws CDF-flagged of which %d differ from the oracle "
+                "(all verified)" % (self.requests, self.positions, self.acc_flagged,
+                                    self.cut_flagged, self.excluded, self.cdf_flagged,
+                                    self.cdf_differ))
 
 
 def compare_sample(ref, gpu, K, V, greedy=False) -> SampleReport:
@@ -101,19 +104,25 @@ def compare_sample(ref, gpu, K, V, greedy=False) -> SampleReport:
             continue
         L = int(ref["accept_len"][b])
         flags = ref["flags"][b]
-        acc_flag = next((i for i in range(K + 1) if flags[i] & oracle.FLAG_ACCEPT), None)
+        acc_flag = next((i for i in range(K + 1)
+                         if flags[i] & (oracle.FLAG_ACCEPT | oracle.FLAG_CUT)), None)
+        cut = acc_flag is not None and bool(flags[acc_flag] & oracle.FLAG_CUT)
         cdf_flag = next((i for i in range(K + 1) if flags[i] & oracle.FLAG_CDF), None)
         if greedy:
             acc_flag = cdf_flag = None
         rt = ref["tokens"][b]
         if acc_flag is not None:
             i = acc_flag
-            rep.acc_flagged += 1
+            if cut:
+                rep.cut_flagged += 1
+            else:
+                rep.acc_flagged += 1
             rep.excluded += K + 1 - i
             if not (g_tok[b, :i] == rt[:i]).all() or g_len[b] < i + 1:
                 rep.errors.append((b, "prefix before flagged test at %d differs" % i))
             if g_prob is not None:
-                ok = np.abs(g_prob[b, :i + 1] - ref["accept_prob"][b, :i + 1]) <= PROB_ATOL
+                upto = i if cut else i + 1  # a flagged cut may move theta_i itself
+                ok = np.abs(g_prob[b, :upto] - ref["accept_prob"][b, :upto]) <= PROB_ATOL
                 if i < K and not ok.all():
                     rep.errors.append((b, "accept_prob differs before flagged position"))
             continue
@@ -156,7 +165,8 @@ def verify_draws(wl, rep: SampleReport, temperature=None):
     T = wl.T if temperature is None else temperature
     out = oracle.sample(sub(wl.target), sub(wl.draft), sub(wl.draft_tokens), sub(wl.uniforms),
                         T, draft_lens=sub(wl.draft_lens), probe_tokens=toks,
-                        token_mask=sub(wl.token_mask))
+                        token_mask=sub(wl.token_mask), top_k=wl.top_k,
+                        top_p=float(np.float32(wl.top_p)))
     u = wl.uniforms[idx, wl.K].astype(np.float64)
     lo, hi = out["probe"][:, 0], out["probe"][:, 1]
     ok = (hi > lo) & (lo <= u + FLAG_TOL) & (hi >= u - FLAG_TOL)
@@ -179,4 +189,4 @@ def assert_report(rep: SampleReport, max_flag_rate=None):
     assert not rep.to_verify, "verify_draws() was not run"
     assert not rep.errors, "%d mismatching requests, first: %s" % (len(rep.errors), rep.errors[:5])
     if max_flag_rate is not None:
-        assert rep.acc_flagged <= max_flag_rate * rep.positions, rep.summary()
+        assert rep.acc_flagged + rep.cut_flagged <= max_flag_rate * rep.positions, rep.summary()

@@ -66,9 +66,12 @@ def _check(t: torch.Tensor, name, device, dtype=None, shape=None):
 _workspaces = {}
 
 
-def workspace(B: int, K: int, V: int, device: torch.device):
+def workspace(B: int, K: int, V: int, device: torch.device, *, need: Optional[int] = None):
+    """The (device, stream)'s workspace, grown to the bytes a (B, K, V) call
+    needs (or to ``need`` bytes when given)."""
     lib = _native.lib()
-    need = int(lib.spec_verify_workspace_size(B, K, V))
+    if need is None:
+        need = int(lib.spec_verify_workspace_size(B, K, V))
     if need == 0 and B > 0:
         raise ValueError("unsupported shape B=%d K=%d V=%d" % (B, K, V))
     stream = torch.cuda.current_stream(device)
@@ -129,14 +132,15 @@ def _check_mask(token_mask, B, K, V, device):
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature,
                        out: Optional[VerifyOutputs] = None, *, draft_lens=None,
                        packed=True, accept_prob=True, status=True,
-                       token_mask=None) -> VerifyOutputs:
+                       token_mask=None, top_k=0, top_p=1.0) -> VerifyOutputs:
     """Rejection-sampling verification of one batch (see spec_verify.h).
 
     target_logits [B, K+1, V] bf16/fp32 CUDA; draft_logits [B, K, V] same
     dtype or None (one-hot drafts); draft_tokens [B, K] int32; uniforms
     [B, K+1] fp32; temperature >= 0 (0 = greedy rule); token_mask
     [B, K+1, ceil(V/32)] int32 grammar masks or None (bit j % 32 of word
-    j // 32 set = token j allowed at that position)."""
+    j // 32 set = token j allowed at that position); top_k (0 = off) and
+    top_p (1.0 = off) filter every sampled distribution."""
     B, K, V, device = _validate_batch(target_logits, draft_tokens, draft_lens)
     if draft_logits is not None:
         _check(draft_logits, "draft_logits", device, target_logits.dtype, (B, K, V))
@@ -151,7 +155,10 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temp
     tail = (_p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, K, V,
             _p(draft_lens), _p(out.cu_accept), _p(out.packed), _p(out.batch_id),
             _p(out.accept_prob), _p(out.status), _p(ws), ws.numel(), _stream(device))
-    if token_mask is None:
+    if top_k != 0 or top_p != 1.0:
+        rc = lib.spec_verify_sample_filtered(*head, int(top_k), ctypes.c_float(float(top_p)),
+                                             _p(token_mask), *tail)
+    elif token_mask is None:
         rc = lib.spec_verify_sample(*head, *tail)
     else:
         rc = lib.spec_verify_sample_masked(*head, _p(token_mask), *tail)
@@ -227,6 +234,66 @@ def spec_verify_tree(target_logits, tree_parent, tree_tokens, max_depth=None,
         _p(target_logits), parent.ctypes.data_as(ctypes.c_void_p), _p(tree_tokens),
         _p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, N, V, int(max_depth),
         _p(out.path), _p(out.status), _stream(device))
+    if rc:
+        raise VerifyError(rc)
+    return out
+
+
+def spec_verify_typical(target_logits, draft_tokens, uniforms, temperature, eps=0.09, delta=0.3,
+                        out: Optional[VerifyOutputs] = None, *, draft_lens=None, packed=True,
+                        accept_prob=True, status=True) -> VerifyOutputs:
+    """Typical acceptance (see spec_verify.h): x_i passes while p_i(x_i) >
+    min(eps, delta * exp(-H(p_i))); the token after the accepted ones is
+    drawn from the target distribution there with uniforms[:, K]."""
+    B, K, V, device = _validate_batch(target_logits, draft_tokens, draft_lens)
+    _check(uniforms, "uniforms", device, torch.float32, (B, K + 1))
+    if out is None:
+        out = alloc_outputs(B, K, device, packed=packed, accept_prob=accept_prob, status=status)
+    ws = workspace(B, K, V, device)
+    rc = _native.lib().spec_verify_typical(
+        _p(target_logits), _p(draft_tokens), _p(uniforms), ctypes.c_float(float(temperature)),
+        ctypes.c_float(float(eps)), ctypes.c_float(float(delta)), _p(out.tokens),
+        _p(out.accept_len), _dtype_code(target_logits), B, K, V, _p(draft_lens), _p(out.cu_accept),
+        _p(out.packed), _p(out.batch_id), _p(out.accept_prob), _p(out.status), _p(ws), ws.numel(),
+        _stream(device))
+    if rc:
+        raise VerifyError(rc)
+    return out
+
+
+def spec_verify_tree_typical(target_logits, tree_parent, tree_tokens, uniforms, temperature,
+                             eps=0.09, delta=0.3, max_depth=None,
+                             out: Optional[TreeOutputs] = None, *, path=True,
+                             status=True) -> TreeOutputs:
+    """Typical acceptance over a candidate tree: tree_parent host [N],
+    tree_tokens [B, N] int32, uniforms [B] fp32 for the final draw."""
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N+1, V]")
+    B, N1, V = target_logits.shape
+    N = N1 - 1
+    device = target_logits.device
+    _check(target_logits, "target_logits", device)
+    parent = np.ascontiguousarray(np.asarray(tree_parent, dtype=np.int32).reshape(-1))
+    if parent.size != N:
+        raise ValueError("tree_parent must have N = %d entries" % N)
+    _check(tree_tokens, "tree_tokens", device, torch.int32, (B, N))
+    _check(uniforms, "uniforms", device, torch.float32, (B,))
+    if max_depth is None:
+        max_depth = tree_depth(parent)
+    D1 = int(max_depth) + 1
+    if out is None:
+        i32 = dict(dtype=torch.int32, device=device)
+        out = TreeOutputs(tokens=torch.empty((B, D1), **i32), accept_len=torch.empty((B,), **i32),
+                          path=torch.empty((B, D1), **i32) if path else None,
+                          status=torch.empty((B,), **i32) if status else None)
+    lib = _native.lib()
+    ws = workspace(B, N, V, device, need=int(lib.spec_verify_tree_workspace_size(B, N, V)))
+    rc = lib.spec_verify_tree_typical(
+        _p(target_logits), parent.ctypes.data_as(ctypes.c_void_p), _p(tree_tokens), _p(uniforms),
+        ctypes.c_float(float(temperature)), ctypes.c_float(float(eps)),
+        ctypes.c_float(float(delta)), _p(out.tokens), _p(out.accept_len),
+        _dtype_code(target_logits), B, N, V, int(max_depth), _p(out.path), _p(out.status),
+        _p(ws), ws.numel(), _stream(device))
     if rc:
         raise VerifyError(rc)
     return out

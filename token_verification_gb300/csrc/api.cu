@@ -26,6 +26,8 @@ static WorkspaceLayout layout_for(int B, int R, int V) {
   l.zero_bytes = o;
   l.rec = o;        o = align256(o + sizeof(float2) * (size_t)B * R * NC);
   l.lx = o;         o = align256(o + sizeof(float) * (size_t)B * R);
+  l.thr = o;        o = align256(o + sizeof(float) * (size_t)B * R);
+  l.ent = o;        o = align256(o + sizeof(float) * (size_t)B * R * NC);
   l.total = o;
   return l;
 }
@@ -85,7 +87,8 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
                                int32_t* out_packed, int32_t* out_batch_id, float* out_accept_prob,
                                int32_t* out_status, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int greedy_prob,
-                               const uint32_t* mask = nullptr) {
+                               const uint32_t* mask = nullptr, int top_k = 0,
+                               float top_p = 1.f, float eps = 0.f, float delta = 0.f) {
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
   if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return SV_ERR_SHAPE;
   if (B == 0) {
@@ -121,11 +124,28 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.mask = mask;
   p.mask_words = (V + 31) / 32;
   p.mask_bulk = (mask && vec && aligned16(mask) && p.mask_words % 4 == 0) ? 1 : 0;
+  p.top_k = top_k;
+  p.top_p = top_p;
+  p.filter = (mode != kGreedy && ((top_k > 0 && top_k < V) || top_p < 1.f)) ? 1 : 0;
+  if (p.filter) {  // rows split into whole chunks of at most kFilterSlabBytes per CTA
+    const int esz = dtype == SV_BF16 ? 2 : 4;
+    const int NC = (V + kChunk - 1) / kChunk;
+    const int max_cpc = kFilterSlabBytes / (kChunk * esz);
+    const int ncta0 = (NC + max_cpc - 1) / max_cpc;
+    if (ncta0 > kFilterMaxCta) return SV_ERR_SHAPE;
+    p.filter_cpc = (NC + ncta0 - 1) / ncta0;
+    p.filter_ncta = (NC + p.filter_cpc - 1) / p.filter_cpc;
+    if ((long long)B * R * p.filter_ncta >= (1LL << 31)) return SV_ERR_SHAPE;
+  }
   char* base = static_cast<char*>(ws);
   p.err = reinterpret_cast<int*>(base + l.counters);
   p.fin_ticket = p.err + 1;
   p.rec = reinterpret_cast<float2*>(base + l.rec);
   p.lx = reinterpret_cast<float*>(base + l.lx);
+  p.thr = reinterpret_cast<float*>(base + l.thr);
+  p.ent = reinterpret_cast<float*>(base + l.ent);
+  p.eps = eps;
+  p.delta = delta;
   p.B = B;
   p.K = K;
   p.V = V;
@@ -210,6 +230,116 @@ sv_status spec_verify_greedy_masked(const void* target_logits, const int32_t* dr
                        (cudaStream_t)stream, 0, token_mask);
 }
 
+sv_status spec_verify_sample_filtered(const void* target_logits, const void* draft_logits,
+                                      const int32_t* draft_tokens, const float* uniforms,
+                                      float temperature, int top_k, float top_p,
+                                      const uint32_t* token_mask, int32_t* out_tokens,
+                                      int32_t* out_accept_len, sv_dtype dtype, int B, int K, int V,
+                                      const int32_t* draft_lens, int32_t* out_cu_accept,
+                                      int32_t* out_packed, int32_t* out_batch_id,
+                                      float* out_accept_prob, int32_t* out_status,
+                                      void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
+  if (top_k < 0 || !(top_p > 0.f && top_p <= 1.f)) return SV_ERR_FILTER;
+  if (token_mask && ((uintptr_t)token_mask & 3u)) return SV_ERR_NULL;
+  const int mode = temperature == 0.f ? kGreedy : (draft_logits ? kDense : kOneHot);
+  return verify_common(mode, target_logits, mode == kDense ? draft_logits : nullptr, draft_tokens,
+                       uniforms, temperature, out_tokens, out_accept_len, dtype, B, K, V,
+                       draft_lens, out_cu_accept, out_packed, out_batch_id, out_accept_prob,
+                       out_status, workspace, ws_bytes, (cudaStream_t)stream, 1, token_mask, top_k,
+                       top_p);
+}
+
+sv_status spec_verify_typical(const void* target_logits, const int32_t* draft_tokens,
+                              const float* uniforms, float temperature, float eps, float delta,
+                              int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
+                              int K, int V, const int32_t* draft_lens, int32_t* out_cu_accept,
+                              int32_t* out_packed, int32_t* out_batch_id, float* out_accept_prob,
+                              int32_t* out_status, void* workspace, size_t ws_bytes,
+                              sv_stream_t stream) {
+  if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
+  if (!(eps >= 0.f) || !(delta >= 0.f) || isinf(eps) || isinf(delta)) return SV_ERR_FILTER;
+  const int mode = temperature == 0.f ? kGreedy : kTypical;
+  return verify_common(mode, target_logits, nullptr, draft_tokens, uniforms, temperature,
+                       out_tokens, out_accept_len, dtype, B, K, V, draft_lens, out_cu_accept,
+                       out_packed, out_batch_id, out_accept_prob, out_status, workspace, ws_bytes,
+                       (cudaStream_t)stream, 1, nullptr, 0, 1.f, eps, delta);
+}
+
+size_t spec_verify_tree_workspace_size(int B, int N, int V) {
+  if (B < 0 || B > SV_MAX_B || N < 0 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_V) return 0;
+  return layout_for(B, N + 1, V).total;
+}
+
+sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tree_parent,
+                                   const int32_t* tree_tokens, const float* uniforms,
+                                   float temperature, float eps, float delta, int32_t* out_tokens,
+                                   int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
+                                   int max_depth, int32_t* out_path, int32_t* out_status,
+                                   void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
+  if (B < 0 || B > SV_MAX_B || N < 0 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_V ||
+      max_depth < 0 || max_depth > SV_MAX_TREE_NODES)
+    return SV_ERR_SHAPE;
+  if (!(temperature > 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
+  if (!(eps >= 0.f) || !(delta >= 0.f) || isinf(eps) || isinf(delta)) return SV_ERR_FILTER;
+  if (B == 0) return SV_OK;
+  if (!target_logits || !out_tokens || !out_accept_len || !uniforms) return SV_ERR_NULL;
+  if (N > 0 && (!tree_parent || !tree_tokens)) return SV_ERR_NULL;
+  TreeTypical t;
+  memset(&t, 0, sizeof t);
+  for (int n = 1; n <= N; ++n) {
+    const int pa = tree_parent[n - 1];
+    if (pa < 0 || pa >= n) return SV_ERR_TREE;
+    t.parent[n] = (short)pa;
+    t.depth[n] = (short)(t.depth[pa] + 1);
+    if (t.depth[n] > max_depth) return SV_ERR_TREE;
+  }
+  const int R = N + 1;
+  const WorkspaceLayout l = layout_for(B, R, V);
+  if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < l.total) return SV_ERR_WORKSPACE;
+  const int vec_elems = dtype == SV_BF16 ? 8 : 4;
+  const bool vec = (V % vec_elems == 0) && aligned16(target_logits);
+  const int G = chunks_per_task(dtype, vec);
+  VerifyParams p;
+  memset(&p, 0, sizeof p);
+  p.target = target_logits;
+  char* base = static_cast<char*>(workspace);
+  p.err = reinterpret_cast<int*>(base + l.counters);
+  p.fin_ticket = p.err + 1;
+  p.rec = reinterpret_cast<float2*>(base + l.rec);
+  p.lx = reinterpret_cast<float*>(base + l.lx);
+  p.thr = reinterpret_cast<float*>(base + l.thr);
+  p.ent = reinterpret_cast<float*>(base + l.ent);
+  p.mask_words = (V + 31) / 32;
+  p.top_p = 1.f;
+  p.eps = eps;
+  p.delta = delta;
+  p.B = B;
+  p.K = N;  // the tree's rows play the part of positions 0..N
+  p.V = V;
+  p.NC = (V + kChunk - 1) / kChunk;
+  p.R = R;
+  p.TPR = (p.NC + G - 1) / G;
+  p.item_chunks = G;
+  p.total_tasks = (long long)B * R * p.TPR;
+  if (p.total_tasks >= (1LL << 31)) return SV_ERR_SHAPE;
+  p.div_tpr = make_fastdiv((uint32_t)p.TPR);
+  p.div_r = make_fastdiv((uint32_t)R);
+  p.cc = (float)(1.4426950408889634 / (double)temperature);
+  t.tokens = tree_tokens;
+  t.uniforms = uniforms;
+  t.out_tokens = out_tokens;
+  t.out_accept_len = out_accept_len;
+  t.out_path = out_path;
+  t.out_status = out_status;
+  t.N = N;
+  t.D1 = max_depth + 1;
+  if (prepare_workspace(workspace, l, B, R, (cudaStream_t)stream) != cudaSuccess) return SV_ERR_CUDA;
+  return launch_tree_typical(dtype, vec, p, t, (cudaStream_t)stream) == cudaSuccess ? SV_OK
+                                                                                   : SV_ERR_CUDA;
+}
+
 sv_status spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens,
                              int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
                              int K, int V, const int32_t* draft_lens, int32_t* out_cu_accept,
@@ -274,6 +404,7 @@ const char* spec_verify_status_string(sv_status s) {
     case SV_ERR_TREE: return "parent array is not a tree of depth <= max_depth";
     case SV_ERR_WORKSPACE: return "workspace NULL, misaligned or too small";
     case SV_ERR_CUDA: return "CUDA launch failed";
+    case SV_ERR_FILTER: return "top_k negative or top_p outside (0, 1]";
   }
   return "unknown status";
 }

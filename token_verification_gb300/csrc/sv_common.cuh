@@ -33,7 +33,7 @@ constexpr int kBadLogits = 2;
 constexpr int kBadDraftLen = 4;
 constexpr int kTimeout = 8;
 
-enum Mode : int { kOneHot = 0, kDense = 1, kGreedy = 2 };
+enum Mode : int { kOneHot = 0, kDense = 1, kGreedy = 2, kTypical = 3 };
 
 // ---------------------------------------------------------------------------
 // scalar primitives
@@ -440,9 +440,12 @@ __device__ __forceinline__ float lane_max_bf16(const uint4 (&raw)[4]) {
 // all -inf chunk; NaN marks a chunk that holds NaN or +inf.  The bf16 vector
 // tile uses packed instructions (bf16x2 max, fma.rn.f32x2, add.rn.f32x2);
 // every weight is rounded exactly as the scalar fmaf + ex2 of the rescan.
+// With `ent` given, *ent receives sum_j w_j t_j over the chunk, t_j = (l_j -
+// max) c the base-2 exponent of w_j (the chunk's share of the row entropy;
+// -inf elements, whose weight is 0, add nothing).
 template <typename T, int VEC>
 __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
-                                                float cc, int mask_local) {
+                                                float cc, int mask_local, float* ent = nullptr) {
   using L = Lane<T, VEC>;
   constexpr bool kPacked = sizeof(T) == 2 && VEC == 8;
   float lm = -INFINITY;
@@ -455,10 +458,13 @@ __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw
       for (int e = 0; e < VEC; ++e) lm = max_nan(lm, L::get(raw[k], e));
   }
   const float cm = warp_max_nan(lm);
-  if (!is_finite(cm)) return make_float2(cm == -INFINITY ? -INFINITY : qnan(), 0.f);
+  if (!is_finite(cm)) {
+    if (ent) *ent = 0.f;
+    return make_float2(cm == -INFINITY ? -INFINITY : qnan(), 0.f);
+  }
   if (mask_local >= 0) mask_element<T, VEC>(raw, mask_local);
   const float nb = -cm * cc;
-  float s;
+  float s, et = 0.f;
   if constexpr (kPacked) {
     const f32x2 c2 = pack2(cc, cc), nb2 = pack2(nb, nb);
     f32x2 acc[4];  // four independent accumulation chains
@@ -471,7 +477,9 @@ __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw
       for (int q = 0; q < 4; ++q) {
         float a0, a1;
         unpack2(fma2(pack2(bf16_lo(w[q]), bf16_hi(w[q])), c2, nb2), a0, a1);
-        acc[q] = add2(acc[q], pack2(ex2(a0), ex2(a1)));
+        const float e0 = ex2(a0), e1 = ex2(a1);
+        acc[q] = add2(acc[q], pack2(e0, e1));
+        if (ent) et = fmaf(e1, fmaxf(a1, -256.f), fmaf(e0, fmaxf(a0, -256.f), et));
       }
     }
     float s0, s1, s2, s3;
@@ -484,11 +492,14 @@ __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw
     for (int k = 0; k < L::NV; ++k)
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
-        const float w = ex2(fmaf(L::get(raw[k], e), cc, nb));
+        const float a = fmaf(L::get(raw[k], e), cc, nb);
+        const float w = ex2(a);
         if ((k * VEC + e) & 1) s1 += w; else s0 += w;
+        if (ent) et = fmaf(w, fmaxf(a, -256.f), et);
       }
     s = s0 + s1;
   }
+  if (ent) *ent = warp_sum(et);
   return make_float2(cm, warp_sum(s));
 }
 
@@ -575,6 +586,23 @@ __device__ __forceinline__ float2 combine_softmax_records(const float2* rec, int
     s += r.y * ex2(fmaf(r.x, cc, nb));
   }
   return make_float2(m, warp_sum(s));
+}
+
+// Entropy accumulator of a row from its chunk records and the chunks'
+// accumulators (see chunk_softmax): sum_j w_j t_j in the frame of the row
+// max m, with w_j = 2^t_j, t_j = (l_j - m) c.  A chunk of maximum m_c
+// contributes 2^((m_c - m) c) (A_c + (m_c - m) c S_c).  The row entropy in
+// nats is then ln S - ln 2 * A / S.
+__device__ __forceinline__ float combine_entropy(const float2* rec, const float* ent, int NC,
+                                                 float cc, float m) {
+  float a = 0.f;
+  for (int c = lane_id(); c < NC; c += kWarp) {
+    const float2 r = __ldcg(rec + c);
+    if (!(r.y > 0.f)) continue;
+    const float d = (r.x - m) * cc;
+    a += ex2(d) * fmaf(d, r.y, __ldcg(ent + c));
+  }
+  return warp_sum(a);
 }
 
 }  // namespace sv

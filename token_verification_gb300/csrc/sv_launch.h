@@ -18,6 +18,7 @@ struct RowSum {
   float s;
   float wx;
   int idx;
+  float h;  // typical acceptance: the row's entropy in nats
 };
 
 struct VerifyParams {
@@ -36,6 +37,14 @@ struct VerifyParams {
   const uint32_t* mask;  // [B, K+1, mask_words] grammar masks, or null
   int mask_words;        // ceil(V / 32)
   int mask_bulk;         // mask rows are 16-byte aligned: copied with the logits
+  int top_k;             // 0: off
+  float top_p;           // 1: off
+  int filter;            // top-k / top-p active: kernel A is the row-per-cluster filter kernel
+  int filter_ncta;       // CTAs per row (cluster size) in the filter kernel
+  int filter_cpc;        // chunks per filter CTA
+  float* thr;            // [B*R] each row's cut value (lowest kept logit), filter calls
+  float* ent;            // [B*R*NC] chunk entropy accumulators (typical acceptance)
+  float eps, delta;      // typical acceptance: p(x) > min(eps, delta * exp(-H))
   // workspace
   int* err;          // [1] set when a bounded wait gave up
   int* fin_ticket;   // [1] requests finalised in this call
@@ -68,11 +77,24 @@ struct TreeParams {
   short next_sibling[kMaxTreeNodes + 1];
 };
 
+// Candidate tree for typical acceptance (built on the host).
+struct TreeTypical {
+  const int* tokens;      // [B, N] node n's token at n - 1
+  const float* uniforms;  // [B] the final draw
+  int* out_tokens;        // [B, D1]
+  int* out_accept_len;    // [B]
+  int* out_path;          // [B, D1] or null
+  int* out_status;        // [B] or null
+  int N, D1;
+  short parent[kMaxTreeNodes + 1];  // parent[n] for n >= 1
+  short depth[kMaxTreeNodes + 1];
+};
+
 enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Workspace layout for B requests, K positions, V vocabulary (dense case).
 struct WorkspaceLayout {
-  size_t counters, zero_bytes, rec, lx, total;
+  size_t counters, zero_bytes, rec, lx, thr, ent, total;
 };
 WorkspaceLayout workspace_layout(int B, int K, int V);
 
@@ -89,11 +111,17 @@ int chunks_per_task(int dtype, bool vec);
 size_t fin_cache_bytes(const VerifyParams& p);
 size_t fin_smem_bytes(const VerifyParams& p, bool dense);
 constexpr size_t kFinCacheLimit = 48 * 1024;
+// Filter kernel: each CTA holds up to this many bytes of its row (whole
+// chunks), and a row spreads over at most kFilterMaxCta CTAs.
+constexpr int kFilterSlabBytes = 64 * 1024;
+constexpr int kFilterMaxCta = 8;
 constexpr size_t kFinSmemMax = kFinCacheLimit + sizeof(float) * ((1 << 24) / kChunk);  // V <= 2^24
 
-// mode: 0 one-hot sampling, 1 dense sampling, 2 greedy
+// mode: 0 one-hot sampling, 1 dense sampling, 2 greedy, 3 typical acceptance
 cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream);
 cudaError_t launch_tree(int dtype, bool vec, const TreeParams& p, cudaStream_t stream);
+cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeTypical& t,
+                                cudaStream_t stream);
 
 }  // namespace sv

@@ -42,6 +42,25 @@ __device__ __forceinline__ const T* row_ptr(const void* base, long long row, int
   return reinterpret_cast<const T*>(base) + row * (long long)V;
 }
 
+// Elements below a row's top-k / top-p cut value become -inf.
+template <typename T, int VEC>
+__device__ __forceinline__ void threshold_chunk(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
+                                                float thr) {
+  using L = Lane<T, VEC>;
+#pragma unroll
+  for (int k = 0; k < L::NV; ++k) {
+    uint32_t bits = 0;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) bits |= (L::get(raw[k], e) >= thr ? 1u : 0u) << e;
+    L::allow_only(raw[k], bits);
+  }
+}
+
+// The row's top-k / top-p cut value (-inf: nothing cut).
+__device__ __forceinline__ float row_cut(const VerifyParams& p, long long rowid) {
+  return p.filter ? __ldcg(p.thr + rowid) : -INFINITY;
+}
+
 // Grammar mask row of position i of request b (target row i and dense
 // draft row i share it), or null without masks.
 __device__ __forceinline__ const uint32_t* mask_row(const VerifyParams& p, int b, int i) {
@@ -149,13 +168,154 @@ __device__ int select_in_tile(const float (&w)[NV * VEC], const float (&gsum)[NV
   return tok;
 }
 
-// Draw from w_j = 2^((l_j - m) c) over one row (w = 0 at mask_x and at the
-// tokens the grammar mask row `mrow` rules out) given the row's softmax
-// chunk records: the crossing chunk from the records, then one rescan of
-// that chunk in its own frame.
+// ---------------------------------------------------------------------------
+// contiguous-run draws (vector paths): lane l takes chunks / elements
+// [l*n, (l+1)*n), so one warp scan of the lane sums and one ballot locate the
+// crossing lane, and that lane walks its own run
+// ---------------------------------------------------------------------------
+
+// The chunk where the cumulative weight (in chunk order) first exceeds
+// u * total, over NC chunk weights weight(c).  frac = the share of that
+// chunk's weight below the target; with no crossing (rounding only) the last
+// chunk of positive weight with frac = 2.  Returns -1 without any weight.
+template <class F>
+__device__ int find_chunk_runs(F weight, int NC, float u, float* frac) {
+  const int lane = lane_id();
+  const int per = (NC + kWarp - 1) / kWarp;
+  const int c0 = lane * per;
+  float s = 0.f;
+  for (int i = 0; i < per; ++i)
+    if (c0 + i < NC) s += weight(c0 + i);
+  const float incl = warp_incl_scan(s);
+  const float target = u * __shfl_sync(0xffffffffu, incl, kWarp - 1);
+  const unsigned hit = __ballot_sync(0xffffffffu, s > 0.f && incl > target);
+  int c = -1;
+  float f = 0.f;
+  if (hit) {
+    const int l = __ffs(hit) - 1;
+    if (lane == l) {
+      float acc = incl - s;
+      for (int i = 0; i < per && c0 + i < NC; ++i) {
+        const float w = weight(c0 + i);
+        if (w > 0.f && acc + w > target) {
+          c = c0 + i;
+          f = fminf(fmaxf((target - acc) / w, 0.f), 1.f);
+          break;
+        }
+        acc += w;
+      }
+      if (c < 0) {  // rounding inside the lane: its last positive chunk
+        for (int i = 0; i < per && c0 + i < NC; ++i)
+          if (weight(c0 + i) > 0.f) c = c0 + i;
+        f = 2.f;
+      }
+    }
+    c = __shfl_sync(0xffffffffu, c, l);
+    f = __shfl_sync(0xffffffffu, f, l);
+  } else {
+    const unsigned pos = __ballot_sync(0xffffffffu, s > 0.f);
+    if (!pos) return -1;
+    const int l = 31 - __clz(pos);
+    if (lane == l)
+      for (int i = 0; i < per && c0 + i < NC; ++i)
+        if (weight(c0 + i) > 0.f) c = c0 + i;
+    c = __shfl_sync(0xffffffffu, c, l);
+    f = 2.f;
+  }
+  *frac = f;
+  return c;
+}
+
+// Elements 32*lane .. 32*lane+31 of chunk c, widened to fp32 (-inf past V).
+template <typename T>
+__device__ __forceinline__ void load_run(const T* row, int V, int c, float (&v)[kWarp]) {
+  constexpr int E = 16 / sizeof(T);
+  const int j0 = c * kChunk + lane_id() * kWarp;
+#pragma unroll
+  for (int g = 0; g < kWarp / E; ++g) {
+    const int j = j0 + g * E;
+    uint4 q = make_uint4(0u, 0u, 0u, 0u);
+    const bool in = j < V;  // V is a multiple of E on the vector paths
+    if (in) q = __ldg(reinterpret_cast<const uint4*>(row + j));
+    const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int e = 0; e < E; ++e) {
+      float x;
+      if constexpr (sizeof(T) == 2)
+        x = __uint_as_float((e & 1) ? (wds[e >> 1] & 0xffff0000u) : (wds[e >> 1] << 16));
+      else
+        x = __uint_as_float(wds[e]);
+      v[g * E + e] = in ? x : -INFINITY;
+    }
+  }
+}
+
+// Which of this lane's 32 elements of chunk c are allowed: the grammar mask
+// word (one word covers exactly the lane's run), the top-k / top-p cut and
+// the excluded token x.
+__device__ __forceinline__ uint32_t run_allowed(const float (&v)[kWarp], const uint32_t* mrow,
+                                                int mask_words, int c, float cut, int x) {
+  const int lane = lane_id();
+  uint32_t a = 0xffffffffu;
+  if (mrow) a = mask_word(mrow, mask_words, c);
+  if (cut > -INFINITY) {
+#pragma unroll
+    for (int e = 0; e < kWarp; ++e)
+      if (!(v[e] >= cut)) a &= ~(1u << e);
+  }
+  const int xo = x - (c * kChunk + lane * kWarp);
+  if (xo >= 0 && xo < kWarp) a &= ~(1u << xo);
+  return a;
+}
+
+// Smallest element whose cumulative weight (in index order) exceeds frac
+// times the chunk total, over the lanes' runs of weights w; zero weights are
+// never chosen; the last positive element if rounding leaves none.
+__device__ int pick_in_runs(const float (&w)[kWarp], float frac, int base_j) {
+  const int lane = lane_id();
+  float s = 0.f;
+#pragma unroll
+  for (int e = 0; e < kWarp; ++e) s += w[e];
+  const float incl = warp_incl_scan(s);
+  const float thr = frac * __shfl_sync(0xffffffffu, incl, kWarp - 1);
+  const unsigned hit = __ballot_sync(0xffffffffu, s > 0.f && incl > thr);
+  int t = -1, l;
+  if (hit) {
+    l = __ffs(hit) - 1;
+    if (lane == l) {
+      float acc = incl - s;
+      int last = -1;
+#pragma unroll
+      for (int e = 0; e < kWarp; ++e) {
+        acc += w[e];
+        if (w[e] > 0.f) {
+          last = e;
+          if (t < 0 && acc > thr) t = e;
+        }
+      }
+      if (t < 0) t = last;
+    }
+  } else {
+    const unsigned pos = __ballot_sync(0xffffffffu, s > 0.f);
+    if (!pos) return -1;
+    l = 31 - __clz(pos);
+    if (lane == l)
+#pragma unroll
+      for (int e = 0; e < kWarp; ++e)
+        if (w[e] > 0.f) t = e;
+  }
+  t = __shfl_sync(0xffffffffu, t, l);
+  return base_j + l * kWarp + t;
+}
+
+// Draw from w_j = 2^((l_j - m) c) over one row (w = 0 at mask_x, at the
+// tokens the grammar mask row `mrow` rules out and below the top-k / top-p
+// cut value) given the row's softmax chunk records: the crossing chunk from
+// the records, then one rescan of that chunk in its own frame.
 template <typename T, int VEC, bool kSharedRecords = false>
 __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V, float m, float cc,
-                                 float u, int mask_x, const uint32_t* mrow, int mask_words) {
+                                 float u, int mask_x, const uint32_t* mrow, int mask_words,
+                                 float cut) {
   using L = Lane<T, VEC>;
   const int lane = lane_id();
   const float nb = -m * cc;
@@ -164,37 +324,52 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
     const float2 r = record(c);
     return r.y * ex2(fmaf(r.x, cc, nb));
   };
-  float wc[kRecCache];  // one batch of loads for the first 256 chunks
-  float tot = 0.f;
+  if constexpr (VEC * sizeof(T) == 16) {
+    float frac = 0.f;
+    const int c = find_chunk_runs(weight, NC, u, &frac);
+    if (c < 0) return -1;
+    float v[kWarp];
+    load_run<T>(row, V, c, v);
+    const uint32_t a = run_allowed(v, mrow, mask_words, c, cut, mask_x);
+    const float nbc = -record(c).x * cc;
+    float w[kWarp];
 #pragma unroll
-  for (int t = 0; t < kRecCache; ++t) {
-    const int c = lane + t * kWarp;
-    wc[t] = c < NC ? weight(c) : 0.f;
-    tot += wc[t];
-  }
-  for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
-  tot = warp_sum(tot);
-  float frac = 0.f;
-  const int c = find_chunk(wc, weight, NC, u * tot, &frac);
-  if (c < 0) return -1;
-  typename L::Raw raw[L::NV];
-  load_chunk<T, VEC>(row, V, c, raw);
-  if (mrow) allow_only_chunk<T, VEC>(raw, mask_word(mrow, mask_words, c));
-  const float nbc = -record(c).x * cc;
-  float w[L::NV * VEC];
-  float gsum[L::NV];
+    for (int e = 0; e < kWarp; ++e) w[e] = ((a >> e) & 1u) ? ex2(fmaf(v[e], cc, nbc)) : 0.f;
+    return pick_in_runs(w, frac, c * kChunk);
+  } else {
+    float wc[kRecCache];  // one batch of loads for the first 256 chunks
+    float tot = 0.f;
 #pragma unroll
-  for (int k = 0; k < L::NV; ++k) {
-    gsum[k] = 0.f;
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) {
-      float we = ex2(fmaf(L::get(raw[k], e), cc, nbc));
-      if (c * kChunk + tile_offset<VEC>(k, e, lane) == mask_x) we = 0.f;
-      w[k * VEC + e] = we;
-      gsum[k] += we;
+    for (int t = 0; t < kRecCache; ++t) {
+      const int c = lane + t * kWarp;
+      wc[t] = c < NC ? weight(c) : 0.f;
+      tot += wc[t];
     }
+    for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
+    tot = warp_sum(tot);
+    float frac = 0.f;
+    const int c = find_chunk(wc, weight, NC, u * tot, &frac);
+    if (c < 0) return -1;
+    typename L::Raw raw[L::NV];
+    load_chunk<T, VEC>(row, V, c, raw);
+    if (mrow) allow_only_chunk<T, VEC>(raw, mask_word(mrow, mask_words, c));
+    if (cut > -INFINITY) threshold_chunk<T, VEC>(raw, cut);
+    const float nbc = -record(c).x * cc;
+    float w[L::NV * VEC];
+    float gsum[L::NV];
+#pragma unroll
+    for (int k = 0; k < L::NV; ++k) {
+      gsum[k] = 0.f;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) {
+        float we = ex2(fmaf(L::get(raw[k], e), cc, nbc));
+        if (c * kChunk + tile_offset<VEC>(k, e, lane) == mask_x) we = 0.f;
+        w[k * VEC + e] = we;
+        gsum[k] += we;
+      }
+    }
+    return select_in_tile<L::NV, VEC>(w, gsum, frac, c * kChunk);
   }
-  return select_in_tile<L::NV, VEC>(w, gsum, frac, c * kChunk);
 }
 
 // Residual weight max(0, p_j - q_j) from the two rows' maxima and 1/sums.
@@ -292,7 +467,7 @@ __device__ __forceinline__ bool row_needed(const VerifyParams& p, int r, int Kb)
 template <int MODE, typename T>
 __device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb, int x,
                                 float2* copy) {
-  RowSum rs{qnan(), 0.f, 0.f, -1};
+  RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
   const long long rowid = (long long)b * p.R + r;
   const float2* rec = p.rec + rowid * p.NC;
   if (MODE == kGreedy) {
@@ -307,6 +482,10 @@ __device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb, int
   rs.m = ms.x;
   rs.s = ms.y;
   if (has_x && is_finite(ms.x)) rs.wx = ex2(fmaf(lx, p.cc, -ms.x * p.cc));
+  if (MODE == kTypical && is_finite(ms.x) && ms.y > 0.f) {
+    const float a = combine_entropy(rec, p.ent + rowid * p.NC, p.NC, p.cc, ms.x);
+    rs.h = __logf(ms.y) - 0.6931471805599453f * a / ms.y;
+  }
   return rs;
 }
 
@@ -326,7 +505,7 @@ struct Residual {
 template <int MODE, typename T, int VEC>
 __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const float2* srec, int x,
-                                              float u, float uK, Residual* resid);
+                                              float u, float uK, int timed_out, Residual* resid);
 template <typename T, int VEC>
 __device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
                                            float* sums, int rank, int ncta);
@@ -384,16 +563,19 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   if (threadIdx.x == 0) s_resid.n = -1;
   pdl_wait();
   pdl_launch_dependents();
+  // issued before the row summaries so that its latency overlaps theirs
+  const int timed_out = (leader && warp == 0) ? __ldcg(p.err) : 0;
   if (leader) {
     for (int r = warp; r < p.R; r += kWarps) {
-      RowSum rs{qnan(), 0.f, 0.f, -1};
+      RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
       if (row_needed(p, r, Kb))
         rs = summarise_row<MODE, T>(p, b, r, Kb, r == warp ? x0 : row_token(p, b, r, Kb),
                                     s_rec ? s_rec + (long long)r * p.NC : nullptr);
       if (lane == 0) srow[r] = rs;
     }
     __syncthreads();
-    if (warp == 0) finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_rec, x, u, uK, &s_resid);
+    if (warp == 0)
+      finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_rec, x, u, uK, timed_out, &s_resid);
   }
   if (MODE == kDense) {
     // Dense drafts: the request's CTAs learn n from the first one, read the
@@ -432,12 +614,12 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
 template <int MODE, typename T, int VEC>
 __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const float2* srec, int x,
-                                              float u, float uK, Residual* resid) {
+                                              float u, float uK, int timed_out, Residual* resid) {
   const int lane = lane_id();
   const int K = p.K;
   // A bounded wait that gave up in kernel A (a device fault) invalidates the
   // whole call: its chunk records may be missing.
-  int status = __ldcg(p.err) ? kTimeout : 0;
+  int status = timed_out ? kTimeout : 0;
   if (Kb < 0 || Kb > K) {
     status |= kBadDraftLen;
     Kb = 0;
@@ -447,7 +629,7 @@ __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int 
   float theta = -1.f;
   bool pending = false;
   if (!status) {
-    RowSum rt{qnan(), 0.f, 0.f, -1}, rd{qnan(), 0.f, 0.f, -1};
+    RowSum rt{qnan(), 0.f, 0.f, -1, 0.f}, rd{qnan(), 0.f, 0.f, -1, 0.f};
     if (lane <= Kb) rt = srow[lane];
     if (MODE == kDense && lane < Kb) rd = srow[K + 1 + lane];
     bool bad = lane <= Kb && !is_finite(rt.m);
@@ -457,6 +639,10 @@ __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int 
       if (MODE == kGreedy) {
         acc = (x == rt.idx);
         theta = acc ? 1.f : 0.f;
+      } else if (MODE == kTypical) {  // p(x) > min(eps, delta * exp(-H)); reports p(x)
+        const float px = rt.wx / rt.s;
+        theta = px;
+        acc = px > fminf(p.eps, p.delta * __expf(-rt.h));
       } else {
         if (MODE == kOneHot) {  // q = point mass at x: accept iff u < p(x)
           const float px = rt.wx / (rt.s + rt.wx);
@@ -491,12 +677,13 @@ __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int 
         } else {
           const T* row = row_ptr<T>(p.target, (long long)b * (K + 1) + n, p.V);
           const uint32_t* mrow = mask_row(p, b, n);
+          const float cut = row_cut(p, (long long)b * p.R + n);
           token = srec ? draw_from_records<T, VEC, true>(row, srec + (long long)n * p.NC, p.NC,
                                                          p.V, m_n, p.cc, uK, residual ? x_n : -1,
-                                                         mrow, p.mask_words)
+                                                         mrow, p.mask_words, cut)
                        : draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + n) * p.NC,
                                                    p.NC, p.V, m_n, p.cc, uK, residual ? x_n : -1,
-                                                   mrow, p.mask_words);
+                                                   mrow, p.mask_words, cut);
           if (token < 0) status = kBadLogits;
         }
       }
@@ -514,8 +701,15 @@ __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int 
 
 template <int MODE, typename T, int VEC>
 __device__ __forceinline__ float2 chunk_record(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
-                                               int c, float cc, int mask_x) {
+                                               int c, float cc, int mask_x,
+                                               float* ent = nullptr) {
   if (MODE == kGreedy) return chunk_argmax<T, VEC>(raw, c * kChunk);
+  if (MODE == kTypical) {  // no exclusion; the chunk's entropy accumulator too
+    float a = 0.f;
+    const float2 r = chunk_softmax<T, VEC>(raw, cc, -1, &a);
+    if (lane_id() == 0) *ent = a;
+    return r;
+  }
   const int ml = (mask_x >= c * kChunk && mask_x < (c + 1) * kChunk) ? mask_x - c * kChunk : -1;
   return chunk_softmax<T, VEC>(raw, cc, ml);
 }
@@ -539,8 +733,9 @@ __device__ __forceinline__ Item decode_item(const VerifyParams& p, uint32_t it) 
   k.nch = min(p.item_chunks, p.NC - k.c0);
   k.need = row_needed(p, r, Kb);
   const int i = r > p.K ? r - p.K - 1 : r;
-  k.x = (MODE != kGreedy && k.need && i < Kb) ? __ldg(p.draft_tokens + (long long)b * p.K + i)
-                                              : -1;
+  k.x = (MODE != kGreedy && p.draft_tokens && k.need && i < Kb)
+            ? __ldg(p.draft_tokens + (long long)b * p.K + i)
+            : -1;
   return k;
 }
 
@@ -585,6 +780,7 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
   using L = Lane<T, VEC>;
   constexpr int G = L::G;
   pdl_launch_dependents();
+  pdl_wait();  // launched early (programmatic dependent launch): wait for the predecessor
   const int lane = lane_id();
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -607,8 +803,9 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
       if (g < k.nch) {
         if (mrow) allow_only_chunk<T, VEC>(raw[g], word[g]);
         record_draft_logit<T, VEC>(p, raw[g], k.c0 + g, k.rowid, k.x);
-        const float2 out =
-            chunk_record<MODE, T, VEC>(raw[g], k.c0 + g, p.cc, MODE == kOneHot ? k.x : -1);
+        const float2 out = chunk_record<MODE, T, VEC>(
+            raw[g], k.c0 + g, p.cc, MODE == kOneHot ? k.x : -1,
+            MODE == kTypical ? p.ent + (long long)k.rowid * p.NC + k.c0 + g : nullptr);
         if (lane == 0) rec[k.c0 + g] = out;
       }
   }
@@ -661,6 +858,7 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
   constexpr int S = ST::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
+  pdl_wait();  // launched early (programmatic dependent launch): wait for the predecessor
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t base = smem_u32(smem);
   auto stage_of = [&](int s) { return base + s * ST::kStageBytes; };
@@ -756,13 +954,317 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
         allow_only_chunk<T, VEC>(raw, word);
       }
       record_draft_logit<T, VEC>(p, raw, c, m.x, m.w);
-      const float2 out = chunk_record<MODE, T, VEC>(raw, c, p.cc, MODE == kOneHot ? m.w : -1);
+      const float2 out = chunk_record<MODE, T, VEC>(
+          raw, c, p.cc, MODE == kOneHot ? m.w : -1,
+          MODE == kTypical ? p.ent + (long long)m.x * p.NC + c : nullptr);
       if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
     }
     // this warp's values from the stage are consumed: hand it back
     __syncwarp();
     if (lane == 0) mbar_arrive(empty_of(s));
   }
+}
+
+// ---------------------------------------------------------------------------
+// kernel A for top-k / top-p calls: one row per thread-block cluster
+// ---------------------------------------------------------------------------
+//
+// Filtering needs, per row, the k-th largest logit and the value at which
+// the mass of the leading value classes reaches top_p - an order statistic
+// and a quantile of the mass, which a single streaming pass cannot give.  So
+// a cluster of CTAs holds the whole row in shared memory (one bulk copy per
+// CTA slab of up to 64 KB) and makes every further pass there; HBM is still
+// read once.  The cut values are found by radix descent on order-preserving
+// keys, 8 bits per pass (2 passes for bf16, 4 for fp32): a 256-bin histogram
+// per CTA of the elements still matching the key prefix, summed over the
+// cluster through distributed shared memory, then one warp picks the bin
+// where the running count (top-k) or mass (top-p) from the top reaches the
+// target.  Masses are summed as 2^-38 fixed-point integers, so the totals do
+// not depend on the order of the atomic adds and every CTA of the cluster
+// takes the same decisions.  Finally each warp reduces its chunks to the same
+// records kernel A writes, over the kept elements only, and the row's cut
+// value goes to the workspace for the finalize kernel's rescans.
+
+constexpr int kFilterThreads = 512;
+constexpr int kFilterWarps = kFilterThreads / kWarp;
+
+// Unsigned keys in the order of the values (-0.0 is taken as +0.0).
+__device__ __forceinline__ uint32_t order_key(float v) {
+  uint32_t b = __float_as_uint(v);
+  if (b == 0x80000000u) b = 0u;
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+}
+__device__ __forceinline__ float key_value(uint32_t k) {
+  return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
+}
+
+__device__ __forceinline__ float slab_value(const uint16_t* slab, int i) {
+  return __uint_as_float((uint32_t)slab[i] << 16);
+}
+__device__ __forceinline__ float slab_value(const float* slab, int i) { return slab[i]; }
+
+// Shared memory of a filter CTA after its slab (16-byte aligned offsets).
+struct FilterShared {
+  uint32_t part[kFilterWarps / 2][256][2];  // per warp pair: low / high limbs of each bin
+  unsigned long long hist[2][256];  // this CTA's bins, read by the cluster (double-buffered)
+  unsigned long long tot[256];      // cluster totals of the current pass
+  float red[kFilterWarps];          // block reduction scratch
+  float row_max;                    // this CTA's max (read by the cluster)
+  int sel_digit;
+  unsigned long long sel_front;
+};
+
+__host__ __device__ constexpr size_t filter_shared_bytes(int cpc, int esz) {
+  return (size_t)cpc * kChunk * esz + sizeof(FilterShared);
+}
+
+// Masses are counted in units of 2^-38 of the row's largest probability and
+// added as two 19-bit limbs with native 32-bit shared atomics into
+// histograms private to a pair of warps (a warp pair sees at most 4096
+// elements of a 64 KB slab, so a limb sum stays below 2^31); the limbs are
+// recombined exactly into 64-bit totals.
+constexpr float kMassScale = 274877906944.0f;  // 2^38
+constexpr int kLimbBits = 19;
+
+// One warp: the digit whose bin holds the target, scanning bins from 255
+// down.  front is the sum of the bins above it; without a bin that reaches
+// the target (rounding only) the lowest non-empty bin is taken.
+__device__ void pick_digit(const unsigned long long* tot, double base, double target,
+                           FilterShared* sh) {
+  const int lane = lane_id();
+  unsigned long long part[8], s = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    part[j] = tot[255 - (lane * 8 + j)];
+    s += part[j];
+  }
+  unsigned long long incl = s;
+#pragma unroll
+  for (int o = 1; o < kWarp; o <<= 1) {
+    const unsigned long long v = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += v;
+  }
+  const unsigned long long excl = incl - s;
+  const unsigned hit = __ballot_sync(0xffffffffu, base + (double)incl >= target);
+  if (hit) {
+    if (lane == __ffs(hit) - 1) {
+      unsigned long long acc = excl;
+      for (int j = 0; j < 8; ++j) {
+        if (base + (double)(acc + part[j]) >= target) {
+          sh->sel_digit = 255 - (lane * 8 + j);
+          sh->sel_front = acc;
+          break;
+        }
+        acc += part[j];
+      }
+    }
+  } else {
+    int low = -1;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      if (part[j]) low = j;
+    const unsigned any = __ballot_sync(0xffffffffu, low >= 0);
+    const int l = any ? 31 - __clz(any) : 0;
+    if (lane == l) {
+      const int j = low < 0 ? 7 : low;
+      unsigned long long acc = excl;
+      for (int t = 0; t < j; ++t) acc += part[t];
+      sh->sel_digit = 255 - (lane * 8 + j);
+      sh->sel_front = acc;
+    }
+  }
+}
+
+// Radix descent over the slab's keys, all CTAs of the cluster together.
+// COUNT: the key of the k-th largest element (target = k).  MASS: the key of
+// the value class where the running mass from the top reaches the target
+// (top_p times the total mass of the elements >= keep); `total` receives the
+// total in the first pass.  Elements below `keep` are ignored.
+template <typename T, bool MASS>
+__device__ uint32_t radix_descent(const T* slab, int n, float keep, float m, float cc,
+                                  double target_or_p, FilterShared* sh, int& pass, int ncta) {
+  cg::cluster_group cluster = cg::this_cluster();
+  constexpr int D = sizeof(T) == 2 ? 2 : 4;
+  uint32_t prefix = 0, pmask = 0;
+  double front = 0.0, target = MASS ? 0.0 : target_or_p;
+  const float nb = -m * cc;
+  for (int d = 0; d < D; ++d, ++pass) {
+    const int shift = 24 - 8 * d;
+    const int buf = pass & 1;
+    uint32_t* part = &sh->part[0][0][0];
+    for (int i = threadIdx.x; i < (kFilterWarps / 2) * 256 * 2; i += blockDim.x) part[i] = 0u;
+    __syncthreads();
+    uint32_t(*mine)[2] = sh->part[(threadIdx.x >> 5) >> 1];
+    const int lane = lane_id();
+    // warp-uniform loop: the lanes that fall into the same bin are merged
+    // first (match + per-group reduction), so one atomic per distinct bin
+    for (int i0 = threadIdx.x - lane; i0 < n; i0 += blockDim.x) {
+      const int i = i0 + lane;
+      int bin = 256;  // no bin
+      unsigned long long q = 0;
+      if (i < n) {
+        const float v = slab_value(slab, i);
+        const uint32_t key = order_key(v);
+        if (v >= keep && (key & pmask) == prefix) {
+          bin = (key >> shift) & 255;
+          if (MASS) q = __float2ull_rn(ex2(fmaf(v, cc, nb)) * kMassScale);
+        }
+      }
+      const unsigned grp = __match_any_sync(0xffffffffu, bin);
+      const bool leader = bin < 256 && lane == __ffs(grp) - 1;
+      if (MASS) {
+        const uint32_t lo = __reduce_add_sync(grp, (uint32_t)(q & ((1u << kLimbBits) - 1u)));
+        const uint32_t hi = __reduce_add_sync(grp, (uint32_t)(q >> kLimbBits));
+        if (leader) {
+          atomicAdd(&mine[bin][0], lo);
+          atomicAdd(&mine[bin][1], hi);
+        }
+      } else if (leader) {
+        atomicAdd(&mine[bin][0], (uint32_t)__popc(grp));
+      }
+    }
+    __syncthreads();
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+      unsigned long long t = 0;
+      for (int w = 0; w < kFilterWarps / 2; ++w)
+        t += ((unsigned long long)sh->part[w][i][1] << kLimbBits) + sh->part[w][i][0];
+      sh->hist[buf][i] = t;
+    }
+    cluster.sync();  // every CTA's histogram of this pass is complete
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) {
+      unsigned long long t = 0;
+      for (int r = 0; r < ncta; ++r) t += cluster.map_shared_rank(sh, r)->hist[buf][i];
+      sh->tot[i] = t;
+    }
+    __syncthreads();
+    if (MASS && d == 0) {  // the first pass sees every element >= keep
+      if (threadIdx.x < kWarp) {
+        unsigned long long t = 0;
+        for (int i = threadIdx.x; i < 256; i += kWarp) t += sh->tot[i];
+        for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+        if (threadIdx.x == 0) sh->sel_front = t;
+      }
+      __syncthreads();
+      target = target_or_p * (double)sh->sel_front;
+      __syncthreads();
+    }
+    if (threadIdx.x < kWarp) pick_digit(sh->tot, front, target, sh);
+    __syncthreads();
+    const int digit = sh->sel_digit;
+    front += (double)sh->sel_front;
+    if (!MASS) {  // counts: the target becomes the rank inside the chosen bin
+      target -= (double)sh->sel_front;
+      front = 0.0;
+    }
+    prefix |= (uint32_t)digit << shift;
+    pmask |= 0xffu << shift;
+    __syncthreads();
+  }
+  if (D == 2) prefix |= (prefix & 0x80000000u) ? 0u : 0xffffu;  // bf16: the low half of its keys
+  return prefix;
+}
+
+template <int MODE, typename T, int VEC>
+__global__ void __launch_bounds__(kFilterThreads) filter_rows_kernel(const VerifyParams p) {
+  using L = Lane<T, VEC>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  cg::cluster_group cluster = cg::this_cluster();
+  const int ncta = p.filter_ncta;
+  const int rank = (int)cluster.block_rank();
+  const int rowid = blockIdx.x / ncta;
+  pdl_launch_dependents();
+  pdl_wait();
+  const int b = (int)fast_div((uint32_t)rowid, p.div_r);
+  const int r = rowid - b * p.R;
+  const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : p.K;
+  if (!row_needed(p, r, Kb)) return;  // the whole cluster leaves: no barrier is pending
+  const int i_pos = r > p.K ? r - p.K - 1 : r;
+  const int x = i_pos < Kb ? __ldg(p.draft_tokens + (long long)b * p.K + i_pos) : -1;
+  const T* row = item_row<T>(p, rowid);
+  const uint32_t* mrow = item_mask(p, rowid);
+  const int cpc = p.filter_cpc;
+  const int c_lo = min(p.NC, rank * cpc), c_hi = min(p.NC, c_lo + cpc);
+  const int e_lo = c_lo * kChunk;
+  const int n = max(0, min(p.V, c_hi * kChunk) - e_lo);
+  T* slab = reinterpret_cast<T*>(smem);
+  FilterShared* sh = reinterpret_cast<FilterShared*>(smem + (size_t)cpc * kChunk * sizeof(T));
+  const int lane = lane_id(), warp = threadIdx.x >> 5;
+
+  // 1. the slab: one bulk copy on the vector path, plain loads otherwise
+  if constexpr (VEC * sizeof(T) == 16) {
+    __shared__ __align__(8) unsigned long long bar;
+    const uint32_t bar_a = smem_u32(&bar);
+    if (threadIdx.x == 0) {
+      mbar_init(bar_a, 1);
+      fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      if (n > 0)
+        bulk_load(smem_u32(slab), row + e_lo, (uint32_t)(n * sizeof(T)), bar_a);
+      else
+        asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar_a) : "memory");
+    }
+    if (!mbar_wait(bar_a, 0) && threadIdx.x == 0) atomicOr(p.err, 1);
+  } else {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) slab[i] = row[e_lo + i];
+  }
+  __syncthreads();
+  // 2. grammar mask: disallowed logits become -inf
+  if (mrow) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      const int j = e_lo + i;
+      if (!((__ldg(mrow + (j >> 5)) >> (j & 31)) & 1u)) {
+        if constexpr (sizeof(T) == 2) slab[i] = (T)0xff80u;
+        else slab[i] = -INFINITY;
+      }
+    }
+    __syncthreads();
+  }
+  // 3. the row's max over the cluster (NaN wins)
+  float lm = -INFINITY;
+  for (int i = threadIdx.x; i < n; i += blockDim.x) lm = max_nan(lm, slab_value(slab, i));
+  lm = warp_max_nan(lm);
+  if (lane == 0) sh->red[warp] = lm;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = -INFINITY;
+    for (int w = 0; w < kFilterWarps; ++w) t = max_nan(t, sh->red[w]);
+    sh->row_max = t;
+  }
+  cluster.sync();
+  float m = -INFINITY;
+  for (int q = 0; q < ncta; ++q) m = max_nan(m, cluster.map_shared_rank(sh, q)->row_max);
+  // 4. the cut value (only for rows with a finite max; others keep their
+  //    markers and are reported by the finalize kernel)
+  float thr = -INFINITY;
+  int pass = 0;
+  if (is_finite(m)) {
+    if (p.top_k > 0 && p.top_k < p.V)
+      thr = key_value(radix_descent<T, false>(slab, n, -INFINITY, m, p.cc, (double)p.top_k, sh,
+                                              pass, ncta));
+    if (p.top_p < 1.f)
+      thr = key_value(radix_descent<T, true>(slab, n, thr, m, p.cc, (double)p.top_p, sh, pass,
+                                             ncta));
+  }
+  // 5. chunk records over the kept elements, as kernel A writes them
+  for (int cl = warp; cl < c_hi - c_lo; cl += kFilterWarps) {
+    const int c = c_lo + cl;
+    typename L::Raw raw[L::NV];
+    const T* base = slab + cl * kChunk;
+#pragma unroll
+    for (int k = 0; k < L::NV; ++k) {
+      const int off = tile_offset<VEC>(k, 0, lane);
+      raw[k] = (c * kChunk + off < p.V) ? *reinterpret_cast<const typename L::Raw*>(base + off)
+                                        : L::pad();
+    }
+    if (thr > -INFINITY) threshold_chunk<T, VEC>(raw, thr);
+    record_draft_logit<T, VEC>(p, raw, c, rowid, x);
+    const float2 out = chunk_record<MODE, T, VEC>(raw, c, p.cc, MODE == kOneHot ? x : -1);
+    if (lane == 0) p.rec[(long long)rowid * p.NC + c] = out;
+  }
+  if (rank == 0 && threadIdx.x == 0) p.thr[rowid] = thr;
+  cluster.sync();  // no CTA leaves while another may still read its shared memory
 }
 
 // ---------------------------------------------------------------------------
@@ -793,6 +1295,8 @@ __device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const R
   const int lo = (int)((long long)NC * rank / ncta);
   const int hi = (int)((long long)NC * (rank + 1) / ncta);
   const uint32_t* mrow = mask_row(p, b, st.n);
+  const float cut_t = row_cut(p, (long long)b * p.R + st.n);
+  const float cut_d = row_cut(p, (long long)b * p.R + K + 1 + st.n);
   for (int c0 = lo + warp * G; c0 < hi; c0 += nwarps * G) {
     typename L::Raw rt[G][L::NV], rd[G][L::NV];
     uint32_t word[G];
@@ -810,6 +1314,8 @@ __device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const R
           allow_only_chunk<T, VEC>(rt[g], word[g]);
           allow_only_chunk<T, VEC>(rd[g], word[g]);
         }
+        if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt[g], cut_t);
+        if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd[g], cut_d);
         float w = 0.f;
 #pragma unroll
         for (int k = 0; k < L::NV; ++k)
@@ -837,7 +1343,35 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
   const float nbp = -st.mp * cc, nbq = -st.mq * cc;
   const float uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
   const uint32_t* mrow = mask_row(p, b, st.n);
+  const float cut_t = row_cut(p, (long long)b * p.R + st.n);
+  const float cut_d = row_cut(p, (long long)b * p.R + K + 1 + st.n);
   auto weight = [&](int c) { return sums[c]; };
+  int token;
+  if constexpr (VEC * sizeof(T) == 16) {
+    float frac = 0.f;
+    const int c = find_chunk_runs(weight, NC, uK, &frac);
+    if (c < 0) {  // no residual mass (rounding only): draw from p_n
+      token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V,
+                                                     st.mp, cc, uK, -1, mrow, p.mask_words, cut_t)
+                   : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
+                                               p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
+    } else {
+      float vt[kWarp], vd[kWarp];
+      load_run<T>(tr, p.V, c, vt);
+      load_run<T>(dr, p.V, c, vd);
+      const uint32_t at = run_allowed(vt, mrow, p.mask_words, c, cut_t, -1);
+      const uint32_t ad = run_allowed(vd, mrow, p.mask_words, c, cut_d, -1);
+      float w[kWarp];
+#pragma unroll
+      for (int e = 0; e < kWarp; ++e)
+        w[e] = residual_weight(((at >> e) & 1u) ? vt[e] : -INFINITY,
+                               ((ad >> e) & 1u) ? vd[e] : -INFINITY, cc, nbp, st.ip, nbq, st.iq);
+      token = pick_in_runs(w, frac, c * kChunk);
+    }
+    const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
+    write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
+    return;
+  }
   float wc[kRecCache];
   float tot = 0.f;
 #pragma unroll
@@ -848,12 +1382,11 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
   }
   for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
   tot = warp_sum(tot);
-  int token;
   if (!(tot > 0.f)) {  // no residual mass (rounding only): draw from p_n
     token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V, st.mp,
-                                                   cc, uK, -1, mrow, p.mask_words)
+                                                   cc, uK, -1, mrow, p.mask_words, cut_t)
                  : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
-                                             p.V, st.mp, cc, uK, -1, mrow, p.mask_words);
+                                             p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
   } else {
     float frac = 0.f;
     const int c = find_chunk(wc, weight, NC, uK * tot, &frac);
@@ -865,6 +1398,8 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
       allow_only_chunk<T, VEC>(rt, word);
       allow_only_chunk<T, VEC>(rd, word);
     }
+    if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt, cut_t);
+    if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd, cut_d);
     float w[L::NV * VEC];
     float gsum[L::NV];
 #pragma unroll
@@ -927,14 +1462,30 @@ int residual_cluster(const VerifyParams& p, int sms) {
 }
 
 template <int MODE, typename T, int VEC>
-cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
+cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
   DeviceInfo di;
   cudaError_t err = device_info(&di);
   if (err != cudaSuccess) return err;
   VerifyParams pc = p;
   void* args[] = {&pc};
   // A: chunk records
-  if constexpr (VEC * sizeof(T) == 16) {
+  if (p.filter) {
+    if constexpr (MODE == kGreedy || MODE == kTypical) {
+      return cudaErrorInvalidValue;  // greedy and typical calls are never filtered
+    } else {
+      const void* fk = reinterpret_cast<const void*>(filter_rows_kernel<MODE, T, VEC>);
+      static bool fattr = false;
+      if (!fattr) {
+        err = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)(kFilterSlabBytes + sizeof(FilterShared)));
+        if (err != cudaSuccess) return err;
+        fattr = true;
+      }
+      err = launch_pdl(fk, dim3((unsigned)(p.B * p.R * p.filter_ncta)), dim3(kFilterThreads), s,
+                       args, filter_shared_bytes(p.filter_cpc, (int)sizeof(T)), p.filter_ncta);
+      if (err != cudaSuccess) return err;
+    }
+  } else if constexpr (VEC * sizeof(T) == 16) {
     constexpr int smem_max = Stream<T>::smem_bytes(true);
     const int smem = Stream<T>::smem_bytes(p.mask_bulk != 0);
     static int occ = 0;
@@ -949,7 +1500,9 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
     }
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(p.total_tasks < cap ? p.total_tasks : cap);
-    verify_stream_kernel<MODE, T, VEC><<<grid, kStreamThreads, smem, s>>>(p);
+    err = launch_pdl(reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC>),
+                     dim3(grid), dim3(kStreamThreads), s, args, smem);
+    if (err != cudaSuccess) return err;
   } else {
     static int occ = 0;
     if (!occ) occ = blocks_per_sm(verify_rows_kernel<MODE, T, VEC>);
@@ -957,10 +1510,22 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
     const long long want = (p.total_tasks + warps_per_cta - 1) / warps_per_cta;
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(want < cap ? want : cap);
-    verify_rows_kernel<MODE, T, VEC><<<grid, kThreads, 0, s>>>(p);
+    err = launch_pdl(reinterpret_cast<const void*>(verify_rows_kernel<MODE, T, VEC>), dim3(grid),
+                     dim3(kThreads), s, args);
+    if (err != cudaSuccess) return err;
   }
-  err = cudaGetLastError();
+  return cudaGetLastError();
+}
+
+template <int MODE, typename T, int VEC>
+cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
+  cudaError_t err = launch_records<MODE, T, VEC>(p, s);
   if (err != cudaSuccess) return err;
+  DeviceInfo di;
+  err = device_info(&di);
+  if (err != cudaSuccess) return err;
+  VerifyParams pc = p;
+  void* args[] = {&pc};
   // F: acceptance tests and draws, one CTA per request
   const void* fin = reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>);
   const size_t fin_smem = fin_smem_bytes(p, MODE == kDense);
@@ -973,6 +1538,120 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
   }
   const int ncta = MODE == kDense ? residual_cluster(p, di.sms) : 1;
   return launch_pdl(fin, dim3(p.B * ncta), dim3(fin_threads<MODE>()), s, args, fin_smem, ncta);
+}
+
+// ---------------------------------------------------------------------------
+// typical acceptance on a candidate tree (after kernel A over all tree rows)
+// ---------------------------------------------------------------------------
+
+// One CTA per request: every row's summary (max, sum, entropy), every node's
+// typical test under its parent's distribution, the accepted subtree by one
+// thread in node order (a parent precedes its children), the deepest
+// accepted node (lowest id among equals), then the draw from its row.
+constexpr int kTreeTypicalThreads = 256;
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const VerifyParams p,
+                                                                         const TreeTypical t) {
+  __shared__ RowSum srow[kMaxTreeNodes + 1];
+  __shared__ unsigned char spass[kMaxTreeNodes + 1], sacc[kMaxTreeNodes + 1];
+  __shared__ int s_best, s_status;
+  const int b = blockIdx.x;
+  const int lane = lane_id(), warp = threadIdx.x >> 5;
+  const int N = t.N;
+  // tree tokens do not depend on kernel A
+  int bad = 0;
+  for (int n = threadIdx.x; n < N; n += blockDim.x) {
+    const int tok = __ldg(t.tokens + (long long)b * N + n);
+    bad |= (tok < 0 || tok >= p.V);
+  }
+  bad = __syncthreads_or(bad);
+  pdl_wait();
+  pdl_launch_dependents();
+  for (int r = warp; r <= N; r += kTreeTypicalThreads / kWarp) {
+    const RowSum rs = summarise_row<kTypical, T>(p, b, r, N, -1, nullptr);
+    if (lane == 0) srow[r] = rs;
+  }
+  __syncthreads();
+  for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x) {
+    const int pa = t.parent[n];
+    const RowSum rp = srow[pa];
+    unsigned char ok = 0;
+    if (!bad && is_finite(rp.m) && rp.s > 0.f) {
+      const int tok = __ldg(t.tokens + (long long)b * N + n - 1);
+      const float lp = load_logit(row_ptr<T>(p.target, (long long)b * (N + 1) + pa, p.V), tok);
+      const float px = ex2(fmaf(lp, p.cc, -rp.m * p.cc)) / rp.s;
+      ok = px > fminf(p.eps, p.delta * __expf(-rp.h));
+    }
+    spass[n] = ok;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int status = bad ? kBadToken : (__ldcg(p.err) ? kTimeout : 0);
+    sacc[0] = 1;
+    int best = 0;
+    if (!status && !is_finite(srow[0].m)) status = kBadLogits;
+    for (int n = 1; n <= N && !status; ++n) {
+      sacc[n] = sacc[t.parent[n]] && spass[n];
+      if (!sacc[n]) continue;
+      if (!is_finite(srow[n].m)) status = kBadLogits;  // an accepted node's row is needed
+      if (t.depth[n] > t.depth[best]) best = n;
+    }
+    s_best = best;
+    s_status = status;
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  const int status0 = s_status, best = s_best;
+  int token = -1;
+  if (!status0) {
+    const RowSum rb = srow[best];
+    const T* row = row_ptr<T>(p.target, (long long)b * (N + 1) + best, p.V);
+    const float u = __ldg(t.uniforms + b);
+    token = draw_from_records<T, VEC>(row, p.rec + ((long long)b * (N + 1) + best) * p.NC, p.NC,
+                                      p.V, rb.m, p.cc, u, -1, nullptr, 0, -INFINITY);
+  }
+  const int status = status0 ? status0 : (token < 0 ? kBadLogits : 0);
+  const int d = status ? -1 : t.depth[best];
+  // path and tokens, root first (one lane per level): level k < d holds the
+  // token of the path's node at level k + 1, level d the drawn token
+  for (int k = lane; k < t.D1; k += kWarp) {
+    int node = -1, tok = -1;
+    if (!status && k <= d) {
+      int a = best;  // the path's node at level k + 1 (best itself when k = d)
+      for (int up = d; up > k + 1; --up) a = t.parent[a];
+      if (k < d) {
+        tok = __ldg(t.tokens + (long long)b * N + a - 1);
+        node = t.parent[a];
+      } else {
+        tok = token;
+        node = best;
+      }
+    }
+    if (t.out_path) t.out_path[(long long)b * t.D1 + k] = node;
+    t.out_tokens[(long long)b * t.D1 + k] = tok;
+  }
+  if (lane == 0) {
+    t.out_accept_len[b] = status ? 0 : d + 1;
+    if (t.out_status) t.out_status[b] = status;
+    // the last request of the call clears the workspace counters
+    if (atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
+      *p.err = 0;
+      *p.fin_ticket = 0;
+    }
+  }
+}
+
+template <typename T, int VEC>
+cudaError_t launch_tree_typical_typed(const VerifyParams& p, const TreeTypical& t,
+                                      cudaStream_t s) {
+  cudaError_t err = launch_records<kTypical, T, VEC>(p, s);
+  if (err != cudaSuccess) return err;
+  VerifyParams pc = p;
+  TreeTypical tc = t;
+  void* args[] = {&pc, &tc};
+  return launch_pdl(reinterpret_cast<const void*>(tree_typical_kernel<T, VEC>), dim3(p.B),
+                    dim3(kTreeTypicalThreads), s, args);
 }
 
 template <int MODE>
@@ -995,11 +1674,21 @@ int chunks_per_task(int dtype, bool vec) {
   return Lane<float, 1>::G;
 }
 
+cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeTypical& t,
+                                cudaStream_t stream) {
+  if (dtype == kBF16)
+    return vec ? launch_tree_typical_typed<uint16_t, 8>(p, t, stream)
+               : launch_tree_typical_typed<uint16_t, 1>(p, t, stream);
+  return vec ? launch_tree_typical_typed<float, 4>(p, t, stream)
+             : launch_tree_typical_typed<float, 1>(p, t, stream);
+}
+
 cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream) {
   switch (mode) {
     case kOneHot: return launch_mode<kOneHot>(dtype, vec, p, stream);
     case kDense: return launch_mode<kDense>(dtype, vec, p, stream);
+    case kTypical: return launch_mode<kTypical>(dtype, vec, p, stream);
     default: return launch_mode<kGreedy>(dtype, vec, p, stream);
   }
 }

@@ -40,7 +40,9 @@ Recipe (all draws from numpy's PCG64 streams, seeded per quantity):
 The standard workloads mirror the vocabularies and draft lengths the pages
 use (Llama-3, Qwen, DeepSeek-V3 vocabularies; K = 1..5; batch up to 256);
 workload 5 is workload 2 under grammar masks, workload 6 the n-gram proposer
-that makes workload 2's kind of drafts.
+that makes workload 2's kind of drafts, workload 7 workload 2 with top-p
+sampling, workloads 8 and 9 typical acceptance on workload 4's tree and on
+workload 2's chains.
 """
 from __future__ import annotations
 
@@ -65,6 +67,15 @@ WORKLOADS = {
     5: dict(name="qwen-vocab-onehot-grammar-B256-K5-V152064", kind="sample", B=256, K=5,
             V=152064, dtype="bf16", T=1.0, drafts="onehot", p_argmax=0.6,
             grammar=dict(p_free=0.3, allowed_frac=0.02)),
+    # workload 2 sampled with temperature 0.8 and top_p 0.95
+    7: dict(name="qwen-vocab-onehot-topp-B256-K5-V152064", kind="sample", B=256, K=5,
+            V=152064, dtype="bf16", T=0.8, drafts="onehot", p_argmax=0.6, top_p=0.95),
+    # typical acceptance (Medusa's rule, eps 0.09, delta 0.3): on workload 4's tree and on
+    # workload 2's chains
+    8: dict(name="medusa-tree-typical-B32-N60-V32000", kind="tree_typical", B=32, V=32000,
+            dtype="bf16", sigma=0.5, tree="medusa60", T=1.0, eps=0.09, delta=0.3),
+    9: dict(name="qwen-vocab-onehot-typical-B256-K5-V152064", kind="typical", B=256, K=5,
+            V=152064, dtype="bf16", T=1.0, drafts="onehot", p_argmax=0.6, eps=0.09, delta=0.3),
     # the n-gram proposer that makes workload 2's drafts (prompt_lookup_max 4, K 5)
     6: dict(name="ngram-propose-B256-L4096-V152064", kind="ngram", B=256, K=5, V=152064,
             L=4096, n_min=1, n_max=4),
@@ -89,6 +100,10 @@ class Workload:
     node_tokens: Optional[np.ndarray] = None
     max_depth: int = 0
     token_mask: Optional[np.ndarray] = None  # [B, K+1, ceil(V/32)] uint32
+    top_k: int = 0                           # sampling filters (0 / 1.0: off)
+    top_p: float = 1.0
+    eps: float = 0.0                         # typical acceptance thresholds
+    delta: float = 0.0
     history: Optional[np.ndarray] = None     # [B, L] int32 n-gram proposer contexts
     history_lens: Optional[np.ndarray] = None
     meta: dict = field(default_factory=dict)
@@ -311,7 +326,7 @@ def make_tree_case(B, V, parent, *, dtype="bf16", sigma=0.5, seed=0, mask_frac=0
 # ---------------------------------------------------------------------------
 
 def make_workload(index: int, seed: int = 0) -> Workload:
-    """The standard workload ``index`` (0..6), seeded by ``seed + index``
+    """The standard workload ``index`` (0..9), seeded by ``seed + index``
     for its uniforms and by (seed + index, stream) for everything else."""
     w = WORKLOADS[index]
     s = seed + index
@@ -320,14 +335,20 @@ def make_workload(index: int, seed: int = 0) -> Workload:
         wl = Workload(dtype="int32", B=w["B"], V=w["V"], target=np.empty(0, np.float32),
                       K=w["K"], history=ctx["tokens"], history_lens=ctx["lens"],
                       meta=dict(n_min=w["n_min"], n_max=w["n_max"], L=w["L"]))
-    elif w["kind"] == "tree":
+    elif w["kind"] in ("tree", "tree_typical"):
         wl = make_tree_case(w["B"], w["V"], medusa60_parent(), dtype=w["dtype"],
                             sigma=w["sigma"], seed=s)
+        if w["kind"] == "tree_typical":  # one uniform per request for the final draw
+            wl.uniforms = np.random.default_rng(int(s)).random(w["B"], dtype=np.float32)
     else:
         wl = make_sample_case(w["B"], w["K"], w["V"], dtype=w["dtype"], T=w["T"],
                               drafts=w["drafts"], sigma=w.get("sigma", 0.0),
                               p_argmax=w.get("p_argmax", 0.6), seed=s, uniform_seed=s,
                               grammar=w.get("grammar"))
+        wl.top_k, wl.top_p = w.get("top_k", 0), w.get("top_p", 1.0)
+    if w["kind"] in ("typical", "tree_typical"):
+        wl.T, wl.eps, wl.delta = w["T"], w["eps"], w["delta"]
+        wl.meta["typical"] = True
     wl.meta["workload"] = w["name"]
     wl.meta["index"] = index
     return wl
