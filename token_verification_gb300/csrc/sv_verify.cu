@@ -1003,6 +1003,23 @@ __device__ __forceinline__ float slab_value(const uint16_t* slab, int i) {
 }
 __device__ __forceinline__ float slab_value(const float* slab, int i) { return slab[i]; }
 
+// The 16 bytes of slab group g as fp32 values (8 bf16 or 4 fp32).
+template <typename T>
+__device__ __forceinline__ void slab_group(const T* slab, int g, float (&v)[16 / sizeof(T)]) {
+  const uint4 q = reinterpret_cast<const uint4*>(slab)[g];
+  const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+  if constexpr (sizeof(T) == 2) {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      v[2 * j] = __uint_as_float(w[j] << 16);
+      v[2 * j + 1] = __uint_as_float(w[j] & 0xffff0000u);
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 4; ++j) v[j] = __uint_as_float(w[j]);
+  }
+}
+
 // Shared memory of a filter CTA after its slab (16-byte aligned offsets).
 struct FilterShared {
   uint32_t part[kFilterWarps / 2][256][2];  // per warp pair: low / high limbs of each bin
@@ -1023,8 +1040,18 @@ __host__ __device__ constexpr size_t filter_shared_bytes(int cpc, int esz) {
 // histograms private to a pair of warps (a warp pair sees at most 4096
 // elements of a 64 KB slab, so a limb sum stays below 2^31); the limbs are
 // recombined exactly into 64-bit totals.
-constexpr float kMassScale = 274877906944.0f;  // 2^38
 constexpr int kLimbBits = 19;
+
+// floor(w * 2^38) for a weight (or a sum of up to 16 weights) w in [0, 16],
+// from the bits of w with integer operations only (w = mant * 2^(e - 150),
+// so w * 2^38 = mant * 2^(e - 112)).
+__device__ __forceinline__ unsigned long long fixed_mass(float w) {
+  const uint32_t b = __float_as_uint(w);
+  const int e = (int)(b >> 23);
+  if (e == 0) return 0ull;  // zero (weights below 2^-126 are flushed)
+  const unsigned long long mant = (b & 0x7fffffu) | 0x800000u;
+  return e >= 112 ? mant << (e - 112) : (e > 112 - 24 ? mant >> (112 - e) : 0ull);
+}
 
 // One warp: the digit whose bin holds the target, scanning bins from 255
 // down.  front is the sum of the bins above it; without a bin that reaches
@@ -1095,33 +1122,43 @@ __device__ uint32_t radix_descent(const T* slab, int n, float keep, float m, flo
     for (int i = threadIdx.x; i < (kFilterWarps / 2) * 256 * 2; i += blockDim.x) part[i] = 0u;
     __syncthreads();
     uint32_t(*mine)[2] = sh->part[(threadIdx.x >> 5) >> 1];
-    const int lane = lane_id();
-    // warp-uniform loop: the lanes that fall into the same bin are merged
-    // first (match + per-group reduction), so one atomic per distinct bin
-    for (int i0 = threadIdx.x - lane; i0 < n; i0 += blockDim.x) {
-      const int i = i0 + lane;
-      int bin = 256;  // no bin
-      unsigned long long q = 0;
-      if (i < n) {
-        const float v = slab_value(slab, i);
-        const uint32_t key = order_key(v);
-        if (v >= keep && (key & pmask) == prefix) {
-          bin = (key >> shift) & 255;
-          if (MASS) q = __float2ull_rn(ex2(fmaf(v, cc, nb)) * kMassScale);
-        }
-      }
-      const unsigned grp = __match_any_sync(0xffffffffu, bin);
-      const bool leader = bin < 256 && lane == __ffs(grp) - 1;
+    // Each thread reads 16-byte groups of consecutive elements and merges
+    // runs of elements that fall into the same bin before one atomic per
+    // run (a run's mass is summed in fp32, at most 8 weights, then fixed).
+    constexpr int E = 16 / (int)sizeof(T);
+    int run_bin = -1;
+    float run_mass = 0.f;
+    uint32_t run_count = 0;
+    auto flush = [&]() {
+      if (run_bin < 0) return;
       if (MASS) {
-        const uint32_t lo = __reduce_add_sync(grp, (uint32_t)(q & ((1u << kLimbBits) - 1u)));
-        const uint32_t hi = __reduce_add_sync(grp, (uint32_t)(q >> kLimbBits));
-        if (leader) {
-          atomicAdd(&mine[bin][0], lo);
-          atomicAdd(&mine[bin][1], hi);
-        }
-      } else if (leader) {
-        atomicAdd(&mine[bin][0], (uint32_t)__popc(grp));
+        const unsigned long long q = fixed_mass(run_mass);
+        atomicAdd(&mine[run_bin][0], (uint32_t)(q & ((1u << kLimbBits) - 1u)));
+        atomicAdd(&mine[run_bin][1], (uint32_t)(q >> kLimbBits));
+      } else {
+        atomicAdd(&mine[run_bin][0], run_count);
       }
+    };
+    for (int g = threadIdx.x; g * E < n; g += blockDim.x) {
+      float v[E];
+      slab_group<T>(slab, g, v);
+#pragma unroll
+      for (int e = 0; e < E; ++e) {
+        if (g * E + e >= n || !(v[e] >= keep)) continue;
+        const uint32_t key = order_key(v[e]);
+        if ((key & pmask) != prefix) continue;
+        const int bin = (key >> shift) & 255;
+        if (bin != run_bin) {
+          flush();
+          run_bin = bin;
+          run_mass = 0.f;
+          run_count = 0;
+        }
+        if (MASS) run_mass += ex2(fmaf(v[e], cc, nb));
+        else ++run_count;
+      }
+      flush();
+      run_bin = -1;
     }
     __syncthreads();
     for (int i = threadIdx.x; i < 256; i += blockDim.x) {
@@ -1223,7 +1260,16 @@ __global__ void __launch_bounds__(kFilterThreads) filter_rows_kernel(const Verif
   }
   // 3. the row's max over the cluster (NaN wins)
   float lm = -INFINITY;
-  for (int i = threadIdx.x; i < n; i += blockDim.x) lm = max_nan(lm, slab_value(slab, i));
+  {
+    constexpr int E = 16 / (int)sizeof(T);
+    for (int g = threadIdx.x; g * E < n; g += blockDim.x) {
+      float v[E];
+      slab_group<T>(slab, g, v);
+#pragma unroll
+      for (int e = 0; e < E; ++e)
+        if (g * E + e < n) lm = max_nan(lm, v[e]);
+    }
+  }
   lm = warp_max_nan(lm);
   if (lane == 0) sh->red[warp] = lm;
   __syncthreads();
@@ -1276,27 +1322,22 @@ __host__ __device__ constexpr int residual_group() {
   return Lane<T, VEC>::G > 1 ? Lane<T, VEC>::G / 2 : 1;
 }
 
-// Request b was rejected at st.n: the chunk sums of max(0, p_n - q_n) over
-// the (target, draft) row pair.  CTA `rank` of the request's `ncta` takes a
-// contiguous range of chunks, its warps groups of consecutive chunks; each
-// sum goes to sums[c] (the first CTA's shared memory).  Called by every
-// thread of the CTA.
-template <typename T, int VEC>
-__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
-                                           float* sums, int rank, int ncta) {
+// The residual chunk sums over chunks [lo, hi) (kExtra: with grammar masks
+// and top-k / top-p cuts applied).
+template <typename T, int VEC, bool kExtra>
+__device__ __forceinline__ void residual_sums_loop(const VerifyParams& p, int b, const Residual& st,
+                                                   float* sums, int lo, int hi) {
   using L = Lane<T, VEC>;
   constexpr int G = residual_group<T, VEC>();
   const int lane = lane_id(), warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int K = p.K, NC = p.NC;
+  const int K = p.K;
   const float cc = p.cc;
   const T* tr = row_ptr<T>(p.target, (long long)b * (K + 1) + st.n, p.V);
   const T* dr = row_ptr<T>(p.draft, (long long)b * K + st.n, p.V);
   const float nbp = -st.mp * cc, nbq = -st.mq * cc;
-  const int lo = (int)((long long)NC * rank / ncta);
-  const int hi = (int)((long long)NC * (rank + 1) / ncta);
-  const uint32_t* mrow = mask_row(p, b, st.n);
-  const float cut_t = row_cut(p, (long long)b * p.R + st.n);
-  const float cut_d = row_cut(p, (long long)b * p.R + K + 1 + st.n);
+  const uint32_t* mrow = kExtra ? mask_row(p, b, st.n) : nullptr;
+  const float cut_t = kExtra ? row_cut(p, (long long)b * p.R + st.n) : -INFINITY;
+  const float cut_d = kExtra ? row_cut(p, (long long)b * p.R + K + 1 + st.n) : -INFINITY;
   for (int c0 = lo + warp * G; c0 < hi; c0 += nwarps * G) {
     typename L::Raw rt[G][L::NV], rd[G][L::NV];
     uint32_t word[G];
@@ -1305,17 +1346,19 @@ __device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const R
       if (c0 + g < hi) {
         load_chunk<T, VEC>(tr, p.V, c0 + g, rt[g]);
         load_chunk<T, VEC>(dr, p.V, c0 + g, rd[g]);
-        if (mrow) word[g] = mask_word(mrow, p.mask_words, c0 + g);
+        if (kExtra && mrow) word[g] = mask_word(mrow, p.mask_words, c0 + g);
       }
 #pragma unroll
     for (int g = 0; g < G; ++g)
       if (c0 + g < hi) {
-        if (mrow) {
-          allow_only_chunk<T, VEC>(rt[g], word[g]);
-          allow_only_chunk<T, VEC>(rd[g], word[g]);
+        if (kExtra) {
+          if (mrow) {
+            allow_only_chunk<T, VEC>(rt[g], word[g]);
+            allow_only_chunk<T, VEC>(rd[g], word[g]);
+          }
+          if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt[g], cut_t);
+          if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd[g], cut_d);
         }
-        if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt[g], cut_t);
-        if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd[g], cut_d);
         float w = 0.f;
 #pragma unroll
         for (int k = 0; k < L::NV; ++k)
@@ -1327,6 +1370,23 @@ __device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const R
         if (lane == 0) sums[c0 + g] = w;
       }
   }
+}
+
+// Request b was rejected at st.n: the chunk sums of max(0, p_n - q_n) over
+// the (target, draft) row pair.  CTA `rank` of the request's `ncta` takes a
+// contiguous range of chunks, its warps groups of consecutive chunks; each
+// sum goes to sums[c] (the first CTA's shared memory).  Calls without grammar
+// masks or filters take a loop without their checks.  Called by every thread
+// of the CTA.
+template <typename T, int VEC>
+__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
+                                           float* sums, int rank, int ncta) {
+  const int lo = (int)((long long)p.NC * rank / ncta);
+  const int hi = (int)((long long)p.NC * (rank + 1) / ncta);
+  if (p.mask || p.filter)
+    residual_sums_loop<T, VEC, true>(p, b, st, sums, lo, hi);
+  else
+    residual_sums_loop<T, VEC, false>(p, b, st, sums, lo, hi);
 }
 
 // One warp: the residual draw from the chunk sums (the crossing chunk, then
@@ -1370,53 +1430,53 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
     }
     const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
     write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
-    return;
-  }
-  float wc[kRecCache];
-  float tot = 0.f;
-#pragma unroll
-  for (int t = 0; t < kRecCache; ++t) {
-    const int c = lane + t * kWarp;
-    wc[t] = c < NC ? weight(c) : 0.f;
-    tot += wc[t];
-  }
-  for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
-  tot = warp_sum(tot);
-  if (!(tot > 0.f)) {  // no residual mass (rounding only): draw from p_n
-    token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V, st.mp,
-                                                   cc, uK, -1, mrow, p.mask_words, cut_t)
-                 : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
-                                             p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
   } else {
-    float frac = 0.f;
-    const int c = find_chunk(wc, weight, NC, uK * tot, &frac);
-    typename L::Raw rt[L::NV], rd[L::NV];
-    load_chunk<T, VEC>(tr, p.V, c, rt);
-    load_chunk<T, VEC>(dr, p.V, c, rd);
-    if (mrow) {
-      const uint32_t word = mask_word(mrow, p.mask_words, c);
-      allow_only_chunk<T, VEC>(rt, word);
-      allow_only_chunk<T, VEC>(rd, word);
+    float wc[kRecCache];
+    float tot = 0.f;
+#pragma unroll
+    for (int t = 0; t < kRecCache; ++t) {
+      const int c = lane + t * kWarp;
+      wc[t] = c < NC ? weight(c) : 0.f;
+      tot += wc[t];
     }
-    if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt, cut_t);
-    if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd, cut_d);
-    float w[L::NV * VEC];
-    float gsum[L::NV];
-#pragma unroll
-    for (int k = 0; k < L::NV; ++k) {
-      gsum[k] = 0.f;
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        const float we =
-            residual_weight(L::get(rt[k], e), L::get(rd[k], e), cc, nbp, st.ip, nbq, st.iq);
-        w[k * VEC + e] = we;
-        gsum[k] += we;
+    for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
+    tot = warp_sum(tot);
+    if (!(tot > 0.f)) {  // no residual mass (rounding only): draw from p_n
+      token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V, st.mp,
+                                                     cc, uK, -1, mrow, p.mask_words, cut_t)
+                   : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
+                                               p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
+    } else {
+      float frac = 0.f;
+      const int c = find_chunk(wc, weight, NC, uK * tot, &frac);
+      typename L::Raw rt[L::NV], rd[L::NV];
+      load_chunk<T, VEC>(tr, p.V, c, rt);
+      load_chunk<T, VEC>(dr, p.V, c, rd);
+      if (mrow) {
+        const uint32_t word = mask_word(mrow, p.mask_words, c);
+        allow_only_chunk<T, VEC>(rt, word);
+        allow_only_chunk<T, VEC>(rd, word);
       }
+      if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt, cut_t);
+      if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd, cut_d);
+      float w[L::NV * VEC];
+      float gsum[L::NV];
+#pragma unroll
+      for (int k = 0; k < L::NV; ++k) {
+        gsum[k] = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) {
+          const float we =
+              residual_weight(L::get(rt[k], e), L::get(rd[k], e), cc, nbp, st.ip, nbq, st.iq);
+          w[k * VEC + e] = we;
+          gsum[k] += we;
+        }
+      }
+      token = select_in_tile<L::NV, VEC>(w, gsum, frac, c * kChunk);
     }
-    token = select_in_tile<L::NV, VEC>(w, gsum, frac, c * kChunk);
+    const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
+    write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
   }
-  const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
-  write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
 }
 
 // ---------------------------------------------------------------------------
@@ -1500,9 +1560,17 @@ cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
     }
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(p.total_tasks < cap ? p.total_tasks : cap);
-    err = launch_pdl(reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC>),
-                     dim3(grid), dim3(kStreamThreads), s, args, smem);
-    if (err != cudaSuccess) return err;
+    // Chained to the previous call's finalize kernel by programmatic dependent
+    // launch, except behind dense-draft calls, whose finalize CTAs fill whole
+    // SMs: there it measured slower (one-hot B256 K5: +2.8%, dense B64 K3:
+    // -3%), so dense calls launch it plainly.
+    if (MODE != kDense) {
+      err = launch_pdl(reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC>),
+                       dim3(grid), dim3(kStreamThreads), s, args, smem);
+      if (err != cudaSuccess) return err;
+    } else {
+      verify_stream_kernel<MODE, T, VEC><<<grid, kStreamThreads, smem, s>>>(p);
+    }
   } else {
     static int occ = 0;
     if (!occ) occ = blocks_per_sm(verify_rows_kernel<MODE, T, VEC>);
