@@ -1142,42 +1142,112 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
 // typical test under its parent's distribution, the accepted subtree by one
 // thread in node order (a parent precedes its children), the deepest
 // accepted node (lowest id among equals), then the draw from its row.
-constexpr int kTreeTypicalThreads = 256;
+constexpr int kTreeTypicalThreads = 512;
+constexpr size_t kTreeCacheLimit = 96 * 1024;  // records kept in shared memory for the draw
+
+// Summaries of every tree row with the loads of up to 4 rows per warp issued
+// together (rows of up to 64 chunks; wider rows one at a time); the records
+// go to `cache` (shared memory) when given.  Same arithmetic as
+// combine_softmax_records and combine_entropy.
+template <typename T>
+__device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum* srow,
+                                    float2* cache) {
+  const int lane = lane_id(), warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  const int NC = p.NC;
+  const float cc = p.cc;
+  if (NC > 2 * kWarp) {
+    for (int r = warp; r <= N; r += nw) {
+      const RowSum rs = summarise_row<kTypical, T>(p, b, r, N, -1,
+                                                   cache ? cache + (long long)r * NC : nullptr);
+      if (lane == 0) srow[r] = rs;
+    }
+    return;
+  }
+  constexpr int J = 4;
+  for (int r0 = warp; r0 <= N; r0 += nw * J) {
+    float2 rc[J][2];
+    float ea[J][2];
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int r = r0 + j * nw;
+      const long long base = ((long long)b * p.R + r) * NC;
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int c = lane + q * kWarp;
+        const bool in = r <= N && c < NC;
+        rc[j][q] = in ? __ldcg(p.rec + base + c) : make_float2(-INFINITY, 0.f);
+        ea[j][q] = in ? __ldcg(p.ent + base + c) : 0.f;
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < J; ++j) {
+      const int r = r0 + j * nw;
+      if (r > N) break;
+      const float m = warp_max_nan(max_nan(rc[j][0].x, rc[j][1].x));
+      RowSum rs{m == -INFINITY ? -INFINITY : qnan(), 0.f, 0.f, -1, 0.f};
+      if (is_finite(m)) {
+        const float nb = -m * cc;
+        float sum = 0.f, a = 0.f;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const float2 rq = rc[j][q];
+          sum += rq.y * ex2(fmaf(rq.x, cc, nb));
+          if (rq.y > 0.f) {
+            const float d = (rq.x - m) * cc;
+            a += ex2(d) * fmaf(d, rq.y, ea[j][q]);
+          }
+        }
+        sum = warp_sum(sum);
+        a = warp_sum(a);
+        rs.m = m;
+        rs.s = sum;
+        if (sum > 0.f) rs.h = __logf(sum) - 0.6931471805599453f * a / sum;
+      }
+      if (cache) {
+#pragma unroll
+        for (int q = 0; q < 2; ++q)
+          if (lane + q * kWarp < NC) cache[(long long)r * NC + lane + q * kWarp] = rc[j][q];
+      }
+      if (lane == 0) srow[r] = rs;
+    }
+  }
+}
 
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const VerifyParams p,
                                                                          const TreeTypical t) {
+  extern __shared__ float2 s_cache[];
   __shared__ RowSum srow[kMaxTreeNodes + 1];
   __shared__ unsigned char spass[kMaxTreeNodes + 1], sacc[kMaxTreeNodes + 1];
   __shared__ int s_best, s_status;
   const int b = blockIdx.x;
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const int N = t.N;
-  // tree tokens do not depend on kernel A
-  int bad = 0;
-  for (int n = threadIdx.x; n < N; n += blockDim.x) {
-    const int tok = __ldg(t.tokens + (long long)b * N + n);
-    bad |= (tok < 0 || tok >= p.V);
+  const bool cached = (size_t)(N + 1) * p.NC * sizeof(float2) <= kTreeCacheLimit;
+  // the tree tokens and each node's logit in its parent's row are inputs:
+  // read them before waiting for kernel A
+  int bad = 0, tok = 0;
+  float lp = 0.f;
+  const int n_mine = 1 + threadIdx.x;  // N <= 256 < the CTA's threads
+  if (n_mine <= N) {
+    tok = __ldg(t.tokens + (long long)b * N + n_mine - 1);
+    bad = tok < 0 || tok >= p.V;
+    if (!bad)
+      lp = load_logit(row_ptr<T>(p.target, (long long)b * (N + 1) + t.parent[n_mine], p.V), tok);
   }
   bad = __syncthreads_or(bad);
   pdl_wait();
   pdl_launch_dependents();
-  for (int r = warp; r <= N; r += kTreeTypicalThreads / kWarp) {
-    const RowSum rs = summarise_row<kTypical, T>(p, b, r, N, -1, nullptr);
-    if (lane == 0) srow[r] = rs;
-  }
+  summarise_tree_rows<T>(p, b, N, srow, cached ? s_cache : nullptr);
   __syncthreads();
-  for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x) {
-    const int pa = t.parent[n];
-    const RowSum rp = srow[pa];
+  if (n_mine <= N) {
+    const RowSum rp = srow[t.parent[n_mine]];
     unsigned char ok = 0;
     if (!bad && is_finite(rp.m) && rp.s > 0.f) {
-      const int tok = __ldg(t.tokens + (long long)b * N + n - 1);
-      const float lp = load_logit(row_ptr<T>(p.target, (long long)b * (N + 1) + pa, p.V), tok);
       const float px = ex2(fmaf(lp, p.cc, -rp.m * p.cc)) / rp.s;
       ok = px > fminf(p.eps, p.delta * __expf(-rp.h));
     }
-    spass[n] = ok;
+    spass[n_mine] = ok;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -1202,8 +1272,11 @@ __global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const
     const RowSum rb = srow[best];
     const T* row = row_ptr<T>(p.target, (long long)b * (N + 1) + best, p.V);
     const float u = __ldg(t.uniforms + b);
-    token = draw_from_records<T, VEC>(row, p.rec + ((long long)b * (N + 1) + best) * p.NC, p.NC,
-                                      p.V, rb.m, p.cc, u, -1, nullptr, 0, -INFINITY);
+    token = cached ? draw_from_records<T, VEC, true>(row, s_cache + (long long)best * p.NC, p.NC,
+                                                     p.V, rb.m, p.cc, u, -1, nullptr, 0, -INFINITY)
+                   : draw_from_records<T, VEC>(row, p.rec + ((long long)b * (N + 1) + best) * p.NC,
+                                               p.NC, p.V, rb.m, p.cc, u, -1, nullptr, 0,
+                                               -INFINITY);
   }
   const int status = status0 ? status0 : (token < 0 ? kBadLogits : 0);
   const int d = status ? -1 : t.depth[best];
@@ -1244,8 +1317,17 @@ cudaError_t launch_tree_typical_typed(const VerifyParams& p, const TreeTypical& 
   VerifyParams pc = p;
   TreeTypical tc = t;
   void* args[] = {&pc, &tc};
-  return launch_pdl(reinterpret_cast<const void*>(tree_typical_kernel<T, VEC>), dim3(p.B),
-                    dim3(kTreeTypicalThreads), s, args);
+  const void* fn = reinterpret_cast<const void*>(tree_typical_kernel<T, VEC>);
+  static bool attr = false;
+  if (!attr) {
+    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               (int)kTreeCacheLimit);
+    if (err != cudaSuccess) return err;
+    attr = true;
+  }
+  const size_t cache = (size_t)(t.N + 1) * p.NC * sizeof(float2);
+  return launch_pdl(fn, dim3(p.B), dim3(kTreeTypicalThreads), s, args,
+                    cache <= kTreeCacheLimit ? cache : 0);
 }
 
 template <int MODE>
