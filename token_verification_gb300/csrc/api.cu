@@ -5,6 +5,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 #include <unordered_map>
 
@@ -35,18 +36,18 @@ static WorkspaceLayout layout_for(int B, int R, int V) {
 WorkspaceLayout workspace_layout(int B, int K, int V) { return layout_for(B, 2 * K + 1, V); }
 
 cudaError_t device_info(DeviceInfo* out) {
-  static int sms[64] = {0};
+  static std::atomic<int> sms[64];  // 0 until read; racing readers store the same value
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  if (!sms[dev]) {
-    int n = 0;
+  int n = sms[dev].load(std::memory_order_relaxed);
+  if (!n) {
     err = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (err != cudaSuccess) return err;
-    sms[dev] = n;
+    sms[dev].store(n, std::memory_order_relaxed);
   }
-  out->sms = sms[dev];
+  out->sms = n;
   return cudaSuccess;
 }
 

@@ -37,11 +37,6 @@ __device__ __forceinline__ float key_value(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7fffffffu) : ~k);
 }
 
-__device__ __forceinline__ float slab_value(const uint16_t* slab, int i) {
-  return __uint_as_float((uint32_t)slab[i] << 16);
-}
-__device__ __forceinline__ float slab_value(const float* slab, int i) { return slab[i]; }
-
 // The 16 bytes of slab group g as fp32 values (8 bf16 or 4 fp32).
 template <typename T>
 __device__ __forceinline__ void slab_group(const T* slab, int g, float (&v)[16 / sizeof(T)]) {
@@ -406,14 +401,13 @@ cudaError_t launch_filter(int mode, int dtype, bool vec, const VerifyParams& p, 
   } else {
     return cudaErrorInvalidValue;  // greedy and typical calls are never filtered
   }
-  static bool attr[2][2][2] = {};
-  bool& done = attr[mode == kDense][dtype == kBF16][vec ? 1 : 0];
-  if (!done) {
-    const cudaError_t err = cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (int)(kFilterSlabBytes + sizeof(FilterShared)));
-    if (err != cudaSuccess) return err;
-    done = true;
-  }
+  static PerDevice once[2][2][2];
+  const cudaError_t err =
+      per_device(once[mode == kDense][dtype == kBF16][vec ? 1 : 0], nullptr, [&](int&) {
+        return cudaFuncSetAttribute(fk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)(kFilterSlabBytes + sizeof(FilterShared)));
+      });
+  if (err != cudaSuccess) return err;
   return launch_pdl(fk, dim3((unsigned)(p.B * p.R * p.filter_ncta)), dim3(kFilterThreads), s,
                     args, filter_shared_bytes(p.filter_cpc, dtype == kBF16 ? 2 : 4),
                     p.filter_ncta);

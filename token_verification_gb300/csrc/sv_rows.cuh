@@ -4,6 +4,8 @@
 
 #include <cooperative_groups.h>
 
+#include <mutex>
+
 #include "sv_common.cuh"
 #include "sv_launch.h"
 
@@ -96,6 +98,32 @@ __device__ __forceinline__ const uint32_t* item_mask(const VerifyParams& p, int 
   const int b = (int)fast_div((uint32_t)rowid, p.div_r);
   const int r = rowid - b * p.R;
   return mask_row(p, b, r > p.K ? r - p.K - 1 : r);
+}
+
+// One-time set-up of a kernel on each device (function attributes and
+// occupancy are per device): the first call with a device current runs
+// `setup(value)`; later calls return the cached value.  Thread-safe.
+struct PerDevice {
+  std::mutex mu;
+  unsigned long long done = 0;  // bit d: device d set up
+  int value[64] = {};
+};
+template <class F>
+cudaError_t per_device(PerDevice& once, int* value, F setup) {
+  int dev = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(once.mu);
+  if (!((once.done >> dev) & 1ull)) {
+    int v = 0;
+    err = setup(v);
+    if (err != cudaSuccess) return err;
+    once.value[dev] = v;
+    once.done |= 1ull << dev;
+  }
+  if (value) *value = once.value[dev];
+  return cudaSuccess;
 }
 
 // Launch with programmatic dependent launch allowed (and a cluster of

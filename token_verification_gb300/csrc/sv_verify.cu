@@ -1074,16 +1074,19 @@ cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
   } else if constexpr (VEC * sizeof(T) == 16) {
     constexpr int smem_max = Stream<T>::smem_bytes(true);
     const int smem = Stream<T>::smem_bytes(p.mask_bulk != 0);
-    static int occ = 0;
-    if (!occ) {
-      err = cudaFuncSetAttribute(verify_stream_kernel<MODE, T, VEC>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
-      if (err != cudaSuccess) return err;
+    static PerDevice once;
+    int occ = 1;
+    err = per_device(once, &occ, [&](int& v) {
+      cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<MODE, T, VEC>,
+                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+      if (e != cudaSuccess) return e;
       if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-              &occ, verify_stream_kernel<MODE, T, VEC>, kStreamThreads, smem_max) != cudaSuccess ||
-          occ < 1)
-        occ = 1;
-    }
+              &v, verify_stream_kernel<MODE, T, VEC>, kStreamThreads, smem_max) != cudaSuccess ||
+          v < 1)
+        v = 1;
+      return cudaSuccess;
+    });
+    if (err != cudaSuccess) return err;
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(p.total_tasks < cap ? p.total_tasks : cap);
     // Chained to the previous call's finalize kernel by programmatic dependent
@@ -1098,8 +1101,13 @@ cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
       verify_stream_kernel<MODE, T, VEC><<<grid, kStreamThreads, smem, s>>>(p);
     }
   } else {
-    static int occ = 0;
-    if (!occ) occ = blocks_per_sm(verify_rows_kernel<MODE, T, VEC>);
+    static PerDevice once;
+    int occ = 1;
+    err = per_device(once, &occ, [&](int& v) {
+      v = blocks_per_sm(verify_rows_kernel<MODE, T, VEC>);
+      return cudaSuccess;
+    });
+    if (err != cudaSuccess) return err;
     const int warps_per_cta = kThreads / kWarp;
     const long long want = (p.total_tasks + warps_per_cta - 1) / warps_per_cta;
     const long long cap = (long long)di.sms * occ;
@@ -1123,13 +1131,12 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
   // F: acceptance tests and draws, one CTA per request
   const void* fin = reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>);
   const size_t fin_smem = fin_smem_bytes(p, MODE == kDense);
-  static bool fin_attr = false;
-  if (!fin_attr) {
-    err = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kFinSmemMax);
-    if (err != cudaSuccess) return err;
-    fin_attr = true;
-  }
+  static PerDevice once;
+  err = per_device(once, nullptr, [&](int&) {
+    return cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kFinSmemMax);
+  });
+  if (err != cudaSuccess) return err;
   const int ncta = MODE == kDense ? residual_cluster(p, di.sms) : 1;
   return launch_pdl(fin, dim3(p.B * ncta), dim3(fin_threads<MODE>()), s, args, fin_smem, ncta);
 }
@@ -1318,13 +1325,12 @@ cudaError_t launch_tree_typical_typed(const VerifyParams& p, const TreeTypical& 
   TreeTypical tc = t;
   void* args[] = {&pc, &tc};
   const void* fn = reinterpret_cast<const void*>(tree_typical_kernel<T, VEC>);
-  static bool attr = false;
-  if (!attr) {
-    err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               (int)kTreeCacheLimit);
-    if (err != cudaSuccess) return err;
-    attr = true;
-  }
+  static PerDevice once;
+  err = per_device(once, nullptr, [&](int&) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kTreeCacheLimit);
+  });
+  if (err != cudaSuccess) return err;
   const size_t cache = (size_t)(t.N + 1) * p.NC * sizeof(float2);
   return launch_pdl(fn, dim3(p.B), dim3(kTreeTypicalThreads), s, args,
                     cache <= kTreeCacheLimit ? cache : 0);
