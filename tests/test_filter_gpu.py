@@ -1,6 +1,7 @@
 """Top-k / top-p filtered verification: CUDA path vs the fp64 oracle (needs
 a GPU).  The rows of a filtered call are held by clusters of CTAs (1 to 8
-per row); the cases cover both logit types, the bulk-copy and the scalar
+per row); the cases cover the cut found among the candidates and on the
+whole slab, both logit types, the bulk-copy and the scalar
 slab loads, several cluster sizes, exact ties at the cuts (quantised
 logits), dense and one-hot drafts, grammar masks together with the
 filters, ragged drafts, the switches (top_k >= V, top_p = 1), and the
@@ -42,6 +43,12 @@ GRID = [
     (4104, 2, 0.6, "f32", "onehot", 7, 0.3, 0.25),
     (260000, 1, 1.0, "bf16", "onehot", 0, 0.99, None),    # 8 CTAs per row
     (9000, 0, 1.0, "bf16", "onehot", 0, 0.5, None),       # K = 0: only the bonus draw
+    # rows whose cut may lie outside the candidates (weights >= 2^-20 of the
+    # max's) take the full-slab descent: top-p too close to 1, top-k above
+    # the candidate count
+    (32000, 3, 1.0, "bf16", "dense", 0, 0.9999, None),
+    (32000, 2, 0.3, "bf16", "onehot", 20000, 1.0, None),
+    (65536, 2, 0.5, "f32", "onehot", 30000, 0.9, None),
 ]
 
 

@@ -128,7 +128,7 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.top_k = top_k;
   p.top_p = top_p;
   p.filter = (mode != kGreedy && ((top_k > 0 && top_k < V) || top_p < 1.f)) ? 1 : 0;
-  if (p.filter) {  // rows split into whole chunks of at most kFilterSlabBytes per CTA
+  if (p.filter) {  // rows split into slices of whole chunks, at most kFilterSlabBytes per CTA
     const int esz = dtype == SV_BF16 ? 2 : 4;
     const int NC = (V + kChunk - 1) / kChunk;
     const int max_cpc = kFilterSlabBytes / (kChunk * esz);

@@ -111,8 +111,8 @@ int chunks_per_task(int dtype, bool vec);
 size_t fin_cache_bytes(const VerifyParams& p);
 size_t fin_smem_bytes(const VerifyParams& p, bool dense);
 constexpr size_t kFinCacheLimit = 48 * 1024;
-// Filter kernel: each CTA holds up to this many bytes of its row (whole
-// chunks), and a row spreads over at most kFilterMaxCta CTAs.
+// Filter kernel: each CTA takes a slice of up to this many bytes of its row
+// (whole chunks), and a row spreads over at most kFilterMaxCta CTAs.
 constexpr int kFilterSlabBytes = 64 * 1024;
 constexpr int kFilterMaxCta = 8;
 constexpr size_t kFinSmemMax = kFinCacheLimit + sizeof(float) * ((1 << 24) / kChunk);  // V <= 2^24
