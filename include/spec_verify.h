@@ -202,9 +202,9 @@ sv_status spec_verify_greedy_masked(const void* target_logits, const int32_t* dr
  * The acceptance test, the residual norm(max(0, p' - q')) and the bonus draw
  * use the filtered p', q'.  temperature == 0 is the greedy rule (filters do
  * not change the argmax).  token_mask: as in spec_verify_sample_masked, or
- * NULL.  The rows of a filtered call are held in shared memory by clusters of
- * CTAs: V * sizeof(logit) must not exceed 512 KB (V <= 262144 for bf16,
- * 131072 for fp32), else SV_ERR_SHAPE.  SV_ERR_FILTER for a negative top_k or
+ * NULL.  Each row of a filtered call is taken by one CTA: V * sizeof(logit)
+ * must not exceed 512 KB (V <= 262144 for bf16, 131072 for fp32), else
+ * SV_ERR_SHAPE.  SV_ERR_FILTER for a negative top_k or
  * top_p outside (0, 1].  All other arguments, results and the workspace size
  * are those of spec_verify_sample. */
 sv_status spec_verify_sample_filtered(const void* target_logits, const void* draft_logits,

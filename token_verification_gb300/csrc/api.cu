@@ -128,15 +128,9 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.top_k = top_k;
   p.top_p = top_p;
   p.filter = (mode != kGreedy && ((top_k > 0 && top_k < V) || top_p < 1.f)) ? 1 : 0;
-  if (p.filter) {  // rows split into slices of whole chunks, at most kFilterSlabBytes per CTA
-    const int esz = dtype == SV_BF16 ? 2 : 4;
-    const int NC = (V + kChunk - 1) / kChunk;
-    const int max_cpc = kFilterSlabBytes / (kChunk * esz);
-    const int ncta0 = (NC + max_cpc - 1) / max_cpc;
-    if (ncta0 > kFilterMaxCta) return SV_ERR_SHAPE;
-    p.filter_cpc = (NC + ncta0 - 1) / ncta0;
-    p.filter_ncta = (NC + p.filter_cpc - 1) / p.filter_cpc;
-    if ((long long)B * R * p.filter_ncta >= (1LL << 31)) return SV_ERR_SHAPE;
+  if (p.filter) {  // one CTA per row
+    const long long esz = dtype == SV_BF16 ? 2 : 4;
+    if ((long long)V * esz > kFilterRowBytes || (long long)B * R >= (1LL << 31)) return SV_ERR_SHAPE;
   }
   char* base = static_cast<char*>(ws);
   p.err = reinterpret_cast<int*>(base + l.counters);

@@ -40,8 +40,6 @@ struct VerifyParams {
   int top_k;             // 0: off
   float top_p;           // 1: off
   int filter;            // top-k / top-p active: kernel A is the row-per-cluster filter kernel
-  int filter_ncta;       // CTAs per row (cluster size) in the filter kernel
-  int filter_cpc;        // chunks per filter CTA
   float* thr;            // [B*R] each row's cut value (lowest kept logit), filter calls
   float* ent;            // [B*R*NC] chunk entropy accumulators (typical acceptance)
   float eps, delta;      // typical acceptance: p(x) > min(eps, delta * exp(-H))
@@ -111,10 +109,8 @@ int chunks_per_task(int dtype, bool vec);
 size_t fin_cache_bytes(const VerifyParams& p);
 size_t fin_smem_bytes(const VerifyParams& p, bool dense);
 constexpr size_t kFinCacheLimit = 48 * 1024;
-// Filter kernel: each CTA takes a slice of up to this many bytes of its row
-// (whole chunks), and a row spreads over at most kFilterMaxCta CTAs.
-constexpr int kFilterSlabBytes = 64 * 1024;
-constexpr int kFilterMaxCta = 8;
+// Filter kernel: one CTA per row, rows of at most this many bytes.
+constexpr int kFilterRowBytes = 512 * 1024;
 constexpr size_t kFinSmemMax = kFinCacheLimit + sizeof(float) * ((1 << 24) / kChunk);  // V <= 2^24
 
 // mode: 0 one-hot sampling, 1 dense sampling, 2 greedy, 3 typical acceptance
