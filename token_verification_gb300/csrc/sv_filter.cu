@@ -211,6 +211,24 @@ __device__ __forceinline__ void row_chunk(const VerifyParams& p, const Slice<T>&
   if (s.mrow) allow_only_chunk<T, VEC>(raw, mask_word(s.mrow, p.mask_words, c));
 }
 
+// Asks L2 for `bytes` bytes at p (16-byte aligned, a multiple of 16): a
+// bulk prefetch, no data returned.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
+// Element t (bit t of the candidate marks: group t / 8, element t % 8) of a
+// lane's bf16 tile, as its 16 bits.
+__device__ __forceinline__ uint16_t tile_bf16(const uint4 (&raw)[4], int t) {
+  const uint4 r01 = (t & 8) ? raw[1] : raw[0];
+  const uint4 r23 = (t & 8) ? raw[3] : raw[2];
+  const uint4 rk = (t & 16) ? r23 : r01;
+  const uint32_t w01 = (t & 2) ? rk.y : rk.x;
+  const uint32_t w23 = (t & 2) ? rk.w : rk.z;
+  const uint32_t wq = (t & 4) ? w23 : w01;
+  return (uint16_t)((t & 1) ? (wq >> 16) : (wq & 0xffffu));
+}
+
 template <typename T, int VEC>
 __device__ __forceinline__ float tile_max(const typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV]) {
   using L = Lane<T, VEC>;
@@ -390,9 +408,14 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
   for (int i = threadIdx.x; i < (kCutWarps / 2) * 256 * 3; i += blockDim.x)
     (&sh->part[0][0][0])[i] = 0u;
 
-  // 1. the row max (NaN wins): the row's one HBM read, two chunks per warp in
-  //    flight where a tile is 16 registers (bf16 vectors), one otherwise
-  constexpr int kPair = sizeof(typename L::Raw) * L::NV <= 64 ? 2 : 1;
+  // 1. the row max (NaN wins): the row's one HBM read.  On the vector paths
+  //    each warp first asks L2 for all of its chunks (bulk prefetches), so the
+  //    whole row is in flight at once; two chunks per warp are loaded at a
+  //    time where a tile is 16 registers (bf16 vectors), one otherwise
+  constexpr int kPair = L::NV * ((sizeof(typename L::Raw) + 3) / 4) <= 16 ? 2 : 1;  // registers
+  if (VEC * sizeof(T) == 16 && lane == 0)
+    for (int c = warp; c < sl.nch; c += kCutWarps)
+      prefetch_l2(sl.row + c * kChunk, (uint32_t)(min(kChunk, p.V - c * kChunk) * sizeof(T)));
   float lm = -INFINITY;
   for (int c0 = warp; c0 < sl.nch; c0 += kPair * kCutWarps) {
     const int c1 = c0 + kCutWarps;
@@ -421,38 +444,72 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
   float thr = -INFINITY;
   bool done = false;  // records written (the candidate path)
   if (is_finite(m)) {
-    // 2a. the row's mass, its mass outside the candidates and their number;
-    //     each warp stages its candidates' logits (a warp whose stage fills
-    //     up sends the row down the full-row path)
+    // 2a. the row's mass, the candidate marks and their number; each warp
+    //     stages its candidates' logits (a warp whose stage fills up sends
+    //     the row down the full-row path).  The mass outside the candidates
+    //     is the row's mass less the staged candidates'.
     constexpr int kCap = kStageBytes / (int)sizeof(T);
+    constexpr bool kPacked = sizeof(T) == 2 && VEC == 8;
     T* st = reinterpret_cast<T*>(sh->stage[warp]);
     int base = 0;
     bool over = false;
-    float s0 = 0.f, s1 = 0.f, tail = 0.f;
+    float s0 = 0.f, s1 = 0.f;
+    const f32x2 c2 = pack2(p.cc, p.cc), nb2 = pack2(nb, nb);
+    f32x2 acc[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) acc[q] = pack2(0.f, 0.f);
+    // (bf16 vectors: the next chunk's load is issued before this one is
+    // reduced)
+    constexpr bool kPipe = kPair == 2;
+    typename L::Raw raw[L::NV], nxt[L::NV];
+    if (kPipe && warp < sl.nch) row_chunk<T, VEC>(p, sl, warp, nxt);
     for (int c = warp; c < sl.nch; c += kCutWarps) {
-      typename L::Raw raw[L::NV];
-      row_chunk<T, VEC>(p, sl, c, raw);
+      if (kPipe) {
+#pragma unroll
+        for (int k = 0; k < L::NV; ++k) raw[k] = nxt[k];
+        if (c + kCutWarps < sl.nch) row_chunk<T, VEC>(p, sl, c + kCutWarps, nxt);
+      } else {
+        row_chunk<T, VEC>(p, sl, c, raw);
+      }
       uint32_t bits = 0u;
+      if constexpr (kPacked) {  // bf16 pairs: fma.rn.f32x2 and add.rn.f32x2
 #pragma unroll
-      for (int k = 0; k < L::NV; ++k)
+        for (int k = 0; k < L::NV; ++k) {
+          const uint32_t wd[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float a = fmaf(L::get(raw[k], e), p.cc, nb);
-          const float w = ex2(a);
-          if (e & 1) s1 += w; else s0 += w;
-          if (a >= -kCandBits) bits |= 1u << (k * VEC + e);
-          else tail += w;
+          for (int q = 0; q < 4; ++q) {
+            float a0, a1;
+            unpack2(fma2(pack2(bf16_lo(wd[q]), bf16_hi(wd[q])), c2, nb2), a0, a1);
+            acc[q] = add2(acc[q], pack2(ex2(a0), ex2(a1)));
+            bits |= (a0 >= -kCandBits ? 1u : 0u) << (k * 8 + 2 * q);
+            bits |= (a1 >= -kCandBits ? 1u : 0u) << (k * 8 + 2 * q + 1);
+          }
         }
+      } else {
+#pragma unroll
+        for (int k = 0; k < L::NV; ++k)
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) {
+            const float a = fmaf(L::get(raw[k], e), p.cc, nb);
+            const float w = ex2(a);
+            if (e & 1) s1 += w; else s0 += w;
+            if (a >= -kCandBits) bits |= 1u << (k * VEC + e);
+          }
+      }
       const int cnt = __popc(bits);
       const int incl = warp_incl_scan_int(cnt);
       const int total = __shfl_sync(0xffffffffu, incl, kWarp - 1);
       if (!over && base + total <= kCap) {
-        int q = base + incl - cnt;
+        int q = base + incl - cnt;  // the lane's candidates in element order
+        if constexpr (kPacked) {
+          for (uint32_t bb = bits; bb; bb &= bb - 1u) st[q++] = tile_bf16(raw, __ffs(bb) - 1);
+        } else {
 #pragma unroll
-        for (int k = 0; k < L::NV; ++k)
+          for (int k = 0; k < L::NV; ++k)
 #pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            if ((bits >> (k * VEC + e)) & 1u) st[q++] = stage_bits(L::get(raw[k], e), st);
+            for (int e = 0; e < VEC; ++e)
+              if ((bits >> (k * VEC + e)) & 1u) st[q++] = stage_bits(L::get(raw[k], e), st);
+        }
         const int xo = x - c * kChunk;  // the draft token's entry, if it is a candidate here
         if (MODE == kOneHot && xo >= 0 && xo < kChunk && lane == (xo / VEC) % kWarp) {
           const int pos = (xo / (kWarp * VEC)) * VEC + xo % VEC;
@@ -467,11 +524,21 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
         over = true;
       }
     }
+    if constexpr (kPacked) {
+      float a0, a1, a2, a3;
+      unpack2(add2(acc[0], acc[1]), a0, a1);
+      unpack2(add2(acc[2], acc[3]), a2, a3);
+      s0 = a0 + a2;
+      s1 = a1 + a3;
+    }
     const float s = warp_sum(s0 + s1);
-    tail = warp_sum(tail);
+    float sc = 0.f;  // the staged candidates' mass
+    if (!over)
+      for (int i = lane; i < base; i += kWarp) sc += ex2(fmaf(stage_value(st, i), p.cc, nb));
+    sc = warp_sum(sc);
     if (lane == 0) {
       sh->red_s[warp] = s;
-      sh->red_t[warp] = tail;
+      sh->red_t[warp] = sc;
       sh->red_n[warp] = base;
       sh->stage_n[warp] = base;
       if (over) sh->over = 1;
@@ -486,7 +553,7 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
         n += sh->red_n[w];
       }
       sh->row_s = a;
-      sh->row_tail = tt;
+      sh->row_tail = a - tt;
       sh->row_n = n;
     }
     __syncthreads();
