@@ -582,27 +582,27 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
         // 3. chunk records over the kept elements, which are all staged:
         //    {max, sum of 2^((l - max) c) leaving out the draft token
         //    (one-hot)} as the streaming kernel writes them
+        // One thread per chunk, over the chunk's run in its warp's stage.
         const int x_entry = sh->x_entry;
-        const int xc = (x >= 0 && x < p.V) ? x / kChunk : -1;
-        for (int c = warp; c < sl.nch; c += kCutWarps) {
+        const int xc = (MODE == kOneHot && x >= 0 && x < p.V) ? x / kChunk : -1;
+        for (int c = threadIdx.x; c < sl.nch; c += blockDim.x) {
+          const T* cst = reinterpret_cast<const T*>(sh->stage[c % kCutWarps]);
           const int b0 = sh->seg[c], n0 = sh->seg_n[c];
-          float lm2 = -INFINITY;
-          for (int i = lane; i < n0; i += kWarp) {
-            const float v = stage_value(st, b0 + i);
-            if (v >= thr) lm2 = fmaxf(lm2, v);
+          float cm = -INFINITY;
+          for (int i = 0; i < n0; ++i) {
+            const float v = stage_value(cst, b0 + i);
+            if (v >= thr) cm = fmaxf(cm, v);
           }
-          const float cm = warp_max_nan(lm2);
           float cs = 0.f;
           if (cm > -INFINITY) {
             const float nbc = -cm * p.cc;
-            const int skip = (MODE == kOneHot && c == xc) ? x_entry : -1;
-            for (int i = lane; i < n0; i += kWarp) {
-              const float v = stage_value(st, b0 + i);
+            const int skip = c == xc ? x_entry : -1;
+            for (int i = 0; i < n0; ++i) {
+              const float v = stage_value(cst, b0 + i);
               if (v >= thr && b0 + i != skip) cs += ex2(fmaf(v, p.cc, nbc));
             }
           }
-          cs = warp_sum(cs);
-          if (lane == 0) p.rec[(long long)rowid * p.NC + c] = make_float2(cm, cs);
+          p.rec[(long long)rowid * p.NC + c] = make_float2(cm, cs);
         }
         if (threadIdx.x == 0 && x >= 0 && x < p.V) {
           const bool allowed = !sl.mrow || ((__ldg(sl.mrow + (x >> 5)) >> (x & 31)) & 1u);
