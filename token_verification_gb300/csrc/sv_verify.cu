@@ -396,8 +396,8 @@ __device__ void compact_all(const VerifyParams& p, int* smem) {
     const int L = b < B ? __ldcg(p.out_accept_len + b) : 0;
     int tok[kMaxK + 1];
 #pragma unroll
-    for (int k = 0; k <= kMaxK; ++k)
-      tok[k] = (p.out_packed && k < L) ? __ldcg(p.out_tokens + (long long)b * W + k) : -1;
+    for (int k = 0; k <= kMaxK; ++k)  // every token at once, with L (no wait on L)
+      tok[k] = (p.out_packed && b < B && k < W) ? __ldcg(p.out_tokens + (long long)b * W + k) : -1;
     const int cu = offset + block_excl_scan(L, smem);
     if (b < B) {
       if (p.out_cu) p.out_cu[b] = cu;
@@ -1052,10 +1052,11 @@ int blocks_per_sm(K kernel) {
   return n;
 }
 
-// CTAs per request for the dense-draft residual: enough to cover the SMs
-// with one CTA each, at most one per 32 chunks of the row, at most 8.
-int residual_cluster(const VerifyParams& p, int sms) {
-  int c = p.B > 0 ? sms / p.B : 1;
+// CTAs per request for the dense-draft residual: as many as fit on the GPU
+// at once (`slots` finalize CTAs), at most one per 32 chunks of the row (a
+// CTA's 16 warps read 2 chunks of each row at a time), at most 8.
+int residual_cluster(const VerifyParams& p, int slots) {
+  int c = p.B > 0 ? slots / p.B : 1;
   c = c < (p.NC + 31) / 32 ? c : (p.NC + 31) / 32;
   return c < 1 ? 1 : (c > 8 ? 8 : c);
 }
@@ -1132,12 +1133,19 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
   const void* fin = reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>);
   const size_t fin_smem = fin_smem_bytes(p, MODE == kDense);
   static PerDevice once;
-  err = per_device(once, nullptr, [&](int&) {
-    return cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kFinSmemMax);
+  int occ = 1;  // finalize CTAs per SM
+  err = per_device(once, &occ, [&](int& v) {
+    const cudaError_t e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)kFinSmemMax);
+    if (e != cudaSuccess) return e;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fin, fin_threads<MODE>(),
+                                                      (size_t)kFinCacheLimit) != cudaSuccess ||
+        v < 1)
+      v = 1;
+    return cudaSuccess;
   });
   if (err != cudaSuccess) return err;
-  const int ncta = MODE == kDense ? residual_cluster(p, di.sms) : 1;
+  const int ncta = MODE == kDense ? residual_cluster(p, di.sms * occ) : 1;
   return launch_pdl(fin, dim3(p.B * ncta), dim3(fin_threads<MODE>()), s, args, fin_smem, ncta);
 }
 
