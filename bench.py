@@ -35,9 +35,16 @@ sys.path.insert(0, ROOT)
 
 METRIC = "verify calls/s and logits HBM GB/s (% of GB300 peak) at B=256 K=5 V=152064"
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SOURCES = ["token_verification_gb300/csrc/sv_verify.cu",
-                  "token_verification_gb300/csrc/sv_rows.cuh",
-                  "token_verification_gb300/csrc/sv_common.cuh"]
+# the sources of each profiled kernel (a profile's DRAM figure counts only
+# while these are unchanged)
+KERNEL_SOURCES = {
+    "stream": ["token_verification_gb300/csrc/sv_verify.cu",
+               "token_verification_gb300/csrc/sv_rows.cuh",
+               "token_verification_gb300/csrc/sv_common.cuh"],
+    "filter": ["token_verification_gb300/csrc/sv_filter.cu",
+               "token_verification_gb300/csrc/sv_rows.cuh",
+               "token_verification_gb300/csrc/sv_common.cuh"],
+}
 
 
 # ---------------------------------------------------------------------------
@@ -83,26 +90,27 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash():
+def kernel_source_hash(kind="stream"):
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(name):
+def profiled_traffic(entry):
     """DRAM bytes per launch recorded in profiles/<name>.md, if the profile
-    was taken on the current kernel sources (else None)."""
-    if not name:
+    was taken on the current sources of its kernel (else None)."""
+    if not entry:
         return None
+    name, kind = entry
     path = os.path.join(ROOT, "profiles", name + ".md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
     m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
     m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash():
+    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kind):
         return None
     return int(m_bytes.group(1))
 
@@ -582,7 +590,8 @@ def run_ours(args):
 
 
 # ncu summaries under profiles/ that record DRAM traffic per launch
-PROFILE_NAMES = {(2, "sample"): "verify_stream_onehot_B256_K5_V152064"}
+PROFILE_NAMES = {(2, "sample"): ("verify_stream_onehot_B256_K5_V152064", "stream"),
+                 (7, "sample"): ("filter_rows_topp_B256_K5_V152064", "filter")}
 
 
 def main(argv=None):
