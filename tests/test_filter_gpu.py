@@ -49,6 +49,9 @@ GRID = [
     (32000, 3, 1.0, "bf16", "dense", 0, 0.9999, None),
     (32000, 2, 0.3, "bf16", "onehot", 20000, 1.0, None),
     (65536, 2, 0.5, "f32", "onehot", 30000, 0.9, None),
+    # nearly every element within 2^-18 of the max's weight: the candidate
+    # stages fill up and the rows take the full-row path
+    (152064, 2, 2.0, "bf16", "onehot", 0, 0.9, None),
 ]
 
 
@@ -97,3 +100,20 @@ def test_filter_switches_and_argument_checks():
         api.spec_verify_sample(big, None, torch.zeros((2, 1), dtype=torch.int32, device="cuda"),
                                torch.zeros((2, 2), dtype=torch.float32, device="cuda"), 1.0,
                                top_p=0.9)
+
+
+@pytest.mark.parametrize("T,top_k,top_p", [(0.8, 0, 0.95), (1.0, 40, 0.9), (2.0, 0, 0.9)])
+def test_filtered_repeatable(T, top_k, top_p):
+    """The cut and the records come from integer (fixed-point) histograms and
+    fixed-order sums, so a repeated call gives identical outputs whatever the
+    order of the shared-memory atomics: the candidate path (T 0.8), top-k then
+    top-p among the candidates, and the full-row path (T 2: the candidate
+    stages fill up)."""
+    wl = synth.make_sample_case(24, 3, 152064, drafts="onehot", T=T, seed=93)
+    d = parity.to_device(wl)
+    outs = [api.spec_verify_sample(d["target"], None, d["draft_tokens"], d["uniforms"], T,
+                                   top_k=top_k, top_p=top_p) for _ in range(3)]
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        for k in ("tokens", "accept_len", "accept_prob"):
+            assert torch.equal(getattr(outs[0], k), getattr(o, k)), k

@@ -462,8 +462,8 @@ struct Residual {
 
 template <int MODE, typename T, int VEC>
 __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
-                                              const RowSum* srow, const float2* srec, int x,
-                                              float u, float uK, int timed_out, Residual* resid);
+                                              const RowSum* srow, const int* s_tok, int x,
+                                              float u, int timed_out, Residual* resid);
 template <typename T, int VEC>
 __device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
                                            float* sums, int rank, int ncta);
@@ -476,6 +476,30 @@ __device__ __forceinline__ int row_token(const VerifyParams& p, int b, int r, in
   if (!row_needed(p, r, Kb)) return -1;
   const int i = r > p.K ? r - p.K - 1 : r;
   return i < Kb ? __ldg(p.draft_tokens + (long long)b * p.K + i) : -1;
+}
+
+// The token position r draws if the walk stops there (one warp): the
+// residual max(0, p_r - q_r) of a one-hot draft (p_r without x_r; x_r itself
+// when no mass is left beside it), else a draw from p_r (the bonus position,
+// typical acceptance, the bonus of dense drafts).  -1 for a row without a
+// finite max or a failed draw.  Each summarising warp computes it for its own
+// row, so the draw overlaps the other rows and the acceptance tests.
+template <int MODE, typename T, int VEC>
+__device__ __forceinline__ int position_draw(const VerifyParams& p, int b, int r, int Kb,
+                                             const RowSum& rs, int xr, float uK,
+                                             const float2* srec) {
+  if (!is_finite(rs.m)) return -1;
+  const bool residual = MODE == kOneHot && r < Kb;
+  if (residual && !(rs.s > 0.f)) return xr;  // p_r is the point mass at x_r
+  const T* row = row_ptr<T>(p.target, (long long)b * (p.K + 1) + r, p.V);
+  const uint32_t* mrow = mask_row(p, b, r);
+  const float cut = row_cut(p, (long long)b * p.R + r);
+  return srec ? draw_from_records<T, VEC, true>(row, srec + (long long)r * p.NC, p.NC, p.V, rs.m,
+                                                p.cc, uK, residual ? xr : -1, mrow, p.mask_words,
+                                                cut)
+              : draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + r) * p.NC, p.NC,
+                                          p.V, rs.m, p.cc, uK, residual ? xr : -1, mrow,
+                                          p.mask_words, cut);
 }
 
 // The acceptance tests of all positions at once (one lane per position),
@@ -493,6 +517,7 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   __shared__ RowSum srow[kMaxRows];
   __shared__ Residual s_resid;
   __shared__ int s_last[32];
+  __shared__ int s_tok[kMaxRows];  // the token each position would draw
   int ncta = 1, rank = 0;
   if (MODE == kDense) {
     const cg::cluster_group cluster = cg::this_cluster();
@@ -510,13 +535,11 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   const int Kv = (Kb >= 0 && Kb <= K) ? Kb : 0;
   const int x0 = warp < p.R ? row_token(p, b, warp, Kb) : -1;
   int x = -1;
-  float u = 0.f, uK = 0.f;
+  float u = 0.f;
+  const float uK = MODE != kGreedy ? __ldg(p.uniforms + (long long)b * (K + 1) + K) : 0.f;
   if (warp == 0) {
     if (lane < Kv) x = __ldg(p.draft_tokens + (long long)b * K + lane);
-    if (MODE != kGreedy) {
-      if (lane < Kv) u = __ldg(p.uniforms + (long long)b * (K + 1) + lane);
-      uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
-    }
+    if (MODE != kGreedy && lane < Kv) u = __ldg(p.uniforms + (long long)b * (K + 1) + lane);
   }
   if (threadIdx.x == 0) s_resid.n = -1;
   pdl_wait();
@@ -526,14 +549,20 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   if (leader) {
     for (int r = warp; r < p.R; r += kWarps) {
       RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
+      const int xr = r == warp ? x0 : row_token(p, b, r, Kb);
       if (row_needed(p, r, Kb))
-        rs = summarise_row<MODE, T>(p, b, r, Kb, r == warp ? x0 : row_token(p, b, r, Kb),
-                                    s_rec ? s_rec + (long long)r * p.NC : nullptr);
+        rs = summarise_row<MODE, T>(p, b, r, Kb, xr, s_rec ? s_rec + (long long)r * p.NC : nullptr);
       if (lane == 0) srow[r] = rs;
+      // target row r <= K_b: the draw of position r (dense drafts: the bonus
+      // position only; the others draw from the residual)
+      if (MODE != kGreedy && Kb >= 0 && Kb <= K && r <= Kb && (MODE != kDense || r == Kb)) {
+        const int tok = position_draw<MODE, T, VEC>(p, b, r, Kb, rs, xr, uK, s_rec);
+        if (lane == 0) s_tok[r] = tok;
+      }
     }
     __syncthreads();
     if (warp == 0)
-      finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_rec, x, u, uK, timed_out, &s_resid);
+      finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_tok, x, u, timed_out, &s_resid);
   }
   if (MODE == kDense) {
     // Dense drafts: the request's CTAs learn n from the first one, read the
@@ -571,8 +600,8 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
 
 template <int MODE, typename T, int VEC>
 __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
-                                              const RowSum* srow, const float2* srec, int x,
-                                              float u, float uK, int timed_out, Residual* resid) {
+                                              const RowSum* srow, const int* s_tok, int x,
+                                              float u, int timed_out, Residual* resid) {
   const int lane = lane_id();
   const int K = p.K;
   // A bounded wait that gave up in kernel A (a device fault) invalidates the
@@ -629,21 +658,8 @@ __device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int 
         pending = true;  // the whole CTA draws from max(0, p_n - q_n) next
         if (lane == 0) *resid = Residual{n, m_n, 1.f / s_n, mq_n, 1.f / sq_n};
       } else {
-        const bool residual = MODE == kOneHot && n < Kb;
-        if (residual && !(s_n > 0.f)) {
-          token = x_n;  // no mass left beside x_n: p_n itself is the point mass at x_n
-        } else {
-          const T* row = row_ptr<T>(p.target, (long long)b * (K + 1) + n, p.V);
-          const uint32_t* mrow = mask_row(p, b, n);
-          const float cut = row_cut(p, (long long)b * p.R + n);
-          token = srec ? draw_from_records<T, VEC, true>(row, srec + (long long)n * p.NC, p.NC,
-                                                         p.V, m_n, p.cc, uK, residual ? x_n : -1,
-                                                         mrow, p.mask_words, cut)
-                       : draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + n) * p.NC,
-                                                   p.NC, p.V, m_n, p.cc, uK, residual ? x_n : -1,
-                                                   mrow, p.mask_words, cut);
-          if (token < 0) status = kBadLogits;
-        }
+        token = s_tok[n];  // drawn beside the row summaries (position_draw)
+        if (token < 0) status = kBadLogits;
       }
     }
   }
