@@ -447,10 +447,10 @@ __device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb, int
   return rs;
 }
 
-// Threads of a finalize CTA: 16 warps where a rejected request reads its
-// dense row pair, 8 elsewhere.
+// Threads of a finalize CTA: 8 warps (dense drafts: at 128 registers, two
+// CTAs per SM, so a request's residual cluster spans more SMs).
 template <int MODE>
-__host__ __device__ constexpr int fin_threads() { return MODE == kDense ? 512 : 256; }
+__host__ __device__ constexpr int fin_threads() { return 256; }
 constexpr int kMaxRows = 2 * kMaxK + 1;
 
 // The rejected position of a dense-draft request and its two rows' maxima
@@ -461,7 +461,7 @@ struct Residual {
 };
 
 template <int MODE, typename T, int VEC>
-__device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
+__device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const int* s_tok, int x,
                                               float u, int timed_out, Residual* resid);
 template <typename T, int VEC>
@@ -599,7 +599,7 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
 }
 
 template <int MODE, typename T, int VEC>
-__device__ __noinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
+__device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const int* s_tok, int x,
                                               float u, int timed_out, Residual* resid) {
   const int lane = lane_id();
@@ -1069,11 +1069,11 @@ int blocks_per_sm(K kernel) {
 }
 
 // CTAs per request for the dense-draft residual: as many as fit on the GPU
-// at once (`slots` finalize CTAs), at most one per 32 chunks of the row (a
-// CTA's 16 warps read 2 chunks of each row at a time), at most 8.
+// at once (`slots` finalize CTAs), at most one per 16 chunks of the row (a
+// CTA's 8 warps read 2 chunks of each row at a time), at most 8.
 int residual_cluster(const VerifyParams& p, int slots) {
   int c = p.B > 0 ? slots / p.B : 1;
-  c = c < (p.NC + 31) / 32 ? c : (p.NC + 31) / 32;
+  c = c < (p.NC + 15) / 16 ? c : (p.NC + 15) / 16;
   return c < 1 ? 1 : (c > 8 ? 8 : c);
 }
 
