@@ -16,7 +16,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
-SOURCES = ["api.cu", "sv_verify.cu", "sv_filter.cu", "sv_tree.cu", "sv_noalloc.cu", "sv_ngram.cu"]
+SOURCES = ["api.cu", "sv_verify.cu", "sv_finalize.cu", "sv_filter.cu", "sv_tree.cu", "sv_noalloc.cu", "sv_ngram.cu"]
 HEADERS = ["sv_common.cuh", "sv_launch.h", "sv_rows.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",

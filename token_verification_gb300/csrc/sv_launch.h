@@ -118,6 +118,9 @@ cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream);
 cudaError_t launch_tree(int dtype, bool vec, const TreeParams& p, cudaStream_t stream);
 // Kernel A of top-k / top-p calls (sv_filter.cu); mode 0 or 1.
+// Kernel A (or A' for filtered calls) alone: the chunk records.
+cudaError_t launch_records(int mode, int dtype, bool vec, const VerifyParams& p,
+                           cudaStream_t stream);
 cudaError_t launch_filter(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream);
 cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeTypical& t,

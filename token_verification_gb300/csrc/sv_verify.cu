@@ -1,673 +1,29 @@
-// sv_verify.cu - rejection-sampling and greedy verification kernels.
+// sv_verify.cu - kernel A of the verification calls: one streaming read of
+// the logits.
 //
 // Method ("【大模型基础设施工程】15：推测解码与 MTP" (juejin.cn), §2.1 "算法骨架"):
 // for each request, accept draft x_i with probability min(1, p_i(x_i) /
 // q_i(x_i)) in position order; at the first rejection n draw from
 // norm(max(0, p_n - q_n)); if all drafts are accepted draw the extra token
 // from the last position's p.  Greedy rule (§11 of the same page): accept
-// while x_i equals the target argmax.  Requests are independent and verified
-// in parallel ("投机解码" (FastDeploy), "高效投机解码框架设计").
+// while x_i equals the target argmax.  Every one of these needs, per row, the
+// tempered softmax's maximum and sum (or the argmax) and the draft token's
+// logit, which this kernel provides.
 //
 // Kernel A (verify_stream_kernel; verify_rows_kernel on the scalar path)
 //   reads every needed logit once and reduces each 1024-logit chunk of a row
 //   to one 8-byte record.  One producer thread per CTA copies items of 15
 //   consecutive chunks (30 KB of bf16) into a ring of shared-memory stages
 //   with cp.async.bulk; each of the 15 consumer warps reduces one chunk of
-//   every stage.  It has no atomics, fences or cross-CTA communication.
-// Kernel F (finalize_kernel, one CTA per request) combines each row's chunk
-//   records, runs the acceptance tests of all positions at once (one lane
-//   per position), then draws the residual / bonus token: the crossing chunk
-//   from the records, then one rescan of that single chunk.  With dense
-//   drafts a request rejected at n first needs the chunk sums of
-//   max(0, p_n - q_n): a cluster of CTAs per request (each one redoing the
-//   cheap acceptance tests) reads the (target, draft) row pair once for
-//   them, writing into the first CTA's shared memory, whose warp 0 then
-//   draws the token the same way.  The last CTA of the call writes the
-//   padding-free packed output (exclusive scan of accept_len, packed tokens,
-//   per-token batch ids).
-// F starts with programmatic dependent launch and waits on the device for
-// kernel A's records.
+//   every stage.  It has no atomics, fences or cross-CTA communication.  The
+//   per-request work (tests, draws, packed output) is kernel F's
+//   (sv_finalize.cu); filtered calls use kernel A' (sv_filter.cu) instead.
+#include <type_traits>
+
 #include "sv_rows.cuh"
 
 namespace sv {
 namespace {
-
-// ---------------------------------------------------------------------------
-// drawing one token
-// ---------------------------------------------------------------------------
-
-// First chunk c whose cumulative weight exceeds `target` (chunk weights from
-// `weight(c)`, all in one frame).  Returns c and the fraction of chunk c's
-// weight that lies below the target; if rounding leaves the target past the
-// last chunk, returns the last chunk of positive weight with fraction 2
-// (which selects its last positive element).  c = -1 if no weight at all.
-// The chunk weights of the first kRecCache * 32 chunks come from `wc`
-// (cached per lane: chunk lane + 32 t in wc[t]); later chunks from weight(c).
-template <class F>
-__device__ int find_chunk(const float (&wc)[kRecCache], F weight, int NC, float target,
-                          float* frac) {
-  const int lane = lane_id();
-  float base = 0.f;
-  auto round = [&](int c0, float w, int* out) {
-    const float incl = warp_incl_scan(w);
-    const unsigned hit = __ballot_sync(0xffffffffu, w > 0.f && base + incl > target);
-    if (hit) {
-      const int l = __ffs(hit) - 1;
-      const float below = target - (base + __shfl_sync(0xffffffffu, incl - w, l));
-      const float wl = __shfl_sync(0xffffffffu, w, l);
-      *frac = fminf(fmaxf(below / wl, 0.f), 1.f);
-      *out = c0 + l;
-      return true;
-    }
-    base += __shfl_sync(0xffffffffu, incl, kWarp - 1);
-    return false;
-  };
-  int found = -1;
-#pragma unroll
-  for (int t = 0; t < kRecCache; ++t)
-    if (found < 0 && t * kWarp < NC && round(t * kWarp, wc[t], &found)) break;
-  if (found >= 0) return found;
-  for (int c0 = kRecCache * kWarp; c0 < NC; c0 += kWarp) {
-    const int c = c0 + lane;
-    if (round(c0, c < NC ? weight(c) : 0.f, &found)) return found;
-  }
-  for (int c0 = ((NC - 1) / kWarp) * kWarp; c0 >= 0; c0 -= kWarp) {
-    const int c = c0 + lane;
-    const unsigned pos = __ballot_sync(0xffffffffu, c < NC && weight(c) > 0.f);
-    if (pos) {
-      *frac = 2.f;
-      return c0 + 31 - __clz(pos);
-    }
-  }
-  return -1;
-}
-
-// Smallest element whose cumulative weight (in index order) exceeds
-// frac * (tile total), over one chunk tile of weights w held per lane
-// (group k, element e at chunk offset k*32*VEC + lane*VEC + e); zero
-// weights are never chosen.  Falls back to the last positive element.
-template <int NV, int VEC>
-__device__ int select_in_tile(const float (&w)[NV * VEC], const float (&gsum)[NV], float frac,
-                              int base_j) {
-  const int lane = lane_id();
-  float lt = 0.f;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) lt += gsum[k];
-  const float thr = frac * warp_sum(lt);
-  float running = 0.f;
-  int tok = -1;
-#pragma unroll
-  for (int k = 0; k < NV; ++k) {
-    const float incl = warp_incl_scan(gsum[k]);
-    const unsigned hit = __ballot_sync(0xffffffffu, gsum[k] > 0.f && running + incl > thr);
-    if (hit && tok < 0) {
-      const int l = __ffs(hit) - 1;
-      int t = -1;
-      if (lane == l) {
-        float acc = running + incl - gsum[k];
-        int last = -1;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float we = w[k * VEC + e];
-          acc += we;
-          if (we > 0.f) {
-            last = base_j + tile_offset<VEC>(k, e, lane);
-            if (t < 0 && acc > thr) t = last;
-          }
-        }
-        if (t < 0) t = last;
-      }
-      tok = __shfl_sync(0xffffffffu, t, l);
-    }
-    running += __shfl_sync(0xffffffffu, incl, kWarp - 1);
-  }
-  if (tok < 0) {
-    int last = -1;
-#pragma unroll
-    for (int k = 0; k < NV; ++k)
-#pragma unroll
-      for (int e = 0; e < VEC; ++e)
-        if (w[k * VEC + e] > 0.f) last = base_j + tile_offset<VEC>(k, e, lane);
-    tok = __reduce_max_sync(0xffffffffu, last);
-  }
-  return tok;
-}
-
-// ---------------------------------------------------------------------------
-// contiguous-run draws (vector paths): lane l takes chunks / elements
-// [l*n, (l+1)*n), so one warp scan of the lane sums and one ballot locate the
-// crossing lane, and that lane walks its own run
-// ---------------------------------------------------------------------------
-
-// The chunk where the cumulative weight (in chunk order) first exceeds
-// u * total, over NC chunk weights weight(c).  frac = the share of that
-// chunk's weight below the target; with no crossing (rounding only) the last
-// chunk of positive weight with frac = 2.  Returns -1 without any weight.
-template <class F>
-__device__ int find_chunk_runs(F weight, int NC, float u, float* frac) {
-  const int lane = lane_id();
-  const int per = (NC + kWarp - 1) / kWarp;
-  const int c0 = lane * per;
-  float s = 0.f;
-  for (int i = 0; i < per; ++i)
-    if (c0 + i < NC) s += weight(c0 + i);
-  const float incl = warp_incl_scan(s);
-  const float target = u * __shfl_sync(0xffffffffu, incl, kWarp - 1);
-  const unsigned hit = __ballot_sync(0xffffffffu, s > 0.f && incl > target);
-  int c = -1;
-  float f = 0.f;
-  if (hit) {
-    const int l = __ffs(hit) - 1;
-    if (lane == l) {
-      float acc = incl - s;
-      for (int i = 0; i < per && c0 + i < NC; ++i) {
-        const float w = weight(c0 + i);
-        if (w > 0.f && acc + w > target) {
-          c = c0 + i;
-          f = fminf(fmaxf((target - acc) / w, 0.f), 1.f);
-          break;
-        }
-        acc += w;
-      }
-      if (c < 0) {  // rounding inside the lane: its last positive chunk
-        for (int i = 0; i < per && c0 + i < NC; ++i)
-          if (weight(c0 + i) > 0.f) c = c0 + i;
-        f = 2.f;
-      }
-    }
-    c = __shfl_sync(0xffffffffu, c, l);
-    f = __shfl_sync(0xffffffffu, f, l);
-  } else {
-    const unsigned pos = __ballot_sync(0xffffffffu, s > 0.f);
-    if (!pos) return -1;
-    const int l = 31 - __clz(pos);
-    if (lane == l)
-      for (int i = 0; i < per && c0 + i < NC; ++i)
-        if (weight(c0 + i) > 0.f) c = c0 + i;
-    c = __shfl_sync(0xffffffffu, c, l);
-    f = 2.f;
-  }
-  *frac = f;
-  return c;
-}
-
-// Elements 32*lane .. 32*lane+31 of chunk c, widened to fp32 (-inf past V).
-template <typename T>
-__device__ __forceinline__ void load_run(const T* row, int V, int c, float (&v)[kWarp]) {
-  constexpr int E = 16 / sizeof(T);
-  const int j0 = c * kChunk + lane_id() * kWarp;
-#pragma unroll
-  for (int g = 0; g < kWarp / E; ++g) {
-    const int j = j0 + g * E;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    const bool in = j < V;  // V is a multiple of E on the vector paths
-    if (in) q = __ldg(reinterpret_cast<const uint4*>(row + j));
-    const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      float x;
-      if constexpr (sizeof(T) == 2)
-        x = __uint_as_float((e & 1) ? (wds[e >> 1] & 0xffff0000u) : (wds[e >> 1] << 16));
-      else
-        x = __uint_as_float(wds[e]);
-      v[g * E + e] = in ? x : -INFINITY;
-    }
-  }
-}
-
-// Which of this lane's 32 elements of chunk c are allowed: the grammar mask
-// word (one word covers exactly the lane's run), the top-k / top-p cut and
-// the excluded token x.
-__device__ __forceinline__ uint32_t run_allowed(const float (&v)[kWarp], const uint32_t* mrow,
-                                                int mask_words, int c, float cut, int x) {
-  const int lane = lane_id();
-  uint32_t a = 0xffffffffu;
-  if (mrow) a = mask_word(mrow, mask_words, c);
-  if (cut > -INFINITY) {
-#pragma unroll
-    for (int e = 0; e < kWarp; ++e)
-      if (!(v[e] >= cut)) a &= ~(1u << e);
-  }
-  const int xo = x - (c * kChunk + lane * kWarp);
-  if (xo >= 0 && xo < kWarp) a &= ~(1u << xo);
-  return a;
-}
-
-// Smallest element whose cumulative weight (in index order) exceeds frac
-// times the chunk total, over the lanes' runs of weights w; zero weights are
-// never chosen; the last positive element if rounding leaves none.
-__device__ int pick_in_runs(const float (&w)[kWarp], float frac, int base_j) {
-  const int lane = lane_id();
-  float s = 0.f;
-#pragma unroll
-  for (int e = 0; e < kWarp; ++e) s += w[e];
-  const float incl = warp_incl_scan(s);
-  const float thr = frac * __shfl_sync(0xffffffffu, incl, kWarp - 1);
-  const unsigned hit = __ballot_sync(0xffffffffu, s > 0.f && incl > thr);
-  int t = -1, l;
-  if (hit) {
-    l = __ffs(hit) - 1;
-    if (lane == l) {
-      float acc = incl - s;
-      int last = -1;
-#pragma unroll
-      for (int e = 0; e < kWarp; ++e) {
-        acc += w[e];
-        if (w[e] > 0.f) {
-          last = e;
-          if (t < 0 && acc > thr) t = e;
-        }
-      }
-      if (t < 0) t = last;
-    }
-  } else {
-    const unsigned pos = __ballot_sync(0xffffffffu, s > 0.f);
-    if (!pos) return -1;
-    l = 31 - __clz(pos);
-    if (lane == l)
-#pragma unroll
-      for (int e = 0; e < kWarp; ++e)
-        if (w[e] > 0.f) t = e;
-  }
-  t = __shfl_sync(0xffffffffu, t, l);
-  return base_j + l * kWarp + t;
-}
-
-// Draw from w_j = 2^((l_j - m) c) over one row (w = 0 at mask_x, at the
-// tokens the grammar mask row `mrow` rules out and below the top-k / top-p
-// cut value) given the row's softmax chunk records: the crossing chunk from
-// the records, then one rescan of that chunk in its own frame.
-template <typename T, int VEC, bool kSharedRecords = false>
-__device__ int draw_from_records(const T* row, const float2* rec, int NC, int V, float m, float cc,
-                                 float u, int mask_x, const uint32_t* mrow, int mask_words,
-                                 float cut) {
-  using L = Lane<T, VEC>;
-  const int lane = lane_id();
-  const float nb = -m * cc;
-  auto record = [&](int c) { return kSharedRecords ? rec[c] : __ldcg(rec + c); };
-  auto weight = [&](int c) {
-    const float2 r = record(c);
-    return r.y * ex2(fmaf(r.x, cc, nb));
-  };
-  if constexpr (VEC * sizeof(T) == 16) {
-    float frac = 0.f;
-    const int c = find_chunk_runs(weight, NC, u, &frac);
-    if (c < 0) return -1;
-    float v[kWarp];
-    load_run<T>(row, V, c, v);
-    const uint32_t a = run_allowed(v, mrow, mask_words, c, cut, mask_x);
-    const float nbc = -record(c).x * cc;
-    float w[kWarp];
-#pragma unroll
-    for (int e = 0; e < kWarp; ++e) w[e] = ((a >> e) & 1u) ? ex2(fmaf(v[e], cc, nbc)) : 0.f;
-    return pick_in_runs(w, frac, c * kChunk);
-  } else {
-    float wc[kRecCache];  // one batch of loads for the first 256 chunks
-    float tot = 0.f;
-#pragma unroll
-    for (int t = 0; t < kRecCache; ++t) {
-      const int c = lane + t * kWarp;
-      wc[t] = c < NC ? weight(c) : 0.f;
-      tot += wc[t];
-    }
-    for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
-    tot = warp_sum(tot);
-    float frac = 0.f;
-    const int c = find_chunk(wc, weight, NC, u * tot, &frac);
-    if (c < 0) return -1;
-    typename L::Raw raw[L::NV];
-    load_chunk<T, VEC>(row, V, c, raw);
-    if (mrow) allow_only_chunk<T, VEC>(raw, mask_word(mrow, mask_words, c));
-    if (cut > -INFINITY) threshold_chunk<T, VEC>(raw, cut);
-    const float nbc = -record(c).x * cc;
-    float w[L::NV * VEC];
-    float gsum[L::NV];
-#pragma unroll
-    for (int k = 0; k < L::NV; ++k) {
-      gsum[k] = 0.f;
-#pragma unroll
-      for (int e = 0; e < VEC; ++e) {
-        float we = ex2(fmaf(L::get(raw[k], e), cc, nbc));
-        if (c * kChunk + tile_offset<VEC>(k, e, lane) == mask_x) we = 0.f;
-        w[k * VEC + e] = we;
-        gsum[k] += we;
-      }
-    }
-    return select_in_tile<L::NV, VEC>(w, gsum, frac, c * kChunk);
-  }
-}
-
-// Residual weight max(0, p_j - q_j) from the two rows' maxima and 1/sums.
-__device__ __forceinline__ float residual_weight(float lt, float ld, float cc, float nbp, float ip,
-                                                 float nbq, float iq) {
-  const float r = ex2(fmaf(lt, cc, nbp)) * ip - ex2(fmaf(ld, cc, nbq)) * iq;
-  return r > 0.f ? r : 0.f;
-}
-
-__device__ __forceinline__ void write_request(const VerifyParams& p, int b, int status, int n,
-                                              int token, int x) {
-  const int lane = lane_id();
-  const int K = p.K;
-  if (lane <= K)
-    p.out_tokens[(long long)b * (K + 1) + lane] =
-        status ? -1 : (lane < n ? x : (lane == n ? token : -1));
-  if (lane == 0) {
-    p.out_accept_len[b] = status ? 0 : n + 1;
-    if (p.out_status) p.out_status[b] = status;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// padding-free output ("投机解码" (FastDeploy), "高效投机解码框架设计")
-// ---------------------------------------------------------------------------
-
-__device__ int block_sum(int v, int* smem) {
-  const int lane = lane_id(), warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  __syncthreads();
-  if (lane == 0) smem[warp] = v;
-  __syncthreads();
-  int t = 0;
-  for (int w = 0; w < nwarps; ++w) t += smem[w];
-  return t;
-}
-
-__device__ int block_excl_scan(int v, int* smem) {
-  const int lane = lane_id(), warp = threadIdx.x >> 5;
-  const int incl = warp_incl_scan_int(v);
-  __syncthreads();
-  if (lane == kWarp - 1) smem[warp] = incl;
-  __syncthreads();
-  int before = 0;
-  for (int w = 0; w < warp; ++w) before += smem[w];
-  return before + incl - v;
-}
-
-// Exclusive scan of accept_len, packed tokens and per-token batch ids, by
-// one CTA over all B requests (their outputs are complete and visible).
-// Each thread reads all of its request's tokens before writing any, so the
-// copy costs one memory round trip.
-__device__ void compact_all(const VerifyParams& p, int* smem) {
-  const int B = p.B, W = p.K + 1;
-  int offset = 0;
-  for (int b0 = 0; b0 < B; b0 += blockDim.x) {
-    const int b = b0 + threadIdx.x;
-    const int L = b < B ? __ldcg(p.out_accept_len + b) : 0;
-    int tok[kMaxK + 1];
-#pragma unroll
-    for (int k = 0; k <= kMaxK; ++k)  // every token at once, with L (no wait on L)
-      tok[k] = (p.out_packed && b < B && k < W) ? __ldcg(p.out_tokens + (long long)b * W + k) : -1;
-    const int cu = offset + block_excl_scan(L, smem);
-    if (b < B) {
-      if (p.out_cu) p.out_cu[b] = cu;
-#pragma unroll
-      for (int k = 0; k <= kMaxK; ++k)
-        if (k < L) {
-          if (p.out_packed) p.out_packed[cu + k] = tok[k];
-          if (p.out_batch_id) p.out_batch_id[cu + k] = b;
-        }
-    }
-    offset += block_sum(L, smem);
-  }
-  if (p.out_cu && threadIdx.x == 0) p.out_cu[B] = offset;
-  for (long long q = offset + threadIdx.x; q < (long long)B * W; q += blockDim.x) {
-    if (p.out_packed) p.out_packed[q] = -1;
-    if (p.out_batch_id) p.out_batch_id[q] = -1;
-  }
-}
-
-// ---------------------------------------------------------------------------
-// kernel F: per-request finalisation (one CTA per request, after kernel A)
-// ---------------------------------------------------------------------------
-
-// Summary of one row from its chunk records (one warp).
-template <int MODE, typename T>
-__device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb, int x,
-                                float2* copy) {
-  RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
-  const long long rowid = (long long)b * p.R + r;
-  const float2* rec = p.rec + rowid * p.NC;
-  if (MODE == kGreedy) {
-    const float2 a = combine_argmax_records(rec, p.NC);
-    rs.m = a.x;
-    rs.idx = __float_as_int(a.y);
-    return rs;
-  }
-  const bool has_x = x >= 0 && x < p.V;
-  const float lx = __ldcg(p.lx + rowid);  // recorded by kernel A (meaningful if has_x)
-  const float2 ms = combine_softmax_records(rec, p.NC, p.cc, copy);
-  rs.m = ms.x;
-  rs.s = ms.y;
-  if (has_x && is_finite(ms.x)) rs.wx = ex2(fmaf(lx, p.cc, -ms.x * p.cc));
-  if (MODE == kTypical && is_finite(ms.x) && ms.y > 0.f) {
-    const float a = combine_entropy(rec, p.ent + rowid * p.NC, p.NC, p.cc, ms.x);
-    rs.h = __logf(ms.y) - 0.6931471805599453f * a / ms.y;
-  }
-  return rs;
-}
-
-// Threads of a finalize CTA: 8 warps (dense drafts: at 128 registers, two
-// CTAs per SM, so a request's residual cluster spans more SMs).
-template <int MODE>
-__host__ __device__ constexpr int fin_threads() { return 256; }
-constexpr int kMaxRows = 2 * kMaxK + 1;
-
-// The rejected position of a dense-draft request and its two rows' maxima
-// and reciprocal sums (n < 0: nothing left to draw).
-struct Residual {
-  int n;
-  float mp, ip, mq, iq;
-};
-
-template <int MODE, typename T, int VEC>
-__device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
-                                              const RowSum* srow, const int* s_tok, int x,
-                                              float u, int timed_out, Residual* resid);
-template <typename T, int VEC>
-__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
-                                           float* sums, int rank, int ncta);
-template <typename T, int VEC>
-__device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const Residual& st,
-                                           const float* sums, const float2* srec);
-
-// Draft token of row r of request b, or -1 (rows without one, or K_b invalid).
-__device__ __forceinline__ int row_token(const VerifyParams& p, int b, int r, int Kb) {
-  if (!row_needed(p, r, Kb)) return -1;
-  const int i = r > p.K ? r - p.K - 1 : r;
-  return i < Kb ? __ldg(p.draft_tokens + (long long)b * p.K + i) : -1;
-}
-
-// The token position r draws if the walk stops there (one warp): the
-// residual max(0, p_r - q_r) of a one-hot draft (p_r without x_r; x_r itself
-// when no mass is left beside it), else a draw from p_r (the bonus position,
-// typical acceptance, the bonus of dense drafts).  -1 for a row without a
-// finite max or a failed draw.  Each summarising warp computes it for its own
-// row, so the draw overlaps the other rows and the acceptance tests.
-template <int MODE, typename T, int VEC>
-__device__ __forceinline__ int position_draw(const VerifyParams& p, int b, int r, int Kb,
-                                             const RowSum& rs, int xr, float uK,
-                                             const float2* srec) {
-  if (!is_finite(rs.m)) return -1;
-  const bool residual = MODE == kOneHot && r < Kb;
-  if (residual && !(rs.s > 0.f)) return xr;  // p_r is the point mass at x_r
-  const T* row = row_ptr<T>(p.target, (long long)b * (p.K + 1) + r, p.V);
-  const uint32_t* mrow = mask_row(p, b, r);
-  const float cut = row_cut(p, (long long)b * p.R + r);
-  return srec ? draw_from_records<T, VEC, true>(row, srec + (long long)r * p.NC, p.NC, p.V, rs.m,
-                                                p.cc, uK, residual ? xr : -1, mrow, p.mask_words,
-                                                cut)
-              : draw_from_records<T, VEC>(row, p.rec + ((long long)b * p.R + r) * p.NC, p.NC,
-                                          p.V, rs.m, p.cc, uK, residual ? xr : -1, mrow,
-                                          p.mask_words, cut);
-}
-
-// The acceptance tests of all positions at once (one lane per position),
-// then the residual / bonus draw (rejection sampling, [SD] §2.1) or the
-// argmax (greedy).  Rows are summarised by the CTA's warps first; their chunk
-// records are kept in shared memory (dynamic, when they fit) for the draw.
-// Dynamic shared memory: [R*NC] records when cached, then [NC] residual
-// chunk sums (dense drafts).  Dense calls may run a cluster of CTAs per
-// request: the first one does all of the above and writes the outputs; the
-// others only help to read the rejected row pair.
-template <int MODE, typename T, int VEC>
-__global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const VerifyParams p) {
-  constexpr int kWarps = fin_threads<MODE>() / kWarp;
-  extern __shared__ float2 s_dyn[];
-  __shared__ RowSum srow[kMaxRows];
-  __shared__ Residual s_resid;
-  __shared__ int s_last[32];
-  __shared__ int s_tok[kMaxRows];  // the token each position would draw
-  int ncta = 1, rank = 0;
-  if (MODE == kDense) {
-    const cg::cluster_group cluster = cg::this_cluster();
-    ncta = (int)cluster.num_blocks();
-    rank = (int)cluster.block_rank();
-  }
-  const int b = blockIdx.x / ncta;
-  const bool leader = rank == 0;
-  const int lane = lane_id(), warp = threadIdx.x >> 5;
-  const int K = p.K;
-  float2* s_rec = p.fin_cache ? s_dyn : nullptr;
-  float* s_sums = reinterpret_cast<float*>(s_dyn + (p.fin_cache ? (long long)p.R * p.NC : 0));
-  // The request's inputs do not depend on kernel A: read them before waiting.
-  const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
-  const int Kv = (Kb >= 0 && Kb <= K) ? Kb : 0;
-  const int x0 = warp < p.R ? row_token(p, b, warp, Kb) : -1;
-  int x = -1;
-  float u = 0.f;
-  const float uK = MODE != kGreedy ? __ldg(p.uniforms + (long long)b * (K + 1) + K) : 0.f;
-  if (warp == 0) {
-    if (lane < Kv) x = __ldg(p.draft_tokens + (long long)b * K + lane);
-    if (MODE != kGreedy && lane < Kv) u = __ldg(p.uniforms + (long long)b * (K + 1) + lane);
-  }
-  if (threadIdx.x == 0) s_resid.n = -1;
-  pdl_wait();
-  pdl_launch_dependents();
-  // issued before the row summaries so that its latency overlaps theirs
-  const int timed_out = (leader && warp == 0) ? __ldcg(p.err) : 0;
-  if (leader) {
-    for (int r = warp; r < p.R; r += kWarps) {
-      RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
-      const int xr = r == warp ? x0 : row_token(p, b, r, Kb);
-      if (row_needed(p, r, Kb))
-        rs = summarise_row<MODE, T>(p, b, r, Kb, xr, s_rec ? s_rec + (long long)r * p.NC : nullptr);
-      if (lane == 0) srow[r] = rs;
-      // target row r <= K_b: the draw of position r (dense drafts: the bonus
-      // position only; the others draw from the residual)
-      if (MODE != kGreedy && Kb >= 0 && Kb <= K && r <= Kb && (MODE != kDense || r == Kb)) {
-        const int tok = position_draw<MODE, T, VEC>(p, b, r, Kb, rs, xr, uK, s_rec);
-        if (lane == 0) s_tok[r] = tok;
-      }
-    }
-    __syncthreads();
-    if (warp == 0)
-      finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_tok, x, u, timed_out, &s_resid);
-  }
-  if (MODE == kDense) {
-    // Dense drafts: the request's CTAs learn n from the first one, read the
-    // rejected row pair for the residual chunk sums, and the first CTA draws.
-    // Both cluster barriers are passed by every thread of every CTA.
-    cg::cluster_group cluster = cg::this_cluster();
-    if (ncta > 1) {
-      cluster.sync();
-      if (!leader && threadIdx.x == 0) s_resid = *cluster.map_shared_rank(&s_resid, 0);
-    }
-    __syncthreads();
-    const Residual st = s_resid;
-    if (st.n >= 0)
-      residual_sums<T, VEC>(p, b, st, ncta > 1 ? cluster.map_shared_rank(s_sums, 0) : s_sums,
-                            rank, ncta);
-    if (ncta > 1)
-      cluster.sync();  // every sum is in the first CTA's shared memory
-    else
-      __syncthreads();
-    if (leader && warp == 0 && st.n >= 0) residual_pick<T, VEC>(p, b, st, s_sums, s_rec);
-  }
-  if (!leader) return;
-  // The last request of the call clears the counters and writes the packed
-  // output.
-  __syncthreads();
-  if (threadIdx.x == 0) s_last[0] = atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B;
-  __syncthreads();
-  if (!s_last[0]) return;
-  if (threadIdx.x == 0) {
-    *p.err = 0;
-    *p.fin_ticket = 0;
-  }
-  if (p.compact_in_finalize) compact_all(p, s_last);
-}
-
-template <int MODE, typename T, int VEC>
-__device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
-                                              const RowSum* srow, const int* s_tok, int x,
-                                              float u, int timed_out, Residual* resid) {
-  const int lane = lane_id();
-  const int K = p.K;
-  // A bounded wait that gave up in kernel A (a device fault) invalidates the
-  // whole call: its chunk records may be missing.
-  int status = timed_out ? kTimeout : 0;
-  if (Kb < 0 || Kb > K) {
-    status |= kBadDraftLen;
-    Kb = 0;
-  }
-  if (!status && __any_sync(0xffffffffu, lane < Kb && (x < 0 || x >= p.V))) status = kBadToken;
-  int n = 0, token = -1;
-  float theta = -1.f;
-  bool pending = false;
-  if (!status) {
-    RowSum rt{qnan(), 0.f, 0.f, -1, 0.f}, rd{qnan(), 0.f, 0.f, -1, 0.f};
-    if (lane <= Kb) rt = srow[lane];
-    if (MODE == kDense && lane < Kb) rd = srow[K + 1 + lane];
-    bool bad = lane <= Kb && !is_finite(rt.m);
-    if (MODE == kDense && lane < Kb) bad = bad || !is_finite(rd.m);
-    bool acc = false;
-    if (lane < Kb) {
-      if (MODE == kGreedy) {
-        acc = (x == rt.idx);
-        theta = acc ? 1.f : 0.f;
-      } else if (MODE == kTypical) {  // p(x) > min(eps, delta * exp(-H)); reports p(x)
-        const float px = rt.wx / rt.s;
-        theta = px;
-        acc = px > fminf(p.eps, p.delta * __expf(-rt.h));
-      } else {
-        if (MODE == kOneHot) {  // q = point mass at x: accept iff u < p(x)
-          const float px = rt.wx / (rt.s + rt.wx);
-          theta = fminf(1.f, px);
-          acc = u < px;
-        } else {  // accept iff u * q(x) < p(x)
-          const float px = rt.wx / rt.s, qx = rd.wx / rd.s;
-          theta = qx > 0.f ? fminf(1.f, px / qx) : (px > 0.f ? 1.f : 0.f);
-          acc = u * qx < px;
-        }
-      }
-    }
-    const unsigned stop = __ballot_sync(0xffffffffu, lane < Kb && (bad || !acc));
-    n = stop ? __ffs(stop) - 1 : Kb;
-    if (__shfl_sync(0xffffffffu, bad ? 1 : 0, n)) status = kBadLogits;
-    const float m_n = __shfl_sync(0xffffffffu, rt.m, n);
-    const float s_n = __shfl_sync(0xffffffffu, rt.s, n);
-    const int idx_n = __shfl_sync(0xffffffffu, rt.idx, n);
-    const int x_n = __shfl_sync(0xffffffffu, x, n);
-    const float mq_n = __shfl_sync(0xffffffffu, rd.m, n);
-    const float sq_n = __shfl_sync(0xffffffffu, rd.s, n);
-    if (!status) {
-      if (MODE == kGreedy) {
-        token = idx_n;
-      } else if (MODE == kDense && n < Kb) {
-        pending = true;  // the whole CTA draws from max(0, p_n - q_n) next
-        if (lane == 0) *resid = Residual{n, m_n, 1.f / s_n, mq_n, 1.f / sq_n};
-      } else {
-        token = s_tok[n];  // drawn beside the row summaries (position_draw)
-        if (token < 0) status = kBadLogits;
-      }
-    }
-  }
-  if (p.out_accept_prob && lane < K && (MODE != kGreedy || p.greedy_prob))
-    p.out_accept_prob[(long long)b * K + lane] =
-        (!status && lane < Kb && lane <= n) ? theta : -1.f;
-  if (!pending) write_request(p, b, status, n, token, x);
-}
 
 // ---------------------------------------------------------------------------
 // kernel A: chunk records (a single streaming read of the logits)
@@ -891,172 +247,6 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
 }
 
 // ---------------------------------------------------------------------------
-// dense-draft residual (inside kernel F, by all warps of the request's CTA)
-// ---------------------------------------------------------------------------
-
-template <typename T, int VEC>
-__host__ __device__ constexpr int residual_group() {
-  return Lane<T, VEC>::G > 1 ? Lane<T, VEC>::G / 2 : 1;
-}
-
-// The residual chunk sums over chunks [lo, hi) (kExtra: with grammar masks
-// and top-k / top-p cuts applied).
-template <typename T, int VEC, bool kExtra>
-__device__ __forceinline__ void residual_sums_loop(const VerifyParams& p, int b, const Residual& st,
-                                                   float* sums, int lo, int hi) {
-  using L = Lane<T, VEC>;
-  constexpr int G = residual_group<T, VEC>();
-  const int lane = lane_id(), warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-  const int K = p.K;
-  const float cc = p.cc;
-  const T* tr = row_ptr<T>(p.target, (long long)b * (K + 1) + st.n, p.V);
-  const T* dr = row_ptr<T>(p.draft, (long long)b * K + st.n, p.V);
-  const float nbp = -st.mp * cc, nbq = -st.mq * cc;
-  const uint32_t* mrow = kExtra ? mask_row(p, b, st.n) : nullptr;
-  const float cut_t = kExtra ? row_cut(p, (long long)b * p.R + st.n) : -INFINITY;
-  const float cut_d = kExtra ? row_cut(p, (long long)b * p.R + K + 1 + st.n) : -INFINITY;
-  for (int c0 = lo + warp * G; c0 < hi; c0 += nwarps * G) {
-    typename L::Raw rt[G][L::NV], rd[G][L::NV];
-    uint32_t word[G];
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (c0 + g < hi) {
-        load_chunk<T, VEC>(tr, p.V, c0 + g, rt[g]);
-        load_chunk<T, VEC>(dr, p.V, c0 + g, rd[g]);
-        if (kExtra && mrow) word[g] = mask_word(mrow, p.mask_words, c0 + g);
-      }
-#pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (c0 + g < hi) {
-        if (kExtra) {
-          if (mrow) {
-            allow_only_chunk<T, VEC>(rt[g], word[g]);
-            allow_only_chunk<T, VEC>(rd[g], word[g]);
-          }
-          if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt[g], cut_t);
-          if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd[g], cut_d);
-        }
-        float w = 0.f;
-#pragma unroll
-        for (int k = 0; k < L::NV; ++k)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            w += residual_weight(L::get(rt[g][k], e), L::get(rd[g][k], e), cc, nbp, st.ip, nbq,
-                                 st.iq);
-        w = warp_sum(w);
-        if (lane == 0) sums[c0 + g] = w;
-      }
-  }
-}
-
-// Request b was rejected at st.n: the chunk sums of max(0, p_n - q_n) over
-// the (target, draft) row pair.  CTA `rank` of the request's `ncta` takes a
-// contiguous range of chunks, its warps groups of consecutive chunks; each
-// sum goes to sums[c] (the first CTA's shared memory).  Calls without grammar
-// masks or filters take a loop without their checks.  Called by every thread
-// of the CTA.
-template <typename T, int VEC>
-__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
-                                           float* sums, int rank, int ncta) {
-  const int lo = (int)((long long)p.NC * rank / ncta);
-  const int hi = (int)((long long)p.NC * (rank + 1) / ncta);
-  if (p.mask || p.filter)
-    residual_sums_loop<T, VEC, true>(p, b, st, sums, lo, hi);
-  else
-    residual_sums_loop<T, VEC, false>(p, b, st, sums, lo, hi);
-}
-
-// One warp: the residual draw from the chunk sums (the crossing chunk, then
-// a rescan of that chunk of both rows), and the request's outputs.
-template <typename T, int VEC>
-__device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const Residual& st,
-                                           const float* sums, const float2* srec) {
-  using L = Lane<T, VEC>;
-  const int lane = lane_id();
-  const int K = p.K, NC = p.NC;
-  const float cc = p.cc;
-  const T* tr = row_ptr<T>(p.target, (long long)b * (K + 1) + st.n, p.V);
-  const T* dr = row_ptr<T>(p.draft, (long long)b * K + st.n, p.V);
-  const float nbp = -st.mp * cc, nbq = -st.mq * cc;
-  const float uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
-  const uint32_t* mrow = mask_row(p, b, st.n);
-  const float cut_t = row_cut(p, (long long)b * p.R + st.n);
-  const float cut_d = row_cut(p, (long long)b * p.R + K + 1 + st.n);
-  auto weight = [&](int c) { return sums[c]; };
-  int token;
-  if constexpr (VEC * sizeof(T) == 16) {
-    float frac = 0.f;
-    const int c = find_chunk_runs(weight, NC, uK, &frac);
-    if (c < 0) {  // no residual mass (rounding only): draw from p_n
-      token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V,
-                                                     st.mp, cc, uK, -1, mrow, p.mask_words, cut_t)
-                   : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
-                                               p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
-    } else {
-      float vt[kWarp], vd[kWarp];
-      load_run<T>(tr, p.V, c, vt);
-      load_run<T>(dr, p.V, c, vd);
-      const uint32_t at = run_allowed(vt, mrow, p.mask_words, c, cut_t, -1);
-      const uint32_t ad = run_allowed(vd, mrow, p.mask_words, c, cut_d, -1);
-      float w[kWarp];
-#pragma unroll
-      for (int e = 0; e < kWarp; ++e)
-        w[e] = residual_weight(((at >> e) & 1u) ? vt[e] : -INFINITY,
-                               ((ad >> e) & 1u) ? vd[e] : -INFINITY, cc, nbp, st.ip, nbq, st.iq);
-      token = pick_in_runs(w, frac, c * kChunk);
-    }
-    const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
-    write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
-  } else {
-    float wc[kRecCache];
-    float tot = 0.f;
-#pragma unroll
-    for (int t = 0; t < kRecCache; ++t) {
-      const int c = lane + t * kWarp;
-      wc[t] = c < NC ? weight(c) : 0.f;
-      tot += wc[t];
-    }
-    for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
-    tot = warp_sum(tot);
-    if (!(tot > 0.f)) {  // no residual mass (rounding only): draw from p_n
-      token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V, st.mp,
-                                                     cc, uK, -1, mrow, p.mask_words, cut_t)
-                   : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
-                                               p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
-    } else {
-      float frac = 0.f;
-      const int c = find_chunk(wc, weight, NC, uK * tot, &frac);
-      typename L::Raw rt[L::NV], rd[L::NV];
-      load_chunk<T, VEC>(tr, p.V, c, rt);
-      load_chunk<T, VEC>(dr, p.V, c, rd);
-      if (mrow) {
-        const uint32_t word = mask_word(mrow, p.mask_words, c);
-        allow_only_chunk<T, VEC>(rt, word);
-        allow_only_chunk<T, VEC>(rd, word);
-      }
-      if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt, cut_t);
-      if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd, cut_d);
-      float w[L::NV * VEC];
-      float gsum[L::NV];
-#pragma unroll
-      for (int k = 0; k < L::NV; ++k) {
-        gsum[k] = 0.f;
-#pragma unroll
-        for (int e = 0; e < VEC; ++e) {
-          const float we =
-              residual_weight(L::get(rt[k], e), L::get(rd[k], e), cc, nbp, st.ip, nbq, st.iq);
-          w[k * VEC + e] = we;
-          gsum[k] += we;
-        }
-      }
-      token = select_in_tile<L::NV, VEC>(w, gsum, frac, c * kChunk);
-    }
-    const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
-    write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
-  }
-}
-
-// ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
@@ -1067,16 +257,6 @@ int blocks_per_sm(K kernel) {
     n = 1;
   return n;
 }
-
-// CTAs per request for the dense-draft residual: as many as fit on the GPU
-// at once (`slots` finalize CTAs), at most one per 16 chunks of the row (a
-// CTA's 8 warps read 2 chunks of each row at a time), at most 8.
-int residual_cluster(const VerifyParams& p, int slots) {
-  int c = p.B > 0 ? slots / p.B : 1;
-  c = c < (p.NC + 15) / 16 ? c : (p.NC + 15) / 16;
-  return c < 1 ? 1 : (c > 8 ? 8 : c);
-}
-
 template <int MODE, typename T, int VEC>
 cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
   DeviceInfo di;
@@ -1136,266 +316,27 @@ cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-template <int MODE, typename T, int VEC>
-cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
-  cudaError_t err = launch_records<MODE, T, VEC>(p, s);
-  if (err != cudaSuccess) return err;
-  DeviceInfo di;
-  err = device_info(&di);
-  if (err != cudaSuccess) return err;
-  VerifyParams pc = p;
-  void* args[] = {&pc};
-  // F: acceptance tests and draws, one CTA per request
-  const void* fin = reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>);
-  const size_t fin_smem = fin_smem_bytes(p, MODE == kDense);
-  static PerDevice once;
-  int occ = 1;  // finalize CTAs per SM
-  err = per_device(once, &occ, [&](int& v) {
-    const cudaError_t e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)kFinSmemMax);
-    if (e != cudaSuccess) return e;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fin, fin_threads<MODE>(),
-                                                      (size_t)kFinCacheLimit) != cudaSuccess ||
-        v < 1)
-      v = 1;
-    return cudaSuccess;
-  });
-  if (err != cudaSuccess) return err;
-  const int ncta = MODE == kDense ? residual_cluster(p, di.sms * occ) : 1;
-  return launch_pdl(fin, dim3(p.B * ncta), dim3(fin_threads<MODE>()), s, args, fin_smem, ncta);
-}
-
-// ---------------------------------------------------------------------------
-// typical acceptance on a candidate tree (after kernel A over all tree rows)
-// ---------------------------------------------------------------------------
-
-// One CTA per request: every row's summary (max, sum, entropy), every node's
-// typical test under its parent's distribution, the accepted subtree by one
-// thread in node order (a parent precedes its children), the deepest
-// accepted node (lowest id among equals), then the draw from its row.
-constexpr int kTreeTypicalThreads = 512;
-constexpr size_t kTreeCacheLimit = 96 * 1024;  // records kept in shared memory for the draw
-
-// Summaries of every tree row with the loads of up to 4 rows per warp issued
-// together (rows of up to 64 chunks; wider rows one at a time); the records
-// go to `cache` (shared memory) when given.  Same arithmetic as
-// combine_softmax_records and combine_entropy.
-template <typename T>
-__device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum* srow,
-                                    float2* cache) {
-  const int lane = lane_id(), warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  const int NC = p.NC;
-  const float cc = p.cc;
-  if (NC > 2 * kWarp) {
-    for (int r = warp; r <= N; r += nw) {
-      const RowSum rs = summarise_row<kTypical, T>(p, b, r, N, -1,
-                                                   cache ? cache + (long long)r * NC : nullptr);
-      if (lane == 0) srow[r] = rs;
-    }
-    return;
-  }
-  constexpr int J = 4;
-  for (int r0 = warp; r0 <= N; r0 += nw * J) {
-    float2 rc[J][2];
-    float ea[J][2];
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int r = r0 + j * nw;
-      const long long base = ((long long)b * p.R + r) * NC;
-#pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int c = lane + q * kWarp;
-        const bool in = r <= N && c < NC;
-        rc[j][q] = in ? __ldcg(p.rec + base + c) : make_float2(-INFINITY, 0.f);
-        ea[j][q] = in ? __ldcg(p.ent + base + c) : 0.f;
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < J; ++j) {
-      const int r = r0 + j * nw;
-      if (r > N) break;
-      const float m = warp_max_nan(max_nan(rc[j][0].x, rc[j][1].x));
-      RowSum rs{m == -INFINITY ? -INFINITY : qnan(), 0.f, 0.f, -1, 0.f};
-      if (is_finite(m)) {
-        const float nb = -m * cc;
-        float sum = 0.f, a = 0.f;
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const float2 rq = rc[j][q];
-          sum += rq.y * ex2(fmaf(rq.x, cc, nb));
-          if (rq.y > 0.f) {
-            const float d = (rq.x - m) * cc;
-            a += ex2(d) * fmaf(d, rq.y, ea[j][q]);
-          }
-        }
-        sum = warp_sum(sum);
-        a = warp_sum(a);
-        rs.m = m;
-        rs.s = sum;
-        if (sum > 0.f) rs.h = __logf(sum) - 0.6931471805599453f * a / sum;
-      }
-      if (cache) {
-#pragma unroll
-        for (int q = 0; q < 2; ++q)
-          if (lane + q * kWarp < NC) cache[(long long)r * NC + lane + q * kWarp] = rc[j][q];
-      }
-      if (lane == 0) srow[r] = rs;
-    }
-  }
-}
-
-template <typename T, int VEC>
-__global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const VerifyParams p,
-                                                                         const TreeTypical t) {
-  extern __shared__ float2 s_cache[];
-  __shared__ RowSum srow[kMaxTreeNodes + 1];
-  __shared__ unsigned char spass[kMaxTreeNodes + 1], sacc[kMaxTreeNodes + 1];
-  __shared__ int s_best, s_status;
-  const int b = blockIdx.x;
-  const int lane = lane_id(), warp = threadIdx.x >> 5;
-  const int N = t.N;
-  const bool cached = (size_t)(N + 1) * p.NC * sizeof(float2) <= kTreeCacheLimit;
-  // the tree tokens and each node's logit in its parent's row are inputs:
-  // read them before waiting for kernel A
-  int bad = 0, tok = 0;
-  float lp = 0.f;
-  const int n_mine = 1 + threadIdx.x;  // N <= 256 < the CTA's threads
-  if (n_mine <= N) {
-    tok = __ldg(t.tokens + (long long)b * N + n_mine - 1);
-    bad = tok < 0 || tok >= p.V;
-    if (!bad)
-      lp = load_logit(row_ptr<T>(p.target, (long long)b * (N + 1) + t.parent[n_mine], p.V), tok);
-  }
-  bad = __syncthreads_or(bad);
-  pdl_wait();
-  pdl_launch_dependents();
-  summarise_tree_rows<T>(p, b, N, srow, cached ? s_cache : nullptr);
-  __syncthreads();
-  if (n_mine <= N) {
-    const RowSum rp = srow[t.parent[n_mine]];
-    unsigned char ok = 0;
-    if (!bad && is_finite(rp.m) && rp.s > 0.f) {
-      const float px = ex2(fmaf(lp, p.cc, -rp.m * p.cc)) / rp.s;
-      ok = px > fminf(p.eps, p.delta * __expf(-rp.h));
-    }
-    spass[n_mine] = ok;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    int status = bad ? kBadToken : (__ldcg(p.err) ? kTimeout : 0);
-    sacc[0] = 1;
-    int best = 0;
-    if (!status && !is_finite(srow[0].m)) status = kBadLogits;
-    for (int n = 1; n <= N && !status; ++n) {
-      sacc[n] = sacc[t.parent[n]] && spass[n];
-      if (!sacc[n]) continue;
-      if (!is_finite(srow[n].m)) status = kBadLogits;  // an accepted node's row is needed
-      if (t.depth[n] > t.depth[best]) best = n;
-    }
-    s_best = best;
-    s_status = status;
-  }
-  __syncthreads();
-  if (warp != 0) return;
-  const int status0 = s_status, best = s_best;
-  int token = -1;
-  if (!status0) {
-    const RowSum rb = srow[best];
-    const T* row = row_ptr<T>(p.target, (long long)b * (N + 1) + best, p.V);
-    const float u = __ldg(t.uniforms + b);
-    token = cached ? draw_from_records<T, VEC, true>(row, s_cache + (long long)best * p.NC, p.NC,
-                                                     p.V, rb.m, p.cc, u, -1, nullptr, 0, -INFINITY)
-                   : draw_from_records<T, VEC>(row, p.rec + ((long long)b * (N + 1) + best) * p.NC,
-                                               p.NC, p.V, rb.m, p.cc, u, -1, nullptr, 0,
-                                               -INFINITY);
-  }
-  const int status = status0 ? status0 : (token < 0 ? kBadLogits : 0);
-  const int d = status ? -1 : t.depth[best];
-  // path and tokens, root first (one lane per level): level k < d holds the
-  // token of the path's node at level k + 1, level d the drawn token
-  for (int k = lane; k < t.D1; k += kWarp) {
-    int node = -1, tok = -1;
-    if (!status && k <= d) {
-      int a = best;  // the path's node at level k + 1 (best itself when k = d)
-      for (int up = d; up > k + 1; --up) a = t.parent[a];
-      if (k < d) {
-        tok = __ldg(t.tokens + (long long)b * N + a - 1);
-        node = t.parent[a];
-      } else {
-        tok = token;
-        node = best;
-      }
-    }
-    if (t.out_path) t.out_path[(long long)b * t.D1 + k] = node;
-    t.out_tokens[(long long)b * t.D1 + k] = tok;
-  }
-  if (lane == 0) {
-    t.out_accept_len[b] = status ? 0 : d + 1;
-    if (t.out_status) t.out_status[b] = status;
-    // the last request of the call clears the workspace counters
-    if (atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
-      *p.err = 0;
-      *p.fin_ticket = 0;
-    }
-  }
-}
-
-template <typename T, int VEC>
-cudaError_t launch_tree_typical_typed(const VerifyParams& p, const TreeTypical& t,
-                                      cudaStream_t s) {
-  cudaError_t err = launch_records<kTypical, T, VEC>(p, s);
-  if (err != cudaSuccess) return err;
-  VerifyParams pc = p;
-  TreeTypical tc = t;
-  void* args[] = {&pc, &tc};
-  const void* fn = reinterpret_cast<const void*>(tree_typical_kernel<T, VEC>);
-  static PerDevice once;
-  err = per_device(once, nullptr, [&](int&) {
-    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                (int)kTreeCacheLimit);
-  });
-  if (err != cudaSuccess) return err;
-  const size_t cache = (size_t)(t.N + 1) * p.NC * sizeof(float2);
-  return launch_pdl(fn, dim3(p.B), dim3(kTreeTypicalThreads), s, args,
-                    cache <= kTreeCacheLimit ? cache : 0);
-}
-
-template <int MODE>
-cudaError_t launch_mode(int dtype, bool vec, const VerifyParams& p, cudaStream_t s) {
-  if (dtype == kBF16)
-    return vec ? launch_typed<MODE, uint16_t, 8>(p, s) : launch_typed<MODE, uint16_t, 1>(p, s);
-  return vec ? launch_typed<MODE, float, 4>(p, s) : launch_typed<MODE, float, 1>(p, s);
-}
-
 }  // namespace
-
-size_t fin_cache_bytes(const VerifyParams& p) { return sizeof(float2) * (size_t)p.R * p.NC; }
-
-size_t fin_smem_bytes(const VerifyParams& p, bool dense) {
-  return (p.fin_cache ? fin_cache_bytes(p) : 0) + (dense ? sizeof(float) * (size_t)p.NC : 0);
-}
 
 int chunks_per_task(int dtype, bool vec) {
   if (vec) return kConsumers;
   return Lane<float, 1>::G;
 }
 
-cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeTypical& t,
-                                cudaStream_t stream) {
-  if (dtype == kBF16)
-    return vec ? launch_tree_typical_typed<uint16_t, 8>(p, t, stream)
-               : launch_tree_typical_typed<uint16_t, 1>(p, t, stream);
-  return vec ? launch_tree_typical_typed<float, 4>(p, t, stream)
-             : launch_tree_typical_typed<float, 1>(p, t, stream);
-}
-
-cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,
-                          cudaStream_t stream) {
+cudaError_t launch_records(int mode, int dtype, bool vec, const VerifyParams& p,
+                           cudaStream_t stream) {
+  auto typed = [&](auto mode_tag) -> cudaError_t {
+    constexpr int M = decltype(mode_tag)::value;
+    if (dtype == kBF16)
+      return vec ? launch_records<M, uint16_t, 8>(p, stream)
+                 : launch_records<M, uint16_t, 1>(p, stream);
+    return vec ? launch_records<M, float, 4>(p, stream) : launch_records<M, float, 1>(p, stream);
+  };
   switch (mode) {
-    case kOneHot: return launch_mode<kOneHot>(dtype, vec, p, stream);
-    case kDense: return launch_mode<kDense>(dtype, vec, p, stream);
-    case kTypical: return launch_mode<kTypical>(dtype, vec, p, stream);
-    default: return launch_mode<kGreedy>(dtype, vec, p, stream);
+    case kOneHot: return typed(std::integral_constant<int, kOneHot>());
+    case kDense: return typed(std::integral_constant<int, kDense>());
+    case kTypical: return typed(std::integral_constant<int, kTypical>());
+    default: return typed(std::integral_constant<int, kGreedy>());
   }
 }
 
