@@ -128,12 +128,67 @@ struct Stream {
   }
 };
 
+// One logit of a staged chunk (shared-memory byte address of the chunk),
+// widened to fp32.
+__device__ __forceinline__ float stage_logit(uint32_t chunk, int i, const uint16_t*) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(chunk + 2u * (uint32_t)i));
+  return __uint_as_float((uint32_t)v << 16);
+}
+__device__ __forceinline__ float stage_logit(uint32_t chunk, int i, const float*) {
+  float v;
+  asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(chunk + 4u * (uint32_t)i));
+  return v;
+}
+
+// A chunk whose grammar mask allows at most kSparseAllowed of its tokens
+// (structured output): the same record as the dense path - {max over the
+// allowed tokens (NaN wins), sum of 2^((l - max) c) over them leaving out
+// mask_x}, the typical calls' entropy accumulator, the draft token's logit -
+// from the allowed logits alone, read from the stage.  Lane l takes the
+// tokens of its mask word (32 l .. 32 l + 31 of the chunk); bits past V are
+// dropped.
+constexpr int kSparseAllowed = 128;
+
+template <int MODE, typename T>
+__device__ __forceinline__ float2 sparse_chunk_record(const VerifyParams& p, uint32_t chunk, int c,
+                                                      uint32_t word, int rowid, int x,
+                                                      float* ent) {
+  const int lane = lane_id();
+  const T* tag = nullptr;
+  float lm = -INFINITY;
+  for (uint32_t b = word; b; b &= b - 1u) lm = max_nan(lm, stage_logit(chunk, lane * kWarp + __ffs(b) - 1, tag));
+  const float cm = warp_max_nan(lm);
+  const int xo = x - c * kChunk;  // the draft token's logit (-inf where disallowed)
+  if (xo >= 0 && xo < kChunk && lane == (xo >> 5))
+    p.lx[rowid] = ((word >> (xo & 31)) & 1u) ? stage_logit(chunk, xo, tag) : -INFINITY;
+  if (!is_finite(cm)) {
+    if (ent && lane == 0) *ent = 0.f;
+    return make_float2(cm == -INFINITY ? -INFINITY : qnan(), 0.f);
+  }
+  const float nb = -cm * p.cc;
+  float s = 0.f, et = 0.f;
+  for (uint32_t b = word; b; b &= b - 1u) {
+    const int i = lane * kWarp + __ffs(b) - 1;
+    if (MODE == kOneHot && i == xo) continue;
+    const float a = fmaf(stage_logit(chunk, i, tag), p.cc, nb);
+    const float w = ex2(a);
+    s += w;
+    if (ent) et = fmaf(w, fmaxf(a, -256.f), et);
+  }
+  if (ent) {
+    et = warp_sum(et);
+    if (lane == 0) *ent = et;
+  }
+  return make_float2(cm, warp_sum(s));
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
-template <int MODE, typename T, int VEC>
-__global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const VerifyParams p) {
+template <int MODE, typename T, int VEC, bool kMasked>
+__global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const VerifyParams p) {
   using L = Lane<T, VEC>;
   using ST = Stream<T>;
   constexpr int S = ST::kStages;
@@ -221,19 +276,34 @@ __global__ void __launch_bounds__(kStreamThreads) verify_stream_kernel(const Ver
     }
     const int4 m = meta[s];
     if (m.x < 0) break;  // end marker
-    if (w < m.z) {
+    if (kMasked && w < m.z) {  // grammar-masked calls (a separate instantiation)
+      const int c = m.y + w;
+      const uint32_t chunk = stage_of(s) + w * ST::kChunkBytes;
+      float* ent = MODE == kTypical ? p.ent + (long long)m.x * p.NC + c : nullptr;
+      uint32_t word = 0;
+      if (c * kWarp + lane < p.mask_words)
+        word = p.mask_bulk ? reinterpret_cast<const uint32_t*>(
+                                 smem + ST::kMaskOffset + s * ST::kMaskStageBytes +
+                                 w * ST::kMaskChunkBytes)[lane]
+                           : __ldg(item_mask(p, m.x) + c * kWarp + lane);
+      const int first = c * kChunk + lane * kWarp;  // this word's first token
+      if (first + kWarp > p.V) word &= first >= p.V ? 0u : (1u << (p.V - first)) - 1u;
+      float2 out;
+      if (MODE != kGreedy &&
+          __reduce_add_sync(0xffffffffu, (unsigned)__popc(word)) <= (unsigned)kSparseAllowed) {
+        out = sparse_chunk_record<MODE, T>(p, chunk, c, word, m.x, m.w, ent);
+      } else {
+        typename L::Raw raw[L::NV];
+        load_chunk_smem<T, VEC>(chunk, p.V, c, raw);
+        allow_only_chunk<T, VEC>(raw, word);
+        record_draft_logit<T, VEC>(p, raw, c, m.x, m.w);
+        out = chunk_record<MODE, T, VEC>(raw, c, p.cc, MODE == kOneHot ? m.w : -1, ent);
+      }
+      if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
+    } else if (w < m.z) {
       const int c = m.y + w;
       typename L::Raw raw[L::NV];
       load_chunk_smem<T, VEC>(stage_of(s) + w * ST::kChunkBytes, p.V, c, raw);
-      if (p.mask) {
-        uint32_t word = 0;
-        if (c * kWarp + lane < p.mask_words)
-          word = p.mask_bulk ? reinterpret_cast<const uint32_t*>(
-                                   smem + ST::kMaskOffset + s * ST::kMaskStageBytes +
-                                   w * ST::kMaskChunkBytes)[lane]
-                             : __ldg(item_mask(p, m.x) + c * kWarp + lane);
-        allow_only_chunk<T, VEC>(raw, word);
-      }
       record_draft_logit<T, VEC>(p, raw, c, m.x, m.w);
       const float2 out = chunk_record<MODE, T, VEC>(
           raw, c, p.cc, MODE == kOneHot ? m.w : -1,
@@ -271,14 +341,16 @@ cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
   } else if constexpr (VEC * sizeof(T) == 16) {
     constexpr int smem_max = Stream<T>::smem_bytes(true);
     const int smem = Stream<T>::smem_bytes(p.mask_bulk != 0);
-    static PerDevice once;
+    const void* fn = p.mask ? reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC, true>)
+                            : reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC, false>);
+    static PerDevice once[2];
     int occ = 1;
-    err = per_device(once, &occ, [&](int& v) {
-      cudaError_t e = cudaFuncSetAttribute(verify_stream_kernel<MODE, T, VEC>,
-                                           cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    err = per_device(once[p.mask ? 1 : 0], &occ, [&](int& v) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           smem_max);
       if (e != cudaSuccess) return e;
-      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-              &v, verify_stream_kernel<MODE, T, VEC>, kStreamThreads, smem_max) != cudaSuccess ||
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fn, kStreamThreads, smem_max) !=
+              cudaSuccess ||
           v < 1)
         v = 1;
       return cudaSuccess;
@@ -287,16 +359,20 @@ cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
     const long long cap = (long long)di.sms * occ;
     const int grid = (int)(p.total_tasks < cap ? p.total_tasks : cap);
     // Chained to the previous call's finalize kernel by programmatic dependent
-    // launch, except behind dense-draft calls, whose finalize CTAs fill whole
-    // SMs: there it measured slower (one-hot B256 K5: +2.8%, dense B64 K3:
-    // -3%), so dense calls launch it plainly.
+    // launch, except behind dense-draft calls: there it measured slower
+    // (one-hot B256 K5: +2.8%, dense B64 K3: -3%), so dense calls launch it
+    // plainly.
     if (MODE != kDense) {
-      err = launch_pdl(reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC>),
-                       dim3(grid), dim3(kStreamThreads), s, args, smem);
-      if (err != cudaSuccess) return err;
+      err = launch_pdl(fn, dim3(grid), dim3(kStreamThreads), s, args, smem);
     } else {
-      verify_stream_kernel<MODE, T, VEC><<<grid, kStreamThreads, smem, s>>>(p);
+      cudaLaunchConfig_t cfg = {};
+      cfg.gridDim = dim3(grid);
+      cfg.blockDim = dim3(kStreamThreads);
+      cfg.dynamicSmemBytes = smem;
+      cfg.stream = s;
+      err = cudaLaunchKernelExC(&cfg, fn, args);
     }
+    if (err != cudaSuccess) return err;
   } else {
     static PerDevice once;
     int occ = 1;
