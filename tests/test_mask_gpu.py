@@ -63,6 +63,19 @@ def test_masked_sampling_grid(V, K, T, dtype, drafts):
     check_masked(wl)
 
 
+@pytest.mark.parametrize("allowed_frac,drafts", [(0.125, "onehot"), (0.125, "dense"),
+                                                 (0.0005, "onehot")])
+def test_masked_sparse_and_dense_chunks(allowed_frac, drafts):
+    """Chunks whose mask allows at most 128 tokens take the streaming
+    kernel's sparse path, the others the dense one: at an allowed fraction
+    of 1/8 (about 128 per 1024-token chunk) the rows mix both; at 0.0005 most
+    chunks allow none or one token."""
+    wl = synth.make_sample_case(24, 3, 152064, drafts=drafts, T=0.9, sigma=0.5, seed=82,
+                                grammar=dict(p_free=0.2, allowed_frac=allowed_frac,
+                                             junk_tail=True))
+    check_masked(wl)
+
+
 @pytest.mark.parametrize("V,dtype", [(1000, "bf16"), (4104, "bf16"), (32001, "f32"),
                                      (152064, "bf16")])
 def test_masked_greedy(V, dtype):
