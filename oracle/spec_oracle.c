@@ -28,7 +28,7 @@
  *
  * Every quantity is computed in double precision, one request at a time,
  * with plain serial loops: no blocking, fusion or reordering.  Where the
- * pages leave a step open, the reading taken is named R1..R18 in the
+ * pages leave a step open, the reading taken is named R1..R21 in the
  * comments (the same labels are used in the design notes).
  *
  * Logit storage: dtype 0 = IEEE fp32, dtype 1 = bfloat16 given as raw

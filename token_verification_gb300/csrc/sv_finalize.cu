@@ -496,14 +496,17 @@ __device__ __forceinline__ int position_draw(const VerifyParams& p, int b, int r
                                           p.mask_words, cut);
 }
 
-// The acceptance tests of all positions at once (one lane per position),
-// then the residual / bonus draw (rejection sampling, [SD] §2.1) or the
-// argmax (greedy).  Rows are summarised by the CTA's warps first; their chunk
-// records are kept in shared memory (dynamic, when they fit) for the draw.
-// Dynamic shared memory: [R*NC] records when cached, then [NC] residual
-// chunk sums (dense drafts).  Dense calls may run a cluster of CTAs per
-// request: the first one does all of the above and writes the outputs; the
-// others only help to read the rejected row pair.
+// Rows are summarised by the CTA's warps, each of which also draws the token
+// its own position would emit if the walk stopped there (the residual or
+// bonus draw of rejection sampling, §2.1 of the page cited at the top of this
+// file); their chunk records are kept in shared memory (dynamic, when they
+// fit) for the draws.  Then one warp runs the acceptance tests of all
+// positions at once (one lane per position) and takes the stopping
+// position's token, or the argmax (greedy).  Dynamic shared memory: [R*NC]
+// records when cached, then [NC] residual chunk sums (dense drafts).  Dense
+// calls may run a cluster of CTAs per request: the first one does all of the
+// above and writes the outputs; the others only help to read the rejected
+// row pair.
 template <int MODE, typename T, int VEC>
 __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const VerifyParams p) {
   constexpr int kWarps = fin_threads<MODE>() / kWarp;
