@@ -85,3 +85,28 @@ def test_reference_arm_greedy_and_tree_modes():
         assert r.returncode == 0, r.stderr
         d = json.loads(r.stdout.strip().splitlines()[-1])
         assert d["value"] > 0 and d["config"]["mode"] in ("greedy", "tree")
+
+
+def test_profiled_traffic_follows_its_kernel_sources(tmp_path, monkeypatch):
+    """A profile's DRAM bytes are reported only while the sources of the
+    kernel it was taken on are unchanged (each profiled kernel has its own
+    source list); the committed profiles name kernels the bench knows."""
+    for (workload, mode), (name, kind) in bench.PROFILE_NAMES.items():
+        assert kind in bench.KERNEL_SOURCES
+        assert os.path.exists(os.path.join(ROOT, "profiles", name + ".md")), name
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    for kind, files in bench.KERNEL_SOURCES.items():
+        for rel in files:
+            src = tmp_path / rel
+            src.parent.mkdir(parents=True, exist_ok=True)
+            src.write_text("// %s\n" % rel)
+    h = bench.kernel_source_hash("filter")
+    assert h != bench.kernel_source_hash("stream")
+    (prof / "p.md").write_text("kernel_source_hash: %s\ndram_bytes_per_launch: 1234\n" % h)
+    assert bench.profiled_traffic(("p", "filter")) == 1234
+    assert bench.profiled_traffic(("p", "stream")) is None  # another kernel's sources
+    (tmp_path / bench.KERNEL_SOURCES["filter"][0]).write_text("// changed\n")
+    assert bench.profiled_traffic(("p", "filter")) is None  # the kernel changed since
+    assert bench.profiled_traffic(None) is None
