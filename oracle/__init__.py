@@ -32,6 +32,7 @@ _lib = None
 BAD_TOKEN = 1
 BAD_LOGITS = 2
 BAD_DRAFT_LEN = 4
+BAD_TREE = 16
 FLAG_ACCEPT = 1
 FLAG_CDF = 2
 FLAG_CUT = 4
@@ -74,16 +75,20 @@ def configure(lib):
     lib.sv_oracle_greedy.argtypes = [P, I, P, P, I, I, I, I, I, P, P, P, P]
     lib.sv_oracle_greedy.restype = I
     lib.sv_oracle_sample.argtypes = [P, P, I, P, P, P, D, I, I, I, I, I, P, P, P, P, P, P, P, P,
-                                     P, I, D]
+                                     P, I, D, P, P, P]
     lib.sv_oracle_sample.restype = I
-    lib.sv_oracle_tree.argtypes = [P, I, P, P, I, I, I, I, I, I, P, P, P, P]
+    lib.sv_oracle_tree.argtypes = [P, I, P, I, P, I, I, I, I, I, I, P, P, P, P]
     lib.sv_oracle_tree.restype = I
     lib.sv_oracle_compact.argtypes = [P, P, I, I, P, P, P]
     lib.sv_oracle_compact.restype = None
-    lib.sv_oracle_typical.argtypes = [P, I, P, P, P, D, D, D, I, I, I, I, I, P, P, P, P, P]
+    lib.sv_oracle_typical.argtypes = [P, I, P, P, P, D, D, D, I, I, I, I, I, P, P, P, P, P, P, P,
+                                      P, P]
     lib.sv_oracle_typical.restype = I
-    lib.sv_oracle_tree_typical.argtypes = [P, I, P, P, P, D, D, D, I, I, I, I, I, I, P, P, P, P,
-                                           P]
+    lib.sv_oracle_tree_typical.argtypes = [P, I, P, I, P, P, D, D, D, I, I, I, I, I, I, P, P, P,
+                                           P, P, P, P, P, P, P]
+    lib.sv_oracle_tree_sample.argtypes = [P, I, P, I, P, P, D, I, I, I, I, I, I, P, P, P, P, P,
+                                          P, P, P, P, P, P]
+    lib.sv_oracle_tree_sample.restype = I
     lib.sv_oracle_tree_typical.restype = I
     lib.sv_oracle_ngram.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
     lib.sv_oracle_ngram.restype = I
@@ -161,7 +166,8 @@ def inverse_cdf(weights, u):
 # ---------------------------------------------------------------------------
 
 def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=None,
-           threads=1, b_range=None, probe_tokens=None, token_mask=None, top_k=0, top_p=1.0):
+           threads=1, b_range=None, probe_tokens=None, token_mask=None, top_k=0, top_p=1.0,
+           flip=None, cut_logits=None):
     """Rejection-sampling verify (temperature 0 = greedy rule).
 
     target [B, K+1, V], draft [B, K, V] or None (one-hot drafts),
@@ -172,6 +178,13 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
     top_k (0 = off) and top_p (1.0 = off) filter every sampled distribution,
     target and dense draft alike; flags gain FLAG_CUT where a top-p cut is
     within FLAG_TOL of moving.
+    flip [B, K] (bool / uint8) or None: invert the outcome of the marked
+    acceptance tests (to follow the other branch of a flagged test).
+    cut_logits [B, R] or None (R = K+1, plus K with draft logits: target rows
+    then draft rows; NaN = the rule's own cut): forced top-p cuts; the result
+    gains cut_margin [B, R] (0 = the rule's own cut, d > 0 = a different cut
+    at distance d <= FLAG_TOL from the rule, NaN = not admissible, -1 = row
+    not reached).
     Returns a dict of numpy arrays: tokens, accept_len, accept_prob, flags,
     margins, status (and probe [B, 2] when probe_tokens [B] is given: the
     normalised CDF step of that token in the request's final draw).
@@ -194,6 +207,12 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
     if probe_tokens is not None:
         probes = np.ascontiguousarray(probe_tokens, dtype=np.int32).reshape(B)
         out["probe"] = np.full((B, 2), np.nan)
+    fl = None if flip is None else np.ascontiguousarray(flip, dtype=np.uint8).reshape(B, K)
+    cuts = None
+    if cut_logits is not None:
+        R = K + 1 + (K if draft is not None else 0)
+        cuts = np.ascontiguousarray(cut_logits, dtype=np.float64).reshape(B, R)
+        out["cut_margin"] = np.full((B, R), -1.0)
     lib = _load()
 
     def fn(lo, hi):
@@ -202,7 +221,7 @@ def sample(target, draft, draft_tokens, uniforms, temperature, *, draft_lens=Non
             float(temperature), B, K, V, lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
             _ptr(out["accept_prob"]), _ptr(out["flags"]), _ptr(out["margins"]),
             _ptr(out["status"]), _ptr(probes), _ptr(out.get("probe")), _ptr(mask), int(top_k),
-            float(top_p))
+            float(top_p), _ptr(fl), _ptr(cuts), _ptr(out.get("cut_margin")))
 
     _run(fn, B, threads, b_range)
     return out
@@ -230,12 +249,23 @@ def greedy(target, draft_tokens, *, draft_lens=None, threads=1, b_range=None, to
     return out
 
 
+def _parents(parent, B, N):
+    """A shared parent array [N] (stride 0) or one per request [B, N] (stride N)."""
+    par = np.ascontiguousarray(parent, dtype=np.int32)
+    if par.shape == (N,):
+        return par, 0
+    if par.shape == (B, N):
+        return par, N
+    raise ValueError("parent must be [N] or [B, N] (N = %d, B = %d), got %s" % (N, B, par.shape))
+
+
 def tree(target, parent, node_tokens, max_depth, *, threads=1, b_range=None):
-    """Greedy tree verify: tokens / path [B, max_depth+1], accept_len, status."""
+    """Greedy tree verify: tokens / path [B, max_depth+1], accept_len, status.
+    parent: [N] shared by every request, or [B, N] (one tree per request)."""
     target, dt = _logits(target)
     B, N1, V = target.shape
     N = N1 - 1
-    par = np.ascontiguousarray(parent, dtype=np.int32).reshape(N)
+    par, stride = _parents(parent, B, N)
     nt = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
     W = max_depth + 1
     out = dict(tokens=np.full((B, W), -1, np.int32), accept_len=np.zeros(B, np.int32),
@@ -243,20 +273,62 @@ def tree(target, parent, node_tokens, max_depth, *, threads=1, b_range=None):
     lib = _load()
 
     def fn(lo, hi):
-        return lib.sv_oracle_tree(_ptr(target), dt, _ptr(par), _ptr(nt), B, N, V, int(max_depth),
-                                  lo, hi, _ptr(out["tokens"]), _ptr(out["accept_len"]),
-                                  _ptr(out["path"]), _ptr(out["status"]))
+        return lib.sv_oracle_tree(_ptr(target), dt, _ptr(par), stride, _ptr(nt), B, N, V,
+                                  int(max_depth), lo, hi, _ptr(out["tokens"]),
+                                  _ptr(out["accept_len"]), _ptr(out["path"]), _ptr(out["status"]))
+
+    _run(fn, B, threads, b_range)
+    return out
+
+
+def tree_sample(target, parent, node_tokens, uniforms, temperature, max_depth, *, threads=1,
+                b_range=None, flip=None, probe_tokens=None):
+    """Lossless tree verification by rejection sampling over deterministic
+    candidates.  parent [N] or [B, N]; uniforms [B, N+1] (column n drives the
+    test of node n, column 0 the final draw).  Returns tokens / path
+    [B, max_depth+1], accept_len, accept_prob [B, N+1] (theta of each tested
+    node, -1 elsewhere), node_flags [B, N+1] (FLAG_ACCEPT per flagged test),
+    flags [B] (FLAG_CDF for the draw), margins [B], status (and probe [B, 2]
+    with probe_tokens [B]).  flip [B, N+1] inverts the marked node tests."""
+    target, dt = _logits(target)
+    B, N1, V = target.shape
+    N = N1 - 1
+    par, stride = _parents(parent, B, N)
+    nt = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
+    u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B, N + 1)
+    fl = None if flip is None else np.ascontiguousarray(flip, dtype=np.uint8).reshape(B, N + 1)
+    W = max_depth + 1
+    out = dict(tokens=np.full((B, W), -1, np.int32), accept_len=np.zeros(B, np.int32),
+               path=np.full((B, W), -1, np.int32), accept_prob=np.full((B, N + 1), -1.0),
+               node_flags=np.zeros((B, N + 1), np.int32), flags=np.zeros(B, np.int32),
+               margins=np.full(B, np.inf), status=np.zeros(B, np.int32))
+    probes = None
+    if probe_tokens is not None:
+        probes = np.ascontiguousarray(probe_tokens, dtype=np.int32).reshape(B)
+        out["probe"] = np.full((B, 2), np.nan)
+    lib = _load()
+
+    def fn(lo, hi):
+        return lib.sv_oracle_tree_sample(
+            _ptr(target), dt, _ptr(par), stride, _ptr(nt), _ptr(u), float(temperature), B, N, V,
+            int(max_depth), lo, hi, _ptr(fl), _ptr(out["tokens"]), _ptr(out["accept_len"]),
+            _ptr(out["path"]), _ptr(out["accept_prob"]), _ptr(out["node_flags"]),
+            _ptr(out["flags"]), _ptr(out["margins"]), _ptr(out["status"]), _ptr(probes),
+            _ptr(out.get("probe")))
 
     _run(fn, B, threads, b_range)
     return out
 
 
 def typical(target, draft_tokens, uniforms, temperature, eps, delta, *, draft_lens=None,
-            threads=1, b_range=None):
+            threads=1, b_range=None, flip=None, probe_tokens=None):
     """Typical acceptance: accept x_i while p_i(x_i) > min(eps, delta *
     exp(-H(p_i))); the emitted token at the first failure (or the bonus
     position) is drawn from p_n with uniforms[:, K].  Returns tokens,
-    accept_len, accept_prob (p_i(x_i) at tested positions), flags, status."""
+    accept_len, accept_prob (p_i(x_i) at tested positions), flags, margins
+    [B] (the draw's distance to its CDF step's nearer edge), status (and
+    probe [B, 2] with probe_tokens [B]).  flip [B, K] inverts the marked
+    tests."""
     target, dt = _logits(target)
     B, K1, V = target.shape
     K = K1 - 1
@@ -265,7 +337,12 @@ def typical(target, draft_tokens, uniforms, temperature, eps, delta, *, draft_le
     lens = None if draft_lens is None else np.ascontiguousarray(draft_lens, dtype=np.int32)
     out = dict(tokens=np.full((B, K + 1), -1, np.int32), accept_len=np.zeros(B, np.int32),
                accept_prob=np.full((B, K), -1.0), flags=np.zeros((B, K + 1), np.int32),
-               status=np.zeros(B, np.int32))
+               margins=np.full(B, np.inf), status=np.zeros(B, np.int32))
+    fl = None if flip is None else np.ascontiguousarray(flip, dtype=np.uint8).reshape(B, K)
+    probes = None
+    if probe_tokens is not None:
+        probes = np.ascontiguousarray(probe_tokens, dtype=np.int32).reshape(B)
+        out["probe"] = np.full((B, 2), np.nan)
     lib = _load()
 
     def fn(lo, hi):
@@ -273,34 +350,46 @@ def typical(target, draft_tokens, uniforms, temperature, eps, delta, *, draft_le
                                      float(temperature), float(eps), float(delta), B, K, V, lo, hi,
                                      _ptr(out["tokens"]), _ptr(out["accept_len"]),
                                      _ptr(out["accept_prob"]), _ptr(out["flags"]),
-                                     _ptr(out["status"]))
+                                     _ptr(out["status"]), _ptr(fl), _ptr(out["margins"]),
+                                     _ptr(probes), _ptr(out.get("probe")))
 
     _run(fn, B, threads, b_range)
     return out
 
 
 def tree_typical(target, parent, node_tokens, uniforms, temperature, eps, delta, max_depth, *,
-                 threads=1, b_range=None):
+                 threads=1, b_range=None, flip=None, probe_tokens=None):
     """Typical acceptance over a candidate tree: tokens / path [B, max_depth+1],
-    accept_len, flags [B], status.  uniforms [B] drive the final draw."""
+    accept_len, flags [B], node_flags [B, N+1] (FLAG_ACCEPT per flagged node
+    test), margins [B], status (and probe [B, 2] with probe_tokens [B]).
+    parent [N] or [B, N]; uniforms [B] drive the final draw; flip [B, N+1]
+    inverts the marked node tests."""
     target, dt = _logits(target)
     B, N1, V = target.shape
     N = N1 - 1
-    par = np.ascontiguousarray(parent, dtype=np.int32).reshape(N)
+    par, stride = _parents(parent, B, N)
     nt = np.ascontiguousarray(node_tokens, dtype=np.int32).reshape(B, N)
     u = np.ascontiguousarray(uniforms, dtype=np.float64).reshape(B)
+    fl = None if flip is None else np.ascontiguousarray(flip, dtype=np.uint8).reshape(B, N + 1)
     W = max_depth + 1
     out = dict(tokens=np.full((B, W), -1, np.int32), accept_len=np.zeros(B, np.int32),
                path=np.full((B, W), -1, np.int32), flags=np.zeros(B, np.int32),
+               node_flags=np.zeros((B, N + 1), np.int32), margins=np.full(B, np.inf),
                status=np.zeros(B, np.int32))
+    probes = None
+    if probe_tokens is not None:
+        probes = np.ascontiguousarray(probe_tokens, dtype=np.int32).reshape(B)
+        out["probe"] = np.full((B, 2), np.nan)
     lib = _load()
 
     def fn(lo, hi):
-        return lib.sv_oracle_tree_typical(_ptr(target), dt, _ptr(par), _ptr(nt), _ptr(u),
+        return lib.sv_oracle_tree_typical(_ptr(target), dt, _ptr(par), stride, _ptr(nt), _ptr(u),
                                           float(temperature), float(eps), float(delta), B, N, V,
                                           int(max_depth), lo, hi, _ptr(out["tokens"]),
                                           _ptr(out["accept_len"]), _ptr(out["path"]),
-                                          _ptr(out["flags"]), _ptr(out["status"]))
+                                          _ptr(out["flags"]), _ptr(out["status"]), _ptr(fl),
+                                          _ptr(out["node_flags"]), _ptr(out["margins"]),
+                                          _ptr(probes), _ptr(out.get("probe")))
 
     _run(fn, B, threads, b_range)
     return out

@@ -629,6 +629,67 @@ def check_filter_matches_numpy(seed=18):
     assert (one["tokens"][ok, 1] == np.argmax(l[ok, 1], axis=1)).all()
 
 
+def check_forced_cut(seed=27):
+    """The checking hook for cuts made elsewhere: forcing the rule's own cut
+    changes nothing (margin 0); forcing the class above it (one class fewer)
+    when top_p lies 3e-6 above the mass in front of the rule's cut class
+    reports margin 3e-6 and renormalises p over the classes kept, as the
+    numpy filter computes them; a value that is no class of the row, a cut
+    below the top-k cut, another cut than the k-th largest for top-k alone,
+    or a cut further than 1e-5 from the rule is not admissible (NaN)."""
+    rng = np.random.default_rng(seed)
+    B, V, T = 120, 40, 0.9
+    l = (np.round(rng.standard_normal((B, 2, V)) * 4) / 2).astype(np.float32)
+    x = rng.integers(0, V, size=(B, 1)).astype(np.int32)
+    u = np.full((B, 2), 0.5, np.float32)
+    nan = np.full((B, 2), np.nan)
+    seen = 0
+    for b in range(B):
+        row = l[b, 0].astype(np.float64)
+        p = scipy.special.softmax(row / T)
+        vals = np.unique(row)[::-1]
+        mass = np.array([p[row == v].sum() for v in vals])
+        front = np.concatenate([[0.0], np.cumsum(mass)[:-1]])
+        j = int(rng.integers(2, min(6, vals.size - 1)))
+        top_p = float(front[j] + 3e-6)  # keeps classes 0..j
+        if not (mass[j] > 2e-5 and mass[j - 1] > 2e-5):
+            continue
+        seen += 1
+
+        def forced(c):
+            cuts = nan[b:b + 1].copy()
+            cuts[0, 0] = c
+            return oracle.sample(l[b:b + 1], None, x[b:b + 1], u[b:b + 1], T, top_p=top_p,
+                                 cut_logits=cuts)
+
+        plain = oracle.sample(l[b:b + 1], None, x[b:b + 1], u[b:b + 1], T, top_p=top_p)
+        own = forced(vals[j])
+        assert own["cut_margin"][0, 0] == 0.0
+        assert own["accept_prob"][0, 0] == plain["accept_prob"][0, 0]
+        assert (own["tokens"] == plain["tokens"]).all()
+        fewer = forced(vals[j - 1])
+        assert abs(fewer["cut_margin"][0, 0] - 3e-6) < 1e-12, fewer["cut_margin"]
+        kept = np.where(row >= vals[j - 1], p, 0.0)
+        kept /= kept.sum()
+        assert abs(fewer["accept_prob"][0, 0] - min(1.0, kept[x[b, 0]])) < 1e-12
+        assert np.isnan(forced(vals[j - 2])["cut_margin"][0, 0])  # two classes fewer: too far
+        assert np.isnan(forced(vals[j + 1])["cut_margin"][0, 0])  # one class more: too far
+        assert np.isnan(forced(vals[j] + 0.25)["cut_margin"][0, 0])  # no such class
+    assert seen > 20, seen
+    # with top-k: a cut below the k-th largest value is not admissible; for
+    # top-k alone only the k-th largest value itself is
+    row = l[0, 0]
+    vk = np.sort(row)[::-1][4]
+    below = np.unique(row[row < vk])
+    for top_p, c, ok in ((0.99, below.max() if below.size else vk - 1, False),
+                         (1.0, vk, True), (1.0, np.unique(row[row > vk]).min(), False)):
+        cuts = nan[:1].copy()
+        cuts[0, 0] = c
+        out = oracle.sample(l[:1], None, x[:1], u[:1], T, top_k=5, top_p=top_p, cut_logits=cuts)
+        assert (out["cut_margin"][0, 0] == 0.0) if ok else np.isnan(out["cut_margin"][0, 0]), \
+            (top_p, c, out["cut_margin"])
+
+
 def check_exact_filtered(V=6, K=2, T=0.8, seed=19):
     """Exactness with top-k / top-p: with x_i drawn from the filtered draft
     distribution, the emitted token at every position follows the filtered
@@ -902,23 +963,317 @@ def check_tree_brute_force(seed=14):
 
 
 def check_tree_errors():
+    """Bad tokens and parent arrays that are not trees (a parent that is not
+    an earlier node, or deeper than max_depth) are per-request statuses, in
+    the greedy, typical and sampling tree walks alike; the other requests of
+    the call are unaffected."""
     parent = np.array([0, 0, 1], np.int32)
     l = np.zeros((2, 4, 3), np.float32)
     toks = np.array([[0, 1, 2], [0, 3, 2]], np.int32)
-    out = oracle.tree(l, parent, toks, 2)
-    assert list(out["status"]) == [0, oracle.BAD_TOKEN]
-    try:
-        oracle.tree(l, np.array([0, 2, 1], np.int32), toks, 2)
-    except ValueError:
-        pass
-    else:
-        raise AssertionError("a parent that is not an earlier node must be rejected")
-    try:
-        oracle.tree(l, parent, toks, 1)
-    except ValueError:
-        pass
-    else:
-        raise AssertionError("a tree deeper than max_depth must be rejected")
+    u = np.full((2, 4), 0.5)
+    walks = [
+        lambda par, D: oracle.tree(l, par, toks, D),
+        lambda par, D: oracle.tree_typical(l, par, toks, u[:, 0], 1.0, 0.09, 0.3, D),
+        lambda par, D: oracle.tree_sample(l, par, toks, u, 1.0, D),
+    ]
+    for walk in walks:
+        out = walk(parent, 2)
+        assert list(out["status"]) == [0, oracle.BAD_TOKEN]
+        for bad in (np.array([0, 2, 1], np.int32), np.array([1, 0, 1], np.int32),
+                    np.array([0, 0, -1], np.int32)):
+            out = walk(bad, 2)
+            assert out["status"][0] == oracle.BAD_TREE, bad
+            assert out["accept_len"][0] == 0 and (out["tokens"][0] == -1).all()
+        out = walk(parent, 1)  # depth 2 > max_depth 1
+        assert out["status"][0] == oracle.BAD_TREE
+        # one tree per request: request 0 valid, request 1 not a tree
+        per = np.stack([parent, np.array([0, 3, 1], np.int32)])
+        out = walk(per, 2)
+        assert out["status"][0] == 0 and out["status"][1] == oracle.BAD_TREE
+
+
+def check_per_request_trees(seed=23):
+    """A [B, N] parent array (one tree per request) gives each request the
+    result of a call with its own tree alone, for all three tree walks."""
+    rng = np.random.default_rng(seed)
+    B, N, V = 6, 9, 7
+    parents = np.stack([_random_tree(rng, N) for _ in range(B)])
+    D = N
+    l = (rng.standard_normal((B, N + 1, V)) * 1.3).astype(np.float32)
+    toks = rng.integers(0, V, size=(B, N)).astype(np.int32)
+    for b in range(B):  # make some greedy walks go deep
+        for n in range(1, N + 1):
+            if rng.random() < 0.6:
+                toks[b, n - 1] = int(np.argmax(l[b, parents[b, n - 1]]))
+    u = rng.random((B, N + 1))
+    both = [(lambda par, sl: oracle.tree(l[sl], par, toks[sl], D)),
+            (lambda par, sl: oracle.tree_typical(l[sl], par, toks[sl], u[sl, 0], 1.0, 0.1, 0.4, D)),
+            (lambda par, sl: oracle.tree_sample(l[sl], par, toks[sl], u[sl], 0.9, D))]
+    for walk in both:
+        full = walk(parents, slice(0, B))
+        for b in range(B):
+            one = walk(parents[b], slice(b, b + 1))
+            for k in ("tokens", "path", "accept_len", "status"):
+                assert (np.asarray(full[k][b]) == np.asarray(one[k][0])).all(), (b, k)
+
+
+# ---------------------------------------------------------------------------
+# lossless tree verification by rejection sampling
+# ---------------------------------------------------------------------------
+
+def _log_rows(rows):
+    with np.errstate(divide="ignore"):
+        return np.log(np.asarray(rows, np.float64)).astype(np.float32)
+
+
+def check_golden_tree_sample():
+    g = _golden("tree_sample_v4.json")
+    l = _log_rows(g["rows"])[None]
+    toks = np.asarray([g["node_tokens"]], np.int32)
+    for case in g["cases"]:
+        out = oracle.tree_sample(l, g["parent"], toks, np.asarray([case["uniforms"]]), g["T"],
+                                 g["max_depth"])
+        assert out["status"][0] == 0
+        assert list(out["tokens"][0]) == case["tokens"], (case, out["tokens"][0])
+        assert list(out["path"][0]) == case["path"], (case, out["path"][0])
+        assert out["accept_len"][0] == case["accept_len"]
+        np.testing.assert_allclose(out["accept_prob"][0], case["accept_prob"], atol=1e-6)
+
+
+class _TreeRequest:
+    """One tree request evaluated by the oracle for chosen uniforms."""
+
+    def __init__(self, logits, parent, node_tokens, T):
+        self.l = np.ascontiguousarray(logits[None], np.float32)
+        self.parent = np.asarray(parent, np.int32)
+        self.toks = np.asarray([node_tokens], np.int32)
+        self.N = len(parent)
+        self.T = T
+        depth = [0]
+        for pa in parent:
+            depth.append(depth[pa] + 1)
+        self.depth = depth
+
+    def run(self, u):
+        out = oracle.tree_sample(self.l, self.parent, self.toks, np.asarray([u]), self.T,
+                                 max(self.depth))
+        assert out["status"][0] == 0
+        return out["path"][0], out["tokens"][0]
+
+
+def _tree_emission_law(req, v):
+    """Exact law of the token emitted after node v, the walk having reached
+    v (uniform 0 for the tests on v's root path, the earlier siblings on that
+    path rejected), by bisection over the uniforms of v's children in id
+    order and then over the final draw's uniform.  None if v cannot be
+    reached that way."""
+    N, V = req.N, req.l.shape[2]
+    chain, n = [], v
+    while n:
+        chain.append(n)
+        n = int(req.parent[n - 1])
+    u = [0.5] * (N + 1)
+    for n in chain:  # accept the path, reject the earlier siblings
+        u[n] = 0.0
+        for c in range(1, n):
+            if req.parent[c - 1] == req.parent[n - 1]:
+                u[c] = _ONE_MINUS
+    d = req.depth[v]
+    path, _ = req.run(u)
+    if path[d] != v:
+        return None
+    law, reach = np.zeros(V), 1.0
+    children = [c for c in range(1, N + 1) if req.parent[c - 1] == v]
+    for c in children:
+        u[c] = 0.5
+
+        def accepted(a, c=c):
+            uu = list(u)
+            uu[c] = a
+            pth, _ = req.run(uu)
+            return d + 1 < len(pth) and pth[d + 1] == c
+
+        theta = _bisect(accepted)
+        law[req.toks[0, c - 1]] += reach * theta
+        reach *= 1.0 - theta
+        u[c] = _ONE_MINUS
+        if theta >= 1.0 or reach == 0.0:
+            return law
+
+    def token(s):
+        uu = list(u)
+        uu[0] = s
+        pth, tk = req.run(uu)
+        assert len(pth) <= d + 1 or pth[d + 1] < 0, "a rejected child was accepted"
+        return int(tk[d])
+
+    prev = 0.0
+    for t in range(V):
+        edge = 1.0 if t == V - 1 else _bisect(lambda s: token(s) <= t)
+        law[t] += reach * (edge - prev)
+        prev = edge
+    return law
+
+
+def check_exact_tree_sample(seed=24):
+    """Exactness over a candidate tree: whatever node the walk stands on, the
+    token emitted after it is distributed as that node's tempered target
+    distribution, to 1e-12 - with repeated sibling tokens, tokens of zero
+    probability, leaves and a node with a child for every token."""
+    rng = np.random.default_rng(seed)
+    cases = []
+    for trial in range(4):
+        N = int(rng.integers(3, 8))
+        parent = list(_random_tree(rng, N))
+        cases.append((parent, int(rng.integers(3, 6))))
+    cases.append(([0, 0, 0, 0, 1, 1], 4))  # the root has a child for every token
+    for ci, (parent, V) in enumerate(cases):
+        N = len(parent)
+        T = float(rng.choice([0.7, 1.0, 1.6]))
+        l = (rng.standard_normal((N + 1, V)) * 1.2).astype(np.float32)
+        toks = rng.integers(0, V, size=N).astype(np.int32)
+        if ci == 4:
+            toks[:4] = [2, 0, 3, 1]
+        if ci == 1:
+            toks[-1] = toks[0] if parent[-1] == parent[0] else toks[-1]
+            l[0, 1] = -np.inf  # a zero-probability token at the root
+        req = _TreeRequest(l, parent, toks, T)
+        p = scipy.special.softmax(l.astype(np.float64) / T, axis=-1)
+        checked = 0
+        for v in range(N + 1):
+            law = _tree_emission_law(req, v)
+            if law is None:
+                continue
+            checked += 1
+            np.testing.assert_allclose(law, p[v], rtol=0, atol=1e-12,
+                                       err_msg="tree %s node %d" % (parent, v))
+        assert checked >= 2, (parent, checked)
+
+
+def check_tree_sample_chain_is_onehot_verify(seed=25):
+    """A chain-shaped tree (node n's parent is n-1) is one-hot rejection
+    sampling over K = N positions: the same tokens and acceptance
+    probabilities as the chain verification with the uniforms remapped
+    (node n's test uses chain column n-1, the final draw column K)."""
+    rng = np.random.default_rng(seed)
+    B, N, V, T = 200, 4, 50, 0.8
+    l = (rng.standard_normal((B, N + 1, V)) * 2.0).astype(np.float32)
+    x = np.where(rng.random((B, N)) < 0.5, np.argmax(l[:, :N], axis=2),
+                 rng.integers(0, V, size=(B, N))).astype(np.int32)
+    u = rng.random((B, N + 1))
+    chain = oracle.sample(l, None, x, np.concatenate([u[:, 1:], u[:, :1]], axis=1), T)
+    tree = oracle.tree_sample(l, np.arange(N, dtype=np.int32), x, u, T, N)
+    assert (tree["tokens"] == chain["tokens"]).all()
+    assert (tree["accept_len"] == chain["accept_len"]).all()
+    for b in range(B):
+        L = int(chain["accept_len"][b])
+        tested = min(L, N)
+        np.testing.assert_allclose(tree["accept_prob"][b, 1:tested + 1],
+                                   chain["accept_prob"][b, :tested], rtol=0, atol=1e-14)
+        assert list(tree["path"][b, :L]) == list(range(L))
+
+
+def check_flips_invert_tests(seed=26):
+    """The checking hook: flipping a test the request reaches inverts its
+    outcome (and nothing before it); flipping a test it never reaches
+    changes nothing.  Chains (rejection sampling and typical acceptance) and
+    trees (sampling and typical acceptance)."""
+    rng = np.random.default_rng(seed)
+    B, K, V, T = 64, 3, 30, 1.0
+    l = (rng.standard_normal((B, K + 1, V)) * 1.5).astype(np.float32)
+    d = (l[:, :K] + rng.standard_normal((B, K, V)) * 0.6).astype(np.float32)
+    x = np.argmax(d, axis=2).astype(np.int32)
+    u = rng.random((B, K + 1))
+    for run in (lambda f: oracle.sample(l, d, x, u, T, flip=f),
+                lambda f: oracle.sample(l, None, x, u, T, flip=f),
+                lambda f: oracle.typical(l, x, u, T, 0.09, 0.3, flip=f)):
+        base = run(None)
+        for i in range(K):
+            f = np.zeros((B, K), np.uint8)
+            f[:, i] = 1
+            out = run(f)
+            for b in range(B):
+                L0, L1 = int(base["accept_len"][b]), int(out["accept_len"][b])
+                if L0 < i + 1:  # test i not reached
+                    assert (out["tokens"][b] == base["tokens"][b]).all()
+                elif L0 > i + 1:  # accepted at i: now rejected there
+                    assert L1 == i + 1 and (out["tokens"][b, :i] == base["tokens"][b, :i]).all()
+                else:  # rejected at i: now accepted there
+                    assert L1 > i + 1 and (out["tokens"][b, :i + 1] == x[b, :i + 1]).all()
+    parent = np.array([0, 0, 1, 1, 2, 3], np.int32)
+    N = parent.size
+    lt = (rng.standard_normal((B, N + 1, V)) * 1.5).astype(np.float32)
+    toks = np.argsort(-lt[:, parent], axis=2)[:, np.arange(N), np.array([0, 1, 0, 1, 0, 0])]
+    toks = np.ascontiguousarray(toks, dtype=np.int32)
+    ut = rng.random((B, N + 1))
+    # trees: a flipped node on the walked path leaves it; for the sampling
+    # walk, a tested node off the path joins it and an untested one changes
+    # nothing
+    for run, sampling in ((lambda f: oracle.tree_sample(lt, parent, toks, ut, T, 3, flip=f), True),
+                          (lambda f: oracle.tree_typical(lt, parent, toks, ut[:, 0], T, 0.09, 0.3,
+                                                         3, flip=f), False)):
+        base = run(None)
+        moved = 0
+        for n in range(1, N + 1):
+            f = np.zeros((B, N + 1), np.uint8)
+            f[:, n] = 1
+            out = run(f)
+            for b in range(B):
+                on_path = n in list(base["path"][b])
+                if on_path:
+                    assert n not in list(out["path"][b]), (b, n)
+                    moved += 1
+                elif sampling and base["accept_prob"][b, n] >= 0:
+                    assert n in list(out["path"][b]), (b, n)
+                    moved += 1
+                elif sampling:
+                    assert (out["tokens"][b] == base["tokens"][b]).all()
+        assert moved > B, moved
+
+
+def check_probes(seed=28):
+    """The probe that checks a draw made elsewhere: for the emitted token the
+    reported CDF step contains the draw's uniform; for any token it is the
+    step of the draw's weights computed with numpy (one-hot residual p_n
+    without x_n, or the bonus p_K; typical acceptance: p_n; the tree
+    sampler: the residual at the final node)."""
+    rng = np.random.default_rng(seed)
+    B, K, V, T = 80, 2, 30, 1.1
+    l = (rng.standard_normal((B, K + 1, V)) * 1.5).astype(np.float32)
+    x = np.where(rng.random((B, K)) < 0.5, np.argmax(l[:, :K], axis=2),
+                 rng.integers(0, V, size=(B, K))).astype(np.int32)
+    u = rng.random((B, K + 1))
+    p = scipy.special.softmax(l.astype(np.float64) / T, axis=-1)
+
+    def step(w, t):
+        c = np.concatenate([[0.0], np.cumsum(w)]) / w.sum()
+        return c[t], c[t + 1]
+
+    for kind in ("sample", "typical"):
+        run = (lambda pt: oracle.sample(l, None, x, u, T, probe_tokens=pt)) if kind == "sample" \
+            else (lambda pt: oracle.typical(l, x, u, T, 0.09, 0.3, probe_tokens=pt))
+        base = run(None)
+        n = base["accept_len"] - 1
+        own = run(base["tokens"][np.arange(B), n])["probe"]
+        assert ((own[:, 0] <= u[:, K]) & (u[:, K] < own[:, 1])).all(), kind
+        other = rng.integers(0, V, size=B).astype(np.int32)
+        pr = run(other)["probe"]
+        for b in range(B):
+            w = p[b, n[b]].copy()
+            if kind == "sample" and n[b] < K:
+                w[x[b, n[b]]] = 0.0
+            lo, hi = step(w, other[b])
+            assert abs(pr[b, 0] - lo) < 1e-12 and abs(pr[b, 1] - hi) < 1e-12, (kind, b)
+    parent = np.array([0, 0, 1], np.int32)
+    lt = (rng.standard_normal((B, 4, V)) * 1.5).astype(np.float32)
+    toks = np.ascontiguousarray(np.argsort(-lt[:, parent], axis=2)[:, np.arange(3), [0, 1, 0]],
+                                dtype=np.int32)
+    ut = rng.random((B, 4))
+    base = oracle.tree_sample(lt, parent, toks, ut, T, 2)
+    L = base["accept_len"]
+    own = oracle.tree_sample(lt, parent, toks, ut, T, 2,
+                             probe_tokens=base["tokens"][np.arange(B), L - 1])["probe"]
+    assert ((own[:, 0] <= ut[:, 0]) & (ut[:, 0] < own[:, 1])).all()
 
 
 ALL_CHECKS = [
@@ -931,4 +1286,7 @@ ALL_CHECKS = [
     check_mask_layout, check_exact_masked, check_golden_ngram, check_ngram_matches_numpy,
     check_golden_topk_topp, check_filter_matches_numpy, check_exact_filtered,
     check_golden_typical, check_typical_matches_scipy, check_tree_typical_brute_force,
+    check_per_request_trees, check_golden_tree_sample, check_exact_tree_sample,
+    check_tree_sample_chain_is_onehot_verify, check_flips_invert_tests, check_forced_cut,
+    check_probes,
 ]

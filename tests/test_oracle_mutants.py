@@ -17,8 +17,8 @@ SRC = os.path.join(os.path.dirname(oracle.__file__), "spec_oracle.c")
 
 MUTANTS = [
     ("residual clamp dropped", "w[j] = r > 0 ? r : 0.0;", "w[j] = r;", 1),
-    ("non-strict acceptance", "if (!(u[i] * qx < p[x])) {", "if (!(u[i] * qx <= p[x])) {", 1),
-    ("ratio inverted", "if (!(u[i] * qx < p[x])) {", "if (!(u[i] * p[x] < qx)) {", 1),
+    ("non-strict acceptance", "int accept = u[i] * qx < p[x];", "int accept = u[i] * qx <= p[x];", 1),
+    ("ratio inverted", "int accept = u[i] * qx < p[x];", "int accept = u[i] * p[x] < qx;", 1),
     ("bonus from the previous row",
      "load_row(target, dtype, b * (size_t)(K + 1) + (size_t)K_b, V, lrow);",
      "load_row(target, dtype, b * (size_t)(K + 1) + (size_t)(K_b > 0 ? K_b - 1 : 0), V, lrow);", 1),
@@ -34,7 +34,7 @@ MUTANTS = [
      "sv_oracle_inverse_cdf(w, V, u[n], &margin);", 1),
     ("greedy emits the draft at a mismatch", "      n = i;\n      emitted = a;",
      "      n = i;\n      emitted = x;", 1),
-    ("tree ignores the parent link", "if (parent[c - 1] == node &&", "if (", 1),
+    ("tree ignores the parent link", "if (par[c - 1] == node &&", "if (", 1),
     ("packed offsets off by one", "cu[b + 1] = cu[b] + accept_len[b];",
      "cu[b + 1] = cu[b] + accept_len[b] + (b == 0);", 1),
     ("token bound off by one", "if (x < 0 || x >= V) return OR_BAD_TOKEN;",
@@ -67,15 +67,20 @@ MUTANTS = [
     ("top-k drops the class at the cut", "if (l[j] < vk) p[j] = 0.0;", "if (l[j] <= vk) p[j] = 0.0;", 1),
     ("top-p counts the class itself", "if (!dropping && above < top_p) {",
      "if (!dropping && above + mass < top_p) {", 1),
-    ("top-p on the unrenormalised top-k", "    for (int j = 0; j < V; ++j) p[j] /= Z;\n  }\n  int flag = 0;",
-     "  }\n  int flag = 0;", 1),
-    ("draft left unfiltered", "      flags[i] |= filter_top_k_top_p(lrow, q, V, top_k, top_p, order);\n", "", 1),
-    ("bonus row left unfiltered", "    flags[K_b] |= filter_top_k_top_p(lrow, p, V, top_k, top_p, order);\n",
-     "", 1),
+    ("top-p on the unrenormalised top-k",
+     "    for (int j = 0; j < V; ++j) p[j] /= Z;\n  }\n  if (!isnan(forced)) {",
+     "  }\n  if (!isnan(forced)) {", 1),
+    ("draft left unfiltered",
+     "      flags[i] |= filter_top_k_top_p(lrow, q, V, top_k, top_p, order,\n"
+     "                                     cut ? cut[K + 1 + i] : NAN,\n"
+     "                                     cut_margin ? &cut_margin[K + 1 + i] : NULL);\n", "", 1),
+    ("bonus row left unfiltered",
+     "    flags[K_b] |= filter_top_k_top_p(lrow, p, V, top_k, top_p, order, cut ? cut[K_b] : NAN,\n"
+     "                                     cut_margin ? &cut_margin[K_b] : NULL);\n", "", 1),
     ("typical entropy in bits", "if (p[j] > 0) H -= p[j] * log(p[j]);",
      "if (p[j] > 0) H -= p[j] * log2(p[j]);", 1),
     ("typical threshold takes the max", "return t < eps ? t : eps;", "return t > eps ? t : eps;", 1),
-    ("typical test not strict", "if (!(p[x] > thr)) {", "if (!(p[x] >= thr)) {", 1),
+    ("typical test not strict", "int pass = p[x] > thr;", "int pass = p[x] >= thr;", 1),
     ("typical draw from the bonus row", "load_row(target, dtype, (size_t)b * (size_t)(K + 1) + (size_t)n, V, l);",
      "load_row(target, dtype, (size_t)b * (size_t)(K + 1) + (size_t)K_b, V, l);", 1),
     ("typical tree keeps the highest id", "if (acc[n] && depth[n] > depth[best]) best = n;",
@@ -84,6 +89,36 @@ MUTANTS = [
      "double px = pp[(size_t)(acc[pa] ? pa : pa) * (size_t)V + (size_t)t] * (n % 2 ? 1.0 : 0.5);", 1),
     ("n-gram drafts start one late", "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t];",
      "drafts[(size_t)b * (size_t)K + (size_t)t] = c[found + n + t + 1 < len ? found + n + t + 1 : found + n + t];", 1),
+    # lossless tree verification by rejection sampling
+    ("tree sampler keeps a rejected token in the residual", "          w[x] = 0.0;",
+     "          w[x] = w[x];", 1),
+    ("tree sampler tests against p instead of the residual",
+     "double theta = W > 0 ? w[x] / W : 0.0;", "double theta = p[x];", 1),
+    ("tree sampler draws from p", "tokens[len++] = sv_oracle_inverse_cdf(w, V, u[0], &margin);",
+     "tokens[len++] = sv_oracle_inverse_cdf(p, V, u[0], &margin);", 1),
+    ("tree sampler draws with the node's uniform",
+     "tokens[len++] = sv_oracle_inverse_cdf(w, V, u[0], &margin);",
+     "tokens[len++] = sv_oracle_inverse_cdf(w, V, u[node], &margin);", 1),
+    ("tree sampler tests children in reverse order",
+     "for (int c = 1; c <= N && next < 0; ++c) {", "for (int c = N; c >= 1 && next < 0; --c) {", 1),
+    ("tree sampler test not strict", "int accept = u[c] < theta;", "int accept = u[c] <= theta;", 1),
+    ("tree depth limit off by one", "if (depth[n] > max_depth) return OR_BAD_TREE;",
+     "if (depth[n] >= max_depth + (n > 2)) return OR_BAD_TREE;", 1),
+    ("a node may be its own parent", "if (pa < 0 || pa >= n) return OR_BAD_TREE;",
+     "if (pa < 0 || pa > n) return OR_BAD_TREE;", 1),
+    ("per-request trees read the first tree",
+     "const int32_t* par = parent + (size_t)b * (size_t)parent_stride;",
+     "const int32_t* par = parent;", 3),
+    # checking hooks
+    ("forced cut distances swapped", "d = forced < own ? front - top_p : top_p - through;",
+     "d = forced < own ? top_p - through : front - top_p;", 1),
+    ("forced cut drops its own class", "        if (l[j] < forced) p[j] = 0.0;",
+     "        if (l[j] <= forced) p[j] = 0.0;", 1),
+    ("flip ignored (sampling)", "    if (flip && flip[i]) accept = !accept;\n", "", 1),
+    ("flip ignored (typical)",
+     "      if (flip && flip[(size_t)b * (size_t)K + (size_t)i]) pass = !pass;\n", "", 1),
+    ("flip ignored (typical tree)", "          if (fl && fl[n]) acc[n] = !acc[n];\n", "", 1),
+    ("probe step off by one", "    if (j < t) below += w[j];", "    if (j <= t) below += w[j];", 1),
 ]
 
 FAST_CHECKS = [c for c in oc.ALL_CHECKS] + [
