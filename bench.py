@@ -204,6 +204,9 @@ def oracle_run(wl, mode, requests, threads):
                        wl.delta, threads=threads)
     elif mode == "tree":
         oracle.tree(wl.target[sub], wl.parent, wl.node_tokens[sub], wl.max_depth, threads=threads)
+    elif mode == "tree_sample":
+        oracle.tree_sample(wl.target[sub], wl.parent, wl.node_tokens[sub], wl.uniforms[sub], wl.T,
+                           wl.max_depth, threads=threads)
     elif mode == "greedy":
         oracle.greedy(wl.target[sub], wl.draft_tokens[sub], threads=threads,
                       token_mask=None if wl.token_mask is None else wl.token_mask[sub])
@@ -234,8 +237,10 @@ def load_workload(args, seed=0):
     from token_verification_gb300 import synth
     wl = synth.make_workload(args.workload, seed=seed)
     typical = wl.meta.get("typical", False)
+    tree_kind = "tree_typical" if typical else (
+        "tree_sample" if (wl.uniforms is not None and wl.uniforms.ndim == 2) else "tree")
     mode = ("propose" if wl.history is not None
-            else ("tree_typical" if typical else "tree") if wl.parent is not None
+            else tree_kind if wl.parent is not None
             else "greedy" if args.greedy else "typical" if typical else "sample")
     if args.batch:  # a smaller batch of the same workload (profiling captures)
         wl.B = args.batch
@@ -296,10 +301,12 @@ def workload_config(wl, mode):
                    l2="inputs smaller than L2 (%d KB of contexts per call): 2 rotating input "
                       "sets; the figure includes L2 reuse" % (wl.history.nbytes // 1024))
         return cfg
-    if mode in ("tree", "tree_typical"):
+    if mode in ("tree", "tree_typical", "tree_sample"):
         cfg.update(N=int(wl.parent.size), max_depth=wl.max_depth)
         if mode == "tree_typical":
             cfg.update(temperature=wl.T, eps=wl.eps, delta=wl.delta)
+        if mode == "tree_sample":
+            cfg.update(temperature=wl.T)
     else:
         cfg.update(K=wl.K, drafts=wl.meta.get("drafts"), temperature=0.0 if mode == "greedy" else wl.T)
         if wl.token_mask is not None:
@@ -332,9 +339,10 @@ class Case:
             "history_lens": torch.from_numpy(wl.history_lens)}
         if mode == "propose":
             pass
-        elif mode in ("tree", "tree_typical"):
+        elif mode in ("tree", "tree_typical", "tree_sample"):
             self.host["node_tokens"] = torch.from_numpy(wl.node_tokens)
-            if mode == "tree_typical":
+            self.host["parent"] = torch.from_numpy(np.ascontiguousarray(wl.parent, np.int32))
+            if mode in ("tree_typical", "tree_sample"):
                 self.host["uniforms"] = torch.from_numpy(wl.uniforms)
         else:
             self.host["tokens"] = torch.from_numpy(wl.draft_tokens)
@@ -348,10 +356,11 @@ class Case:
         self.sets = []
         for s in range(2):
             perm = torch.from_numpy(np.roll(np.arange(B), s * (B // 2)))
-            self.sets.append({k: v[perm].contiguous().to(device) for k, v in self.host.items()})
+            self.sets.append({k: (v if k == "parent" else v[perm]).contiguous().to(device)
+                              for k, v in self.host.items()})
 
     def alloc(self, packed=True):
-        if self.mode in ("tree", "tree_typical", "propose"):
+        if self.mode in ("tree", "tree_typical", "tree_sample", "propose"):
             return None
         return self.api.alloc_outputs(self.wl.B, self.wl.K, self.device, packed=packed,
                                       accept_prob=packed and self.mode == "sample",
@@ -363,12 +372,17 @@ class Case:
             return api.spec_ngram_propose(inputs["history"], inputs["history_lens"], K=wl.K,
                                           n_min=wl.meta["n_min"], n_max=wl.meta["n_max"], out=out)
         if self.mode == "tree":
-            return api.spec_verify_tree(inputs["target"], wl.parent, inputs["node_tokens"],
+            return api.spec_verify_tree(inputs["target"], inputs["parent"], inputs["node_tokens"],
                                         wl.max_depth, out, path=False, status=False)
         if self.mode == "tree_typical":
-            return api.spec_verify_tree_typical(inputs["target"], wl.parent, inputs["node_tokens"],
-                                                inputs["uniforms"], wl.T, wl.eps, wl.delta,
-                                                wl.max_depth, out, path=False, status=False)
+            return api.spec_verify_tree_typical(inputs["target"], inputs["parent"],
+                                                inputs["node_tokens"], inputs["uniforms"], wl.T,
+                                                wl.eps, wl.delta, wl.max_depth, out, path=False,
+                                                status=False)
+        if self.mode == "tree_sample":
+            return api.spec_verify_tree_sample(inputs["target"], inputs["parent"],
+                                               inputs["node_tokens"], inputs["uniforms"], wl.T,
+                                               wl.max_depth, out, path=False, status=False)
         if self.mode == "typical":
             return api.spec_verify_typical(inputs["target"], inputs["tokens"], inputs["uniforms"],
                                            wl.T, wl.eps, wl.delta, out)
@@ -402,6 +416,8 @@ class Case:
             return "tree_kernel"
         if self.mode == "tree_typical":
             return "verify_stream_kernel + tree_typical_kernel"
+        if self.mode == "tree_sample":
+            return "verify_stream_kernel + tree_sample_kernel"
         if self.mode == "typical":
             return "verify_stream_kernel + finalize_kernel (typical)"
         masked = ", grammar-masked" if self.wl.token_mask is not None else ""
@@ -423,7 +439,7 @@ class Case:
         if self.mode == "tree":
             rows = int(out.accept_len.sum().item())
             return rows * wl.V * esz
-        if self.mode == "tree_typical":  # every candidate row once
+        if self.mode in ("tree_typical", "tree_sample"):  # every candidate row once
             return wl.B * (wl.parent.size + 1) * wl.V * esz
         rows = wl.B * (wl.K + 1) + (wl.B * wl.K if (self.mode == "sample" and wl.draft is not None)
                                      else 0)
@@ -566,7 +582,7 @@ def run_ours(args):
             "ms_per_step": 1e3 * max_elapsed / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": workload_config(wl, mode),
-            "draft_tokens_per_s": (None if mode in ("tree", "tree_typical", "propose")
+            "draft_tokens_per_s": (None if mode in ("tree", "tree_typical", "tree_sample", "propose")
                                    else value * wl.B * wl.K),
             "hbm_gbs": algo_bytes * value / 1e9,
             ("mean_draft_len" if mode == "propose" else "mean_accept_len"): mean_len,

@@ -19,8 +19,8 @@
  *
  * Conventions shared by every entry point
  *   - Tensor pointers are DEVICE pointers to caller-owned, contiguous,
- *     row-major memory, unless marked HOST.  The library never allocates,
- *     frees or retains them; it reads inputs and writes outputs on `stream`.
+ *     row-major memory.  The library never allocates, frees or retains them;
+ *     it reads inputs and writes outputs on `stream`.
  *   - Calls are asynchronous and stream-ordered: they return after queueing
  *     the kernels; nothing is synchronised.  `stream` is a cudaStream_t
  *     (NULL = the legacy default stream).
@@ -62,7 +62,7 @@ typedef enum sv_status {
   SV_ERR_SHAPE = 2,       /* B, K, V, N or max_depth outside the supported range */
   SV_ERR_DTYPE = 3,       /* unknown sv_dtype */
   SV_ERR_TEMPERATURE = 4, /* temperature negative, NaN or infinite */
-  SV_ERR_TREE = 5,        /* parent array: a parent not an earlier node, or depth > max_depth */
+  SV_ERR_TREE = 5,        /* tree parent stride neither 0 nor N */
   SV_ERR_WORKSPACE = 6,   /* workspace NULL, not 256-byte aligned, or too small */
   SV_ERR_CUDA = 7,        /* a CUDA runtime call or kernel launch failed */
   SV_ERR_FILTER = 8       /* top_k negative, top_p outside (0, 1], or eps / delta negative */
@@ -74,7 +74,9 @@ typedef enum sv_dtype { SV_F32 = 0, SV_BF16 = 1 } sv_dtype;
 #define SV_REQ_BAD_TOKEN 1     /* a draft / tree token outside [0, V) */
 #define SV_REQ_BAD_LOGITS 2    /* a needed row has NaN or +inf, or no finite logit */
 #define SV_REQ_BAD_DRAFT_LEN 4 /* draft_lens[b] outside [0, K] */
-#define SV_REQ_TIMEOUT 8       /* a bounded wait for staged logits gave up (device fault) */
+#define SV_REQ_TIMEOUT 8       /* a bounded wait for staged logits gave up (device fault, or
+                                  the limit of spec_verify_set_wait_limit_ns ran out) */
+#define SV_REQ_BAD_TREE 16     /* the request's parent array is not a tree of depth <= max_depth */
 
 /* Limits. */
 #define SV_MAX_K 31             /* draft positions per request */
@@ -205,8 +207,18 @@ sv_status spec_verify_greedy_masked(const void* target_logits, const int32_t* dr
  * NULL.  Each row of a filtered call is taken by one CTA: V * sizeof(logit)
  * must not exceed 512 KB (V <= 262144 for bf16, 131072 for fp32), else
  * SV_ERR_SHAPE.  SV_ERR_FILTER for a negative top_k or
- * top_p outside (0, 1].  All other arguments, results and the workspace size
- * are those of spec_verify_sample. */
+ * top_p outside (0, 1].
+ *   out_cut   [B, R] fp32 or NULL, R = K+1 (one-hot drafts) or 2K+1 (draft
+ *             logits): the lowest logit each filtered distribution keeps -
+ *             row i <= K target position i, row K+1+i the draft of position
+ *             i; NaN for rows the request does not need (beyond K_b, or a
+ *             request with a bad draft length); -inf for a row without a
+ *             finite max.  Written only when a filter is active (top_k in
+ *             (0, V) or top_p < 1).  With top-p the cut is where the fp32
+ *             mass of the leading value classes reaches top_p; it tells a
+ *             caller (or a test) which value classes were kept.
+ * All other arguments, results and the workspace size are those of
+ * spec_verify_sample. */
 sv_status spec_verify_sample_filtered(const void* target_logits, const void* draft_logits,
                                       const int32_t* draft_tokens, const float* uniforms,
                                       float temperature, int top_k, float top_p,
@@ -214,8 +226,9 @@ sv_status spec_verify_sample_filtered(const void* target_logits, const void* dra
                                       int32_t* out_accept_len, sv_dtype dtype, int B, int K, int V,
                                       const int32_t* draft_lens, int32_t* out_cu_accept,
                                       int32_t* out_packed, int32_t* out_batch_id,
-                                      float* out_accept_prob, int32_t* out_status,
-                                      void* workspace, size_t ws_bytes, sv_stream_t stream);
+                                      float* out_accept_prob, float* out_cut,
+                                      int32_t* out_status, void* workspace, size_t ws_bytes,
+                                      sv_stream_t stream);
 
 /* Typical acceptance ("推测解码与 MTP" §10.4: the rule of the original Medusa,
  * an approximation that is not exactly lossless, also offered by EAGLE).
@@ -246,8 +259,8 @@ sv_status spec_verify_typical(const void* target_logits, const int32_t* draft_to
  * passing node (the lowest id among equally deep ones): the tokens of its
  * root path, then one token drawn from its own distribution with
  * uniforms[b].  Rows of passing nodes must be valid (SV_REQ_BAD_LOGITS).
- *   target_logits, tree_parent (HOST), tree_tokens, out_tokens, out_path,
- *   out_accept_len, out_status, max_depth: as in spec_verify_tree.
+ *   target_logits, tree_parent, parent_stride, tree_tokens, out_tokens,
+ *   out_path, out_accept_len, out_status, max_depth: as in spec_verify_tree.
  *   uniforms [B] fp32 in [0, 1).  temperature > 0; eps, delta as in
  *   spec_verify_typical.  workspace: >= spec_verify_tree_workspace_size(B, N,
  *   V) bytes, 256-byte aligned, zero-filled once (spec_verify_workspace_init).
@@ -255,19 +268,59 @@ sv_status spec_verify_typical(const void* target_logits, const int32_t* draft_to
  * parallel). */
 size_t spec_verify_tree_workspace_size(int B, int N, int V);
 sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tree_parent,
-                                   const int32_t* tree_tokens, const float* uniforms,
-                                   float temperature, float eps, float delta, int32_t* out_tokens,
-                                   int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
-                                   int max_depth, int32_t* out_path, int32_t* out_status,
-                                   void* workspace, size_t ws_bytes, sv_stream_t stream);
+                                   int parent_stride, const int32_t* tree_tokens,
+                                   const float* uniforms, float temperature, float eps,
+                                   float delta, int32_t* out_tokens, int32_t* out_accept_len,
+                                   sv_dtype dtype, int B, int N, int V, int max_depth,
+                                   int32_t* out_path, int32_t* out_status, void* workspace,
+                                   size_t ws_bytes, sv_stream_t stream);
+
+/* Lossless tree verification by rejection sampling ("推测解码与 MTP" §10.4:
+ * the methods that verify by rejection sampling, EAGLE among them, are
+ * lossless; the candidate trees of §3.3 "Tree Attention" and §4.2, whose
+ * nodes are each head's top-k candidates).  Every candidate is a
+ * deterministic (one-hot) draft of the distribution at its parent.  From the
+ * root: with p the tempered target distribution at the current node and w = p,
+ * the node's children are tested in increasing id - child c with token x_c
+ * is accepted iff u_c < w(x_c) / sum(w), and a rejected child's token leaves
+ * w (w(x_c) = 0); the first accepted child's token is emitted and the walk
+ * moves to it; when no child is accepted (or at a leaf) one token is drawn
+ * from w / sum(w) with u_0 (the smallest j whose cumulative weight exceeds
+ * u_0 times the total) and the walk ends.  Each emitted token is distributed
+ * exactly as the target's distribution at its node; a token repeated among
+ * siblings has no mass left when its turn comes and is rejected.
+ *   uniforms  [B, N+1] fp32 in [0, 1): column c (1..N) drives the test of
+ *             node c, column 0 the final draw.
+ *   temperature  T > 0; T == 0 runs the greedy walk of spec_verify_tree
+ *             (uniforms and workspace unused).
+ *   target_logits, tree_parent, parent_stride, tree_tokens, out_tokens,
+ *   out_path, out_accept_len, out_status, max_depth: as in spec_verify_tree
+ *   (out_tokens: the accepted candidates' tokens, then the drawn token).
+ *   workspace: >= spec_verify_tree_workspace_size(B, N, V) bytes, as for
+ *   spec_verify_tree_typical.
+ * Every row of the tree is read once (all candidate rows are reduced in
+ * parallel, each row's sums leaving out its children's tokens); only the
+ * walked rows must be valid (SV_REQ_BAD_LOGITS). */
+sv_status spec_verify_tree_sample(const void* target_logits, const int32_t* tree_parent,
+                                  int parent_stride, const int32_t* tree_tokens,
+                                  const float* uniforms, float temperature, int32_t* out_tokens,
+                                  int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
+                                  int max_depth, int32_t* out_path, int32_t* out_status,
+                                  void* workspace, size_t ws_bytes, sv_stream_t stream);
 
 /* Greedy tree verification (Medusa / EAGLE; "推测解码与 MTP" §3.3).
  *
  *   target_logits  [B, N+1, V] dtype: row 0 is the root (the last committed
  *                  token), row n the target's logits after candidate node n.
- *   tree_parent    HOST [N] int32: parent of node n (n = 1..N) at index n-1;
- *                  must satisfy 0 <= parent < n (an earlier node; breadth-first
- *                  order qualifies).  Copied into the launch; not retained.
+ *   tree_parent    [N] or [B, N] int32 (device): parent of node n (n = 1..N)
+ *                  at index n-1; a tree needs 0 <= parent < n (an earlier
+ *                  node; breadth-first order qualifies) and no node deeper
+ *                  than max_depth - a request whose array breaks this gets
+ *                  SV_REQ_BAD_TREE and emits nothing.
+ *   parent_stride  0: every request shares the one [N] tree; N: request b's
+ *                  tree is tree_parent[b*N .. b*N+N) (EAGLE-2's dynamic trees,
+ *                  built per request on the device, §4.3).  Other values:
+ *                  SV_ERR_TREE.
  *   tree_tokens    [B, N] int32: the candidate token of node n at index n-1.
  *   out_tokens     [B, max_depth+1] int32: the target argmax at each node of the
  *                  accepted path (root first): the accepted node tokens followed
@@ -283,10 +336,20 @@ sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tre
  * path; if a caller repeats a token among siblings, the lowest node id wins.
  * Only the rows on the accepted path are read. */
 sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent,
-                           const int32_t* tree_tokens, int32_t* out_tokens,
+                           int parent_stride, const int32_t* tree_tokens, int32_t* out_tokens,
                            int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
                            int max_depth, int32_t* out_path, int32_t* out_status,
                            sv_stream_t stream);
+
+/* The longest time a kernel waits for logits it staged in shared memory
+ * before it gives up: the call then marks every request SV_REQ_TIMEOUT (the
+ * workspace stays usable; the next call starts clean).  Default 2 s, which
+ * only a device fault can exhaust; a serving loop with a watchdog may set
+ * less.  0 makes the waits give up at once, without polling - every call
+ * then reports SV_REQ_TIMEOUT, which is how the timeout path is tested.
+ * Process-wide; applies to the calls queued after it.  Always SV_OK. */
+sv_status spec_verify_set_wait_limit_ns(uint64_t limit_ns);
+uint64_t spec_verify_wait_limit_ns(void);
 
 /* n-gram (prompt-lookup) proposer: the step before verification that makes
  * the one-hot drafts ("投机解码" (FastDeploy docs), "使用 Ngram 解码": drafts
@@ -332,9 +395,11 @@ sv_status spec_ngram_propose(const int32_t* tokens, const int32_t* lens, int B, 
  *   - Limit: spec_verify_workspace_size(B, K, V) must not exceed
  *     SV_NOALLOC_SCRATCH_BYTES; larger problems return SV_ERR_WORKSPACE with
  *     nothing queued.  (B = 256, K = 5, V = 152064 needs about 3.4 MB.)
- *   - The first call on each device looks up the array's device address
- *     (cudaGetSymbolAddress, which may load the module on that device); make
- *     that first call before any stream capture.
+ *   - Each call looks up the array's device address on the current device
+ *     (cudaGetSymbolAddress; it queues no work, and a device reset that
+ *     reloads the module cannot leave a stale address behind).  The first
+ *     call on a device may load the library's module there: make that first
+ *     call before any stream capture.
  *   - Every call on a device uses the same array, which keeps the previous
  *     call's contents; each call first clears, on its stream, the counters
  *     that must start at zero.  Calls that overlap on the GPU (different

@@ -43,7 +43,7 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, n), "libspecverify.so does not export %s" % n
     for n in _native.SYMBOLS:
         assert hasattr(lib, n)
-    assert lib.spec_verify_version() == 100
+    assert lib.spec_verify_version() == 101
 
 
 def test_workspace_size(lib):
@@ -93,18 +93,41 @@ def test_host_validation_codes(lib):
     assert g == 1
 
 
-def tree(lib, parent, N, max_depth, **kw):
-    arr = np.asarray(parent, np.int32)
-    return lib.spec_verify_tree(kw.get("target", FAKE), arr.ctypes.data_as(ctypes.c_void_p), FAKE,
+def tree(lib, N, max_depth, stride=0, **kw):
+    """The greedy tree call with fake device pointers (host checks only: the
+    parent array now lives in device memory and is checked there)."""
+    return lib.spec_verify_tree(kw.get("target", FAKE), kw.get("parent", FAKE), stride, FAKE,
                                 FAKE, FAKE, 1, 2, N, 64, max_depth, NULL, NULL, NULL)
 
 
 def test_tree_host_validation(lib):
-    assert tree(lib, [0, 2, 1], 3, 4) == 5           # parent not an earlier node
-    assert tree(lib, [0, 0, -1], 3, 4) == 5
-    assert tree(lib, [0, 1, 2], 3, 2) == 5           # depth 3 > max_depth 2
-    assert tree(lib, [0] * 257, 257, 2) == 2          # too many nodes
-    assert tree(lib, [0, 1], 2, 2, target=NULL) == 1
+    assert tree(lib, 3, 4, stride=1) == 5            # a parent stride neither 0 nor N
+    assert tree(lib, 3, 4, stride=-3) == 5
+    assert tree(lib, 257, 2) == 2                    # too many nodes
+    assert tree(lib, 3, -1) == 2                     # negative max_depth
+    assert tree(lib, 2, 2, target=NULL) == 1
+    assert tree(lib, 2, 2, parent=NULL) == 1
+    ts = lib.spec_verify_tree_sample(FAKE, FAKE, 0, FAKE, FAKE, ctypes.c_float(-1.0), FAKE, FAKE,
+                                     1, 2, 3, 64, 4, NULL, NULL, FAKE, 0, NULL)
+    assert ts == 4                                   # negative temperature
+    ts = lib.spec_verify_tree_sample(FAKE, FAKE, 0, FAKE, NULL, ctypes.c_float(1.0), FAKE, FAKE,
+                                     1, 2, 3, 64, 4, NULL, NULL, FAKE, 0, NULL)
+    assert ts == 1                                   # uniforms missing
+    ts = lib.spec_verify_tree_sample(FAKE, FAKE, 0, FAKE, FAKE, ctypes.c_float(1.0), FAKE, FAKE,
+                                     1, 2, 3, 64, 4, NULL, NULL, FAKE, 0, NULL)
+    assert ts == 6                                   # workspace too small
+
+
+def test_wait_limit_setting(lib):
+    """The process-wide wait limit round-trips (no GPU involved)."""
+    old = lib.spec_verify_wait_limit_ns()
+    assert old == 2_000_000_000
+    try:
+        assert lib.spec_verify_set_wait_limit_ns(12345) == 0
+        assert lib.spec_verify_wait_limit_ns() == 12345
+    finally:
+        lib.spec_verify_set_wait_limit_ns(old)
+    assert lib.spec_verify_wait_limit_ns() == old
 
 
 def test_status_strings(lib):

@@ -1,11 +1,13 @@
 """Top-k / top-p filtered verification: CUDA path vs the fp64 oracle (needs
-a GPU).  The rows of a filtered call are held by clusters of CTAs (1 to 8
-per row); the cases cover the cut found among the candidates and on the
-whole slab, both logit types, the bulk-copy and the scalar
-slab loads, several cluster sizes, exact ties at the cuts (quantised
-logits), dense and one-hot drafts, grammar masks together with the
-filters, ragged drafts, the switches (top_k >= V, top_p = 1), and the
-argument checks."""
+a GPU).  Each row of a filtered call is taken by one CTA, which finds the cut
+among the row's candidates (elements within 2^-18 of the max's weight) or,
+when the cut may lie outside them, by a radix descent over the whole row.
+The GPU reports every row's cut value; the oracle runs with those cuts
+forced and each must be the rule's own cut or lie within 1e-6 of mass of it
+(tests/parity.py).  The cases cover both logit types, the vector and the
+scalar row loads, exact ties at the cuts (quantised logits), dense and
+one-hot drafts, grammar masks together with the filters, ragged drafts, the
+switches (top_k >= V, top_p = 1), and the argument checks."""
 import numpy as np
 import pytest
 import torch
@@ -21,31 +23,28 @@ def check_filtered(wl, flag_rate=None):
     d = parity.to_device(wl)
     out = api.spec_verify_sample(d["target"], d["draft"], d["draft_tokens"], d["uniforms"], wl.T,
                                  draft_lens=d["draft_lens"], token_mask=d["token_mask"],
-                                 top_k=wl.top_k, top_p=wl.top_p)
+                                 top_k=wl.top_k, top_p=wl.top_p, cut=True)
     torch.cuda.synchronize()
-    ref = parity.oracle_sample(wl, threads=THREADS)
-    rep = parity.compare_sample(ref, out, wl.K, wl.V)
-    parity.verify_draws(wl, rep)
-    parity.assert_report(rep, flag_rate)
+    rep = parity.check_sample(wl, out, threads=THREADS, flag_rate=flag_rate)
     parity.compare_compaction(out, wl.K)
-    return out, ref, rep
+    return out, rep
 
 
 GRID = [
     # V, K, T, dtype, drafts, top_k, top_p, quantize
-    (152064, 3, 0.8, "bf16", "onehot", 0, 0.95, None),   # 4 CTAs per row
+    (152064, 3, 0.8, "bf16", "onehot", 0, 0.95, None),   # the cut among the candidates
     (152064, 2, 1.0, "bf16", "dense", 50, 0.9, None),
-    (32000, 5, 0.7, "bf16", "onehot", 20, 1.0, 1.0),      # 1 CTA, ties at the top-k cut
+    (32000, 5, 0.7, "bf16", "onehot", 20, 1.0, 1.0),      # ties at the top-k cut
     (32000, 3, 1.0, "bf16", "dense", 0, 0.8, 0.5),        # ties at the top-p cut
     (65536, 2, 1.3, "f32", "dense", 100, 0.95, None),     # fp32: 4 radix passes
-    (50257, 3, 0.9, "bf16", "onehot", 0, 0.9, None),      # scalar slab loads, 2 CTAs
+    (50257, 3, 0.9, "bf16", "onehot", 0, 0.9, None),      # scalar row loads (odd V)
     (1000, 4, 1.0, "bf16", "dense", 1, 1.0, None),        # top-k = 1
     (4104, 2, 0.6, "f32", "onehot", 7, 0.3, 0.25),
-    (260000, 1, 1.0, "bf16", "onehot", 0, 0.99, None),    # 8 CTAs per row
+    (260000, 1, 1.0, "bf16", "onehot", 0, 0.99, None),    # the widest rows (508 KB)
     (9000, 0, 1.0, "bf16", "onehot", 0, 0.5, None),       # K = 0: only the bonus draw
-    # rows whose cut may lie outside the candidates (weights >= 2^-20 of the
-    # max's) take the full-slab descent: top-p too close to 1, top-k above
-    # the candidate count
+    # rows whose cut may lie outside the candidates (weights >= 2^-18 of the
+    # max's) take the full-row radix descent: top-p too close to 1, top-k
+    # above the candidate count
     (32000, 3, 1.0, "bf16", "dense", 0, 0.9999, None),
     (32000, 2, 0.3, "bf16", "onehot", 20000, 1.0, None),
     (65536, 2, 0.5, "f32", "onehot", 30000, 0.9, None),
@@ -73,13 +72,16 @@ def test_filtered_with_grammar_masks_and_ragged_drafts():
         check_filtered(wl)
 
 
-def test_filtered_headline_shape():
+def test_filtered_headline_shape(capsys):
     """B=256, K=5, V=152064 one-hot drafts sampled with temperature 0.8 and
-    top_p 0.95 (the vLLM Ascend guide's SamplingParams), full size."""
+    top_p 0.95 (the vLLM Ascend guide's SamplingParams), full size: flagged
+    acceptance tests below 1e-4 of the positions, every cut the rule's own
+    or within 1e-6 of mass of it (counted), everything after it exact."""
     wl = synth.make_sample_case(256, 5, 152064, drafts="onehot", T=0.8, seed=90)
     wl.top_p = 0.95
-    _, _, rep = check_filtered(wl)
-    print("\n[top-p 0.95, B256 K5 V152064] %s" % rep.summary())
+    _, rep = check_filtered(wl, flag_rate=1e-4)
+    with capsys.disabled():
+        print("\n[top-p 0.95, B256 K5 V152064] %s" % rep.summary())
 
 
 def test_filter_switches_and_argument_checks():

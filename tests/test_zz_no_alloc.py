@@ -5,10 +5,11 @@ device in its own pool and gives a plugin only its input and output buffers,
 or a path where a cudaMalloc and the device synchronisation it may cause are
 not allowed) use this entry point: its scratch is a fixed array inside the
 library.  The GPU test calls it through the C ABI twice in a row and checks
-each result against spec_verify_sample with a caller-provided workspace:
-tokens, accept lengths, packed output and statuses identical, accept
-probabilities within 1e-5.  This file is collected last so that a run that
-stops at the first failure has run every other test before it."""
+each result against spec_verify_sample with a caller-provided workspace
+(tokens, accept lengths, packed output and statuses identical, accept
+probabilities within 1e-5) and against the fp64 oracle under the same rule
+as every other sampling test.  This file is collected last so that a run
+that stops at the first failure has run every other test before it."""
 import ctypes
 
 import numpy as np
@@ -58,3 +59,4 @@ def test_noalloc_matches_the_workspace_entry_point_on_two_calls():
         diff = (out.accept_prob - ref.accept_prob).abs().max().item()
         assert diff <= 1e-5, diff
         assert (out.accept_len.cpu().numpy() >= 1).all()
+        parity.check_sample(wl, out)

@@ -17,6 +17,7 @@ SYMBOLS = (
     "spec_verify_version", "spec_verify_sample_noalloc", "spec_verify_sample_masked",
     "spec_verify_greedy_masked", "spec_ngram_propose", "spec_verify_sample_filtered",
     "spec_verify_typical", "spec_verify_tree_typical", "spec_verify_tree_workspace_size",
+    "spec_verify_tree_sample", "spec_verify_set_wait_limit_ns", "spec_verify_wait_limit_ns",
 )
 
 _lock = threading.Lock()
@@ -53,19 +54,25 @@ def lib():
         l.spec_verify_greedy_masked.argtypes = [P, P, P, P, P, I, I, I, I, P, P, P, P, P, P, Z, P]
         l.spec_verify_greedy_masked.restype = I
         l.spec_verify_sample_filtered.argtypes = [P, P, P, P, F, I, F, P, P, P, I, I, I, I, P, P,
-                                                  P, P, P, P, P, Z, P]
+                                                  P, P, P, P, P, P, Z, P]
         l.spec_verify_sample_filtered.restype = I
         l.spec_verify_typical.argtypes = [P, P, P, F, F, F, P, P, I, I, I, I, P, P, P, P, P, P, P,
                                           Z, P]
         l.spec_verify_typical.restype = I
         l.spec_verify_tree_workspace_size.argtypes = [I, I, I]
         l.spec_verify_tree_workspace_size.restype = Z
-        l.spec_verify_tree_typical.argtypes = [P, P, P, P, F, F, F, P, P, I, I, I, I, I, P, P, P, Z,
-                                               P]
+        l.spec_verify_tree_typical.argtypes = [P, P, I, P, P, F, F, F, P, P, I, I, I, I, I, P, P, P,
+                                               Z, P]
+        l.spec_verify_tree_sample.argtypes = [P, P, I, P, P, F, P, P, I, I, I, I, I, P, P, P, Z, P]
+        l.spec_verify_tree_sample.restype = I
+        l.spec_verify_set_wait_limit_ns.argtypes = [ctypes.c_uint64]
+        l.spec_verify_set_wait_limit_ns.restype = I
+        l.spec_verify_wait_limit_ns.argtypes = []
+        l.spec_verify_wait_limit_ns.restype = ctypes.c_uint64
         l.spec_verify_tree_typical.restype = I
         l.spec_ngram_propose.argtypes = [P, P, I, I, I, I, I, P, P, P, P, P]
         l.spec_ngram_propose.restype = I
-        l.spec_verify_tree.argtypes = [P, P, P, P, P, I, I, I, I, I, P, P, P]
+        l.spec_verify_tree.argtypes = [P, P, I, P, P, P, I, I, I, I, I, P, P, P]
         l.spec_verify_tree.restype = I
         l.spec_verify_status_string.argtypes = [I]
         l.spec_verify_status_string.restype = ctypes.c_char_p

@@ -20,6 +20,8 @@ SV_BF16 = 1
 REQ_BAD_TOKEN = 1
 REQ_BAD_LOGITS = 2
 REQ_BAD_DRAFT_LEN = 4
+REQ_TIMEOUT = 8
+REQ_BAD_TREE = 16
 MAX_K = 31
 
 
@@ -95,6 +97,7 @@ class VerifyOutputs:
     batch_id: Optional[torch.Tensor] = None    # [B*(K+1)]
     accept_prob: Optional[torch.Tensor] = None  # [B, K] fp32
     status: Optional[torch.Tensor] = None      # [B]
+    cut: Optional[torch.Tensor] = None         # [B, R] fp32 (filtered calls)
 
 
 def alloc_outputs(B, K, device, *, packed=True, accept_prob=True, status=True):
@@ -132,7 +135,7 @@ def _check_mask(token_mask, B, K, V, device):
 def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temperature,
                        out: Optional[VerifyOutputs] = None, *, draft_lens=None,
                        packed=True, accept_prob=True, status=True,
-                       token_mask=None, top_k=0, top_p=1.0) -> VerifyOutputs:
+                       token_mask=None, top_k=0, top_p=1.0, cut=False) -> VerifyOutputs:
     """Rejection-sampling verification of one batch (see spec_verify.h).
 
     target_logits [B, K+1, V] bf16/fp32 CUDA; draft_logits [B, K, V] same
@@ -140,7 +143,9 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temp
     [B, K+1] fp32; temperature >= 0 (0 = greedy rule); token_mask
     [B, K+1, ceil(V/32)] int32 grammar masks or None (bit j % 32 of word
     j // 32 set = token j allowed at that position); top_k (0 = off) and
-    top_p (1.0 = off) filter every sampled distribution."""
+    top_p (1.0 = off) filter every sampled distribution; cut=True (filtered
+    calls) also returns out.cut [B, R], each row's lowest kept logit (R =
+    K+1 target rows, then K draft rows with draft logits)."""
     B, K, V, device = _validate_batch(target_logits, draft_tokens, draft_lens)
     if draft_logits is not None:
         _check(draft_logits, "draft_logits", device, target_logits.dtype, (B, K, V))
@@ -148,16 +153,23 @@ def spec_verify_sample(target_logits, draft_logits, draft_tokens, uniforms, temp
     _check_mask(token_mask, B, K, V, device)
     if out is None:
         out = alloc_outputs(B, K, device, packed=packed, accept_prob=accept_prob, status=status)
+    filtered = top_k != 0 or top_p != 1.0
+    if filtered and cut and out.cut is None:
+        R = K + 1 + (K if draft_logits is not None else 0)
+        out.cut = torch.empty((B, R), dtype=torch.float32, device=device)
     ws = workspace(B, K, V, device)
     lib = _native.lib()
     head = (_p(target_logits), _p(draft_logits), _p(draft_tokens), _p(uniforms),
             ctypes.c_float(float(temperature)))
-    tail = (_p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, K, V,
-            _p(draft_lens), _p(out.cu_accept), _p(out.packed), _p(out.batch_id),
-            _p(out.accept_prob), _p(out.status), _p(ws), ws.numel(), _stream(device))
-    if top_k != 0 or top_p != 1.0:
+    mid = (_p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, K, V,
+           _p(draft_lens), _p(out.cu_accept), _p(out.packed), _p(out.batch_id),
+           _p(out.accept_prob))
+    end = (_p(out.status), _p(ws), ws.numel(), _stream(device))
+    tail = mid + end
+    if filtered:
         rc = lib.spec_verify_sample_filtered(*head, int(top_k), ctypes.c_float(float(top_p)),
-                                             _p(token_mask), *tail)
+                                             _p(token_mask), *mid,
+                                             _p(out.cut if cut else None), *end)
     elif token_mask is None:
         rc = lib.spec_verify_sample(*head, *tail)
     else:
@@ -200,6 +212,7 @@ class TreeOutputs:
 
 
 def tree_depth(parent) -> int:
+    """Depth of a host-side parent array (parent of node n at index n-1)."""
     d = [0]
     for n, p in enumerate(np.asarray(parent, dtype=np.int64).reshape(-1), start=1):
         if p < 0 or p >= n:
@@ -208,32 +221,79 @@ def tree_depth(parent) -> int:
     return max(d)
 
 
-def spec_verify_tree(target_logits, tree_parent, tree_tokens, max_depth=None,
-                     out: Optional[TreeOutputs] = None, *, path=True, status=True) -> TreeOutputs:
-    """Greedy tree verification.  tree_parent: host sequence [N] (parent of
-    node n at index n-1); tree_tokens [B, N] int32 CUDA."""
+def _tree_args(target_logits, tree_parent, tree_tokens, max_depth):
+    """(B, N, V, device, parent tensor, parent stride, max_depth).  tree_parent:
+    a CUDA int32 tensor [N] (one tree) or [B, N] (a tree per request) - then
+    max_depth must be given - or a host array [N] / [B, N], copied to the
+    device, whose depth is the default max_depth."""
     if target_logits.dim() != 3:
         raise ValueError("target_logits must be [B, N+1, V]")
     B, N1, V = target_logits.shape
     N = N1 - 1
     device = target_logits.device
     _check(target_logits, "target_logits", device)
-    parent = np.ascontiguousarray(np.asarray(tree_parent, dtype=np.int32).reshape(-1))
-    if parent.size != N:
-        raise ValueError("tree_parent must have N = %d entries" % N)
-    _check(tree_tokens, "tree_tokens", device, torch.int32, (B, N))
+    if not (isinstance(tree_parent, torch.Tensor) and tree_parent.device == device):
+        host = np.ascontiguousarray(np.asarray(tree_parent, dtype=np.int32))
+        if max_depth is None:
+            max_depth = max(tree_depth(r) for r in host.reshape(-1, N)) if N else 0
+        tree_parent = torch.from_numpy(host).to(device)
     if max_depth is None:
-        max_depth = tree_depth(parent)
-    D1 = int(max_depth) + 1
+        raise ValueError("max_depth is required with a device-side tree_parent")
+    if tuple(tree_parent.shape) == (N,):
+        stride = 0
+    elif tuple(tree_parent.shape) == (B, N):
+        stride = N
+    else:
+        raise ValueError("tree_parent must be [N] or [B, N] (N = %d)" % N)
+    _check(tree_parent, "tree_parent", device, torch.int32)
+    _check(tree_tokens, "tree_tokens", device, torch.int32, (B, N))
+    return B, N, V, device, tree_parent, stride, int(max_depth)
+
+
+def _tree_outputs(B, D1, device, path, status):
+    i32 = dict(dtype=torch.int32, device=device)
+    return TreeOutputs(tokens=torch.empty((B, D1), **i32), accept_len=torch.empty((B,), **i32),
+                       path=torch.empty((B, D1), **i32) if path else None,
+                       status=torch.empty((B,), **i32) if status else None)
+
+
+def spec_verify_tree(target_logits, tree_parent, tree_tokens, max_depth=None,
+                     out: Optional[TreeOutputs] = None, *, path=True, status=True) -> TreeOutputs:
+    """Greedy tree verification.  tree_parent [N] or [B, N] (parent of node n
+    at index n-1; device tensor, or host array copied to the device);
+    tree_tokens [B, N] int32 CUDA."""
+    B, N, V, device, par, stride, max_depth = _tree_args(target_logits, tree_parent, tree_tokens,
+                                                         max_depth)
     if out is None:
-        i32 = dict(dtype=torch.int32, device=device)
-        out = TreeOutputs(tokens=torch.empty((B, D1), **i32), accept_len=torch.empty((B,), **i32),
-                          path=torch.empty((B, D1), **i32) if path else None,
-                          status=torch.empty((B,), **i32) if status else None)
+        out = _tree_outputs(B, max_depth + 1, device, path, status)
     rc = _native.lib().spec_verify_tree(
-        _p(target_logits), parent.ctypes.data_as(ctypes.c_void_p), _p(tree_tokens),
-        _p(out.tokens), _p(out.accept_len), _dtype_code(target_logits), B, N, V, int(max_depth),
-        _p(out.path), _p(out.status), _stream(device))
+        _p(target_logits), _p(par), stride, _p(tree_tokens), _p(out.tokens), _p(out.accept_len),
+        _dtype_code(target_logits), B, N, V, max_depth, _p(out.path), _p(out.status),
+        _stream(device))
+    if rc:
+        raise VerifyError(rc)
+    return out
+
+
+def spec_verify_tree_sample(target_logits, tree_parent, tree_tokens, uniforms, temperature,
+                            max_depth=None, out: Optional[TreeOutputs] = None, *, path=True,
+                            status=True) -> TreeOutputs:
+    """Lossless tree verification by rejection sampling (see spec_verify.h):
+    tree_parent as for spec_verify_tree, tree_tokens [B, N] int32, uniforms
+    [B, N+1] fp32 (column n: node n's test, column 0: the final draw);
+    temperature 0 runs the greedy walk."""
+    B, N, V, device, par, stride, max_depth = _tree_args(target_logits, tree_parent, tree_tokens,
+                                                         max_depth)
+    _check(uniforms, "uniforms", device, torch.float32, (B, N + 1))
+    if out is None:
+        out = _tree_outputs(B, max_depth + 1, device, path, status)
+    lib = _native.lib()
+    ws = workspace(B, N, V, device, need=int(lib.spec_verify_tree_workspace_size(B, N, V)))
+    rc = lib.spec_verify_tree_sample(
+        _p(target_logits), _p(par), stride, _p(tree_tokens), _p(uniforms),
+        ctypes.c_float(float(temperature)), _p(out.tokens), _p(out.accept_len),
+        _dtype_code(target_logits), B, N, V, max_depth, _p(out.path), _p(out.status), _p(ws),
+        ws.numel(), _stream(device))
     if rc:
         raise VerifyError(rc)
     return out
@@ -265,38 +325,35 @@ def spec_verify_tree_typical(target_logits, tree_parent, tree_tokens, uniforms, 
                              eps=0.09, delta=0.3, max_depth=None,
                              out: Optional[TreeOutputs] = None, *, path=True,
                              status=True) -> TreeOutputs:
-    """Typical acceptance over a candidate tree: tree_parent host [N],
-    tree_tokens [B, N] int32, uniforms [B] fp32 for the final draw."""
-    if target_logits.dim() != 3:
-        raise ValueError("target_logits must be [B, N+1, V]")
-    B, N1, V = target_logits.shape
-    N = N1 - 1
-    device = target_logits.device
-    _check(target_logits, "target_logits", device)
-    parent = np.ascontiguousarray(np.asarray(tree_parent, dtype=np.int32).reshape(-1))
-    if parent.size != N:
-        raise ValueError("tree_parent must have N = %d entries" % N)
-    _check(tree_tokens, "tree_tokens", device, torch.int32, (B, N))
+    """Typical acceptance over a candidate tree: tree_parent as for
+    spec_verify_tree, tree_tokens [B, N] int32, uniforms [B] fp32 for the
+    final draw."""
+    B, N, V, device, par, stride, max_depth = _tree_args(target_logits, tree_parent, tree_tokens,
+                                                         max_depth)
     _check(uniforms, "uniforms", device, torch.float32, (B,))
-    if max_depth is None:
-        max_depth = tree_depth(parent)
-    D1 = int(max_depth) + 1
     if out is None:
-        i32 = dict(dtype=torch.int32, device=device)
-        out = TreeOutputs(tokens=torch.empty((B, D1), **i32), accept_len=torch.empty((B,), **i32),
-                          path=torch.empty((B, D1), **i32) if path else None,
-                          status=torch.empty((B,), **i32) if status else None)
+        out = _tree_outputs(B, max_depth + 1, device, path, status)
     lib = _native.lib()
     ws = workspace(B, N, V, device, need=int(lib.spec_verify_tree_workspace_size(B, N, V)))
     rc = lib.spec_verify_tree_typical(
-        _p(target_logits), parent.ctypes.data_as(ctypes.c_void_p), _p(tree_tokens), _p(uniforms),
+        _p(target_logits), _p(par), stride, _p(tree_tokens), _p(uniforms),
         ctypes.c_float(float(temperature)), ctypes.c_float(float(eps)),
         ctypes.c_float(float(delta)), _p(out.tokens), _p(out.accept_len),
-        _dtype_code(target_logits), B, N, V, int(max_depth), _p(out.path), _p(out.status),
+        _dtype_code(target_logits), B, N, V, max_depth, _p(out.path), _p(out.status),
         _p(ws), ws.numel(), _stream(device))
     if rc:
         raise VerifyError(rc)
     return out
+
+
+def set_wait_limit_ns(limit_ns: int) -> None:
+    """The longest a kernel waits for staged logits before the call reports
+    REQ_TIMEOUT (default 2 s; 0 gives up at once).  Process-wide."""
+    _native.lib().spec_verify_set_wait_limit_ns(int(limit_ns))
+
+
+def wait_limit_ns() -> int:
+    return int(_native.lib().spec_verify_wait_limit_ns())
 
 
 @dataclass

@@ -81,6 +81,10 @@ static void forget_workspace(const void* ws) {
 
 static bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
+// The limit of the kernels' waits for staged logits (spec_verify_set_wait_limit_ns).
+static std::atomic<unsigned long long> g_wait_ns{kWaitLimitNs};
+unsigned long long wait_limit_ns() { return g_wait_ns.load(std::memory_order_relaxed); }
+
 static sv_status verify_common(int mode, const void* target, const void* draft,
                                const int32_t* draft_tokens, const float* uniforms, float T,
                                int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype, int B,
@@ -89,7 +93,8 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
                                int32_t* out_status, void* ws, size_t ws_bytes,
                                cudaStream_t stream, int greedy_prob,
                                const uint32_t* mask = nullptr, int top_k = 0,
-                               float top_p = 1.f, float eps = 0.f, float delta = 0.f) {
+                               float top_p = 1.f, float eps = 0.f, float delta = 0.f,
+                               float* out_cut = nullptr) {
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
   if (B < 0 || B > SV_MAX_B || K < 0 || K > SV_MAX_K || V < 1 || V > SV_MAX_V) return SV_ERR_SHAPE;
   if (B == 0) {
@@ -156,6 +161,8 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.greedy_prob = greedy_prob;
   p.compact_in_finalize = (out_cu || out_packed || out_batch_id) ? 1 : 0;
   p.fin_cache = fin_cache_bytes(p) <= kFinCacheLimit ? 1 : 0;
+  p.out_cut = p.filter ? out_cut : nullptr;
+  p.wait_ns = wait_limit_ns();
   if (prepare_workspace(ws, l, B, R, stream) != cudaSuccess) return SV_ERR_CUDA;
   return launch_verify(mode, dtype, vec, p, stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
@@ -232,8 +239,9 @@ sv_status spec_verify_sample_filtered(const void* target_logits, const void* dra
                                       int32_t* out_accept_len, sv_dtype dtype, int B, int K, int V,
                                       const int32_t* draft_lens, int32_t* out_cu_accept,
                                       int32_t* out_packed, int32_t* out_batch_id,
-                                      float* out_accept_prob, int32_t* out_status,
-                                      void* workspace, size_t ws_bytes, sv_stream_t stream) {
+                                      float* out_accept_prob, float* out_cut,
+                                      int32_t* out_status, void* workspace, size_t ws_bytes,
+                                      sv_stream_t stream) {
   if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
   if (top_k < 0 || !(top_p > 0.f && top_p <= 1.f)) return SV_ERR_FILTER;
   if (token_mask && ((uintptr_t)token_mask & 3u)) return SV_ERR_NULL;
@@ -242,7 +250,7 @@ sv_status spec_verify_sample_filtered(const void* target_logits, const void* dra
                        uniforms, temperature, out_tokens, out_accept_len, dtype, B, K, V,
                        draft_lens, out_cu_accept, out_packed, out_batch_id, out_accept_prob,
                        out_status, workspace, ws_bytes, (cudaStream_t)stream, 1, token_mask, top_k,
-                       top_p);
+                       top_p, 0.f, 0.f, out_cut);
 }
 
 sv_status spec_verify_typical(const void* target_logits, const int32_t* draft_tokens,
@@ -266,39 +274,36 @@ size_t spec_verify_tree_workspace_size(int B, int N, int V) {
   return layout_for(B, N + 1, V).total;
 }
 
-sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tree_parent,
-                                   const int32_t* tree_tokens, const float* uniforms,
-                                   float temperature, float eps, float delta, int32_t* out_tokens,
-                                   int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
-                                   int max_depth, int32_t* out_path, int32_t* out_status,
-                                   void* workspace, size_t ws_bytes, sv_stream_t stream) {
+}  // extern "C"
+
+namespace sv {
+
+// Kernel A over every row of a candidate tree (B * (N+1) rows), then the
+// tree's own finalize kernel: typical acceptance or rejection sampling.
+static sv_status tree_rows_call(int mode, const void* target, const int32_t* tree_parent,
+                                int parent_stride, const int32_t* tree_tokens,
+                                const float* uniforms, float T, float eps, float delta,
+                                int32_t* out_tokens, int32_t* out_accept_len, sv_dtype dtype,
+                                int B, int N, int V, int max_depth, int32_t* out_path,
+                                int32_t* out_status, void* workspace, size_t ws_bytes,
+                                cudaStream_t stream) {
   if (dtype != SV_F32 && dtype != SV_BF16) return SV_ERR_DTYPE;
   if (B < 0 || B > SV_MAX_B || N < 0 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_V ||
       max_depth < 0 || max_depth > SV_MAX_TREE_NODES)
     return SV_ERR_SHAPE;
-  if (!(temperature > 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
-  if (!(eps >= 0.f) || !(delta >= 0.f) || isinf(eps) || isinf(delta)) return SV_ERR_FILTER;
+  if (parent_stride != 0 && parent_stride != N) return SV_ERR_TREE;
   if (B == 0) return SV_OK;
-  if (!target_logits || !out_tokens || !out_accept_len || !uniforms) return SV_ERR_NULL;
+  if (!target || !out_tokens || !out_accept_len || !uniforms) return SV_ERR_NULL;
   if (N > 0 && (!tree_parent || !tree_tokens)) return SV_ERR_NULL;
-  TreeTypical t;
-  memset(&t, 0, sizeof t);
-  for (int n = 1; n <= N; ++n) {
-    const int pa = tree_parent[n - 1];
-    if (pa < 0 || pa >= n) return SV_ERR_TREE;
-    t.parent[n] = (short)pa;
-    t.depth[n] = (short)(t.depth[pa] + 1);
-    if (t.depth[n] > max_depth) return SV_ERR_TREE;
-  }
   const int R = N + 1;
   const WorkspaceLayout l = layout_for(B, R, V);
   if (!workspace || ((uintptr_t)workspace & 255u) || ws_bytes < l.total) return SV_ERR_WORKSPACE;
   const int vec_elems = dtype == SV_BF16 ? 8 : 4;
-  const bool vec = (V % vec_elems == 0) && aligned16(target_logits);
+  const bool vec = (V % vec_elems == 0) && aligned16(target);
   const int G = chunks_per_task(dtype, vec);
   VerifyParams p;
   memset(&p, 0, sizeof p);
-  p.target = target_logits;
+  p.target = target;
   char* base = static_cast<char*>(workspace);
   p.err = reinterpret_cast<int*>(base + l.counters);
   p.fin_ticket = p.err + 1;
@@ -321,7 +326,15 @@ sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tre
   if (p.total_tasks >= (1LL << 31)) return SV_ERR_SHAPE;
   p.div_tpr = make_fastdiv((uint32_t)p.TPR);
   p.div_r = make_fastdiv((uint32_t)R);
-  p.cc = (float)(1.4426950408889634 / (double)temperature);
+  p.cc = (float)(1.4426950408889634 / (double)T);
+  p.wait_ns = wait_limit_ns();
+  p.tree_parent = tree_parent;
+  p.parent_stride = parent_stride;
+  p.tree_tokens = tree_tokens;
+  TreeCall t;
+  memset(&t, 0, sizeof t);
+  t.parent = tree_parent;
+  t.parent_stride = parent_stride;
   t.tokens = tree_tokens;
   t.uniforms = uniforms;
   t.out_tokens = out_tokens;
@@ -330,9 +343,46 @@ sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tre
   t.out_status = out_status;
   t.N = N;
   t.D1 = max_depth + 1;
-  if (prepare_workspace(workspace, l, B, R, (cudaStream_t)stream) != cudaSuccess) return SV_ERR_CUDA;
-  return launch_tree_typical(dtype, vec, p, t, (cudaStream_t)stream) == cudaSuccess ? SV_OK
-                                                                                   : SV_ERR_CUDA;
+  if (prepare_workspace(workspace, l, B, R, stream) != cudaSuccess) return SV_ERR_CUDA;
+  const cudaError_t err = mode == kTreeSample ? launch_tree_sample(dtype, vec, p, t, stream)
+                                              : launch_tree_typical(dtype, vec, p, t, stream);
+  return err == cudaSuccess ? SV_OK : SV_ERR_CUDA;
+}
+
+}  // namespace sv
+
+extern "C" {
+
+sv_status spec_verify_tree_typical(const void* target_logits, const int32_t* tree_parent,
+                                   int parent_stride, const int32_t* tree_tokens,
+                                   const float* uniforms, float temperature, float eps,
+                                   float delta, int32_t* out_tokens, int32_t* out_accept_len,
+                                   sv_dtype dtype, int B, int N, int V, int max_depth,
+                                   int32_t* out_path, int32_t* out_status, void* workspace,
+                                   size_t ws_bytes, sv_stream_t stream) {
+  if (!(temperature > 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
+  if (!(eps >= 0.f) || !(delta >= 0.f) || isinf(eps) || isinf(delta)) return SV_ERR_FILTER;
+  return tree_rows_call(kTypical, target_logits, tree_parent, parent_stride, tree_tokens, uniforms,
+                        temperature, eps, delta, out_tokens, out_accept_len, dtype, B, N, V,
+                        max_depth, out_path, out_status, workspace, ws_bytes,
+                        (cudaStream_t)stream);
+}
+
+sv_status spec_verify_tree_sample(const void* target_logits, const int32_t* tree_parent,
+                                  int parent_stride, const int32_t* tree_tokens,
+                                  const float* uniforms, float temperature, int32_t* out_tokens,
+                                  int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
+                                  int max_depth, int32_t* out_path, int32_t* out_status,
+                                  void* workspace, size_t ws_bytes, sv_stream_t stream) {
+  if (!(temperature >= 0.f) || isinf(temperature)) return SV_ERR_TEMPERATURE;
+  if (temperature == 0.f)  // the greedy rule: the argmax walk
+    return spec_verify_tree(target_logits, tree_parent, parent_stride, tree_tokens, out_tokens,
+                            out_accept_len, dtype, B, N, V, max_depth, out_path, out_status,
+                            stream);
+  return tree_rows_call(kTreeSample, target_logits, tree_parent, parent_stride, tree_tokens,
+                        uniforms, temperature, 0.f, 0.f, out_tokens, out_accept_len, dtype, B, N,
+                        V, max_depth, out_path, out_status, workspace, ws_bytes,
+                        (cudaStream_t)stream);
 }
 
 sv_status spec_verify_greedy(const void* target_logits, const int32_t* draft_tokens,
@@ -347,7 +397,7 @@ sv_status spec_verify_greedy(const void* target_logits, const int32_t* draft_tok
 }
 
 sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent,
-                           const int32_t* tree_tokens, int32_t* out_tokens,
+                           int parent_stride, const int32_t* tree_tokens, int32_t* out_tokens,
                            int32_t* out_accept_len, sv_dtype dtype, int B, int N, int V,
                            int max_depth, int32_t* out_path, int32_t* out_status,
                            sv_stream_t stream) {
@@ -355,25 +405,15 @@ sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent
   if (B < 0 || B > SV_MAX_B || N < 0 || N > SV_MAX_TREE_NODES || V < 1 || V > SV_MAX_V ||
       max_depth < 0 || max_depth > SV_MAX_TREE_NODES)
     return SV_ERR_SHAPE;
+  if (parent_stride != 0 && parent_stride != N) return SV_ERR_TREE;
   if (B == 0) return SV_OK;
   if (!target_logits || !out_tokens || !out_accept_len) return SV_ERR_NULL;
   if (N > 0 && (!tree_parent || !tree_tokens)) return SV_ERR_NULL;
   TreeParams p;
   memset(&p, 0, sizeof p);
-  int depth[SV_MAX_TREE_NODES + 1];
-  depth[0] = 0;
-  int last_child[SV_MAX_TREE_NODES + 1];
-  for (int n = 0; n <= N; ++n) last_child[n] = 0;
-  for (int n = 1; n <= N; ++n) {
-    const int pa = tree_parent[n - 1];
-    if (pa < 0 || pa >= n) return SV_ERR_TREE;
-    depth[n] = depth[pa] + 1;
-    if (depth[n] > max_depth) return SV_ERR_TREE;
-    if (last_child[pa]) p.next_sibling[last_child[pa]] = (short)n;
-    else p.first_child[pa] = (short)n;
-    last_child[pa] = n;
-  }
   p.target = target_logits;
+  p.parent = tree_parent;
+  p.parent_stride = parent_stride;
   p.tokens = tree_tokens;
   p.out_tokens = out_tokens;
   p.out_accept_len = out_accept_len;
@@ -389,6 +429,13 @@ sv_status spec_verify_tree(const void* target_logits, const int32_t* tree_parent
   return launch_tree(dtype, vec, p, (cudaStream_t)stream) == cudaSuccess ? SV_OK : SV_ERR_CUDA;
 }
 
+sv_status spec_verify_set_wait_limit_ns(uint64_t limit_ns) {
+  g_wait_ns.store((unsigned long long)limit_ns, std::memory_order_relaxed);
+  return SV_OK;
+}
+
+uint64_t spec_verify_wait_limit_ns(void) { return (uint64_t)wait_limit_ns(); }
+
 const char* spec_verify_status_string(sv_status s) {
   switch (s) {
     case SV_OK: return "ok";
@@ -396,7 +443,7 @@ const char* spec_verify_status_string(sv_status s) {
     case SV_ERR_SHAPE: return "shape outside the supported range";
     case SV_ERR_DTYPE: return "unknown dtype";
     case SV_ERR_TEMPERATURE: return "temperature negative, NaN or infinite";
-    case SV_ERR_TREE: return "parent array is not a tree of depth <= max_depth";
+    case SV_ERR_TREE: return "tree parent stride is neither 0 nor N";
     case SV_ERR_WORKSPACE: return "workspace NULL, misaligned or too small";
     case SV_ERR_CUDA: return "CUDA launch failed";
     case SV_ERR_FILTER: return "top_k negative or top_p outside (0, 1]";
@@ -404,6 +451,6 @@ const char* spec_verify_status_string(sv_status s) {
   return "unknown status";
 }
 
-int spec_verify_version(void) { return 100; }
+int spec_verify_version(void) { return 101; }
 
 }  // extern "C"

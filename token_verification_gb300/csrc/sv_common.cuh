@@ -32,8 +32,9 @@ constexpr int kBadToken = 1;
 constexpr int kBadLogits = 2;
 constexpr int kBadDraftLen = 4;
 constexpr int kTimeout = 8;
+constexpr int kBadTree = 16;
 
-enum Mode : int { kOneHot = 0, kDense = 1, kGreedy = 2, kTypical = 3 };
+enum Mode : int { kOneHot = 0, kDense = 1, kGreedy = 2, kTypical = 3, kTreeSample = 4 };
 
 // ---------------------------------------------------------------------------
 // scalar primitives
@@ -221,15 +222,19 @@ __device__ __forceinline__ unsigned long long global_ns() {
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
   return t;
 }
-// Wait for phase `parity` of `bar`, for at most kWaitLimitNs of wall time;
-// false if it did not complete.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
+// Wait for phase `parity` of `bar`, for at most `limit_ns` of wall time
+// (kWaitLimitNs by default); false if it did not complete.  limit_ns = 0
+// gives up at once without polling (the caller's own copies are still
+// drained with the default limit before it leaves).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitLimitNs) {
+  if (limit_ns == 0) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const unsigned long long t0 = global_ns();
   for (;;) {
     for (int i = 0; i < 64; ++i)
       if (mbar_try_wait(bar, parity)) return true;
-    if (global_ns() - t0 > kWaitLimitNs) return false;
+    if (global_ns() - t0 > limit_ns) return false;
   }
 }
 __device__ __forceinline__ uint4 lds128(uint32_t addr) {
@@ -443,9 +448,12 @@ __device__ __forceinline__ float lane_max_bf16(const uint4 (&raw)[4]) {
 // With `ent` given, *ent receives sum_j w_j t_j over the chunk, t_j = (l_j -
 // max) c the base-2 exponent of w_j (the chunk's share of the row entropy;
 // -inf elements, whose weight is 0, add nothing).
-template <typename T, int VEC>
-__device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
-                                                float cc, int mask_local, float* ent = nullptr) {
+// `exclude(raw)` runs after the max: it overwrites the elements left out of
+// the sum with -inf (chunk_softmax: at most one, at chunk offset mask_local).
+template <typename T, int VEC, class Exclude>
+__device__ __forceinline__ float2 chunk_softmax_ex(
+    typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV], float cc, Exclude exclude,
+    float* ent = nullptr) {
   using L = Lane<T, VEC>;
   constexpr bool kPacked = sizeof(T) == 2 && VEC == 8;
   float lm = -INFINITY;
@@ -462,7 +470,7 @@ __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw
     if (ent) *ent = 0.f;
     return make_float2(cm == -INFINITY ? -INFINITY : qnan(), 0.f);
   }
-  if (mask_local >= 0) mask_element<T, VEC>(raw, mask_local);
+  exclude(raw);
   const float nb = -cm * cc;
   float s, et = 0.f;
   if constexpr (kPacked) {
@@ -501,6 +509,17 @@ __device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw
   }
   if (ent) *ent = warp_sum(et);
   return make_float2(cm, warp_sum(s));
+}
+
+template <typename T, int VEC>
+__device__ __forceinline__ float2 chunk_softmax(typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV],
+                                                float cc, int mask_local, float* ent = nullptr) {
+  return chunk_softmax_ex<T, VEC>(
+      raw, cc,
+      [mask_local](typename Lane<T, VEC>::Raw(&r)[Lane<T, VEC>::NV]) {
+        if (mask_local >= 0) mask_element<T, VEC>(r, mask_local);
+      },
+      ent);
 }
 
 // Argmax record of one chunk: {max, lowest global index attaining it} (index
@@ -603,6 +622,62 @@ __device__ __forceinline__ float combine_entropy(const float2* rec, const float*
     a += ex2(d) * fmaf(d, r.y, __ldcg(ent + c));
   }
   return warp_sum(a);
+}
+
+// ---------------------------------------------------------------------------
+// candidate trees in device memory
+// ---------------------------------------------------------------------------
+
+constexpr int kTreeMaxNodes = 256;  // candidate nodes per tree (the root excluded)
+
+// Request's parent array (parent of node n = 1..N at parent[n - 1]) into
+// s_par[0..N] (s_par[0] = 0) and every node's depth into s_depth, by pointer
+// jumping (s_anc is scratch): log2(N + 1) rounds of depth[n] += depth[anc[n]],
+// anc[n] = anc[anc[n]].  True when the array is a tree - every parent an
+// earlier node, so the links cannot cycle - of depth <= max_depth.  Called by
+// every thread of the CTA; the same data gives every CTA the same answer.
+__device__ __forceinline__ bool load_tree(const int* parent, int N, int max_depth, short* s_par,
+                                          short* s_depth, short* s_anc) {
+  constexpr int kPer = (kTreeMaxNodes + 1 + 127) / 128;  // nodes per thread (>= 128 threads)
+  int bad = 0;
+  for (int n = threadIdx.x; n <= N; n += blockDim.x) {
+    int pa = 0;
+    if (n > 0) {
+      pa = __ldg(parent + n - 1);
+      if (pa < 0 || pa >= n) {
+        bad = 1;
+        pa = 0;
+      }
+    }
+    s_par[n] = (short)pa;
+    s_anc[n] = (short)pa;
+    s_depth[n] = (short)(n > 0);
+  }
+  if (__syncthreads_or(bad)) return false;
+  for (int span = 1; span <= N; span <<= 1) {
+    short nd[kPer], na[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int n = threadIdx.x + i * (int)blockDim.x;
+      if (n <= N) {
+        const int a = s_anc[n];
+        nd[i] = (short)(s_depth[n] + s_depth[a]);
+        na[i] = s_anc[a];
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+      const int n = threadIdx.x + i * (int)blockDim.x;
+      if (n <= N) {
+        s_depth[n] = nd[i];
+        s_anc[n] = na[i];
+      }
+    }
+    __syncthreads();
+  }
+  for (int n = threadIdx.x; n <= N; n += blockDim.x) bad |= s_depth[n] > max_depth;
+  return !__syncthreads_or(bad);
 }
 
 }  // namespace sv

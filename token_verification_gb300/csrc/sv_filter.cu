@@ -17,8 +17,8 @@ namespace {
 // two rows are in flight per SM.
 //
 // With m known, the weights w = 2^((l - m) c) follow.  Candidates are the
-// elements within 2^-20 of the max's weight; every element above a candidate
-// is one.  One pass sums the row's mass, the mass outside the candidates,
+// elements within 2^-18 of the max's weight (kCandBits); every element above
+// a candidate is one.  One pass sums the row's mass, the mass outside the candidates,
 // marks the candidates and histograms them over distance levels (eighths of
 // a bit of weight below the max: a level is a range of values).  When the cut
 // must lie among the candidates - at least k of them for top-k; for top-p
@@ -67,7 +67,7 @@ __device__ __forceinline__ unsigned long long frac_of(unsigned long long total, 
   return (total >> 32) * p_q + (((total & 0xffffffffull) * p_q) >> 32);
 }
 
-// Distance levels: a candidate's weight exponent a = (l - m) c in [-20, 0]
+// Distance levels: a candidate's weight exponent a = (l - m) c in [-18, 0]
 // falls into level floor(-8 a), kept as digit 255 - level so that larger
 // values have larger digits, as key digits do.
 __device__ __forceinline__ int level_digit(float a) { return 255 - __float2int_rz(-8.f * a); }

@@ -268,13 +268,15 @@ __device__ int pick_in_runs(const float (&w)[kWarp], float frac, int base_j) {
 }
 
 // Draw from w_j = 2^((l_j - m) c) over one row (w = 0 at mask_x, at the
+// `nexcl` tokens of `excl` (the rejected candidates of a tree node), at the
 // tokens the grammar mask row `mrow` rules out and below the top-k / top-p
-// cut value) given the row's softmax chunk records: the crossing chunk from
-// the records, then one rescan of that chunk in its own frame.
+// cut value) given the row's softmax chunk records, which leave out the same
+// tokens: the crossing chunk from the records, then one rescan of that chunk
+// in its own frame.
 template <typename T, int VEC, bool kSharedRecords = false>
 __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V, float m, float cc,
                                  float u, int mask_x, const uint32_t* mrow, int mask_words,
-                                 float cut) {
+                                 float cut, const int* excl = nullptr, int nexcl = 0) {
   using L = Lane<T, VEC>;
   const int lane = lane_id();
   const float nb = -m * cc;
@@ -289,7 +291,11 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
     if (c < 0) return -1;
     float v[kWarp];
     load_run<T>(row, V, c, v);
-    const uint32_t a = run_allowed(v, mrow, mask_words, c, cut, mask_x);
+    uint32_t a = run_allowed(v, mrow, mask_words, c, cut, mask_x);
+    for (int k = 0; k < nexcl; ++k) {
+      const int xo = excl[k] - (c * kChunk + lane * kWarp);
+      if (xo >= 0 && xo < kWarp) a &= ~(1u << xo);
+    }
     const float nbc = -record(c).x * cc;
     float w[kWarp];
 #pragma unroll
@@ -322,7 +328,10 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
 #pragma unroll
       for (int e = 0; e < VEC; ++e) {
         float we = ex2(fmaf(L::get(raw[k], e), cc, nbc));
-        if (c * kChunk + tile_offset<VEC>(k, e, lane) == mask_x) we = 0.f;
+        const int j = c * kChunk + tile_offset<VEC>(k, e, lane);
+        if (j == mask_x) we = 0.f;
+        for (int q = 0; q < nexcl; ++q)
+          if (j == excl[q]) we = 0.f;
         w[k * VEC + e] = we;
         gsum[k] += we;
       }
@@ -541,6 +550,10 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   if (threadIdx.x == 0) s_resid.n = -1;
   pdl_wait();
   pdl_launch_dependents();
+  if (p.out_cut && leader)  // filtered calls: each row's cut value, NaN for rows not needed
+    for (int r = threadIdx.x; r < p.R; r += blockDim.x)
+      p.out_cut[(long long)b * p.R + r] =
+          row_needed(p, r, Kb) ? __ldcg(p.thr + (long long)b * p.R + r) : qnan();
   // issued before the row summaries so that its latency overlaps theirs
   const int timed_out = (leader && warp == 0) ? __ldcg(p.err) : 0;
   if (leader) {
@@ -888,7 +901,7 @@ constexpr size_t kTreeCacheLimit = 96 * 1024;  // records kept in shared memory 
 // together (rows of up to 64 chunks; wider rows one at a time); the records
 // go to `cache` (shared memory) when given.  Same arithmetic as
 // combine_softmax_records and combine_entropy.
-template <typename T>
+template <typename T, bool kEntropy>
 __device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum* srow,
                                     float2* cache) {
   const int lane = lane_id(), warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -896,8 +909,8 @@ __device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum*
   const float cc = p.cc;
   if (NC > 2 * kWarp) {
     for (int r = warp; r <= N; r += nw) {
-      const RowSum rs = summarise_row<kTypical, T>(p, b, r, N, -1,
-                                                   cache ? cache + (long long)r * NC : nullptr);
+      const RowSum rs = summarise_row<kEntropy ? kTypical : kTreeSample, T>(
+          p, b, r, N, -1, cache ? cache + (long long)r * NC : nullptr);
       if (lane == 0) srow[r] = rs;
     }
     return;
@@ -915,7 +928,7 @@ __device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum*
         const int c = lane + q * kWarp;
         const bool in = r <= N && c < NC;
         rc[j][q] = in ? __ldcg(p.rec + base + c) : make_float2(-INFINITY, 0.f);
-        ea[j][q] = in ? __ldcg(p.ent + base + c) : 0.f;
+        ea[j][q] = (kEntropy && in) ? __ldcg(p.ent + base + c) : 0.f;
       }
     }
 #pragma unroll
@@ -931,7 +944,7 @@ __device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum*
         for (int q = 0; q < 2; ++q) {
           const float2 rq = rc[j][q];
           sum += rq.y * ex2(fmaf(rq.x, cc, nb));
-          if (rq.y > 0.f) {
+          if (kEntropy && rq.y > 0.f) {
             const float d = (rq.x - m) * cc;
             a += ex2(d) * fmaf(d, rq.y, ea[j][q]);
           }
@@ -940,7 +953,7 @@ __device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum*
         a = warp_sum(a);
         rs.m = m;
         rs.s = sum;
-        if (sum > 0.f) rs.h = __logf(sum) - 0.6931471805599453f * a / sum;
+        if (kEntropy && sum > 0.f) rs.h = __logf(sum) - 0.6931471805599453f * a / sum;
       }
       if (cache) {
 #pragma unroll
@@ -952,53 +965,107 @@ __device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum*
   }
 }
 
+// The request's candidate tree into shared memory: parents and depths
+// (load_tree), tokens, and each node's token's logit in its parent's row,
+// read before kernel A finishes.  Returns the request's status so far
+// (kBadTree, kBadToken or 0).
+template <typename T>
+__device__ int load_candidates(const VerifyParams& p, const TreeCall& t, int b, short* s_par,
+                               short* s_depth, short* s_anc, int* s_tok, float* s_lx) {
+  const int N = t.N;
+  const bool tree_ok =
+      load_tree(t.parent + (long long)b * t.parent_stride, N, t.D1 - 1, s_par, s_depth, s_anc);
+  int bad = 0;
+  for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x) {
+    const int tok = __ldg(t.tokens + (long long)b * N + n - 1);
+    s_tok[n] = tok;
+    const bool ok = tok >= 0 && tok < p.V;
+    bad |= !ok;
+    s_lx[n] = (tree_ok && ok)
+                  ? load_logit(row_ptr<T>(p.target, (long long)b * (N + 1) + s_par[n], p.V), tok)
+                  : 0.f;
+  }
+  bad = __syncthreads_or(bad);
+  return !tree_ok ? kBadTree : (bad ? kBadToken : 0);
+}
+
+// Path and tokens of a finished walk (one warp): level k < d holds the
+// token of the path's node at level k + 1, level d the drawn token; -1 past
+// them (and everywhere for a request with a status).  The last request of
+// the call clears the workspace counters.
+__device__ void write_tree_result(const VerifyParams& p, const TreeCall& t, int b, int status,
+                                  int best, int d, int token, const short* s_par,
+                                  const int* s_tok) {
+  const int lane = lane_id();
+  for (int k = lane; k < t.D1; k += kWarp) {
+    int node = -1, tok = -1;
+    if (!status && k <= d) {
+      int a = best;  // the path's node at level k + 1 (best itself when k = d)
+      for (int up = d; up > k + 1; --up) a = s_par[a];
+      if (k < d) {
+        tok = s_tok[a];
+        node = s_par[a];
+      } else {
+        tok = token;
+        node = best;
+      }
+    }
+    if (t.out_path) t.out_path[(long long)b * t.D1 + k] = node;
+    t.out_tokens[(long long)b * t.D1 + k] = tok;
+  }
+  if (lane == 0) {
+    t.out_accept_len[b] = status ? 0 : d + 1;
+    if (t.out_status) t.out_status[b] = status;
+    if (atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
+      *p.err = 0;
+      *p.fin_ticket = 0;
+    }
+  }
+}
+
 template <typename T, int VEC>
 __global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const VerifyParams p,
-                                                                         const TreeTypical t) {
+                                                                         const TreeCall t) {
   extern __shared__ float2 s_cache[];
   __shared__ RowSum srow[kMaxTreeNodes + 1];
+  __shared__ short s_par[kMaxTreeNodes + 1], s_depth[kMaxTreeNodes + 1], s_anc[kMaxTreeNodes + 1];
+  __shared__ int s_tok[kMaxTreeNodes + 1];
+  __shared__ float s_lx[kMaxTreeNodes + 1];
   __shared__ unsigned char spass[kMaxTreeNodes + 1], sacc[kMaxTreeNodes + 1];
   __shared__ int s_best, s_status;
   const int b = blockIdx.x;
-  const int lane = lane_id(), warp = threadIdx.x >> 5;
+  const int warp = threadIdx.x >> 5;
   const int N = t.N;
   const bool cached = (size_t)(N + 1) * p.NC * sizeof(float2) <= kTreeCacheLimit;
-  // the tree tokens and each node's logit in its parent's row are inputs:
-  // read them before waiting for kernel A
-  int bad = 0, tok = 0;
-  float lp = 0.f;
-  const int n_mine = 1 + threadIdx.x;  // N <= 256 < the CTA's threads
-  if (n_mine <= N) {
-    tok = __ldg(t.tokens + (long long)b * N + n_mine - 1);
-    bad = tok < 0 || tok >= p.V;
-    if (!bad)
-      lp = load_logit(row_ptr<T>(p.target, (long long)b * (N + 1) + t.parent[n_mine], p.V), tok);
-  }
-  bad = __syncthreads_or(bad);
+  // the tree, its tokens and each node's logit in its parent's row are
+  // inputs: read them before waiting for kernel A
+  const int status_in = load_candidates<T>(p, t, b, s_par, s_depth, s_anc, s_tok, s_lx);
   pdl_wait();
   pdl_launch_dependents();
-  summarise_tree_rows<T>(p, b, N, srow, cached ? s_cache : nullptr);
+  summarise_tree_rows<T, true>(p, b, N, srow, cached ? s_cache : nullptr);
   __syncthreads();
-  if (n_mine <= N) {
-    const RowSum rp = srow[t.parent[n_mine]];
+  for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x) {
     unsigned char ok = 0;
-    if (!bad && is_finite(rp.m) && rp.s > 0.f) {
-      const float px = ex2(fmaf(lp, p.cc, -rp.m * p.cc)) / rp.s;
-      ok = px > fminf(p.eps, p.delta * __expf(-rp.h));
+    if (!status_in) {
+      const RowSum rp = srow[s_par[n]];
+      if (is_finite(rp.m) && rp.s > 0.f) {
+        const float px = ex2(fmaf(s_lx[n], p.cc, -rp.m * p.cc)) / rp.s;
+        ok = px > fminf(p.eps, p.delta * __expf(-rp.h));
+      }
     }
-    spass[n_mine] = ok;
+    spass[n] = ok;
   }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int status = bad ? kBadToken : (__ldcg(p.err) ? kTimeout : 0);
+    int status = status_in ? status_in : (__ldcg(p.err) ? kTimeout : 0);
     sacc[0] = 1;
     int best = 0;
     if (!status && !is_finite(srow[0].m)) status = kBadLogits;
     for (int n = 1; n <= N && !status; ++n) {
-      sacc[n] = sacc[t.parent[n]] && spass[n];
+      sacc[n] = sacc[s_par[n]] && spass[n];
       if (!sacc[n]) continue;
       if (!is_finite(srow[n].m)) status = kBadLogits;  // an accepted node's row is needed
-      if (t.depth[n] > t.depth[best]) best = n;
+      if (s_depth[n] > s_depth[best]) best = n;
     }
     s_best = best;
     s_status = status;
@@ -1018,43 +1085,126 @@ __global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const
                                                -INFINITY);
   }
   const int status = status0 ? status0 : (token < 0 ? kBadLogits : 0);
-  const int d = status ? -1 : t.depth[best];
-  // path and tokens, root first (one lane per level): level k < d holds the
-  // token of the path's node at level k + 1, level d the drawn token
-  for (int k = lane; k < t.D1; k += kWarp) {
-    int node = -1, tok = -1;
-    if (!status && k <= d) {
-      int a = best;  // the path's node at level k + 1 (best itself when k = d)
-      for (int up = d; up > k + 1; --up) a = t.parent[a];
-      if (k < d) {
-        tok = __ldg(t.tokens + (long long)b * N + a - 1);
-        node = t.parent[a];
-      } else {
-        tok = token;
-        node = best;
-      }
+  write_tree_result(p, t, b, status, best, status ? -1 : s_depth[best], token, s_par, s_tok);
+}
+
+// ---------------------------------------------------------------------------
+// lossless tree verification by rejection sampling (after kernel A over
+// every tree row, whose records leave each node's children tokens out)
+// ---------------------------------------------------------------------------
+
+// One CTA per request ("推测解码与 MTP" §10.4: EAGLE verified by rejection
+// sampling is lossless; candidate trees of §3.3 / §4.2).  Every candidate is
+// a one-hot draft of the distribution at its parent.  From the root, the
+// children of the current node are tested in increasing id: with the
+// row's weights w_j = 2^((l_j - m) c), child k (token x_k, not repeated
+// among the earlier children) is accepted iff u_k * W_k < w(x_k), where
+// W_k = S_excl + the weights of the distinct children tokens from k on - the
+// residual left after the earlier children were rejected, a sum of positive
+// terms (no cancellation); S_excl, the row's mass without its children's
+// tokens, comes straight from kernel A's records.  A repeated token has no
+// mass left and is rejected.  The first accepted child is emitted and the
+// walk moves to it; when none is (or at a leaf) one token is drawn from the
+// node's records, which are exactly the residual without the rejected
+// children, with uniforms[b, 0].
+constexpr int kTreeSampleThreads = 512;
+
+template <typename T, int VEC>
+__global__ void __launch_bounds__(kTreeSampleThreads) tree_sample_kernel(const VerifyParams p,
+                                                                        const TreeCall t) {
+  extern __shared__ float2 s_cache[];
+  __shared__ RowSum srow[kMaxTreeNodes + 1];
+  __shared__ short s_par[kMaxTreeNodes + 1], s_depth[kMaxTreeNodes + 1], s_anc[kMaxTreeNodes + 1];
+  __shared__ int s_tok[kMaxTreeNodes + 1];
+  __shared__ float s_lx[kMaxTreeNodes + 1], s_u[kMaxTreeNodes + 1];
+  __shared__ int s_kid[kMaxTreeNodes];
+  __shared__ float s_w[kMaxTreeNodes];
+  __shared__ int s_excl[kMaxTreeNodes];
+  const int b = blockIdx.x;
+  const int lane = lane_id(), warp = threadIdx.x >> 5;
+  const int N = t.N;
+  const bool cached = (size_t)(N + 1) * p.NC * sizeof(float2) <= kTreeCacheLimit;
+  const int status_in = load_candidates<T>(p, t, b, s_par, s_depth, s_anc, s_tok, s_lx);
+  for (int n = threadIdx.x; n <= N; n += blockDim.x)
+    s_u[n] = __ldg(t.uniforms + (long long)b * (N + 1) + n);
+  pdl_wait();
+  pdl_launch_dependents();
+  summarise_tree_rows<T, false>(p, b, N, srow, cached ? s_cache : nullptr);
+  __syncthreads();
+  if (warp != 0) return;
+  int status = status_in ? status_in : (__ldcg(p.err) ? kTimeout : 0);
+  int node = 0, nk_final = 0;
+  const float cc = p.cc;
+  while (!status) {
+    const RowSum rs = srow[node];
+    if (!is_finite(rs.m)) {
+      status = kBadLogits;
+      break;
     }
-    if (t.out_path) t.out_path[(long long)b * t.D1 + k] = node;
-    t.out_tokens[(long long)b * t.D1 + k] = tok;
-  }
-  if (lane == 0) {
-    t.out_accept_len[b] = status ? 0 : d + 1;
-    if (t.out_status) t.out_status[b] = status;
-    // the last request of the call clears the workspace counters
-    if (atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
-      *p.err = 0;
-      *p.fin_ticket = 0;
+    // the node's children in increasing id
+    int nk = 0;
+    for (int c0 = 1; c0 <= N; c0 += kWarp) {
+      const int c = c0 + lane;
+      const bool kid = c <= N && s_par[c] == node;
+      const unsigned m = __ballot_sync(0xffffffffu, kid);
+      if (kid) s_kid[nk + __popc(m & ((1u << lane) - 1u))] = c;
+      nk += __popc(m);
     }
+    __syncwarp();
+    // their tokens' weights, 0 for a token an earlier child already carries
+    for (int k = lane; k < nk; k += kWarp) {
+      const int c = s_kid[k], x = s_tok[c];
+      bool dup = false;
+      for (int j = 0; j < k && !dup; ++j) dup = s_tok[s_kid[j]] == x;
+      s_w[k] = dup ? 0.f : ex2(fmaf(s_lx[c], cc, -rs.m * cc));
+    }
+    __syncwarp();
+    // W_k = S_excl + sum_{j >= k} w_j (suffix sums, blocks from the last);
+    // the first child whose test passes is the accepted one
+    int acc = -1;
+    float carry = rs.s;
+    for (int k0 = ((nk - 1) / kWarp) * kWarp; k0 >= 0 && nk > 0; k0 -= kWarp) {
+      const int k = k0 + (kWarp - 1 - lane);  // lane 0 holds the block's last child
+      const float w = k < nk ? s_w[k] : 0.f;
+      const float suffix = warp_incl_scan(w);  // over this block's children from k on
+      const float Wk = carry + suffix;
+      const bool pass = k < nk && w > 0.f && s_u[s_kid[k]] * Wk < w;
+      const unsigned hit = __ballot_sync(0xffffffffu, pass);
+      if (hit) acc = k0 + (kWarp - 1 - (31 - __clz(hit)));  // the lowest child id of the block
+      carry += __shfl_sync(0xffffffffu, suffix, kWarp - 1);
+    }
+    if (acc < 0) {  // every child rejected, or a leaf: draw here
+      nk_final = nk;
+      break;
+    }
+    node = s_kid[acc];
   }
+  int token = -1;
+  if (!status) {
+    // the final node's children (all rejected) are left out of the draw,
+    // as they are of its records
+    for (int k = lane; k < nk_final; k += kWarp) s_excl[k] = s_tok[s_kid[k]];
+    __syncwarp();
+    const int* excl = s_excl;
+    const RowSum rf = srow[node];
+    const T* row = row_ptr<T>(p.target, (long long)b * (N + 1) + node, p.V);
+    token = cached ? draw_from_records<T, VEC, true>(row, s_cache + (long long)node * p.NC, p.NC,
+                                                     p.V, rf.m, cc, s_u[0], -1, nullptr, 0,
+                                                     -INFINITY, excl, nk_final)
+                   : draw_from_records<T, VEC>(row, p.rec + ((long long)b * (N + 1) + node) * p.NC,
+                                               p.NC, p.V, rf.m, cc, s_u[0], -1, nullptr, 0,
+                                               -INFINITY, excl, nk_final);
+    if (token < 0) status = kBadLogits;
+  }
+  write_tree_result(p, t, b, status, node, status ? -1 : s_depth[node], token, s_par, s_tok);
 }
 
 template <typename T, int VEC>
-cudaError_t launch_tree_typical_typed(const VerifyParams& p, const TreeTypical& t,
-                                      cudaStream_t s) {
+cudaError_t launch_tree_typical_typed(const VerifyParams& p, const TreeCall& t, cudaStream_t s) {
   cudaError_t err = launch_records(kTypical, sizeof(T) == 2 ? kBF16 : kF32, VEC > 1, p, s);
   if (err != cudaSuccess) return err;
   VerifyParams pc = p;
-  TreeTypical tc = t;
+  TreeCall tc = t;
   void* args[] = {&pc, &tc};
   const void* fn = reinterpret_cast<const void*>(tree_typical_kernel<T, VEC>);
   static PerDevice once;
@@ -1065,6 +1215,25 @@ cudaError_t launch_tree_typical_typed(const VerifyParams& p, const TreeTypical& 
   if (err != cudaSuccess) return err;
   const size_t cache = (size_t)(t.N + 1) * p.NC * sizeof(float2);
   return launch_pdl(fn, dim3(p.B), dim3(kTreeTypicalThreads), s, args,
+                    cache <= kTreeCacheLimit ? cache : 0);
+}
+
+template <typename T, int VEC>
+cudaError_t launch_tree_sample_typed(const VerifyParams& p, const TreeCall& t, cudaStream_t s) {
+  cudaError_t err = launch_records(kTreeSample, sizeof(T) == 2 ? kBF16 : kF32, VEC > 1, p, s);
+  if (err != cudaSuccess) return err;
+  VerifyParams pc = p;
+  TreeCall tc = t;
+  void* args[] = {&pc, &tc};
+  const void* fn = reinterpret_cast<const void*>(tree_sample_kernel<T, VEC>);
+  static PerDevice once;
+  err = per_device(once, nullptr, [&](int&) {
+    return cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kTreeCacheLimit);
+  });
+  if (err != cudaSuccess) return err;
+  const size_t cache = (size_t)(t.N + 1) * p.NC * sizeof(float2);
+  return launch_pdl(fn, dim3(p.B), dim3(kTreeSampleThreads), s, args,
                     cache <= kTreeCacheLimit ? cache : 0);
 }
 template <int MODE>
@@ -1082,13 +1251,22 @@ size_t fin_smem_bytes(const VerifyParams& p, bool dense) {
   return (p.fin_cache ? fin_cache_bytes(p) : 0) + (dense ? sizeof(float) * (size_t)p.NC : 0);
 }
 
-cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeTypical& t,
+cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeCall& t,
                                 cudaStream_t stream) {
   if (dtype == kBF16)
     return vec ? launch_tree_typical_typed<uint16_t, 8>(p, t, stream)
                : launch_tree_typical_typed<uint16_t, 1>(p, t, stream);
   return vec ? launch_tree_typical_typed<float, 4>(p, t, stream)
              : launch_tree_typical_typed<float, 1>(p, t, stream);
+}
+
+cudaError_t launch_tree_sample(int dtype, bool vec, const VerifyParams& p, const TreeCall& t,
+                               cudaStream_t stream) {
+  if (dtype == kBF16)
+    return vec ? launch_tree_sample_typed<uint16_t, 8>(p, t, stream)
+               : launch_tree_sample_typed<uint16_t, 1>(p, t, stream);
+  return vec ? launch_tree_sample_typed<float, 4>(p, t, stream)
+             : launch_tree_sample_typed<float, 1>(p, t, stream);
 }
 
 cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,

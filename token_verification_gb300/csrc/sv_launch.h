@@ -59,33 +59,42 @@ struct VerifyParams {
   int greedy_prob;   // greedy rule reached through the sampling entry
   int compact_in_finalize;  // the finalize kernel writes the packed output
   int fin_cache;     // the finalize kernel keeps the request's records in shared memory
+  float* out_cut;    // [B*R] filtered calls: each row's cut value (NaN: row not needed), or null
+  unsigned long long wait_ns;  // limit of the waits for staged logits (0: give up at once)
+  // tree sampling (kernel A leaves each node's children tokens out of its row's sums)
+  const int* tree_parent;  // request b's parents at tree_parent + b * parent_stride
+  int parent_stride;       // 0 (one tree for all requests) or N
+  const int* tree_tokens;  // [B, N]
 };
 
 constexpr int kMaxTreeNodes = 256;
 
+// Greedy tree walk.  The parent arrays live in device memory: request b's
+// at parent + b * parent_stride (parent of node n at index n - 1).
 struct TreeParams {
   const void* target;
+  const int* parent;  // [N] or [B, N]
+  int parent_stride;  // 0 or N
   const int* tokens;  // [B, N]
   int* out_tokens;
   int* out_accept_len;
   int* out_path;
   int* out_status;
   int B, N, V, D1, NC;
-  short first_child[kMaxTreeNodes + 1];  // 0 = none
-  short next_sibling[kMaxTreeNodes + 1];
 };
 
-// Candidate tree for typical acceptance (built on the host).
-struct TreeTypical {
+// Candidate tree of typical acceptance and of tree sampling (after kernel A
+// over every tree row).
+struct TreeCall {
+  const int* parent;      // [N] or [B, N] (device)
+  int parent_stride;      // 0 or N
   const int* tokens;      // [B, N] node n's token at n - 1
-  const float* uniforms;  // [B] the final draw
+  const float* uniforms;  // typical: [B] the final draw; sampling: [B, N+1]
   int* out_tokens;        // [B, D1]
   int* out_accept_len;    // [B]
   int* out_path;          // [B, D1] or null
   int* out_status;        // [B] or null
   int N, D1;
-  short parent[kMaxTreeNodes + 1];  // parent[n] for n >= 1
-  short depth[kMaxTreeNodes + 1];
 };
 
 enum Dtype : int { kF32 = 0, kBF16 = 1 };
@@ -114,6 +123,7 @@ constexpr int kFilterRowBytes = 512 * 1024;
 constexpr size_t kFinSmemMax = kFinCacheLimit + sizeof(float) * ((1 << 24) / kChunk);  // V <= 2^24
 
 // mode: 0 one-hot sampling, 1 dense sampling, 2 greedy, 3 typical acceptance
+// (4, tree sampling, runs through launch_tree_sample)
 cudaError_t launch_verify(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream);
 cudaError_t launch_tree(int dtype, bool vec, const TreeParams& p, cudaStream_t stream);
@@ -123,7 +133,12 @@ cudaError_t launch_records(int mode, int dtype, bool vec, const VerifyParams& p,
                            cudaStream_t stream);
 cudaError_t launch_filter(int mode, int dtype, bool vec, const VerifyParams& p,
                           cudaStream_t stream);
-cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeTypical& t,
+cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeCall& t,
                                 cudaStream_t stream);
+cudaError_t launch_tree_sample(int dtype, bool vec, const VerifyParams& p, const TreeCall& t,
+                               cudaStream_t stream);
+
+// The limit of the kernels' waits for staged logits (set through the C ABI).
+unsigned long long wait_limit_ns();
 
 }  // namespace sv

@@ -7,36 +7,23 @@
 // its scratch from one file-scope device array of SV_NOALLOC_SCRATCH_BYTES,
 // which every GPU that loads the library holds until the process exits.  It
 // calls no cudaMalloc, cudaFree or allocating library routine.
-#include <mutex>
-
 #include "../../include/spec_verify.h"
 #include "sv_launch.h"
 
 namespace {
 
 // The scratch.  In host code this name only stands for the array: its
-// device address comes from cudaGetSymbolAddress, once per device.
+// device address comes from cudaGetSymbolAddress, with the device current.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[SV_NOALLOC_SCRATCH_BYTES];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void* g_scratch_addr[kMaxDevices] = {};
-
-// Device address of the scratch on the current device (looked up on the
-// first call made with that device current).
+// Device address of the scratch on the current device, looked up on every
+// call: the lookup queues no work, and an address cached across calls would
+// go stale if a device reset made the runtime load the module again.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  void* ptr = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_mu);
-  if (!g_scratch_addr[dev]) {
-    void* ptr = nullptr;
-    err = cudaGetSymbolAddress(&ptr, g_noalloc_scratch);
-    if (err != cudaSuccess) return err;
-    g_scratch_addr[dev] = ptr;
-  }
-  *out = g_scratch_addr[dev];
+  *out = ptr;
   return cudaSuccess;
 }
 

@@ -66,6 +66,35 @@ __device__ __forceinline__ float2 chunk_record(typename Lane<T, VEC>::Raw (&raw)
   return chunk_softmax<T, VEC>(raw, cc, ml);
 }
 
+// Tree sampling: the record of chunk c of node r's row leaves out of its sum
+// the tokens of r's children - the candidates tested against that row, every
+// one of which is removed from the residual before the final draw - and
+// keeps them in its max.  Node n's parent and token (n = 1..N) are at index
+// n - 1 of the request's arrays.
+template <typename T, int VEC>
+__device__ __forceinline__ float2 tree_chunk_record(
+    const VerifyParams& p, typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV], int rowid, int c) {
+  using Raw = typename Lane<T, VEC>::Raw;
+  const int b = (int)fast_div((uint32_t)rowid, p.div_r);
+  const int r = rowid - b * p.R;
+  const int N = p.K;
+  const int* par = p.tree_parent + (long long)b * p.parent_stride;
+  const int* tok = p.tree_tokens + (long long)b * N;
+  const int lo = c * kChunk;
+  return chunk_softmax_ex<T, VEC>(raw, p.cc, [&](Raw(&rr)[Lane<T, VEC>::NV]) {
+    for (int n0 = 0; n0 < N; n0 += kWarp) {
+      const int n = n0 + lane_id();
+      int off = -1;
+      if (n < N && __ldg(par + n) == r) {
+        const int t = __ldg(tok + n) - lo;
+        if (t >= 0 && t < kChunk) off = t;
+      }
+      for (unsigned hit = __ballot_sync(0xffffffffu, off >= 0); hit; hit &= hit - 1u)
+        mask_element<T, VEC>(rr, __shfl_sync(0xffffffffu, off, __ffs(hit) - 1));
+    }
+  });
+}
+
 // If the row's draft token x lies in chunk c, the lane holding it records
 // the logit l_x for the finalize kernel (p(x) = 2^((l_x - m) c) / S).
 template <typename T, int VEC>

@@ -44,22 +44,43 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constan
   const int gw = rank * kTreeWarps + warp;
   const int W = CL * kTreeWarps;
 
-  __shared__ int s_tok[kMaxTreeNodes];
+  __shared__ int s_tok[kMaxTreeNodes + 1];
+  __shared__ short s_par[kMaxTreeNodes + 1], s_depth[kMaxTreeNodes + 1], s_anc[kMaxTreeNodes + 1];
+  __shared__ int s_kid[kMaxTreeNodes];
+  __shared__ int s_nkid;
   __shared__ float2 s_warp[kTreeWarps];
   __shared__ float2 s_cta[2];
   __shared__ int s_path[kMaxTreeNodes + 1];
   __shared__ int s_out[kMaxTreeNodes + 1];
 
+  // every CTA of the cluster loads the same tree and reaches the same verdict
+  const bool tree_ok = load_tree(p.parent + (long long)b * p.parent_stride, p.N, p.D1 - 1, s_par,
+                                 s_depth, s_anc);
   int bad = 0;
-  for (int n = threadIdx.x; n < p.N; n += blockDim.x) {
-    const int t = __ldg(p.tokens + (long long)b * p.N + n);
+  for (int n = 1 + threadIdx.x; n <= p.N; n += blockDim.x) {
+    const int t = __ldg(p.tokens + (long long)b * p.N + n - 1);
     s_tok[n] = t;
     bad |= (t < 0 || t >= p.V);
   }
   bad = __syncthreads_or(bad);
-  int status = bad ? kBadToken : 0;
+  int status = !tree_ok ? kBadTree : (bad ? kBadToken : 0);
   int node = 0, depth = 0, parity = 0;
   while (!status) {
+    __syncthreads();  // the previous step's reads of s_kid are done
+    // the current node's children, in increasing id (warp 0)
+    if (warp == 0) {
+      int nk = 0;
+      for (int c0 = 1; c0 <= p.N; c0 += kWarp) {
+        const int c = c0 + lane;
+        const bool kid = c <= p.N && s_par[c] == node;
+        const unsigned m = __ballot_sync(0xffffffffu, kid);
+        if (kid) s_kid[nk + __popc(m & ((1u << lane) - 1u))] = c;
+        nk += __popc(m);
+      }
+      if (lane == 0) s_nkid = nk;
+    }
+    __syncthreads();
+    const int nkid = s_nkid;
     const T* row = reinterpret_cast<const T*>(p.target) + ((long long)b * (p.N + 1) + node) * p.V;
     float2 best = make_float2(-INFINITY, __int_as_float(0x7fffffff));
     bool first = true;
@@ -68,9 +89,9 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constan
       load_chunk<T, VEC>(row, p.V, c, raw);
       if (PREFETCH && lane == 0) {
         const unsigned bytes = (unsigned)(min(kChunk, p.V - c * kChunk) * sizeof(T));
-        for (int ch = p.first_child[node]; ch; ch = p.next_sibling[ch])
+        for (int k = 0; k < nkid; ++k)
           prefetch_l2(reinterpret_cast<const T*>(p.target) +
-                          ((long long)b * (p.N + 1) + ch) * p.V + (long long)c * kChunk,
+                          ((long long)b * (p.N + 1) + s_kid[k]) * p.V + (long long)c * kChunk,
                       bytes);
       }
       const float2 r = chunk_argmax<T, VEC>(raw, c * kChunk);
@@ -98,10 +119,10 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constan
       s_out[depth] = a;
     }
     ++depth;
-    int next = 0;
-    for (int ch = p.first_child[node]; ch; ch = p.next_sibling[ch])
-      if (s_tok[ch - 1] == a) {
-        next = ch;
+    int next = 0;  // the lowest child carrying the argmax
+    for (int k = 0; k < nkid; ++k)
+      if (s_tok[s_kid[k]] == a) {
+        next = s_kid[k];
         break;
       }
     if (!next) break;

@@ -84,9 +84,13 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
       if (g < k.nch) {
         if (mrow) allow_only_chunk<T, VEC>(raw[g], word[g]);
         record_draft_logit<T, VEC>(p, raw[g], k.c0 + g, k.rowid, k.x);
-        const float2 out = chunk_record<MODE, T, VEC>(
-            raw[g], k.c0 + g, p.cc, MODE == kOneHot ? k.x : -1,
-            MODE == kTypical ? p.ent + (long long)k.rowid * p.NC + k.c0 + g : nullptr);
+        float2 out;
+        if constexpr (MODE == kTreeSample)
+          out = tree_chunk_record<T, VEC>(p, raw[g], k.rowid, k.c0 + g);
+        else
+          out = chunk_record<MODE, T, VEC>(
+              raw[g], k.c0 + g, p.cc, MODE == kOneHot ? k.x : -1,
+              MODE == kTypical ? p.ent + (long long)k.rowid * p.NC + k.c0 + g : nullptr);
         if (lane == 0) rec[k.c0 + g] = out;
       }
   }
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
     uint32_t k = 0;  // stages issued
     bool ok = true;
     auto acquire = [&](int s) {  // wait until stage s may be refilled
-      return k < (uint32_t)S || mbar_wait(empty_of(s), ((k / S) - 1) & 1u);
+      return k < (uint32_t)S || mbar_wait(empty_of(s), ((k / S) - 1) & 1u, p.wait_ns);
     };
     for (uint32_t it = lo; it < hi && ok; ++it) {
       const Item item = decode_item<MODE>(p, it);
@@ -269,14 +273,14 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
   const int w = warp - 1;  // consumer index: chunk w of every stage
   for (uint32_t k = 0;; ++k) {
     const int s = (int)(k % S);
-    const bool ok = __all_sync(0xffffffffu, mbar_wait(full_of(s), (k / S) & 1u));
+    const bool ok = __all_sync(0xffffffffu, mbar_wait(full_of(s), (k / S) & 1u, p.wait_ns));
     if (!ok) {  // the producer or a copy stopped: leave (the call reports a timeout)
       if (lane == 0) atomicOr(p.err, 1);
       break;
     }
     const int4 m = meta[s];
     if (m.x < 0) break;  // end marker
-    if (kMasked && w < m.z) {  // grammar-masked calls (a separate instantiation)
+    if (kMasked && MODE != kTreeSample && w < m.z) {  // grammar-masked calls (a separate instantiation)
       const int c = m.y + w;
       const uint32_t chunk = stage_of(s) + w * ST::kChunkBytes;
       float* ent = MODE == kTypical ? p.ent + (long long)m.x * p.NC + c : nullptr;
@@ -305,9 +309,13 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
       typename L::Raw raw[L::NV];
       load_chunk_smem<T, VEC>(stage_of(s) + w * ST::kChunkBytes, p.V, c, raw);
       record_draft_logit<T, VEC>(p, raw, c, m.x, m.w);
-      const float2 out = chunk_record<MODE, T, VEC>(
-          raw, c, p.cc, MODE == kOneHot ? m.w : -1,
-          MODE == kTypical ? p.ent + (long long)m.x * p.NC + c : nullptr);
+      float2 out;
+      if constexpr (MODE == kTreeSample)
+        out = tree_chunk_record<T, VEC>(p, raw, m.x, c);
+      else
+        out = chunk_record<MODE, T, VEC>(
+            raw, c, p.cc, MODE == kOneHot ? m.w : -1,
+            MODE == kTypical ? p.ent + (long long)m.x * p.NC + c : nullptr);
       if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
     }
     // this warp's values from the stage are consumed: hand it back
@@ -341,8 +349,9 @@ cudaError_t launch_records(const VerifyParams& p, cudaStream_t s) {
   } else if constexpr (VEC * sizeof(T) == 16) {
     constexpr int smem_max = Stream<T>::smem_bytes(true);
     const int smem = Stream<T>::smem_bytes(p.mask_bulk != 0);
-    const void* fn = p.mask ? reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC, true>)
-                            : reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC, false>);
+    const void* fn = reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC, false>);
+    if constexpr (MODE != kTreeSample)
+      if (p.mask) fn = reinterpret_cast<const void*>(verify_stream_kernel<MODE, T, VEC, true>);
     static PerDevice once[2];
     int occ = 1;
     err = per_device(once[p.mask ? 1 : 0], &occ, [&](int& v) {
@@ -412,6 +421,7 @@ cudaError_t launch_records(int mode, int dtype, bool vec, const VerifyParams& p,
     case kOneHot: return typed(std::integral_constant<int, kOneHot>());
     case kDense: return typed(std::integral_constant<int, kDense>());
     case kTypical: return typed(std::integral_constant<int, kTypical>());
+    case kTreeSample: return typed(std::integral_constant<int, kTreeSample>());
     default: return typed(std::integral_constant<int, kGreedy>());
   }
 }

@@ -42,7 +42,9 @@ use (Llama-3, Qwen, DeepSeek-V3 vocabularies; K = 1..5; batch up to 256);
 workload 5 is workload 2 under grammar masks, workload 6 the n-gram proposer
 that makes workload 2's kind of drafts, workload 7 workload 2 with top-p
 sampling, workloads 8 and 9 typical acceptance on workload 4's tree and on
-workload 2's chains.
+workload 2's chains, workload 10 lossless tree verification by rejection
+sampling on workload 4's tree (uniforms [B, N+1]: node n's test in column n,
+the final draw in column 0).
 """
 from __future__ import annotations
 
@@ -76,6 +78,9 @@ WORKLOADS = {
             dtype="bf16", sigma=0.5, tree="medusa60", T=1.0, eps=0.09, delta=0.3),
     9: dict(name="qwen-vocab-onehot-typical-B256-K5-V152064", kind="typical", B=256, K=5,
             V=152064, dtype="bf16", T=1.0, drafts="onehot", p_argmax=0.6, eps=0.09, delta=0.3),
+    # lossless tree verification by rejection sampling on workload 4's tree
+    10: dict(name="medusa-tree-sample-B32-N60-V32000", kind="tree_sample", B=32, V=32000,
+             dtype="bf16", sigma=0.5, tree="medusa60", T=1.0),
     # the n-gram proposer that makes workload 2's drafts (prompt_lookup_max 4, K 5)
     6: dict(name="ngram-propose-B256-L4096-V152064", kind="ngram", B=256, K=5, V=152064,
             L=4096, n_min=1, n_max=4),
@@ -335,11 +340,15 @@ def make_workload(index: int, seed: int = 0) -> Workload:
         wl = Workload(dtype="int32", B=w["B"], V=w["V"], target=np.empty(0, np.float32),
                       K=w["K"], history=ctx["tokens"], history_lens=ctx["lens"],
                       meta=dict(n_min=w["n_min"], n_max=w["n_max"], L=w["L"]))
-    elif w["kind"] in ("tree", "tree_typical"):
+    elif w["kind"] in ("tree", "tree_typical", "tree_sample"):
         wl = make_tree_case(w["B"], w["V"], medusa60_parent(), dtype=w["dtype"],
                             sigma=w["sigma"], seed=s)
         if w["kind"] == "tree_typical":  # one uniform per request for the final draw
             wl.uniforms = np.random.default_rng(int(s)).random(w["B"], dtype=np.float32)
+        if w["kind"] == "tree_sample":  # node n's test in column n, the final draw in column 0
+            wl.uniforms = np.random.default_rng(int(s)).random((w["B"], len(wl.parent) + 1),
+                                                              dtype=np.float32)
+            wl.T = w["T"]
     else:
         wl = make_sample_case(w["B"], w["K"], w["V"], dtype=w["dtype"], T=w["T"],
                               drafts=w["drafts"], sigma=w.get("sigma", 0.0),
