@@ -20,6 +20,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import re
 import statistics
@@ -91,6 +92,8 @@ def hbm_peak():
 
 
 def kernel_source_hash(kind="stream"):
+    if kind not in KERNEL_SOURCES:
+        return None
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kind]:
         with open(os.path.join(ROOT, rel), "rb") as f:
@@ -98,21 +101,26 @@ def kernel_source_hash(kind="stream"):
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(entry):
-    """DRAM bytes per launch recorded in profiles/<name>.md, if the profile
-    was taken on the current sources of its kernel (else None)."""
-    if not entry:
+def profiled_traffic(name):
+    """DRAM bytes per launch of the ncu capture `name` recorded in
+    profiles/traffic.json, if it was taken on the current sources of its
+    kernel (else None)."""
+    if not name:
         return None
-    name, kind = entry
-    path = os.path.join(ROOT, "profiles", name + ".md")
-    if not os.path.exists(path):
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)[name]
+    except (OSError, KeyError, ValueError):
         return None
-    txt = open(path).read()
-    m_hash = re.search(r"kernel_source_hash:\s*([0-9a-f]+)", txt)
-    m_bytes = re.search(r"dram_bytes_per_launch:\s*([0-9]+)", txt)
-    if not m_hash or not m_bytes or m_hash.group(1) != kernel_source_hash(kind):
+    if entry.get("kernel_source_hash") != kernel_source_hash(entry.get("kernel", "")):
         return None
-    return int(m_bytes.group(1))
+    return int(entry["dram_bytes_per_launch"])
+
+
+# the ncu capture (profiles/traffic.json) of each benchmarked (workload, mode)
+PROFILE_NAMES = {(2, "sample"): "verify_stream_onehot_B256_K5_V152064",
+                 (7, "sample"): "filter_rows_topp_B256_K5_V152064"}
 
 
 class ClockSampler:
@@ -218,30 +226,42 @@ def oracle_run(wl, mode, requests, threads):
     return time.perf_counter() - t0
 
 
-def cpu_baseline(wl, mode, budget_s=12.0):
-    threads = os.cpu_count() or 1
-    probe = min(wl.B, max(threads, 8))
+def _oracle_rate(wl, mode, threads, budget_s):
+    """Calls/s of the oracle with `threads` threads: the median of 3 timed
+    runs over a sample of requests sized to about budget_s / 3 each."""
+    probe = min(wl.B, max(threads, 2))
     per_req = oracle_run(wl, mode, probe, threads) / probe
-    reqs = min(wl.B, max(probe, int(budget_s / max(per_req, 1e-9))))
-    reps = max(1, min(400, int(budget_s / max(per_req * reqs, 1e-9)))) if reqs == wl.B else 1
-    total, done = 0.0, 0
-    for _ in range(reps):
-        total += oracle_run(wl, mode, reqs, threads)
-        done += reqs
-    return {"value": (done / wl.B) / total, "unit": "calls/s", "cores": threads, "kind": "oracle",
-            "sample": "%d requests of the B=%d batch (%.1f s of fp64 CPU work, %d threads)"
-                      % (done, wl.B, total, threads)}
+    reqs = min(wl.B, max(probe, int(budget_s / 3 / max(per_req, 1e-9))))
+    reps = max(1, min(200, int(budget_s / 3 / max(per_req * reqs, 1e-9)))) if reqs == wl.B else 1
+    rates = []
+    for _ in range(3):
+        t = sum(oracle_run(wl, mode, reqs, threads) for _ in range(reps))
+        rates.append((reps * reqs / wl.B) / t)
+    return statistics.median(rates), "%d x %d of the B=%d requests, median of 3" % (reps, reqs, wl.B)
 
 
-def load_workload(args, seed=0):
+def cpu_baseline(wl, mode, budget_s=12.0):
+    """The oracle on the host cores (all threads) and on one thread."""
+    threads = os.cpu_count() or 1
+    value, sample = _oracle_rate(wl, mode, threads, budget_s)
+    single, s_sample = _oracle_rate(wl, mode, 1, budget_s / 3)
+    return {"value": value, "unit": "calls/s", "cores": threads, "kind": "oracle",
+            "sample": sample + " (%d threads)" % threads,
+            "single_thread": {"value": single, "unit": "calls/s", "cores": 1,
+                              "sample": s_sample}}
+
+
+def load_workload(args, seed=0, index=None, greedy=None):
     from token_verification_gb300 import synth
-    wl = synth.make_workload(args.workload, seed=seed)
+    index = args.workload if index is None else index
+    greedy = args.greedy if greedy is None else greedy
+    wl = synth.make_workload(index, seed=seed)
     typical = wl.meta.get("typical", False)
     tree_kind = "tree_typical" if typical else (
         "tree_sample" if (wl.uniforms is not None and wl.uniforms.ndim == 2) else "tree")
     mode = ("propose" if wl.history is not None
             else tree_kind if wl.parent is not None
-            else "greedy" if args.greedy else "typical" if typical else "sample")
+            else "greedy" if greedy else "typical" if typical else "sample")
     if args.batch:  # a smaller batch of the same workload (profiling captures)
         wl.B = args.batch
         for name in ("target", "draft", "draft_tokens", "uniforms", "node_tokens", "token_mask",
@@ -258,25 +278,26 @@ def load_workload(args, seed=0):
 # ---------------------------------------------------------------------------
 
 def run_reference(args):
+    """The reference arm: the fp64 oracle on the host cores, each step one
+    whole call (every request of the batch)."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     wl, mode = load_workload(args)
     threads = os.cpu_count() or 1
-    req = min(args.ref_requests, wl.B)
     for _ in range(args.warmup):
-        oracle_run(wl, mode, req, threads)
+        oracle_run(wl, mode, wl.B, threads)
     t = 0.0
     for _ in range(args.steps):
-        t += oracle_run(wl, mode, req, threads)
-    value = (args.steps * req / wl.B) / t
+        t += oracle_run(wl, mode, wl.B, threads)
+    value = args.steps / t
     line = {"impl": "reference", "metric": metric_name(wl, mode, args), "value": value,
             "unit": "calls/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": 1e3 * t / args.steps, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": workload_config(wl, mode),
             "cpu_baseline": {"value": value, "unit": "calls/s", "cores": threads, "kind": "oracle",
-                             "sample": "%d of %d requests per step" % (req, wl.B)},
+                             "sample": "every step a whole call: all %d requests" % wl.B},
             "e2e": {"value": value, "unit": "calls/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -292,16 +313,37 @@ def metric_name(wl, mode, args):
         wl.meta["workload"], mode)
 
 
+L2_BYTES = 129 * 2**20  # GB300
+
+
+def input_bytes(wl, mode):
+    """Bytes of one input set (what a call reads from its inputs)."""
+    if mode == "propose":
+        return int(wl.history.nbytes)
+    total = wl.target.nbytes
+    if wl.draft is not None and mode == "sample":
+        total += wl.draft.nbytes
+    if wl.token_mask is not None:
+        total += wl.token_mask.nbytes
+    return int(total)
+
+
+def n_input_sets(set_bytes):
+    """Input sets to rotate through so that a set comes back only after more
+    than twice the L2's capacity of other inputs: 2 when a set is larger
+    than L2, else at least 4 (at most 4096)."""
+    if set_bytes > L2_BYTES:
+        return 2
+    return int(min(4096, max(4, 1 + math.ceil(2 * L2_BYTES / max(set_bytes, 1)))))
+
+
 def workload_config(wl, mode):
     cfg = {"workload": wl.meta["workload"], "mode": mode, "B": wl.B, "V": wl.V,
            "logits": wl.dtype, "parallelism": "dp%d" % dist_env()[0]}
     if mode == "propose":
         del cfg["logits"]
-        cfg.update(L=wl.meta["L"], K=wl.K, n_min=wl.meta["n_min"], n_max=wl.meta["n_max"],
-                   l2="inputs smaller than L2 (%d KB of contexts per call): 2 rotating input "
-                      "sets; the figure includes L2 reuse" % (wl.history.nbytes // 1024))
-        return cfg
-    if mode in ("tree", "tree_typical", "tree_sample"):
+        cfg.update(L=wl.meta["L"], K=wl.K, n_min=wl.meta["n_min"], n_max=wl.meta["n_max"])
+    elif mode in ("tree", "tree_typical", "tree_sample"):
         cfg.update(N=int(wl.parent.size), max_depth=wl.max_depth)
         if mode == "tree_typical":
             cfg.update(temperature=wl.T, eps=wl.eps, delta=wl.delta)
@@ -315,19 +357,20 @@ def workload_config(wl, mode):
             cfg.update(top_k=wl.top_k, top_p=wl.top_p)
         if mode == "typical":
             cfg.update(eps=wl.eps, delta=wl.delta)
-    total = wl.target.nbytes + (wl.draft.nbytes if (wl.draft is not None and mode == "sample") else 0)
-    cfg["l2"] = ("inputs larger than L2: %d MB of logits per call, 2 rotating input sets"
-                 % (total // 2**20) if total > 129 * 2**20 else
-                 "inputs smaller than L2 (%d KB per call): 2 rotating input sets; the figure "
-                 "includes L2 reuse" % (total // 1024))
+    nb, ns = input_bytes(wl, mode), n_input_sets(input_bytes(wl, mode))
+    cfg["l2"] = ("%s: %d rotating input sets of %.1f MB (a set returns after %.0f MB of other "
+                 "inputs, more than twice the %d MB L2)"
+                 % ("inputs larger than L2" if nb > L2_BYTES else "inputs smaller than L2", ns,
+                    nb / 2**20, (ns - 1) * nb / 2**20, L2_BYTES // 2**20))
     return cfg
 
 
 class Case:
-    """One workload resident on the device (two rotating input sets, the
-    second with its requests rotated by B/2) and the C-ABI call on it."""
+    """One workload resident on the device: `n_sets` input sets (copies,
+    the requests rotated), enough that a set is not in L2 when it comes
+    back, and the C-ABI call on them."""
 
-    def __init__(self, wl, mode, device):
+    def __init__(self, wl, mode, device, n_sets=None):
         import torch
         from token_verification_gb300 import api
         self.api, self.torch = api, torch
@@ -353,11 +396,14 @@ class Case:
                 if wl.draft is not None:
                     self.host["draft"] = to_t(wl.draft)
         B = wl.B
+        self.n_sets = n_input_sets(input_bytes(wl, mode)) if n_sets is None else n_sets
+        base = {k: v.to(device) for k, v in self.host.items()}
         self.sets = []
-        for s in range(2):
-            perm = torch.from_numpy(np.roll(np.arange(B), s * (B // 2)))
-            self.sets.append({k: (v if k == "parent" else v[perm]).contiguous().to(device)
-                              for k, v in self.host.items()})
+        for s in range(self.n_sets):
+            perm = torch.from_numpy(np.roll(np.arange(B), (s * max(1, B // 2)) % max(B, 1))).to(device)
+            self.sets.append({k: (v.clone() if k == "parent" else v[perm].contiguous())
+                              for k, v in base.items()})
+        del base
 
     def alloc(self, packed=True):
         if self.mode in ("tree", "tree_typical", "tree_sample", "propose"):
@@ -395,7 +441,7 @@ class Case:
                                       top_p=wl.top_p)
 
     def step(self, i, out):
-        return self.call(self.sets[i & 1], out)
+        return self.call(self.sets[i % self.n_sets], out)
 
     def results(self, out):
         """The call's per-request token rows and lengths (what a caller reads back)."""
@@ -403,7 +449,7 @@ class Case:
             return out.drafts, out.draft_lens
         return out.tokens, out.accept_len
 
-    def launches(self, packed):
+    def launches(self):
         if self.mode in ("tree", "propose"):
             return 1
         # stream, finalize (the residual draw and the packed output included)
@@ -429,22 +475,115 @@ class Case:
             "greedy" if self.mode == "greedy" else "one-hot", masked)
 
     def algorithmic_bytes(self, out):
-        """Logit bytes the method needs per call: every row once (sampling,
-        greedy), plus the grammar mask words when masked; the rows on the
-        accepted path (tree)."""
+        """Bytes the method needs per call: every needed logit once
+        (sampling, greedy), plus the grammar mask words when masked; the
+        rows on the accepted path (greedy tree); every candidate row (the
+        tree calls that reduce all rows); every context token (proposer)."""
         wl = self.wl
-        if self.mode == "propose":  # every context token once
+        if self.mode == "propose":
             return int(wl.history_lens.astype(np.int64).sum()) * 4
         esz = 2 if wl.dtype == "bf16" else 4
         if self.mode == "tree":
             rows = int(out.accept_len.sum().item())
             return rows * wl.V * esz
-        if self.mode in ("tree_typical", "tree_sample"):  # every candidate row once
+        if self.mode in ("tree_typical", "tree_sample"):
             return wl.B * (wl.parent.size + 1) * wl.V * esz
         rows = wl.B * (wl.K + 1) + (wl.B * wl.K if (self.mode == "sample" and wl.draft is not None)
                                      else 0)
         masks = 0 if wl.token_mask is None else wl.token_mask.nbytes
         return rows * wl.V * esz + masks
+
+
+class Replay:
+    """The case's calls captured in CUDA graphs of `per_graph` complete calls
+    each, call i on input set i % n_sets, enough graphs to go through every
+    set; replays cycle through the graphs.  A serving loop captures its
+    decode step the same way, so host-side launch work does not gate the
+    device."""
+
+    def __init__(self, case, per_graph, out, stream):
+        import torch
+        self.per_graph = per_graph
+        side = torch.cuda.Stream(case.device)
+        side.wait_stream(stream)
+        self.graphs = []
+        n_graphs = max(1, -(-case.n_sets // per_graph)) if case.n_sets > per_graph else 1
+        with torch.cuda.stream(side):
+            for i in range(3):  # this stream's workspace is set up outside the capture
+                out = case.step(i, out) or out
+            torch.cuda.synchronize()
+            for g in range(n_graphs):
+                graph = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(graph, stream=side):
+                    for i in range(per_graph):
+                        out = case.step(g * per_graph + i, out) or out
+                self.graphs.append(graph)
+        torch.cuda.synchronize()
+        self.out = out
+        self.next = 0
+
+    def replay(self, calls):
+        """Queue exactly `calls` calls (a multiple of per_graph)."""
+        for _ in range(calls // self.per_graph):
+            self.graphs[self.next].replay()
+            self.next = (self.next + 1) % len(self.graphs)
+
+
+def per_graph_for(steps, cap):
+    """The largest graph size up to `cap` that divides `steps`."""
+    return max(d for d in range(1, max(1, min(cap, steps)) + 1) if steps % d == 0)
+
+
+def timed_seconds(torch, stream, fn):
+    """Device time of the work `fn` queues on `stream` (CUDA events)."""
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / 1e3
+
+
+def measure_config(args, index, greedy, device, calls=1000, warmup=10, oracle_budget=4.0):
+    """One workload's row of the per-config record: calls/s over `calls`
+    graph-replayed calls (rotating input sets), the roofline fraction of its
+    algorithmic bytes, and the oracle on the host cores."""
+    import torch
+    wl, mode = load_workload(args, index=index, greedy=greedy)
+    case = Case(wl, mode, device)
+    out = case.alloc(packed=True)
+    stream = torch.cuda.current_stream(device)
+    for i in range(warmup):
+        out = case.step(i, out) or out
+    torch.cuda.synchronize()
+    rep = Replay(case, 100, out, stream)
+    rep.replay(100 * max(1, len(rep.graphs)))  # one pass over every set
+    sec = timed_seconds(torch, stream, lambda: rep.replay(calls))
+    out = rep.out
+    value = calls / sec
+    algo = case.algorithmic_bytes(out)
+    peak, _ = hbm_peak()
+    tok, lens = case.results(out)
+    row = {"workload": wl.meta["workload"], "mode": mode, "calls_per_s": value,
+           "us_per_call": 1e6 / value,
+           "draft_tokens_per_s": (value * wl.B * wl.K if mode in ("sample", "greedy", "typical")
+                                  else None),
+           "algorithmic_bytes": algo, "hbm_gbs": algo * value / 1e9,
+           "frac": algo * value / 1e9 / peak,
+           ("mean_draft_len" if mode == "propose" else "mean_accept_len"):
+               float(lens.float().mean().item()),
+           "input_sets": case.n_sets, "calls_timed": calls, "kernel": case.kernel_label()}
+    if not args.no_cpu_baseline:
+        row["cpu_baseline"] = cpu_baseline(wl, mode, budget_s=oracle_budget)
+    del rep, case, out
+    torch.cuda.empty_cache()
+    return row
+
+
+# every standard workload (the five of the brief first, then the extensions)
+PER_CONFIG = [(0, False), (1, False), (2, False), (3, False), (3, True), (4, False),
+              (5, False), (6, False), (7, False), (8, False), (9, False), (10, False)]
 
 
 def run_ours(args):
@@ -461,39 +600,21 @@ def run_ours(args):
     wl, mode = load_workload(args, seed=shard_seed(0, rank))
     case = Case(wl, mode, device)
     out = case.alloc(packed=True)
-    out_kernel = case.alloc(packed=False)
     stream = torch.cuda.current_stream(device)
 
     for i in range(args.warmup):
         out = case.step(i, out) or out
-    if out_kernel is None:  # the tree call has no packed output: same outputs
-        out_kernel = out
     torch.cuda.synchronize()
 
-    # The timed calls are replayed from a CUDA graph of `per_graph` calls (the
-    # two input sets alternating, every call complete), as a serving loop
-    # captures its decode step, so that host-side launch work does not gate
-    # the device; --no-graph launches every call from Python instead.
-    graph = None
+    # Exactly K calls are timed, replayed from CUDA graphs of `per_graph`
+    # complete calls each (--no-graph: one Python call per step).
     steps = args.steps
+    replay = None
     if not args.no_graph:
-        # the largest graph size up to --graph-calls that divides K: exactly K calls are timed
-        per_graph = max(d for d in range(1, max(1, min(args.graph_calls, args.steps)) + 1)
-                        if args.steps % d == 0)
-        side = torch.cuda.Stream(device)
-        side.wait_stream(stream)
-        with torch.cuda.stream(side):
-            for i in range(3):  # this stream's workspace is set up outside the capture
-                out = case.step(i, out) or out
-            torch.cuda.synchronize()
-            graph = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(graph, stream=side):
-                for i in range(per_graph):
-                    out = case.step(i, out) or out
+        replay = Replay(case, per_graph_for(steps, args.graph_calls), out, stream)
+        out = replay.out
+        replay.replay(replay.per_graph * len(replay.graphs))
         torch.cuda.synchronize()
-        graph.replay()
-        torch.cuda.synchronize()
-        replays = args.steps // per_graph
 
     sampler = ClockSampler(local) if rank == 0 else None
     if sampler:
@@ -505,9 +626,8 @@ def run_ours(args):
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     w0 = time.time()
     ev0.record(stream)
-    if graph is not None:
-        for _ in range(replays):
-            graph.replay()
+    if replay is not None:
+        replay.replay(steps)
     else:
         for i in range(steps):
             case.step(i, out)
@@ -523,18 +643,19 @@ def run_ours(args):
     mean_len = float(case.results(out)[1].float().mean().item())
     algo_bytes = case.algorithmic_bytes(out)
 
-    # the dominant kernels, timed per call without the packed output, with
-    # event pairs on the launching stream (see profiles/ for each kernel's
-    # share of the call)
-    kernel_iters = max(20, min(args.steps, 2000))
-    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(kernel_iters)]
-    for i in range(kernel_iters):
-        evs[i][0].record(stream)
-        out_kernel = case.step(i, out_kernel) or out_kernel
-        evs[i][1].record(stream)
-    torch.cuda.synchronize()
-    kern_ms = statistics.mean(a.elapsed_time(b) for a, b in evs)
+    # The roofline: the call's average duration over a longer window of the
+    # same replay (CUDA events on the launching stream), every call complete
+    # (the dominant kernel and the small per-request one), so the fraction
+    # is a lower bound for the dominant kernel alone.
+    roof_calls = 0
+    if replay is not None:
+        roof = Replay(case, 100, out, stream)
+        roof.replay(100 * len(roof.graphs))
+        roof_calls = 100 * max(10, len(roof.graphs))
+        call_s = timed_seconds(torch, stream, lambda: roof.replay(roof_calls)) / roof_calls
+        del roof
+    else:
+        call_s = elapsed / steps
     if sampler:
         sampler.stop()
 
@@ -558,14 +679,7 @@ def run_ours(args):
 
         for _ in range(2):
             e2e_step()
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
-        b.record(stream)
-        torch.cuda.synchronize()
-        e2e_s = a.elapsed_time(b) / 1e3
+        e2e_s = timed_seconds(torch, stream, lambda: [e2e_step() for _ in range(e2e_steps)])
         h2d = sum(v.numel() * v.element_size() for v in pin.values())
         d2h = res_tok.numel() * 4 + res_len.numel() * 4
         e2e = {"value": e2e_steps / e2e_s, "unit": "calls/s", "h2d_bytes_per_step": h2d,
@@ -573,7 +687,7 @@ def run_ours(args):
 
     if rank == 0:
         peak, peak_kind = hbm_peak()
-        achieved = algo_bytes / (kern_ms / 1e3) / 1e9
+        achieved = algo_bytes / call_s / 1e9
         value = total_calls / max_elapsed
         line = {
             "metric": metric_name(wl, mode, args), "value": value, "unit": "calls/s",
@@ -582,32 +696,39 @@ def run_ours(args):
             "ms_per_step": 1e3 * max_elapsed / steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
             "config": workload_config(wl, mode),
-            "draft_tokens_per_s": (None if mode in ("tree", "tree_typical", "tree_sample", "propose")
-                                   else value * wl.B * wl.K),
+            "draft_tokens_per_s": (value * wl.B * wl.K if mode in ("sample", "greedy", "typical")
+                                   else None),
             "hbm_gbs": algo_bytes * value / 1e9,
             ("mean_draft_len" if mode == "propose" else "mean_accept_len"): mean_len,
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                          "frac": achieved / peak, "peak_source": peak_kind,
-                         "kernel": case.kernel_label(), "kernel_ms": kern_ms,
+                         "kernel": case.kernel_label(), "call_ms": call_s * 1e3,
+                         "calls_timed": roof_calls or steps,
                          "algorithmic_bytes": algo_bytes,
                          "traffic": profiled_traffic(PROFILE_NAMES.get((args.workload, mode)))},
-            "gpu_launches": steps * case.launches(True),
-            "launch": ("CUDA graph of %d calls, replayed" % per_graph) if graph is not None
+            "gpu_launches": steps * case.launches(),
+            "launch": ("CUDA graphs of %d calls, replayed" % replay.per_graph) if replay
                       else "one Python call per step",
             "clocks": sampler.summary() if sampler else None,
             "e2e": e2e,
         }
         if not args.no_cpu_baseline and world == 1:
             line["cpu_baseline"] = cpu_baseline(wl, mode)
+        if world == 1 and not args.no_per_config and args.workload == 2 and not args.batch:
+            del case, out, replay
+            torch.cuda.empty_cache()
+            rows = {}
+            for index, greedy in PER_CONFIG:
+                key = "%d%s" % (index, "-greedy" if greedy else "")
+                try:
+                    rows[key] = measure_config(args, index, greedy, device)
+                except Exception as e:  # a failure is reported, not hidden
+                    rows[key] = {"error": "%s: %s" % (type(e).__name__, e)}
+            line["per_config"] = rows
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
-
-
-# ncu summaries under profiles/ that record DRAM traffic per launch
-PROFILE_NAMES = {(2, "sample"): ("verify_stream_onehot_B256_K5_V152064", "stream"),
-                 (7, "sample"): ("filter_rows_topp_B256_K5_V152064", "filter")}
 
 
 def main(argv=None):
@@ -618,9 +739,10 @@ def main(argv=None):
     ap.add_argument("--workload", type=int, default=2)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=200)
-    ap.add_argument("--ref-requests", type=int, default=8)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the per-config record of every standard workload")
     ap.add_argument("--batch", type=int, default=0,
                     help="use only the first BATCH requests (small profiling cases)")
     ap.add_argument("--no-graph", action="store_true",

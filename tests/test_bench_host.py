@@ -88,12 +88,17 @@ def test_reference_arm_greedy_and_tree_modes():
 
 
 def test_profiled_traffic_follows_its_kernel_sources(tmp_path, monkeypatch):
-    """A profile's DRAM bytes are reported only while the sources of the
-    kernel it was taken on are unchanged (each profiled kernel has its own
-    source list); the committed profiles name kernels the bench knows."""
-    for (workload, mode), (name, kind) in bench.PROFILE_NAMES.items():
-        assert kind in bench.KERNEL_SOURCES
-        assert os.path.exists(os.path.join(ROOT, "profiles", name + ".md")), name
+    """A profile's DRAM bytes (profiles/traffic.json) are reported only while
+    the sources of the kernel it was taken on are unchanged (each profiled
+    kernel has its own source list); the committed entries name kernels the
+    bench knows and summaries that exist."""
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        committed = json.load(f)
+    for (workload, mode), name in bench.PROFILE_NAMES.items():
+        assert name in committed
+    for name, entry in committed.items():
+        assert entry["kernel"] in bench.KERNEL_SOURCES
+        assert os.path.exists(os.path.join(ROOT, entry["summary"])), name
     prof = tmp_path / "profiles"
     prof.mkdir()
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
@@ -104,9 +109,22 @@ def test_profiled_traffic_follows_its_kernel_sources(tmp_path, monkeypatch):
             src.write_text("// %s\n" % rel)
     h = bench.kernel_source_hash("filter")
     assert h != bench.kernel_source_hash("stream")
-    (prof / "p.md").write_text("kernel_source_hash: %s\ndram_bytes_per_launch: 1234\n" % h)
-    assert bench.profiled_traffic(("p", "filter")) == 1234
-    assert bench.profiled_traffic(("p", "stream")) is None  # another kernel's sources
+    (prof / "traffic.json").write_text(json.dumps(
+        {"p": {"kernel": "filter", "kernel_source_hash": h, "dram_bytes_per_launch": 1234},
+         "q": {"kernel": "stream", "kernel_source_hash": h, "dram_bytes_per_launch": 99}}))
+    assert bench.profiled_traffic("p") == 1234
+    assert bench.profiled_traffic("q") is None  # another kernel's sources
     (tmp_path / bench.KERNEL_SOURCES["filter"][0]).write_text("// changed\n")
-    assert bench.profiled_traffic(("p", "filter")) is None  # the kernel changed since
-    assert bench.profiled_traffic(None) is None
+    assert bench.profiled_traffic("p") is None  # the kernel changed since
+    assert bench.profiled_traffic(None) is None and bench.profiled_traffic("nope") is None
+
+
+def test_input_sets_exceed_l2():
+    """Rotating input sets: a set comes back only after more than twice the
+    L2 of other inputs (2 sets when one is larger than L2, else at least 4)."""
+    for nbytes in (114688, 99 * 2**20, 115 * 2**20, 124928000, 467140608):
+        n = bench.n_input_sets(nbytes)
+        assert n >= 2 and (nbytes > bench.L2_BYTES or n >= 4)
+        assert (n - 1) * nbytes >= (2 * bench.L2_BYTES if nbytes <= bench.L2_BYTES else nbytes)
+    assert bench.per_graph_for(20, 100) == 20 and bench.per_graph_for(20000, 100) == 100
+    assert bench.per_graph_for(7, 100) == 7 and bench.per_graph_for(101, 100) == 1
