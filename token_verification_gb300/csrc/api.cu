@@ -17,14 +17,19 @@ namespace sv {
 
 static size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// The region that must hold zeros when a call starts (the error flag and
-// the finalize ticket) comes first; every call leaves it zero again.
+// The region that must hold zeros when a call starts (the error flag, the
+// finalize ticket, the streaming kernel's work counter and the dense-draft
+// residual's counters) comes first; every call leaves it zero again.
 static WorkspaceLayout layout_for(int B, int R, int V) {
   const size_t NC = ((size_t)V + kChunk - 1) / kChunk;
   WorkspaceLayout l;
   size_t o = 0;
-  l.counters = o;   o = align256(o + 2 * sizeof(int));
+  l.counters = o;   o += 8 * sizeof(int);
+  l.arrive = o;     o = align256(o + sizeof(int) * (size_t)B);
   l.zero_bytes = o;
+  l.pend = o;       o = align256(o + 2 * sizeof(int) * (size_t)B);
+  l.rpar = o;       o = align256(o + sizeof(float4) * (size_t)B);
+  l.rsums = o;      o = align256(o + sizeof(float) * (size_t)B * NC);
   l.rec = o;        o = align256(o + sizeof(float2) * (size_t)B * R * NC);
   l.lx = o;         o = align256(o + sizeof(float) * (size_t)B * R);
   l.thr = o;        o = align256(o + sizeof(float) * (size_t)B * R);
@@ -140,6 +145,14 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   char* base = static_cast<char*>(ws);
   p.err = reinterpret_cast<int*>(base + l.counters);
   p.fin_ticket = p.err + 1;
+  p.work = reinterpret_cast<unsigned*>(p.err + 2);
+  p.n_pend = p.err + 3;
+  p.r_exit = p.err + 4;
+  p.arrive = reinterpret_cast<int*>(base + l.arrive);
+  p.pend = reinterpret_cast<int*>(base + l.pend);
+  p.rpn = p.pend + B;
+  p.rpar = reinterpret_cast<float4*>(base + l.rpar);
+  p.rsums = reinterpret_cast<float*>(base + l.rsums);
   p.rec = reinterpret_cast<float2*>(base + l.rec);
   p.lx = reinterpret_cast<float*>(base + l.lx);
   p.thr = reinterpret_cast<float*>(base + l.thr);
@@ -307,6 +320,14 @@ static sv_status tree_rows_call(int mode, const void* target, const int32_t* tre
   char* base = static_cast<char*>(workspace);
   p.err = reinterpret_cast<int*>(base + l.counters);
   p.fin_ticket = p.err + 1;
+  p.work = reinterpret_cast<unsigned*>(p.err + 2);
+  p.n_pend = p.err + 3;
+  p.r_exit = p.err + 4;
+  p.arrive = reinterpret_cast<int*>(base + l.arrive);
+  p.pend = reinterpret_cast<int*>(base + l.pend);
+  p.rpn = p.pend + B;
+  p.rpar = reinterpret_cast<float4*>(base + l.rpar);
+  p.rsums = reinterpret_cast<float*>(base + l.rsums);
   p.rec = reinterpret_cast<float2*>(base + l.rec);
   p.lx = reinterpret_cast<float*>(base + l.lx);
   p.thr = reinterpret_cast<float*>(base + l.thr);

@@ -194,6 +194,24 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
           "r"(dst), "l"(src), "r"(bytes), "r"(bar)
       : "memory");
 }
+// An L2 cache policy that makes the lines it brings in the first to be
+// evicted: a single streaming pass over the logits then leaves in L2 what
+// the later kernels of the call need (their code, the chunk records, the
+// counters) instead of data it will never read again.
+__device__ __forceinline__ unsigned long long l2_evict_first_policy() {
+  unsigned long long pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+// A bulk copy like bulk_copy below, with an L2 cache policy.
+__device__ __forceinline__ void bulk_copy_hint(uint32_t dst, const void* src, uint32_t bytes,
+                                               uint32_t bar, unsigned long long pol) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(pol)
+      : "memory");
+}
 // One arrival that also announces `bytes` of copies, and a copy that only
 // completes bytes (for several copies signalling one barrier phase).
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {

@@ -13,14 +13,15 @@
 //   records, draws beside each row's summary the token its position would
 //   draw (the crossing chunk from the records, then one rescan of that single
 //   chunk), and runs the acceptance tests of all positions at once (one lane
-//   per position).  With dense drafts a request rejected at n first needs the
-//   chunk sums of max(0, p_n - q_n): a cluster of CTAs per request reads the
-//   (target, draft) row pair once for them, writing into the first CTA's
-//   shared memory, whose warp 0 then draws the token.  The last CTA of the
-//   call writes the padding-free packed output (exclusive scan of
-//   accept_len, packed tokens, per-token batch ids).  F starts with
-//   programmatic dependent launch and waits on the device for kernel A's
-//   records.  Typical acceptance on candidate trees has its own kernel here.
+//   per position).  The last CTA of the call writes the padding-free packed
+//   output (exclusive scan of accept_len, packed tokens, per-token batch
+//   ids).  F starts with programmatic dependent launch and waits on the
+//   device for kernel A's records.
+// Kernel R (dense drafts only) follows F: a request rejected at n needs the
+//   chunk sums of max(0, p_n - q_n), one more pass over its (target, draft)
+//   row pair; F publishes those requests, R spreads their row pairs over
+//   every warp of the GPU, draws their tokens and writes the packed output.  Typical acceptance and rejection sampling on candidate
+//   trees have their own finalize kernels here.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -185,34 +186,42 @@ __device__ int find_chunk_runs(F weight, int NC, float u, float* frac) {
   return c;
 }
 
-// Elements 32*lane .. 32*lane+31 of chunk c, widened to fp32 (-inf past V).
+// Elements 32*lane .. 32*lane+31 of chunk c as stored (-inf past V): four
+// 128-bit words of bf16 pairs, or eight of fp32; get(e) widens element e.
 template <typename T>
-__device__ __forceinline__ void load_run(const T* row, int V, int c, float (&v)[kWarp]) {
-  constexpr int E = 16 / sizeof(T);
+struct Run {
+  static constexpr int E = 16 / (int)sizeof(T);  // elements per 128-bit word
+  uint4 q[kWarp / E];
+  __device__ __forceinline__ float get(int e) const {
+    const uint4 w = q[e / E];
+    const int i = e % E;
+    if constexpr (sizeof(T) == 2) {
+      const uint32_t pr = (i >> 1) == 0 ? w.x : (i >> 1) == 1 ? w.y : (i >> 1) == 2 ? w.z : w.w;
+      return __uint_as_float((i & 1) ? (pr & 0xffff0000u) : (pr << 16));
+    } else {
+      return __uint_as_float(i == 0 ? w.x : i == 1 ? w.y : i == 2 ? w.z : w.w);
+    }
+  }
+};
+
+template <typename T>
+__device__ __forceinline__ void load_run(const T* row, int V, int c, Run<T>& r) {
+  constexpr int E = Run<T>::E;
   const int j0 = c * kChunk + lane_id() * kWarp;
+  const uint4 pad = sizeof(T) == 2 ? make_uint4(0xff80ff80u, 0xff80ff80u, 0xff80ff80u, 0xff80ff80u)
+                                   : make_uint4(0xff800000u, 0xff800000u, 0xff800000u, 0xff800000u);
 #pragma unroll
   for (int g = 0; g < kWarp / E; ++g) {
-    const int j = j0 + g * E;
-    uint4 q = make_uint4(0u, 0u, 0u, 0u);
-    const bool in = j < V;  // V is a multiple of E on the vector paths
-    if (in) q = __ldg(reinterpret_cast<const uint4*>(row + j));
-    const uint32_t wds[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int e = 0; e < E; ++e) {
-      float x;
-      if constexpr (sizeof(T) == 2)
-        x = __uint_as_float((e & 1) ? (wds[e >> 1] & 0xffff0000u) : (wds[e >> 1] << 16));
-      else
-        x = __uint_as_float(wds[e]);
-      v[g * E + e] = in ? x : -INFINITY;
-    }
+    const int j = j0 + g * E;  // V is a multiple of E on the vector paths
+    r.q[g] = j < V ? __ldg(reinterpret_cast<const uint4*>(row + j)) : pad;
   }
 }
 
 // Which of this lane's 32 elements of chunk c are allowed: the grammar mask
 // word (one word covers exactly the lane's run), the top-k / top-p cut and
 // the excluded token x.
-__device__ __forceinline__ uint32_t run_allowed(const float (&v)[kWarp], const uint32_t* mrow,
+template <typename T>
+__device__ __forceinline__ uint32_t run_allowed(const Run<T>& v, const uint32_t* mrow,
                                                 int mask_words, int c, float cut, int x) {
   const int lane = lane_id();
   uint32_t a = 0xffffffffu;
@@ -220,7 +229,7 @@ __device__ __forceinline__ uint32_t run_allowed(const float (&v)[kWarp], const u
   if (cut > -INFINITY) {
 #pragma unroll
     for (int e = 0; e < kWarp; ++e)
-      if (!(v[e] >= cut)) a &= ~(1u << e);
+      if (!(v.get(e) >= cut)) a &= ~(1u << e);
   }
   const int xo = x - (c * kChunk + lane * kWarp);
   if (xo >= 0 && xo < kWarp) a &= ~(1u << xo);
@@ -228,13 +237,16 @@ __device__ __forceinline__ uint32_t run_allowed(const float (&v)[kWarp], const u
 }
 
 // Smallest element whose cumulative weight (in index order) exceeds frac
-// times the chunk total, over the lanes' runs of weights w; zero weights are
-// never chosen; the last positive element if rounding leaves none.
-__device__ int pick_in_runs(const float (&w)[kWarp], float frac, int base_j) {
+// times the chunk total, over the lanes' runs of weights weight(e) (element
+// e of this lane's run, recomputed from registers rather than stored); zero
+// weights are never chosen; the last positive element if rounding leaves
+// none.
+template <class Wt>
+__device__ int pick_in_runs(Wt weight, float frac, int base_j) {
   const int lane = lane_id();
   float s = 0.f;
 #pragma unroll
-  for (int e = 0; e < kWarp; ++e) s += w[e];
+  for (int e = 0; e < kWarp; ++e) s += weight(e);
   const float incl = warp_incl_scan(s);
   const float thr = frac * __shfl_sync(0xffffffffu, incl, kWarp - 1);
   const unsigned hit = __ballot_sync(0xffffffffu, s > 0.f && incl > thr);
@@ -246,8 +258,9 @@ __device__ int pick_in_runs(const float (&w)[kWarp], float frac, int base_j) {
       int last = -1;
 #pragma unroll
       for (int e = 0; e < kWarp; ++e) {
-        acc += w[e];
-        if (w[e] > 0.f) {
+        const float we = weight(e);
+        acc += we;
+        if (we > 0.f) {
           last = e;
           if (t < 0 && acc > thr) t = e;
         }
@@ -261,7 +274,7 @@ __device__ int pick_in_runs(const float (&w)[kWarp], float frac, int base_j) {
     if (lane == l)
 #pragma unroll
       for (int e = 0; e < kWarp; ++e)
-        if (w[e] > 0.f) t = e;
+        if (weight(e) > 0.f) t = e;
   }
   t = __shfl_sync(0xffffffffu, t, l);
   return base_j + l * kWarp + t;
@@ -289,18 +302,17 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
     float frac = 0.f;
     const int c = find_chunk_runs(weight, NC, u, &frac);
     if (c < 0) return -1;
-    float v[kWarp];
+    Run<T> v;
     load_run<T>(row, V, c, v);
-    uint32_t a = run_allowed(v, mrow, mask_words, c, cut, mask_x);
+    uint32_t a = run_allowed<T>(v, mrow, mask_words, c, cut, mask_x);
     for (int k = 0; k < nexcl; ++k) {
       const int xo = excl[k] - (c * kChunk + lane * kWarp);
       if (xo >= 0 && xo < kWarp) a &= ~(1u << xo);
     }
     const float nbc = -record(c).x * cc;
-    float w[kWarp];
-#pragma unroll
-    for (int e = 0; e < kWarp; ++e) w[e] = ((a >> e) & 1u) ? ex2(fmaf(v[e], cc, nbc)) : 0.f;
-    return pick_in_runs(w, frac, c * kChunk);
+    return pick_in_runs(
+        [&](int e) { return ((a >> e) & 1u) ? ex2(fmaf(v.get(e), cc, nbc)) : 0.f; }, frac,
+        c * kChunk);
   } else {
     float wc[kRecCache];  // one batch of loads for the first 256 chunks
     float tot = 0.f;
@@ -450,8 +462,7 @@ __device__ RowSum summarise_row(const VerifyParams& p, int b, int r, int Kb, int
   return rs;
 }
 
-// Threads of a finalize CTA: 8 warps (dense drafts: at 128 registers, two
-// CTAs per SM, so a request's residual cluster spans more SMs).
+// Threads of a finalize CTA: 8 warps.
 template <int MODE>
 __host__ __device__ constexpr int fin_threads() { return 256; }
 constexpr int kMaxRows = 2 * kMaxK + 1;
@@ -467,10 +478,7 @@ template <int MODE, typename T, int VEC>
 __device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const int* s_tok, int x,
                                               float u, int timed_out, Residual* resid);
-template <typename T, int VEC>
-__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
-                                           float* sums, int rank, int ncta);
-template <typename T, int VEC>
+template <typename T, int VEC, bool kGlobalSums = false>
 __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const Residual& st,
                                            const float* sums, const float2* srec);
 
@@ -512,10 +520,8 @@ __device__ __forceinline__ int position_draw(const VerifyParams& p, int b, int r
 // fit) for the draws.  Then one warp runs the acceptance tests of all
 // positions at once (one lane per position) and takes the stopping
 // position's token, or the argmax (greedy).  Dynamic shared memory: [R*NC]
-// records when cached, then [NC] residual chunk sums (dense drafts).  Dense
-// calls may run a cluster of CTAs per request: the first one does all of the
-// above and writes the outputs; the others only help to read the rejected
-// row pair.
+// records when cached.  A dense-draft request rejected at n is published for
+// kernel R, which writes its outputs.
 template <int MODE, typename T, int VEC>
 __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const VerifyParams p) {
   constexpr int kWarps = fin_threads<MODE>() / kWarp;
@@ -524,18 +530,10 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   __shared__ Residual s_resid;
   __shared__ int s_last[32];
   __shared__ int s_tok[kMaxRows];  // the token each position would draw
-  int ncta = 1, rank = 0;
-  if (MODE == kDense) {
-    const cg::cluster_group cluster = cg::this_cluster();
-    ncta = (int)cluster.num_blocks();
-    rank = (int)cluster.block_rank();
-  }
-  const int b = blockIdx.x / ncta;
-  const bool leader = rank == 0;
+  const int b = blockIdx.x;
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const int K = p.K;
   float2* s_rec = p.fin_cache ? s_dyn : nullptr;
-  float* s_sums = reinterpret_cast<float*>(s_dyn + (p.fin_cache ? (long long)p.R * p.NC : 0));
   // The request's inputs do not depend on kernel A: read them before waiting.
   const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
   const int Kv = (Kb >= 0 && Kb <= K) ? Kb : 0;
@@ -550,62 +548,48 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   if (threadIdx.x == 0) s_resid.n = -1;
   pdl_wait();
   pdl_launch_dependents();
-  if (p.out_cut && leader)  // filtered calls: each row's cut value, NaN for rows not needed
+  if (p.out_cut)  // filtered calls: each row's cut value, NaN for rows not needed
     for (int r = threadIdx.x; r < p.R; r += blockDim.x)
       p.out_cut[(long long)b * p.R + r] =
           row_needed(p, r, Kb) ? __ldcg(p.thr + (long long)b * p.R + r) : qnan();
   // issued before the row summaries so that its latency overlaps theirs
-  const int timed_out = (leader && warp == 0) ? __ldcg(p.err) : 0;
-  if (leader) {
-    for (int r = warp; r < p.R; r += kWarps) {
-      RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
-      const int xr = r == warp ? x0 : row_token(p, b, r, Kb);
-      if (row_needed(p, r, Kb))
-        rs = summarise_row<MODE, T>(p, b, r, Kb, xr, s_rec ? s_rec + (long long)r * p.NC : nullptr);
-      if (lane == 0) srow[r] = rs;
-      // target row r <= K_b: the draw of position r (dense drafts: the bonus
-      // position only; the others draw from the residual)
-      if (MODE != kGreedy && Kb >= 0 && Kb <= K && r <= Kb && (MODE != kDense || r == Kb)) {
-        const int tok = position_draw<MODE, T, VEC>(p, b, r, Kb, rs, xr, uK, s_rec);
-        if (lane == 0) s_tok[r] = tok;
-      }
+  const int timed_out = warp == 0 ? __ldcg(p.err) : 0;
+  for (int r = warp; r < p.R; r += kWarps) {
+    RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
+    const int xr = r == warp ? x0 : row_token(p, b, r, Kb);
+    if (row_needed(p, r, Kb))
+      rs = summarise_row<MODE, T>(p, b, r, Kb, xr, s_rec ? s_rec + (long long)r * p.NC : nullptr);
+    if (lane == 0) srow[r] = rs;
+    // target row r <= K_b: the draw of position r (dense drafts: the bonus
+    // position only; the others draw from the residual)
+    if (MODE != kGreedy && Kb >= 0 && Kb <= K && r <= Kb && (MODE != kDense || r == Kb)) {
+      const int tok = position_draw<MODE, T, VEC>(p, b, r, Kb, rs, xr, uK, s_rec);
+      if (lane == 0) s_tok[r] = tok;
     }
-    __syncthreads();
-    if (warp == 0)
-      finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_tok, x, u, timed_out, &s_resid);
   }
-  if (MODE == kDense) {
-    // Dense drafts: the request's CTAs learn n from the first one, read the
-    // rejected row pair for the residual chunk sums, and the first CTA draws.
-    // Both cluster barriers are passed by every thread of every CTA.
-    cg::cluster_group cluster = cg::this_cluster();
-    if (ncta > 1) {
-      cluster.sync();
-      if (!leader && threadIdx.x == 0) s_resid = *cluster.map_shared_rank(&s_resid, 0);
-    }
-    __syncthreads();
-    const Residual st = s_resid;
-    if (st.n >= 0)
-      residual_sums<T, VEC>(p, b, st, ncta > 1 ? cluster.map_shared_rank(s_sums, 0) : s_sums,
-                            rank, ncta);
-    if (ncta > 1)
-      cluster.sync();  // every sum is in the first CTA's shared memory
-    else
-      __syncthreads();
-    if (leader && warp == 0 && st.n >= 0) residual_pick<T, VEC>(p, b, st, s_sums, s_rec);
-  }
-  if (!leader) return;
-  // The last request of the call clears the counters and writes the packed
-  // output.
   __syncthreads();
+  if (warp == 0)
+    finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_tok, x, u, timed_out, &s_resid);
+  __syncthreads();
+  // Dense drafts, rejected at n: the request is published for the residual
+  // kernel, which reads its row pair with every SM and writes its outputs.
+  if (MODE == kDense && threadIdx.x == 0 && s_resid.n >= 0) {
+    const int slot = atomicAdd(p.n_pend, 1);
+    p.pend[slot] = b;
+    p.rpn[slot] = s_resid.n;
+    p.rpar[slot] = make_float4(s_resid.mp, s_resid.ip, s_resid.mq, s_resid.iq);
+  }
+  // The last request of the call clears the counters and (without dense
+  // drafts, whose residual kernel comes last) writes the packed output.
   if (threadIdx.x == 0) s_last[0] = atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B;
   __syncthreads();
   if (!s_last[0]) return;
   if (threadIdx.x == 0) {
     *p.err = 0;
     *p.fin_ticket = 0;
+    *p.work = 0u;
   }
-  if (p.compact_in_finalize) compact_all(p, s_last);
+  if (MODE != kDense && p.compact_in_finalize) compact_all(p, s_last);
 }
 
 template <int MODE, typename T, int VEC>
@@ -688,14 +672,17 @@ __host__ __device__ constexpr int residual_group() {
   return Lane<T, VEC>::G > 1 ? Lane<T, VEC>::G / 2 : 1;
 }
 
-// The residual chunk sums over chunks [lo, hi) (kExtra: with grammar masks
-// and top-k / top-p cuts applied).
+// One warp: the residual chunk sums max(0, p_n - q_n) of chunks [c0, hi),
+// at most residual_group() of them, over request b's (target, draft) row
+// pair at the rejected position st.n (kExtra: with grammar masks and top-k /
+// top-p cuts applied), into sums[c].
 template <typename T, int VEC, bool kExtra>
-__device__ __forceinline__ void residual_sums_loop(const VerifyParams& p, int b, const Residual& st,
-                                                   float* sums, int lo, int hi) {
+__device__ __forceinline__ void residual_group_sums(const VerifyParams& p, int b,
+                                                    const Residual& st, float* sums, int c0,
+                                                    int hi) {
   using L = Lane<T, VEC>;
   constexpr int G = residual_group<T, VEC>();
-  const int lane = lane_id(), warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+  const int lane = lane_id();
   const int K = p.K;
   const float cc = p.cc;
   const T* tr = row_ptr<T>(p.target, (long long)b * (K + 1) + st.n, p.V);
@@ -704,60 +691,56 @@ __device__ __forceinline__ void residual_sums_loop(const VerifyParams& p, int b,
   const uint32_t* mrow = kExtra ? mask_row(p, b, st.n) : nullptr;
   const float cut_t = kExtra ? row_cut(p, (long long)b * p.R + st.n) : -INFINITY;
   const float cut_d = kExtra ? row_cut(p, (long long)b * p.R + K + 1 + st.n) : -INFINITY;
-  for (int c0 = lo + warp * G; c0 < hi; c0 += nwarps * G) {
-    typename L::Raw rt[G][L::NV], rd[G][L::NV];
-    uint32_t word[G];
+  typename L::Raw rt[G][L::NV], rd[G][L::NV];
+  uint32_t word[G];
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (c0 + g < hi) {
-        load_chunk<T, VEC>(tr, p.V, c0 + g, rt[g]);
-        load_chunk<T, VEC>(dr, p.V, c0 + g, rd[g]);
-        if (kExtra && mrow) word[g] = mask_word(mrow, p.mask_words, c0 + g);
-      }
+  for (int g = 0; g < G; ++g)
+    if (c0 + g < hi) {
+      load_chunk<T, VEC>(tr, p.V, c0 + g, rt[g]);
+      load_chunk<T, VEC>(dr, p.V, c0 + g, rd[g]);
+      if (kExtra && mrow) word[g] = mask_word(mrow, p.mask_words, c0 + g);
+    }
 #pragma unroll
-    for (int g = 0; g < G; ++g)
-      if (c0 + g < hi) {
-        if (kExtra) {
-          if (mrow) {
-            allow_only_chunk<T, VEC>(rt[g], word[g]);
-            allow_only_chunk<T, VEC>(rd[g], word[g]);
-          }
-          if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt[g], cut_t);
-          if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd[g], cut_d);
+  for (int g = 0; g < G; ++g)
+    if (c0 + g < hi) {
+      if (kExtra) {
+        if (mrow) {
+          allow_only_chunk<T, VEC>(rt[g], word[g]);
+          allow_only_chunk<T, VEC>(rd[g], word[g]);
         }
-        float w = 0.f;
-#pragma unroll
-        for (int k = 0; k < L::NV; ++k)
-#pragma unroll
-          for (int e = 0; e < VEC; ++e)
-            w += residual_weight(L::get(rt[g][k], e), L::get(rd[g][k], e), cc, nbp, st.ip, nbq,
-                                 st.iq);
-        w = warp_sum(w);
-        if (lane == 0) sums[c0 + g] = w;
+        if (cut_t > -INFINITY) threshold_chunk<T, VEC>(rt[g], cut_t);
+        if (cut_d > -INFINITY) threshold_chunk<T, VEC>(rd[g], cut_d);
       }
-  }
-}
-
-// Request b was rejected at st.n: the chunk sums of max(0, p_n - q_n) over
-// the (target, draft) row pair.  CTA `rank` of the request's `ncta` takes a
-// contiguous range of chunks, its warps groups of consecutive chunks; each
-// sum goes to sums[c] (the first CTA's shared memory).  Calls without grammar
-// masks or filters take a loop without their checks.  Called by every thread
-// of the CTA.
-template <typename T, int VEC>
-__device__ __noinline__ void residual_sums(const VerifyParams& p, int b, const Residual& st,
-                                           float* sums, int rank, int ncta) {
-  const int lo = (int)((long long)p.NC * rank / ncta);
-  const int hi = (int)((long long)p.NC * (rank + 1) / ncta);
-  if (p.mask || p.filter)
-    residual_sums_loop<T, VEC, true>(p, b, st, sums, lo, hi);
-  else
-    residual_sums_loop<T, VEC, false>(p, b, st, sums, lo, hi);
+      float w = 0.f;
+#pragma unroll
+      for (int k = 0; k < L::NV; ++k)
+#pragma unroll
+        for (int e = 0; e < VEC; ++e)
+          w += residual_weight(L::get(rt[g][k], e), L::get(rd[g][k], e), cc, nbp, st.ip, nbq,
+                               st.iq);
+      w = warp_sum(w);
+      if (lane == 0) sums[c0 + g] = w;
+    }
 }
 
 // One warp: the residual draw from the chunk sums (the crossing chunk, then
 // a rescan of that chunk of both rows), and the request's outputs.
+// A rejected row pair whose residual has no mass (only through rounding:
+// max(0, p - q) sums to 0 only when p = q) draws from p_n instead.
 template <typename T, int VEC>
+__device__ __noinline__ int residual_fallback(const VerifyParams& p, int b, const Residual& st,
+                                              const float2* srec, float uK) {
+  const int NC = p.NC;
+  const T* tr = row_ptr<T>(p.target, (long long)b * (p.K + 1) + st.n, p.V);
+  const uint32_t* mrow = mask_row(p, b, st.n);
+  const float cut_t = row_cut(p, (long long)b * p.R + st.n);
+  return srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V, st.mp,
+                                                p.cc, uK, -1, mrow, p.mask_words, cut_t)
+              : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC, p.V,
+                                          st.mp, p.cc, uK, -1, mrow, p.mask_words, cut_t);
+}
+
+template <typename T, int VEC, bool kGlobalSums>
 __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const Residual& st,
                                            const float* sums, const float2* srec) {
   using L = Lane<T, VEC>;
@@ -767,34 +750,34 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
   const T* tr = row_ptr<T>(p.target, (long long)b * (K + 1) + st.n, p.V);
   const T* dr = row_ptr<T>(p.draft, (long long)b * K + st.n, p.V);
   const float nbp = -st.mp * cc, nbq = -st.mq * cc;
+  // the loads that do not depend on the sums, issued together
   const float uK = __ldg(p.uniforms + (long long)b * (K + 1) + K);
+  const int x_all = lane < K ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
   const uint32_t* mrow = mask_row(p, b, st.n);
   const float cut_t = row_cut(p, (long long)b * p.R + st.n);
   const float cut_d = row_cut(p, (long long)b * p.R + K + 1 + st.n);
-  auto weight = [&](int c) { return sums[c]; };
+  auto weight = [&](int c) { return kGlobalSums ? __ldcg(sums + c) : sums[c]; };
   int token;
   if constexpr (VEC * sizeof(T) == 16) {
     float frac = 0.f;
     const int c = find_chunk_runs(weight, NC, uK, &frac);
     if (c < 0) {  // no residual mass (rounding only): draw from p_n
-      token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V,
-                                                     st.mp, cc, uK, -1, mrow, p.mask_words, cut_t)
-                   : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
-                                               p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
+      token = residual_fallback<T, VEC>(p, b, st, srec, uK);
     } else {
-      float vt[kWarp], vd[kWarp];
+      Run<T> vt, vd;
       load_run<T>(tr, p.V, c, vt);
       load_run<T>(dr, p.V, c, vd);
-      const uint32_t at = run_allowed(vt, mrow, p.mask_words, c, cut_t, -1);
-      const uint32_t ad = run_allowed(vd, mrow, p.mask_words, c, cut_d, -1);
-      float w[kWarp];
-#pragma unroll
-      for (int e = 0; e < kWarp; ++e)
-        w[e] = residual_weight(((at >> e) & 1u) ? vt[e] : -INFINITY,
-                               ((ad >> e) & 1u) ? vd[e] : -INFINITY, cc, nbp, st.ip, nbq, st.iq);
-      token = pick_in_runs(w, frac, c * kChunk);
+      const uint32_t at = run_allowed<T>(vt, mrow, p.mask_words, c, cut_t, -1);
+      const uint32_t ad = run_allowed<T>(vd, mrow, p.mask_words, c, cut_d, -1);
+      token = pick_in_runs(
+          [&](int e) {
+            return residual_weight(((at >> e) & 1u) ? vt.get(e) : -INFINITY,
+                                   ((ad >> e) & 1u) ? vd.get(e) : -INFINITY, cc, nbp, st.ip, nbq,
+                                   st.iq);
+          },
+          frac, c * kChunk);
     }
-    const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
+    const int x = lane < st.n ? x_all : -1;
     write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
   } else {
     float wc[kRecCache];
@@ -808,10 +791,7 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
     for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) tot += weight(c);
     tot = warp_sum(tot);
     if (!(tot > 0.f)) {  // no residual mass (rounding only): draw from p_n
-      token = srec ? draw_from_records<T, VEC, true>(tr, srec + (long long)st.n * NC, NC, p.V, st.mp,
-                                                     cc, uK, -1, mrow, p.mask_words, cut_t)
-                   : draw_from_records<T, VEC>(tr, p.rec + ((long long)b * p.R + st.n) * NC, NC,
-                                               p.V, st.mp, cc, uK, -1, mrow, p.mask_words, cut_t);
+      token = residual_fallback<T, VEC>(p, b, st, srec, uK);
     } else {
       float frac = 0.f;
       const int c = find_chunk(wc, weight, NC, uK * tot, &frac);
@@ -840,23 +820,71 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
       }
       token = select_in_tile<L::NV, VEC>(w, gsum, frac, c * kChunk);
     }
-    const int x = lane < st.n ? __ldg(p.draft_tokens + (long long)b * K + lane) : -1;
+    const int x = lane < st.n ? x_all : -1;
     write_request(p, b, token < 0 ? kBadLogits : 0, st.n, token, x);
   }
+}
+
+// ---------------------------------------------------------------------------
+// kernel R: the dense-draft residual over every SM (after kernel F)
+// ---------------------------------------------------------------------------
+
+// The requests kernel F published - rejected at n with dense drafts - need
+// the chunk sums of max(0, p_n - q_n), one more pass over their (target,
+// draft) row pair, before their token can be drawn.  Every warp of the grid
+// takes (request, chunk group) items in turn - a chunk group is
+// residual_group() chunks - writes their sums to the request's slot and
+// counts the group in the slot's arrival counter (acquire-release); the warp
+// that completes a request's last group draws its token from the sums (the
+// crossing chunk, then a rescan of that chunk of both rows) and writes its
+// outputs, while the other warps go on.  The last CTA to finish writes the
+// packed output of the whole call and clears the counters.  Launched with
+// programmatic dependent launch behind kernel F, so its CTAs are resident
+// when F ends.
+constexpr int kResThreads = 256;
+
+template <typename T, int VEC, bool kExtra>
+__global__ void __launch_bounds__(kResThreads, 2) residual_kernel(const VerifyParams p) {
+  __shared__ int s_flag[32];
+  pdl_wait();
+  pdl_launch_dependents();
+  constexpr int G = residual_group<T, VEC>();
+  const int lane = lane_id();
+  const int NC = p.NC;
+  const int groups = (NC + G - 1) / G;
+  const long long items = (long long)__ldcg(p.n_pend) * groups;
+  const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
+       it += warps) {
+    const int slot = (int)(it / groups), c0 = (int)(it - (long long)slot * groups) * G;
+    const float4 q = __ldcg(p.rpar + slot);
+    const Residual st{__ldcg(p.rpn + slot), q.x, q.y, q.z, q.w};
+    const int b = __ldcg(p.pend + slot);
+    float* sums = p.rsums + (long long)slot * NC;
+    residual_group_sums<T, VEC, kExtra>(p, b, st, sums, c0, min(NC, c0 + G));
+    int last = 0;
+    if (lane == 0) last = atomic_add_acq_rel(p.arrive + slot, 1) + 1 == groups;
+    if (__shfl_sync(0xffffffffu, last, 0)) {  // every sum of this request is in
+      residual_pick<T, VEC, true>(p, b, st, sums, nullptr);
+      if (lane == 0) p.arrive[slot] = 0;
+    }
+  }
+  // the last CTA to leave: the packed output of the whole call, counters
+  __syncthreads();
+  if (threadIdx.x == 0) s_flag[0] = atomic_add_acq_rel(p.r_exit, 1) + 1 == (int)gridDim.x;
+  __syncthreads();
+  if (!s_flag[0]) return;
+  if (threadIdx.x == 0) {
+    *p.n_pend = 0;
+    *p.r_exit = 0;
+  }
+  if (p.compact_in_finalize) compact_all(p, s_flag);
 }
 
 // ---------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------
 
-// CTAs per request for the dense-draft residual: as many as fit on the GPU
-// at once (`slots` finalize CTAs), at most one per 16 chunks of the row (a
-// CTA's 8 warps read 2 chunks of each row at a time), at most 8.
-int residual_cluster(const VerifyParams& p, int slots) {
-  int c = p.B > 0 ? slots / p.B : 1;
-  c = c < (p.NC + 15) / 16 ? c : (p.NC + 15) / 16;
-  return c < 1 ? 1 : (c > 8 ? 8 : c);
-}
 template <int MODE, typename T, int VEC>
 cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
   cudaError_t err = launch_records(MODE, sizeof(T) == 2 ? kBF16 : kF32, VEC > 1, p, s);
@@ -868,22 +896,33 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
   void* args[] = {&pc};
   // F: acceptance tests and draws, one CTA per request
   const void* fin = reinterpret_cast<const void*>(finalize_kernel<MODE, T, VEC>);
-  const size_t fin_smem = fin_smem_bytes(p, MODE == kDense);
   static PerDevice once;
-  int occ = 1;  // finalize CTAs per SM
-  err = per_device(once, &occ, [&](int& v) {
-    const cudaError_t e = cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               (int)kFinSmemMax);
-    if (e != cudaSuccess) return e;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, fin, fin_threads<MODE>(),
-                                                      (size_t)kFinCacheLimit) != cudaSuccess ||
+  err = per_device(once, nullptr, [&](int&) {
+    return cudaFuncSetAttribute(fin, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                (int)kFinCacheLimit);
+  });
+  if (err != cudaSuccess) return err;
+  err = launch_pdl(fin, dim3(p.B), dim3(fin_threads<MODE>()), s, args, fin_smem_bytes(p, false));
+  if (err != cudaSuccess || MODE != kDense) return err;
+  // R: the residual of the requests F published, over every SM (calls with
+  // grammar masks or top-k / top-p cuts take a variant that applies them)
+  const bool extra = p.mask || p.filter;
+  const void* rk = extra ? reinterpret_cast<const void*>(residual_kernel<T, VEC, true>)
+                         : reinterpret_cast<const void*>(residual_kernel<T, VEC, false>);
+  static PerDevice once_r[2];
+  int occ = 1;
+  err = per_device(once_r[extra ? 1 : 0], &occ, [&](int& v) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&v, rk, kResThreads, 0) != cudaSuccess ||
         v < 1)
       v = 1;
     return cudaSuccess;
   });
   if (err != cudaSuccess) return err;
-  const int ncta = MODE == kDense ? residual_cluster(p, di.sms * occ) : 1;
-  return launch_pdl(fin, dim3(p.B * ncta), dim3(fin_threads<MODE>()), s, args, fin_smem, ncta);
+  constexpr int G = residual_group<T, VEC>();
+  const long long want =
+      ((long long)p.B * ((p.NC + G - 1) / G) + kResThreads / kWarp - 1) / (kResThreads / kWarp);
+  const long long cap = (long long)di.sms * occ;
+  return launch_pdl(rk, dim3((unsigned)(want < cap ? want : cap)), dim3(kResThreads), s, args);
 }
 
 // ---------------------------------------------------------------------------
@@ -1019,6 +1058,7 @@ __device__ void write_tree_result(const VerifyParams& p, const TreeCall& t, int 
     if (atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B) {
       *p.err = 0;
       *p.fin_ticket = 0;
+      *p.work = 0u;
     }
   }
 }
@@ -1247,9 +1287,7 @@ cudaError_t launch_mode(int dtype, bool vec, const VerifyParams& p, cudaStream_t
 
 size_t fin_cache_bytes(const VerifyParams& p) { return sizeof(float2) * (size_t)p.R * p.NC; }
 
-size_t fin_smem_bytes(const VerifyParams& p, bool dense) {
-  return (p.fin_cache ? fin_cache_bytes(p) : 0) + (dense ? sizeof(float) * (size_t)p.NC : 0);
-}
+size_t fin_smem_bytes(const VerifyParams& p, bool) { return p.fin_cache ? fin_cache_bytes(p) : 0; }
 
 cudaError_t launch_tree_typical(int dtype, bool vec, const VerifyParams& p, const TreeCall& t,
                                 cudaStream_t stream) {

@@ -46,6 +46,16 @@ struct VerifyParams {
   // workspace
   int* err;          // [1] set when a bounded wait gave up
   int* fin_ticket;   // [1] requests finalised in this call
+  unsigned* work;    // [1] the streaming kernel's next item (taken by atomic add)
+  // dense drafts: the requests rejected at n whose residual the residual
+  // kernel reads (published by the finalize kernel)
+  int* n_pend;       // [1] rejected requests published
+  int* r_exit;       // [1] residual CTAs finished
+  int* arrive;       // [B] chunk groups done per published slot
+  int* pend;         // [B] the request of each slot
+  int* rpn;          // [B] its rejected position n
+  float4* rpar;      // [B] {row max, 1/sum} of its target and draft rows at n
+  float* rsums;      // [B*NC] residual chunk sums per slot
   float2* rec;       // [B*R*NC]
   float* lx;         // [B*R] the logit of each row's draft token
   int B, K, V;
@@ -101,7 +111,7 @@ enum Dtype : int { kF32 = 0, kBF16 = 1 };
 
 // Workspace layout for B requests, K positions, V vocabulary (dense case).
 struct WorkspaceLayout {
-  size_t counters, zero_bytes, rec, lx, thr, ent, total;
+  size_t counters, arrive, zero_bytes, pend, rpar, rsums, rec, lx, thr, ent, total;
 };
 WorkspaceLayout workspace_layout(int B, int K, int V);
 

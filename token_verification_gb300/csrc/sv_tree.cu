@@ -8,14 +8,16 @@
 // node's row, moves to the child carrying that token, and stops at a node
 // without such a child; the argmax there is the extra token.
 //
-// One thread-block cluster per request.  Each step, the cluster's warps split
-// the current row into 1024-element chunks (exact argmax, lowest index on
-// ties), each CTA reduces its warps, the CTAs exchange their results through
-// distributed shared memory after a cluster barrier, and every CTA derives the
-// same next node from the same data, so all of them run the same number of
-// steps.  Only the rows on the accepted path are read; with PREFETCH, the
-// children's rows are pulled into L2 while the current row is reduced, so the
-// next step's loads hit L2.
+// One thread-block cluster per request.  Each step reduces the current node's
+// row and, speculatively, the rows of all its children in one batch of loads
+// (the cluster's warps split every row of the set into 1024-element chunks;
+// exact argmax, lowest index on ties); CTAs exchange their partial results
+// through distributed shared memory after one cluster barrier, and every CTA
+// derives the same outcome from the same data, so all of them run the same
+// number of steps.  The node's argmax picks the child; that child's argmax is
+// already known and picks the grandchild, which the next step starts from:
+// one step resolves two levels of the walk.  Only the rows of the walked
+// nodes and their children are read.
 #include <cooperative_groups.h>
 
 #include "sv_common.cuh"
@@ -28,12 +30,27 @@ namespace {
 
 constexpr int kTreeThreads = 128;
 constexpr int kTreeWarps = kTreeThreads / kWarp;
+constexpr int kRowBatch = 4;  // rows of the step's set whose chunks a warp loads together
 
-__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+__device__ __forceinline__ void pdl_begin() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
-template <typename T, int VEC, bool PREFETCH>
+// The lowest child of `node` whose token is `tok` (0 if none); a warp-wide
+// call, the same answer in every lane.
+__device__ __forceinline__ int child_with_token(const short* s_par, const int* s_tok, int N,
+                                                int node, int tok) {
+  for (int c0 = 1; c0 <= N; c0 += kWarp) {
+    const int c = c0 + lane_id();
+    const unsigned hit =
+        __ballot_sync(0xffffffffu, c <= N && s_par[c] == node && s_tok[c] == tok);
+    if (hit) return c0 + __ffs(hit) - 1;
+  }
+  return 0;
+}
+
+template <typename T, int VEC>
 __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constant__ TreeParams p) {
   using L = Lane<T, VEC>;
   cg::cluster_group cluster = cg::this_cluster();
@@ -46,13 +63,15 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constan
 
   __shared__ int s_tok[kMaxTreeNodes + 1];
   __shared__ short s_par[kMaxTreeNodes + 1], s_depth[kMaxTreeNodes + 1], s_anc[kMaxTreeNodes + 1];
-  __shared__ int s_kid[kMaxTreeNodes];
-  __shared__ int s_nkid;
-  __shared__ float2 s_warp[kTreeWarps];
-  __shared__ float2 s_cta[2];
+  __shared__ int s_row[kMaxTreeNodes + 1];  // the step's rows: the node, then its children
+  __shared__ int s_nrow;
+  __shared__ float2 s_warp[kTreeWarps][kMaxTreeNodes + 1];
+  __shared__ float2 s_cta[2][kMaxTreeNodes + 1];  // this CTA's result per row (two steps' worth)
+  __shared__ int s_arg[kMaxTreeNodes + 1];         // the cluster's argmax per row (INT_MAX: bad)
   __shared__ int s_path[kMaxTreeNodes + 1];
   __shared__ int s_out[kMaxTreeNodes + 1];
 
+  pdl_begin();
   // every CTA of the cluster loads the same tree and reaches the same verdict
   const bool tree_ok = load_tree(p.parent + (long long)b * p.parent_stride, p.N, p.D1 - 1, s_par,
                                  s_depth, s_anc);
@@ -65,68 +84,93 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constan
   bad = __syncthreads_or(bad);
   int status = !tree_ok ? kBadTree : (bad ? kBadToken : 0);
   int node = 0, depth = 0, parity = 0;
+  const T* base = reinterpret_cast<const T*>(p.target) + (long long)b * (p.N + 1) * p.V;
   while (!status) {
-    __syncthreads();  // the previous step's reads of s_kid are done
-    // the current node's children, in increasing id (warp 0)
-    if (warp == 0) {
-      int nk = 0;
+    __syncthreads();  // the previous step's reads of s_row / s_arg are done
+    if (warp == 0) {  // the set: the node, then its children in increasing id
+      int n_set = 1;
+      if (lane == 0) s_row[0] = node;
       for (int c0 = 1; c0 <= p.N; c0 += kWarp) {
         const int c = c0 + lane;
         const bool kid = c <= p.N && s_par[c] == node;
         const unsigned m = __ballot_sync(0xffffffffu, kid);
-        if (kid) s_kid[nk + __popc(m & ((1u << lane) - 1u))] = c;
-        nk += __popc(m);
+        if (kid) s_row[n_set + __popc(m & ((1u << lane) - 1u))] = c;
+        n_set += __popc(m);
       }
-      if (lane == 0) s_nkid = nk;
+      if (lane == 0) s_nrow = n_set;
     }
     __syncthreads();
-    const int nkid = s_nkid;
-    const T* row = reinterpret_cast<const T*>(p.target) + ((long long)b * (p.N + 1) + node) * p.V;
-    float2 best = make_float2(-INFINITY, __int_as_float(0x7fffffff));
-    bool first = true;
-    for (int c = gw; c < p.NC; c += W) {
-      typename L::Raw raw[L::NV];
-      load_chunk<T, VEC>(row, p.V, c, raw);
-      if (PREFETCH && lane == 0) {
-        const unsigned bytes = (unsigned)(min(kChunk, p.V - c * kChunk) * sizeof(T));
-        for (int k = 0; k < nkid; ++k)
-          prefetch_l2(reinterpret_cast<const T*>(p.target) +
-                          ((long long)b * (p.N + 1) + s_kid[k]) * p.V + (long long)c * kChunk,
-                      bytes);
+    const int nrow = s_nrow;
+    // each warp reduces its chunks of every row of the set, kRowBatch rows'
+    // loads in flight at once
+    for (int r0 = 0; r0 < nrow; r0 += kRowBatch) {
+      float2 best[kRowBatch];
+#pragma unroll
+      for (int j = 0; j < kRowBatch; ++j) best[j] = make_float2(-INFINITY, __int_as_float(0x7fffffff));
+      bool first = true;
+      for (int c = gw; c < p.NC; c += W) {
+        typename L::Raw raw[kRowBatch][L::NV];
+#pragma unroll
+        for (int j = 0; j < kRowBatch; ++j)
+          if (r0 + j < nrow) load_chunk<T, VEC>(base + (long long)s_row[r0 + j] * p.V, p.V, c, raw[j]);
+#pragma unroll
+        for (int j = 0; j < kRowBatch; ++j)
+          if (r0 + j < nrow) {
+            const float2 r = chunk_argmax<T, VEC>(raw[j], c * kChunk);
+            if (first || r.x > best[j].x || (r.x != r.x && best[j].x == best[j].x)) best[j] = r;
+          }
+        first = false;
       }
-      const float2 r = chunk_argmax<T, VEC>(raw, c * kChunk);
-      if (first || r.x > best.x || (r.x != r.x && best.x == best.x)) best = r;
-      first = false;
+      if (lane == 0)
+#pragma unroll
+        for (int j = 0; j < kRowBatch; ++j)
+          if (r0 + j < nrow) s_warp[warp][r0 + j] = best[j];
     }
-    if (lane == 0) s_warp[warp] = best;
     __syncthreads();
-    if (warp == 0) {
-      float2 v = lane < kTreeWarps ? s_warp[lane] : make_float2(-INFINITY, __int_as_float(0x7fffffff));
+    // this CTA's result per row, then the cluster's
+    for (int r = warp; r < nrow; r += kTreeWarps) {
+      float2 v = lane < kTreeWarps ? s_warp[lane][r]
+                                   : make_float2(-INFINITY, __int_as_float(0x7fffffff));
       v = warp_combine_argmax(v);
-      if (lane == 0) s_cta[parity] = v;
+      if (lane == 0) s_cta[parity][r] = v;
     }
     cluster.sync();
-    float2 v = make_float2(-INFINITY, __int_as_float(0x7fffffff));
-    if (lane < CL) v = *cluster.map_shared_rank(&s_cta[parity], lane);
-    v = warp_combine_argmax(v);
-    if (!is_finite(v.x)) {
+    for (int r = warp; r < nrow; r += kTreeWarps) {
+      float2 v = make_float2(-INFINITY, __int_as_float(0x7fffffff));
+      if (lane < CL) v = *cluster.map_shared_rank(&s_cta[parity][r], lane);
+      v = warp_combine_argmax(v);
+      if (lane == 0) s_arg[r] = is_finite(v.x) ? __float_as_int(v.y) : 0x7fffffff;
+    }
+    __syncthreads();
+    // the node's argmax picks the child; the child's (already reduced) picks
+    // the grandchild, where the next step starts
+    const int a = s_arg[0];
+    if (a == 0x7fffffff) {
       status = kBadLogits;
       break;
     }
-    const int a = __float_as_int(v.y);
     if (threadIdx.x == 0) {
       s_path[depth] = node;
       s_out[depth] = a;
     }
     ++depth;
-    int next = 0;  // the lowest child carrying the argmax
-    for (int k = 0; k < nkid; ++k)
-      if (s_tok[s_kid[k]] == a) {
-        next = s_kid[k];
-        break;
-      }
-    if (!next) break;
-    node = next;
+    const int c = child_with_token(s_par, s_tok, p.N, node, a);
+    if (!c) break;
+    int rc = 1;  // the child's place in the set (children follow in increasing id)
+    while (s_row[rc] != c) ++rc;
+    const int ac = s_arg[rc];
+    if (ac == 0x7fffffff) {
+      status = kBadLogits;
+      break;
+    }
+    if (threadIdx.x == 0) {
+      s_path[depth] = c;
+      s_out[depth] = ac;
+    }
+    ++depth;
+    const int g = child_with_token(s_par, s_tok, p.N, c, ac);
+    if (!g) break;
+    node = g;
     parity ^= 1;
   }
   cluster.sync();  // keep every CTA's shared memory alive until all reads are done
@@ -145,7 +189,7 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constan
   }
 }
 
-template <typename T, int VEC, bool PREFETCH>
+template <typename T, int VEC>
 cudaError_t launch_tree_typed(const TreeParams& p, cudaStream_t s) {
   DeviceInfo di;
   cudaError_t err = device_info(&di);
@@ -159,24 +203,24 @@ cudaError_t launch_tree_typed(const TreeParams& p, cudaStream_t s) {
   cfg.blockDim = dim3(kTreeThreads);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = (unsigned)cl;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, tree_kernel<T, VEC, PREFETCH>, p);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, tree_kernel<T, VEC>, p);
 }
 
 }  // namespace
 
 cudaError_t launch_tree(int dtype, bool vec, const TreeParams& p, cudaStream_t stream) {
   if (dtype == kBF16)
-    return vec ? launch_tree_typed<uint16_t, 8, true>(p, stream)
-               : launch_tree_typed<uint16_t, 1, false>(p, stream);
-  return vec ? launch_tree_typed<float, 4, true>(p, stream)
-             : launch_tree_typed<float, 1, false>(p, stream);
+    return vec ? launch_tree_typed<uint16_t, 8>(p, stream) : launch_tree_typed<uint16_t, 1>(p, stream);
+  return vec ? launch_tree_typed<float, 4>(p, stream) : launch_tree_typed<float, 1>(p, stream);
 }
 
 }  // namespace sv

@@ -15,8 +15,9 @@
 //   to one 8-byte record.  One producer thread per CTA copies items of 15
 //   consecutive chunks (30 KB of bf16) into a ring of shared-memory stages
 //   with cp.async.bulk; each of the 15 consumer warps reduces one chunk of
-//   every stage.  It has no atomics, fences or cross-CTA communication.  The
-//   per-request work (tests, draws, packed output) is kernel F's
+//   every stage.  The only shared state is a work counter from which the
+//   producers take their items.  The per-request work (tests, draws, packed
+//   output) is kernel F's
 //   (sv_finalize.cu); filtered calls use kernel A' (sv_filter.cu) instead.
 #include <type_traits>
 
@@ -97,14 +98,15 @@ __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyPa
 }
 
 // Streaming variant (vector paths).  Warp 0, lane 0 is the producer: it
-// walks the CTA's contiguous range of items (an item = up to kConsumers
+// takes items from the call's work counter (an item = up to kConsumers
 // consecutive chunks of one row, 30 KB of bf16), and copies each item with
 // one cp.async.bulk into the next of kStages shared-memory stages, together
 // with the item's description.  Each consumer warp w reduces chunk w of every
 // stage into one record.  A stage has a "full" mbarrier (completed by the
 // copy) and an "empty" one (completed when all consumers are done with it).
-// No atomics, fences or cross-CTA traffic: per-request work happens in the
-// finalize kernel.  After the last item the producer publishes an end marker.
+// Per-request work happens in the finalize kernel, whose last CTA returns the
+// work counter to zero.  After the last item the producer publishes an end
+// marker.
 #ifndef SV_STREAM_STAGES_BF16
 #define SV_STREAM_STAGES_BF16 3
 #endif
@@ -214,10 +216,7 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
     fence_mbar_init();
   }
   __syncthreads();
-  // this CTA's contiguous range of items
   const uint32_t total = (uint32_t)p.total_tasks;
-  const uint32_t lo = (uint32_t)(((unsigned long long)total * blockIdx.x) / gridDim.x);
-  const uint32_t hi = (uint32_t)(((unsigned long long)total * (blockIdx.x + 1)) / gridDim.x);
 
   if (warp == 0) {
     if (lane != 0) return;
@@ -226,7 +225,16 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
     auto acquire = [&](int s) {  // wait until stage s may be refilled
       return k < (uint32_t)S || mbar_wait(empty_of(s), ((k / S) - 1) & 1u, p.wait_ns);
     };
-    for (uint32_t it = lo; it < hi && ok; ++it) {
+    // Items are taken from the call's work counter one at a time, the next
+    // one's index fetched while the current one is copied, so every CTA
+    // finishes within about one item of the others whatever its share of
+    // the bandwidth; the grid goes through the rows in order.
+    uint32_t next = atomicAdd(p.work, 1u);
+    const unsigned long long evict_first = l2_evict_first_policy();
+    while (ok) {
+      const uint32_t it = next;
+      if (it >= total) break;
+      next = atomicAdd(p.work, 1u);
       const Item item = decode_item<MODE>(p, it);
       if (!item.need) continue;
       const int s = (int)(k % S);
@@ -243,10 +251,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
         const int w0 = item.c0 * kWarp;
         const uint32_t mbytes = (uint32_t)(min(item.nch * kWarp, p.mask_words - w0) * 4);
         mbar_arrive_expect_tx(full_of(s), bytes + mbytes);
-        bulk_copy(stage_of(s), src, bytes, full_of(s));
+        bulk_copy_hint(stage_of(s), src, bytes, full_of(s), evict_first);
         bulk_copy(mask_of(s), item_mask(p, item.rowid) + w0, mbytes, full_of(s));
       } else {
-        bulk_load(stage_of(s), src, bytes, full_of(s));
+        mbar_arrive_expect_tx(full_of(s), bytes);
+        bulk_copy_hint(stage_of(s), src, bytes, full_of(s), evict_first);
       }
       ++k;
     }
