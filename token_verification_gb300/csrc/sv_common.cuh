@@ -649,14 +649,12 @@ __device__ __forceinline__ float combine_entropy(const float2* rec, const float*
 constexpr int kTreeMaxNodes = 256;  // candidate nodes per tree (the root excluded)
 
 // Request's parent array (parent of node n = 1..N at parent[n - 1]) into
-// s_par[0..N] (s_par[0] = 0) and every node's depth into s_depth, by pointer
-// jumping (s_anc is scratch): log2(N + 1) rounds of depth[n] += depth[anc[n]],
-// anc[n] = anc[anc[n]].  True when the array is a tree - every parent an
-// earlier node, so the links cannot cycle - of depth <= max_depth.  Called by
-// every thread of the CTA; the same data gives every CTA the same answer.
-__device__ __forceinline__ bool load_tree(const int* parent, int N, int max_depth, short* s_par,
-                                          short* s_depth, short* s_anc) {
-  constexpr int kPer = (kTreeMaxNodes + 1 + 127) / 128;  // nodes per thread (>= 128 threads)
+// s_par[0..N] (s_par[0] = 0), with s_anc = s_par and s_depth[n] = (n > 0) as
+// the start of tree_depths_ok.  True when every parent is an earlier node, so
+// the links cannot cycle (an out-of-range parent is stored as 0).  Called by
+// every thread of the CTA.
+__device__ __forceinline__ bool load_parents(const int* parent, int N, short* s_par,
+                                             short* s_depth, short* s_anc) {
   int bad = 0;
   for (int n = threadIdx.x; n <= N; n += blockDim.x) {
     int pa = 0;
@@ -671,7 +669,40 @@ __device__ __forceinline__ bool load_tree(const int* parent, int N, int max_dept
     s_anc[n] = (short)pa;
     s_depth[n] = (short)(n > 0);
   }
-  if (__syncthreads_or(bad)) return false;
+  return !__syncthreads_or(bad);
+}
+
+// Every node's depth into s_depth by pointer jumping over the links that
+// load_parents stored (s_anc is scratch): rounds of depth[n] += depth[anc[n]],
+// anc[n] = anc[anc[n]] until the jumps span the tree.  True when no node is
+// deeper than max_depth.  Trees of fewer than 64 nodes are done by warp 0 in
+// registers (nodes lane and lane + 32, exchanged by shuffles); larger ones
+// in shared memory by the CTA (>= 128 threads).  Called by every thread of
+// the CTA; the same data gives every CTA the same answer.
+__device__ __forceinline__ bool tree_depths_ok(int N, int max_depth, short* s_depth, short* s_anc) {
+  int bad = 0;
+  if (N < 2 * kWarp) {
+    if (threadIdx.x < kWarp) {
+      const int lane = threadIdx.x, n1 = lane + kWarp;
+      int d0 = lane <= N ? s_depth[lane] : 0, a0 = lane <= N ? s_anc[lane] : 0;
+      int d1 = n1 <= N ? s_depth[n1] : 0, a1 = n1 <= N ? s_anc[n1] : 0;
+      for (int span = 1; span <= N; span <<= 1) {
+        const int x0 = __shfl_sync(0xffffffffu, d0, a0 & 31), y0 = __shfl_sync(0xffffffffu, d1, a0 & 31);
+        const int p0 = __shfl_sync(0xffffffffu, a0, a0 & 31), q0 = __shfl_sync(0xffffffffu, a1, a0 & 31);
+        const int x1 = __shfl_sync(0xffffffffu, d0, a1 & 31), y1 = __shfl_sync(0xffffffffu, d1, a1 & 31);
+        const int p1 = __shfl_sync(0xffffffffu, a0, a1 & 31), q1 = __shfl_sync(0xffffffffu, a1, a1 & 31);
+        d0 += a0 < kWarp ? x0 : y0;
+        a0 = a0 < kWarp ? p0 : q0;
+        d1 += a1 < kWarp ? x1 : y1;
+        a1 = a1 < kWarp ? p1 : q1;
+      }
+      if (lane <= N) s_depth[lane] = (short)d0;
+      if (n1 <= N) s_depth[n1] = (short)d1;
+      bad = (lane <= N && d0 > max_depth) || (n1 <= N && d1 > max_depth);
+    }
+    return !__syncthreads_or(bad);
+  }
+  constexpr int kPer = (kTreeMaxNodes + 1 + 127) / 128;  // nodes per thread (>= 128 threads)
   for (int span = 1; span <= N; span <<= 1) {
     short nd[kPer], na[kPer];
 #pragma unroll
@@ -696,6 +727,20 @@ __device__ __forceinline__ bool load_tree(const int* parent, int N, int max_dept
   }
   for (int n = threadIdx.x; n <= N; n += blockDim.x) bad |= s_depth[n] > max_depth;
   return !__syncthreads_or(bad);
+}
+
+// load_parents, then tree_depths_ok: true when the request's parent array is
+// a tree of depth <= max_depth.
+__device__ __forceinline__ bool load_tree(const int* parent, int N, int max_depth, short* s_par,
+                                          short* s_depth, short* s_anc) {
+  if (!load_parents(parent, N, s_par, s_depth, s_anc)) return false;
+  return tree_depths_ok(N, max_depth, s_depth, s_anc);
+}
+
+// Asks L2 for `bytes` bytes at ptr (16-byte aligned, a multiple of 16): a
+// bulk prefetch, no data returned.
+__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 }  // namespace sv

@@ -67,6 +67,65 @@ __device__ __forceinline__ unsigned long long frac_of(unsigned long long total, 
   return (total >> 32) * p_q + (((total & 0xffffffffull) * p_q) >> 32);
 }
 
+// The least value v of type T (bf16 as its float value) with fmaf(v, c,
+// -m c) >= -kCandBits: every element at or above it is a candidate, none
+// below.  The float bound m - kCandBits / c is moved by single steps of T's
+// spacing until it is the least one (fmaf is monotone in v).
+template <typename T>
+__device__ float cand_bound(float m, float cc) {
+  const float nb = -m * cc;
+  auto ok = [&](float v) { return fmaf(v, cc, nb) >= -kCandBits; };
+  auto up = [](float v) {  // the next value of T above v
+    if (sizeof(T) == 2) {
+      const uint32_t b = __float_as_uint(v) >> 16;
+      const uint32_t n = (b & 0x8000u) ? (b == 0x8000u ? 0x0001u : b - 1u) : b + 1u;
+      return __uint_as_float(n << 16);
+    }
+    return nextafterf(v, INFINITY);
+  };
+  auto down = [](float v) {
+    if (sizeof(T) == 2) {
+      const uint32_t b = __float_as_uint(v) >> 16;
+      const uint32_t n = (b & 0x8000u) ? b + 1u : (b == 0u ? 0x8001u : b - 1u);
+      return __uint_as_float(n << 16);
+    }
+    return nextafterf(v, -INFINITY);
+  };
+  float v = m - kCandBits / cc;
+  if (sizeof(T) == 2) v = __uint_as_float(__float_as_uint(v) & 0xffff0000u);  // toward zero
+  if (!(v >= -FLT_MAX))  // every finite element is a candidate: the least finite value
+    return sizeof(T) == 2 ? __uint_as_float(0xff7f0000u) : -FLT_MAX;
+  for (int i = 0; i < 64 && !ok(v); ++i) v = up(v);
+  for (int i = 0; i < 64 && ok(down(v)); ++i) v = down(v);
+  return v;
+}
+
+// Both halves of a bf16 pair set to v (a bf16 value held as a float).
+__device__ __forceinline__ uint32_t bf16_pair_of(float v) {
+  const uint32_t h = __float_as_uint(v) >> 16;
+  return h | (h << 16);
+}
+
+// Sets bit POS of `bits` if the low bf16 of w is >= the threshold's, bit
+// POS + 1 if the high one is (a packed comparison; -inf never, NaN never).
+template <int POS>
+__device__ __forceinline__ void mark_ge_bf16x2(uint32_t& bits, uint32_t w, uint32_t t2) {
+  asm("{\n\t.reg .pred p, q;\n\t.reg .b16 wl, wh, tl, th;\n\t"
+      "mov.b32 {wl, wh}, %1;\n\tmov.b32 {tl, th}, %2;\n\t"
+      "setp.ge.bf16 p, wl, tl;\n\tsetp.ge.bf16 q, wh, th;\n\t"
+      "@p or.b32 %0, %0, %3;\n\t@q or.b32 %0, %0, %4;\n\t}"
+      : "+r"(bits)
+      : "r"(w), "r"(t2), "n"(1u << POS), "n"(2u << POS));
+}
+
+template <int K>
+__device__ __forceinline__ void mark_group_bf16(uint32_t& bits, const uint4& g, uint32_t t2) {
+  mark_ge_bf16x2<8 * K + 0>(bits, g.x, t2);
+  mark_ge_bf16x2<8 * K + 2>(bits, g.y, t2);
+  mark_ge_bf16x2<8 * K + 4>(bits, g.z, t2);
+  mark_ge_bf16x2<8 * K + 6>(bits, g.w, t2);
+}
+
 // Distance levels: a candidate's weight exponent a = (l - m) c in [-18, 0]
 // falls into level floor(-8 a), kept as digit 255 - level so that larger
 // values have larger digits, as key digits do.
@@ -82,9 +141,10 @@ struct CutShared {
   unsigned char stage[kCutWarps][kStageBytes];
   int seg[kMaxChunks], seg_n[kMaxChunks];
   int stage_n[kCutWarps];
-  float red_m[kCutWarps], red_s[kCutWarps], red_t[kCutWarps];
+  float red_t[kCutWarps];
   int red_n[kCutWarps];
-  float row_max, row_s, row_tail;
+  float2 rec1[kMaxChunks];  // per chunk {max, sum of 2^((l - max) c)} over the whole chunk
+  float row_max, row_s, row_tail, cand_lo;
   int row_n, over, x_entry;
   int list_n;  // elements of the cut's level
   uint32_t list_key[kListCap];
@@ -209,12 +269,6 @@ __device__ __forceinline__ void row_chunk(const VerifyParams& p, const Slice<T>&
                                           typename Lane<T, VEC>::Raw (&raw)[Lane<T, VEC>::NV]) {
   load_chunk<T, VEC>(s.row, p.V, c, raw);
   if (s.mrow) allow_only_chunk<T, VEC>(raw, mask_word(s.mrow, p.mask_words, c));
-}
-
-// Asks L2 for `bytes` bytes at p (16-byte aligned, a multiple of 16): a
-// bulk prefetch, no data returned.
-__device__ __forceinline__ void prefetch_l2(const void* ptr, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
 }
 
 // Element t (bit t of the candidate marks: group t / 8, element t % 8) of a
@@ -390,8 +444,11 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
   extern __shared__ __align__(16) unsigned char smem[];
   CutShared* sh = reinterpret_cast<CutShared*>(smem);
   const int rowid = blockIdx.x;
-  pdl_launch_dependents();
+  // Launched early (programmatic dependent launch): wait for the predecessor,
+  // then let the finalize kernel launch - it reads the call's inputs before
+  // its own wait, which is safe once everything before this kernel is done.
   pdl_wait();
+  pdl_launch_dependents();
   const int b = (int)fast_div((uint32_t)rowid, p.div_r);
   const int r = rowid - b * p.R;
   const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : p.K;
@@ -402,38 +459,63 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
   sl.row = item_row<T>(p, rowid);
   sl.mrow = item_mask(p, rowid);
   sl.nch = p.NC;
+  // the draft token's logit (and whether the mask allows it), loaded now and
+  // used at the end
+  float x_logit = -INFINITY;
+  if (threadIdx.x == 0 && x >= 0 && x < p.V) {
+    const bool allowed = !sl.mrow || ((__ldg(sl.mrow + (x >> 5)) >> (x & 31)) & 1u);
+    if (allowed) x_logit = load_logit(sl.row, x);
+  }
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const bool use_k = p.top_k > 0 && p.top_k < p.V, use_p = p.top_p < 1.f;
   const uint32_t p_q = use_p ? (uint32_t)(p.top_p * 4294967296.f) : 0u;  // top_p * 2^32 (< 1)
   for (int i = threadIdx.x; i < (kCutWarps / 2) * 256 * 3; i += blockDim.x)
     (&sh->part[0][0][0])[i] = 0u;
 
-  // 1. the row max (NaN wins): the row's one HBM read.  On the vector paths
-  //    each warp first asks L2 for all of its chunks (bulk prefetches), so the
+  // 1. per chunk its max and the sum of 2^((l - max_c) c), as the streaming
+  //    kernel's records - the row's one HBM read.  On the vector paths each
+  //    warp first asks L2 for all of its chunks (bulk prefetches), so the
   //    whole row is in flight at once; two chunks per warp are loaded at a
-  //    time where a tile is 16 registers (bf16 vectors), one otherwise
+  //    time where a tile is 16 registers (bf16 vectors), one otherwise.  The
+  //    row max (NaN wins) and the row's mass in its frame follow from them.
   constexpr int kPair = L::NV * ((sizeof(typename L::Raw) + 3) / 4) <= 16 ? 2 : 1;  // registers
   if (VEC * sizeof(T) == 16 && lane == 0)
     for (int c = warp; c < sl.nch; c += kCutWarps)
       prefetch_l2(sl.row + c * kChunk, (uint32_t)(min(kChunk, p.V - c * kChunk) * sizeof(T)));
-  float lm = -INFINITY;
+  auto no_exclusion = [](typename L::Raw(&)[L::NV]) {};
   for (int c0 = warp; c0 < sl.nch; c0 += kPair * kCutWarps) {
     const int c1 = c0 + kCutWarps;
     typename L::Raw r0[L::NV], r1[L::NV];
     row_chunk<T, VEC>(p, sl, c0, r0);
     if (kPair == 2 && c1 < sl.nch) row_chunk<T, VEC>(p, sl, c1, r1);
-    lm = max_nan(lm, tile_max<T, VEC>(r0));
-    if (kPair == 2 && c1 < sl.nch) lm = max_nan(lm, tile_max<T, VEC>(r1));
+    const float2 q0 = chunk_softmax_ex<T, VEC>(r0, p.cc, no_exclusion);
+    if (lane == 0) sh->rec1[c0] = q0;
+    if (kPair == 2 && c1 < sl.nch) {
+      const float2 q1 = chunk_softmax_ex<T, VEC>(r1, p.cc, no_exclusion);
+      if (lane == 0) sh->rec1[c1] = q1;
+    }
   }
-  lm = warp_max_nan(lm);
-  if (lane == 0) sh->red_m[warp] = lm;
   __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = -INFINITY;
-    for (int w = 0; w < kCutWarps; ++w) t = max_nan(t, sh->red_m[w]);
-    sh->row_max = t;
-    sh->over = 0;
-    sh->x_entry = -1;
+  if (warp == 0) {
+    float mm = -INFINITY;
+    for (int c = lane; c < sl.nch; c += kWarp) mm = max_nan(mm, sh->rec1[c].x);
+    mm = warp_max_nan(mm);
+    float a = 0.f;
+    if (is_finite(mm))
+      for (int c = lane; c < sl.nch; c += kWarp) {
+        const float2 r = sh->rec1[c];
+        if (r.x > -INFINITY) a = fmaf(r.y, ex2((r.x - mm) * p.cc), a);
+      }
+    a = warp_sum(a);
+    if (lane == 0) {
+      sh->row_max = mm;
+      sh->row_s = a;
+      sh->over = 0;
+      sh->x_entry = -1;
+      // the candidates' bound: the least value v with fmaf(v, c, -m c) >=
+      // -18, as a value of the row's type (compared raw in pass 2)
+      if (is_finite(mm)) sh->cand_lo = cand_bound<T>(mm, p.cc);
+    }
   }
   __syncthreads();
   const float m = sh->row_max;
@@ -444,22 +526,20 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
   float thr = -INFINITY;
   bool done = false;  // records written (the candidate path)
   if (is_finite(m)) {
-    // 2a. the row's mass, the candidate marks and their number; each warp
-    //     stages its candidates' logits (a warp whose stage fills up sends
-    //     the row down the full-row path).  The mass outside the candidates
-    //     is the row's mass less the staged candidates'.
+    // 2a. the candidates - the elements within 2^-18 of the max's weight -
+    //     marked by a comparison with their bound, the row re-read from L2;
+    //     each warp stages its candidates' logits (a warp whose stage fills
+    //     up sends the row down the full-row path), then the candidates'
+    //     mass; the mass outside them is the row's mass less theirs
     constexpr int kCap = kStageBytes / (int)sizeof(T);
     constexpr bool kPacked = sizeof(T) == 2 && VEC == 8;
     T* st = reinterpret_cast<T*>(sh->stage[warp]);
+    const float lo = sh->cand_lo;
+    const uint32_t lo2 = kPacked ? bf16_pair_of(lo) : 0u;
     int base = 0;
     bool over = false;
-    float s0 = 0.f, s1 = 0.f;
-    const f32x2 c2 = pack2(p.cc, p.cc), nb2 = pack2(nb, nb);
-    f32x2 acc[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) acc[q] = pack2(0.f, 0.f);
     // (bf16 vectors: the next chunk's load is issued before this one is
-    // reduced)
+    // marked)
     constexpr bool kPipe = kPair == 2;
     typename L::Raw raw[L::NV], nxt[L::NV];
     if (kPipe && warp < sl.nch) row_chunk<T, VEC>(p, sl, warp, nxt);
@@ -472,29 +552,17 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
         row_chunk<T, VEC>(p, sl, c, raw);
       }
       uint32_t bits = 0u;
-      if constexpr (kPacked) {  // bf16 pairs: fma.rn.f32x2 and add.rn.f32x2
-#pragma unroll
-        for (int k = 0; k < L::NV; ++k) {
-          const uint32_t wd[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            float a0, a1;
-            unpack2(fma2(pack2(bf16_lo(wd[q]), bf16_hi(wd[q])), c2, nb2), a0, a1);
-            acc[q] = add2(acc[q], pack2(ex2(a0), ex2(a1)));
-            bits |= (a0 >= -kCandBits ? 1u : 0u) << (k * 8 + 2 * q);
-            bits |= (a1 >= -kCandBits ? 1u : 0u) << (k * 8 + 2 * q + 1);
-          }
-        }
+      if constexpr (kPacked) {  // the tile's 4 groups of 8 (bit 8 k + e: group k, element e)
+        mark_group_bf16<0>(bits, raw[0], lo2);
+        mark_group_bf16<1>(bits, raw[1], lo2);
+        mark_group_bf16<2>(bits, raw[2], lo2);
+        mark_group_bf16<3>(bits, raw[3], lo2);
       } else {
 #pragma unroll
         for (int k = 0; k < L::NV; ++k)
 #pragma unroll
-          for (int e = 0; e < VEC; ++e) {
-            const float a = fmaf(L::get(raw[k], e), p.cc, nb);
-            const float w = ex2(a);
-            if (e & 1) s1 += w; else s0 += w;
-            if (a >= -kCandBits) bits |= 1u << (k * VEC + e);
-          }
+          for (int e = 0; e < VEC; ++e)
+            if (L::get(raw[k], e) >= lo) bits |= 1u << (k * VEC + e);
       }
       const int cnt = __popc(bits);
       const int incl = warp_incl_scan_int(cnt);
@@ -524,20 +592,11 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
         over = true;
       }
     }
-    if constexpr (kPacked) {
-      float a0, a1, a2, a3;
-      unpack2(add2(acc[0], acc[1]), a0, a1);
-      unpack2(add2(acc[2], acc[3]), a2, a3);
-      s0 = a0 + a2;
-      s1 = a1 + a3;
-    }
-    const float s = warp_sum(s0 + s1);
     float sc = 0.f;  // the staged candidates' mass
     if (!over)
       for (int i = lane; i < base; i += kWarp) sc += ex2(fmaf(stage_value(st, i), p.cc, nb));
     sc = warp_sum(sc);
     if (lane == 0) {
-      sh->red_s[warp] = s;
       sh->red_t[warp] = sc;
       sh->red_n[warp] = base;
       sh->stage_n[warp] = base;
@@ -545,15 +604,13 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
     }
     __syncthreads();
     if (threadIdx.x == 0) {
-      float a = 0.f, tt = 0.f;
+      float tt = 0.f;
       int n = 0;
       for (int w = 0; w < kCutWarps; ++w) {
-        a += sh->red_s[w];
         tt += sh->red_t[w];
         n += sh->red_n[w];
       }
-      sh->row_s = a;
-      sh->row_tail = a - tt;
+      sh->row_tail = sh->row_s - tt;
       sh->row_n = n;
     }
     __syncthreads();
@@ -582,33 +639,37 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
         // 3. chunk records over the kept elements, which are all staged:
         //    {max, sum of 2^((l - max) c) leaving out the draft token
         //    (one-hot)} as the streaming kernel writes them
-        // One thread per chunk, over the chunk's run in its warp's stage.
+        // Warp w takes its own chunks (w + 16 t), whose runs are in its
+        // stage: the run's first 32 values are held one per lane (the rest,
+        // in long runs, are read again), the max comes from one warp-wide
+        // reduction of order keys, the sum from a fixed-order warp sum.
         const int x_entry = sh->x_entry;
         const int xc = (MODE == kOneHot && x >= 0 && x < p.V) ? x / kChunk : -1;
-        for (int c = threadIdx.x; c < sl.nch; c += blockDim.x) {
-          const T* cst = reinterpret_cast<const T*>(sh->stage[c % kCutWarps]);
+        const T* cst = reinterpret_cast<const T*>(sh->stage[warp]);
+        for (int c = warp; c < sl.nch; c += kCutWarps) {
           const int b0 = sh->seg[c], n0 = sh->seg_n[c];
-          float cm = -INFINITY;
-          for (int i = 0; i < n0; ++i) {
+          const float v0 = lane < n0 ? stage_value(cst, b0 + lane) : -INFINITY;
+          uint32_t kmax = v0 >= thr ? order_key(v0) : 0u;
+          for (int i = lane + kWarp; i < n0; i += kWarp) {
             const float v = stage_value(cst, b0 + i);
-            if (v >= thr) cm = fmaxf(cm, v);
+            if (v >= thr) kmax = max(kmax, order_key(v));
           }
+          kmax = __reduce_max_sync(0xffffffffu, kmax);
+          const float cm = kmax ? key_value(kmax) : -INFINITY;
           float cs = 0.f;
-          if (cm > -INFINITY) {
+          if (kmax) {
             const float nbc = -cm * p.cc;
-            const int skip = c == xc ? x_entry : -1;
-            for (int i = 0; i < n0; ++i) {
+            const int skip = (c == xc ? x_entry : -1) - b0;  // its place in the run
+            if (v0 >= thr && lane != skip) cs = ex2(fmaf(v0, p.cc, nbc));
+            for (int i = lane + kWarp; i < n0; i += kWarp) {
               const float v = stage_value(cst, b0 + i);
-              if (v >= thr && b0 + i != skip) cs += ex2(fmaf(v, p.cc, nbc));
+              if (v >= thr && i != skip) cs += ex2(fmaf(v, p.cc, nbc));
             }
+            cs = warp_sum(cs);
           }
-          p.rec[(long long)rowid * p.NC + c] = make_float2(cm, cs);
+          if (lane == 0) p.rec[(long long)rowid * p.NC + c] = make_float2(cm, cs);
         }
-        if (threadIdx.x == 0 && x >= 0 && x < p.V) {
-          const bool allowed = !sl.mrow || ((__ldg(sl.mrow + (x >> 5)) >> (x & 31)) & 1u);
-          const float v = load_logit(sl.row, x);
-          p.lx[rowid] = (allowed && v >= thr) ? v : -INFINITY;
-        }
+        if (threadIdx.x == 0 && x >= 0 && x < p.V) p.lx[rowid] = x_logit >= thr ? x_logit : -INFINITY;
         done = true;
       }
     }

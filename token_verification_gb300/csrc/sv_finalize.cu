@@ -534,7 +534,9 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const int K = p.K;
   float2* s_rec = p.fin_cache ? s_dyn : nullptr;
-  // The request's inputs do not depend on kernel A: read them before waiting.
+  // The request's inputs are read before waiting for kernel A: kernel A lets
+  // this kernel launch only after its own wait, when every earlier producer
+  // of the inputs has finished.
   const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
   const int Kv = (Kb >= 0 && Kb <= K) ? Kb : 0;
   const int x0 = warp < p.R ? row_token(p, b, warp, Kb) : -1;
@@ -1012,11 +1014,21 @@ template <typename T>
 __device__ int load_candidates(const VerifyParams& p, const TreeCall& t, int b, short* s_par,
                                short* s_depth, short* s_anc, int* s_tok, float* s_lx) {
   const int N = t.N;
+  constexpr int kPer = (kMaxTreeNodes + 127) / 128;  // nodes per thread (>= 128 threads)
+  int tk[kPer];  // the tokens' loads are issued before the parents'
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int n = 1 + threadIdx.x + i * (int)blockDim.x;
+    tk[i] = n <= N ? __ldg(t.tokens + (long long)b * N + n - 1) : 0;
+  }
   const bool tree_ok =
       load_tree(t.parent + (long long)b * t.parent_stride, N, t.D1 - 1, s_par, s_depth, s_anc);
   int bad = 0;
-  for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x) {
-    const int tok = __ldg(t.tokens + (long long)b * N + n - 1);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int n = 1 + threadIdx.x + i * (int)blockDim.x;
+    if (n > N) continue;
+    const int tok = tk[i];
     s_tok[n] = tok;
     const bool ok = tok >= 0 && tok < p.V;
     bad |= !ok;

@@ -73,13 +73,23 @@ __global__ void __launch_bounds__(kTreeThreads) tree_kernel(const __grid_constan
 
   pdl_begin();
   // every CTA of the cluster loads the same tree and reaches the same verdict
+  constexpr int kPer = (kMaxTreeNodes + kTreeThreads - 1) / kTreeThreads;
+  int tok[kPer];
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int n = 1 + threadIdx.x + i * kTreeThreads;
+    tok[i] = n <= p.N ? __ldg(p.tokens + (long long)b * p.N + n - 1) : 0;
+  }
   const bool tree_ok = load_tree(p.parent + (long long)b * p.parent_stride, p.N, p.D1 - 1, s_par,
                                  s_depth, s_anc);
   int bad = 0;
-  for (int n = 1 + threadIdx.x; n <= p.N; n += blockDim.x) {
-    const int t = __ldg(p.tokens + (long long)b * p.N + n - 1);
-    s_tok[n] = t;
-    bad |= (t < 0 || t >= p.V);
+#pragma unroll
+  for (int i = 0; i < kPer; ++i) {
+    const int n = 1 + threadIdx.x + i * kTreeThreads;
+    if (n <= p.N) {
+      s_tok[n] = tok[i];
+      bad |= (tok[i] < 0 || tok[i] >= p.V);
+    }
   }
   bad = __syncthreads_or(bad);
   int status = !tree_ok ? kBadTree : (bad ? kBadToken : 0);

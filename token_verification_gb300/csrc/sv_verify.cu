@@ -61,8 +61,11 @@ template <int MODE, typename T, int VEC>
 __global__ void __launch_bounds__(kThreads, 2) verify_rows_kernel(const VerifyParams p) {
   using L = Lane<T, VEC>;
   constexpr int G = L::G;
+  // Launched early (programmatic dependent launch): wait for the predecessor,
+  // then let the finalize kernel launch - it reads the call's inputs before
+  // its own wait, which is safe once everything before this kernel is done.
+  pdl_wait();
   pdl_launch_dependents();
-  pdl_wait();  // launched early (programmatic dependent launch): wait for the predecessor
   const int lane = lane_id();
   const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
   const long long nw = ((long long)gridDim.x * blockDim.x) >> 5;
@@ -199,8 +202,11 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
   using ST = Stream<T>;
   constexpr int S = ST::kStages;
   extern __shared__ __align__(128) unsigned char smem[];
+  // Launched early (programmatic dependent launch): wait for the predecessor,
+  // then let the finalize kernel launch - it reads the call's inputs before
+  // its own wait, which is safe once everything before this kernel is done.
+  pdl_wait();
   pdl_launch_dependents();
-  pdl_wait();  // launched early (programmatic dependent launch): wait for the predecessor
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const uint32_t base = smem_u32(smem);
   auto stage_of = [&](int s) { return base + s * ST::kStageBytes; };
