@@ -107,12 +107,12 @@ __device__ __forceinline__ uint32_t bf16_pair_of(float v) {
 }
 
 // Sets bit POS of `bits` if the low bf16 of w is >= the threshold's, bit
-// POS + 1 if the high one is (a packed comparison; -inf never, NaN never).
+// POS + 1 if the high one is: one packed comparison (its first predicate
+// is the low halves') and two predicated ORs; -inf and NaN never pass.
 template <int POS>
 __device__ __forceinline__ void mark_ge_bf16x2(uint32_t& bits, uint32_t w, uint32_t t2) {
-  asm("{\n\t.reg .pred p, q;\n\t.reg .b16 wl, wh, tl, th;\n\t"
-      "mov.b32 {wl, wh}, %1;\n\tmov.b32 {tl, th}, %2;\n\t"
-      "setp.ge.bf16 p, wl, tl;\n\tsetp.ge.bf16 q, wh, th;\n\t"
+  asm("{\n\t.reg .pred p, q;\n\t"
+      "setp.ge.bf16x2 p|q, %1, %2;\n\t"
       "@p or.b32 %0, %0, %3;\n\t@q or.b32 %0, %0, %4;\n\t}"
       : "+r"(bits)
       : "r"(w), "r"(t2), "n"(1u << POS), "n"(2u << POS));
@@ -133,7 +133,7 @@ __device__ __forceinline__ int level_digit(float a) { return 255 - __float2int_r
 
 // Shared memory of a filter CTA.  Histograms per warp pair, of three 13-bit
 // limbs (a warp pair sees at most 2^15 elements, so a limb sum stays below
-// 2^28).  Each warp stages the logits of its candidates in (chunk, lane,
+// 2^28; three 32-bit atomics cost less than one 64-bit one).  Each warp stages the logits of its candidates in (chunk, lane,
 // element) order; chunk c's run starts at seg[c] in the stage of warp c % 16.
 struct CutShared {
   uint32_t part[kCutWarps / 2][256][3];  // per warp pair: limbs of each bin (counts: [0])
@@ -162,7 +162,7 @@ __device__ __forceinline__ uint16_t stage_bits(float v, const uint16_t*) {
 __device__ __forceinline__ float stage_bits(float v, const float*) { return v; }
 
 // Adds one element's weight w (MASS: as a fixed-point mass) or a count of
-// `n` to bin `bin` of a per-warp histogram.
+// `n` to bin `bin` of a warp pair's histogram.
 template <bool MASS>
 __device__ __forceinline__ void add_to_bin(uint32_t (*mine)[3], int bin, float w, uint32_t n = 1) {
   if (MASS) {
@@ -539,18 +539,9 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
     int base = 0;
     bool over = false;
     // (bf16 vectors: the next chunk's load is issued before this one is
-    // marked)
+    // marked, into the other of two tiles)
     constexpr bool kPipe = kPair == 2;
-    typename L::Raw raw[L::NV], nxt[L::NV];
-    if (kPipe && warp < sl.nch) row_chunk<T, VEC>(p, sl, warp, nxt);
-    for (int c = warp; c < sl.nch; c += kCutWarps) {
-      if (kPipe) {
-#pragma unroll
-        for (int k = 0; k < L::NV; ++k) raw[k] = nxt[k];
-        if (c + kCutWarps < sl.nch) row_chunk<T, VEC>(p, sl, c + kCutWarps, nxt);
-      } else {
-        row_chunk<T, VEC>(p, sl, c, raw);
-      }
+    auto mark_and_stage = [&](typename L::Raw(&raw)[L::NV], int c) {
       uint32_t bits = 0u;
       if constexpr (kPacked) {  // the tile's 4 groups of 8 (bit 8 k + e: group k, element e)
         mark_group_bf16<0>(bits, raw[0], lo2);
@@ -590,6 +581,24 @@ __global__ void __launch_bounds__(kCutThreads, 2) filter_rows_kernel(const Verif
         base += total;
       } else {
         over = true;
+      }
+    };
+    typename L::Raw ra[L::NV], rb[L::NV];
+    if (kPipe) {
+      if (warp < sl.nch) row_chunk<T, VEC>(p, sl, warp, ra);
+      for (int c = warp; c < sl.nch; c += 2 * kCutWarps) {
+        const int c1 = c + kCutWarps;
+        if (c1 < sl.nch) row_chunk<T, VEC>(p, sl, c1, rb);
+        mark_and_stage(ra, c);
+        if (c1 < sl.nch) {
+          if (c1 + kCutWarps < sl.nch) row_chunk<T, VEC>(p, sl, c1 + kCutWarps, ra);
+          mark_and_stage(rb, c1);
+        }
+      }
+    } else {
+      for (int c = warp; c < sl.nch; c += kCutWarps) {
+        row_chunk<T, VEC>(p, sl, c, ra);
+        mark_and_stage(ra, c);
       }
     }
     float sc = 0.f;  // the staged candidates' mass
