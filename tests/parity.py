@@ -21,7 +21,9 @@ excluding it:
   * draws: the token must equal the oracle's; where it does not, the
     oracle's draw must be flagged with a margin of at most STRICT_TOL, and
     the GPU's token's exact (fp64) CDF step, from the oracle's probe, must
-    come within FLAG_TOL * W of u * W;
+    come within FLAG_TOL * W of u * W; the differing draws are counted by
+    margin band, and in a flag-rate run they may be at most MAX_DIFFER_RATE
+    of the positions;
   * accept probabilities within PROB_ATOL, at every position (-1 where a
     position was not tested).
 Greedy and tree-greedy verification are compared bit-exactly.
@@ -39,6 +41,12 @@ PROB_ATOL = 1e-5
 FLAG_TOL = 1e-5     # the oracle's flag band
 STRICT_TOL = 1e-6   # a GPU result may leave the oracle's only within this margin
 BANDS = (1e-5, 1e-6, 1e-7, 1e-8)
+# Draws that differ from the oracle's (each within STRICT_TOL and verified)
+# may be at most this share of the positions in a flag-rate run: the oracle
+# alone puts 7.8e-3 of the draws of the 152064-token one-hot workload within
+# 1e-6 of a step edge, where an fp32 sampler may legitimately land on either
+# side; the GPU has differed on at most 4.1e-4.
+MAX_DIFFER_RATE = 1e-3
 
 
 def to_device(wl, device="cuda"):
@@ -236,6 +244,7 @@ def assert_report(rep: SampleReport, max_flag_rate=None):
     assert not rep.errors, "%d mismatching requests, first: %s" % (len(rep.errors), rep.errors[:5])
     if max_flag_rate is not None:
         assert rep.acc_flagged <= max_flag_rate * rep.positions, rep.summary()
+        assert rep.cdf_differ <= MAX_DIFFER_RATE * rep.positions, rep.summary()
 
 
 def check_sample(wl, gpu, temperature=None, threads=16, flag_rate=None) -> SampleReport:

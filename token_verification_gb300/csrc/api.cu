@@ -347,6 +347,15 @@ static sv_status tree_rows_call(int mode, const void* target, const int32_t* tre
   if (p.total_tasks >= (1LL << 31)) return SV_ERR_SHAPE;
   p.div_tpr = make_fastdiv((uint32_t)p.TPR);
   p.div_r = make_fastdiv((uint32_t)R);
+  // every row of the tree is needed and the rows are contiguous: on the
+  // streaming path items run across row boundaries, all G chunks long
+  const long long chunks = (long long)B * R * p.NC;
+  if (vec && chunks < (1LL << 31)) {
+    p.flat = 1;
+    p.total_chunks = (int)chunks;
+    p.div_nc = make_fastdiv((uint32_t)p.NC);
+    p.total_tasks = (chunks + G - 1) / G;
+  }
   p.cc = (float)(1.4426950408889634 / (double)T);
   p.wait_ns = wait_limit_ns();
   p.tree_parent = tree_parent;

@@ -65,6 +65,13 @@ struct VerifyParams {
   int item_chunks;   // chunks per stream item
   long long total_tasks;  // < 2^31 (checked on the host)
   FastDiv div_tpr, div_r; // divide by TPR and by R
+  // Items across row boundaries: item it is chunks it*item_chunks onwards of
+  // the call's rows in order (every row needed, rows at a stride of V, no
+  // draft tokens or masks: the tree calls), so every item but the last is
+  // item_chunks long whatever V; 0: items stop at the end of each row.
+  int flat;
+  int total_chunks;       // B * R * NC when flat (< 2^31)
+  FastDiv div_nc;         // divide by NC
   float cc;          // log2(e) / T
   int greedy_prob;   // greedy rule reached through the sampling entry
   int compact_in_finalize;  // the finalize kernel writes the packed output

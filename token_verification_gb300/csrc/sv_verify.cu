@@ -39,6 +39,16 @@ struct Item {
 template <int MODE>
 __device__ __forceinline__ Item decode_item(const VerifyParams& p, uint32_t it) {
   Item k;
+  if (p.flat) {  // items across row boundaries (tree calls: no draft tokens)
+    const uint32_t g0 = it * (uint32_t)p.item_chunks;
+    const uint32_t row = fast_div(g0, p.div_nc);
+    k.rowid = (int)row;
+    k.c0 = (int)(g0 - row * (uint32_t)p.NC);
+    k.nch = min(p.item_chunks, p.total_chunks - (int)g0);
+    k.need = true;
+    k.x = -1;
+    return k;
+  }
   const uint32_t row = fast_div(it, p.div_tpr);  // total items < 2^31
   const int part = (int)(it - row * (uint32_t)p.TPR);
   const int b = (int)fast_div(row, p.div_r);
@@ -251,8 +261,18 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
       }
       meta[s] = make_int4(item.rowid, item.c0, item.nch, item.x);
       const T* src = item_row<T>(p, item.rowid) + (long long)item.c0 * kChunk;
-      const uint32_t bytes =
+      uint32_t bytes =
           (uint32_t)(min(item.nch * kChunk, p.V - item.c0 * kChunk) * (int)sizeof(T));
+      if (p.flat) {  // through the item's last chunk, rows being contiguous
+        int cl = item.c0 + item.nch - 1, rows = 0;
+        while (cl >= p.NC) {
+          cl -= p.NC;
+          ++rows;
+        }
+        bytes = (uint32_t)(((long long)rows * p.V + min((cl + 1) * kChunk, p.V) -
+                            (long long)item.c0 * kChunk) *
+                           (long long)sizeof(T));
+      }
       if (p.mask_bulk) {  // the item's mask words travel with its logits
         const int w0 = item.c0 * kWarp;
         const uint32_t mbytes = (uint32_t)(min(item.nch * kWarp, p.mask_words - w0) * 4);
@@ -320,18 +340,27 @@ __global__ void __launch_bounds__(kStreamThreads, 2) verify_stream_kernel(const 
       }
       if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
     } else if (w < m.z) {
-      const int c = m.y + w;
+      int c = m.y + w, row = m.x;
+      uint32_t off = w * ST::kChunkBytes;
+      if (!kMasked && p.flat && c >= p.NC) {  // past the end of the item's first row
+        while (c >= p.NC) {
+          c -= p.NC;
+          ++row;
+        }
+        off = (uint32_t)((((long long)(row - m.x) * p.V) + (long long)(c - m.y) * kChunk) *
+                         (long long)sizeof(T));
+      }
       typename L::Raw raw[L::NV];
-      load_chunk_smem<T, VEC>(stage_of(s) + w * ST::kChunkBytes, p.V, c, raw);
-      record_draft_logit<T, VEC>(p, raw, c, m.x, m.w);
+      load_chunk_smem<T, VEC>(stage_of(s) + off, p.V, c, raw);
+      record_draft_logit<T, VEC>(p, raw, c, row, m.w);
       float2 out;
       if constexpr (MODE == kTreeSample)
-        out = tree_chunk_record<T, VEC>(p, raw, m.x, c);
+        out = tree_chunk_record<T, VEC>(p, raw, row, c);
       else
         out = chunk_record<MODE, T, VEC>(
             raw, c, p.cc, MODE == kOneHot ? m.w : -1,
-            MODE == kTypical ? p.ent + (long long)m.x * p.NC + c : nullptr);
-      if (lane == 0) p.rec[(long long)m.x * p.NC + c] = out;
+            MODE == kTypical ? p.ent + (long long)row * p.NC + c : nullptr);
+      if (lane == 0) p.rec[(long long)row * p.NC + c] = out;
     }
     // this warp's values from the stage are consumed: hand it back
     __syncwarp();
