@@ -81,7 +81,24 @@ __device__ __forceinline__ float2 tree_chunk_record(
   const int* par = p.tree_parent + (long long)b * p.parent_stride;
   const int* tok = p.tree_tokens + (long long)b * N;
   const int lo = c * kChunk;
+  // Trees of up to 64 nodes: the children's offsets in this chunk are looked
+  // up before the max, two nodes per lane, their four loads in flight at once.
+  int off0 = -1, off1 = -1;
+  if (N <= 2 * kWarp) {
+    const int n0 = lane_id(), n1 = n0 + kWarp;
+    const int pa0 = n0 < N ? __ldg(par + n0) : -1, pa1 = n1 < N ? __ldg(par + n1) : -1;
+    const int t0 = n0 < N ? __ldg(tok + n0) - lo : -1, t1 = n1 < N ? __ldg(tok + n1) - lo : -1;
+    if (pa0 == r && t0 >= 0 && t0 < kChunk) off0 = t0;
+    if (pa1 == r && t1 >= 0 && t1 < kChunk) off1 = t1;
+  }
   return chunk_softmax_ex<T, VEC>(raw, p.cc, [&](Raw(&rr)[Lane<T, VEC>::NV]) {
+    if (N <= 2 * kWarp) {
+      for (unsigned hit = __ballot_sync(0xffffffffu, off0 >= 0); hit; hit &= hit - 1u)
+        mask_element<T, VEC>(rr, __shfl_sync(0xffffffffu, off0, __ffs(hit) - 1));
+      for (unsigned hit = __ballot_sync(0xffffffffu, off1 >= 0); hit; hit &= hit - 1u)
+        mask_element<T, VEC>(rr, __shfl_sync(0xffffffffu, off1, __ffs(hit) - 1));
+      return;
+    }
     for (int n0 = 0; n0 < N; n0 += kWarp) {
       const int n = n0 + lane_id();
       int off = -1;
