@@ -47,6 +47,7 @@ BANDS = (1e-5, 1e-6, 1e-7, 1e-8)
 # 1e-6 of a step edge, where an fp32 sampler may legitimately land on either
 # side; the GPU has differed on at most 4.1e-4.
 MAX_DIFFER_RATE = 1e-3
+MIN_RATE_POSITIONS = 10000  # the rate is asserted over runs at least this large
 
 
 def to_device(wl, device="cuda"):
@@ -244,7 +245,8 @@ def assert_report(rep: SampleReport, max_flag_rate=None):
     assert not rep.errors, "%d mismatching requests, first: %s" % (len(rep.errors), rep.errors[:5])
     if max_flag_rate is not None:
         assert rep.acc_flagged <= max_flag_rate * rep.positions, rep.summary()
-        assert rep.cdf_differ <= MAX_DIFFER_RATE * rep.positions, rep.summary()
+        if rep.positions >= MIN_RATE_POSITIONS:
+            assert rep.cdf_differ <= MAX_DIFFER_RATE * rep.positions, rep.summary()
 
 
 def check_sample(wl, gpu, temperature=None, threads=16, flag_rate=None) -> SampleReport:

@@ -522,21 +522,27 @@ __device__ __forceinline__ int position_draw(const VerifyParams& p, int b, int r
 // position's token, or the argmax (greedy).  Dynamic shared memory: [R*NC]
 // records when cached.  A dense-draft request rejected at n is published for
 // kernel R, which writes its outputs.
-template <int MODE, typename T, int VEC>
-__global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const VerifyParams p) {
-  constexpr int kWarps = fin_threads<MODE>() / kWarp;
-  extern __shared__ float2 s_dyn[];
-  __shared__ RowSum srow[kMaxRows];
-  __shared__ Residual s_resid;
-  __shared__ int s_last[32];
-  __shared__ int s_tok[kMaxRows];  // the token each position would draw
-  const int b = blockIdx.x;
+// Shared memory of one request's finalisation.
+struct FinShared {
+  RowSum srow[kMaxRows];
+  Residual resid;
+  int last[32];
+  int tok[kMaxRows];  // the token each position would draw
+};
+
+// Request b's finalisation by the calling CTA (every thread; any multiple
+// of 32 threads).  wait() is called by every thread once the request's
+// inputs are loaded and before its records are read.  s_rec: the request's
+// [R*NC] records copied to shared memory for the draws, or null.
+template <int MODE, typename T, int VEC, class Wait>
+__device__ __forceinline__ void finalize_one(const VerifyParams& p, int b, FinShared& fs,
+                                             float2* s_rec, Wait wait) {
+  const int nwarps = (int)(blockDim.x >> 5);
   const int lane = lane_id(), warp = threadIdx.x >> 5;
   const int K = p.K;
-  float2* s_rec = p.fin_cache ? s_dyn : nullptr;
-  // The request's inputs are read before waiting for kernel A: kernel A lets
-  // this kernel launch only after its own wait, when every earlier producer
-  // of the inputs has finished.
+  // The request's inputs are read before waiting for its records: kernel A
+  // lets the finalize kernel launch only after its own wait, when every
+  // earlier producer of the inputs has finished.
   const int Kb = p.draft_lens ? __ldg(p.draft_lens + b) : K;
   const int Kv = (Kb >= 0 && Kb <= K) ? Kb : 0;
   const int x0 = warp < p.R ? row_token(p, b, warp, Kb) : -1;
@@ -547,51 +553,62 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
     if (lane < Kv) x = __ldg(p.draft_tokens + (long long)b * K + lane);
     if (MODE != kGreedy && lane < Kv) u = __ldg(p.uniforms + (long long)b * (K + 1) + lane);
   }
-  if (threadIdx.x == 0) s_resid.n = -1;
-  pdl_wait();
-  pdl_launch_dependents();
+  if (threadIdx.x == 0) fs.resid.n = -1;
+  wait(Kb);
   if (p.out_cut)  // filtered calls: each row's cut value, NaN for rows not needed
     for (int r = threadIdx.x; r < p.R; r += blockDim.x)
       p.out_cut[(long long)b * p.R + r] =
           row_needed(p, r, Kb) ? __ldcg(p.thr + (long long)b * p.R + r) : qnan();
   // issued before the row summaries so that its latency overlaps theirs
   const int timed_out = warp == 0 ? __ldcg(p.err) : 0;
-  for (int r = warp; r < p.R; r += kWarps) {
+  for (int r = warp; r < p.R; r += nwarps) {
     RowSum rs{qnan(), 0.f, 0.f, -1, 0.f};
     const int xr = r == warp ? x0 : row_token(p, b, r, Kb);
     if (row_needed(p, r, Kb))
       rs = summarise_row<MODE, T>(p, b, r, Kb, xr, s_rec ? s_rec + (long long)r * p.NC : nullptr);
-    if (lane == 0) srow[r] = rs;
+    if (lane == 0) fs.srow[r] = rs;
     // target row r <= K_b: the draw of position r (dense drafts: the bonus
     // position only; the others draw from the residual)
     if (MODE != kGreedy && Kb >= 0 && Kb <= K && r <= Kb && (MODE != kDense || r == Kb)) {
       const int tok = position_draw<MODE, T, VEC>(p, b, r, Kb, rs, xr, uK, s_rec);
-      if (lane == 0) s_tok[r] = tok;
+      if (lane == 0) fs.tok[r] = tok;
     }
   }
   __syncthreads();
   if (warp == 0)
-    finalize_request<MODE, T, VEC>(p, b, Kb, srow, s_tok, x, u, timed_out, &s_resid);
+    finalize_request<MODE, T, VEC>(p, b, Kb, fs.srow, fs.tok, x, u, timed_out, &fs.resid);
   __syncthreads();
   // Dense drafts, rejected at n: the request is published for the residual
   // kernel, which reads its row pair with every SM and writes its outputs.
-  if (MODE == kDense && threadIdx.x == 0 && s_resid.n >= 0) {
+  if (MODE == kDense && threadIdx.x == 0 && fs.resid.n >= 0) {
     const int slot = atomicAdd(p.n_pend, 1);
     p.pend[slot] = b;
-    p.rpn[slot] = s_resid.n;
-    p.rpar[slot] = make_float4(s_resid.mp, s_resid.ip, s_resid.mq, s_resid.iq);
+    p.rpn[slot] = fs.resid.n;
+    p.rpar[slot] = make_float4(fs.resid.mp, fs.resid.ip, fs.resid.mq, fs.resid.iq);
   }
   // The last request of the call clears the counters and (without dense
   // drafts, whose residual kernel comes last) writes the packed output.
-  if (threadIdx.x == 0) s_last[0] = atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B;
+  if (threadIdx.x == 0) fs.last[0] = atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B;
   __syncthreads();
-  if (!s_last[0]) return;
+  if (!fs.last[0]) return;
   if (threadIdx.x == 0) {
     *p.err = 0;
     *p.fin_ticket = 0;
     *p.work = 0u;
   }
-  if (MODE != kDense && p.compact_in_finalize) compact_all(p, s_last);
+  if (MODE != kDense && p.compact_in_finalize) compact_all(p, fs.last);
+}
+
+// Kernel F: one CTA per request, chained to kernel A by programmatic
+// dependent launch.  Dynamic shared memory: [R*NC] records when cached.
+template <int MODE, typename T, int VEC>
+__global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const VerifyParams p) {
+  extern __shared__ float2 s_dyn[];
+  __shared__ FinShared fs;
+  finalize_one<MODE, T, VEC>(p, blockIdx.x, fs, p.fin_cache ? s_dyn : nullptr, [](int) {
+    pdl_wait();
+    pdl_launch_dependents();
+  });
 }
 
 template <int MODE, typename T, int VEC>
