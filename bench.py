@@ -39,7 +39,8 @@ FALLBACK_HBM_GBS = 6800.0
 # the sources of each profiled kernel (a profile's DRAM figure counts only
 # while these are unchanged)
 KERNEL_SOURCES = {
-    "stream": ["token_verification_gb300/csrc/sv_verify.cu",
+    "stream": ["token_verification_gb300/csrc/sv_stream.cuh",
+               "token_verification_gb300/csrc/sv_verify.cu",
                "token_verification_gb300/csrc/sv_rows.cuh",
                "token_verification_gb300/csrc/sv_common.cuh"],
     "filter": ["token_verification_gb300/csrc/sv_filter.cu",
