@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libspecverify.so")
 SOURCES = ["api.cu", "sv_verify.cu", "sv_finalize.cu", "sv_filter.cu", "sv_tree.cu", "sv_noalloc.cu", "sv_ngram.cu"]
-HEADERS = ["sv_common.cuh", "sv_launch.h", "sv_rows.cuh"]
+HEADERS = ["sv_common.cuh", "sv_launch.h", "sv_rows.cuh", "sv_stream.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-I" + os.path.join(ROOT, "include")]
