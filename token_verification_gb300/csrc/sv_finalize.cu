@@ -949,9 +949,9 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
 // ---------------------------------------------------------------------------
 
 // One CTA per request: every row's summary (max, sum, entropy), every node's
-// typical test under its parent's distribution, the accepted subtree by one
-// thread in node order (a parent precedes its children), the deepest
-// accepted node (lowest id among equals), then the draw from its row.
+// typical test under its parent's distribution, the accepted subtree a depth
+// level at a time, the deepest accepted node (lowest id among equals) by one
+// reduction, then the draw from its row.
 constexpr int kTreeTypicalThreads = 512;
 constexpr size_t kTreeCacheLimit = 96 * 1024;  // records kept in shared memory for the draw
 
@@ -1102,6 +1102,7 @@ __global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const
   __shared__ float s_lx[kMaxTreeNodes + 1];
   __shared__ unsigned char spass[kMaxTreeNodes + 1], sacc[kMaxTreeNodes + 1];
   __shared__ int s_best, s_status;
+  __shared__ unsigned s_key[kTreeTypicalThreads / kWarp];
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5;
   const int N = t.N;
@@ -1124,19 +1125,35 @@ __global__ void __launch_bounds__(kTreeTypicalThreads) tree_typical_kernel(const
     }
     spass[n] = ok;
   }
+  // The accepted nodes, a depth level at a time (a node is accepted when it
+  // passes and its parent is accepted; the tree was checked, every node's
+  // depth is at most max_depth), then the deepest one, the lowest id among
+  // equals, by one reduction of (depth, -id) keys.
+  if (threadIdx.x == 0) sacc[0] = 1;
   __syncthreads();
+  if (!status_in)
+    for (int d = 1; d < t.D1; ++d) {
+      for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x)
+        if (s_depth[n] == d) sacc[n] = sacc[s_par[n]] && spass[n];
+      __syncthreads();
+    }
+  unsigned key = 0u;
+  int bad = 0;
+  if (!status_in)
+    for (int n = 1 + threadIdx.x; n <= N; n += blockDim.x)
+      if (sacc[n]) {
+        key = max(key, ((unsigned)s_depth[n] << 16) | (0xffffu - (unsigned)n));
+        bad |= !is_finite(srow[n].m);  // an accepted node's row is needed
+      }
+  key = __reduce_max_sync(0xffffffffu, key);
+  if (lane_id() == 0) s_key[warp] = key;
+  bad = __syncthreads_or(bad);
   if (threadIdx.x == 0) {
     int status = status_in ? status_in : (__ldcg(p.err) ? kTimeout : 0);
-    sacc[0] = 1;
-    int best = 0;
-    if (!status && !is_finite(srow[0].m)) status = kBadLogits;
-    for (int n = 1; n <= N && !status; ++n) {
-      sacc[n] = sacc[s_par[n]] && spass[n];
-      if (!sacc[n]) continue;
-      if (!is_finite(srow[n].m)) status = kBadLogits;  // an accepted node's row is needed
-      if (s_depth[n] > s_depth[best]) best = n;
-    }
-    s_best = best;
+    if (!status && (!is_finite(srow[0].m) || bad)) status = kBadLogits;
+    unsigned k = 0u;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) k = max(k, s_key[w]);
+    s_best = k ? (int)(0xffffu - (k & 0xffffu)) : 0;
     s_status = status;
   }
   __syncthreads();
