@@ -513,15 +513,6 @@ __device__ __forceinline__ int position_draw(const VerifyParams& p, int b, int r
                                           p.mask_words, cut);
 }
 
-// Rows are summarised by the CTA's warps, each of which also draws the token
-// its own position would emit if the walk stopped there (the residual or
-// bonus draw of rejection sampling, §2.1 of the page cited at the top of this
-// file); their chunk records are kept in shared memory (dynamic, when they
-// fit) for the draws.  Then one warp runs the acceptance tests of all
-// positions at once (one lane per position) and takes the stopping
-// position's token, or the argmax (greedy).  Dynamic shared memory: [R*NC]
-// records when cached.  A dense-draft request rejected at n is published for
-// kernel R, which writes its outputs.
 // Shared memory of one request's finalisation.
 struct FinShared {
   RowSum srow[kMaxRows];
@@ -531,9 +522,17 @@ struct FinShared {
 };
 
 // Request b's finalisation by the calling CTA (every thread; any multiple
-// of 32 threads).  wait() is called by every thread once the request's
-// inputs are loaded and before its records are read.  s_rec: the request's
-// [R*NC] records copied to shared memory for the draws, or null.
+// of 32 threads).  Rows are summarised by the CTA's warps, each of which also
+// draws the token its own position would emit if the walk stopped there (the
+// residual or bonus draw of rejection sampling, §2.1 of the page cited at
+// the top of this file); their chunk records are kept in shared memory (when
+// they fit) for the draws.  Then one warp runs the acceptance tests of all
+// positions at once (one lane per position) and takes the stopping
+// position's token, or the argmax (greedy).  A dense-draft request rejected
+// at n is published for kernel R, which writes its outputs.  wait() is called
+// by every thread once the request's inputs are loaded and before its
+// records are read.  s_rec: the request's [R*NC] records copied to shared
+// memory for the draws, or null.
 template <int MODE, typename T, int VEC, class Wait>
 __device__ __forceinline__ void finalize_one(const VerifyParams& p, int b, FinShared& fs,
                                              float2* s_rec, Wait wait) {

@@ -10,15 +10,16 @@
 // tempered softmax's maximum and sum (or the argmax) and the draft token's
 // logit, which this kernel provides.
 //
-// Kernel A (verify_stream_kernel; verify_rows_kernel on the scalar path)
-//   reads every needed logit once and reduces each 1024-logit chunk of a row
-//   to one 8-byte record.  One producer thread per CTA copies items of 15
-//   consecutive chunks (30 KB of bf16) into a ring of shared-memory stages
-//   with cp.async.bulk; each of the 15 consumer warps reduces one chunk of
-//   every stage.  The only shared state is a work counter from which the
-//   producers take their items.  The per-request work (tests, draws, packed
-//   output) is kernel F's
-//   (sv_finalize.cu); filtered calls use kernel A' (sv_filter.cu) instead.
+// Kernel A (verify_stream_kernel; verify_rows_kernel on the scalar path;
+//   both in sv_stream.cuh) reads every needed logit once and reduces each
+//   1024-logit chunk of a row to one 8-byte record.  One producer thread per
+//   CTA copies items of 15 consecutive chunks (30 KB of bf16) into a ring of
+//   shared-memory stages with cp.async.bulk; each of the 15 consumer warps
+//   reduces one chunk of every stage.  The only shared state is a work
+//   counter from which the producers take their items.  This file launches
+//   it per mode; the per-request work (tests, draws, packed output) is
+//   kernel F's (sv_finalize.cu); filtered calls use kernel A' (sv_filter.cu)
+//   instead.
 #include "sv_stream.cuh"
 
 namespace sv {
