@@ -92,13 +92,29 @@ def hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def _code_only(text):
+    """C++ source without its // comments and blank runs: edits to comments
+    alone do not change the compiled kernel."""
+    out = []
+    for line in text.splitlines():
+        i = line.find("//")
+        if i >= 0 and line.count('"', 0, i) % 2 == 0:
+            line = line[:i]
+        line = line.rstrip()
+        if line:
+            out.append(line)
+    return "\n".join(out)
+
+
 def kernel_source_hash(kind="stream"):
+    """Hash of the code (comments left out) of the sources a profiled kernel
+    is built from."""
     if kind not in KERNEL_SOURCES:
         return None
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES[kind]:
-        with open(os.path.join(ROOT, rel), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as f:
+            h.update(_code_only(f.read()).encode("utf-8"))
     return h.hexdigest()[:16]
 
 

@@ -89,9 +89,9 @@ def test_reference_arm_greedy_and_tree_modes():
 
 def test_profiled_traffic_follows_its_kernel_sources(tmp_path, monkeypatch):
     """A profile's DRAM bytes (profiles/traffic.json) are reported only while
-    the sources of the kernel it was taken on are unchanged (each profiled
-    kernel has its own source list); the committed entries name kernels the
-    bench knows and summaries that exist."""
+    the code of the kernel it was taken on is unchanged (each profiled kernel
+    has its own source list; comments do not count); the committed entries
+    name kernels the bench knows and summaries that exist."""
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         committed = json.load(f)
     for (workload, mode), name in bench.PROFILE_NAMES.items():
@@ -106,15 +106,19 @@ def test_profiled_traffic_follows_its_kernel_sources(tmp_path, monkeypatch):
         for rel in files:
             src = tmp_path / rel
             src.parent.mkdir(parents=True, exist_ok=True)
-            src.write_text("// %s\n" % rel)
+            src.write_text("// %s\nint f_%d;\n" % (rel, len(rel)))
     h = bench.kernel_source_hash("filter")
     assert h != bench.kernel_source_hash("stream")
+    # an edit to comments alone keeps the hash; an edit to code changes it
+    src = tmp_path / bench.KERNEL_SOURCES["filter"][0]
+    src.write_text("// reworded\n" + src.read_text() + "   // and more\n\n")
+    assert bench.kernel_source_hash("filter") == h
     (prof / "traffic.json").write_text(json.dumps(
         {"p": {"kernel": "filter", "kernel_source_hash": h, "dram_bytes_per_launch": 1234},
          "q": {"kernel": "stream", "kernel_source_hash": h, "dram_bytes_per_launch": 99}}))
     assert bench.profiled_traffic("p") == 1234
     assert bench.profiled_traffic("q") is None  # another kernel's sources
-    (tmp_path / bench.KERNEL_SOURCES["filter"][0]).write_text("// changed\n")
+    (tmp_path / bench.KERNEL_SOURCES["filter"][0]).write_text("int changed;\n")
     assert bench.profiled_traffic("p") is None  # the kernel changed since
     assert bench.profiled_traffic(None) is None and bench.profiled_traffic("nope") is None
 
