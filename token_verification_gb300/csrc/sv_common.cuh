@@ -494,24 +494,46 @@ __device__ __forceinline__ float2 chunk_softmax_ex(
   if constexpr (kPacked) {
     const f32x2 c2 = pack2(cc, cc), nb2 = pack2(nb, nb);
     f32x2 acc[4];  // four independent accumulation chains
+    f32x2 eacc[2];  // the entropy accumulator: w t as one packed fma per pair
 #pragma unroll
     for (int q = 0; q < 4; ++q) acc[q] = pack2(0.f, 0.f);
+    eacc[0] = eacc[1] = pack2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
+        const f32x2 a2 = fma2(pack2(bf16_lo(w[q]), bf16_hi(w[q])), c2, nb2);
         float a0, a1;
-        unpack2(fma2(pack2(bf16_lo(w[q]), bf16_hi(w[q])), c2, nb2), a0, a1);
-        const float e0 = ex2(a0), e1 = ex2(a1);
-        acc[q] = add2(acc[q], pack2(e0, e1));
-        if (ent) et = fmaf(e1, fmaxf(a1, -256.f), fmaf(e0, fmaxf(a0, -256.f), et));
+        unpack2(a2, a0, a1);
+        const f32x2 e2 = pack2(ex2(a0), ex2(a1));
+        acc[q] = add2(acc[q], e2);
+        if (ent) eacc[q & 1] = fma2(e2, a2, eacc[q & 1]);
       }
     }
     float s0, s1, s2, s3;
     unpack2(add2(acc[0], acc[1]), s0, s1);
     unpack2(add2(acc[2], acc[3]), s2, s3);
     s = (s0 + s1) + (s2 + s3);
+    if (ent) {
+      float t0, t1;
+      unpack2(add2(eacc[0], eacc[1]), t0, t1);
+      et = t0 + t1;
+      // a -inf logit (weight 0, exponent -inf) made the product NaN: this
+      // lane's accumulator again with the exponent clamped (rare)
+      if (et != et) {
+        et = 0.f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const uint32_t w[4] = {raw[k].x, raw[k].y, raw[k].z, raw[k].w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const float a0 = fmaf(bf16_lo(w[q]), cc, nb), a1 = fmaf(bf16_hi(w[q]), cc, nb);
+            et = fmaf(ex2(a1), fmaxf(a1, -256.f), fmaf(ex2(a0), fmaxf(a0, -256.f), et));
+          }
+        }
+      }
+    }
   } else {
     float s0 = 0.f, s1 = 0.f;
 #pragma unroll
