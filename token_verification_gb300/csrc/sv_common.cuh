@@ -50,6 +50,18 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// The factor that moves a sum of 2^(l c - fl(m c)) - a chunk record's
+// weights, each in the frame of its own rounded offset fl(m c) - into the
+// frame fl(M c) of a larger maximum M: 2^(fl(m c) - fl(M c)), the difference
+// of the two rounded offsets (exact when they are within a factor of two).
+// 2^(fmaf(m, c, -fl(M c))) would carry the rounding error of m c into the
+// exponent: up to half an ulp of M c, about 7e-7 of relative error in a sum
+// of logits near 20 / c, which the residual max(0, p - q) of a small mass
+// amplifies in its draws.  mc = fl(M c) = __fmul_rn(M, c).
+__device__ __forceinline__ float reframe(float m, float mc, float c) {
+  return ex2(__fmul_rn(m, c) - mc);
+}
+
 // max that propagates NaN (a NaN anywhere in a row must surface).
 __device__ __forceinline__ float max_nan(float a, float b) {
   float r;
@@ -613,7 +625,8 @@ __device__ __forceinline__ float2 combine_argmax_records(const float2* rec, int 
   return warp_combine_argmax(best);
 }
 
-// Combine a row's softmax chunk records into {m, S} with S in the frame of m.
+// Combine a row's softmax chunk records into {m, S} with S in the frame of
+// fl(m c) (the weights 2^(l c - fl(m c))).
 constexpr int kRecCache = 8;  // records cached per lane (rows of up to 256 chunks)
 
 // `copy` (shared memory, or nullptr) receives the records as they are read.
@@ -636,13 +649,13 @@ __device__ __forceinline__ float2 combine_softmax_records(const float2* rec, int
   }
   const float m = warp_max_nan(lm);
   if (!is_finite(m)) return make_float2(m == -INFINITY ? -INFINITY : qnan(), 0.f);
-  const float nb = -m * cc;
+  const float mc = __fmul_rn(m, cc);  // the row's frame (the draws' weights use it too)
   float s = 0.f;
 #pragma unroll
-  for (int t = 0; t < kRecCache; ++t) s += cache[t].y * ex2(fmaf(cache[t].x, cc, nb));
+  for (int t = 0; t < kRecCache; ++t) s += cache[t].y * reframe(cache[t].x, mc, cc);
   for (int c = lane + kRecCache * kWarp; c < NC; c += kWarp) {
     const float2 r = __ldcg(rec + c);
-    s += r.y * ex2(fmaf(r.x, cc, nb));
+    s += r.y * reframe(r.x, mc, cc);
   }
   return make_float2(m, warp_sum(s));
 }

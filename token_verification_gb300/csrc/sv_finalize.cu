@@ -292,11 +292,11 @@ __device__ int draw_from_records(const T* row, const float2* rec, int NC, int V,
                                  float cut, const int* excl = nullptr, int nexcl = 0) {
   using L = Lane<T, VEC>;
   const int lane = lane_id();
-  const float nb = -m * cc;
+  const float mc = __fmul_rn(m, cc);
   auto record = [&](int c) { return kSharedRecords ? rec[c] : __ldcg(rec + c); };
   auto weight = [&](int c) {
     const float2 r = record(c);
-    return r.y * ex2(fmaf(r.x, cc, nb));
+    return r.y * reframe(r.x, mc, cc);
   };
   if constexpr (VEC * sizeof(T) == 16) {
     float frac = 0.f;
@@ -995,12 +995,12 @@ __device__ void summarise_tree_rows(const VerifyParams& p, int b, int N, RowSum*
       const float m = warp_max_nan(max_nan(rc[j][0].x, rc[j][1].x));
       RowSum rs{m == -INFINITY ? -INFINITY : qnan(), 0.f, 0.f, -1, 0.f};
       if (is_finite(m)) {
-        const float nb = -m * cc;
+        const float mc = __fmul_rn(m, cc);
         float sum = 0.f, a = 0.f;
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
           const float2 rq = rc[j][q];
-          sum += rq.y * ex2(fmaf(rq.x, cc, nb));
+          sum += rq.y * reframe(rq.x, mc, cc);
           if (kEntropy && rq.y > 0.f) {
             const float d = (rq.x - m) * cc;
             a += ex2(d) * fmaf(d, rq.y, ea[j][q]);
