@@ -148,6 +148,7 @@ static sv_status verify_common(int mode, const void* target, const void* draft,
   p.work = reinterpret_cast<unsigned*>(p.err + 2);
   p.n_pend = p.err + 3;
   p.r_exit = p.err + 4;
+  p.n_bonus = p.err + 5;
   p.arrive = reinterpret_cast<int*>(base + l.arrive);
   p.pend = reinterpret_cast<int*>(base + l.pend);
   p.rpn = p.pend + B;
@@ -323,6 +324,7 @@ static sv_status tree_rows_call(int mode, const void* target, const int32_t* tre
   p.work = reinterpret_cast<unsigned*>(p.err + 2);
   p.n_pend = p.err + 3;
   p.r_exit = p.err + 4;
+  p.n_bonus = p.err + 5;
   p.arrive = reinterpret_cast<int*>(base + l.arrive);
   p.pend = reinterpret_cast<int*>(base + l.pend);
   p.rpn = p.pend + B;

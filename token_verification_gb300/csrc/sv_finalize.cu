@@ -20,8 +20,11 @@
 // Kernel R (dense drafts only) follows F: a request rejected at n needs the
 //   chunk sums of max(0, p_n - q_n), one more pass over its (target, draft)
 //   row pair; F publishes those requests, R spreads their row pairs over
-//   every warp of the GPU, draws their tokens and writes the packed output.  Typical acceptance and rejection sampling on candidate
-//   trees have their own finalize kernels here.
+//   every warp of the GPU and draws their tokens.  F publishes the requests
+//   whose drafts all passed too: their bonus draws from p (one warp each)
+//   run in R beside the residual passes, off F's critical path.  R's last
+//   CTA writes the packed output.  Typical acceptance and rejection
+//   sampling on candidate trees have their own finalize kernels here.
 #include "sv_rows.cuh"
 
 namespace sv {
@@ -566,9 +569,9 @@ __device__ __forceinline__ void finalize_one(const VerifyParams& p, int b, FinSh
     if (row_needed(p, r, Kb))
       rs = summarise_row<MODE, T>(p, b, r, Kb, xr, s_rec ? s_rec + (long long)r * p.NC : nullptr);
     if (lane == 0) fs.srow[r] = rs;
-    // target row r <= K_b: the draw of position r (dense drafts: the bonus
-    // position only; the others draw from the residual)
-    if (MODE != kGreedy && Kb >= 0 && Kb <= K && r <= Kb && (MODE != kDense || r == Kb)) {
+    // target row r <= K_b: the draw of position r (dense drafts draw in
+    // kernel R: from the residual, or at the bonus position from p)
+    if (MODE != kGreedy && MODE != kDense && Kb >= 0 && Kb <= K && r <= Kb) {
       const int tok = position_draw<MODE, T, VEC>(p, b, r, Kb, rs, xr, uK, s_rec);
       if (lane == 0) fs.tok[r] = tok;
     }
@@ -580,7 +583,9 @@ __device__ __forceinline__ void finalize_one(const VerifyParams& p, int b, FinSh
   // Dense drafts, rejected at n: the request is published for the residual
   // kernel, which reads its row pair with every SM and writes its outputs.
   if (MODE == kDense && threadIdx.x == 0 && fs.resid.n >= 0) {
-    const int slot = atomicAdd(p.n_pend, 1);
+    // residual slots fill the slot arrays from the front, bonus draws from
+    // the back (a request publishes at most one of either)
+    const int slot = fs.resid.n < Kb ? atomicAdd(p.n_pend, 1) : p.B - 1 - atomicAdd(p.n_bonus, 1);
     p.pend[slot] = b;
     p.rpn[slot] = fs.resid.n;
     p.rpar[slot] = make_float4(fs.resid.mp, fs.resid.ip, fs.resid.mq, fs.resid.iq);
@@ -666,8 +671,10 @@ __device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, i
     if (!status) {
       if (MODE == kGreedy) {
         token = idx_n;
-      } else if (MODE == kDense && n < Kb) {
-        pending = true;  // the whole CTA draws from max(0, p_n - q_n) next
+      } else if (MODE == kDense) {
+        // kernel R draws: from max(0, p_n - q_n) (n < K_b), or from p_n (the
+        // bonus position n = K_b: mq and iq are not used)
+        pending = true;
         if (lane == 0) *resid = Residual{n, m_n, 1.f / s_n, mq_n, 1.f / sq_n};
       } else {
         token = s_tok[n];  // drawn beside the row summaries (position_draw)
@@ -870,10 +877,24 @@ __global__ void __launch_bounds__(kResThreads, 2) residual_kernel(const VerifyPa
   const int lane = lane_id();
   const int NC = p.NC;
   const int groups = (NC + G - 1) / G;
-  const long long items = (long long)__ldcg(p.n_pend) * groups;
+  const long long ritems = (long long)__ldcg(p.n_pend) * groups;
+  const long long items = ritems + __ldcg(p.n_bonus);
   const long long warps = (long long)gridDim.x * (blockDim.x >> 5);
   for (long long it = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); it < items;
        it += warps) {
+    if (it >= ritems) {  // a request whose drafts all passed: its bonus draw from p_K_b
+      const int slot = p.B - 1 - (int)(it - ritems);
+      const int b = __ldcg(p.pend + slot), n = __ldcg(p.rpn + slot);
+      const float m = __ldcg(p.rpar + slot).x;
+      const long long r = (long long)b * p.R + n;
+      const float uK = __ldg(p.uniforms + (long long)b * (p.K + 1) + p.K);
+      const int x = lane < n ? __ldg(p.draft_tokens + (long long)b * p.K + lane) : -1;
+      const int token = draw_from_records<T, VEC>(
+          row_ptr<T>(p.target, (long long)b * (p.K + 1) + n, p.V), p.rec + r * NC, NC, p.V, m,
+          p.cc, uK, -1, mask_row(p, b, n), p.mask_words, row_cut(p, r));
+      write_request(p, b, token < 0 ? kBadLogits : 0, n, token, x);
+      continue;
+    }
     const int slot = (int)(it / groups), c0 = (int)(it - (long long)slot * groups) * G;
     const float4 q = __ldcg(p.rpar + slot);
     const Residual st{__ldcg(p.rpn + slot), q.x, q.y, q.z, q.w};
@@ -894,6 +915,7 @@ __global__ void __launch_bounds__(kResThreads, 2) residual_kernel(const VerifyPa
   if (!s_flag[0]) return;
   if (threadIdx.x == 0) {
     *p.n_pend = 0;
+    *p.n_bonus = 0;
     *p.r_exit = 0;
   }
   if (p.compact_in_finalize) compact_all(p, s_flag);
@@ -937,8 +959,8 @@ cudaError_t launch_typed(const VerifyParams& p, cudaStream_t s) {
   });
   if (err != cudaSuccess) return err;
   constexpr int G = residual_group<T, VEC>();
-  const long long want =
-      ((long long)p.B * ((p.NC + G - 1) / G) + kResThreads / kWarp - 1) / (kResThreads / kWarp);
+  const long long want = ((long long)p.B * ((p.NC + G - 1) / G + 1) + kResThreads / kWarp - 1) /
+                         (kResThreads / kWarp);
   const long long cap = (long long)di.sms * occ;
   return launch_pdl(rk, dim3((unsigned)(want < cap ? want : cap)), dim3(kResThreads), s, args);
 }

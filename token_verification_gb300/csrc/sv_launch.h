@@ -51,9 +51,10 @@ struct VerifyParams {
   // kernel reads (published by the finalize kernel)
   int* n_pend;       // [1] rejected requests published
   int* r_exit;       // [1] residual CTAs finished
+  int* n_bonus;      // [1] dense requests whose drafts all passed (bonus draws in kernel R)
   int* arrive;       // [B] chunk groups done per published slot
-  int* pend;         // [B] the request of each slot
-  int* rpn;          // [B] its rejected position n
+  int* pend;         // [B] the request of each slot (bonus draws from the back)
+  int* rpn;          // [B] its rejected position n (or K_b for a bonus draw)
   float4* rpar;      // [B] {row max, 1/sum} of its target and draft rows at n
   float* rsums;      // [B*NC] residual chunk sums per slot
   float2* rec;       // [B*R*NC]
