@@ -189,6 +189,68 @@ __device__ int find_chunk_runs(F weight, int NC, float u, float* frac) {
   return c;
 }
 
+// find_chunk_runs with each lane's run of chunk weights read once into
+// registers (rows of up to 8 * 32 chunks; longer rows take find_chunk_runs):
+// the same sums in the same order, one read of weights that are costly to
+// read (global memory).
+template <class F>
+__device__ int find_chunk_runs_once(F weight, int NC, float u, float* frac) {
+  constexpr int kRun = 8;
+  const int per = (NC + kWarp - 1) / kWarp;
+  if (per > kRun) return find_chunk_runs(weight, NC, u, frac);
+  const int lane = lane_id();
+  const int c0 = lane * per;
+  float w[kRun];
+  float s = 0.f;
+#pragma unroll
+  for (int i = 0; i < kRun; ++i) {
+    w[i] = (i < per && c0 + i < NC) ? weight(c0 + i) : 0.f;
+    if (i < per && c0 + i < NC) s += w[i];
+  }
+  const float incl = warp_incl_scan(s);
+  const float target = u * __shfl_sync(0xffffffffu, incl, kWarp - 1);
+  const unsigned hit = __ballot_sync(0xffffffffu, s > 0.f && incl > target);
+  int c = -1;
+  float f = 0.f;
+  if (hit) {
+    const int l = __ffs(hit) - 1;
+    if (lane == l) {
+      float acc = incl - s;
+#pragma unroll
+      for (int i = 0; i < kRun; ++i) {
+        if (c < 0 && i < per && c0 + i < NC) {
+          if (w[i] > 0.f && acc + w[i] > target) {
+            c = c0 + i;
+            f = fminf(fmaxf((target - acc) / w[i], 0.f), 1.f);
+          } else {
+            acc += w[i];
+          }
+        }
+      }
+      if (c < 0) {  // rounding inside the lane: its last positive chunk
+#pragma unroll
+        for (int i = 0; i < kRun; ++i)
+          if (i < per && c0 + i < NC && w[i] > 0.f) c = c0 + i;
+        f = 2.f;
+      }
+    }
+    c = __shfl_sync(0xffffffffu, c, l);
+    f = __shfl_sync(0xffffffffu, f, l);
+  } else {
+    const unsigned pos = __ballot_sync(0xffffffffu, s > 0.f);
+    if (!pos) return -1;
+    const int l = 31 - __clz(pos);
+    if (lane == l)
+#pragma unroll
+      for (int i = 0; i < kRun; ++i)
+        if (i < per && c0 + i < NC && w[i] > 0.f) c = c0 + i;
+    c = __shfl_sync(0xffffffffu, c, l);
+    f = 2.f;
+  }
+  *frac = f;
+  return c;
+}
+
 // Elements 32*lane .. 32*lane+31 of chunk c as stored (-inf past V): four
 // 128-bit words of bf16 pairs, or eight of fp32; get(e) widens element e.
 template <typename T>
@@ -590,8 +652,11 @@ __device__ __forceinline__ void finalize_one(const VerifyParams& p, int b, FinSh
     p.rpn[slot] = fs.resid.n;
     p.rpar[slot] = make_float4(fs.resid.mp, fs.resid.ip, fs.resid.mq, fs.resid.iq);
   }
-  // The last request of the call clears the counters and (without dense
-  // drafts, whose residual kernel comes last) writes the packed output.
+  // Dense drafts: kernel R, which waits for this kernel to end, clears the
+  // counters and writes the packed output, so the CTA is done.
+  if (MODE == kDense) return;
+  // The last request of the call clears the counters and writes the packed
+  // output.
   if (threadIdx.x == 0) fs.last[0] = atomic_add_acq_rel(p.fin_ticket, 1) + 1 == p.B;
   __syncthreads();
   if (!fs.last[0]) return;
@@ -600,7 +665,7 @@ __device__ __forceinline__ void finalize_one(const VerifyParams& p, int b, FinSh
     *p.fin_ticket = 0;
     *p.work = 0u;
   }
-  if (MODE != kDense && p.compact_in_finalize) compact_all(p, fs.last);
+  if (p.compact_in_finalize) compact_all(p, fs.last);
 }
 
 // Kernel F: one CTA per request, chained to kernel A by programmatic
@@ -785,7 +850,8 @@ __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const R
   int token;
   if constexpr (VEC * sizeof(T) == 16) {
     float frac = 0.f;
-    const int c = find_chunk_runs(weight, NC, uK, &frac);
+    const int c = kGlobalSums ? find_chunk_runs_once(weight, NC, uK, &frac)
+                              : find_chunk_runs(weight, NC, uK, &frac);
     if (c < 0) {  // no residual mass (rounding only): draw from p_n
       token = residual_fallback<T, VEC>(p, b, st, srec, uK);
     } else {
@@ -913,7 +979,9 @@ __global__ void __launch_bounds__(kResThreads, 2) residual_kernel(const VerifyPa
   if (threadIdx.x == 0) s_flag[0] = atomic_add_acq_rel(p.r_exit, 1) + 1 == (int)gridDim.x;
   __syncthreads();
   if (!s_flag[0]) return;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0) {  // every counter of the call (kernel F left them to this kernel)
+    *p.err = 0;
+    *p.work = 0u;
     *p.n_pend = 0;
     *p.n_bonus = 0;
     *p.r_exit = 0;
