@@ -542,7 +542,8 @@ struct Residual {
 template <int MODE, typename T, int VEC>
 __device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const int* s_tok, int x,
-                                              float u, int timed_out, Residual* resid);
+                                              float u, int timed_out, Residual* resid,
+                                              float uK, const float2* s_rec);
 template <typename T, int VEC, bool kGlobalSums = false>
 __device__ __noinline__ void residual_pick(const VerifyParams& p, int b, const Residual& st,
                                            const float* sums, const float2* srec);
@@ -587,14 +588,15 @@ struct FinShared {
 };
 
 // Request b's finalisation by the calling CTA (every thread; any multiple
-// of 32 threads).  Rows are summarised by the CTA's warps, each of which also
-// draws the token its own position would emit if the walk stopped there (the
-// residual or bonus draw of rejection sampling, §2.1 of the page cited at
-// the top of this file); their chunk records are kept in shared memory (when
-// they fit) for the draws.  Then one warp runs the acceptance tests of all
-// positions at once (one lane per position) and takes the stopping
-// position's token, or the argmax (greedy).  A dense-draft request rejected
-// at n is published for kernel R, which writes its outputs.  wait() is called
+// of 32 threads).  Rows are summarised by the CTA's warps; with one-hot
+// drafts each of them also draws the token its own position would emit if
+// the walk stopped there (the residual or bonus draw of rejection sampling,
+// §2.1 of the page cited at the top of this file); the chunk records are
+// kept in shared memory (when they fit) for the draws.  Then one warp runs
+// the acceptance tests of all positions at once (one lane per position) and
+// takes the stopping position's token (typical acceptance: draws it then),
+// or the argmax (greedy).  A dense-draft request is published for kernel R,
+// which draws its token and writes its outputs.  wait() is called
 // by every thread once the request's inputs are loaded and before its
 // records are read.  s_rec: the request's [R*NC] records copied to shared
 // memory for the draws, or null.
@@ -631,16 +633,18 @@ __device__ __forceinline__ void finalize_one(const VerifyParams& p, int b, FinSh
     if (row_needed(p, r, Kb))
       rs = summarise_row<MODE, T>(p, b, r, Kb, xr, s_rec ? s_rec + (long long)r * p.NC : nullptr);
     if (lane == 0) fs.srow[r] = rs;
-    // target row r <= K_b: the draw of position r (dense drafts draw in
-    // kernel R: from the residual, or at the bonus position from p)
-    if (MODE != kGreedy && MODE != kDense && Kb >= 0 && Kb <= K && r <= Kb) {
+    // target row r <= K_b: the draw of position r, for one-hot drafts
+    // beside the summaries (typical acceptance draws after the tests, at the
+    // stopping position only; dense drafts draw in kernel R)
+    if (MODE == kOneHot && Kb >= 0 && Kb <= K && r <= Kb) {
       const int tok = position_draw<MODE, T, VEC>(p, b, r, Kb, rs, xr, uK, s_rec);
       if (lane == 0) fs.tok[r] = tok;
     }
   }
   __syncthreads();
   if (warp == 0)
-    finalize_request<MODE, T, VEC>(p, b, Kb, fs.srow, fs.tok, x, u, timed_out, &fs.resid);
+    finalize_request<MODE, T, VEC>(p, b, Kb, fs.srow, fs.tok, x, u, timed_out, &fs.resid, uK,
+                                   s_rec);
   __syncthreads();
   // Dense drafts, rejected at n: the request is published for the residual
   // kernel, which reads its row pair with every SM and writes its outputs.
@@ -683,7 +687,8 @@ __global__ void __launch_bounds__(fin_threads<MODE>()) finalize_kernel(const Ver
 template <int MODE, typename T, int VEC>
 __device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, int Kb,
                                               const RowSum* srow, const int* s_tok, int x,
-                                              float u, int timed_out, Residual* resid) {
+                                              float u, int timed_out, Residual* resid,
+                                              float uK, const float2* s_rec) {
   const int lane = lane_id();
   const int K = p.K;
   // A bounded wait that gave up in kernel A (a device fault) invalidates the
@@ -742,7 +747,10 @@ __device__ __forceinline__ void finalize_request(const VerifyParams& p, int b, i
         pending = true;
         if (lane == 0) *resid = Residual{n, m_n, 1.f / s_n, mq_n, 1.f / sq_n};
       } else {
-        token = s_tok[n];  // drawn beside the row summaries (position_draw)
+        // one-hot drafts: drawn beside the row summaries; typical acceptance:
+        // drawn now, at the stopping position only
+        token = MODE == kOneHot ? s_tok[n]
+                                : position_draw<MODE, T, VEC>(p, b, n, Kb, srow[n], x_n, uK, s_rec);
         if (token < 0) status = kBadLogits;
       }
     }
