@@ -532,8 +532,10 @@ template <int MODE>
 __host__ __device__ constexpr int fin_threads() { return 256; }
 constexpr int kMaxRows = 2 * kMaxK + 1;
 
-// The rejected position of a dense-draft request and its two rows' maxima
-// and reciprocal sums (n < 0: nothing left to draw).
+// Where a dense-draft request draws - its rejected position n (< K_b), or
+// the bonus position n = K_b when every draft passed - with the target and
+// draft rows' maxima and reciprocal sums there (mq and iq unused at the
+// bonus position; n < 0: nothing left to draw).
 struct Residual {
   int n;
   float mp, ip, mq, iq;
@@ -584,7 +586,7 @@ struct FinShared {
   RowSum srow[kMaxRows];
   Residual resid;
   int last[32];
-  int tok[kMaxRows];  // the token each position would draw
+  int tok[kMaxRows];  // one-hot drafts: the token each position would draw
 };
 
 // Request b's finalisation by the calling CTA (every thread; any multiple
