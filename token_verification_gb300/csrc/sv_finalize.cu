@@ -10,13 +10,14 @@
 // (FastDeploy), "高效投机解码框架设计").
 //
 // Kernel F (finalize_kernel, one CTA per request) combines each row's chunk
-//   records, draws beside each row's summary the token its position would
-//   draw (the crossing chunk from the records, then one rescan of that single
-//   chunk), and runs the acceptance tests of all positions at once (one lane
-//   per position).  The last CTA of the call writes the padding-free packed
-//   output (exclusive scan of accept_len, packed tokens, per-token batch
-//   ids).  F starts with programmatic dependent launch and waits on the
-//   device for kernel A's records.
+//   records, with one-hot drafts draws beside each row's summary the token
+//   its position would draw (the crossing chunk from the records, then one
+//   rescan of that single chunk), and runs the acceptance tests of all
+//   positions at once (one lane per position); typical acceptance draws after
+//   the tests, at the stopping position only.  The last CTA of the call
+//   writes the padding-free packed output (exclusive scan of accept_len,
+//   packed tokens, per-token batch ids).  F starts with programmatic
+//   dependent launch and waits on the device for kernel A's records.
 // Kernel R (dense drafts only) follows F: a request rejected at n needs the
 //   chunk sums of max(0, p_n - q_n), one more pass over its (target, draft)
 //   row pair; F publishes those requests, R spreads their row pairs over
